@@ -1,0 +1,239 @@
+"""fp64 CPU oracle for the fused attention forward and split-KV decode.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this module.  The library's product
+path never calls it and shares no code with it.
+
+What it computes is the plain definition, written out step by step so that it
+can be checked by eye:
+
+    S = scale * Q K^T  (masked entries = -inf)
+    P = softmax(S) along the key axis     (two passes: row max, then exp / sum)
+    O = P V,   LSE = ln sum_j exp(S_ij)
+
+Sources (pages on softmax attention):
+
+* "Agent 帮我写 CUDA：一个 Softmax Attention 算子的开发全记录" (a fp32 softmax-attention
+  CUDA development log), section 二 "参考基线": the operator is
+  softmax(Q K^T / sqrt(D)) V on ``[B,H,N,D]`` tensors, checked against
+  ``scaled_dot_product_attention``.  Section 四 "Tiled Attention 的核心思想" gives
+  the online-softmax recurrence; online softmax reaches exactly the two-pass
+  result below (up to rounding order), so the oracle uses the two-pass form.
+* "Ask, Don't Equip: Question-Driven Coding Agents for Deep Kernel Optimization",
+  section "研究动机": the feature surface (GQA, causal and sliding-window masks,
+  split-KV decode).  It gives no formulas; the readings used here are:
+    - GQA: query head h reads KV head ``h // (Hq // Hkv)``;
+    - causal is bottom-right aligned: key j is visible to query i iff
+      ``j <= i + Nk - Nq``;
+    - a window w > 0 keeps the last w keys up to and including the diagonal:
+      ``j > i + Nk - Nq - w``;
+    - a row with no visible key has O = 0 and LSE = -inf;
+    - LSE is the natural log of the softmax denominator of the scaled scores;
+    - split-KV decode cuts each sequence's keys into chunks of ``chunk`` keys
+      starting at key 0 (the last chunk may be short); each chunk yields its own
+      normalised output and LSE, and the combine step weights chunk c by
+      ``exp(LSE_c - max_c LSE_c)``.
+
+Every pin of this module lives in ``tests/test_oracle.py``.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+__all__ = [
+    "visible_mask", "kv_head", "attention_forward", "attention_rows",
+    "attention_probabilities", "decode_forward", "decode_split_partials",
+    "decode_combine",
+]
+
+
+def _f64(x) -> np.ndarray:
+    """Exact fp64 copy of a tensor or array (bf16 and fp32 values are exact in fp64)."""
+    if hasattr(x, "detach"):                      # torch tensor, bf16 included
+        x = x.detach().to("cpu")
+        import torch
+        x = x.to(torch.float64).numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def kv_head(h: int, Hq: int, Hkv: int) -> int:
+    """KV head read by query head ``h`` (GQA groups of consecutive query heads)."""
+    if Hq % Hkv:
+        raise ValueError("Hq must be a multiple of Hkv")
+    return h // (Hq // Hkv)
+
+
+def visible_mask(rows: np.ndarray, Nq: int, Nk: int, causal: bool, window: int) -> np.ndarray:
+    """Boolean ``[len(rows), Nk]``: True where key j is visible to query row i."""
+    i = np.asarray(rows, dtype=np.int64)[:, None]
+    j = np.arange(Nk, dtype=np.int64)[None, :]
+    diag = i + (Nk - Nq)                   # bottom-right aligned diagonal
+    vis = np.ones((i.shape[0], Nk), dtype=bool)
+    if causal:
+        vis &= j <= diag
+    if window > 0:
+        vis &= j > diag - window
+    return vis
+
+
+def _softmax_rows(S: np.ndarray):
+    """Two-pass row softmax of a masked score block.
+
+    Returns ``(P, lse)``.  Fully masked rows give P = 0 and lse = -inf.
+    """
+    M = S.max(axis=1)                                  # pass 1: row max
+    empty = ~np.isfinite(M)                            # every key masked
+    M_safe = np.where(empty, 0.0, M)
+    E = np.exp(S - M_safe[:, None])                    # pass 2: exp (masked -> 0)
+    l = E.sum(axis=1)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        P = np.where(empty[:, None], 0.0, E / np.where(empty, 1.0, l)[:, None])
+        lse = np.where(empty, -np.inf, M_safe + np.log(np.where(empty, 1.0, l)))
+    return P, lse
+
+
+def _scores(q_rows: np.ndarray, k_head: np.ndarray, scale: float) -> np.ndarray:
+    """S = scale * Q_rows K^T, shape ``[rows, Nk]``."""
+    return scale * (q_rows @ k_head.T)
+
+
+def attention_forward(q, k, v, scale: float, causal: bool = False, window: int = 0,
+                      row_block: int = 512):
+    """Full forward: ``O [B,Hq,Nq,D]`` and ``LSE [B,Hq,Nq]`` in fp64.
+
+    ``q``: ``[B,Hq,Nq,D]``; ``k``, ``v``: ``[B,Hkv,Nk,D]``.  S is formed
+    explicitly for ``row_block`` query rows at a time.
+    """
+    Q, K, V = _f64(q), _f64(k), _f64(v)
+    B, Hq, Nq, D = Q.shape
+    Hkv, Nk = K.shape[1], K.shape[2]
+    O = np.zeros((B, Hq, Nq, V.shape[3]))
+    LSE = np.zeros((B, Hq, Nq))
+    for b in range(B):
+        for h in range(Hq):
+            kh = kv_head(h, Hq, Hkv)
+            for i0 in range(0, Nq, row_block):
+                rows = np.arange(i0, min(i0 + row_block, Nq))
+                S = _scores(Q[b, h, rows], K[b, kh], scale)
+                S[~visible_mask(rows, Nq, Nk, causal, window)] = -np.inf
+                P, lse = _softmax_rows(S)
+                O[b, h, rows] = P @ V[b, kh]
+                LSE[b, h, rows] = lse
+    return O, LSE
+
+
+def attention_rows(q, k, v, scale: float, rows, causal: bool = False, window: int = 0):
+    """O and LSE of selected query rows only.
+
+    ``rows`` is a sequence of ``(b, h, i)``; returns ``O [len(rows), D]`` and
+    ``LSE [len(rows)]``.  Same definition as :func:`attention_forward`, one row at
+    a time, for checking large workloads on sampled outputs.
+    """
+    B, Hq, Nq, _ = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    O = np.zeros((len(rows), v.shape[3]))
+    LSE = np.zeros(len(rows))
+    for n, (b, h, i) in enumerate(rows):
+        kh = kv_head(h, Hq, Hkv)
+        qi = _f64(q[b, h, i])[None, :]
+        Kh, Vh = _f64(k[b, kh]), _f64(v[b, kh])
+        S = _scores(qi, Kh, scale)
+        S[~visible_mask(np.array([i]), Nq, Nk, causal, window)] = -np.inf
+        P, lse = _softmax_rows(S)
+        O[n] = (P @ Vh)[0]
+        LSE[n] = lse[0]
+    return O, LSE
+
+
+def attention_probabilities(q, k, scale: float, causal: bool = False, window: int = 0):
+    """The full probability matrix ``P [B,Hq,Nq,Nk]`` (small shapes only)."""
+    Q, K = _f64(q), _f64(k)
+    B, Hq, Nq, _ = Q.shape
+    Hkv, Nk = K.shape[1], K.shape[2]
+    P = np.zeros((B, Hq, Nq, Nk))
+    for b in range(B):
+        for h in range(Hq):
+            S = _scores(Q[b, h], K[b, kv_head(h, Hq, Hkv)], scale)
+            S[~visible_mask(np.arange(Nq), Nq, Nk, causal, window)] = -np.inf
+            P[b, h] = _softmax_rows(S)[0]
+    return P
+
+
+# ---------------------------------------------------------------------------
+# Decode: one query token per sequence against a contiguous KV cache
+# ``[B, Nk_max, Hkv, D]`` of which sequence b uses the first ``seqlens[b]`` rows.
+# ---------------------------------------------------------------------------
+
+def _decode_one(q_bh: np.ndarray, K: np.ndarray, V: np.ndarray, scale: float):
+    """O and LSE of one query vector against key rows ``K`` / value rows ``V``."""
+    S = _scores(q_bh[None, :], K, scale)
+    P, lse = _softmax_rows(S)
+    return (P @ V)[0], lse[0]
+
+
+def decode_forward(q, k_cache, v_cache, seqlens, scale: float, batches=None):
+    """Unsplit decode: ``O [B,Hq,D]``, ``LSE [B,Hq]`` over keys ``j < seqlens[b]``.
+
+    ``batches`` optionally restricts the work to some sequences (other rows are
+    left at zero).
+    """
+    B, Hq, D = q.shape
+    Hkv = k_cache.shape[2]
+    lens = [int(x) for x in seqlens]
+    O = np.zeros((B, Hq, v_cache.shape[3]))
+    LSE = np.zeros((B, Hq))
+    for b in (range(B) if batches is None else batches):
+        Kb = _f64(k_cache[b, :lens[b]])                 # [Nk_b, Hkv, D]
+        Vb = _f64(v_cache[b, :lens[b]])
+        qb = _f64(q[b])
+        for h in range(Hq):
+            kh = kv_head(h, Hq, Hkv)
+            O[b, h], LSE[b, h] = _decode_one(qb[h], Kb[:, kh], Vb[:, kh], scale)
+    return O, LSE
+
+
+def decode_split_partials(q, k_cache, v_cache, seqlens, scale: float, chunk: int,
+                          batches=None):
+    """Split-KV step: per (b, h, chunk c) the chunk's normalised output and LSE.
+
+    Returns ``O_part [B,Hq,S_max,D]``, ``LSE_part [B,Hq,S_max]`` and the number
+    of chunks per sequence ``n_split [B]``; entries at ``c >= n_split[b]`` stay 0.
+    """
+    B, Hq, D = q.shape
+    Hkv, Nk_max = k_cache.shape[2], k_cache.shape[1]
+    S_max = -(-Nk_max // chunk)
+    lens = [int(x) for x in seqlens]
+    n_split = np.array([-(-n // chunk) for n in lens], dtype=np.int64)
+    O_part = np.zeros((B, Hq, S_max, v_cache.shape[3]))
+    LSE_part = np.zeros((B, Hq, S_max))
+    for b in (range(B) if batches is None else batches):
+        qb = _f64(q[b])
+        for c in range(n_split[b]):
+            j0, j1 = c * chunk, min((c + 1) * chunk, lens[b])
+            Kc = _f64(k_cache[b, j0:j1])
+            Vc = _f64(v_cache[b, j0:j1])
+            for h in range(Hq):
+                kh = kv_head(h, Hq, Hkv)
+                O_part[b, h, c], LSE_part[b, h, c] = _decode_one(qb[h], Kc[:, kh], Vc[:, kh], scale)
+    return O_part, LSE_part, n_split
+
+
+def decode_combine(O_part, LSE_part, n_split):
+    """Combine step: LSE-weighted merge of the chunk results.
+
+    ``M = max_c LSE_c``, ``w_c = exp(LSE_c - M)``, ``O = sum_c w_c O_c / sum_c w_c``,
+    ``LSE = M + ln sum_c w_c`` over the valid chunks ``c < n_split[b]``.
+    """
+    O_part, LSE_part = _f64(O_part), _f64(LSE_part)
+    B, Hq, _, D = O_part.shape
+    O = np.zeros((B, Hq, D))
+    LSE = np.zeros((B, Hq))
+    for b in range(B):
+        n = int(n_split[b])
+        L = LSE_part[b, :, :n]                          # [Hq, n]
+        M = L.max(axis=1)
+        w = np.exp(L - M[:, None])
+        s = w.sum(axis=1)
+        O[b] = np.einsum("hc,hcd->hd", w, O_part[b, :, :n]) / s[:, None]
+        LSE[b] = M + np.log(s)
+    return O, LSE

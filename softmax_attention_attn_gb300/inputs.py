@@ -1,0 +1,91 @@
+"""Seeded synthetic inputs for the attention workloads.
+
+This module only draws random numbers and lays them out; it holds none of the
+attention arithmetic.  Both the CUDA path (through the tests and the benchmark)
+and the CPU oracle consume what it returns, so the two sides always see the
+same values.
+
+Recipe (every draw uses ``torch.Generator("cpu")``):
+
+* prefill workloads: one generator seeded with ``seed`` draws fp32 N(0, 1)
+  tensors in the order Q ``[B,Hq,Nq,D]``, K ``[B,Hkv,Nk,D]``, V ``[B,Hkv,Nk,D]``;
+  bf16 workloads cast those fp32 values with round-to-nearest-even.
+* decode workloads: a generator seeded with ``seed`` draws the per-sequence
+  key counts ``Nk_b ~ U{nk_lo..nk_hi}`` first and then Q ``[B,Hq,D]``.  Sequence
+  ``b`` then draws its own K and V rows ``[Nk_b,Hkv,D]`` (K first) from a
+  generator seeded with ``decode_row_seed(seed, b)``, so any single sequence can
+  be regenerated without replaying the others.  Cache rows at or beyond
+  ``Nk_b`` hold finite sentinels (K = 64, V = 1e4) so that a masking leak
+  shows up as a large error instead of passing unnoticed.
+"""
+from __future__ import annotations
+
+import torch
+
+K_SENTINEL = 64.0
+V_SENTINEL = 1.0e4
+
+_DTYPES = {"fp32": torch.float32, "bf16": torch.bfloat16}
+
+
+def _cast(t: torch.Tensor, dtype: str) -> torch.Tensor:
+    if dtype not in _DTYPES:
+        raise ValueError(f"unknown dtype {dtype!r}")
+    return t if dtype == "fp32" else t.to(_DTYPES[dtype])
+
+
+def prefill_inputs(B: int, Hq: int, Hkv: int, Nq: int, Nk: int, D: int,
+                   dtype: str = "bf16", seed: int = 0):
+    """Q, K, V for one prefill workload, contiguous ``[B,H,N,D]`` CPU tensors."""
+    g = torch.Generator("cpu").manual_seed(seed)
+    q = torch.randn(B, Hq, Nq, D, generator=g, dtype=torch.float32)
+    k = torch.randn(B, Hkv, Nk, D, generator=g, dtype=torch.float32)
+    v = torch.randn(B, Hkv, Nk, D, generator=g, dtype=torch.float32)
+    return _cast(q, dtype), _cast(k, dtype), _cast(v, dtype)
+
+
+def decode_row_seed(seed: int, b: int) -> int:
+    """Seed of the generator that draws sequence ``b``'s K/V rows."""
+    return seed * 1_000_003 + 1 + b
+
+
+def decode_seqlens_and_q(B: int, Hq: int, D: int, nk_lo: int, nk_hi: int,
+                         seed: int = 0, dtype: str = "bf16"):
+    """Per-sequence key counts (int32 ``[B]``) and the query ``[B,Hq,D]``."""
+    g = torch.Generator("cpu").manual_seed(seed)
+    seqlens = torch.randint(nk_lo, nk_hi + 1, (B,), generator=g, dtype=torch.int64)
+    q = torch.randn(B, Hq, D, generator=g, dtype=torch.float32)
+    return seqlens.to(torch.int32), _cast(q, dtype)
+
+
+def decode_kv_rows(seed: int, b: int, nk: int, Hkv: int, D: int, dtype: str = "bf16"):
+    """The ``nk`` valid K and V rows ``[nk,Hkv,D]`` of sequence ``b``."""
+    g = torch.Generator("cpu").manual_seed(decode_row_seed(seed, b))
+    k = torch.randn(nk, Hkv, D, generator=g, dtype=torch.float32)
+    v = torch.randn(nk, Hkv, D, generator=g, dtype=torch.float32)
+    return _cast(k, dtype), _cast(v, dtype)
+
+
+def decode_inputs(B: int, Hq: int, Hkv: int, D: int, nk_lo: int, nk_hi: int,
+                  seed: int = 0, nk_max: int | None = None, dtype: str = "bf16",
+                  pin_memory: bool = False):
+    """Full decode workload: ``(q, k_cache, v_cache, seqlens)``.
+
+    ``k_cache``/``v_cache`` are ``[B,Nk_max,Hkv,D]`` with ``Nk_max`` defaulting to
+    ``nk_hi``; rows past each sequence's length hold the sentinels.
+    """
+    seqlens, q = decode_seqlens_and_q(B, Hq, D, nk_lo, nk_hi, seed, dtype)
+    nk_max = nk_hi if nk_max is None else nk_max
+    if int(seqlens.max()) > nk_max:
+        raise ValueError("nk_max is below a drawn sequence length")
+    tdt = _DTYPES[dtype]
+    k_cache = torch.empty(B, nk_max, Hkv, D, dtype=tdt, pin_memory=pin_memory)
+    v_cache = torch.empty(B, nk_max, Hkv, D, dtype=tdt, pin_memory=pin_memory)
+    for b in range(B):
+        nk = int(seqlens[b])
+        kb, vb = decode_kv_rows(seed, b, nk, Hkv, D, dtype)
+        k_cache[b, :nk] = kb
+        v_cache[b, :nk] = vb
+        k_cache[b, nk:] = K_SENTINEL
+        v_cache[b, nk:] = V_SENTINEL
+    return q, k_cache, v_cache, seqlens

@@ -1,0 +1,395 @@
+"""Pins of the fp64 oracle against what the mathematics fixes (CPU only).
+
+Each ``pin_*`` function checks the oracle module passed in against a closed
+form, an invariant, a hand-derived example or an independent brute force.
+``test_mutants_are_caught`` plants plausible mistakes in the oracle (on the CPU)
+and checks that at least one pin fails for each, so the battery is known to
+have teeth.
+"""
+import math
+import os
+import re
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.attention as ORA
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def rnd(seed, *shape):
+    return np.random.default_rng(seed).standard_normal(shape)
+
+
+def visible_list(i, Nq, Nk, causal, window):
+    return [j for j in range(Nk)
+            if (not causal or j <= i + Nk - Nq) and (window <= 0 or j > i + Nk - Nq - window)]
+
+
+# ---------------------------------------------------------------- brute force
+def brute_force(q, k, v, scale, causal, window):
+    """Pure-Python loops with exactly rounded sums (math.fsum)."""
+    B, Hq, Nq, D = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    g = Hq // Hkv
+    O = np.zeros((B, Hq, Nq, v.shape[3]))
+    L = np.zeros((B, Hq, Nq))
+    for b in range(B):
+        for h in range(Hq):
+            kh = h // g
+            for i in range(Nq):
+                js = visible_list(i, Nq, Nk, causal, window)
+                if not js:
+                    L[b, h, i] = -math.inf
+                    continue
+                s = {j: scale * math.fsum(float(q[b, h, i, d]) * float(k[b, kh, j, d]) for d in range(D))
+                     for j in js}
+                m = max(s.values())
+                e = {j: math.exp(s[j] - m) for j in js}
+                l = math.fsum(e.values())
+                for d in range(v.shape[3]):
+                    O[b, h, i, d] = math.fsum(e[j] * float(v[b, kh, j, d]) for j in js) / l
+                L[b, h, i] = m + math.log(l)
+    return O, L
+
+
+CASES = [  # (B, Hq, Hkv, Nq, Nk, D, causal, window)
+    (1, 2, 1, 3, 5, 4, False, 0),
+    (2, 4, 2, 5, 5, 3, True, 0),
+    (1, 2, 2, 4, 7, 2, True, 0),      # Nq < Nk: bottom-right causal
+    (1, 3, 1, 6, 6, 3, True, 2),      # causal + window
+    (1, 2, 1, 5, 4, 2, False, 3),     # window without causal
+    (1, 2, 1, 6, 3, 2, True, 0),      # Nq > Nk: some rows fully masked
+]
+
+
+def pin_brute_force(ora):
+    for n, (B, Hq, Hkv, Nq, Nk, D, causal, window) in enumerate(CASES):
+        q, k, v = rnd(10 + n, B, Hq, Nq, D), rnd(20 + n, B, Hkv, Nk, D), rnd(30 + n, B, Hkv, Nk, D)
+        scale = 1.0 / math.sqrt(D)
+        O, L = ora.attention_forward(q, k, v, scale, causal, window, row_block=2)
+        Ob, Lb = brute_force(q, k, v, scale, causal, window)
+        assert np.allclose(O, Ob, rtol=0, atol=1e-12), f"case {n}: O differs from brute force"
+        fin = np.isfinite(Lb)
+        assert np.array_equal(fin, np.isfinite(L)), f"case {n}: LSE finiteness differs"
+        assert np.allclose(L[fin], Lb[fin], rtol=0, atol=1e-12), f"case {n}: LSE differs"
+        assert np.all(L[~fin] == -np.inf) and np.all(O[~fin] == 0)
+
+
+def pin_sdpa(ora):
+    """Agreement with torch's scaled_dot_product_attention in float64 on CPU."""
+    for n, (B, Hq, Hkv, Nq, Nk, D) in enumerate([(2, 4, 2, 9, 9, 8), (1, 8, 2, 17, 17, 16)]):
+        q, k, v = rnd(40 + n, B, Hq, Nq, D), rnd(50 + n, B, Hkv, Nk, D), rnd(60 + n, B, Hkv, Nk, D)
+        for causal in (False, True):
+            O, _ = ora.attention_forward(q, k, v, 0.3, causal, 0)
+            g = Hq // Hkv
+            kt = torch.from_numpy(k).repeat_interleave(g, dim=1)
+            vt = torch.from_numpy(v).repeat_interleave(g, dim=1)
+            ref = torch.nn.functional.scaled_dot_product_attention(
+                torch.from_numpy(q), kt, vt, is_causal=causal, scale=0.3).numpy()
+            assert np.allclose(O, ref, rtol=0, atol=1e-12), "O differs from SDPA"
+
+
+# ---------------------------------------------------------------- closed forms
+def pin_zero_query(ora):
+    """Q = 0: O = mean of the visible V rows, LSE = ln(#visible)."""
+    for (B, Hq, Hkv, Nq, Nk, D, causal, window) in CASES:
+        q = np.zeros((B, Hq, Nq, D))
+        k, v = rnd(1, B, Hkv, Nk, D), rnd(2, B, Hkv, Nk, D)
+        O, L = ora.attention_forward(q, k, v, 0.7, causal, window)
+        for b in range(B):
+            for h in range(Hq):
+                kh = h // (Hq // Hkv)
+                for i in range(Nq):
+                    js = visible_list(i, Nq, Nk, causal, window)
+                    if not js:
+                        assert L[b, h, i] == -np.inf and np.all(O[b, h, i] == 0)
+                        continue
+                    assert abs(L[b, h, i] - math.log(len(js))) < 1e-13
+                    assert np.allclose(O[b, h, i], v[b, kh, js].mean(axis=0), rtol=0, atol=1e-13)
+
+
+def pin_single_key(ora):
+    """Nk = 1: O = V[0] of the query head's KV head, LSE = scale * q . k0."""
+    B, Hq, Hkv, Nq, D = 2, 6, 3, 4, 5
+    q, k, v = rnd(3, B, Hq, Nq, D), rnd(4, B, Hkv, 1, D), rnd(5, B, Hkv, 1, D)
+    O, L = ora.attention_forward(q, k, v, 0.4, False, 0)
+    for b in range(B):
+        for h in range(Hq):
+            kh = h // 2
+            for i in range(Nq):
+                assert np.allclose(O[b, h, i], v[b, kh, 0], rtol=0, atol=1e-14)
+                assert abs(L[b, h, i] - 0.4 * float(np.dot(q[b, h, i], k[b, kh, 0]))) < 1e-13
+
+
+def pin_probability_rows(ora):
+    """Rows of P sum to 1 (0 for fully masked rows) and sum_j exp(s_ij - LSE_i) = 1."""
+    for (B, Hq, Hkv, Nq, Nk, D, causal, window) in CASES:
+        q, k, v = rnd(6, B, Hq, Nq, D), rnd(7, B, Hkv, Nk, D), rnd(8, B, Hkv, Nk, D)
+        P = ora.attention_probabilities(q, k, 0.5, causal, window)
+        _, L = ora.attention_forward(q, k, v, 0.5, causal, window)
+        for b in range(B):
+            for h in range(Hq):
+                kh = h // (Hq // Hkv)
+                for i in range(Nq):
+                    js = visible_list(i, Nq, Nk, causal, window)
+                    hidden = [j for j in range(Nk) if j not in js]
+                    assert np.all(P[b, h, i, hidden] == 0)
+                    if js:
+                        assert abs(P[b, h, i].sum() - 1) < 1e-13
+                        s = [0.5 * math.fsum(q[b, h, i] * k[b, kh, j]) for j in js]
+                        assert abs(math.fsum(math.exp(x - L[b, h, i]) for x in s) - 1) < 1e-12
+
+
+def pin_causal_first_row(ora):
+    """Causal with Nq = Nk: row 0 returns V[0] and LSE_0 = scale * q0 . k0."""
+    B, Hq, Hkv, N, D = 2, 4, 2, 7, 6
+    q, k, v = rnd(9, B, Hq, N, D), rnd(10, B, Hkv, N, D), rnd(11, B, Hkv, N, D)
+    O, L = ora.attention_forward(q, k, v, 0.25, True, 0)
+    for b in range(B):
+        for h in range(Hq):
+            kh = h // 2
+            assert np.allclose(O[b, h, 0], v[b, kh, 0], rtol=0, atol=1e-14)
+            assert abs(L[b, h, 0] - 0.25 * float(np.dot(q[b, h, 0], k[b, kh, 0]))) < 1e-13
+
+
+def pin_dominant_key(ora):
+    """A key parallel to the query with a huge score selects its V row."""
+    B, H, Nq, Nk, D = 1, 1, 3, 9, 8
+    q, k, v = rnd(12, B, H, Nq, D), rnd(13, B, H, Nk, D), rnd(14, B, H, Nk, D)
+    i, jstar, scale = 1, 6, 1 / math.sqrt(D)
+    others = max(scale * float(np.dot(q[0, 0, i], k[0, 0, j])) for j in range(Nk) if j != jstar)
+    c = (others + 60.0) / (scale * float(np.dot(q[0, 0, i], q[0, 0, i])))
+    k[0, 0, jstar] = c * q[0, 0, i]
+    O, L = ora.attention_forward(q, k, v, scale, False, 0)
+    assert np.allclose(O[0, 0, i], v[0, 0, jstar], rtol=1e-18, atol=1e-20 * float(np.abs(v).max()) + 1e-24)
+    assert abs(L[0, 0, i] - scale * float(np.dot(q[0, 0, i], k[0, 0, jstar]))) < 1e-12
+
+
+# ---------------------------------------------------------------- invariants
+def pin_invariants(ora):
+    B, Hq, Hkv, Nq, Nk, D = 1, 4, 2, 6, 6, 5
+    q, k, v = rnd(15, B, Hq, Nq, D), rnd(16, B, Hkv, Nk, D), rnd(17, B, Hkv, Nk, D)
+    O, L = ora.attention_forward(q, k, v, 0.6, False, 0)
+    # joint permutation of K and V rows (non-causal)
+    perm = np.random.default_rng(18).permutation(Nk)
+    Op, Lp = ora.attention_forward(q, k[:, :, perm], v[:, :, perm], 0.6, False, 0)
+    assert np.allclose(Op, O, atol=1e-13) and np.allclose(Lp, L, atol=1e-13), "permutation"
+    # V -> a V + c maps O -> a O + c
+    Oa, _ = ora.attention_forward(q, k, 2.5 * v - 1.25, 0.6, False, 0)
+    assert np.allclose(Oa, 2.5 * O - 1.25, atol=1e-12), "affine V"
+    # adding w to every key shifts row i's scores by scale*q_i.w: O fixed, LSE shifted
+    w = rnd(19, D)
+    Ow, Lw = ora.attention_forward(q, k + w, v, 0.6, False, 0)
+    assert np.allclose(Ow, O, atol=1e-12), "score shift changes O"
+    assert np.allclose(Lw, L + 0.6 * np.einsum("bhid,d->bhi", q, w), atol=1e-12), "score shift LSE"
+    # GQA equals MHA on repeated K/V
+    g = Hq // Hkv
+    Om, Lm = ora.attention_forward(q, np.repeat(k, g, axis=1), np.repeat(v, g, axis=1), 0.6, False, 0)
+    assert np.allclose(Om, O, atol=1e-14) and np.allclose(Lm, L, atol=1e-14), "GQA vs MHA"
+    # causal (Nq = Nk) row i equals dense attention over keys 0..i
+    Oc, Lc = ora.attention_forward(q, k, v, 0.6, True, 0)
+    for i in range(Nq):
+        Od, Ld = ora.attention_forward(q[:, :, i:i + 1], k[:, :, :i + 1], v[:, :, :i + 1], 0.6, False, 0)
+        assert np.allclose(Oc[:, :, i], Od[:, :, 0], atol=1e-13) and np.allclose(Lc[:, :, i], Ld[:, :, 0], atol=1e-13)
+    # causal + window w, row i equals dense attention over keys i-w+1..i
+    wdw = 2
+    Ow2, Lw2 = ora.attention_forward(q, k, v, 0.6, True, wdw)
+    for i in range(Nq):
+        j0 = max(0, i - wdw + 1)
+        Od, Ld = ora.attention_forward(q[:, :, i:i + 1], k[:, :, j0:i + 1], v[:, :, j0:i + 1], 0.6, False, 0)
+        assert np.allclose(Ow2[:, :, i], Od[:, :, 0], atol=1e-13) and np.allclose(Lw2[:, :, i], Ld[:, :, 0], atol=1e-13)
+    # selected rows agree with the full forward
+    rows = [(0, 3, 2), (0, 0, 5), (0, 1, 0)]
+    Or, Lr = ora.attention_rows(q, k, v, 0.6, rows, True, 0)
+    for n, (b, h, i) in enumerate(rows):
+        assert np.allclose(Or[n], Oc[b, h, i], atol=1e-14) and abs(Lr[n] - Lc[b, h, i]) < 1e-14
+
+
+def _decode_case(seed=21, B=3, Hq=4, Hkv=2, D=6, Nk_max=11):
+    r = np.random.default_rng(seed)
+    seqlens = np.array([11, 1, 7][:B])
+    q = r.standard_normal((B, Hq, D))
+    kc = r.standard_normal((B, Nk_max, Hkv, D))
+    vc = r.standard_normal((B, Nk_max, Hkv, D))
+    for b in range(B):                          # sentinels in the unused tail
+        kc[b, seqlens[b]:] = 64.0
+        vc[b, seqlens[b]:] = 1e4
+    return q, kc, vc, seqlens
+
+
+def pin_decode(ora):
+    """Decode = prefill of one query against the sequence's keys; split+combine = unsplit."""
+    q, kc, vc, lens = _decode_case()
+    B, Hq, D = q.shape
+    O, L = ora.decode_forward(q, kc, vc, lens, 0.45)
+    for b in range(B):
+        n = lens[b]
+        kb = kc[b, :n].transpose(1, 0, 2)[None]      # [1, Hkv, n, D]
+        vb = vc[b, :n].transpose(1, 0, 2)[None]
+        Op, Lp = brute_force(q[b][None, :, None, :], kb, vb, 0.45, False, 0)
+        assert np.allclose(O[b], Op[0, :, 0], atol=1e-12) and np.allclose(L[b], Lp[0, :, 0], atol=1e-12)
+    for chunk in (1, 2, 3, 4, 8, 16):
+        Op, Lp, ns = ora.decode_split_partials(q, kc, vc, lens, 0.45, chunk)
+        assert list(ns) == [-(-int(n) // chunk) for n in lens]
+        Oc, Lc = ora.decode_combine(Op, Lp, ns)
+        assert np.allclose(Oc, O, atol=1e-12) and np.allclose(Lc, L, atol=1e-12), f"chunk {chunk}"
+    # each partial is the attention of its own chunk
+    Op, Lp, ns = ora.decode_split_partials(q, kc, vc, lens, 0.45, 4)
+    b, c = 0, 2                                    # keys 8..10 of sequence 0
+    kb = kc[b, 8:11].transpose(1, 0, 2)[None]
+    vb = vc[b, 8:11].transpose(1, 0, 2)[None]
+    Oe, Le = brute_force(q[b][None, :, None, :], kb, vb, 0.45, False, 0)
+    assert np.allclose(Op[b, :, c], Oe[0, :, 0], atol=1e-12) and np.allclose(Lp[b, :, c], Le[0, :, 0], atol=1e-12)
+
+
+# ---------------------------------------------------------------- golden
+def _read_golden(name):
+    env = {"ln": math.log}
+    table = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            head, vals = line.split(":")
+            case, field, row = head.split()
+            assert re.fullmatch(r"[0-9lnN()/.+\- ]*", vals), vals
+            table.setdefault((case, field), {})[int(row)] = [eval(t, {"__builtins__": {}}, env) for t in vals.split()]
+    return {key: np.array([rows[r] for r in sorted(rows)]) for key, rows in table.items()}
+
+
+def pin_golden(ora):
+    G = _read_golden("closed_form_tiny.txt")
+    Q, K, V = (G[("input", f)][None, None] for f in "QKV")
+    for case, causal, window in (("dense", False, 0), ("causal", True, 0), ("window1", True, 1)):
+        O, L = ora.attention_forward(Q, K, V, 1.0, causal, window)
+        assert np.allclose(O[0, 0], G[(case, "O")], rtol=0, atol=1e-14), case
+        assert np.allclose(L[0, 0], G[(case, "LSE")][0], rtol=0, atol=1e-14), case
+    # split-KV of query row 0 with chunk 2, against the hand-derived partials
+    q = Q[0, :, 0][None]                          # [1, 1, D]
+    kc = K[0].transpose(1, 0, 2)[None]            # [1, Nk, 1, D]
+    vc = V[0].transpose(1, 0, 2)[None]
+    Op, Lp, ns = ora.decode_split_partials(q, kc, vc, [3], 1.0, 2)
+    assert np.allclose(Op[0, 0], G[("split2", "O")], atol=1e-14)
+    assert np.allclose(Lp[0, 0], G[("split2", "LSE")][0], atol=1e-14)
+    Oc, Lc = ora.decode_combine(Op, Lp, ns)
+    assert np.allclose(Oc[0, 0], G[("split2", "combinedO")][0], atol=1e-14)
+    assert abs(Lc[0, 0] - G[("split2", "combinedLSE")][0][0]) < 1e-14
+
+
+PINS = [pin_brute_force, pin_sdpa, pin_zero_query, pin_single_key, pin_probability_rows,
+        pin_causal_first_row, pin_dominant_key, pin_invariants, pin_decode, pin_golden]
+
+
+@pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
+def test_oracle_pin(pin):
+    pin(ORA)
+
+
+# ---------------------------------------------------------------- mutation
+def _mut_no_scale(q_rows, k_head, scale):
+    return q_rows @ k_head.T
+
+
+def _mut_sqrt_scale(q_rows, k_head, scale):
+    return math.sqrt(scale) * (q_rows @ k_head.T)
+
+
+def _mut_kv_head_modulo(h, Hq, Hkv):
+    return h % Hkv
+
+
+def _mut_causal_top_left(rows, Nq, Nk, causal, window):
+    i = np.asarray(rows)[:, None]
+    j = np.arange(Nk)[None, :]
+    vis = np.ones((i.shape[0], Nk), bool)
+    if causal:
+        vis &= j <= i
+    if window > 0:
+        vis &= j > i + Nk - Nq - window
+    return vis
+
+
+def _mut_causal_strict(rows, Nq, Nk, causal, window):
+    i = np.asarray(rows)[:, None]
+    j = np.arange(Nk)[None, :]
+    vis = np.ones((i.shape[0], Nk), bool)
+    if causal:
+        vis &= j < i + Nk - Nq
+    if window > 0:
+        vis &= j > i + Nk - Nq - window
+    return vis
+
+
+def _mut_window_wide(rows, Nq, Nk, causal, window):
+    i = np.asarray(rows)[:, None]
+    j = np.arange(Nk)[None, :]
+    vis = np.ones((i.shape[0], Nk), bool)
+    if causal:
+        vis &= j <= i + Nk - Nq
+    if window > 0:
+        vis &= j >= i + Nk - Nq - window
+    return vis
+
+
+def _wrap_softmax(kind):
+    good = ORA._softmax_rows
+
+    def bad(S):
+        P, lse = good(S)
+        if kind == "log2":
+            return P, lse / math.log(2)
+        if kind == "no_max":
+            M = np.where(np.isfinite(S.max(axis=1)), S.max(axis=1), 0.0)
+            return P, lse - M
+        if kind == "key_axis_swapped":
+            E = np.exp(S - np.where(np.isfinite(S), S, -np.inf).max(axis=0, keepdims=True))
+            E = np.nan_to_num(E)
+            with np.errstate(invalid="ignore", divide="ignore"):
+                P2 = np.nan_to_num(E / E.sum(axis=0, keepdims=True))
+            return P2, lse
+        raise AssertionError(kind)
+    return bad
+
+
+def _mut_combine_unweighted(O_part, LSE_part, n_split):
+    O_part, LSE_part = np.asarray(O_part), np.asarray(LSE_part)
+    B, Hq, _, D = O_part.shape
+    O = np.zeros((B, Hq, D))
+    L = np.zeros((B, Hq))
+    for b in range(B):
+        n = int(n_split[b])
+        O[b] = O_part[b, :, :n].mean(axis=1)
+        L[b] = np.log(np.exp(LSE_part[b, :, :n]).sum(axis=1))
+    return O, L
+
+
+MUTANTS = {
+    "no_scale": ("_scores", _mut_no_scale),
+    "sqrt_scale": ("_scores", _mut_sqrt_scale),
+    "kv_head_modulo": ("kv_head", _mut_kv_head_modulo),
+    "causal_top_left": ("visible_mask", _mut_causal_top_left),
+    "causal_strict": ("visible_mask", _mut_causal_strict),
+    "window_off_by_one": ("visible_mask", _mut_window_wide),
+    "lse_log2": ("_softmax_rows", _wrap_softmax("log2")),
+    "lse_missing_max": ("_softmax_rows", _wrap_softmax("no_max")),
+    "softmax_over_queries": ("_softmax_rows", _wrap_softmax("key_axis_swapped")),
+    "combine_unweighted": ("decode_combine", _mut_combine_unweighted),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutants_are_caught(name, monkeypatch):
+    attr, fn = MUTANTS[name]
+    monkeypatch.setattr(ORA, attr, fn)
+    failed = []
+    for pin in PINS:
+        try:
+            with np.errstate(all="ignore"):
+                pin(ORA)
+        except (AssertionError, ValueError, IndexError, ZeroDivisionError):
+            failed.append(pin.__name__)
+    assert failed, f"mutant {name} passed every pin"
