@@ -1,0 +1,156 @@
+/*
+ * attn.h — C ABI of the GB300 (sm_103a) fused softmax-attention library.
+ *
+ * The operation is softmax attention O = softmax(Q K^T * scale + mask) V,
+ * computed with online softmax so that the score matrix S is never stored,
+ * plus the per-row log-sum-exp LSE = ln sum_j exp(s_ij).
+ *
+ * Sources (web pages on softmax attention):
+ *   [DEVLOG] "Agent 帮我写 CUDA：一个 Softmax Attention 算子的开发全记录", a fp32
+ *            softmax-attention CUDA development log: section 二 "参考基线" (the
+ *            operator on [B,H,N,D] tensors and its SDPA reference), section 三
+ *            "Step 1：Naive 版本" (raw-pointer kernel signature, a shared library
+ *            called from Python), section 四 "Tiled Attention 的核心思想" (the
+ *            online-softmax recurrence and the tile loop).
+ *   [ASK]    "Ask, Don't Equip: Question-Driven Coding Agents for Deep Kernel
+ *            Optimization", section "研究动机": GQA, causal / sliding-window masks
+ *            and split-KV decode as parts of the attention forward's feature
+ *            surface.
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller.  The library
+ *     never allocates, frees or copies device memory and never synchronises,
+ *     except in attn_get_device_error().  Work is queued on `stream`
+ *     (NULL = the legacy default stream) and runs asynchronously.
+ *   - Tensors are dense and contiguous, row-major in the order their shape is
+ *     written.  Every tensor pointer must be 16-byte aligned.
+ *   - Masking: key j is visible to query i iff j < Nk, and, when causal != 0,
+ *     j <= i + Nk - Nq (bottom-right aligned: j <= i when Nq == Nk), and, when
+ *     window > 0, j > i + Nk - Nq - window (the last `window` keys up to the
+ *     diagonal).  window <= 0 disables the window.  There is no additive mask
+ *     tensor.  A query row that sees no key gets O = 0 and LSE = -inf.
+ *   - GQA: query head h reads KV head h / (Hq / Hkv); Hq must be a multiple of
+ *     Hkv (Hkv == Hq is plain multi-head attention, Hkv == 1 multi-query).
+ *   - LSE is the natural logarithm of the softmax denominator of the scaled,
+ *     masked scores, in fp32.
+ *   - Return value: ATTN_OK (0) or a negative ATTN_ERR_* code.  Argument errors
+ *     are detected on the host before anything is queued.  Errors found on the
+ *     device (an expired bounded wait, an out-of-range sequence length) are
+ *     recorded in a per-device error word and reported by the next call to
+ *     attn_get_device_error().
+ */
+#ifndef SOFTMAX_ATTENTION_ATTN_GB300_ATTN_H
+#define SOFTMAX_ATTENTION_ATTN_GB300_ATTN_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* attn_stream_t;
+
+enum attn_status {
+  ATTN_OK = 0,
+  ATTN_ERR_NULL = -1,        /* a required pointer is NULL                              */
+  ATTN_ERR_DIM = -2,         /* a size is non-positive or too large                     */
+  ATTN_ERR_GQA = -3,         /* Hq is not a multiple of Hkv                             */
+  ATTN_ERR_HEAD_DIM = -4,    /* head dimension D not supported by this entry point      */
+  ATTN_ERR_ALIGN = -5,       /* a tensor pointer is not 16-byte aligned                 */
+  ATTN_ERR_SCALE = -6,       /* scale is not finite or not > 0                          */
+  ATTN_ERR_CUDA = -7,        /* a CUDA runtime / launch error                           */
+  ATTN_ERR_TIMEOUT = -8,     /* a bounded device-side wait expired (kernel gave up)     */
+  ATTN_ERR_DEVICE = -9,      /* the current device is not an sm_103 GPU                */
+  ATTN_ERR_SEQLEN = -10,     /* a decode sequence length is < 1 or > Nk_max (device)   */
+  ATTN_ERR_CHUNK = -11,      /* split-KV chunk size not supported                       */
+  ATTN_ERR_CAPACITY = -12    /* a size exceeds a fixed capacity of the entry point      */
+};
+
+/*
+ * attn_fwd — bf16 fused attention forward on tensor cores (tcgen05 / TMEM).
+ *   [DEVLOG] 二 "参考基线" (operator), 四 "Tiled Attention 的核心思想" (online
+ *   softmax over K/V tiles); [ASK] "研究动机" (GQA, causal, sliding window).
+ *
+ *   q   : bf16 [B, Hq,  Nq, D]        k, v : bf16 [B, Hkv, Nk, D]
+ *   o   : bf16 [B, Hq,  Nq, D] (out)  lse  : fp32 [B, Hq, Nq] (out; may be NULL)
+ *   D must be 128.  Scores and accumulation are fp32; P is rounded to bf16
+ *   before the P V product; O is rounded to bf16 (round-to-nearest-even).
+ *   scale multiplies Q K^T (1/sqrt(D) for standard attention).
+ *   Errors: ATTN_ERR_NULL, _DIM, _GQA, _HEAD_DIM, _ALIGN, _SCALE, _DEVICE, _CUDA.
+ */
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+             int B, int Hq, int Hkv, int Nq, int Nk, int D,
+             float scale, int causal, int window, attn_stream_t stream);
+
+/*
+ * attn_fwd_fp32 — fp32 fused attention forward on the FP32 SIMT pipes.
+ *   [DEVLOG] 三 (fp32 [B,H,N,D] operator), 四 (tiled online softmax),
+ *   五 (16-byte vector loads, padded shared-memory rows).
+ *
+ *   Same shapes, masks and error codes as attn_fwd, with fp32 q, k, v, o.
+ *   D must be 32, 64 or 128.  No reduced-precision arithmetic is used.
+ */
+int attn_fwd_fp32(const float* q, const float* k, const float* v, float* o, float* lse,
+                  int B, int Hq, int Hkv, int Nq, int Nk, int D,
+                  float scale, int causal, int window, attn_stream_t stream);
+
+/*
+ * attn_decode_workspace_size — bytes of device workspace that
+ * attn_decode_splitkv fills and attn_decode_combine reads:
+ *   fp32 O_part [B, Hq, S_max, D] followed by fp32 LSE_part [B, Hq, S_max],
+ *   S_max = ceil(Nk_max / chunk).  Returns 0 for invalid sizes.
+ */
+size_t attn_decode_workspace_size(int B, int Hq, int D, int Nk_max, int chunk);
+
+/*
+ * attn_decode_splitkv — split-KV decode, partial step.   [ASK] "研究动机"
+ *   (split-KV decode); each chunk's result is the tiled online softmax of
+ *   [DEVLOG] 四 restricted to the chunk's keys.
+ *
+ *   q        : bf16 [B, Hq, D]              (one query token per sequence)
+ *   k_cache  : bf16 [B, Nk_max, Hkv, D]     v_cache : bf16 [B, Nk_max, Hkv, D]
+ *   seqlens  : int32 [B] (device)           sequence b uses rows 0..seqlens[b]-1
+ *   workspace: device buffer of attn_decode_workspace_size(B, Hq, D, Nk_max, chunk)
+ *              bytes.  For each b, head h and chunk c < ceil(seqlens[b]/chunk)
+ *              (keys c*chunk .. min((c+1)*chunk, seqlens[b]) - 1) it receives the
+ *              chunk's normalised output O_c and its LSE_c; other entries are
+ *              left untouched.
+ *   D must be 128; Hq / Hkv must be 1, 2, 4 or 8; chunk must be a multiple of
+ *   64 in [64, 1024].  A seqlens[b] outside [1, Nk_max] sets ATTN_ERR_SEQLEN in
+ *   the device error word and that sequence is skipped.
+ *   Errors: ATTN_ERR_NULL, _DIM, _GQA, _HEAD_DIM, _ALIGN, _SCALE, _CHUNK,
+ *   _DEVICE, _CUDA.
+ */
+int attn_decode_splitkv(const void* q, const void* k_cache, const void* v_cache,
+                        const int* seqlens, void* workspace,
+                        int B, int Hq, int Hkv, int Nk_max, int D,
+                        float scale, int chunk, attn_stream_t stream);
+
+/*
+ * attn_decode_combine — split-KV decode, combine step.  LSE-weighted merge of
+ * the chunk results written by attn_decode_splitkv:
+ *   M = max_c LSE_c,  w_c = exp(LSE_c - M),  O = sum_c w_c O_c / sum_c w_c,
+ *   LSE = M + ln sum_c w_c,   over c < ceil(seqlens[b] / chunk).
+ *   o : bf16 [B, Hq, D] (out)        lse : fp32 [B, Hq] (out; may be NULL)
+ *   Arguments B, Hq, Nk_max, D, chunk must equal those of the splitkv call.
+ *   Errors: as attn_decode_splitkv.
+ */
+int attn_decode_combine(const void* workspace, const int* seqlens, void* o, float* lse,
+                        int B, int Hq, int Nk_max, int D, int chunk,
+                        attn_stream_t stream);
+
+/*
+ * attn_get_device_error — synchronises `stream`, then returns and clears the
+ * current device's error word (ATTN_OK if no kernel reported an error).  A
+ * CUDA error seen while synchronising is returned as ATTN_ERR_CUDA.
+ */
+int attn_get_device_error(attn_stream_t stream);
+
+/* attn_strerror — static, human-readable text for a status code. */
+const char* attn_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SOFTMAX_ATTENTION_ATTN_GB300_ATTN_H */

@@ -1,0 +1,175 @@
+"""ctypes binding of the C ABI in ``include/attn.h`` (argument marshalling only).
+
+Every function here forwards torch tensors' device pointers to the library;
+all arithmetic runs in the library's CUDA kernels.  There is no CPU or PyTorch
+fallback: if ``libattn.so`` is missing or fails to load, :func:`lib` raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libattn.so")
+
+ATTN_OK = 0
+STATUS = {
+    0: "ATTN_OK", -1: "ATTN_ERR_NULL", -2: "ATTN_ERR_DIM", -3: "ATTN_ERR_GQA",
+    -4: "ATTN_ERR_HEAD_DIM", -5: "ATTN_ERR_ALIGN", -6: "ATTN_ERR_SCALE", -7: "ATTN_ERR_CUDA",
+    -8: "ATTN_ERR_TIMEOUT", -9: "ATTN_ERR_DEVICE", -10: "ATTN_ERR_SEQLEN",
+    -11: "ATTN_ERR_CHUNK", -12: "ATTN_ERR_CAPACITY",
+}
+
+_c_int, _c_float, _vp = ctypes.c_int, ctypes.c_float, ctypes.c_void_p
+SIGNATURES = {
+    "attn_fwd": (_c_int, [_vp, _vp, _vp, _vp, _vp] + [_c_int] * 6 + [_c_float, _c_int, _c_int, _vp]),
+    "attn_fwd_fp32": (_c_int, [_vp, _vp, _vp, _vp, _vp] + [_c_int] * 6 + [_c_float, _c_int, _c_int, _vp]),
+    "attn_decode_workspace_size": (ctypes.c_size_t, [_c_int] * 5),
+    "attn_decode_splitkv": (_c_int, [_vp] * 5 + [_c_int] * 5 + [_c_float, _c_int, _vp]),
+    "attn_decode_combine": (_c_int, [_vp] * 4 + [_c_int] * 5 + [_vp]),
+    "attn_get_device_error": (_c_int, [_vp]),
+    "attn_strerror": (ctypes.c_char_p, [_c_int]),
+}
+
+_LIB = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {STATUS.get(code, code)} ({strerror(code)})")
+
+
+def lib(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load ``libattn.so`` (once) and declare its signatures."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: run softmax_attention_attn_gb300.build.build() first")
+        handle = ctypes.CDLL(path)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(handle, name)
+            fn.restype, fn.argtypes = res, args
+        _LIB = handle
+    return _LIB
+
+
+def strerror(code: int) -> str:
+    return lib().attn_strerror(int(code)).decode()
+
+
+def _check(code: int, where: str) -> None:
+    if code != ATTN_OK:
+        raise AttnError(code, where)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _require(t, dtype, name):
+    import torch
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _fwd(name, dtype, q, k, v, o, lse, scale, causal, window, stream):
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _require(t, dtype, n)
+    B, Hq, Nq, D = q.shape
+    _, Hkv, Nk, _ = k.shape
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(B, Hq, Nq, device=q.device, dtype=torch.float32)
+    _require(o, dtype, "o")
+    _require(lse, torch.float32, "lse")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    code = getattr(lib(), name)(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Nq, Nk, D,
+                                scale, int(bool(causal)), int(window), _stream(stream))
+    _check(code, name)
+    return o, lse
+
+
+def attn_fwd(q, k, v, o=None, lse=None, scale=None, causal=False, window=0, stream=None):
+    """bf16 forward: q ``[B,Hq,Nq,D]``, k/v ``[B,Hkv,Nk,D]`` -> (o, lse)."""
+    import torch
+    return _fwd("attn_fwd", torch.bfloat16, q, k, v, o, lse, scale, causal, window, stream)
+
+
+def attn_fwd_fp32(q, k, v, o=None, lse=None, scale=None, causal=False, window=0, stream=None):
+    """fp32 forward: same layouts as :func:`attn_fwd`."""
+    import torch
+    return _fwd("attn_fwd_fp32", torch.float32, q, k, v, o, lse, scale, causal, window, stream)
+
+
+def attn_decode_workspace_size(B, Hq, D, Nk_max, chunk=512) -> int:
+    return int(lib().attn_decode_workspace_size(B, Hq, D, Nk_max, chunk))
+
+
+def attn_decode_splitkv(q, k_cache, v_cache, seqlens, workspace, scale=None, chunk=512, stream=None):
+    """Partial step: fills ``workspace`` (uint8 CUDA tensor) with per-chunk O and LSE."""
+    import torch
+    _require(q, torch.bfloat16, "q")
+    _require(k_cache, torch.bfloat16, "k_cache")
+    _require(v_cache, torch.bfloat16, "v_cache")
+    _require(seqlens, torch.int32, "seqlens")
+    B, Hq, D = q.shape
+    _, Nk_max, Hkv, _ = k_cache.shape
+    need = attn_decode_workspace_size(B, Hq, D, Nk_max, chunk)
+    if workspace.numel() * workspace.element_size() < need:
+        raise ValueError(f"workspace holds fewer than {need} bytes")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    code = lib().attn_decode_splitkv(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seqlens), _ptr(workspace),
+                                     B, Hq, Hkv, Nk_max, D, scale, int(chunk), _stream(stream))
+    _check(code, "attn_decode_splitkv")
+    return workspace
+
+
+def attn_decode_combine(workspace, seqlens, B, Hq, Nk_max, D, o=None, lse=None, chunk=512,
+                        device=None, stream=None):
+    """Combine step: merges the chunk results into ``o [B,Hq,D]`` bf16 and ``lse [B,Hq]``."""
+    import torch
+    device = workspace.device if device is None else device
+    if o is None:
+        o = torch.empty(B, Hq, D, device=device, dtype=torch.bfloat16)
+    if lse is None:
+        lse = torch.empty(B, Hq, device=device, dtype=torch.float32)
+    _require(o, torch.bfloat16, "o")
+    _require(lse, torch.float32, "lse")
+    _require(seqlens, torch.int32, "seqlens")
+    code = lib().attn_decode_combine(_ptr(workspace), _ptr(seqlens), _ptr(o), _ptr(lse),
+                                     B, Hq, Nk_max, D, int(chunk), _stream(stream))
+    _check(code, "attn_decode_combine")
+    return o, lse
+
+
+def attn_decode(q, k_cache, v_cache, seqlens, workspace=None, o=None, lse=None, scale=None,
+                chunk=512, stream=None):
+    """Split-KV decode: partial step then combine step on the same stream."""
+    import torch
+    B, Hq, D = q.shape
+    Nk_max = k_cache.shape[1]
+    if workspace is None:
+        workspace = torch.empty(attn_decode_workspace_size(B, Hq, D, Nk_max, chunk),
+                                device=q.device, dtype=torch.uint8)
+    attn_decode_splitkv(q, k_cache, v_cache, seqlens, workspace, scale, chunk, stream)
+    return attn_decode_combine(workspace, seqlens, B, Hq, Nk_max, D, o, lse, chunk, q.device, stream)
+
+
+def get_device_error(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device error word."""
+    return int(lib().attn_get_device_error(_stream(stream)))

@@ -1,0 +1,455 @@
+// attn_decode.cu — split-KV decode for sm_103a: partial step and combine step.
+//
+// Split-KV decode is one mode of the attention forward's feature surface in
+// "Ask, Don't Equip: Question-Driven Coding Agents for Deep Kernel Optimization"
+// (section "研究动机"); each chunk is the tiled online-softmax attention of
+// "Agent 帮我写 CUDA：一个 Softmax Attention 算子的开发全记录" (section 四)
+// restricted to the chunk's keys.  Chunks cover keys [c*chunk, (c+1)*chunk) of
+// each sequence; the combine step weights chunk c by exp(LSE_c - max LSE).
+//
+// The partial step is bound by HBM bandwidth (about 2 flops per byte), so it
+// uses no tensor cores.  Design:
+//   * persistent CTAs walk a work list of (sequence b, chunk c, KV head) items,
+//     built in shared memory from the device-side sequence lengths (no host
+//     round trip); the KV heads of one chunk are adjacent items, so
+//     neighbouring CTAs read neighbouring 256-byte rows of the cache;
+//   * one producer thread streams 64-key K and V tiles ([64 keys][128] bf16,
+//     16 KB) through a 5-slot TMA ring, so 80 KB per CTA (two CTAs per SM)
+//     are in flight;
+//   * four consumer warps: all G = Hq/Hkv query heads of the KV head share
+//     each K/V tile.  For the scores, a thread multiplies 16 bytes of 8 key
+//     rows by the G query slices it holds in registers and a 16-lane
+//     reduce-scatter (halving exchange) finishes the dot products with about
+//     one shuffle per score.  The chunk's softmax runs in shared memory in the
+//     exp2 domain; P V accumulates per thread and is reduced across the eight
+//     key groups through shared memory.
+#include <cuda_runtime.h>
+#include <math_constants.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace attn {
+namespace decode {
+
+constexpr int HD = 128;
+constexpr int TILE = 64;                      // keys per TMA tile
+constexpr int TILE_BYTES = TILE * HD * 2;     // 16 KB
+constexpr int STAGES = 5;
+constexpr int NCW = 4;                        // consumer warps
+constexpr int NC = NCW * 32;                  // consumer threads
+constexpr int NTHREADS = NC + 32;             // + producer warp
+
+struct Layout {
+  int ring, work, stats, bars, misc, split, bytes;
+};
+
+__host__ __device__ inline Layout layout(int G, int chunk, int B) {
+  Layout L;
+  L.ring = 0;
+  L.work = L.ring + STAGES * TILE_BYTES;
+  const int scores = G * chunk * 4;
+  const int red = 8 * G * HD * 4;
+  L.stats = L.work + (scores > red ? scores : red);
+  L.bars = L.stats + 2 * 8 * 4;                // m[8], l[8]
+  L.misc = L.bars + 2 * STAGES * 8;
+  L.split = L.misc + 16;                       // misc: abort flag, stop flag
+  L.bytes = L.split + (B + 1) * 4;
+  return L;
+}
+
+// 16-lane reduce-scatter: V partial sums per lane -> complete sums, R = max(V/16,1)
+// per lane.  Lane g (0..15) ends with value indices g*R .. g*R+R-1 (V >= 16) or
+// g/2 (V == 8, lane pairs hold the same value).
+template <int V>
+__device__ __forceinline__ void reduce_scatter16(float (&v)[V], int g) {
+#pragma unroll
+  for (int st = 0; st < 4; ++st) {
+    const int o = 8 >> st;
+    const int n = V >> st;
+    const bool hi = (g & o) != 0;
+    if (n > 1) {
+#pragma unroll
+      for (int i = 0; i < n / 2; ++i) {
+        const float keep = hi ? v[i + n / 2] : v[i];
+        const float send = hi ? v[i] : v[i + n / 2];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+      }
+    } else {
+      v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
+    }
+  }
+}
+
+__device__ __forceinline__ void bf16x8_to_float(const uint4& u, float (&f)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+struct Work {
+  int b, c, kvh, n_valid, ntl;
+};
+
+__device__ __forceinline__ Work decode_work(int w, const int* split, int B, int Hkv, int chunk,
+                                            const int* __restrict__ seqlens) {
+  Work r;
+  const int gc = w / Hkv;
+  r.kvh = w - gc * Hkv;
+  int lo = 0, hi = B;  // largest b with split[b] <= gc
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (split[mid] <= gc) lo = mid; else hi = mid;
+  }
+  r.b = lo;
+  r.c = gc - split[lo];
+  const int L = __ldg(seqlens + lo);
+  r.n_valid = min(chunk, L - r.c * chunk);
+  r.ntl = (r.n_valid + TILE - 1) / TILE;
+  return r;
+}
+
+template <int G>
+__global__ void __launch_bounds__(NTHREADS, 2)
+attn_decode_splitkv_kernel(const __grid_constant__ CUtensorMap tm_k,
+                           const __grid_constant__ CUtensorMap tm_v,
+                           const __nv_bfloat16* __restrict__ q, const int* __restrict__ seqlens,
+                           float* __restrict__ ws_o, float* __restrict__ ws_lse, int B, int Hq,
+                           int Hkv, int Nk_max, int chunk, int S_max, float c_log2, int* err) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  const uint32_t sb = smem_u32(smem);
+  const Layout L = layout(G, chunk, B);
+  float* work = reinterpret_cast<float*>(smem + L.work);   // scores / p, then reduction buffer
+  float* st_m = reinterpret_cast<float*>(smem + L.stats);
+  float* st_l = st_m + 8;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc);
+  int* split = reinterpret_cast<int*>(smem + L.split);
+  auto bar_full = [&](int s) { return sb + L.bars + 8u * s; };
+  auto bar_empty = [&](int s) { return sb + L.bars + 8u * (STAGES + s); };
+
+  const int warp = warp_id_uniform();
+  const int lane = static_cast<int>(lane_id());
+  const int tid = static_cast<int>(threadIdx.x);
+
+  if (tid == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(bar_full(s), 1);
+      mbar_init(bar_empty(s), NCW);
+    }
+    abort_flag[0] = 0;
+    abort_flag[1] = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  // ---- work list: split[b] = number of chunks of sequences 0..b-1 (one warp)
+  if (warp == 0) {
+    const int per = (B + 31) / 32;
+    const int b0 = min(B, lane * per), b1 = min(B, b0 + per);
+    int local = 0;
+    for (int b = b0; b < b1; ++b) {
+      const int Lb = seqlens[b];
+      if (Lb < 1 || Lb > Nk_max) {
+        atomicCAS(err, 0, ATTN_ERR_SEQLEN);
+        continue;
+      }
+      local += (Lb + chunk - 1) / chunk;
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    int run = incl - local;
+    for (int b = b0; b < b1; ++b) {
+      split[b] = run;
+      const int Lb = seqlens[b];
+      if (Lb >= 1 && Lb <= Nk_max) run += (Lb + chunk - 1) / chunk;
+    }
+    if (lane == 31) split[B] = incl;
+  }
+  __syncthreads();
+  const int total = split[B] * Hkv;
+
+  if (warp == NCW) {
+    // ================================================================ producer
+    if (lane == 0) {
+      int it = 0;
+      bool ok = true;
+      for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+        const Work wk = decode_work(w, split, B, Hkv, chunk, seqlens);
+        for (int kv = 0; kv < 2 && ok; ++kv) {
+          const CUtensorMap* m = kv ? &tm_v : &tm_k;
+          for (int tl = 0; tl < wk.ntl; ++tl, ++it) {
+            const int s = it % STAGES, u = it / STAGES;
+            if (u > 0 && !mbar_wait(bar_empty(s), (u - 1) & 1, abort_flag, err)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(bar_full(s), TILE_BYTES);
+            tma_load_4d(sb + L.ring + s * TILE_BYTES, m, bar_full(s), 0, wk.kvh,
+                        wk.c * chunk + tl * TILE, wk.b);
+          }
+        }
+      }
+      if (!ok) {
+        for (int i = max(0, it - STAGES); i < it; ++i) {
+          const unsigned long long t0 = global_ns();
+          while (!mbar_try_wait(bar_full(i % STAGES), (i / STAGES) & 1))
+            if (global_ns() - t0 > kAttnWaitNs) break;
+        }
+      }
+    }
+    return;
+  }
+
+  // ==================================================================== consumers
+  // A failed (timed-out) wait never breaks out of the item early: every
+  // consumer keeps reaching the same named barriers, and the decision to stop
+  // is taken at the end of the item from one shared copy of the abort flag.
+  volatile int* stop = abort_flag + 1;
+  const int g16 = tid & 15;       // 16-byte column slice of a 256-byte row
+  const int ksub = tid >> 4;      // key sub-group 0..7
+  constexpr int V = 8 * G;        // partial sums per thread per tile
+  constexpr int R = V >= 16 ? V / 16 : 1;
+  int it = 0;
+  for (int w = blockIdx.x; w < total; w += gridDim.x) {
+    const Work wk = decode_work(w, split, B, Hkv, chunk, seqlens);
+    const int h0 = wk.kvh * G;
+    float qr[G][8];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const uint4 u = __ldg(reinterpret_cast<const uint4*>(q + (static_cast<size_t>(wk.b) * Hq + h0 + h) * HD) + g16);
+      bf16x8_to_float(u, qr[h]);
+    }
+    // ---- phase 1: scores s[h][key] = q_h . k_key
+    bool ok = true;
+    for (int tl = 0; tl < wk.ntl; ++tl, ++it) {
+      const int s = it % STAGES;
+      ok = ok && __all_sync(0xffffffffu, mbar_wait(bar_full(s), (it / STAGES) & 1, abort_flag, err));
+      if (!ok) continue;
+      const uint8_t* tile = smem + L.ring + s * TILE_BYTES;
+      float v[V];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int key = ksub + 8 * i;
+        const uint4 u = *reinterpret_cast<const uint4*>(tile + key * (HD * 2) + g16 * 16);
+        float kf[8];
+        bf16x8_to_float(u, kf);
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          float a = 0.f;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) a = fmaf(qr[h][e], kf[e], a);
+          v[i * G + h] = a;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_empty(s));
+      reduce_scatter16<V>(v, g16);
+      if (V >= 16 || (g16 & 1) == 0) {
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          const int idx = V >= 16 ? g16 * R + r : (g16 >> 1);
+          const int i = idx / G, h = idx % G;
+          const int key = tl * TILE + ksub + 8 * i;
+          work[h * chunk + key] = key < wk.n_valid ? v[r] : -CUDART_INF_F;
+        }
+      }
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(NC) : "memory");
+    // ---- phase 2: chunk softmax per head (exp2 domain), p written in place
+    const int nk_pad = wk.ntl * TILE;
+    for (int h = warp; h < G; h += NCW) {
+      float* sh = work + h * chunk;
+      float mx = -CUDART_INF_F;
+      for (int j = lane; j < nk_pad; j += 32) mx = fmaxf(mx, sh[j]);
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      const float m = (mx == -CUDART_INF_F) ? 0.f : mx * c_log2;
+      float sum = 0.f;
+      for (int j = lane; j < nk_pad; j += 32) {
+        const float pv = ex2_approx(fmaf(sh[j], c_log2, -m));
+        sh[j] = pv;
+        sum += pv;
+      }
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      if (lane == 0) {
+        st_m[h] = m;
+        st_l[h] = sum;
+      }
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(NC) : "memory");
+    // ---- phase 3: O = sum_key p[h][key] v_key
+    float acc[G][8];
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[h][e] = 0.f;
+    for (int tl = 0; tl < wk.ntl; ++tl, ++it) {
+      const int s = it % STAGES;
+      ok = ok && __all_sync(0xffffffffu, mbar_wait(bar_full(s), (it / STAGES) & 1, abort_flag, err));
+      if (!ok) continue;
+      const uint8_t* tile = smem + L.ring + s * TILE_BYTES;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int key = ksub + 8 * i;
+        const uint4 u = *reinterpret_cast<const uint4*>(tile + key * (HD * 2) + g16 * 16);
+        float vf[8];
+        bf16x8_to_float(u, vf);
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          const float pw = work[h * chunk + tl * TILE + key];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) acc[h][e] = fmaf(pw, vf[e], acc[h][e]);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_empty(s));
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(NC) : "memory");  // p no longer needed
+    float* red = work;                                      // [8][G][HD]
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      float4* dst = reinterpret_cast<float4*>(red + (ksub * G + h) * HD + g16 * 8);
+      dst[0] = make_float4(acc[h][0], acc[h][1], acc[h][2], acc[h][3]);
+      dst[1] = make_float4(acc[h][4], acc[h][5], acc[h][6], acc[h][7]);
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(NC) : "memory");
+    {
+      const int d = tid;  // 0..127
+      const size_t base = (static_cast<size_t>(wk.b) * Hq + h0) * S_max + wk.c;
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        float o = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) o += red[(k * G + h) * HD + d];
+        ws_o[(base + static_cast<size_t>(h) * S_max) * HD + d] = o / st_l[h];
+      }
+      if (tid < G) ws_lse[base + static_cast<size_t>(tid) * S_max] = (st_m[tid] + log2f(st_l[tid])) * 0.69314718055994531f;
+      if (tid == 0) *stop = *abort_flag;
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(NC) : "memory");  // red free for the next item
+    if (*stop) break;
+  }
+}
+
+// One warp per (b, h): LSE-weighted merge of the chunk results.
+__global__ void __launch_bounds__(128)
+attn_decode_combine_kernel(const float* __restrict__ ws_o, const float* __restrict__ ws_lse,
+                           const int* __restrict__ seqlens, __nv_bfloat16* __restrict__ o,
+                           float* __restrict__ lse, int B, int Hq, int Nk_max, int chunk, int S_max,
+                           int* err) {
+  const int lane = static_cast<int>(lane_id());
+  const int bh = static_cast<int>(blockIdx.x) * 4 + static_cast<int>(threadIdx.x >> 5);
+  if (bh >= B * Hq) return;
+  const int b = bh / Hq;
+  const int Lb = __ldg(seqlens + b);
+  __nv_bfloat16* orow = o + static_cast<size_t>(bh) * HD + lane * 4;
+  if (Lb < 1 || Lb > Nk_max) {
+    if (lane == 0) atomicCAS(err, 0, ATTN_ERR_SEQLEN);
+    *reinterpret_cast<uint2*>(orow) = make_uint2(0u, 0u);
+    if (lane == 0 && lse != nullptr) lse[bh] = -CUDART_INF_F;
+    return;
+  }
+  const int n = (Lb + chunk - 1) / chunk;
+  const float* lp = ws_lse + static_cast<size_t>(bh) * S_max;
+  const float* op = ws_o + static_cast<size_t>(bh) * S_max * HD + lane * 4;
+  float M = -CUDART_INF_F;
+  for (int c = lane; c < n; c += 32) M = fmaxf(M, lp[c]);
+#pragma unroll
+  for (int k = 16; k >= 1; k >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, k));
+  constexpr float LOG2E = 1.4426950408889634f;
+  float s = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int c0 = 0; c0 < n; c0 += 32) {
+    const float wc = (c0 + lane < n) ? ex2_approx((lp[c0 + lane] - M) * LOG2E) : 0.f;
+    s += wc;
+    const int cnt = min(32, n - c0);
+    for (int j = 0; j < cnt; ++j) {
+      const float w = __shfl_sync(0xffffffffu, wc, j);
+      const float4 x = *reinterpret_cast<const float4*>(op + static_cast<size_t>(c0 + j) * HD);
+      acc.x = fmaf(w, x.x, acc.x);
+      acc.y = fmaf(w, x.y, acc.y);
+      acc.z = fmaf(w, x.z, acc.z);
+      acc.w = fmaf(w, x.w, acc.w);
+    }
+  }
+#pragma unroll
+  for (int k = 16; k >= 1; k >>= 1) s += __shfl_xor_sync(0xffffffffu, s, k);
+  const float inv = 1.f / s;
+  *reinterpret_cast<uint2*>(orow) =
+      make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+  if (lane == 0 && lse != nullptr) lse[bh] = M + logf(s);
+}
+
+template <int G>
+int launch_split(const CUtensorMap& tk, const CUtensorMap& tv, const void* q, const int* seqlens,
+                 float* ws_o, float* ws_lse, int B, int Hq, int Hkv, int Nk_max, float scale,
+                 int chunk, int S_max, int num_sms, cudaStream_t stream, int* err) {
+  const Layout L = layout(G, chunk, B);
+  const int smem = L.bytes + 1024;
+  static int attr_dev = -1;
+  static int attr_bytes = 0;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (attr_dev != dev || attr_bytes < smem) {
+    if (cudaFuncSetAttribute(attn_decode_splitkv_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    attr_dev = dev;
+    attr_bytes = smem;
+  }
+  const int grid = 2 * num_sms;
+  attn_decode_splitkv_kernel<G><<<grid, NTHREADS, smem, stream>>>(
+      tk, tv, static_cast<const __nv_bfloat16*>(q), seqlens, ws_o, ws_lse, B, Hq, Hkv, Nk_max, chunk,
+      S_max, scale * 1.4426950408889634f, err);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // namespace decode
+
+int launch_decode_splitkv(const void* q, const void* k_cache, const void* v_cache,
+                          const int* seqlens, void* workspace, int B, int Hq, int Hkv,
+                          int Nk_max, float scale, int chunk, int num_sms, cudaStream_t stream,
+                          int* err) {
+  using namespace decode;
+  CUtensorMap tk, tv;
+  const uint32_t box[4] = {HD, 1, TILE, 1};
+  if (!encode_tiled_4d(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, k_cache, HD, Hkv, Nk_max, B, 2, box,
+                       CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !encode_tiled_4d(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, v_cache, HD, Hkv, Nk_max, B, 2, box,
+                       CU_TENSOR_MAP_SWIZZLE_NONE))
+    return ATTN_ERR_CUDA;
+  const int S_max = (Nk_max + chunk - 1) / chunk;
+  float* ws_o = static_cast<float*>(workspace);
+  float* ws_lse = ws_o + static_cast<size_t>(B) * Hq * S_max * HD;
+  switch (Hq / Hkv) {
+    case 1: return launch_split<1>(tk, tv, q, seqlens, ws_o, ws_lse, B, Hq, Hkv, Nk_max, scale, chunk, S_max, num_sms, stream, err);
+    case 2: return launch_split<2>(tk, tv, q, seqlens, ws_o, ws_lse, B, Hq, Hkv, Nk_max, scale, chunk, S_max, num_sms, stream, err);
+    case 4: return launch_split<4>(tk, tv, q, seqlens, ws_o, ws_lse, B, Hq, Hkv, Nk_max, scale, chunk, S_max, num_sms, stream, err);
+    case 8: return launch_split<8>(tk, tv, q, seqlens, ws_o, ws_lse, B, Hq, Hkv, Nk_max, scale, chunk, S_max, num_sms, stream, err);
+    default: return ATTN_ERR_GQA;
+  }
+}
+
+int launch_decode_combine(const void* workspace, const int* seqlens, void* o, float* lse, int B,
+                          int Hq, int Nk_max, int chunk, cudaStream_t stream, int* err) {
+  using namespace decode;
+  const int S_max = (Nk_max + chunk - 1) / chunk;
+  const float* ws_o = static_cast<const float*>(workspace);
+  const float* ws_lse = ws_o + static_cast<size_t>(B) * Hq * S_max * HD;
+  const int grid = (B * Hq + 3) / 4;
+  attn_decode_combine_kernel<<<grid, 128, 0, stream>>>(ws_o, ws_lse, seqlens,
+                                                        static_cast<__nv_bfloat16*>(o), lse, B, Hq,
+                                                        Nk_max, chunk, S_max, err);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // namespace attn

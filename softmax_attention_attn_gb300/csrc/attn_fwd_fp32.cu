@@ -1,0 +1,277 @@
+// attn_fwd_fp32.cu — fp32 fused attention forward on the FP32 SIMT pipes.
+//
+// Follows "Agent 帮我写 CUDA：一个 Softmax Attention 算子的开发全记录": the tiled
+// kernel of section 四 (a block owns a tile of query rows, loops over K/V tiles
+// held in shared memory and merges the online-softmax state across tiles), the
+// 16-byte vector loads and padded shared-memory rows of section 五, and the
+// head-dimension-specific compilation of section 六 (one instantiation per D).
+// Differences for sm_103a: K/V tiles are double-buffered with cp.async so the
+// next tile streams in while the current one is used, each thread computes a
+// 4x4 block of scores (register tiling instead of one warp per row), and the
+// softmax statistics are reduced with half-warp shuffles.  Exponentials use the
+// exp2 form: 2^(s*scale*log2 e - m).  No TF32 or other reduced-precision
+// arithmetic is used.
+#include <cuda_runtime.h>
+#include <math_constants.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace attn {
+namespace fwd_fp32 {
+
+constexpr int BM = 64;   // query rows per CTA
+constexpr int BN = 64;   // keys per tile
+constexpr int NT = 256;  // threads: 16 row groups x 16 column groups
+
+template <int D>
+struct Smem {
+  static constexpr int LD = D + 4;  // padded row (floats) — conflict-free 16-byte reads
+  static constexpr int PLD = BN + 4;
+  static constexpr int Q = 0;
+  static constexpr int K = Q + BM * LD;           // two buffers
+  static constexpr int V = K + 2 * BN * LD;       // two buffers
+  static constexpr int P = V + 2 * BN * LD;
+  static constexpr int FLOATS = P + BM * PLD;
+  static constexpr int BYTES = FLOATS * 4;
+};
+
+__device__ __forceinline__ void cp_async16(float* dst, const float* src, bool valid) {
+  const uint32_t d = smem_u32(dst);
+  const int n = valid ? 16 : 0;  // 0 source bytes: the 16 destination bytes are zero-filled
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src), "r"(n) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+// rows [row0, row0+64) of a [N, D] head into smem with leading dimension LD
+template <int D>
+__device__ __forceinline__ void load_rows(float* dst, const float* head, int row0, int N) {
+  constexpr int LD = Smem<D>::LD;
+  constexpr int VEC = D / 4;  // float4 per row
+  for (int i = threadIdx.x; i < 64 * VEC; i += NT) {
+    const int r = i / VEC, c = (i % VEC) * 4;
+    const int gr = row0 + r;
+    const bool valid = gr < N;
+    cp_async16(dst + r * LD + c, head + static_cast<size_t>(valid ? gr : 0) * D + c, valid);
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(NT) attn_fwd_fp32_kernel(const float* __restrict__ Q,
+                                                          const float* __restrict__ K,
+                                                          const float* __restrict__ V,
+                                                          float* __restrict__ O,
+                                                          float* __restrict__ LSE, int Hq, int Hkv,
+                                                          int Nq, int Nk, float c, int causal,
+                                                          int window) {
+  using S = Smem<D>;
+  constexpr int LD = S::LD, PLD = S::PLD;
+  constexpr int DC = D / 16;  // output columns per thread
+  extern __shared__ float4 smem4[];
+  float* sm = reinterpret_cast<float*>(smem4);
+  float* Qs = sm + S::Q;
+  float* Ps = sm + S::P;
+
+  const int tid = threadIdx.x, ty = tid / 16, tx = tid % 16;
+  const int qblk = causal ? static_cast<int>(gridDim.x - 1 - blockIdx.x) : static_cast<int>(blockIdx.x);
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int kvh = h / (Hq / Hkv);
+  const int q0 = qblk * BM;
+  const int off = Nk - Nq;
+  const float* Qh = Q + (static_cast<size_t>(b) * Hq + h) * Nq * D;
+  const float* Kh = K + (static_cast<size_t>(b) * Hkv + kvh) * Nk * D;
+  const float* Vh = V + (static_cast<size_t>(b) * Hkv + kvh) * Nk * D;
+
+  int kv_hi = Nk;
+  if (causal) kv_hi = min(kv_hi, min(q0 + BM - 1, Nq - 1) + off + 1);
+  int kv_lo = 0;
+  if (window > 0) kv_lo = max(0, q0 + off - window + 1);
+  int j_begin = 0, n_tiles = 0;
+  if (kv_hi > kv_lo) {
+    j_begin = kv_lo / BN;
+    n_tiles = (kv_hi + BN - 1) / BN - j_begin;
+  }
+  const int tile_hi_min = causal ? min(q0 + off, Nk - 1) : Nk - 1;
+  const int tile_lo_max = window > 0 ? q0 + BM - 1 + off - window + 1 : 0;
+
+  if (n_tiles > 0) {
+    load_rows<D>(Qs, Qh, q0, Nq);
+    load_rows<D>(sm + S::K, Kh, j_begin * BN, Nk);
+    load_rows<D>(sm + S::V, Vh, j_begin * BN, Nk);
+  }
+  cp_async_commit();
+
+  float m[4], l[4], acc[4][DC];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    m[i] = -CUDART_INF_F;
+    l[i] = 0.f;
+#pragma unroll
+    for (int d = 0; d < DC; ++d) acc[i][d] = 0.f;
+  }
+
+  for (int jj = 0; jj < n_tiles; ++jj) {
+    const int buf = jj & 1;
+    const float* Ks = sm + S::K + buf * BN * LD;
+    const float* Vs = sm + S::V + buf * BN * LD;
+    cp_async_wait_all();
+    __syncthreads();  // tile jj visible; everyone is done with tile jj-1
+    if (jj + 1 < n_tiles) {
+      load_rows<D>(sm + S::K + (buf ^ 1) * BN * LD, Kh, (j_begin + jj + 1) * BN, Nk);
+      load_rows<D>(sm + S::V + (buf ^ 1) * BN * LD, Vh, (j_begin + jj + 1) * BN, Nk);
+    }
+    cp_async_commit();
+
+    // ---- scores: rows ty*4+i, keys tx+16*n
+    float s[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int n = 0; n < 4; ++n) s[i][n] = 0.f;
+#pragma unroll 4
+    for (int d = 0; d < D; d += 4) {
+      float4 qv[4], kv[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) qv[i] = *reinterpret_cast<const float4*>(Qs + (ty * 4 + i) * LD + d);
+#pragma unroll
+      for (int n = 0; n < 4; ++n) kv[n] = *reinterpret_cast<const float4*>(Ks + (tx + 16 * n) * LD + d);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int n = 0; n < 4; ++n) {
+          s[i][n] = fmaf(qv[i].x, kv[n].x, s[i][n]);
+          s[i][n] = fmaf(qv[i].y, kv[n].y, s[i][n]);
+          s[i][n] = fmaf(qv[i].z, kv[n].z, s[i][n]);
+          s[i][n] = fmaf(qv[i].w, kv[n].w, s[i][n]);
+        }
+    }
+    const int k0 = (j_begin + jj) * BN;
+    const bool need_mask = (k0 + BN - 1 > tile_hi_min) || (k0 < tile_lo_max);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int row = q0 + ty * 4 + i;
+      const int diag = row + off;
+      const int hi_r = causal ? min(diag, Nk - 1) : Nk - 1;
+      const int lo_r = window > 0 ? diag - window + 1 : 0;
+      float mx = -CUDART_INF_F;
+#pragma unroll
+      for (int n = 0; n < 4; ++n) {
+        float x = s[i][n] * c;
+        if (need_mask) {
+          const int key = k0 + tx + 16 * n;
+          if (key > hi_r || key < lo_r) x = -CUDART_INF_F;
+        }
+        s[i][n] = x;
+        mx = fmaxf(mx, x);
+      }
+#pragma unroll
+      for (int o = 8; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      const float m_new = fmaxf(m[i], mx);
+      const float m_use = (m_new == -CUDART_INF_F) ? 0.f : m_new;
+      const float alpha = ex2_approx(m[i] - m_use);  // m = -inf -> 0
+      m[i] = m_new;
+      float sum = 0.f;
+#pragma unroll
+      for (int n = 0; n < 4; ++n) {
+        const float pv = ex2_approx(s[i][n] - m_use);
+        sum += pv;
+        Ps[(ty * 4 + i) * PLD + tx + 16 * n] = pv;
+      }
+#pragma unroll
+      for (int o = 8; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      l[i] = l[i] * alpha + sum;
+#pragma unroll
+      for (int d = 0; d < DC; ++d) acc[i][d] *= alpha;
+    }
+    __syncthreads();  // P tile complete
+
+    // ---- O += P V: rows ty*4+i, columns (see col())
+#pragma unroll 2
+    for (int kk = 0; kk < BN; kk += 4) {
+      float4 pr[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) pr[i] = *reinterpret_cast<const float4*>(Ps + (ty * 4 + i) * PLD + kk);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float* vrow = Vs + (kk + u) * LD;
+        float vv[DC];
+        if constexpr (DC == 8) {
+          const float4 a = *reinterpret_cast<const float4*>(vrow + tx * 4);
+          const float4 bb = *reinterpret_cast<const float4*>(vrow + 64 + tx * 4);
+          vv[0] = a.x; vv[1] = a.y; vv[2] = a.z; vv[3] = a.w;
+          vv[4] = bb.x; vv[5] = bb.y; vv[6] = bb.z; vv[7] = bb.w;
+        } else if constexpr (DC == 4) {
+          const float4 a = *reinterpret_cast<const float4*>(vrow + tx * 4);
+          vv[0] = a.x; vv[1] = a.y; vv[2] = a.z; vv[3] = a.w;
+        } else {
+          const float2 a = *reinterpret_cast<const float2*>(vrow + tx * 2);
+          vv[0] = a.x; vv[1] = a.y;
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float pw = u == 0 ? pr[i].x : u == 1 ? pr[i].y : u == 2 ? pr[i].z : pr[i].w;
+#pragma unroll
+          for (int d = 0; d < DC; ++d) acc[i][d] = fmaf(pw, vv[d], acc[i][d]);
+        }
+      }
+    }
+  }
+  cp_async_wait_all();
+
+  // ---- epilogue
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int row = q0 + ty * 4 + i;
+    if (row >= Nq) continue;
+    const float inv_l = l[i] > 0.f ? 1.f / l[i] : 0.f;
+    float* orow = O + ((static_cast<size_t>(b) * Hq + h) * Nq + row) * D;
+    if constexpr (DC == 8) {
+      *reinterpret_cast<float4*>(orow + tx * 4) =
+          make_float4(acc[i][0] * inv_l, acc[i][1] * inv_l, acc[i][2] * inv_l, acc[i][3] * inv_l);
+      *reinterpret_cast<float4*>(orow + 64 + tx * 4) =
+          make_float4(acc[i][4] * inv_l, acc[i][5] * inv_l, acc[i][6] * inv_l, acc[i][7] * inv_l);
+    } else if constexpr (DC == 4) {
+      *reinterpret_cast<float4*>(orow + tx * 4) =
+          make_float4(acc[i][0] * inv_l, acc[i][1] * inv_l, acc[i][2] * inv_l, acc[i][3] * inv_l);
+    } else {
+      *reinterpret_cast<float2*>(orow + tx * 2) = make_float2(acc[i][0] * inv_l, acc[i][1] * inv_l);
+    }
+    if (tx == 0 && LSE != nullptr)
+      LSE[(static_cast<size_t>(b) * Hq + h) * Nq + row] =
+          l[i] > 0.f ? (m[i] + log2f(l[i])) * 0.69314718055994531f : -CUDART_INF_F;
+  }
+}
+
+template <int D>
+int launch(const float* q, const float* k, const float* v, float* o, float* lse, int B, int Hq,
+           int Hkv, int Nq, int Nk, float scale, int causal, int window, cudaStream_t stream) {
+  static int attr_dev = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (attr_dev != dev) {
+    if (cudaFuncSetAttribute(attn_fwd_fp32_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Smem<D>::BYTES) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    attr_dev = dev;
+  }
+  const dim3 grid((Nq + BM - 1) / BM, Hq, B);
+  attn_fwd_fp32_kernel<D><<<grid, NT, Smem<D>::BYTES, stream>>>(
+      q, k, v, o, lse, Hq, Hkv, Nq, Nk, scale * 1.4426950408889634f, causal, window > 0 ? window : 0);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // namespace fwd_fp32
+
+int launch_fwd_fp32(const float* q, const float* k, const float* v, float* o, float* lse, int B,
+                    int Hq, int Hkv, int Nq, int Nk, int D, float scale, int causal, int window,
+                    cudaStream_t stream, int* /*err*/) {
+  switch (D) {
+    case 32: return fwd_fp32::launch<32>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, window, stream);
+    case 64: return fwd_fp32::launch<64>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, window, stream);
+    case 128: return fwd_fp32::launch<128>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, window, stream);
+    default: return ATTN_ERR_HEAD_DIM;
+  }
+}
+
+}  // namespace attn

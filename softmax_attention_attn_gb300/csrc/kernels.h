@@ -1,0 +1,49 @@
+// kernels.h — launchers shared between the C-ABI translation unit and the
+// kernel translation units.  Arguments are validated by the caller (attn_abi.cu).
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "attn.h"
+
+namespace attn {
+
+struct FwdParams {
+  __nv_bfloat16* o;
+  float* lse;
+  int B, Hq, Hkv, Nq, Nk;
+  int group;         // Hq / Hkv
+  float scale_log2;  // scale * log2(e)
+  int causal, window;
+  int* err;          // device error word
+};
+
+// Tensor maps (cuTensorMapEncodeTiled, fetched from the driver at run time).
+// Dimensions are innermost first; strides are packed (contiguous tensor).
+bool encode_tiled_3d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t d0,
+                     uint64_t d1, uint64_t d2, uint32_t esize, const uint32_t box[3],
+                     CUtensorMapSwizzle swz);
+bool encode_tiled_4d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t d0,
+                     uint64_t d1, uint64_t d2, uint64_t d3, uint32_t esize, const uint32_t box[4],
+                     CUtensorMapSwizzle swz);
+
+int launch_fwd_bf16(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                    int Hq, int Hkv, int Nq, int Nk, float scale, int causal, int window,
+                    cudaStream_t stream, int* err);
+
+int launch_fwd_fp32(const float* q, const float* k, const float* v, float* o, float* lse, int B,
+                    int Hq, int Hkv, int Nq, int Nk, int D, float scale, int causal, int window,
+                    cudaStream_t stream, int* err);
+
+int launch_decode_splitkv(const void* q, const void* k_cache, const void* v_cache,
+                          const int* seqlens, void* workspace, int B, int Hq, int Hkv,
+                          int Nk_max, float scale, int chunk, int num_sms, cudaStream_t stream,
+                          int* err);
+
+int launch_decode_combine(const void* workspace, const int* seqlens, void* o, float* lse, int B,
+                          int Hq, int Nk_max, int chunk, cudaStream_t stream, int* err);
+
+}  // namespace attn

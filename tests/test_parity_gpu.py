@@ -1,0 +1,216 @@
+"""GPU parity: the CUDA kernels (through the C ABI) against the fp64 oracle.
+
+Tolerances (fixed by the attention-forward target):
+  * fp32 inputs: max-abs error <= 1e-4 on O and on LSE;
+  * bf16 inputs (fp32 accumulation): max-abs error <= 2e-2 on O and
+    |dLSE| <= 1e-2 * max(1, |LSE|) on LSE.
+Rows that see no key must give O = 0 and LSE = -inf on both sides.
+Small and ragged shapes are compared element by element; the full benchmark
+workloads are compared on sampled rows that the oracle computes one by one.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from softmax_attention_attn_gb300 import binding, inputs
+
+pytestmark = pytest.mark.gpu
+
+FP32_TOL = 1e-4
+BF16_O_TOL = 2e-2
+BF16_LSE_REL = 1e-2
+
+
+@pytest.fixture(scope="module")
+def dev(cuda_lib):
+    return torch.device("cuda:0")
+
+
+def check(o_gpu, lse_gpu, O, L, o_tol, lse_tol, lse_relative):
+    o = o_gpu.float().cpu().numpy().reshape(O.shape)
+    l = lse_gpu.float().cpu().numpy().reshape(L.shape)
+    assert np.isfinite(o).all(), "non-finite output"
+    err_o = float(np.abs(o - O).max()) if O.size else 0.0
+    fin = np.isfinite(L)
+    fin_ok = np.array_equal(np.isfinite(l), fin) and bool(np.all(l[~fin] == -np.inf))
+    err_l = 0.0
+    if fin.any() and fin_ok:
+        d = np.abs(l[fin] - L[fin])
+        if lse_relative:
+            d = d / np.maximum(1.0, np.abs(L[fin]))
+        err_l = float(d.max())
+    msg = f"O max-abs err {err_o:.3e} (tol {o_tol}), LSE err {err_l:.3e} (tol {lse_tol}), finiteness ok {fin_ok}"
+    assert fin_ok and err_o <= o_tol and err_l <= lse_tol, msg
+    return err_o
+
+
+def sample_rows(B, H, N, n, seed, tile=128):
+    rng = np.random.default_rng(seed)
+    rows = {(int(rng.integers(B)), int(rng.integers(H)), int(rng.integers(N))) for _ in range(n)}
+    for i in (0, 1, tile - 1, tile, 2 * tile - 1, 2 * tile, N - 2, N - 1):
+        if 0 <= i < N:
+            rows.add((int(rng.integers(B)), int(rng.integers(H)), i))
+    return sorted(rows)
+
+
+# ---------------------------------------------------------------- fp32 path
+def run_fp32(dev, B, Hq, Hkv, Nq, Nk, D, causal=False, window=0, seed=0):
+    q, k, v = inputs.prefill_inputs(B, Hq, Hkv, Nq, Nk, D, "fp32", seed)
+    o, lse = binding.attn_fwd_fp32(q.to(dev), k.to(dev), v.to(dev), causal=causal, window=window)
+    return q, k, v, o, lse
+
+
+def test_fp32_small_config(dev):
+    """fp32 dense non-causal, B=2 H=4 N=64 D=32."""
+    q, k, v, o, lse = run_fp32(dev, 2, 4, 4, 64, 64, 32)
+    O, L = oracle.attention_forward(q, k, v, 1 / math.sqrt(32))
+    check(o, lse, O, L, FP32_TOL, FP32_TOL, False)
+
+
+@pytest.mark.parametrize("D", [32, 64, 128])
+@pytest.mark.parametrize("N", [64, 256, 1024, 4096])
+def test_fp32_sweep(dev, N, D):
+    """fp32 dense non-causal sweep, B=2 H=8."""
+    q, k, v, o, lse = run_fp32(dev, 2, 8, 8, N, N, D, seed=N + D)
+    if N <= 1024:
+        O, L = oracle.attention_forward(q, k, v, 1 / math.sqrt(D))
+        check(o, lse, O, L, FP32_TOL, FP32_TOL, False)
+    else:
+        rows = sample_rows(2, 8, N, 48, seed=N, tile=64)
+        O, L = oracle.attention_rows(q, k, v, 1 / math.sqrt(D), rows)
+        idx = tuple(np.array(rows).T)
+        check(o.cpu()[idx], lse.cpu()[idx], O, L, FP32_TOL, FP32_TOL, False)
+
+
+FP32_EDGE = [  # (B, Hq, Hkv, Nq, Nk, D, causal, window)
+    (1, 2, 2, 100, 77, 64, False, 0),
+    (1, 4, 2, 130, 130, 32, True, 0),
+    (2, 2, 1, 65, 200, 128, True, 0),     # Nq < Nk: bottom-right causal
+    (1, 2, 1, 200, 65, 64, True, 0),      # Nq > Nk: fully masked rows
+    (1, 2, 2, 150, 150, 32, True, 40),    # causal + window
+    (1, 2, 2, 150, 150, 64, False, 33),   # window only
+    (1, 2, 2, 1, 1, 32, False, 0),
+    (1, 1, 1, 3, 1000, 128, False, 0),
+]
+
+
+@pytest.mark.parametrize("case", FP32_EDGE, ids=str)
+def test_fp32_edge_cases(dev, case):
+    B, Hq, Hkv, Nq, Nk, D, causal, window = case
+    q, k, v, o, lse = run_fp32(dev, B, Hq, Hkv, Nq, Nk, D, causal, window, seed=7)
+    O, L = oracle.attention_forward(q, k, v, 1 / math.sqrt(D), causal, window)
+    check(o, lse, O, L, FP32_TOL, FP32_TOL, False)
+
+
+# ---------------------------------------------------------------- bf16 path
+def run_bf16(dev, B, Hq, Hkv, Nq, Nk, causal=False, window=0, seed=0):
+    q, k, v = inputs.prefill_inputs(B, Hq, Hkv, Nq, Nk, 128, "bf16", seed)
+    o, lse = binding.attn_fwd(q.to(dev), k.to(dev), v.to(dev), causal=causal, window=window)
+    return q, k, v, o, lse
+
+
+BF16_CASES = [  # (B, Hq, Hkv, Nq, Nk, causal, window)
+    (1, 2, 2, 128, 128, False, 0),        # one tile
+    (1, 2, 2, 300, 300, False, 0),        # ragged tail, two Q tiles
+    (2, 4, 2, 513, 513, True, 0),         # GQA, causal, ragged
+    (1, 2, 1, 256, 1000, True, 0),        # Nq < Nk
+    (1, 2, 2, 700, 300, True, 0),         # Nq > Nk: fully masked rows
+    (1, 2, 2, 1000, 1000, True, 100),     # causal + window
+    (1, 2, 2, 600, 600, False, 64),       # window only
+    (1, 1, 1, 1, 1, False, 0),
+    (1, 2, 2, 5, 3000, False, 0),
+    (1, 3, 1, 257, 129, False, 0),
+    (1, 4, 4, 1024, 1024, False, 0),      # several full K/V tiles
+]
+
+
+@pytest.mark.parametrize("case", BF16_CASES, ids=str)
+def test_bf16_cases(dev, case):
+    B, Hq, Hkv, Nq, Nk, causal, window = case
+    q, k, v, o, lse = run_bf16(dev, B, Hq, Hkv, Nq, Nk, causal, window, seed=11)
+    O, L = oracle.attention_forward(q, k, v, 1 / math.sqrt(128), causal, window)
+    check(o, lse, O, L, BF16_O_TOL, BF16_LSE_REL, True)
+
+
+@pytest.mark.parametrize("name,B,Hq,Hkv,N,causal", [
+    ("dense_B1_H32_N8192", 1, 32, 32, 8192, False),
+    ("causal_gqa_B4_H32_KV8_N4096", 4, 32, 8, 4096, True),
+])
+def test_bf16_benchmark_workloads_sampled(dev, name, B, Hq, Hkv, N, causal):
+    """The benchmark's prefill workloads, checked on sampled rows."""
+    q, k, v, o, lse = run_bf16(dev, B, Hq, Hkv, N, N, causal, 0, seed=0)
+    assert torch.isfinite(o.float()).all().item() and torch.isfinite(lse).all().item()
+    rows = sample_rows(B, Hq, N, 96, seed=5)
+    O, L = oracle.attention_rows(q, k, v, 1 / math.sqrt(128), rows, causal)
+    idx = tuple(np.array(rows).T)
+    check(o.cpu()[idx], lse.cpu()[idx], O, L, BF16_O_TOL, BF16_LSE_REL, True)
+
+
+# ---------------------------------------------------------------- decode
+def run_decode(dev, B, Hq, Hkv, lens, nk_max, chunk, seed=0):
+    _, q = inputs.decode_seqlens_and_q(B, Hq, 128, 1, 2, seed)
+    seqlens = torch.tensor(lens, dtype=torch.int32)
+    kc = torch.full((B, nk_max, Hkv, 128), inputs.K_SENTINEL, dtype=torch.bfloat16)
+    vc = torch.full((B, nk_max, Hkv, 128), inputs.V_SENTINEL, dtype=torch.bfloat16)
+    for b, n in enumerate(lens):
+        kb, vb = inputs.decode_kv_rows(seed, b, n, Hkv, 128)
+        kc[b, :n], vc[b, :n] = kb, vb
+    ws = torch.empty(binding.attn_decode_workspace_size(B, Hq, 128, nk_max, chunk), device=dev,
+                     dtype=torch.uint8)
+    o, lse = binding.attn_decode(q.to(dev), kc.to(dev), vc.to(dev), seqlens.to(dev), ws, chunk=chunk)
+    return q, kc, vc, seqlens, ws, o, lse
+
+
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+@pytest.mark.parametrize("chunk", [64, 512, 1024])
+def test_decode_small(dev, G, chunk):
+    lens = [1, 64, 511, 512, 513, 1500, 2048]
+    B, Hkv = len(lens), 2
+    Hq = G * Hkv
+    q, kc, vc, seqlens, ws, o, lse = run_decode(dev, B, Hq, Hkv, lens, 2048, chunk, seed=G + chunk)
+    scale = 1 / math.sqrt(128)
+    O, L = oracle.decode_forward(q, kc, vc, seqlens, scale)
+    check(o, lse, O, L, BF16_O_TOL, BF16_LSE_REL, True)
+    # the partial step on its own, valid chunks only
+    Op, Lp, ns = oracle.decode_split_partials(q, kc, vc, seqlens, scale, chunk)
+    S_max = Op.shape[2]
+    wsf = ws.view(torch.float32).cpu().numpy()
+    go = wsf[: B * Hq * S_max * 128].reshape(B, Hq, S_max, 128)
+    gl = wsf[B * Hq * S_max * 128: B * Hq * S_max * 129].reshape(B, Hq, S_max)
+    for b in range(B):
+        n = int(ns[b])
+        assert np.abs(go[b, :, :n] - Op[b, :, :n]).max() <= BF16_O_TOL
+        assert (np.abs(gl[b, :, :n] - Lp[b, :, :n]) / np.maximum(1, np.abs(Lp[b, :, :n]))).max() <= BF16_LSE_REL
+    assert binding.get_device_error() == 0
+
+
+def test_decode_benchmark_workload_sampled(dev):
+    """B=64 Hq=32 Hkv=8, Nk_b ~ U[512, 32768], chunk 512: sampled sequences."""
+    q, kc, vc, seqlens = inputs.decode_inputs(64, 32, 8, 128, 512, 32768, seed=0)
+    o, lse = binding.attn_decode(q.to(dev), kc.to(dev), vc.to(dev), seqlens.to(dev), chunk=512)
+    lens = seqlens.numpy()
+    batches = sorted({int(lens.argmax()), int(lens.argmin()), 0, 17, 40, 63})
+    O, L = oracle.decode_forward(q, kc, vc, seqlens, 1 / math.sqrt(128), batches=batches)
+    check(o.cpu()[batches], lse.cpu()[batches], O[batches], L[batches], BF16_O_TOL, BF16_LSE_REL, True)
+    assert binding.get_device_error() == 0
+
+
+def test_decode_bad_seqlen_reported(dev):
+    """A sequence length outside [1, Nk_max] is skipped and reported; others stay correct."""
+    B, Hq, Hkv, nk_max = 3, 8, 2, 1024
+    _, q = inputs.decode_seqlens_and_q(B, Hq, 128, 1, 2, 4)
+    kc = torch.zeros(B, nk_max, Hkv, 128, dtype=torch.bfloat16)
+    vc = torch.zeros(B, nk_max, Hkv, 128, dtype=torch.bfloat16)
+    kb, vb = inputs.decode_kv_rows(4, 1, 700, Hkv, 128)
+    kc[1, :700], vc[1, :700] = kb, vb
+    seqlens = torch.tensor([0, 700, nk_max + 5], dtype=torch.int32)
+    assert binding.get_device_error() == 0
+    o, lse = binding.attn_decode(q.to(dev), kc.to(dev), vc.to(dev), seqlens.to(dev), chunk=512)
+    assert binding.get_device_error() == -10  # ATTN_ERR_SEQLEN
+    O, L = oracle.decode_forward(q, kc, vc, [1, 700, 1], 1 / math.sqrt(128), batches=[1])
+    check(o.cpu()[1:2], lse.cpu()[1:2], O[1:2], L[1:2], BF16_O_TOL, BF16_LSE_REL, True)
+    assert torch.all(o.cpu()[[0, 2]].float() == 0) and torch.all(lse.cpu()[[0, 2]] == -math.inf)
+    assert binding.get_device_error() == 0
