@@ -17,6 +17,10 @@ Recipe (every draw uses ``torch.Generator("cpu")``):
   be regenerated without replaying the others.  Cache rows at or beyond
   ``Nk_b`` hold finite sentinels (K = 64, V = 1e4) so that a masking leak
   shows up as a large error instead of passing unnoticed.
+* large decode workloads may draw each sequence's K/V rows on a CUDA device
+  instead (``device=...``): same per-sequence seeds and distribution, but a
+  CUDA generator, so the values differ from the CPU draw; a check against the
+  oracle then copies the sampled sequences' rows back from that device.
 """
 from __future__ import annotations
 
@@ -58,32 +62,36 @@ def decode_seqlens_and_q(B: int, Hq: int, D: int, nk_lo: int, nk_hi: int,
     return seqlens.to(torch.int32), _cast(q, dtype)
 
 
-def decode_kv_rows(seed: int, b: int, nk: int, Hkv: int, D: int, dtype: str = "bf16"):
+def decode_kv_rows(seed: int, b: int, nk: int, Hkv: int, D: int, dtype: str = "bf16",
+                   device="cpu"):
     """The ``nk`` valid K and V rows ``[nk,Hkv,D]`` of sequence ``b``."""
-    g = torch.Generator("cpu").manual_seed(decode_row_seed(seed, b))
-    k = torch.randn(nk, Hkv, D, generator=g, dtype=torch.float32)
-    v = torch.randn(nk, Hkv, D, generator=g, dtype=torch.float32)
+    g = torch.Generator(device).manual_seed(decode_row_seed(seed, b))
+    k = torch.randn(nk, Hkv, D, generator=g, dtype=torch.float32, device=device)
+    v = torch.randn(nk, Hkv, D, generator=g, dtype=torch.float32, device=device)
     return _cast(k, dtype), _cast(v, dtype)
 
 
 def decode_inputs(B: int, Hq: int, Hkv: int, D: int, nk_lo: int, nk_hi: int,
                   seed: int = 0, nk_max: int | None = None, dtype: str = "bf16",
-                  pin_memory: bool = False):
+                  pin_memory: bool = False, device="cpu"):
     """Full decode workload: ``(q, k_cache, v_cache, seqlens)``.
 
     ``k_cache``/``v_cache`` are ``[B,Nk_max,Hkv,D]`` with ``Nk_max`` defaulting to
-    ``nk_hi``; rows past each sequence's length hold the sentinels.
+    ``nk_hi``; rows past each sequence's length hold the sentinels.  With a
+    CUDA ``device`` the caches are drawn and returned on that device (``q`` and
+    ``seqlens`` are always drawn on the CPU and returned there).
     """
     seqlens, q = decode_seqlens_and_q(B, Hq, D, nk_lo, nk_hi, seed, dtype)
     nk_max = nk_hi if nk_max is None else nk_max
     if int(seqlens.max()) > nk_max:
         raise ValueError("nk_max is below a drawn sequence length")
     tdt = _DTYPES[dtype]
-    k_cache = torch.empty(B, nk_max, Hkv, D, dtype=tdt, pin_memory=pin_memory)
-    v_cache = torch.empty(B, nk_max, Hkv, D, dtype=tdt, pin_memory=pin_memory)
+    on_cpu = torch.device(device).type == "cpu"
+    k_cache = torch.empty(B, nk_max, Hkv, D, dtype=tdt, device=device, pin_memory=pin_memory and on_cpu)
+    v_cache = torch.empty(B, nk_max, Hkv, D, dtype=tdt, device=device, pin_memory=pin_memory and on_cpu)
     for b in range(B):
         nk = int(seqlens[b])
-        kb, vb = decode_kv_rows(seed, b, nk, Hkv, D, dtype)
+        kb, vb = decode_kv_rows(seed, b, nk, Hkv, D, dtype, device)
         k_cache[b, :nk] = kb
         v_cache[b, :nk] = vb
         k_cache[b, nk:] = K_SENTINEL
