@@ -64,7 +64,10 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
-    ap.add_argument("--no-extras", action="store_true", help="skip the secondary workloads")
+    ap.add_argument("--workload", choices=["dense", "causal", "decode", "fp32"], default="dense",
+                    help="workload of the timed loop (default: the dense bf16 prefill)")
+    ap.add_argument("--no-extras", action="store_true", help="skip the other workloads")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffers) measurement")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-oracle sample budget")
     return ap.parse_args()
 
@@ -189,38 +192,40 @@ def cpu_oracle_sample(budget_s, seed=0):
 
 # ------------------------------------------------------------------ reference arm
 def run_reference(args, rank, world):
+    """The CPU oracle, as it stands, on a bounded sample of the dense workload per step."""
     if rank != 0:
         return
+    import numpy as np
     import oracle
     from softmax_attention_attn_gb300 import inputs
     q, k, v = inputs.prefill_inputs(1, MAIN["Hq"], MAIN["Hkv"], MAIN["N"], MAIN["N"], MAIN["D"], "bf16", 0)
+    # input preparation (untimed): the oracle's fp64 view of the bf16 values
+    q64, k64, v64 = (x.to(dtype=__import__("torch").float64).numpy() for x in (q, k, v))
     scale = 1 / math.sqrt(MAIN["D"])
     rows_per_step = 64
-    import numpy as np
     rng = np.random.default_rng(0)
 
-    def step(i):
+    def step():
         h = int(rng.integers(MAIN["Hq"]))
         i0 = int(rng.integers(0, MAIN["N"] - rows_per_step))
-        rows = [(0, h, i) for i in range(i0, i0 + rows_per_step)]
-        oracle.attention_rows(q, k, v, scale, rows)
+        oracle.attention_forward(q64[:, h:h + 1, i0:i0 + rows_per_step], k64[:, h:h + 1], v64[:, h:h + 1], scale)
 
-    for i in range(args.warmup):
-        step(i)
+    for _ in range(args.warmup):
+        step()
     t0 = time.perf_counter()
-    for i in range(args.steps):
-        step(i)
+    for _ in range(args.steps):
+        step()
     dt = time.perf_counter() - t0
     f = 4.0 * rows_per_step * MAIN["N"] * MAIN["D"] * args.steps
     value = f / dt / 1e12
-    sample = (f"{rows_per_step} query rows of one head of the dense workload (B=1 H=32 N=8192 D=128) "
-              "per step, fp64 numpy oracle")
+    sample = (f"{rows_per_step} query rows x all 8192 keys of one head of the dense workload "
+              "(B=1 H=32 N=8192 D=128) per step, fp64 numpy oracle; matmul on numpy's BLAS threads")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
             "config": {"workload": "bf16 dense prefill B=1 H=32 N=8192 D=128 (oracle on sampled rows)",
-                       "global_batch": 1, "seq_len": MAIN["N"], "parallelism": "replicas"},
+                       "global_batch": 1, "seq_len": MAIN["N"], "parallelism": "single"},
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": len(os.sched_getaffinity(0)),
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -229,10 +234,78 @@ def run_reference(args, rank, world):
 
 
 # ------------------------------------------------------------------ GB300 arm
+WORKLOAD_NAMES = {
+    "dense": "bf16 dense prefill B=1 H=32 N=8192 D=128 (non-causal)",
+    "causal": "bf16 causal GQA prefill B=4 Hq=32 Hkv=8 N=4096 D=128",
+    "decode": "bf16 split-KV decode B=64 Hq=32 Hkv=8 D=128, Nk_b~U[512,32768], chunk 512",
+    "fp32": "fp32 dense prefill B=2 H=8 N=4096 D=128",
+}
+
+
+def make_workload(name, dev, seed, peaks, peak_src, sm_max_mhz):
+    """Inputs resident on ``dev`` plus the step function and its roofline terms."""
+    import torch
+    from softmax_attention_attn_gb300 import binding, inputs
+    w = {"name": name, "desc": WORKLOAD_NAMES[name]}
+    if name in ("dense", "causal", "fp32"):
+        c = {"dense": MAIN, "causal": CAUSAL, "fp32": FP32}[name]
+        dt = "fp32" if name == "fp32" else "bf16"
+        host = inputs.prefill_inputs(c["B"], c["Hq"], c["Hkv"], c["N"], c["N"], c["D"], dt, seed)
+        q, k, v = (x.to(dev) for x in host)
+        o = torch.empty_like(q)
+        lse = torch.empty(c["B"], c["Hq"], c["N"], device=dev, dtype=torch.float32)
+        call = binding.attn_fwd_fp32 if name == "fp32" else binding.attn_fwd
+        w["fn"] = lambda: call(q, k, v, o, lse, causal=c["causal"])
+        w["work"] = flops(**c)
+        w["unit"] = "TFLOP/s"
+        w["launches"] = 1
+        w["dtype"] = dt
+        w["seq_len"], w["batch"] = c["N"], c["B"]
+        if name == "fp32":
+            w["bound"] = "alu"
+            w["peak"] = GB300_SMS * FP32_SIMT_FLOP_PER_CLK_SM * sm_max_mhz * 1e6 / 1e12
+            w["peak_source"] = f"152 SMs x 256 FP32 FLOP/clk x {sm_max_mhz:.0f} MHz"
+        else:
+            w["bound"] = "tensor"
+            w["peak"] = peaks["bf16_tflops"]
+            w["peak_source"] = f"{peak_src} dense bf16 (burst)"
+        w["e2e_in"] = [(x, t) for x, t in zip(host, (q, k, v))]
+        w["e2e_out"] = [o, lse]
+    else:
+        d = DECODE
+        qh, kc, vc, sl = inputs.decode_inputs(d["B"], d["Hq"], d["Hkv"], d["D"], d["nk_lo"], d["nk_hi"],
+                                              seed=seed, device=dev)
+        q, sl_d = qh.to(dev), sl.to(dev)
+        ws = torch.empty(binding.attn_decode_workspace_size(d["B"], d["Hq"], d["D"], d["nk_hi"], d["chunk"]),
+                         device=dev, dtype=torch.uint8)
+        o = torch.empty(d["B"], d["Hq"], d["D"], device=dev, dtype=torch.bfloat16)
+        lse = torch.empty(d["B"], d["Hq"], device=dev)
+        w["fn"] = lambda: binding.attn_decode(q, kc, vc, sl_d, ws, o, lse, chunk=d["chunk"])
+        w["split_fn"] = lambda: binding.attn_decode_splitkv(q, kc, vc, sl_d, ws, chunk=d["chunk"])
+        kv_bytes = int(sl.sum()) * d["Hkv"] * d["D"] * 2 * 2
+        w["kv_bytes"] = kv_bytes
+        w["work"] = kv_bytes + q.numel() * 2 + o.numel() * 2 + lse.numel() * 4
+        w["unit"] = "GB/s"
+        w["launches"] = 2
+        w["dtype"] = "bf16"
+        w["seq_len"], w["batch"] = d["nk_hi"], d["B"]
+        w["bound"] = "hbm"
+        w["peak"] = peaks["hbm_gbs"]
+        w["peak_source"] = f"{peak_src} copy bandwidth"
+        w["e2e_in"] = [(qh, q), (sl, sl_d), (None, kc), (None, vc)]
+        w["e2e_out"] = [o, lse]
+    return w
+
+
+def rate(w, ms):
+    scale = 1e12 if w["unit"] == "TFLOP/s" else 1e9
+    return w["work"] / (ms * 1e-3) / scale
+
+
 def run_gb300(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
-    from softmax_attention_attn_gb300 import binding, build, inputs
+    from softmax_attention_attn_gb300 import binding, build
 
     build.build()
     binding.lib()
@@ -240,6 +313,7 @@ def run_gb300(args, rank, world, local_rank):
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream()
     peaks, peak_src = load_peaks()
+    sm_max = float(peaks.get("sm_max_mhz", 2070.0))
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
     def max_over_ranks(x):
@@ -253,119 +327,95 @@ def run_gb300(args, rank, world, local_rank):
         if world > 1:
             dist.barrier()
 
-    # ---------------- main workload: dense bf16 prefill
-    c = MAIN
-    qh, kh, vh = inputs.prefill_inputs(c["B"], c["Hq"], c["Hkv"], c["N"], c["N"], c["D"], "bf16", seed=rank)
-    q, k, v = qh.to(dev), kh.to(dev), vh.to(dev)
-    o = torch.empty_like(q)
-    lse = torch.empty(c["B"], c["Hq"], c["N"], device=dev, dtype=torch.float32)
-    fwd = lambda: binding.attn_fwd(q, k, v, o, lse, causal=False)  # noqa: E731
+    # ---------------- the timed workload
+    w = make_workload(args.workload, dev, rank, peaks, peak_src, sm_max)
     for _ in range(args.warmup):
         flush.zero_()
-        fwd()
+        w["fn"]()
     torch.cuda.synchronize()
     with ClockSampler(local_rank) as clk:
         barrier()
         torch.cuda.synchronize()
         wall0 = time.perf_counter()
-        ms = time_steps(torch, fwd, args.steps, 0, flush, stream)
+        ms = time_steps(torch, w["fn"], args.steps, 0, flush, stream)
         torch.cuda.synchronize()
         barrier()
         wall1 = time.perf_counter()
     clocks = clk.summary()
     ms_step = max_over_ranks(sum(ms) / len(ms))
-    f_main = flops(**c)
-    value = world * f_main / (ms_step * 1e-3) / 1e12
-    achieved = f_main / (ms_step * 1e-3) / 1e12
+    value = world * rate(w, ms_step)
+    if w["name"] == "decode":   # roofline of the dominant kernel: the split-KV partial step
+        ms_k = max_over_ranks(statistics.mean(time_steps(torch, w["split_fn"], min(args.steps, 50), 3, flush, stream)))
+        achieved = w["kv_bytes"] / (ms_k * 1e-3) / 1e9
+        traffic = None
+    else:
+        achieved = rate(w, ms_step)
+        traffic = kernel_traffic() if w["name"] == "dense" else None
     rc = binding.get_device_error()
     if rc != 0:
         raise RuntimeError(f"device error word {rc} after the timed region")
 
-    # ---------------- end to end: pinned host buffers, copies inside every step
-    qp, kp, vp = (x.pin_memory() for x in (qh, kh, vh))
-    op = torch.empty(o.shape, dtype=o.dtype).pin_memory()
-    lp = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    e2e_steps = max(5, min(args.steps, 100))
+    # ---------------- end to end: pinned host inputs copied in, results copied out, every step
+    e2e = None
+    if not args.no_e2e:
+        pins = [(x.pin_memory() if x is not None else torch.empty(t.shape, dtype=t.dtype).pin_memory(), t)
+                for x, t in w["e2e_in"]]
+        outs = [(torch.empty(t.shape, dtype=t.dtype).pin_memory(), t) for t in w["e2e_out"]]
+        if w["name"] == "decode":   # the host copy of the caches is the device draw
+            for hp, t in pins[2:]:
+                hp.copy_(t)
+        e2e_steps = max(5, min(args.steps, 100 if w["name"] != "decode" else 10))
 
-    def e2e_step():
-        q.copy_(qp, non_blocking=True)
-        k.copy_(kp, non_blocking=True)
-        v.copy_(vp, non_blocking=True)
-        fwd()
-        op.copy_(o, non_blocking=True)
-        lp.copy_(lse, non_blocking=True)
+        def e2e_step():
+            for hp, t in pins:
+                t.copy_(hp, non_blocking=True)
+            w["fn"]()
+            for hp, t in outs:
+                hp.copy_(t, non_blocking=True)
 
-    for _ in range(3):
-        e2e_step()
-    torch.cuda.synchronize()
-    barrier()
-    t0 = time.perf_counter()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    ev1.record(stream)
-    torch.cuda.synchronize()
-    barrier()
-    e2e_ms = max_over_ranks(max(ev0.elapsed_time(ev1), (time.perf_counter() - t0) * 1e3) / e2e_steps)
-    h2d = sum(x.numel() * x.element_size() for x in (qp, kp, vp))
-    d2h = op.numel() * op.element_size() + lp.numel() * lp.element_size()
-    del qp, kp, vp, op, lp
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        t0 = time.perf_counter()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        e2e_ms = max_over_ranks(max(ev0.elapsed_time(ev1), (time.perf_counter() - t0) * 1e3) / e2e_steps)
+        e2e = {"value": world * rate(w, e2e_ms), "unit": w["unit"],
+               "h2d_bytes_per_step": sum(hp.numel() * hp.element_size() for hp, _ in pins),
+               "d2h_bytes_per_step": sum(hp.numel() * hp.element_size() for hp, _ in outs),
+               "ms_per_step": e2e_ms}
+        del pins, outs
+    main_work_desc = w["desc"]
+    main = {k: w[k] for k in ("name", "unit", "bound", "peak", "peak_source", "dtype", "seq_len", "batch", "launches")}
+    del w
+    torch.cuda.empty_cache()
 
-    # ---------------- secondary workloads
+    # ---------------- the other workloads, shorter loops
     workloads = {}
     if not args.no_extras:
         xs = max(5, min(args.steps // 10, 50))
-        # causal GQA prefill
-        c4 = CAUSAL
-        q4, k4, v4 = (x.to(dev) for x in inputs.prefill_inputs(c4["B"], c4["Hq"], c4["Hkv"], c4["N"], c4["N"],
-                                                               c4["D"], "bf16", seed=rank))
-        o4 = torch.empty_like(q4)
-        l4 = torch.empty(c4["B"], c4["Hq"], c4["N"], device=dev)
-        t4 = time_steps(torch, lambda: binding.attn_fwd(q4, k4, v4, o4, l4, causal=True), xs, 3, flush, stream)
-        m4 = max_over_ranks(statistics.mean(t4))
-        a4 = flops(**c4) / (m4 * 1e-3) / 1e12
-        workloads["bf16_causal_gqa_B4_Hq32_Hkv8_N4096"] = {
-            "value": world * a4, "unit": "TFLOP/s", "ms_per_step": m4,
-            "frac_of_bf16_peak": a4 / peaks["bf16_tflops"], "peak": f"{peaks['bf16_tflops']} ({peak_src})"}
-        del q4, k4, v4, o4, l4
-        # split-KV decode
-        d = DECODE
-        qd, kc, vc, sl = inputs.decode_inputs(d["B"], d["Hq"], d["Hkv"], d["D"], d["nk_lo"], d["nk_hi"],
-                                              seed=rank, device=dev)
-        qd, sl_d = qd.to(dev), sl.to(dev)
-        ws = torch.empty(binding.attn_decode_workspace_size(d["B"], d["Hq"], d["D"], d["nk_hi"], d["chunk"]),
-                         device=dev, dtype=torch.uint8)
-        od = torch.empty(d["B"], d["Hq"], d["D"], device=dev, dtype=torch.bfloat16)
-        ld = torch.empty(d["B"], d["Hq"], device=dev)
-        kv_bytes = int(sl.sum()) * d["Hkv"] * d["D"] * 2 * 2
-        alg_bytes = kv_bytes + qd.numel() * 2 + od.numel() * 2 + ld.numel() * 4
-        ts = time_steps(torch, lambda: binding.attn_decode_splitkv(qd, kc, vc, sl_d, ws, chunk=d["chunk"]),
-                        xs, 3, flush, stream)
-        tt = time_steps(torch, lambda: binding.attn_decode(qd, kc, vc, sl_d, ws, od, ld, chunk=d["chunk"]),
-                        xs, 3, flush, stream)
-        ms_s, ms_t = max_over_ranks(statistics.mean(ts)), max_over_ranks(statistics.mean(tt))
-        workloads["bf16_splitkv_decode_B64_Hq32_Hkv8_chunk512"] = {
-            "value": world * alg_bytes / (ms_t * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms_t,
-            "frac_of_hbm_peak": alg_bytes / (ms_t * 1e-3) / 1e9 / peaks["hbm_gbs"],
-            "splitkv_kernel_gbs": kv_bytes / (ms_s * 1e-3) / 1e9, "splitkv_kernel_ms": ms_s,
-            "splitkv_frac_of_hbm_peak": kv_bytes / (ms_s * 1e-3) / 1e9 / peaks["hbm_gbs"],
-            "algorithmic_bytes": alg_bytes, "peak": f"{peaks['hbm_gbs']} GB/s ({peak_src})"}
-        del qd, kc, vc, ws, od, ld
-        torch.cuda.empty_cache()
-        # fp32 prefill
-        c2 = FP32
-        q2, k2, v2 = (x.to(dev) for x in inputs.prefill_inputs(c2["B"], c2["Hq"], c2["Hkv"], c2["N"], c2["N"],
-                                                               c2["D"], "fp32", seed=rank))
-        t2 = time_steps(torch, lambda: binding.attn_fwd_fp32(q2, k2, v2), xs, 3, flush, stream)
-        m2 = max_over_ranks(statistics.mean(t2))
-        a2 = flops(**c2) / (m2 * 1e-3) / 1e12
-        sm_mhz = (clocks or {}).get("sm_max_mhz") or peaks.get("sm_max_mhz", 2070.0)
-        fp32_peak = GB300_SMS * FP32_SIMT_FLOP_PER_CLK_SM * sm_mhz * 1e6 / 1e12
-        workloads["fp32_B2_H8_N4096_D128"] = {
-            "value": world * a2, "unit": "TFLOP/s", "ms_per_step": m2, "frac_of_fp32_simt_peak": a2 / fp32_peak,
-            "peak": f"{fp32_peak:.1f} TFLOP/s (152 SMs x 256 FLOP/clk x max SM clock)"}
-        del q2, k2, v2
+        for name in ("dense", "causal", "decode", "fp32"):
+            if name == args.workload:
+                continue
+            x = make_workload(name, dev, rank, peaks, peak_src, sm_max)
+            mx = max_over_ranks(statistics.mean(time_steps(torch, x["fn"], xs, 3, flush, stream)))
+            r = rate(x, mx)
+            entry = {"workload": x["desc"], "value": world * r, "unit": x["unit"], "ms_per_step": mx,
+                     "bound": x["bound"], "frac": r / x["peak"], "peak": x["peak"], "peak_source": x["peak_source"]}
+            if name == "decode":
+                mk = max_over_ranks(statistics.mean(time_steps(torch, x["split_fn"], xs, 3, flush, stream)))
+                entry["splitkv_kernel_ms"] = mk
+                entry["splitkv_kernel_gbs"] = x["kv_bytes"] / (mk * 1e-3) / 1e9
+                entry["splitkv_frac"] = entry["splitkv_kernel_gbs"] / x["peak"]
+            workloads[name] = entry
+            del x
+            torch.cuda.empty_cache()
         if binding.get_device_error() != 0:
             raise RuntimeError("device error word set by a secondary workload")
 
@@ -374,18 +424,16 @@ def run_gb300(args, rank, world, local_rank):
         cpu = cpu_oracle_sample(args.cpu_seconds)
 
     line = {
-        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "metric": METRIC, "value": value, "unit": main["unit"], "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": "bf16 dense prefill B=1 H=32 N=8192 D=128 (non-causal)", "global_batch": world,
-                   "seq_len": c["N"], "parallelism": "replicas" if world > 1 else "single",
+        "vs_baseline": None, "dtype": main["dtype"], "data": "synthetic",
+        "config": {"workload": main_work_desc, "global_batch": world * main["batch"], "seq_len": main["seq_len"],
+                   "parallelism": "replicas" if world > 1 else "single",
                    "l2": "flushed (256 MiB write) before every step", "timing": "CUDA events per step"},
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                     "frac": achieved / peaks["bf16_tflops"], "traffic": kernel_traffic(),
-                     "peak_source": f"{peak_src} dense bf16 (burst)"},
-        "e2e": {"value": world * f_main / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "gpu_launches": args.steps,
+        "roofline": {"bound": main["bound"], "achieved": achieved, "peak": main["peak"], "unit": main["unit"],
+                     "frac": achieved / main["peak"], "traffic": traffic, "peak_source": main["peak_source"]},
+        "e2e": e2e,
+        "gpu_launches": args.steps * main["launches"],
         "wall_s_timed_region": wall1 - wall0,
         "clocks": clocks,
         "workloads": workloads,
