@@ -140,6 +140,37 @@ int attn_decode_combine(const void* workspace, const int* seqlens, void* o, floa
                         attn_stream_t stream);
 
 /*
+ * attn_decode_noalloc — split-KV decode (partial step, then combine step) that
+ * allocates nothing and needs no workspace from the caller.  The pages have no
+ * counterpart: this entry point exists for callers that cannot allocate device
+ * memory themselves, e.g. a plugin inside a host runtime that owns the whole
+ * device memory pool, or a latency-critical caller that must never reach
+ * cudaMalloc.
+ *
+ *   Arguments, layouts, results and error codes are those of
+ *   attn_decode_splitkv followed by attn_decode_combine, with o / lse as the
+ *   outputs.  The per-chunk partials live in a scratch array inside the
+ *   library image of ATTN_DECODE_NOALLOC_SCRATCH_BYTES (16 MiB); every GPU that
+ *   loads this part of the library keeps it until the process exits.  Sizes
+ *   needing more scratch than that, i.e.
+ *   attn_decode_workspace_size(B, Hq, D, Nk_max, chunk) > 16 MiB, are rejected
+ *   with ATTN_ERR_CAPACITY before anything is queued (this capacity check comes
+ *   before the other argument checks).
+ *   The first call on a device looks up the scratch array's device address
+ *   (cudaGetSymbolAddress, once per device): make that first call before any
+ *   stream capture.  All calls share the one array, so calls whose kernels
+ *   overlap on the GPU (different streams without ordering) race and corrupt
+ *   each other's results; calls on one stream are ordered and safe.  Nothing in
+ *   the scratch needs to start at zero: every entry the combine step reads is
+ *   written by the partial step of the same call.
+ */
+#define ATTN_DECODE_NOALLOC_SCRATCH_BYTES (16u << 20)
+int attn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                        const int* seqlens, void* o, float* lse,
+                        int B, int Hq, int Hkv, int Nk_max, int D,
+                        float scale, int chunk, attn_stream_t stream);
+
+/*
  * attn_get_device_error — synchronises `stream`, then returns and clears the
  * current device's error word (ATTN_OK if no kernel reported an error).  A
  * CUDA error seen while synchronising is returned as ATTN_ERR_CUDA.

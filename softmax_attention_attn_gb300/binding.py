@@ -28,6 +28,7 @@ SIGNATURES = {
     "attn_decode_workspace_size": (ctypes.c_size_t, [_c_int] * 5),
     "attn_decode_splitkv": (_c_int, [_vp] * 5 + [_c_int] * 5 + [_c_float, _c_int, _vp]),
     "attn_decode_combine": (_c_int, [_vp] * 4 + [_c_int] * 5 + [_vp]),
+    "attn_decode_noalloc": (_c_int, [_vp] * 6 + [_c_int] * 5 + [_c_float, _c_int, _vp]),
     "attn_get_device_error": (_c_int, [_vp]),
     "attn_strerror": (ctypes.c_char_p, [_c_int]),
 }
@@ -168,6 +169,29 @@ def attn_decode(q, k_cache, v_cache, seqlens, workspace=None, o=None, lse=None, 
                                 device=q.device, dtype=torch.uint8)
     attn_decode_splitkv(q, k_cache, v_cache, seqlens, workspace, scale, chunk, stream)
     return attn_decode_combine(workspace, seqlens, B, Hq, Nk_max, D, o, lse, chunk, q.device, stream)
+
+
+def attn_decode_noalloc(q, k_cache, v_cache, seqlens, o=None, lse=None, scale=None, chunk=512,
+                        stream=None):
+    """Split-KV decode without a caller workspace (scratch inside the library)."""
+    import torch
+    _require(q, torch.bfloat16, "q")
+    _require(k_cache, torch.bfloat16, "k_cache")
+    _require(v_cache, torch.bfloat16, "v_cache")
+    _require(seqlens, torch.int32, "seqlens")
+    B, Hq, D = q.shape
+    _, Nk_max, Hkv, _ = k_cache.shape
+    if o is None:
+        o = torch.empty(B, Hq, D, device=q.device, dtype=torch.bfloat16)
+    if lse is None:
+        lse = torch.empty(B, Hq, device=q.device, dtype=torch.float32)
+    _require(o, torch.bfloat16, "o")
+    _require(lse, torch.float32, "lse")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    code = lib().attn_decode_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seqlens), _ptr(o), _ptr(lse),
+                                     B, Hq, Hkv, Nk_max, D, scale, int(chunk), _stream(stream))
+    _check(code, "attn_decode_noalloc")
+    return o, lse
 
 
 def get_device_error(stream=None) -> int:

@@ -20,7 +20,8 @@ BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_NAME = "libattn.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
 
-SOURCES = ["attn_abi.cu", "attn_fwd_bf16.cu", "attn_fwd_fp32.cu", "attn_decode.cu"]
+SOURCES = ["attn_abi.cu", "attn_fwd_bf16.cu", "attn_fwd_fp32.cu", "attn_decode.cu",
+           "attn_decode_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                      "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]
