@@ -49,7 +49,7 @@ constexpr int TILE_BYTES = 2 * KBLK_BYTES;   // 128 x 128 bf16
 constexpr int SMEM_Q = 0;
 constexpr int SMEM_RING = SMEM_Q + NQT * TILE_BYTES;
 constexpr int SMEM_BAR = SMEM_RING + STAGES * TILE_BYTES;
-constexpr int NUM_BARS = 2 + 2 * STAGES + 3 * NQT;
+constexpr int NUM_BARS = 2 + 2 * STAGES + 4 * NQT;
 constexpr int SMEM_MISC = SMEM_BAR + NUM_BARS * 8;
 constexpr int SMEM_USED = SMEM_MISC + 16;
 constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack for 1024-byte alignment
@@ -78,11 +78,12 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint3
   }
 }
 
-// O (tmem) (+)= P (tmem, bf16) x V_tile (smem, MN-major: d contiguous).
-__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem,
-                                         bool accumulate) {
+// O (tmem) (+)= P (tmem, bf16) x V_tile (smem, MN-major: d contiguous), for the
+// 16-key steps kk in [kk0, kk0 + 4): one half of the tile's keys.
+__device__ __forceinline__ void issue_pv_half(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem,
+                                              bool accumulate, int kk0) {
 #pragma unroll
-  for (int kk = 0; kk < BN / 16; ++kk) {
+  for (int kk = kk0; kk < kk0 + BN / 32; ++kk) {
     const uint64_t b = smem_desc_sw128(v_smem + static_cast<uint32_t>(kk * 16 * 128),
                                        KBLK_BYTES, 1024);
     mma_bf16_ts(d_tmem, p_tmem + static_cast<uint32_t>(kk * 8), b, IDESC_PV,
@@ -115,8 +116,10 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
   auto bar_kv_full = [&](int s) { return sb + SMEM_BAR + 8u * (2 + s); };
   auto bar_kv_empty = [&](int s) { return sb + SMEM_BAR + 8u * (2 + STAGES + s); };
   auto bar_s_full = [&](int t) { return sb + SMEM_BAR + 8u * (2 + 2 * STAGES + t); };
-  auto bar_p_full = [&](int t) { return sb + SMEM_BAR + 8u * (2 + 2 * STAGES + NQT + t); };
-  auto bar_o_full = [&](int t) { return sb + SMEM_BAR + 8u * (2 + 2 * STAGES + 2 * NQT + t); };
+  // P of Q tile t is handed over in two halves (keys 0-63, keys 64-127)
+  auto bar_p_lo = [&](int t) { return sb + SMEM_BAR + 8u * (2 + 2 * STAGES + NQT + t); };
+  auto bar_p_hi = [&](int t) { return sb + SMEM_BAR + 8u * (2 + 2 * STAGES + 2 * NQT + t); };
+  auto bar_o_full = [&](int t) { return sb + SMEM_BAR + 8u * (2 + 2 * STAGES + 3 * NQT + t); };
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + SMEM_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SMEM_MISC + 4);
 
@@ -146,7 +149,8 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     }
     for (int t = 0; t < NQT; ++t) {
       mbar_init(bar_s_full(t), 1);
-      mbar_init(bar_p_full(t), BM);
+      mbar_init(bar_p_lo(t), BM / 32);   // one arrival per softmax warp
+      mbar_init(bar_p_hi(t), BM / 32);
       mbar_init(bar_o_full(t), 1);
     }
     *abort_flag = 0;
@@ -222,9 +226,13 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
         }
         if (!mbar_wait(bar_kv_full(vs), vu & 1, abort_flag, p.err)) { ok = false; break; }
         for (int t = 0; t < NQT; ++t) {
-          if (!mbar_wait(bar_p_full(t), jj & 1, abort_flag, p.err)) { ok = false; break; }
+          const uint32_t vsm = sb + SMEM_RING + vs * TILE_BYTES;
+          if (!mbar_wait(bar_p_lo(t), jj & 1, abort_flag, p.err)) { ok = false; break; }
           tc_fence_after();
-          issue_pv(tmem + o_col(t), tmem + s_col(t), sb + SMEM_RING + vs * TILE_BYTES, jj > 0);
+          issue_pv_half(tmem + o_col(t), tmem + s_col(t), vsm, jj > 0, 0);
+          if (!mbar_wait(bar_p_hi(t), jj & 1, abort_flag, p.err)) { ok = false; break; }
+          tc_fence_after();
+          issue_pv_half(tmem + o_col(t), tmem + s_col(t), vsm, true, BN / 32);
           if (t == NQT - 1) mma_commit(bar_kv_empty(vs));
           if (last) {
             mma_commit(bar_o_full(t));
@@ -286,27 +294,56 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
       }
       float mx[8];
 #pragma unroll
-      for (int g = 0; g < 8; ++g) mx[g] = s[g];
+      for (int g = 0; g < 8; ++g) mx[g] = fmaxf(s[g], s[8 + g]);
 #pragma unroll
-      for (int i = 8; i < BN; i += 8)
+      for (int i = 16; i < BN; i += 16)
 #pragma unroll
-        for (int g = 0; g < 8; ++g) mx[g] = fmaxf(mx[g], s[i + g]);
-      float rmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                         fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        for (int g = 0; g < 8; ++g) mx[g] = fmax3(mx[g], s[i + g], s[i + 8 + g]);
+      const float rmax = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
       const float m_new = fmaxf(m, rmax * c);
       float alpha = 1.f;
+      bool grow = false;
       if (jj == 0) {
         m = m_new;
       } else {
-        const bool grow = m_new > m + RESCALE_LOG2;
+        grow = m_new > m + RESCALE_LOG2;
         if (grow) {
           alpha = ex2_approx(m - m_new);
           m = m_new;
         }
-        if (__any_sync(0xffffffffu, grow)) {
-          // O row *= alpha (PV of the previous tile is complete: its commit
-          // preceded the S commit this thread waited on)
+      }
+      // O row *= alpha happens after P's first half is written (fewer live
+      // registers) and before that half is handed over, so no PV of this tile
+      // can start earlier.  PV of the previous tile is complete: its commit
+      // preceded the S commit this thread waited on.
+      const bool rescale = __any_sync(0xffffffffu, grow);
+      l *= alpha;
+      const float m_use = (m == -CUDART_INF_F) ? 0.f : m;
+      // p = 2^(s*c - m), summed and packed to bf16 pairs; each half of the keys is
+      // handed to the MMA warp as soon as it is in tensor memory.
+      const uint64_t c2 = f2_pack(c, c);
+      const uint64_t nm2 = f2_pack(-m_use, -m_use);
+      uint64_t sum2[2] = {0ull, 0ull};
 #pragma unroll
+      for (int half = 0; half < 2; ++half) {  // P columns [32*half, +32) = keys [64*half, +64)
+#pragma unroll
+        for (int qtr = 0; qtr < 2; ++qtr) {   // 16 columns = 32 keys at a time
+          const int c0 = 64 * half + 32 * qtr;
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const uint64_t x2 = f2_fma(f2_pack(s[c0 + 2 * i], s[c0 + 2 * i + 1]), c2, nm2);
+            float x0, x1;
+            f2_unpack(x2, x0, x1);
+            const float p0 = ex2_approx(x0);
+            const float p1 = ex2_approx(x1);
+            sum2[i & 1] = f2_add(sum2[i & 1], f2_pack(p0, p1));
+            pk[i] = pack_bf16x2(p0, p1);
+          }
+          tmem_st16(s_addr + 32 * half + 16 * qtr, pk);
+        }
+        if (half == 0 && rescale) {
+#pragma unroll 1
           for (int ch = 0; ch < 4; ++ch) {
             uint32_t o[32];
             tmem_ld32(o_addr + ch * 32, o);
@@ -316,26 +353,15 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
             tmem_st32(o_addr + ch * 32, o);
           }
         }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(half == 0 ? bar_p_lo(t) : bar_p_hi(t));
       }
-      l *= alpha;
-      const float m_use = (m == -CUDART_INF_F) ? 0.f : m;
-      float sum[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {  // P columns [32*half, 32*half+32) = keys [64*half, +64)
-        uint32_t pk[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float p0 = ex2_approx(fmaf(s[64 * half + 2 * i], c, -m_use));
-          const float p1 = ex2_approx(fmaf(s[64 * half + 2 * i + 1], c, -m_use));
-          sum[i & 3] += p0 + p1;
-          pk[i] = pack_bf16x2(p0, p1);
-        }
-        tmem_st32(s_addr + 32 * half, pk);
-      }
-      l += (sum[0] + sum[1]) + (sum[2] + sum[3]);
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bar_p_full(t));
+      float sa, sb2, sc, sd;
+      f2_unpack(sum2[0], sa, sb2);
+      f2_unpack(sum2[1], sc, sd);
+      l += (sa + sb2) + (sc + sd);
     }
 
     // ---- epilogue: O / l -> bf16, LSE
