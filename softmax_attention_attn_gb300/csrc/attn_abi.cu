@@ -130,8 +130,8 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   if (D != 128) return ATTN_ERR_HEAD_DIM;
   DeviceInfo* dev = nullptr;
   if ((rc = device_info(&dev)) != ATTN_OK) return rc;
-  return (launch_fwd_bf16(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, window,
-                                reinterpret_cast<cudaStream_t>(stream), dev->err));
+  return launch_fwd_bf16(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, window, dev->num_sms,
+                         reinterpret_cast<cudaStream_t>(stream), dev->err);
 }
 
 int attn_fwd_fp32(const float* q, const float* k, const float* v, float* o, float* lse, int B,

@@ -9,12 +9,17 @@
 // decomposition of the PTO FlashAttention article's section "为什么 PTO 适合
 // Agent 来优化"; here each stage is mapped onto Blackwell hardware:
 //
-//   * one CTA owns two 128-row Q tiles of one (batch, head) and streams 128-key
-//     K/V tiles through a 4-slot TMA ring (128-byte swizzle, mbarrier
-//     transaction counts);
-//   * warp 9 (one elected thread) issues tcgen05.mma: S_t = Q_t K^T into tensor
-//     memory (fp32, 128 columns per Q tile), then O_t += P_t V with P read from
-//     tensor memory (the TS form) and V from shared memory (MN-major operand);
+//   * persistent CTAs (one per SM) walk a list of work units — two 128-row Q
+//     tiles of one (batch, head); causal lists put the longest units first —
+//     and stream 128-key K/V tiles through a 5-slot TMA ring (128-byte
+//     swizzle, mbarrier transaction counts).  Barriers and tensor memory are set
+//     up once; the next unit's Q, K/V and first S overlap the last unit's
+//     epilogue;
+//   * warps 9 and 10 (one elected thread each) issue tcgen05.mma for Q tile 0
+//     and 1: S_t = Q_t K^T into tensor memory (fp32, 128 columns per Q tile),
+//     then O_t += P_t V with P read from tensor memory (the TS form) and V from
+//     shared memory (MN-major operand); the issuers take strict turns, each
+//     waiting for its own inputs while the other one issues;
 //   * warps 0-3 and 4-7 are the softmax warpgroups of Q tile 0 and 1: thread r
 //     owns row r, loads its 128 scores from tensor memory, applies the mask,
 //     updates the running max / sum in the exp2 domain, rescales its O row in
@@ -43,20 +48,20 @@ constexpr int BM = 128;                      // query rows per Q tile
 constexpr int BN = 128;                      // keys per K/V tile
 constexpr int HD = 128;                      // head dimension
 constexpr int NQT = 2;                       // Q tiles per CTA
-constexpr int STAGES = 4;                    // K/V ring slots (one K or one V tile each)
+constexpr int STAGES = 5;                    // K/V ring slots (one K or one V tile each)
 constexpr int KBLK_BYTES = BN * 64 * 2;      // 64-column (128-byte) slab of a 128-row tile
 constexpr int TILE_BYTES = 2 * KBLK_BYTES;   // 128 x 128 bf16
 constexpr int SMEM_Q = 0;
 constexpr int SMEM_RING = SMEM_Q + NQT * TILE_BYTES;
 constexpr int SMEM_BAR = SMEM_RING + STAGES * TILE_BYTES;
-constexpr int NUM_BARS = 2 + 2 * STAGES + 4 * NQT;
+constexpr int NUM_BARS = 3 + 2 * STAGES + 6 * NQT;
 constexpr int SMEM_MISC = SMEM_BAR + NUM_BARS * 8;
 constexpr int SMEM_USED = SMEM_MISC + 16;
 constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack for 1024-byte alignment
 constexpr int NUM_SOFTMAX_WARPS = 4 * NQT;
 constexpr int WARP_TMA = NUM_SOFTMAX_WARPS;
-constexpr int WARP_MMA = NUM_SOFTMAX_WARPS + 1;
-constexpr int NTHREADS = (NUM_SOFTMAX_WARPS + 2) * 32;
+constexpr int WARP_MMA = NUM_SOFTMAX_WARPS + 1;      // issuer of Q tile t is warp WARP_MMA + t
+constexpr int NTHREADS = (NUM_SOFTMAX_WARPS + 1 + NQT) * 32;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float RESCALE_LOG2 = 8.0f;         // keep a stale max while the growth is <= 2^8
 constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, BN, 0);
@@ -99,6 +104,65 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
+// A work unit: 256 query rows (two Q tiles) of one (batch, head).
+struct Unit {
+  int q0, b, h, kvh;
+  int jb0, je0, jb1, je1;  // key-tile range [jb, je) of Q tile 0 / 1 (empty: jb == je)
+  int j_begin, j_end;      // the union, streamed through the K/V ring
+};
+
+__device__ __forceinline__ Unit make_unit(int w, const FwdParams& p, int n_qblk) {
+  Unit u;
+  int qblk, bh;
+  if (p.causal) {  // longest q-blocks of every head first: causal work grows with q0
+    const int rank = w / (p.B * p.Hq);
+    bh = w % (p.B * p.Hq);
+    qblk = n_qblk - 1 - rank;
+  } else {         // q-blocks of one head are adjacent units and share its K/V in L2
+    qblk = w % n_qblk;
+    bh = w / n_qblk;
+  }
+  u.b = bh / p.Hq;
+  u.h = bh % p.Hq;
+  u.kvh = u.h / p.group;
+  u.q0 = qblk * (BM * NQT);
+  const int off = p.Nk - p.Nq;  // bottom-right diagonal offset
+  int jb[NQT], je[NQT];
+#pragma unroll
+  for (int t = 0; t < NQT; ++t) {
+    jb[t] = je[t] = 0;
+    const int r0 = u.q0 + t * BM;
+    if (r0 >= p.Nq) continue;
+    const int r1 = min(r0 + BM - 1, p.Nq - 1);
+    int hi = p.Nk;
+    if (p.causal) hi = min(hi, r1 + off + 1);
+    int lo = 0;
+    if (p.window > 0) lo = max(0, r0 + off - p.window + 1);
+    if (hi > lo) {
+      jb[t] = lo / BN;
+      je[t] = (hi + BN - 1) / BN;
+    }
+  }
+  u.jb0 = jb[0];
+  u.je0 = je[0];
+  u.jb1 = jb[1];
+  u.je1 = je[1];
+  u.j_begin = u.j_end = 0;
+#pragma unroll
+  for (int t = 0; t < NQT; ++t) {
+    if (je[t] > jb[t]) {
+      u.j_begin = (u.j_end > u.j_begin) ? min(u.j_begin, jb[t]) : jb[t];
+      u.j_end = max(u.j_end, je[t]);
+    }
+  }
+  return u;
+}
+
+__device__ __forceinline__ void own_range(const Unit& u, int t, int& jb, int& je) {
+  jb = t == 0 ? u.jb0 : u.jb1;
+  je = t == 0 ? u.je0 : u.je1;
+}
+
 __global__ void __launch_bounds__(NTHREADS, 1)
 attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
@@ -111,47 +175,40 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
   const int warp = warp_id_uniform();
   const int lane = static_cast<int>(lane_id());
 
-  const uint32_t bar_q = sb + SMEM_BAR;
-  const uint32_t bar_mma_done = sb + SMEM_BAR + 8;
-  auto bar_kv_full = [&](int s) { return sb + SMEM_BAR + 8u * (2 + s); };
-  auto bar_kv_empty = [&](int s) { return sb + SMEM_BAR + 8u * (2 + STAGES + s); };
-  auto bar_s_full = [&](int t) { return sb + SMEM_BAR + 8u * (2 + 2 * STAGES + t); };
-  // P of Q tile t is handed over in two halves (keys 0-63, keys 64-127)
-  auto bar_p_lo = [&](int t) { return sb + SMEM_BAR + 8u * (2 + 2 * STAGES + NQT + t); };
-  auto bar_p_hi = [&](int t) { return sb + SMEM_BAR + 8u * (2 + 2 * STAGES + 2 * NQT + t); };
-  auto bar_o_full = [&](int t) { return sb + SMEM_BAR + 8u * (2 + 2 * STAGES + 3 * NQT + t); };
+  // ---- barriers (phases run on across the units a CTA processes)
+  const uint32_t bar_q_full = sb + SMEM_BAR;            // Q tiles of a unit landed
+  const uint32_t bar_q_empty = sb + SMEM_BAR + 8;       // both issuers' last S of a unit done
+  const uint32_t bar_mma_done = sb + SMEM_BAR + 16;     // every MMA of both issuers done
+  auto bar_kv_full = [&](int s) { return sb + SMEM_BAR + 8u * (3 + s); };
+  auto bar_kv_empty = [&](int s) { return sb + SMEM_BAR + 8u * (3 + STAGES + s); };
+  auto bar_t = [&](int kind, int t) { return sb + SMEM_BAR + 8u * (3 + 2 * STAGES + kind * NQT + t); };
+  auto bar_s_full = [&](int t) { return bar_t(0, t); };   // S_t of a key tile in TMEM
+  auto bar_p_lo = [&](int t) { return bar_t(1, t); };     // P_t keys 0-63 in TMEM (+ O_t rescaled)
+  auto bar_p_hi = [&](int t) { return bar_t(2, t); };     // P_t keys 64-127 in TMEM
+  auto bar_o_full = [&](int t) { return bar_t(3, t); };   // O_t of a unit complete
+  auto bar_o_empty = [&](int t) { return bar_t(4, t); };  // epilogue has read O_t
+  auto bar_turn = [&](int t) { return bar_t(5, t); };     // issue turn handed to issuer t
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + SMEM_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SMEM_MISC + 4);
 
-  // ---- work unit: (batch b, head h, 256 query rows starting at q0)
-  const int qblk = p.causal ? static_cast<int>(gridDim.x - 1 - blockIdx.x) : static_cast<int>(blockIdx.x);
-  const int h = static_cast<int>(blockIdx.y);
-  const int b = static_cast<int>(blockIdx.z);
-  const int kvh = h / p.group;
-  const int q0 = qblk * (BM * NQT);
-  const int off = p.Nk - p.Nq;  // bottom-right diagonal offset
-  int kv_hi = p.Nk;             // exclusive key bound of the CTA
-  if (p.causal) kv_hi = min(kv_hi, min(q0 + BM * NQT - 1, p.Nq - 1) + off + 1);
-  int kv_lo = 0;
-  if (p.window > 0) kv_lo = max(0, q0 + off - p.window + 1);
-  int j_begin = 0, n_tiles = 0;
-  if (kv_hi > kv_lo) {
-    j_begin = kv_lo / BN;
-    n_tiles = (kv_hi + BN - 1) / BN - j_begin;
-  }
+  const int n_qblk = (p.Nq + BM * NQT - 1) / (BM * NQT);
+  const int n_units = n_qblk * p.Hq * p.B;
 
   if (threadIdx.x == 0) {
-    mbar_init(bar_q, 1);
-    mbar_init(bar_mma_done, 1);
+    mbar_init(bar_q_full, 1);
+    mbar_init(bar_q_empty, NQT);
+    mbar_init(bar_mma_done, NQT);
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(bar_kv_full(s), 1);
-      mbar_init(bar_kv_empty(s), 1);
+      mbar_init(bar_kv_empty(s), NQT);   // released once both Q tiles are done with it
     }
     for (int t = 0; t < NQT; ++t) {
       mbar_init(bar_s_full(t), 1);
       mbar_init(bar_p_lo(t), BM / 32);   // one arrival per softmax warp
       mbar_init(bar_p_hi(t), BM / 32);
       mbar_init(bar_o_full(t), 1);
+      mbar_init(bar_o_empty(t), BM / 32);
+      mbar_init(bar_turn(t), 1);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -168,84 +225,136 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
 
   if (warp == WARP_TMA) {
     // ================================================================ producer
-    if (lane == 0 && n_tiles > 0) {
+    if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      mbar_arrive_expect_tx(bar_q, NQT * TILE_BYTES);
-      for (int t = 0; t < NQT; ++t)
-        for (int kb = 0; kb < 2; ++kb)
-          tma_load_3d(sb + SMEM_Q + t * TILE_BYTES + kb * KBLK_BYTES, &tm_q, bar_q, kb * 64,
-                      q0 + t * BM, b * p.Hq + h);
-      int it = 0;
+      int it = 0;   // ring position (runs on across units)
+      int nq = 0;   // units with work so far (phase of q_full / q_empty)
       bool ok = true;
-      for (int jj = 0; jj < n_tiles && ok; ++jj) {
-        const int krow = (j_begin + jj) * BN;
-        for (int kv = 0; kv < 2; ++kv, ++it) {
-          const int s = it % STAGES, u = it / STAGES;
-          if (u > 0 && !mbar_wait(bar_kv_empty(s), (u - 1) & 1, abort_flag, p.err)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(bar_kv_full(s), TILE_BYTES);
-          const CUtensorMap* m = kv ? &tm_v : &tm_k;
+      for (int w = blockIdx.x; w < n_units && ok; w += gridDim.x) {
+        const Unit u = make_unit(w, p, n_qblk);
+        if (u.j_end <= u.j_begin) continue;
+        if (nq > 0 && !mbar_wait(bar_q_empty, (nq - 1) & 1, abort_flag, p.err)) { ok = false; break; }
+        mbar_arrive_expect_tx(bar_q_full, NQT * TILE_BYTES);
+        for (int t = 0; t < NQT; ++t)
           for (int kb = 0; kb < 2; ++kb)
-            tma_load_3d(sb + SMEM_RING + s * TILE_BYTES + kb * KBLK_BYTES, m, bar_kv_full(s),
-                        kb * 64, krow, b * p.Hkv + kvh);
+            tma_load_3d(sb + SMEM_Q + t * TILE_BYTES + kb * KBLK_BYTES, &tm_q, bar_q_full, kb * 64,
+                        u.q0 + t * BM, u.b * p.Hq + u.h);
+        ++nq;
+        for (int j = u.j_begin; j < u.j_end && ok; ++j) {
+          for (int kv = 0; kv < 2; ++kv, ++it) {
+            const int s = it % STAGES, use = it / STAGES;
+            if (use > 0 && !mbar_wait(bar_kv_empty(s), (use - 1) & 1, abort_flag, p.err)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(bar_kv_full(s), TILE_BYTES);
+            const CUtensorMap* m = kv ? &tm_v : &tm_k;
+            for (int kb = 0; kb < 2; ++kb)
+              tma_load_3d(sb + SMEM_RING + s * TILE_BYTES + kb * KBLK_BYTES, m, bar_kv_full(s),
+                          kb * 64, j * BN, u.b * p.Hkv + u.kvh);
+          }
         }
       }
       if (!ok) {  // give up: let the copies already issued land before the CTA exits
-        drain_wait(bar_q, 0);
+        if (nq > 0) drain_wait(bar_q_full, (nq - 1) & 1);
         for (int i = max(0, it - STAGES); i < it; ++i) drain_wait(bar_kv_full(i % STAGES), (i / STAGES) & 1);
       }
     }
-  } else if (warp == WARP_MMA) {
-    // ================================================================ MMA issuer
-    if (lane == 0 && n_tiles > 0) {
-      bool ok = mbar_wait(bar_q, 0, abort_flag, p.err);
-      int it = 0;
-      if (ok) ok = mbar_wait(bar_kv_full(0), 0, abort_flag, p.err);
-      if (ok) {
-        tc_fence_after();
-        for (int t = 0; t < NQT; ++t) {
-          issue_qk(tmem + s_col(t), sb + SMEM_Q + t * TILE_BYTES, sb + SMEM_RING);
-          mma_commit(bar_s_full(t));
-        }
-        mma_commit(bar_kv_empty(0));
-      }
-      it = 1;
-      for (int jj = 0; jj < n_tiles && ok; ++jj) {
-        const int vs = it % STAGES, vu = it / STAGES;
-        ++it;
-        const bool last = (jj == n_tiles - 1);
-        int ks = 0, ku = 0;
-        if (!last) {
-          ks = it % STAGES;
-          ku = it / STAGES;
-          ++it;
-        }
-        if (!mbar_wait(bar_kv_full(vs), vu & 1, abort_flag, p.err)) { ok = false; break; }
-        for (int t = 0; t < NQT; ++t) {
-          const uint32_t vsm = sb + SMEM_RING + vs * TILE_BYTES;
-          if (!mbar_wait(bar_p_lo(t), jj & 1, abort_flag, p.err)) { ok = false; break; }
-          tc_fence_after();
-          issue_pv_half(tmem + o_col(t), tmem + s_col(t), vsm, jj > 0, 0);
-          if (!mbar_wait(bar_p_hi(t), jj & 1, abort_flag, p.err)) { ok = false; break; }
-          tc_fence_after();
-          issue_pv_half(tmem + o_col(t), tmem + s_col(t), vsm, true, BN / 32);
-          if (t == NQT - 1) mma_commit(bar_kv_empty(vs));
-          if (last) {
-            mma_commit(bar_o_full(t));
-          } else {
-            if (t == 0) {
-              if (!mbar_wait(bar_kv_full(ks), ku & 1, abort_flag, p.err)) { ok = false; break; }
-              tc_fence_after();
-            }
-            issue_qk(tmem + s_col(t), sb + SMEM_Q + t * TILE_BYTES, sb + SMEM_RING + ks * TILE_BYTES);
-            mma_commit(bar_s_full(t));
-            if (t == NQT - 1) mma_commit(bar_kv_empty(ks));
+  } else if (warp >= WARP_MMA) {
+    // ================================================================ MMA issuers
+    // One thread per Q tile issues that tile's S = Q K^T and O += P V.  The two
+    // issuers take turns, so the tensor pipe sees the order PV_0 S_0 PV_1 S_1
+    // ... as from a single issuer, but each issuer does its own waiting for
+    // inputs while the other one issues.  MMAs of one thread execute in issue
+    // order, which orders S_t(j+1) after PV_t(j) (P_t aliases S_t).
+    const int t = warp - WARP_MMA;
+    if (lane == 0) {
+      const uint32_t q_sm = sb + SMEM_Q + t * TILE_BYTES;
+      auto slot_of = [](int pos) { return pos % STAGES; };
+      auto phase_of = [](int pos) { return static_cast<uint32_t>((pos / STAGES) & 1); };
+      int it_base = 0;  // ring position of the current unit's first K tile
+      int nq = 0;       // units with work so far
+      int gstep = 0;    // steps taken in turn order so far
+      int n_own = 0;    // own key tiles so far (phase of s_full / p_lo / p_hi)
+      int n_out = 0;    // units that produced O_t so far (phase of o_full / o_empty)
+      bool ok = true;
+      for (int w = blockIdx.x; w < n_units && ok; w += gridDim.x) {
+        const Unit u = make_unit(w, p, n_qblk);
+        if (u.j_end <= u.j_begin) continue;
+        int jb, je;
+        own_range(u, t, jb, je);
+        if (je <= jb) jb = je = u.j_end;  // no own tiles: the slots are only released
+        auto kpos = [&](int j) { return it_base + 2 * (j - u.j_begin); };
+        // Tiles outside this Q tile's range: wait for the fill, then release the
+        // slot without using it (a release never runs ahead of its fill).
+        auto skip_tile = [&](int j) {
+          for (int kv = 0; kv < 2; ++kv) {
+            const int pos = kpos(j) + kv;
+            if (!mbar_wait(bar_kv_full(slot_of(pos)), phase_of(pos), abort_flag, p.err)) return false;
+            mbar_arrive(bar_kv_empty(slot_of(pos)));
           }
+          return true;
+        };
+        if (!mbar_wait(bar_q_full, nq & 1, abort_flag, p.err)) { ok = false; break; }
+        if (jb < je) {  // first S of this unit (outside the turn order)
+          if (!mbar_wait(bar_kv_full(slot_of(kpos(jb))), phase_of(kpos(jb)), abort_flag, p.err)) { ok = false; break; }
+          tc_fence_after();
+          issue_qk(tmem + s_col(t), q_sm, sb + SMEM_RING + slot_of(kpos(jb)) * TILE_BYTES);
+          mma_commit(bar_s_full(t));
+          mma_commit(bar_kv_empty(slot_of(kpos(jb))));
+          if (je - jb == 1) mma_commit(bar_q_empty);  // that was this unit's last S
+        } else {
+          mbar_arrive(bar_q_empty);
         }
+        for (int j = u.j_begin; j < u.j_end && ok; ++j, ++gstep) {
+          const bool own = (j >= jb && j < je);
+          const int lt = n_own + (j - jb);
+          const int vpos = kpos(j) + 1;
+          const uint32_t vsm = sb + SMEM_RING + slot_of(vpos) * TILE_BYTES;
+          if (own) {
+            if (!mbar_wait(bar_kv_full(slot_of(vpos)), phase_of(vpos), abort_flag, p.err)) { ok = false; break; }
+            if (!mbar_wait(bar_p_lo(t), lt & 1, abort_flag, p.err)) { ok = false; break; }
+            // PV overwrites O_t at the unit's first key tile: the epilogue of the
+            // previous unit must have read it out.
+            if (j == jb && n_out > 0 &&
+                !mbar_wait(bar_o_empty(t), (n_out - 1) & 1, abort_flag, p.err)) { ok = false; break; }
+          }
+          if (t == 1 || gstep > 0) {
+            const uint32_t par = static_cast<uint32_t>((t == 0 ? gstep - 1 : gstep) & 1);
+            if (!mbar_wait(bar_turn(t), par, abort_flag, p.err)) { ok = false; break; }
+          }
+          if (own) {
+            tc_fence_after();
+            issue_pv_half(tmem + o_col(t), tmem + s_col(t), vsm, j > jb, 0);
+            if (!mbar_wait(bar_p_hi(t), lt & 1, abort_flag, p.err)) { ok = false; break; }
+            tc_fence_after();
+            issue_pv_half(tmem + o_col(t), tmem + s_col(t), vsm, true, BN / 32);
+            mma_commit(bar_kv_empty(slot_of(vpos)));
+            if (j + 1 == je) {
+              mma_commit(bar_o_full(t));
+            } else {
+              const int npos = kpos(j + 1);
+              if (!mbar_wait(bar_kv_full(slot_of(npos)), phase_of(npos), abort_flag, p.err)) { ok = false; break; }
+              tc_fence_after();
+              issue_qk(tmem + s_col(t), q_sm, sb + SMEM_RING + slot_of(npos) * TILE_BYTES);
+              mma_commit(bar_s_full(t));
+              mma_commit(bar_kv_empty(slot_of(npos)));
+              if (j + 2 == je) mma_commit(bar_q_empty);  // this unit's last S
+            }
+          } else if (!skip_tile(j)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive(bar_turn(1 - t));
+        }
+        if (je > jb) {
+          n_own += je - jb;
+          ++n_out;
+        }
+        it_base += 2 * (u.j_end - u.j_begin);
+        ++nq;
       }
       // every MMA issued above must finish before tensor memory is released
       mma_commit(bar_mma_done);
@@ -255,147 +364,163 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     // ================================================================ softmax + epilogue
     const int t = warp / 4;
     const int quad = warp % 4;
-    const int row = q0 + t * BM + quad * 32 + lane;
     const uint32_t lane_sel = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t s_addr = tmem + lane_sel + s_col(t);
     const uint32_t o_addr = tmem + lane_sel + o_col(t);
     const float c = p.scale_log2;
-
-    // visible keys of this row: lo_r <= key <= hi_r
-    const int diag = row + off;
-    const int hi_r = p.causal ? min(diag, p.Nk - 1) : p.Nk - 1;
-    const int lo_r = p.window > 0 ? diag - p.window + 1 : 0;
-    // tile-uniform bounds: a K tile inside [tile_lo_max, tile_hi_min] needs no mask
-    const int trow0 = q0 + t * BM;
-    const int tile_hi_min = p.causal ? min(trow0 + off, p.Nk - 1) : p.Nk - 1;
-    const int tile_lo_max = p.window > 0 ? trow0 + BM - 1 + off - p.window + 1 : 0;
-
-    float m = -CUDART_INF_F;  // running max of scale*log2(e)*s (possibly stale)
-    float l = 0.f;            // running sum of 2^(s*c - m)
+    const int off = p.Nk - p.Nq;
+    int n_own = 0;  // own key tiles so far (phase of s_full)
+    int n_out = 0;  // units that produced O_t so far (phase of o_full)
     bool ok = true;
-    for (int jj = 0; jj < n_tiles; ++jj) {
-      const int k0 = (j_begin + jj) * BN;
-      ok = __all_sync(0xffffffffu, mbar_wait(bar_s_full(t), jj & 1, abort_flag, p.err));
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t sr[4][32];
+    for (int w = blockIdx.x; w < n_units && ok; w += gridDim.x) {
+      const Unit u = make_unit(w, p, n_qblk);
+      int jb, je;
+      own_range(u, t, jb, je);
+      const int n_tiles = max(0, je - jb);
+      const int row = u.q0 + t * BM + quad * 32 + lane;
+      // visible keys of this row: lo_r <= key <= hi_r
+      const int diag = row + off;
+      const int hi_r = p.causal ? min(diag, p.Nk - 1) : p.Nk - 1;
+      const int lo_r = p.window > 0 ? diag - p.window + 1 : 0;
+      // tile-uniform bounds: a K tile inside [tile_lo_max, tile_hi_min] needs no mask
+      const int trow0 = u.q0 + t * BM;
+      const int tile_hi_min = p.causal ? min(trow0 + off, p.Nk - 1) : p.Nk - 1;
+      const int tile_lo_max = p.window > 0 ? trow0 + BM - 1 + off - p.window + 1 : 0;
+
+      float m = -CUDART_INF_F;  // running max of scale*log2(e)*s (possibly stale)
+      float l = 0.f;            // running sum of 2^(s*c - m)
+      for (int jj = 0; jj < n_tiles; ++jj) {
+        const int k0 = (jb + jj) * BN;
+        const int lt = n_own + jj;
+        ok = __all_sync(0xffffffffu, mbar_wait(bar_s_full(t), lt & 1, abort_flag, p.err));
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t sr[4][32];
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) tmem_ld32(s_addr + ch * 32, sr[ch]);
-      tmem_wait_ld();
-      float s[BN];
+        for (int ch = 0; ch < 4; ++ch) tmem_ld32(s_addr + ch * 32, sr[ch]);
+        tmem_wait_ld();
+        float s[BN];
 #pragma unroll
-      for (int i = 0; i < BN; ++i) s[i] = __uint_as_float(sr[i >> 5][i & 31]);
-      if (k0 + BN - 1 > tile_hi_min || k0 < tile_lo_max) {
+        for (int i = 0; i < BN; ++i) s[i] = __uint_as_float(sr[i >> 5][i & 31]);
+        if (k0 + BN - 1 > tile_hi_min || k0 < tile_lo_max) {
 #pragma unroll
-        for (int i = 0; i < BN; ++i) {
-          const int key = k0 + i;
-          if (key > hi_r || key < lo_r) s[i] = -CUDART_INF_F;
+          for (int i = 0; i < BN; ++i) {
+            const int key = k0 + i;
+            if (key > hi_r || key < lo_r) s[i] = -CUDART_INF_F;
+          }
         }
-      }
-      float mx[8];
+        float mx[8];
 #pragma unroll
-      for (int g = 0; g < 8; ++g) mx[g] = fmaxf(s[g], s[8 + g]);
+        for (int g = 0; g < 8; ++g) mx[g] = fmaxf(s[g], s[8 + g]);
 #pragma unroll
-      for (int i = 16; i < BN; i += 16)
+        for (int i = 16; i < BN; i += 16)
 #pragma unroll
-        for (int g = 0; g < 8; ++g) mx[g] = fmax3(mx[g], s[i + g], s[i + 8 + g]);
-      const float rmax = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
-      const float m_new = fmaxf(m, rmax * c);
-      float alpha = 1.f;
-      bool grow = false;
-      if (jj == 0) {
-        m = m_new;
-      } else {
-        grow = m_new > m + RESCALE_LOG2;
-        if (grow) {
-          alpha = ex2_approx(m - m_new);
+          for (int g = 0; g < 8; ++g) mx[g] = fmax3(mx[g], s[i + g], s[i + 8 + g]);
+        const float rmax = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+        const float m_new = fmaxf(m, rmax * c);
+        float alpha = 1.f;
+        bool grow = false;
+        if (jj == 0) {
           m = m_new;
-        }
-      }
-      // O row *= alpha happens after P's first half is written (fewer live
-      // registers) and before that half is handed over, so no PV of this tile
-      // can start earlier.  PV of the previous tile is complete: its commit
-      // preceded the S commit this thread waited on.
-      const bool rescale = __any_sync(0xffffffffu, grow);
-      l *= alpha;
-      const float m_use = (m == -CUDART_INF_F) ? 0.f : m;
-      // p = 2^(s*c - m), summed and packed to bf16 pairs; each half of the keys is
-      // handed to the MMA warp as soon as it is in tensor memory.
-      const uint64_t c2 = f2_pack(c, c);
-      const uint64_t nm2 = f2_pack(-m_use, -m_use);
-      uint64_t sum2[2] = {0ull, 0ull};
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {  // P columns [32*half, +32) = keys [64*half, +64)
-#pragma unroll
-        for (int qtr = 0; qtr < 2; ++qtr) {   // 16 columns = 32 keys at a time
-          const int c0 = 64 * half + 32 * qtr;
-          uint32_t pk[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const uint64_t x2 = f2_fma(f2_pack(s[c0 + 2 * i], s[c0 + 2 * i + 1]), c2, nm2);
-            float x0, x1;
-            f2_unpack(x2, x0, x1);
-            const float p0 = ex2_approx(x0);
-            const float p1 = ex2_approx(x1);
-            sum2[i & 1] = f2_add(sum2[i & 1], f2_pack(p0, p1));
-            pk[i] = pack_bf16x2(p0, p1);
+        } else {
+          grow = m_new > m + RESCALE_LOG2;
+          if (grow) {
+            alpha = ex2_approx(m - m_new);
+            m = m_new;
           }
-          tmem_st16(s_addr + 32 * half + 16 * qtr, pk);
         }
-        if (half == 0 && rescale) {
+        // O row *= alpha happens after P's first half is written (fewer live
+        // registers) and before that half is handed over, so no PV of this tile
+        // can start earlier.  PV of the previous tile is complete: its commit
+        // preceded the S commit this thread waited on.
+        const bool rescale = __any_sync(0xffffffffu, grow);
+        l *= alpha;
+        const float m_use = (m == -CUDART_INF_F) ? 0.f : m;
+        // p = 2^(s*c - m), summed and packed to bf16 pairs; each half of the keys
+        // is handed to the MMA warp as soon as it is in tensor memory.
+        const uint64_t c2 = f2_pack(c, c);
+        const uint64_t nm2 = f2_pack(-m_use, -m_use);
+        uint64_t sum2[2] = {0ull, 0ull};
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {  // P columns [32*half, +32) = keys [64*half, +64)
+#pragma unroll
+          for (int qtr = 0; qtr < 2; ++qtr) {   // 16 columns = 32 keys at a time
+            const int c0 = 64 * half + 32 * qtr;
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const uint64_t x2 = f2_fma(f2_pack(s[c0 + 2 * i], s[c0 + 2 * i + 1]), c2, nm2);
+              float x0, x1;
+              f2_unpack(x2, x0, x1);
+              const float p0 = ex2_approx(x0);
+              const float p1 = ex2_approx(x1);
+              sum2[i & 1] = f2_add(sum2[i & 1], f2_pack(p0, p1));
+              pk[i] = pack_bf16x2(p0, p1);
+            }
+            tmem_st16(s_addr + 32 * half + 16 * qtr, pk);
+          }
+          if (half == 0 && rescale) {
 #pragma unroll 1
-          for (int ch = 0; ch < 4; ++ch) {
-            uint32_t o[32];
-            tmem_ld32(o_addr + ch * 32, o);
-            tmem_wait_ld();
+            for (int ch = 0; ch < 4; ++ch) {
+              uint32_t o[32];
+              tmem_ld32(o_addr + ch * 32, o);
+              tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st32(o_addr + ch * 32, o);
+              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+              tmem_st32(o_addr + ch * 32, o);
+            }
           }
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(half == 0 ? bar_p_lo(t) : bar_p_hi(t));
         }
-        tmem_wait_st();
+        float sa, sb2, sc, sd;
+        f2_unpack(sum2[0], sa, sb2);
+        f2_unpack(sum2[1], sc, sd);
+        l += (sa + sb2) + (sc + sd);
+      }
+      if (!ok) break;
+      n_own += n_tiles;
+
+      // ---- epilogue: read O_t out of tensor memory (then hand it back to the
+      // MMA issuer), O / l -> bf16, LSE
+      uint32_t o[HD];
+      if (n_tiles > 0) {
+        ok = __all_sync(0xffffffffu, mbar_wait(bar_o_full(t), n_out & 1, abort_flag, p.err));
+        if (!ok) break;
+        ++n_out;
+        tc_fence_after();
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          uint32_t (&oc)[32] = *reinterpret_cast<uint32_t(*)[32]>(o + 32 * ch);
+          tmem_ld32(o_addr + ch * 32, oc);
+        }
+        tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(half == 0 ? bar_p_lo(t) : bar_p_hi(t));
-      }
-      float sa, sb2, sc, sd;
-      f2_unpack(sum2[0], sa, sb2);
-      f2_unpack(sum2[1], sc, sd);
-      l += (sa + sb2) + (sc + sd);
-    }
-
-    // ---- epilogue: O / l -> bf16, LSE
-    bool have_o = n_tiles > 0 && ok;
-    if (have_o) {
-      have_o = __all_sync(0xffffffffu, mbar_wait(bar_o_full(t), 0, abort_flag, p.err));
-      if (have_o) tc_fence_after();
-    }
-    const bool row_ok = row < p.Nq;
-    const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
-    __nv_bfloat16* orow = p.o + ((static_cast<size_t>(b) * p.Hq + h) * p.Nq + (row_ok ? row : 0)) * HD;
-#pragma unroll
-    for (int ch = 0; ch < 4; ++ch) {
-      uint32_t o[32];
-      if (have_o) {
-        tmem_ld32(o_addr + ch * 32, o);
-        tmem_wait_ld();
+        if (lane == 0) mbar_arrive(bar_o_empty(t));
       } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) o[i] = 0u;
+        for (int i = 0; i < HD; ++i) o[i] = 0u;
       }
-      uint32_t w[16];
+      if (row < p.Nq) {
+        const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+        __nv_bfloat16* orow = p.o + ((static_cast<size_t>(u.b) * p.Hq + u.h) * p.Nq + row) * HD;
 #pragma unroll
-      for (int i = 0; i < 16; ++i)
-        w[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
-      if (row_ok) {
-        uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        for (int i = 0; i < HD / 8; ++i) {
+          const uint4 v4 = make_uint4(
+              pack_bf16x2(__uint_as_float(o[8 * i + 0]) * inv_l, __uint_as_float(o[8 * i + 1]) * inv_l),
+              pack_bf16x2(__uint_as_float(o[8 * i + 2]) * inv_l, __uint_as_float(o[8 * i + 3]) * inv_l),
+              pack_bf16x2(__uint_as_float(o[8 * i + 4]) * inv_l, __uint_as_float(o[8 * i + 5]) * inv_l),
+              pack_bf16x2(__uint_as_float(o[8 * i + 6]) * inv_l, __uint_as_float(o[8 * i + 7]) * inv_l));
+          reinterpret_cast<uint4*>(orow)[i] = v4;
+        }
+        if (p.lse != nullptr) {
+          const float lse = (l > 0.f) ? (m + log2f(l)) * 0.69314718055994531f : -CUDART_INF_F;
+          p.lse[(static_cast<size_t>(u.b) * p.Hq + u.h) * p.Nq + row] = lse;
+        }
       }
-    }
-    if (row_ok && p.lse != nullptr) {
-      const float lse = (l > 0.f) ? (m + log2f(l)) * 0.69314718055994531f : -CUDART_INF_F;
-      p.lse[(static_cast<size_t>(b) * p.Hq + h) * p.Nq + row] = lse;
     }
   }
 
@@ -412,7 +537,7 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
 // --------------------------------------------------------------------- host
 int launch_fwd_bf16(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                     int Hq, int Hkv, int Nq, int Nk, float scale, int causal, int window,
-                    cudaStream_t stream, int* err) {
+                    int num_sms, cudaStream_t stream, int* err) {
   using namespace fwd_bf16;
   CUtensorMap tq, tk, tv;
   const uint32_t box[3] = {64, 128, 1};
@@ -445,7 +570,11 @@ int launch_fwd_bf16(const void* q, const void* k, const void* v, void* o, float*
   prm.causal = causal ? 1 : 0;
   prm.window = window > 0 ? window : 0;
   prm.err = err;
-  const dim3 grid((Nq + BM * NQT - 1) / (BM * NQT), Hq, B);
+  // persistent: at most one CTA per SM, each walking units blockIdx.x, +gridDim.x, ...
+  const long long n_qblk = (Nq + BM * NQT - 1) / (BM * NQT);
+  const long long units = n_qblk * Hq * B;
+  if (units > 0x7fffffffLL) return ATTN_ERR_DIM;
+  const int grid = static_cast<int>(units < num_sms ? units : num_sms);
   attn_fwd_bf16_kernel<<<grid, NTHREADS, SMEM_ALLOC, stream>>>(tq, tk, tv, prm);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
