@@ -69,6 +69,8 @@ def parse_args():
     ap.add_argument("--no-extras", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffers) measurement")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-oracle sample budget")
+    ap.add_argument("--decode-batch", type=int, default=DECODE["B"],
+                    help="sequences in the decode workload (smaller for profiler captures)")
     return ap.parse_args()
 
 
@@ -242,7 +244,7 @@ WORKLOAD_NAMES = {
 }
 
 
-def make_workload(name, dev, seed, peaks, peak_src, sm_max_mhz):
+def make_workload(name, dev, seed, peaks, peak_src, sm_max_mhz, decode_batch=None):
     """Inputs resident on ``dev`` plus the step function and its roofline terms."""
     import torch
     from softmax_attention_attn_gb300 import binding, inputs
@@ -272,7 +274,8 @@ def make_workload(name, dev, seed, peaks, peak_src, sm_max_mhz):
         w["e2e_in"] = [(x, t) for x, t in zip(host, (q, k, v))]
         w["e2e_out"] = [o, lse]
     else:
-        d = DECODE
+        d = dict(DECODE, B=decode_batch or DECODE["B"])
+        w["desc"] = WORKLOAD_NAMES["decode"].replace("B=64", f"B={d['B']}")
         qh, kc, vc, sl = inputs.decode_inputs(d["B"], d["Hq"], d["Hkv"], d["D"], d["nk_lo"], d["nk_hi"],
                                               seed=seed, device=dev)
         q, sl_d = qh.to(dev), sl.to(dev)
@@ -328,7 +331,7 @@ def run_gb300(args, rank, world, local_rank):
             dist.barrier()
 
     # ---------------- the timed workload
-    w = make_workload(args.workload, dev, rank, peaks, peak_src, sm_max)
+    w = make_workload(args.workload, dev, rank, peaks, peak_src, sm_max, args.decode_batch)
     for _ in range(args.warmup):
         flush.zero_()
         w["fn"]()
@@ -403,7 +406,7 @@ def run_gb300(args, rank, world, local_rank):
         for name in ("dense", "causal", "decode", "fp32"):
             if name == args.workload:
                 continue
-            x = make_workload(name, dev, rank, peaks, peak_src, sm_max)
+            x = make_workload(name, dev, rank, peaks, peak_src, sm_max, args.decode_batch)
             mx = max_over_ranks(statistics.mean(time_steps(torch, x["fn"], xs, 3, flush, stream)))
             r = rate(x, mx)
             entry = {"workload": x["desc"], "value": world * r, "unit": x["unit"], "ms_per_step": mx,
