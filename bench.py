@@ -300,6 +300,17 @@ def make_workload(name, dev, seed, peaks, peak_src, sm_max_mhz, decode_batch=Non
     return w
 
 
+def max_over_ranks_of(x, world, device):
+    """Maximum of a per-rank float over all ranks (the step time of the slowest rank)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def rate(w, ms):
     scale = 1e12 if w["unit"] == "TFLOP/s" else 1e9
     return w["work"] / (ms * 1e-3) / scale
@@ -320,11 +331,7 @@ def run_gb300(args, rank, world, local_rank):
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
     def max_over_ranks(x):
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return max_over_ranks_of(x, world, dev)
 
     def barrier():
         if world > 1:
