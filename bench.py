@@ -45,6 +45,10 @@ MAIN = dict(B=1, Hq=32, Hkv=32, N=8192, D=128, causal=False)
 CAUSAL = dict(B=4, Hq=32, Hkv=8, N=4096, D=128, causal=True)
 DECODE = dict(B=64, Hq=32, Hkv=8, D=128, nk_lo=512, nk_hi=32768, chunk=512)
 FP32 = dict(B=2, Hq=8, Hkv=8, N=4096, D=128, causal=False)
+# widened prefill workloads: sliding window, chunked prefill (Nq < Nk), head dim 64
+WINDOW = dict(B=1, Hq=32, Hkv=8, Nq=16384, Nk=16384, D=128, causal=True, window=4096)
+CHUNKED = dict(B=1, Hq=32, Hkv=8, Nq=2048, Nk=16384, D=128, causal=True, window=0)
+DENSE64 = dict(B=1, Hq=32, Hkv=32, N=8192, D=64, causal=False)
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FP32_SIMT_FLOP_PER_CLK_SM = 256.0   # 128 FP32 lanes x 2 (fused multiply-add)
 GB300_SMS = 152
@@ -58,13 +62,28 @@ def flops(B, Hq, N, D, causal, **_):
     return f / 2 if causal else f
 
 
+def visible_pairs(Nq, Nk, causal, window):
+    """Number of (query, key) pairs the mask leaves visible (bottom-right aligned)."""
+    import numpy as np
+    i = np.arange(Nq, dtype=np.int64)
+    hi = np.minimum(Nk - 1, i + (Nk - Nq)) if causal else np.full(Nq, Nk - 1)
+    lo = np.maximum(0, i + (Nk - Nq) - window + 1) if window > 0 else np.zeros(Nq, dtype=np.int64)
+    return int(np.maximum(0, hi - lo + 1).sum())
+
+
+def masked_flops(B, Hq, Nq, Nk, D, causal, window, **_):
+    """4*D per visible (query, key) pair: the exact count for window / chunked workloads."""
+    return 4.0 * B * Hq * D * visible_pairs(Nq, Nk, causal, window)
+
+
 def parse_args():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
-    ap.add_argument("--workload", choices=["dense", "causal", "decode", "fp32"], default="dense",
+    ap.add_argument("--workload", choices=["dense", "causal", "decode", "fp32", "window", "chunked", "d64"],
+                    default="dense",
                     help="workload of the timed loop (default: the dense bf16 prefill)")
     ap.add_argument("--no-extras", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffers) measurement")
@@ -241,6 +260,9 @@ WORKLOAD_NAMES = {
     "causal": "bf16 causal GQA prefill B=4 Hq=32 Hkv=8 N=4096 D=128",
     "decode": "bf16 split-KV decode B=64 Hq=32 Hkv=8 D=128, Nk_b~U[512,32768], chunk 512",
     "fp32": "fp32 dense prefill B=2 H=8 N=4096 D=128",
+    "window": "bf16 causal sliding-window (4096) prefill B=1 Hq=32 Hkv=8 N=16384 D=128",
+    "chunked": "bf16 chunked prefill (causal, bottom-right) B=1 Hq=32 Hkv=8 Nq=2048 Nk=16384 D=128",
+    "d64": "bf16 dense prefill B=1 H=32 N=8192 D=64 (non-causal)",
 }
 
 
@@ -249,20 +271,23 @@ def make_workload(name, dev, seed, peaks, peak_src, sm_max_mhz, decode_batch=Non
     import torch
     from softmax_attention_attn_gb300 import binding, inputs
     w = {"name": name, "desc": WORKLOAD_NAMES[name]}
-    if name in ("dense", "causal", "fp32"):
-        c = {"dense": MAIN, "causal": CAUSAL, "fp32": FP32}[name]
+    if name in ("dense", "causal", "fp32", "window", "chunked", "d64"):
+        c = {"dense": MAIN, "causal": CAUSAL, "fp32": FP32, "window": WINDOW, "chunked": CHUNKED,
+             "d64": DENSE64}[name]
+        Nq, Nk = c.get("Nq", c.get("N")), c.get("Nk", c.get("N"))
         dt = "fp32" if name == "fp32" else "bf16"
-        host = inputs.prefill_inputs(c["B"], c["Hq"], c["Hkv"], c["N"], c["N"], c["D"], dt, seed)
+        host = inputs.prefill_inputs(c["B"], c["Hq"], c["Hkv"], Nq, Nk, c["D"], dt, seed)
         q, k, v = (x.to(dev) for x in host)
         o = torch.empty_like(q)
-        lse = torch.empty(c["B"], c["Hq"], c["N"], device=dev, dtype=torch.float32)
+        lse = torch.empty(c["B"], c["Hq"], Nq, device=dev, dtype=torch.float32)
         call = binding.attn_fwd_fp32 if name == "fp32" else binding.attn_fwd
-        w["fn"] = lambda: call(q, k, v, o, lse, causal=c["causal"])
-        w["work"] = flops(**c)
+        wnd = c.get("window", 0)
+        w["fn"] = lambda: call(q, k, v, o, lse, causal=c["causal"], window=wnd)
+        w["work"] = masked_flops(c["B"], c["Hq"], Nq, Nk, c["D"], c["causal"], wnd) if "Nq" in c else flops(**c)
         w["unit"] = "TFLOP/s"
         w["launches"] = 1
         w["dtype"] = dt
-        w["seq_len"], w["batch"] = c["N"], c["B"]
+        w["seq_len"], w["batch"] = Nk, c["B"]
         if name == "fp32":
             w["bound"] = "alu"
             w["peak"] = GB300_SMS * FP32_SIMT_FLOP_PER_CLK_SM * sm_max_mhz * 1e6 / 1e12
@@ -410,7 +435,7 @@ def run_gb300(args, rank, world, local_rank):
     workloads = {}
     if not args.no_extras:
         xs = max(5, min(args.steps // 10, 50))
-        for name in ("dense", "causal", "decode", "fp32"):
+        for name in ("dense", "causal", "decode", "fp32", "window", "chunked", "d64"):
             if name == args.workload:
                 continue
             x = make_workload(name, dev, rank, peaks, peak_src, sm_max, args.decode_batch)

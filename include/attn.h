@@ -73,7 +73,7 @@ enum attn_status {
  *
  *   q   : bf16 [B, Hq,  Nq, D]        k, v : bf16 [B, Hkv, Nk, D]
  *   o   : bf16 [B, Hq,  Nq, D] (out)  lse  : fp32 [B, Hq, Nq] (out; may be NULL)
- *   D must be 128.  Scores and accumulation are fp32; P is rounded to bf16
+ *   D must be 64 or 128.  Scores and accumulation are fp32; P is rounded to bf16
  *   before the P V product; O is rounded to bf16 (round-to-nearest-even).
  *   scale multiplies Q K^T (1/sqrt(D) for standard attention).
  *   Errors: ATTN_ERR_NULL, _DIM, _GQA, _HEAD_DIM, _ALIGN, _SCALE, _DEVICE, _CUDA.

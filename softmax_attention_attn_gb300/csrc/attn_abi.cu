@@ -80,7 +80,7 @@ int check_common(const void* q, const void* k, const void* v, const void* o, con
                  int B, int Hq, int Hkv, int Nq, int Nk, int D, float scale) {
   if (!q || !k || !v || !o) return ATTN_ERR_NULL;
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || Nq <= 0 || Nk <= 0 || D <= 0) return ATTN_ERR_DIM;
-  if (B > 65535 || Hq > 65535) return ATTN_ERR_DIM;  // grid y / z limits
+  if (B > 65535 || Hq > 65535) return ATTN_ERR_DIM;  // fp32 grid y / z limits
   if (Hq % Hkv != 0) return ATTN_ERR_GQA;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || (lse && !aligned16(lse)))
     return ATTN_ERR_ALIGN;
@@ -127,10 +127,10 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
              attn_stream_t stream) {
   int rc = check_common(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, scale);
   if (rc != ATTN_OK) return rc;
-  if (D != 128) return ATTN_ERR_HEAD_DIM;
+  if (D != 64 && D != 128) return ATTN_ERR_HEAD_DIM;
   DeviceInfo* dev = nullptr;
   if ((rc = device_info(&dev)) != ATTN_OK) return rc;
-  return launch_fwd_bf16(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, window, dev->num_sms,
+  return launch_fwd_bf16(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, scale, causal, window, dev->num_sms,
                          reinterpret_cast<cudaStream_t>(stream), dev->err);
 }
 

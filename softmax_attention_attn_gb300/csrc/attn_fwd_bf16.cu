@@ -46,52 +46,61 @@ namespace fwd_bf16 {
 
 constexpr int BM = 128;                      // query rows per Q tile
 constexpr int BN = 128;                      // keys per K/V tile
-constexpr int HD = 128;                      // head dimension
-constexpr int NQT = 2;                       // Q tiles per CTA
-constexpr int STAGES = 5;                    // K/V ring slots (one K or one V tile each)
-constexpr int KBLK_BYTES = BN * 64 * 2;      // 64-column (128-byte) slab of a 128-row tile
-constexpr int TILE_BYTES = 2 * KBLK_BYTES;   // 128 x 128 bf16
-constexpr int SMEM_Q = 0;
-constexpr int SMEM_RING = SMEM_Q + NQT * TILE_BYTES;
-constexpr int SMEM_BAR = SMEM_RING + STAGES * TILE_BYTES;
-constexpr int NUM_BARS = 3 + 2 * STAGES + 6 * NQT;
-constexpr int SMEM_MISC = SMEM_BAR + NUM_BARS * 8;
-constexpr int SMEM_USED = SMEM_MISC + 16;
-constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack for 1024-byte alignment
+constexpr int NQT = 2;                       // Q tiles per work unit
+constexpr int KBLK_BYTES = 128 * 64 * 2;     // 64-column (128-byte) slab of a 128-row tile
 constexpr int NUM_SOFTMAX_WARPS = 4 * NQT;
 constexpr int WARP_TMA = NUM_SOFTMAX_WARPS;
 constexpr int WARP_MMA = NUM_SOFTMAX_WARPS + 1;      // issuer of Q tile t is warp WARP_MMA + t
 constexpr int NTHREADS = (NUM_SOFTMAX_WARPS + 1 + NQT) * 32;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float RESCALE_LOG2 = 8.0f;         // keep a stale max while the growth is <= 2^8
-constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, BN, 0);
-constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, HD, 1);
 
-static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
+// Shape constants for head dimension HD (64 or 128).
+template <int HD>
+struct Cfg {
+  static constexpr int KBLKS = HD / 64;                 // 128-byte slabs per tile row
+  static constexpr int TILE_BYTES = KBLKS * KBLK_BYTES; // one 128-row Q, K or V tile
+  static constexpr int STAGES = HD == 128 ? 5 : 10;     // K/V ring slots (one K or V tile each)
+  static constexpr int SMEM_Q = 0;
+  static constexpr int SMEM_RING = SMEM_Q + NQT * TILE_BYTES;
+  static constexpr int SMEM_BAR = SMEM_RING + STAGES * TILE_BYTES;
+  static constexpr int NUM_BARS = 3 + 2 * STAGES + 6 * NQT;
+  static constexpr int SMEM_MISC = SMEM_BAR + NUM_BARS * 8;
+  static constexpr int SMEM_ALLOC = SMEM_MISC + 16 + 1024;  // + slack for 1024-byte alignment
+  static constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, BN, 0);
+  static constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, HD, 1);
+  static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
+  static_assert(2 * BN + 2 * HD <= TMEM_COLS, "tensor memory budget");
+};
 
 __device__ __forceinline__ uint32_t s_col(int t) { return static_cast<uint32_t>(t * BN); }
+template <int HD>
 __device__ __forceinline__ uint32_t o_col(int t) { return static_cast<uint32_t>(NQT * BN + t * HD); }
 
 // S (tmem) = Q_tile (smem) x K_tile^T (smem); both K-major, 128-byte swizzle.
+template <int HD>
 __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
 #pragma unroll
   for (int kk = 0; kk < HD / 16; ++kk) {
     const uint32_t koff = static_cast<uint32_t>((kk >> 2) * KBLK_BYTES + (kk & 3) * 32);
     const uint64_t a = smem_desc_sw128(q_smem + koff, 16, 1024);
     const uint64_t b = smem_desc_sw128(k_smem + koff, 16, 1024);
-    mma_bf16_ss(d_tmem, a, b, IDESC_QK, kk > 0 ? 1u : 0u);
+    mma_bf16_ss(d_tmem, a, b, Cfg<HD>::IDESC_QK, kk > 0 ? 1u : 0u);
   }
 }
 
 // O (tmem) (+)= P (tmem, bf16) x V_tile (smem, MN-major: d contiguous), for the
-// 16-key steps kk in [kk0, kk0 + 4): one half of the tile's keys.
+// 16-key steps kk in [kk0, kk0 + 4): one half of the tile's keys.  With HD =
+// 128 the two 64-column slabs of V are KBLK_BYTES apart (the leading byte
+// offset of the MN-major operand); with HD = 64 there is one slab.
+template <int HD>
 __device__ __forceinline__ void issue_pv_half(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem,
                                               bool accumulate, int kk0) {
 #pragma unroll
   for (int kk = kk0; kk < kk0 + BN / 32; ++kk) {
     const uint64_t b = smem_desc_sw128(v_smem + static_cast<uint32_t>(kk * 16 * 128),
                                        KBLK_BYTES, 1024);
-    mma_bf16_ts(d_tmem, p_tmem + static_cast<uint32_t>(kk * 8), b, IDESC_PV,
+    mma_bf16_ts(d_tmem, p_tmem + static_cast<uint32_t>(kk * 8), b, Cfg<HD>::IDESC_PV,
                 (accumulate || kk > 0) ? 1u : 0u);
   }
 }
@@ -163,10 +172,19 @@ __device__ __forceinline__ void own_range(const Unit& u, int t, int& jb, int& je
   je = t == 0 ? u.je0 : u.je1;
 }
 
+template <int HD>
 __global__ void __launch_bounds__(NTHREADS, 1)
 attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+  using C = Cfg<HD>;
+  constexpr int KBLKS = C::KBLKS;
+  constexpr int TILE_BYTES = C::TILE_BYTES;
+  constexpr int STAGES = C::STAGES;
+  constexpr int SMEM_Q = C::SMEM_Q;
+  constexpr int SMEM_RING = C::SMEM_RING;
+  constexpr int SMEM_BAR = C::SMEM_BAR;
+  constexpr int SMEM_MISC = C::SMEM_MISC;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -238,7 +256,7 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
         if (nq > 0 && !mbar_wait(bar_q_empty, (nq - 1) & 1, abort_flag, p.err)) { ok = false; break; }
         mbar_arrive_expect_tx(bar_q_full, NQT * TILE_BYTES);
         for (int t = 0; t < NQT; ++t)
-          for (int kb = 0; kb < 2; ++kb)
+          for (int kb = 0; kb < KBLKS; ++kb)
             tma_load_3d(sb + SMEM_Q + t * TILE_BYTES + kb * KBLK_BYTES, &tm_q, bar_q_full, kb * 64,
                         u.q0 + t * BM, u.b * p.Hq + u.h);
         ++nq;
@@ -251,7 +269,7 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
             }
             mbar_arrive_expect_tx(bar_kv_full(s), TILE_BYTES);
             const CUtensorMap* m = kv ? &tm_v : &tm_k;
-            for (int kb = 0; kb < 2; ++kb)
+            for (int kb = 0; kb < KBLKS; ++kb)
               tma_load_3d(sb + SMEM_RING + s * TILE_BYTES + kb * KBLK_BYTES, m, bar_kv_full(s),
                           kb * 64, j * BN, u.b * p.Hkv + u.kvh);
           }
@@ -301,7 +319,7 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
         if (jb < je) {  // first S of this unit (outside the turn order)
           if (!mbar_wait(bar_kv_full(slot_of(kpos(jb))), phase_of(kpos(jb)), abort_flag, p.err)) { ok = false; break; }
           tc_fence_after();
-          issue_qk(tmem + s_col(t), q_sm, sb + SMEM_RING + slot_of(kpos(jb)) * TILE_BYTES);
+          issue_qk<HD>(tmem + s_col(t), q_sm, sb + SMEM_RING + slot_of(kpos(jb)) * TILE_BYTES);
           mma_commit(bar_s_full(t));
           mma_commit(bar_kv_empty(slot_of(kpos(jb))));
           if (je - jb == 1) mma_commit(bar_q_empty);  // that was this unit's last S
@@ -327,10 +345,10 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
           }
           if (own) {
             tc_fence_after();
-            issue_pv_half(tmem + o_col(t), tmem + s_col(t), vsm, j > jb, 0);
+            issue_pv_half<HD>(tmem + o_col<HD>(t), tmem + s_col(t), vsm, j > jb, 0);
             if (!mbar_wait(bar_p_hi(t), lt & 1, abort_flag, p.err)) { ok = false; break; }
             tc_fence_after();
-            issue_pv_half(tmem + o_col(t), tmem + s_col(t), vsm, true, BN / 32);
+            issue_pv_half<HD>(tmem + o_col<HD>(t), tmem + s_col(t), vsm, true, BN / 32);
             mma_commit(bar_kv_empty(slot_of(vpos)));
             if (j + 1 == je) {
               mma_commit(bar_o_full(t));
@@ -338,7 +356,7 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
               const int npos = kpos(j + 1);
               if (!mbar_wait(bar_kv_full(slot_of(npos)), phase_of(npos), abort_flag, p.err)) { ok = false; break; }
               tc_fence_after();
-              issue_qk(tmem + s_col(t), q_sm, sb + SMEM_RING + slot_of(npos) * TILE_BYTES);
+              issue_qk<HD>(tmem + s_col(t), q_sm, sb + SMEM_RING + slot_of(npos) * TILE_BYTES);
               mma_commit(bar_s_full(t));
               mma_commit(bar_kv_empty(slot_of(npos)));
               if (j + 2 == je) mma_commit(bar_q_empty);  // this unit's last S
@@ -366,7 +384,7 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     const int quad = warp % 4;
     const uint32_t lane_sel = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t s_addr = tmem + lane_sel + s_col(t);
-    const uint32_t o_addr = tmem + lane_sel + o_col(t);
+    const uint32_t o_addr = tmem + lane_sel + o_col<HD>(t);
     const float c = p.scale_log2;
     const int off = p.Nk - p.Nq;
     int n_own = 0;  // own key tiles so far (phase of s_full)
@@ -461,7 +479,7 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
           }
           if (half == 0 && rescale) {
 #pragma unroll 1
-            for (int ch = 0; ch < 4; ++ch) {
+            for (int ch = 0; ch < HD / 32; ++ch) {
               uint32_t o[32];
               tmem_ld32(o_addr + ch * 32, o);
               tmem_wait_ld();
@@ -492,7 +510,7 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
         ++n_out;
         tc_fence_after();
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
+        for (int ch = 0; ch < HD / 32; ++ch) {
           uint32_t (&oc)[32] = *reinterpret_cast<uint32_t(*)[32]>(o + 32 * ch);
           tmem_ld32(o_addr + ch * 32, oc);
         }
@@ -535,10 +553,13 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
 }  // namespace fwd_bf16
 
 // --------------------------------------------------------------------- host
-int launch_fwd_bf16(const void* q, const void* k, const void* v, void* o, float* lse, int B,
-                    int Hq, int Hkv, int Nq, int Nk, float scale, int causal, int window,
-                    int num_sms, cudaStream_t stream, int* err) {
-  using namespace fwd_bf16;
+namespace fwd_bf16 {
+
+template <int HD>
+int launch_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                int Hkv, int Nq, int Nk, float scale, int causal, int window, int num_sms,
+                cudaStream_t stream, int* err) {
+  using C = Cfg<HD>;
   CUtensorMap tq, tk, tv;
   const uint32_t box[3] = {64, 128, 1};
   if (!encode_tiled_3d(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, q, HD, Nq, static_cast<uint64_t>(B) * Hq,
@@ -552,8 +573,8 @@ int launch_fwd_bf16(const void* q, const void* k, const void* v, void* o, float*
   int dev = 0;
   cudaGetDevice(&dev);
   if (attr_set_dev != dev) {
-    if (cudaFuncSetAttribute(attn_fwd_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             SMEM_ALLOC) != cudaSuccess)
+    if (cudaFuncSetAttribute(attn_fwd_bf16_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::SMEM_ALLOC) != cudaSuccess)
       return ATTN_ERR_CUDA;
     attr_set_dev = dev;
   }
@@ -575,8 +596,25 @@ int launch_fwd_bf16(const void* q, const void* k, const void* v, void* o, float*
   const long long units = n_qblk * Hq * B;
   if (units > 0x7fffffffLL) return ATTN_ERR_DIM;
   const int grid = static_cast<int>(units < num_sms ? units : num_sms);
-  attn_fwd_bf16_kernel<<<grid, NTHREADS, SMEM_ALLOC, stream>>>(tq, tk, tv, prm);
+  attn_fwd_bf16_kernel<HD><<<grid, NTHREADS, C::SMEM_ALLOC, stream>>>(tq, tk, tv, prm);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // namespace fwd_bf16
+
+int launch_fwd_bf16(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                    int Hq, int Hkv, int Nq, int Nk, int D, float scale, int causal, int window,
+                    int num_sms, cudaStream_t stream, int* err) {
+  switch (D) {
+    case 64:
+      return fwd_bf16::launch_impl<64>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, window,
+                                       num_sms, stream, err);
+    case 128:
+      return fwd_bf16::launch_impl<128>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, window,
+                                        num_sms, stream, err);
+    default:
+      return ATTN_ERR_HEAD_DIM;
+  }
 }
 
 }  // namespace attn

@@ -31,7 +31,7 @@ bool encode_tiled_4d(CUtensorMap* map, CUtensorMapDataType dt, const void* base,
                      CUtensorMapSwizzle swz);
 
 int launch_fwd_bf16(const void* q, const void* k, const void* v, void* o, float* lse, int B,
-                    int Hq, int Hkv, int Nq, int Nk, float scale, int causal, int window,
+                    int Hq, int Hkv, int Nq, int Nk, int D, float scale, int causal, int window,
                     int num_sms, cudaStream_t stream, int* err);
 
 int launch_fwd_fp32(const float* q, const float* k, const float* v, float* o, float* lse, int B,

@@ -75,3 +75,11 @@ def test_warmup_below_three_is_rejected():
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
                         "--steps", "3", "--warmup", "2"], capture_output=True, text=True, timeout=600)
     assert r.returncode != 0
+
+
+def test_visible_pairs_matches_enumeration():
+    for Nq, Nk, causal, window in [(5, 5, True, 0), (3, 7, True, 0), (7, 3, True, 0), (6, 6, True, 2),
+                                   (5, 4, False, 3), (4, 4, False, 0)]:
+        brute = sum(1 for i in range(Nq) for j in range(Nk)
+                    if (not causal or j <= i + Nk - Nq) and (window <= 0 or j > i + Nk - Nq - window))
+        assert bench.visible_pairs(Nq, Nk, causal, window) == brute

@@ -106,8 +106,8 @@ def test_fp32_edge_cases(dev, case):
 
 
 # ---------------------------------------------------------------- bf16 path
-def run_bf16(dev, B, Hq, Hkv, Nq, Nk, causal=False, window=0, seed=0):
-    q, k, v = inputs.prefill_inputs(B, Hq, Hkv, Nq, Nk, 128, "bf16", seed)
+def run_bf16(dev, B, Hq, Hkv, Nq, Nk, causal=False, window=0, seed=0, D=128):
+    q, k, v = inputs.prefill_inputs(B, Hq, Hkv, Nq, Nk, D, "bf16", seed)
     o, lse = binding.attn_fwd(q.to(dev), k.to(dev), v.to(dev), causal=causal, window=window)
     return q, k, v, o, lse
 
@@ -133,6 +133,40 @@ def test_bf16_cases(dev, case):
     q, k, v, o, lse = run_bf16(dev, B, Hq, Hkv, Nq, Nk, causal, window, seed=11)
     O, L = oracle.attention_forward(q, k, v, 1 / math.sqrt(128), causal, window)
     check(o, lse, O, L, BF16_O_TOL, BF16_LSE_REL, True)
+
+
+BF16_D64_CASES = [  # (B, Hq, Hkv, Nq, Nk, causal, window)
+    (1, 2, 2, 128, 128, False, 0),
+    (1, 2, 2, 300, 300, False, 0),
+    (2, 4, 2, 513, 513, True, 0),
+    (1, 2, 1, 256, 1000, True, 0),
+    (1, 2, 2, 700, 300, True, 0),
+    (1, 2, 2, 1000, 1000, True, 100),
+    (1, 4, 4, 2048, 2048, False, 0),
+]
+
+
+@pytest.mark.parametrize("case", BF16_D64_CASES, ids=str)
+def test_bf16_head_dim_64(dev, case):
+    B, Hq, Hkv, Nq, Nk, causal, window = case
+    q, k, v, o, lse = run_bf16(dev, B, Hq, Hkv, Nq, Nk, causal, window, seed=13, D=64)
+    O, L = oracle.attention_forward(q, k, v, 1 / math.sqrt(64), causal, window)
+    check(o, lse, O, L, BF16_O_TOL, BF16_LSE_REL, True)
+
+
+@pytest.mark.parametrize("name,B,Hq,Hkv,Nq,Nk,D,causal,window", [
+    ("sliding_window_4096_B1_H32_KV8_N16384", 1, 32, 8, 16384, 16384, 128, True, 4096),
+    ("chunked_prefill_B1_H32_KV8_Nq2048_Nk16384", 1, 32, 8, 2048, 16384, 128, True, 0),
+    ("dense_d64_B1_H32_N8192", 1, 32, 32, 8192, 8192, 64, False, 0),
+])
+def test_bf16_widened_workloads_sampled(dev, name, B, Hq, Hkv, Nq, Nk, D, causal, window):
+    """Sliding window, chunked prefill (Nq < Nk, bottom-right causal) and D=64 at full size."""
+    q, k, v, o, lse = run_bf16(dev, B, Hq, Hkv, Nq, Nk, causal, window, seed=1, D=D)
+    assert torch.isfinite(o.float()).all().item() and torch.isfinite(lse).all().item()
+    rows = sample_rows(B, Hq, Nq, 64, seed=9)
+    O, L = oracle.attention_rows(q, k, v, 1 / math.sqrt(D), rows, causal, window)
+    idx = tuple(np.array(rows).T)
+    check(o.cpu()[idx], lse.cpu()[idx], O, L, BF16_O_TOL, BF16_LSE_REL, True)
 
 
 @pytest.mark.parametrize("name,B,Hq,Hkv,N,causal", [
