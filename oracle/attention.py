@@ -32,7 +32,12 @@ Sources (pages on softmax attention):
     - split-KV decode cuts each sequence's keys into chunks of ``chunk`` keys
       starting at key 0 (the last chunk may be short); each chunk yields its own
       normalised output and LSE, and the combine step weights chunk c by
-      ``exp(LSE_c - max_c LSE_c)``.
+      ``exp(LSE_c - max_c LSE_c)``;
+    - a paged KV cache (paged and contiguous caches are both on the list) holds
+      pages of ``page_size`` token rows ``[num_pages, page_size, Hkv, D]``; a
+      block table ``[B, max_pages]`` names, for sequence b, the page of its
+      logical page i, so key j of sequence b is row ``j % page_size`` of page
+      ``block_table[b, j // page_size]``.
 
 Every pin of this module lives in ``tests/test_oracle.py``.
 """
@@ -43,7 +48,7 @@ import numpy as np
 __all__ = [
     "visible_mask", "kv_head", "attention_forward", "attention_rows",
     "attention_probabilities", "decode_forward", "decode_split_partials",
-    "decode_combine",
+    "decode_combine", "paged_rows", "decode_forward_paged",
 ]
 
 
@@ -236,4 +241,39 @@ def decode_combine(O_part, LSE_part, n_split):
         s = w.sum(axis=1)
         O[b] = np.einsum("hc,hcd->hd", w, O_part[b, :, :n]) / s[:, None]
         LSE[b] = M + np.log(s)
+    return O, LSE
+
+
+# ---------------------------------------------------------------------------
+# Paged KV cache: key j of sequence b is row j % page_size of page
+# block_table[b, j // page_size].
+# ---------------------------------------------------------------------------
+
+def paged_rows(pages, block_table_b, n: int):
+    """The first ``n`` token rows of one sequence, gathered from its pages."""
+    page_size = pages.shape[1]
+    j = np.arange(n)
+    page = np.asarray(block_table_b)[j // page_size]
+    return _f64(pages[page, j % page_size]) if n else np.zeros((0,) + tuple(pages.shape[2:]))
+
+
+def decode_forward_paged(q, k_pages, v_pages, block_table, seqlens, scale: float, batches=None):
+    """Decode against a paged cache: ``O [B,Hq,D]``, ``LSE [B,Hq]``.
+
+    Same definition as :func:`decode_forward`, with sequence b's keys gathered
+    through its block-table row.
+    """
+    B, Hq, D = q.shape
+    Hkv = k_pages.shape[2]
+    bt = np.asarray(block_table)
+    lens = [int(x) for x in seqlens]
+    O = np.zeros((B, Hq, v_pages.shape[3]))
+    LSE = np.zeros((B, Hq))
+    for b in (range(B) if batches is None else batches):
+        Kb = paged_rows(k_pages, bt[b], lens[b])          # [Nk_b, Hkv, D]
+        Vb = paged_rows(v_pages, bt[b], lens[b])
+        qb = _f64(q[b])
+        for h in range(Hq):
+            kh = kv_head(h, Hq, Hkv)
+            O[b, h], LSE[b, h] = _decode_one(qb[h], Kb[:, kh], Vb[:, kh], scale)
     return O, LSE

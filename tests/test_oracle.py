@@ -245,6 +245,36 @@ def pin_decode(ora):
     assert np.allclose(Op[b, :, c], Oe[0, :, 0], atol=1e-12) and np.allclose(Lp[b, :, c], Le[0, :, 0], atol=1e-12)
 
 
+def pin_paged_decode(ora):
+    """Paged decode equals contiguous decode of the same rows, for any page placement."""
+    q, kc, vc, lens = _decode_case()
+    B, Hq, D = q.shape
+    Nk_max, Hkv = kc.shape[1], kc.shape[2]
+    O, L = ora.decode_forward(q, kc, vc, lens, 0.45)
+    for page_size in (1, 2, 4):
+        max_pages = -(-Nk_max // page_size)
+        perm = np.random.default_rng(page_size).permutation(B * max_pages)
+        bt = perm.reshape(B, max_pages)
+        kp = np.full((B * max_pages, page_size, Hkv, D), np.nan)
+        vp = np.full((B * max_pages, page_size, Hkv, D), np.nan)
+        for b in range(B):
+            for j in range(Nk_max):
+                kp[bt[b, j // page_size], j % page_size] = kc[b, j]
+                vp[bt[b, j // page_size], j % page_size] = vc[b, j]
+        Op, Lp = ora.decode_forward_paged(q, kp, vp, bt, lens, 0.45)
+        assert np.allclose(Op, O, rtol=0, atol=1e-14) and np.allclose(Lp, L, rtol=0, atol=1e-14), page_size
+    # a hand-built 2-page layout of the golden example's keys (pages in reverse order)
+    G = _read_golden("closed_form_tiny.txt")
+    Kg, Vg = G[("input", "K")], G[("input", "V")]            # [3, 2]
+    kp = np.zeros((2, 2, 1, 2))
+    vp = np.zeros((2, 2, 1, 2))
+    kp[1, :, 0], kp[0, :1, 0] = Kg[:2], Kg[2:]
+    vp[1, :, 0], vp[0, :1, 0] = Vg[:2], Vg[2:]
+    Op, Lp = ora.decode_forward_paged(G[("input", "Q")][:1][None], kp, vp, [[1, 0]], [3], 1.0)
+    assert np.allclose(Op[0, 0], G[("dense", "O")][0], atol=1e-14)
+    assert abs(Lp[0, 0] - G[("dense", "LSE")][0][0]) < 1e-14
+
+
 # ---------------------------------------------------------------- golden
 def _read_golden(name):
     env = {"ln": math.log}
@@ -281,7 +311,7 @@ def pin_golden(ora):
 
 
 PINS = [pin_brute_force, pin_sdpa, pin_zero_query, pin_single_key, pin_probability_rows,
-        pin_causal_first_row, pin_dominant_key, pin_invariants, pin_decode, pin_golden]
+        pin_causal_first_row, pin_dominant_key, pin_invariants, pin_decode, pin_paged_decode, pin_golden]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
@@ -367,6 +397,13 @@ def _mut_combine_unweighted(O_part, LSE_part, n_split):
     return O, L
 
 
+def _mut_paged_rows_swapped(pages, block_table_b, n):
+    page_size = pages.shape[1]
+    j = np.arange(n)
+    page = np.asarray(block_table_b)[j % page_size] if n else np.zeros(0, dtype=int)
+    return np.asarray(pages[page, j // page_size], dtype=np.float64) if n else np.zeros((0,) + tuple(pages.shape[2:]))
+
+
 MUTANTS = {
     "no_scale": ("_scores", _mut_no_scale),
     "sqrt_scale": ("_scores", _mut_sqrt_scale),
@@ -378,6 +415,7 @@ MUTANTS = {
     "lse_missing_max": ("_softmax_rows", _wrap_softmax("no_max")),
     "softmax_over_queries": ("_softmax_rows", _wrap_softmax("key_axis_swapped")),
     "combine_unweighted": ("decode_combine", _mut_combine_unweighted),
+    "paged_index_swapped": ("paged_rows", _mut_paged_rows_swapped),
 }
 
 
