@@ -82,7 +82,8 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
-    ap.add_argument("--workload", choices=["dense", "causal", "decode", "fp32", "window", "chunked", "d64"],
+    ap.add_argument("--workload", choices=["dense", "causal", "decode", "fp32", "window", "chunked", "d64",
+                                           "paged"],
                     default="dense",
                     help="workload of the timed loop (default: the dense bf16 prefill)")
     ap.add_argument("--no-extras", action="store_true", help="skip the other workloads")
@@ -263,6 +264,7 @@ WORKLOAD_NAMES = {
     "window": "bf16 causal sliding-window (4096) prefill B=1 Hq=32 Hkv=8 N=16384 D=128",
     "chunked": "bf16 chunked prefill (causal, bottom-right) B=1 Hq=32 Hkv=8 Nq=2048 Nk=16384 D=128",
     "d64": "bf16 dense prefill B=1 H=32 N=8192 D=64 (non-causal)",
+    "paged": "bf16 split-KV decode on a paged cache (page 256) B=64 Hq=32 Hkv=8 D=128, Nk_b~U[512,32768], chunk 512",
 }
 
 
@@ -300,16 +302,33 @@ def make_workload(name, dev, seed, peaks, peak_src, sm_max_mhz, decode_batch=Non
         w["e2e_out"] = [o, lse]
     else:
         d = dict(DECODE, B=decode_batch or DECODE["B"])
-        w["desc"] = WORKLOAD_NAMES["decode"].replace("B=64", f"B={d['B']}")
-        qh, kc, vc, sl = inputs.decode_inputs(d["B"], d["Hq"], d["Hkv"], d["D"], d["nk_lo"], d["nk_hi"],
-                                              seed=seed, device=dev)
-        q, sl_d = qh.to(dev), sl.to(dev)
+        w["desc"] = WORKLOAD_NAMES[name].replace("B=64", f"B={d['B']}")
         ws = torch.empty(binding.attn_decode_workspace_size(d["B"], d["Hq"], d["D"], d["nk_hi"], d["chunk"]),
                          device=dev, dtype=torch.uint8)
         o = torch.empty(d["B"], d["Hq"], d["D"], device=dev, dtype=torch.bfloat16)
         lse = torch.empty(d["B"], d["Hq"], device=dev)
-        w["fn"] = lambda: binding.attn_decode(q, kc, vc, sl_d, ws, o, lse, chunk=d["chunk"])
-        w["split_fn"] = lambda: binding.attn_decode_splitkv(q, kc, vc, sl_d, ws, chunk=d["chunk"])
+        if name == "decode":
+            qh, kc, vc, sl = inputs.decode_inputs(d["B"], d["Hq"], d["Hkv"], d["D"], d["nk_lo"], d["nk_hi"],
+                                                  seed=seed, device=dev)
+            q, sl_d = qh.to(dev), sl.to(dev)
+            w["fn"] = lambda: binding.attn_decode(q, kc, vc, sl_d, ws, o, lse, chunk=d["chunk"])
+            w["split_fn"] = lambda: binding.attn_decode_splitkv(q, kc, vc, sl_d, ws, chunk=d["chunk"])
+            extra_in = [(sl, sl_d), (None, kc), (None, vc)]
+        else:
+            qh, kc, vc, bt, sl = inputs.paged_decode_inputs(d["B"], d["Hq"], d["Hkv"], d["D"], d["nk_lo"],
+                                                            d["nk_hi"], 256, seed=seed, device=dev)
+            q, sl_d, bt_d = qh.to(dev), sl.to(dev), bt.to(dev)
+            w["fn"] = lambda: binding.attn_decode_paged(q, kc, vc, bt_d, sl_d, ws, o, lse, chunk=d["chunk"])
+            lib = binding.lib()
+
+            def split_paged():
+                rc = lib.attn_decode_splitkv_paged(
+                    binding._ptr(q), binding._ptr(kc), binding._ptr(vc), binding._ptr(bt_d), binding._ptr(sl_d),
+                    binding._ptr(ws), d["B"], d["Hq"], d["Hkv"], kc.shape[0], 256, bt.shape[1], d["D"],
+                    1 / math.sqrt(d["D"]), d["chunk"], binding._stream(None))
+                assert rc == 0
+            w["split_fn"] = split_paged
+            extra_in = [(sl, sl_d), (bt, bt_d), (None, kc), (None, vc)]
         kv_bytes = int(sl.sum()) * d["Hkv"] * d["D"] * 2 * 2
         w["kv_bytes"] = kv_bytes
         w["work"] = kv_bytes + q.numel() * 2 + o.numel() * 2 + lse.numel() * 4
@@ -320,7 +339,7 @@ def make_workload(name, dev, seed, peaks, peak_src, sm_max_mhz, decode_batch=Non
         w["bound"] = "hbm"
         w["peak"] = peaks["hbm_gbs"]
         w["peak_source"] = f"{peak_src} copy bandwidth"
-        w["e2e_in"] = [(qh, q), (sl, sl_d), (None, kc), (None, vc)]
+        w["e2e_in"] = [(qh, q)] + extra_in
         w["e2e_out"] = [o, lse]
     return w
 
@@ -379,7 +398,7 @@ def run_gb300(args, rank, world, local_rank):
     clocks = clk.summary()
     ms_step = max_over_ranks(sum(ms) / len(ms))
     value = world * rate(w, ms_step)
-    if w["name"] == "decode":   # roofline of the dominant kernel: the split-KV partial step
+    if w["name"] in ("decode", "paged"):   # roofline of the dominant kernel: the split-KV partial step
         ms_k = max_over_ranks(statistics.mean(time_steps(torch, w["split_fn"], min(args.steps, 50), 3, flush, stream)))
         achieved = w["kv_bytes"] / (ms_k * 1e-3) / 1e9
         traffic = None
@@ -396,10 +415,11 @@ def run_gb300(args, rank, world, local_rank):
         pins = [(x.pin_memory() if x is not None else torch.empty(t.shape, dtype=t.dtype).pin_memory(), t)
                 for x, t in w["e2e_in"]]
         outs = [(torch.empty(t.shape, dtype=t.dtype).pin_memory(), t) for t in w["e2e_out"]]
-        if w["name"] == "decode":   # the host copy of the caches is the device draw
-            for hp, t in pins[2:]:
-                hp.copy_(t)
-        e2e_steps = max(5, min(args.steps, 100 if w["name"] != "decode" else 10))
+        if w["name"] in ("decode", "paged"):   # the host copy of the caches is the device draw
+            for (x, t), (hp, _) in zip(w["e2e_in"], pins):
+                if x is None:
+                    hp.copy_(t)
+        e2e_steps = max(5, min(args.steps, 100 if w["name"] not in ("decode", "paged") else 10))
 
         def e2e_step():
             for hp, t in pins:
@@ -435,7 +455,7 @@ def run_gb300(args, rank, world, local_rank):
     workloads = {}
     if not args.no_extras:
         xs = max(5, min(args.steps // 10, 50))
-        for name in ("dense", "causal", "decode", "fp32", "window", "chunked", "d64"):
+        for name in ("dense", "causal", "decode", "paged", "fp32", "window", "chunked", "d64"):
             if name == args.workload:
                 continue
             x = make_workload(name, dev, rank, peaks, peak_src, sm_max, args.decode_batch)
@@ -443,7 +463,7 @@ def run_gb300(args, rank, world, local_rank):
             r = rate(x, mx)
             entry = {"workload": x["desc"], "value": world * r, "unit": x["unit"], "ms_per_step": mx,
                      "bound": x["bound"], "frac": r / x["peak"], "peak": x["peak"], "peak_source": x["peak_source"]}
-            if name == "decode":
+            if name in ("decode", "paged"):
                 mk = max_over_ranks(statistics.mean(time_steps(torch, x["split_fn"], xs, 3, flush, stream)))
                 entry["splitkv_kernel_ms"] = mk
                 entry["splitkv_kernel_gbs"] = x["kv_bytes"] / (mk * 1e-3) / 1e9

@@ -63,7 +63,8 @@ enum attn_status {
   ATTN_ERR_DEVICE = -9,      /* the current device is not an sm_103 GPU                */
   ATTN_ERR_SEQLEN = -10,     /* a decode sequence length is < 1 or > Nk_max (device)   */
   ATTN_ERR_CHUNK = -11,      /* split-KV chunk size not supported                       */
-  ATTN_ERR_CAPACITY = -12    /* a size exceeds a fixed capacity of the entry point      */
+  ATTN_ERR_CAPACITY = -12,   /* a size exceeds a fixed capacity of the entry point      */
+  ATTN_ERR_PAGE = -13        /* a block-table entry in use is outside [0, num_pages)    */
 };
 
 /*
@@ -125,6 +126,28 @@ int attn_decode_splitkv(const void* q, const void* k_cache, const void* v_cache,
                         const int* seqlens, void* workspace,
                         int B, int Hq, int Hkv, int Nk_max, int D,
                         float scale, int chunk, attn_stream_t stream);
+
+/*
+ * attn_decode_splitkv_paged — split-KV decode, partial step, on a paged KV
+ * cache.   [ASK] "研究动机" (paged and contiguous KV caches, split-KV decode).
+ *
+ *   k_pages, v_pages : bf16 [num_pages, page_size, Hkv, D]   (a shared page pool)
+ *   block_table      : int32 [B, max_pages] (device); key j of sequence b is row
+ *                      j % page_size of page block_table[b, j / page_size]
+ *   Other arguments, the workspace layout and the results are those of
+ *   attn_decode_splitkv with Nk_max = max_pages * page_size (size the
+ *   workspace and call attn_decode_combine with that Nk_max).  page_size must
+ *   be a multiple of 64 (a 64-key tile never straddles two pages).  Only the
+ *   block-table entries of pages that hold keys j < seqlens[b] are read; an
+ *   entry outside [0, num_pages) sets ATTN_ERR_PAGE in the device error word
+ *   (that tile reads zeros).
+ *   Errors: as attn_decode_splitkv, plus ATTN_ERR_DIM for a page_size that is
+ *   not a positive multiple of 64.
+ */
+int attn_decode_splitkv_paged(const void* q, const void* k_pages, const void* v_pages,
+                              const int* block_table, const int* seqlens, void* workspace,
+                              int B, int Hq, int Hkv, int num_pages, int page_size, int max_pages,
+                              int D, float scale, int chunk, attn_stream_t stream);
 
 /*
  * attn_decode_combine — split-KV decode, combine step.  LSE-weighted merge of

@@ -18,7 +18,7 @@ STATUS = {
     0: "ATTN_OK", -1: "ATTN_ERR_NULL", -2: "ATTN_ERR_DIM", -3: "ATTN_ERR_GQA",
     -4: "ATTN_ERR_HEAD_DIM", -5: "ATTN_ERR_ALIGN", -6: "ATTN_ERR_SCALE", -7: "ATTN_ERR_CUDA",
     -8: "ATTN_ERR_TIMEOUT", -9: "ATTN_ERR_DEVICE", -10: "ATTN_ERR_SEQLEN",
-    -11: "ATTN_ERR_CHUNK", -12: "ATTN_ERR_CAPACITY",
+    -11: "ATTN_ERR_CHUNK", -12: "ATTN_ERR_CAPACITY", -13: "ATTN_ERR_PAGE",
 }
 
 _c_int, _c_float, _vp = ctypes.c_int, ctypes.c_float, ctypes.c_void_p
@@ -28,6 +28,7 @@ SIGNATURES = {
     "attn_decode_workspace_size": (ctypes.c_size_t, [_c_int] * 5),
     "attn_decode_splitkv": (_c_int, [_vp] * 5 + [_c_int] * 5 + [_c_float, _c_int, _vp]),
     "attn_decode_combine": (_c_int, [_vp] * 4 + [_c_int] * 5 + [_vp]),
+    "attn_decode_splitkv_paged": (_c_int, [_vp] * 6 + [_c_int] * 7 + [_c_float, _c_int, _vp]),
     "attn_decode_noalloc": (_c_int, [_vp] * 6 + [_c_int] * 5 + [_c_float, _c_int, _vp]),
     "attn_get_device_error": (_c_int, [_vp]),
     "attn_strerror": (ctypes.c_char_p, [_c_int]),
@@ -169,6 +170,32 @@ def attn_decode(q, k_cache, v_cache, seqlens, workspace=None, o=None, lse=None, 
                                 device=q.device, dtype=torch.uint8)
     attn_decode_splitkv(q, k_cache, v_cache, seqlens, workspace, scale, chunk, stream)
     return attn_decode_combine(workspace, seqlens, B, Hq, Nk_max, D, o, lse, chunk, q.device, stream)
+
+
+def attn_decode_paged(q, k_pages, v_pages, block_table, seqlens, workspace=None, o=None, lse=None,
+                      scale=None, chunk=512, stream=None):
+    """Split-KV decode on a paged cache: partial step, then combine step."""
+    import torch
+    _require(q, torch.bfloat16, "q")
+    _require(k_pages, torch.bfloat16, "k_pages")
+    _require(v_pages, torch.bfloat16, "v_pages")
+    _require(block_table, torch.int32, "block_table")
+    _require(seqlens, torch.int32, "seqlens")
+    B, Hq, D = q.shape
+    num_pages, page_size, Hkv, _ = k_pages.shape
+    max_pages = block_table.shape[1]
+    nk_max = max_pages * page_size
+    need = attn_decode_workspace_size(B, Hq, D, nk_max, chunk)
+    if workspace is None:
+        workspace = torch.empty(need, device=q.device, dtype=torch.uint8)
+    if workspace.numel() * workspace.element_size() < need:
+        raise ValueError(f"workspace holds fewer than {need} bytes")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    code = lib().attn_decode_splitkv_paged(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table),
+                                           _ptr(seqlens), _ptr(workspace), B, Hq, Hkv, num_pages,
+                                           page_size, max_pages, D, scale, int(chunk), _stream(stream))
+    _check(code, "attn_decode_splitkv_paged")
+    return attn_decode_combine(workspace, seqlens, B, Hq, nk_max, D, o, lse, chunk, q.device, stream)
 
 
 def attn_decode_noalloc(q, k_cache, v_cache, seqlens, o=None, lse=None, scale=None, chunk=512,

@@ -183,6 +183,26 @@ int attn_decode_splitkv(const void* q, const void* k_cache, const void* v_cache,
                                       reinterpret_cast<cudaStream_t>(stream), dev->err));
 }
 
+int attn_decode_splitkv_paged(const void* q, const void* k_pages, const void* v_pages,
+                              const int* block_table, const int* seqlens, void* workspace, int B,
+                              int Hq, int Hkv, int num_pages, int page_size, int max_pages, int D,
+                              float scale, int chunk, attn_stream_t stream) {
+  if (!q || !k_pages || !v_pages || !block_table || !seqlens || !workspace) return ATTN_ERR_NULL;
+  if (num_pages <= 0 || max_pages <= 0 || page_size <= 0 || page_size % 64 != 0) return ATTN_ERR_DIM;
+  if (static_cast<long long>(max_pages) * page_size > 0x7fffffffLL) return ATTN_ERR_DIM;
+  int rc = check_decode(B, Hq, Hkv, max_pages * page_size, D, chunk);
+  if (rc != ATTN_OK) return rc;
+  if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(workspace) ||
+      !aligned16(seqlens) || !aligned16(block_table))
+    return ATTN_ERR_ALIGN;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_SCALE;
+  DeviceInfo* dev = nullptr;
+  if ((rc = device_info(&dev)) != ATTN_OK) return rc;
+  return launch_decode_splitkv_paged(q, k_pages, v_pages, block_table, seqlens, workspace, B, Hq,
+                                     Hkv, num_pages, page_size, max_pages, scale, chunk,
+                                     dev->num_sms, reinterpret_cast<cudaStream_t>(stream), dev->err);
+}
+
 int attn_decode_combine(const void* workspace, const int* seqlens, void* o, float* lse, int B,
                         int Hq, int Nk_max, int D, int chunk, attn_stream_t stream) {
   if (!workspace || !seqlens || !o) return ATTN_ERR_NULL;
@@ -228,6 +248,7 @@ const char* attn_strerror(int code) {
     case ATTN_ERR_SEQLEN: return "a decode sequence length is outside [1, Nk_max]";
     case ATTN_ERR_CHUNK: return "split-KV chunk must be a multiple of 64 in [64, 1024]";
     case ATTN_ERR_CAPACITY: return "a size exceeds a fixed capacity of the entry point";
+    case ATTN_ERR_PAGE: return "a block-table entry in use is outside [0, num_pages)";
     default: return "unknown status code";
   }
 }

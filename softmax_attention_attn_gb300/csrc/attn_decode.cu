@@ -112,13 +112,23 @@ __device__ __forceinline__ Work decode_work(int w, const int* split, int B, int 
   return r;
 }
 
-template <int G>
+// Paged cache: key j of sequence b is row j % page_size of page
+// block_table[b * max_pages + j / page_size] of a page pool [num_pages,
+// page_size, Hkv, D]; page_size is a multiple of the 64-key tile, so a tile
+// never straddles two pages.
+struct Paging {
+  const int* block_table;
+  int max_pages, page_size, num_pages;
+};
+
+template <int G, bool PAGED>
 __global__ void __launch_bounds__(NTHREADS, 2)
 attn_decode_splitkv_kernel(const __grid_constant__ CUtensorMap tm_k,
                            const __grid_constant__ CUtensorMap tm_v,
                            const __nv_bfloat16* __restrict__ q, const int* __restrict__ seqlens,
                            float* __restrict__ ws_o, float* __restrict__ ws_lse, int B, int Hq,
-                           int Hkv, int Nk_max, int chunk, int S_max, float c_log2, int* err) {
+                           int Hkv, int Nk_max, int chunk, int S_max, float c_log2, int* err,
+                           const Paging pg) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -192,8 +202,19 @@ attn_decode_splitkv_kernel(const __grid_constant__ CUtensorMap tm_k,
               break;
             }
             mbar_arrive_expect_tx(bar_full(s), TILE_BYTES);
-            tma_load_4d(sb + L.ring + s * TILE_BYTES, m, bar_full(s), 0, wk.kvh,
-                        wk.c * chunk + tl * TILE, wk.b);
+            const int key0 = wk.c * chunk + tl * TILE;
+            if constexpr (PAGED) {
+              const int lp = key0 / pg.page_size;
+              int page = __ldg(pg.block_table + static_cast<size_t>(wk.b) * pg.max_pages + lp);
+              if (page < 0 || page >= pg.num_pages) {  // reported; the copy reads zeros instead
+                atomicCAS(err, 0, ATTN_ERR_PAGE);
+                page = pg.num_pages;
+              }
+              tma_load_4d(sb + L.ring + s * TILE_BYTES, m, bar_full(s), 0, wk.kvh,
+                          key0 - lp * pg.page_size, page);
+            } else {
+              tma_load_4d(sb + L.ring + s * TILE_BYTES, m, bar_full(s), 0, wk.kvh, key0, wk.b);
+            }
           }
         }
       }
@@ -303,6 +324,10 @@ attn_decode_splitkv_kernel(const __grid_constant__ CUtensorMap tm_k,
         const uint4 u = *reinterpret_cast<const uint4*>(tile + key * (HD * 2) + g16 * 16);
         float vf[8];
         bf16x8_to_float(u, vf);
+        if (tl * TILE + key >= wk.n_valid) {  // rows past the sequence: never let them in (p is 0,
+#pragma unroll                                // but 0 * NaN from an unused cache row is not)
+          for (int e = 0; e < 8; ++e) vf[e] = 0.f;
+        }
 #pragma unroll
         for (int h = 0; h < G; ++h) {
           const float pw = work[h * chunk + tl * TILE + key];
@@ -389,10 +414,10 @@ attn_decode_combine_kernel(const float* __restrict__ ws_o, const float* __restri
   if (lane == 0 && lse != nullptr) lse[bh] = M + logf(s);
 }
 
-template <int G>
+template <int G, bool PAGED>
 int launch_split(const CUtensorMap& tk, const CUtensorMap& tv, const void* q, const int* seqlens,
                  float* ws_o, float* ws_lse, int B, int Hq, int Hkv, int Nk_max, float scale,
-                 int chunk, int S_max, int num_sms, cudaStream_t stream, int* err) {
+                 int chunk, int S_max, int num_sms, cudaStream_t stream, int* err, const Paging& pg) {
   const Layout L = layout(G, chunk, B);
   const int smem = L.bytes + 1024;
   static int attr_dev = -1;
@@ -400,17 +425,33 @@ int launch_split(const CUtensorMap& tk, const CUtensorMap& tv, const void* q, co
   int dev = 0;
   cudaGetDevice(&dev);
   if (attr_dev != dev || attr_bytes < smem) {
-    if (cudaFuncSetAttribute(attn_decode_splitkv_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem) != cudaSuccess)
+    if (cudaFuncSetAttribute(attn_decode_splitkv_kernel<G, PAGED>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
       return ATTN_ERR_CUDA;
     attr_dev = dev;
     attr_bytes = smem;
   }
   const int grid = 2 * num_sms;
-  attn_decode_splitkv_kernel<G><<<grid, NTHREADS, smem, stream>>>(
+  attn_decode_splitkv_kernel<G, PAGED><<<grid, NTHREADS, smem, stream>>>(
       tk, tv, static_cast<const __nv_bfloat16*>(q), seqlens, ws_o, ws_lse, B, Hq, Hkv, Nk_max, chunk,
-      S_max, scale * 1.4426950408889634f, err);
+      S_max, scale * 1.4426950408889634f, err, pg);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+template <bool PAGED>
+int launch_split_any(const CUtensorMap& tk, const CUtensorMap& tv, const void* q, const int* seqlens,
+                     void* workspace, int B, int Hq, int Hkv, int Nk_max, float scale, int chunk,
+                     int num_sms, cudaStream_t stream, int* err, const Paging& pg) {
+  const int S_max = (Nk_max + chunk - 1) / chunk;
+  float* ws_o = static_cast<float*>(workspace);
+  float* ws_lse = ws_o + static_cast<size_t>(B) * Hq * S_max * HD;
+  switch (Hq / Hkv) {
+    case 1: return launch_split<1, PAGED>(tk, tv, q, seqlens, ws_o, ws_lse, B, Hq, Hkv, Nk_max, scale, chunk, S_max, num_sms, stream, err, pg);
+    case 2: return launch_split<2, PAGED>(tk, tv, q, seqlens, ws_o, ws_lse, B, Hq, Hkv, Nk_max, scale, chunk, S_max, num_sms, stream, err, pg);
+    case 4: return launch_split<4, PAGED>(tk, tv, q, seqlens, ws_o, ws_lse, B, Hq, Hkv, Nk_max, scale, chunk, S_max, num_sms, stream, err, pg);
+    case 8: return launch_split<8, PAGED>(tk, tv, q, seqlens, ws_o, ws_lse, B, Hq, Hkv, Nk_max, scale, chunk, S_max, num_sms, stream, err, pg);
+    default: return ATTN_ERR_GQA;
+  }
 }
 
 }  // namespace decode
@@ -427,16 +468,26 @@ int launch_decode_splitkv(const void* q, const void* k_cache, const void* v_cach
       !encode_tiled_4d(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, v_cache, HD, Hkv, Nk_max, B, 2, box,
                        CU_TENSOR_MAP_SWIZZLE_NONE))
     return ATTN_ERR_CUDA;
-  const int S_max = (Nk_max + chunk - 1) / chunk;
-  float* ws_o = static_cast<float*>(workspace);
-  float* ws_lse = ws_o + static_cast<size_t>(B) * Hq * S_max * HD;
-  switch (Hq / Hkv) {
-    case 1: return launch_split<1>(tk, tv, q, seqlens, ws_o, ws_lse, B, Hq, Hkv, Nk_max, scale, chunk, S_max, num_sms, stream, err);
-    case 2: return launch_split<2>(tk, tv, q, seqlens, ws_o, ws_lse, B, Hq, Hkv, Nk_max, scale, chunk, S_max, num_sms, stream, err);
-    case 4: return launch_split<4>(tk, tv, q, seqlens, ws_o, ws_lse, B, Hq, Hkv, Nk_max, scale, chunk, S_max, num_sms, stream, err);
-    case 8: return launch_split<8>(tk, tv, q, seqlens, ws_o, ws_lse, B, Hq, Hkv, Nk_max, scale, chunk, S_max, num_sms, stream, err);
-    default: return ATTN_ERR_GQA;
-  }
+  const Paging none{nullptr, 0, 0, 0};
+  return launch_split_any<false>(tk, tv, q, seqlens, workspace, B, Hq, Hkv, Nk_max, scale, chunk,
+                                 num_sms, stream, err, none);
+}
+
+int launch_decode_splitkv_paged(const void* q, const void* k_pages, const void* v_pages,
+                                const int* block_table, const int* seqlens, void* workspace, int B,
+                                int Hq, int Hkv, int num_pages, int page_size, int max_pages,
+                                float scale, int chunk, int num_sms, cudaStream_t stream, int* err) {
+  using namespace decode;
+  CUtensorMap tk, tv;
+  const uint32_t box[4] = {HD, 1, TILE, 1};
+  if (!encode_tiled_4d(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, k_pages, HD, Hkv, page_size, num_pages,
+                       2, box, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !encode_tiled_4d(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, v_pages, HD, Hkv, page_size, num_pages,
+                       2, box, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return ATTN_ERR_CUDA;
+  const Paging pg{block_table, max_pages, page_size, num_pages};
+  return launch_split_any<true>(tk, tv, q, seqlens, workspace, B, Hq, Hkv, max_pages * page_size,
+                                scale, chunk, num_sms, stream, err, pg);
 }
 
 int launch_decode_combine(const void* workspace, const int* seqlens, void* o, float* lse, int B,

@@ -43,6 +43,11 @@ int launch_decode_splitkv(const void* q, const void* k_cache, const void* v_cach
                           int Nk_max, float scale, int chunk, int num_sms, cudaStream_t stream,
                           int* err);
 
+int launch_decode_splitkv_paged(const void* q, const void* k_pages, const void* v_pages,
+                                const int* block_table, const int* seqlens, void* workspace, int B,
+                                int Hq, int Hkv, int num_pages, int page_size, int max_pages,
+                                float scale, int chunk, int num_sms, cudaStream_t stream, int* err);
+
 int launch_decode_combine(const void* workspace, const int* seqlens, void* o, float* lse, int B,
                           int Hq, int Nk_max, int chunk, cudaStream_t stream, int* err);
 

@@ -97,3 +97,38 @@ def decode_inputs(B: int, Hq: int, Hkv: int, D: int, nk_lo: int, nk_hi: int,
         k_cache[b, nk:] = K_SENTINEL
         v_cache[b, nk:] = V_SENTINEL
     return q, k_cache, v_cache, seqlens
+
+
+def paged_decode_inputs(B: int, Hq: int, Hkv: int, D: int, nk_lo: int, nk_hi: int,
+                        page_size: int, seed: int = 0, dtype: str = "bf16", device="cpu",
+                        spare_pages: int = 0):
+    """Paged decode workload: ``(q, k_pages, v_pages, block_table, seqlens)``.
+
+    Sequence lengths, Q and every sequence's K/V rows are the draws of
+    :func:`decode_inputs` (same seed, same device rule).  The pages a sequence
+    needs are placed at page ids given by a permutation drawn from a generator
+    seeded ``seed + 7`` (so sequences are scattered over the pool); the tail of
+    a last page holds the sentinels, ``spare_pages`` unused pages are added to
+    the pool, and unused block-table entries are 0.
+    """
+    seqlens, q = decode_seqlens_and_q(B, Hq, D, nk_lo, nk_hi, seed, dtype)
+    lens = [int(x) for x in seqlens]
+    max_pages = -(-nk_hi // page_size)
+    need = [-(-n // page_size) for n in lens]
+    num_pages = sum(need) + spare_pages
+    perm = torch.randperm(num_pages, generator=torch.Generator("cpu").manual_seed(seed + 7))
+    block_table = torch.zeros(B, max_pages, dtype=torch.int32)
+    tdt = _DTYPES[dtype]
+    k_pages = torch.full((num_pages, page_size, Hkv, D), K_SENTINEL, dtype=tdt, device=device)
+    v_pages = torch.full((num_pages, page_size, Hkv, D), V_SENTINEL, dtype=tdt, device=device)
+    nxt = 0
+    for b in range(B):
+        kb, vb = decode_kv_rows(seed, b, lens[b], Hkv, D, dtype, device)
+        for i in range(need[b]):
+            page = int(perm[nxt])
+            nxt += 1
+            block_table[b, i] = page
+            rows = min(page_size, lens[b] - i * page_size)
+            k_pages[page, :rows] = kb[i * page_size: i * page_size + rows]
+            v_pages[page, :rows] = vb[i * page_size: i * page_size + rows]
+    return q, k_pages, v_pages, block_table, seqlens

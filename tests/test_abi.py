@@ -116,6 +116,24 @@ def test_decode_argument_errors(L):
     assert comb(lse=MIS) == -5
 
 
+def test_paged_decode_argument_errors(L):
+    def paged(q=P, kp=P, vp=P, bt=P, sl=P, ws=P, B=4, Hq=32, Hkv=8, num_pages=100, page_size=256,
+              max_pages=8, D=128, scale=0.1, chunk=512):
+        return L.attn_decode_splitkv_paged(q, kp, vp, bt, sl, ws, B, Hq, Hkv, num_pages, page_size,
+                                           max_pages, D, scale, chunk, None)
+
+    assert paged(bt=None) == -1
+    assert paged(page_size=100) == -2          # not a multiple of 64
+    assert paged(page_size=0) == -2
+    assert paged(num_pages=0) == -2
+    assert paged(max_pages=-1) == -2
+    assert paged(Hq=32, Hkv=3) == -3
+    assert paged(D=64) == -4
+    assert paged(chunk=96) == -11
+    assert paged(bt=MIS) == -5
+    assert paged(scale=0.0) == -6
+
+
 def test_workspace_size(L):
     # O_part [B,Hq,S_max,D] + LSE_part [B,Hq,S_max], fp32, rounded up to 256 bytes
     n = L.attn_decode_workspace_size(64, 32, 128, 32768, 512)

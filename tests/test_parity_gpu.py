@@ -242,6 +242,52 @@ def test_decode_benchmark_workload_sampled(dev):
     assert binding.get_device_error() == 0
 
 
+@pytest.mark.parametrize("page_size,chunk,G", [(64, 512, 4), (256, 512, 4), (128, 64, 2), (512, 1024, 8)])
+def test_decode_paged_small(dev, page_size, chunk, G):
+    """Paged cache with sequences scattered over the pool (and spare pages)."""
+    B, Hkv = 7, 2
+    Hq = G * Hkv
+    q, kp, vp, bt, sl = inputs.paged_decode_inputs(B, Hq, Hkv, 128, 1, 3000, page_size, seed=page_size + G,
+                                                   spare_pages=5)
+    o, lse = binding.attn_decode_paged(q.to(dev), kp.to(dev), vp.to(dev), bt.to(dev), sl.to(dev), chunk=chunk)
+    O, L = oracle.decode_forward_paged(q, kp, vp, bt, sl, 1 / math.sqrt(128))
+    check(o, lse, O, L, BF16_O_TOL, BF16_LSE_REL, True)
+    assert binding.get_device_error() == 0
+
+
+def test_decode_paged_benchmark_workload_sampled(dev):
+    """B=64 Hq=32 Hkv=8, Nk_b ~ U[512, 32768], page 256, chunk 512: sampled sequences."""
+    q, kp, vp, bt, sl = inputs.paged_decode_inputs(64, 32, 8, 128, 512, 32768, 256, seed=0, device=dev)
+    o, lse = binding.attn_decode_paged(q.to(dev), kp, vp, bt.to(dev), sl.to(dev), chunk=512)
+    lens = sl.numpy()
+    batches = sorted({int(lens.argmax()), int(lens.argmin()), 3, 31, 50})
+    O = np.zeros((len(batches), 32, 128))
+    L = np.zeros((len(batches), 32))
+    for n, b in enumerate(batches):
+        pages = bt[b, : -(-int(lens[b]) // 256)].long()
+        kb, vb = kp[pages.to(dev)].cpu(), vp[pages.to(dev)].cpu()   # this sequence's pages, in order
+        Ob, Lb = oracle.decode_forward_paged(q[b:b + 1], kb, vb, [list(range(len(pages)))], [int(lens[b])],
+                                             1 / math.sqrt(128))
+        O[n], L[n] = Ob[0], Lb[0]
+    check(o.cpu()[batches], lse.cpu()[batches], O, L, BF16_O_TOL, BF16_LSE_REL, True)
+    assert binding.get_device_error() == 0
+
+
+def test_decode_nan_in_unused_cache_rows_does_not_leak(dev):
+    """Rows past a sequence's end may hold anything, NaN included."""
+    lens = [5, 700, 1]
+    B, Hq, Hkv, nk_max = 3, 8, 2, 1024
+    _, q = inputs.decode_seqlens_and_q(B, Hq, 128, 1, 2, 6)
+    kc = torch.full((B, nk_max, Hkv, 128), float("nan"), dtype=torch.bfloat16)
+    vc = torch.full((B, nk_max, Hkv, 128), float("nan"), dtype=torch.bfloat16)
+    for b, n in enumerate(lens):
+        kb, vb = inputs.decode_kv_rows(6, b, n, Hkv, 128)
+        kc[b, :n], vc[b, :n] = kb, vb
+    o, lse = binding.attn_decode(q.to(dev), kc.to(dev), vc.to(dev), torch.tensor(lens, dtype=torch.int32).to(dev))
+    O, L = oracle.decode_forward(q, kc, vc, lens, 1 / math.sqrt(128))
+    check(o, lse, O, L, BF16_O_TOL, BF16_LSE_REL, True)
+
+
 def test_decode_bad_seqlen_reported(dev):
     """A sequence length outside [1, Nk_max] is skipped and reported; others stay correct."""
     B, Hq, Hkv, nk_max = 3, 8, 2, 1024
