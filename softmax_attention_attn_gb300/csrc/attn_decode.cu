@@ -190,6 +190,7 @@ attn_decode_splitkv_kernel(const __grid_constant__ CUtensorMap tm_k,
     // ================================================================ producer
     if (lane == 0) {
       int it = 0;
+      int cached_lp = -1, cached_b = -1, cached_page = 0;
       bool ok = true;
       for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
         const Work wk = decode_work(w, split, B, Hkv, chunk, seqlens);
@@ -205,7 +206,12 @@ attn_decode_splitkv_kernel(const __grid_constant__ CUtensorMap tm_k,
             const int key0 = wk.c * chunk + tl * TILE;
             if constexpr (PAGED) {
               const int lp = key0 / pg.page_size;
-              int page = __ldg(pg.block_table + static_cast<size_t>(wk.b) * pg.max_pages + lp);
+              if (lp != cached_lp || wk.b != cached_b) {  // one block-table read per page
+                cached_page = __ldg(pg.block_table + static_cast<size_t>(wk.b) * pg.max_pages + lp);
+                cached_lp = lp;
+                cached_b = wk.b;
+              }
+              int page = cached_page;
               if (page < 0 || page >= pg.num_pages) {  // reported; the copy reads zeros instead
                 atomicCAS(err, 0, ATTN_ERR_PAGE);
                 page = pg.num_pages;
