@@ -83,7 +83,7 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--workload", choices=["dense", "causal", "decode", "fp32", "window", "chunked", "d64",
-                                           "paged"],
+                                           "paged", "fp16"],
                     default="dense",
                     help="workload of the timed loop (default: the dense bf16 prefill)")
     ap.add_argument("--no-extras", action="store_true", help="skip the other workloads")
@@ -264,6 +264,7 @@ WORKLOAD_NAMES = {
     "window": "bf16 causal sliding-window (4096) prefill B=1 Hq=32 Hkv=8 N=16384 D=128",
     "chunked": "bf16 chunked prefill (causal, bottom-right) B=1 Hq=32 Hkv=8 Nq=2048 Nk=16384 D=128",
     "d64": "bf16 dense prefill B=1 H=32 N=8192 D=64 (non-causal)",
+    "fp16": "fp16 dense prefill B=1 H=32 N=8192 D=128 (non-causal)",
     "paged": "bf16 split-KV decode on a paged cache (page 256) B=64 Hq=32 Hkv=8 D=128, Nk_b~U[512,32768], chunk 512",
 }
 
@@ -273,16 +274,16 @@ def make_workload(name, dev, seed, peaks, peak_src, sm_max_mhz, decode_batch=Non
     import torch
     from softmax_attention_attn_gb300 import binding, inputs
     w = {"name": name, "desc": WORKLOAD_NAMES[name]}
-    if name in ("dense", "causal", "fp32", "window", "chunked", "d64"):
+    if name in ("dense", "causal", "fp32", "window", "chunked", "d64", "fp16"):
         c = {"dense": MAIN, "causal": CAUSAL, "fp32": FP32, "window": WINDOW, "chunked": CHUNKED,
-             "d64": DENSE64}[name]
+             "d64": DENSE64, "fp16": MAIN}[name]
         Nq, Nk = c.get("Nq", c.get("N")), c.get("Nk", c.get("N"))
-        dt = "fp32" if name == "fp32" else "bf16"
+        dt = {"fp32": "fp32", "fp16": "fp16"}.get(name, "bf16")
         host = inputs.prefill_inputs(c["B"], c["Hq"], c["Hkv"], Nq, Nk, c["D"], dt, seed)
         q, k, v = (x.to(dev) for x in host)
         o = torch.empty_like(q)
         lse = torch.empty(c["B"], c["Hq"], Nq, device=dev, dtype=torch.float32)
-        call = binding.attn_fwd_fp32 if name == "fp32" else binding.attn_fwd
+        call = {"fp32": binding.attn_fwd_fp32, "fp16": binding.attn_fwd_fp16}.get(name, binding.attn_fwd)
         wnd = c.get("window", 0)
         w["fn"] = lambda: call(q, k, v, o, lse, causal=c["causal"], window=wnd)
         w["work"] = masked_flops(c["B"], c["Hq"], Nq, Nk, c["D"], c["causal"], wnd) if "Nq" in c else flops(**c)
@@ -297,7 +298,7 @@ def make_workload(name, dev, seed, peaks, peak_src, sm_max_mhz, decode_batch=Non
         else:
             w["bound"] = "tensor"
             w["peak"] = peaks["bf16_tflops"]
-            w["peak_source"] = f"{peak_src} dense bf16 (burst)"
+            w["peak_source"] = f"{peak_src} dense bf16 (burst)" + (" = fp16 dense rate" if name == "fp16" else "")
         w["e2e_in"] = [(x, t) for x, t in zip(host, (q, k, v))]
         w["e2e_out"] = [o, lse]
     else:
@@ -455,7 +456,7 @@ def run_gb300(args, rank, world, local_rank):
     workloads = {}
     if not args.no_extras:
         xs = max(5, min(args.steps // 10, 50))
-        for name in ("dense", "causal", "decode", "paged", "fp32", "window", "chunked", "d64"):
+        for name in ("dense", "causal", "decode", "paged", "fp32", "window", "chunked", "d64", "fp16"):
             if name == args.workload:
                 continue
             x = make_workload(name, dev, rank, peaks, peak_src, sm_max, args.decode_batch)

@@ -84,6 +84,16 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
              float scale, int causal, int window, attn_stream_t stream);
 
 /*
+ * attn_fwd_fp16 — fp16 variant of attn_fwd (same kernel, fp16 tensor-core
+ * operands).  [ASK] "研究动机" (bf16 / fp16 / fp8 precisions on the feature
+ * surface).  Same shapes, masks, D and error codes as attn_fwd with fp16 q, k,
+ * v and o; P is rounded to fp16 before the P V product; O is rounded to fp16.
+ */
+int attn_fwd_fp16(const void* q, const void* k, const void* v, void* o, float* lse,
+                  int B, int Hq, int Hkv, int Nq, int Nk, int D,
+                  float scale, int causal, int window, attn_stream_t stream);
+
+/*
  * attn_fwd_fp32 — fp32 fused attention forward on the FP32 SIMT pipes.
  *   [DEVLOG] 三 (fp32 [B,H,N,D] operator), 四 (tiled online softmax),
  *   五 (16-byte vector loads, padded shared-memory rows).

@@ -25,6 +25,7 @@ _c_int, _c_float, _vp = ctypes.c_int, ctypes.c_float, ctypes.c_void_p
 SIGNATURES = {
     "attn_fwd": (_c_int, [_vp, _vp, _vp, _vp, _vp] + [_c_int] * 6 + [_c_float, _c_int, _c_int, _vp]),
     "attn_fwd_fp32": (_c_int, [_vp, _vp, _vp, _vp, _vp] + [_c_int] * 6 + [_c_float, _c_int, _c_int, _vp]),
+    "attn_fwd_fp16": (_c_int, [_vp, _vp, _vp, _vp, _vp] + [_c_int] * 6 + [_c_float, _c_int, _c_int, _vp]),
     "attn_decode_workspace_size": (ctypes.c_size_t, [_c_int] * 5),
     "attn_decode_splitkv": (_c_int, [_vp] * 5 + [_c_int] * 5 + [_c_float, _c_int, _vp]),
     "attn_decode_combine": (_c_int, [_vp] * 4 + [_c_int] * 5 + [_vp]),
@@ -110,6 +111,12 @@ def attn_fwd(q, k, v, o=None, lse=None, scale=None, causal=False, window=0, stre
     """bf16 forward: q ``[B,Hq,Nq,D]``, k/v ``[B,Hkv,Nk,D]`` -> (o, lse)."""
     import torch
     return _fwd("attn_fwd", torch.bfloat16, q, k, v, o, lse, scale, causal, window, stream)
+
+
+def attn_fwd_fp16(q, k, v, o=None, lse=None, scale=None, causal=False, window=0, stream=None):
+    """fp16 forward: same layouts as :func:`attn_fwd`."""
+    import torch
+    return _fwd("attn_fwd_fp16", torch.float16, q, k, v, o, lse, scale, causal, window, stream)
 
 
 def attn_fwd_fp32(q, k, v, o=None, lse=None, scale=None, causal=False, window=0, stream=None):

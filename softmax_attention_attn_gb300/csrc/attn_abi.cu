@@ -122,16 +122,28 @@ using namespace attn;
 
 extern "C" {
 
-int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
-             int Hkv, int Nq, int Nk, int D, float scale, int causal, int window,
-             attn_stream_t stream) {
+static int fwd_tc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                  int Hkv, int Nq, int Nk, int D, int f16, float scale, int causal, int window,
+                  attn_stream_t stream) {
   int rc = check_common(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, scale);
   if (rc != ATTN_OK) return rc;
   if (D != 64 && D != 128) return ATTN_ERR_HEAD_DIM;
   DeviceInfo* dev = nullptr;
   if ((rc = device_info(&dev)) != ATTN_OK) return rc;
-  return launch_fwd_bf16(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, scale, causal, window, dev->num_sms,
-                         reinterpret_cast<cudaStream_t>(stream), dev->err);
+  return launch_fwd_tc(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, f16, scale, causal, window,
+                       dev->num_sms, reinterpret_cast<cudaStream_t>(stream), dev->err);
+}
+
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+             int Hkv, int Nq, int Nk, int D, float scale, int causal, int window,
+             attn_stream_t stream) {
+  return fwd_tc(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, 0, scale, causal, window, stream);
+}
+
+int attn_fwd_fp16(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                  int Hkv, int Nq, int Nk, int D, float scale, int causal, int window,
+                  attn_stream_t stream) {
+  return fwd_tc(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, 1, scale, causal, window, stream);
 }
 
 int attn_fwd_fp32(const float* q, const float* k, const float* v, float* o, float* lse, int B,

@@ -1,4 +1,4 @@
-// attn_fwd_bf16.cu — bf16 fused attention forward for sm_103a on tcgen05.
+// attn_fwd_bf16.cu — bf16 / fp16 fused attention forward for sm_103a on tcgen05.
 //
 // What it computes (softmax attention, "Agent 帮我写 CUDA：一个 Softmax Attention
 // 算子的开发全记录" section 二 "参考基线"; online softmax over K/V tiles, same page
@@ -55,8 +55,9 @@ constexpr int NTHREADS = (NUM_SOFTMAX_WARPS + 1 + NQT) * 32;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float RESCALE_LOG2 = 8.0f;         // keep a stale max while the growth is <= 2^8
 
-// Shape constants for head dimension HD (64 or 128).
-template <int HD>
+// Shape constants for head dimension HD (64 or 128); F16 selects fp16 instead
+// of bf16 operands.
+template <int HD, bool F16 = false>
 struct Cfg {
   static constexpr int KBLKS = HD / 64;                 // 128-byte slabs per tile row
   static constexpr int TILE_BYTES = KBLKS * KBLK_BYTES; // one 128-row Q, K or V tile
@@ -67,8 +68,9 @@ struct Cfg {
   static constexpr int NUM_BARS = 3 + 2 * STAGES + 6 * NQT;
   static constexpr int SMEM_MISC = SMEM_BAR + NUM_BARS * 8;
   static constexpr int SMEM_ALLOC = SMEM_MISC + 16 + 1024;  // + slack for 1024-byte alignment
-  static constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, BN, 0);
-  static constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, HD, 1);
+  static constexpr uint32_t AB_FORMAT = F16 ? 0u : 1u;  // instruction-descriptor A/B format
+  static constexpr uint32_t IDESC_QK = idesc_f16kind_f32(128, BN, 0, AB_FORMAT);
+  static constexpr uint32_t IDESC_PV = idesc_f16kind_f32(128, HD, 1, AB_FORMAT);
   static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
   static_assert(2 * BN + 2 * HD <= TMEM_COLS, "tensor memory budget");
 };
@@ -77,15 +79,22 @@ __device__ __forceinline__ uint32_t s_col(int t) { return static_cast<uint32_t>(
 template <int HD>
 __device__ __forceinline__ uint32_t o_col(int t) { return static_cast<uint32_t>(NQT * BN + t * HD); }
 
+// Two floats -> one 32-bit pair of the operand type (bf16 or fp16), RNE.
+template <bool F16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if constexpr (F16) return pack_f16x2(lo, hi);
+  else return pack_bf16x2(lo, hi);
+}
+
 // S (tmem) = Q_tile (smem) x K_tile^T (smem); both K-major, 128-byte swizzle.
-template <int HD>
+template <int HD, bool F16>
 __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
 #pragma unroll
   for (int kk = 0; kk < HD / 16; ++kk) {
     const uint32_t koff = static_cast<uint32_t>((kk >> 2) * KBLK_BYTES + (kk & 3) * 32);
     const uint64_t a = smem_desc_sw128(q_smem + koff, 16, 1024);
     const uint64_t b = smem_desc_sw128(k_smem + koff, 16, 1024);
-    mma_bf16_ss(d_tmem, a, b, Cfg<HD>::IDESC_QK, kk > 0 ? 1u : 0u);
+    mma_bf16_ss(d_tmem, a, b, Cfg<HD, F16>::IDESC_QK, kk > 0 ? 1u : 0u);
   }
 }
 
@@ -93,14 +102,14 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint3
 // 16-key steps kk in [kk0, kk0 + 4): one half of the tile's keys.  With HD =
 // 128 the two 64-column slabs of V are KBLK_BYTES apart (the leading byte
 // offset of the MN-major operand); with HD = 64 there is one slab.
-template <int HD>
+template <int HD, bool F16>
 __device__ __forceinline__ void issue_pv_half(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem,
                                               bool accumulate, int kk0) {
 #pragma unroll
   for (int kk = kk0; kk < kk0 + BN / 32; ++kk) {
     const uint64_t b = smem_desc_sw128(v_smem + static_cast<uint32_t>(kk * 16 * 128),
                                        KBLK_BYTES, 1024);
-    mma_bf16_ts(d_tmem, p_tmem + static_cast<uint32_t>(kk * 8), b, Cfg<HD>::IDESC_PV,
+    mma_bf16_ts(d_tmem, p_tmem + static_cast<uint32_t>(kk * 8), b, Cfg<HD, F16>::IDESC_PV,
                 (accumulate || kk > 0) ? 1u : 0u);
   }
 }
@@ -172,12 +181,12 @@ __device__ __forceinline__ void own_range(const Unit& u, int t, int& jb, int& je
   je = t == 0 ? u.je0 : u.je1;
 }
 
-template <int HD>
+template <int HD, bool F16>
 __global__ void __launch_bounds__(NTHREADS, 1)
 attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
-  using C = Cfg<HD>;
+  using C = Cfg<HD, F16>;
   constexpr int KBLKS = C::KBLKS;
   constexpr int TILE_BYTES = C::TILE_BYTES;
   constexpr int STAGES = C::STAGES;
@@ -319,7 +328,7 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
         if (jb < je) {  // first S of this unit (outside the turn order)
           if (!mbar_wait(bar_kv_full(slot_of(kpos(jb))), phase_of(kpos(jb)), abort_flag, p.err)) { ok = false; break; }
           tc_fence_after();
-          issue_qk<HD>(tmem + s_col(t), q_sm, sb + SMEM_RING + slot_of(kpos(jb)) * TILE_BYTES);
+          issue_qk<HD, F16>(tmem + s_col(t), q_sm, sb + SMEM_RING + slot_of(kpos(jb)) * TILE_BYTES);
           mma_commit(bar_s_full(t));
           mma_commit(bar_kv_empty(slot_of(kpos(jb))));
           if (je - jb == 1) mma_commit(bar_q_empty);  // that was this unit's last S
@@ -345,10 +354,10 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
           }
           if (own) {
             tc_fence_after();
-            issue_pv_half<HD>(tmem + o_col<HD>(t), tmem + s_col(t), vsm, j > jb, 0);
+            issue_pv_half<HD, F16>(tmem + o_col<HD>(t), tmem + s_col(t), vsm, j > jb, 0);
             if (!mbar_wait(bar_p_hi(t), lt & 1, abort_flag, p.err)) { ok = false; break; }
             tc_fence_after();
-            issue_pv_half<HD>(tmem + o_col<HD>(t), tmem + s_col(t), vsm, true, BN / 32);
+            issue_pv_half<HD, F16>(tmem + o_col<HD>(t), tmem + s_col(t), vsm, true, BN / 32);
             mma_commit(bar_kv_empty(slot_of(vpos)));
             if (j + 1 == je) {
               mma_commit(bar_o_full(t));
@@ -356,7 +365,7 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
               const int npos = kpos(j + 1);
               if (!mbar_wait(bar_kv_full(slot_of(npos)), phase_of(npos), abort_flag, p.err)) { ok = false; break; }
               tc_fence_after();
-              issue_qk<HD>(tmem + s_col(t), q_sm, sb + SMEM_RING + slot_of(npos) * TILE_BYTES);
+              issue_qk<HD, F16>(tmem + s_col(t), q_sm, sb + SMEM_RING + slot_of(npos) * TILE_BYTES);
               mma_commit(bar_s_full(t));
               mma_commit(bar_kv_empty(slot_of(npos)));
               if (j + 2 == je) mma_commit(bar_q_empty);  // this unit's last S
@@ -473,7 +482,7 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
               const float p0 = ex2_approx(x0);
               const float p1 = ex2_approx(x1);
               sum2[i & 1] = f2_add(sum2[i & 1], f2_pack(p0, p1));
-              pk[i] = pack_bf16x2(p0, p1);
+              pk[i] = pack2<F16>(p0, p1);
             }
             tmem_st16(s_addr + 32 * half + 16 * qtr, pk);
           }
@@ -524,15 +533,16 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
       }
       if (row < p.Nq) {
         const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
-        __nv_bfloat16* orow = p.o + ((static_cast<size_t>(u.b) * p.Hq + u.h) * p.Nq + row) * HD;
+        uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) +
+                                               ((static_cast<size_t>(u.b) * p.Hq + u.h) * p.Nq + row) * HD);
 #pragma unroll
         for (int i = 0; i < HD / 8; ++i) {
           const uint4 v4 = make_uint4(
-              pack_bf16x2(__uint_as_float(o[8 * i + 0]) * inv_l, __uint_as_float(o[8 * i + 1]) * inv_l),
-              pack_bf16x2(__uint_as_float(o[8 * i + 2]) * inv_l, __uint_as_float(o[8 * i + 3]) * inv_l),
-              pack_bf16x2(__uint_as_float(o[8 * i + 4]) * inv_l, __uint_as_float(o[8 * i + 5]) * inv_l),
-              pack_bf16x2(__uint_as_float(o[8 * i + 6]) * inv_l, __uint_as_float(o[8 * i + 7]) * inv_l));
-          reinterpret_cast<uint4*>(orow)[i] = v4;
+              pack2<F16>(__uint_as_float(o[8 * i + 0]) * inv_l, __uint_as_float(o[8 * i + 1]) * inv_l),
+              pack2<F16>(__uint_as_float(o[8 * i + 2]) * inv_l, __uint_as_float(o[8 * i + 3]) * inv_l),
+              pack2<F16>(__uint_as_float(o[8 * i + 4]) * inv_l, __uint_as_float(o[8 * i + 5]) * inv_l),
+              pack2<F16>(__uint_as_float(o[8 * i + 6]) * inv_l, __uint_as_float(o[8 * i + 7]) * inv_l));
+          orow[i] = v4;
         }
         if (p.lse != nullptr) {
           const float lse = (l > 0.f) ? (m + log2f(l)) * 0.69314718055994531f : -CUDART_INF_F;
@@ -555,31 +565,32 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
 // --------------------------------------------------------------------- host
 namespace fwd_bf16 {
 
-template <int HD>
+template <int HD, bool F16>
 int launch_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
                 int Hkv, int Nq, int Nk, float scale, int causal, int window, int num_sms,
                 cudaStream_t stream, int* err) {
-  using C = Cfg<HD>;
+  using C = Cfg<HD, F16>;
+  const CUtensorMapDataType dt = F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   CUtensorMap tq, tk, tv;
   const uint32_t box[3] = {64, 128, 1};
-  if (!encode_tiled_3d(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, q, HD, Nq, static_cast<uint64_t>(B) * Hq,
+  if (!encode_tiled_3d(&tq, dt, q, HD, Nq, static_cast<uint64_t>(B) * Hq,
                        2, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_tiled_3d(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, k, HD, Nk, static_cast<uint64_t>(B) * Hkv,
+      !encode_tiled_3d(&tk, dt, k, HD, Nk, static_cast<uint64_t>(B) * Hkv,
                        2, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_tiled_3d(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, v, HD, Nk, static_cast<uint64_t>(B) * Hkv,
+      !encode_tiled_3d(&tv, dt, v, HD, Nk, static_cast<uint64_t>(B) * Hkv,
                        2, box, CU_TENSOR_MAP_SWIZZLE_128B))
     return ATTN_ERR_CUDA;
   static int attr_set_dev = -1;
   int dev = 0;
   cudaGetDevice(&dev);
   if (attr_set_dev != dev) {
-    if (cudaFuncSetAttribute(attn_fwd_bf16_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(attn_fwd_bf16_kernel<HD, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::SMEM_ALLOC) != cudaSuccess)
       return ATTN_ERR_CUDA;
     attr_set_dev = dev;
   }
   FwdParams prm;
-  prm.o = static_cast<__nv_bfloat16*>(o);
+  prm.o = o;
   prm.lse = lse;
   prm.B = B;
   prm.Hq = Hq;
@@ -596,25 +607,25 @@ int launch_impl(const void* q, const void* k, const void* v, void* o, float* lse
   const long long units = n_qblk * Hq * B;
   if (units > 0x7fffffffLL) return ATTN_ERR_DIM;
   const int grid = static_cast<int>(units < num_sms ? units : num_sms);
-  attn_fwd_bf16_kernel<HD><<<grid, NTHREADS, C::SMEM_ALLOC, stream>>>(tq, tk, tv, prm);
+  attn_fwd_bf16_kernel<HD, F16><<<grid, NTHREADS, C::SMEM_ALLOC, stream>>>(tq, tk, tv, prm);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 }  // namespace fwd_bf16
 
-int launch_fwd_bf16(const void* q, const void* k, const void* v, void* o, float* lse, int B,
-                    int Hq, int Hkv, int Nq, int Nk, int D, float scale, int causal, int window,
-                    int num_sms, cudaStream_t stream, int* err) {
-  switch (D) {
-    case 64:
-      return fwd_bf16::launch_impl<64>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, window,
-                                       num_sms, stream, err);
-    case 128:
-      return fwd_bf16::launch_impl<128>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, window,
-                                        num_sms, stream, err);
-    default:
-      return ATTN_ERR_HEAD_DIM;
-  }
+int launch_fwd_tc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                  int Hkv, int Nq, int Nk, int D, int f16, float scale, int causal, int window,
+                  int num_sms, cudaStream_t stream, int* err) {
+  using fwd_bf16::launch_impl;
+  if (D == 64 && !f16)
+    return launch_impl<64, false>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, window, num_sms, stream, err);
+  if (D == 128 && !f16)
+    return launch_impl<128, false>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, window, num_sms, stream, err);
+  if (D == 64 && f16)
+    return launch_impl<64, true>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, window, num_sms, stream, err);
+  if (D == 128 && f16)
+    return launch_impl<128, true>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, window, num_sms, stream, err);
+  return ATTN_ERR_HEAD_DIM;
 }
 
 }  // namespace attn

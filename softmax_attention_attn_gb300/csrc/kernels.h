@@ -12,7 +12,7 @@
 namespace attn {
 
 struct FwdParams {
-  __nv_bfloat16* o;
+  void* o;           // bf16 or fp16 output
   float* lse;
   int B, Hq, Hkv, Nq, Nk;
   int group;         // Hq / Hkv
@@ -30,9 +30,10 @@ bool encode_tiled_4d(CUtensorMap* map, CUtensorMapDataType dt, const void* base,
                      uint64_t d1, uint64_t d2, uint64_t d3, uint32_t esize, const uint32_t box[4],
                      CUtensorMapSwizzle swz);
 
-int launch_fwd_bf16(const void* q, const void* k, const void* v, void* o, float* lse, int B,
-                    int Hq, int Hkv, int Nq, int Nk, int D, float scale, int causal, int window,
-                    int num_sms, cudaStream_t stream, int* err);
+// Tensor-core forward; f16 != 0 selects fp16 operands and output instead of bf16.
+int launch_fwd_tc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                  int Hkv, int Nq, int Nk, int D, int f16, float scale, int causal, int window,
+                  int num_sms, cudaStream_t stream, int* err);
 
 int launch_fwd_fp32(const float* q, const float* k, const float* v, float* o, float* lse, int B,
                     int Hq, int Hkv, int Nq, int Nk, int D, float scale, int causal, int window,

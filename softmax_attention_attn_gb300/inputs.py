@@ -9,7 +9,7 @@ Recipe (every draw uses ``torch.Generator("cpu")``):
 
 * prefill workloads: one generator seeded with ``seed`` draws fp32 N(0, 1)
   tensors in the order Q ``[B,Hq,Nq,D]``, K ``[B,Hkv,Nk,D]``, V ``[B,Hkv,Nk,D]``;
-  bf16 workloads cast those fp32 values with round-to-nearest-even.
+  bf16 / fp16 workloads cast those fp32 values with round-to-nearest-even.
 * decode workloads: a generator seeded with ``seed`` draws the per-sequence
   key counts ``Nk_b ~ U{nk_lo..nk_hi}`` first and then Q ``[B,Hq,D]``.  Sequence
   ``b`` then draws its own K and V rows ``[Nk_b,Hkv,D]`` (K first) from a
@@ -29,7 +29,7 @@ import torch
 K_SENTINEL = 64.0
 V_SENTINEL = 1.0e4
 
-_DTYPES = {"fp32": torch.float32, "bf16": torch.bfloat16}
+_DTYPES = {"fp32": torch.float32, "bf16": torch.bfloat16, "fp16": torch.float16}
 
 
 def _cast(t: torch.Tensor, dtype: str) -> torch.Tensor:

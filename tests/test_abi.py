@@ -29,7 +29,7 @@ def declared_functions():
 
 def test_header_declares_entry_points():
     names = declared_functions()
-    for must in ("attn_fwd", "attn_fwd_fp32", "attn_decode_splitkv", "attn_decode_combine",
+    for must in ("attn_fwd", "attn_fwd_fp16", "attn_fwd_fp32", "attn_decode_splitkv", "attn_decode_combine",
                  "attn_decode_workspace_size", "attn_get_device_error", "attn_strerror"):
         assert must in names
 
@@ -70,7 +70,7 @@ def fwd(L, name="attn_fwd", q=P, k=P, v=P, o=P, lse=P, B=1, Hq=4, Hkv=2, Nq=8, N
     return getattr(L, name)(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, scale, causal, window, None)
 
 
-@pytest.mark.parametrize("name", ["attn_fwd", "attn_fwd_fp32"])
+@pytest.mark.parametrize("name", ["attn_fwd", "attn_fwd_fp16", "attn_fwd_fp32"])
 def test_forward_argument_errors(L, name):
     assert fwd(L, name, q=None) == -1
     assert fwd(L, name, o=None) == -1
@@ -88,6 +88,7 @@ def test_forward_argument_errors(L, name):
 
 def test_head_dim_per_entry_point(L):
     assert fwd(L, "attn_fwd", D=32) == -4
+    assert fwd(L, "attn_fwd_fp16", D=256) == -4
     assert fwd(L, "attn_fwd_fp32", D=256) == -4
 
 

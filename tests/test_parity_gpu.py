@@ -154,6 +154,33 @@ def test_bf16_head_dim_64(dev, case):
     check(o, lse, O, L, BF16_O_TOL, BF16_LSE_REL, True)
 
 
+FP16_CASES = [  # (B, Hq, Hkv, Nq, Nk, D, causal, window)
+    (1, 2, 2, 300, 300, 128, False, 0),
+    (2, 4, 2, 513, 513, 128, True, 0),
+    (1, 2, 1, 256, 1000, 128, True, 0),
+    (1, 2, 2, 1000, 1000, 64, True, 100),
+    (1, 4, 4, 1024, 1024, 64, False, 0),
+]
+
+
+@pytest.mark.parametrize("case", FP16_CASES, ids=str)
+def test_fp16_forward(dev, case):
+    B, Hq, Hkv, Nq, Nk, D, causal, window = case
+    q, k, v = inputs.prefill_inputs(B, Hq, Hkv, Nq, Nk, D, "fp16", seed=17)
+    o, lse = binding.attn_fwd_fp16(q.to(dev), k.to(dev), v.to(dev), causal=causal, window=window)
+    O, L = oracle.attention_forward(q, k, v, 1 / math.sqrt(D), causal, window)
+    check(o, lse, O, L, BF16_O_TOL, BF16_LSE_REL, True)
+
+
+def test_fp16_dense_workload_sampled(dev):
+    q, k, v = inputs.prefill_inputs(1, 32, 32, 8192, 8192, 128, "fp16", seed=0)
+    o, lse = binding.attn_fwd_fp16(q.to(dev), k.to(dev), v.to(dev))
+    rows = sample_rows(1, 32, 8192, 64, seed=4)
+    O, L = oracle.attention_rows(q, k, v, 1 / math.sqrt(128), rows)
+    idx = tuple(np.array(rows).T)
+    check(o.cpu()[idx], lse.cpu()[idx], O, L, BF16_O_TOL, BF16_LSE_REL, True)
+
+
 @pytest.mark.parametrize("name,B,Hq,Hkv,Nq,Nk,D,causal,window", [
     ("sliding_window_4096_B1_H32_KV8_N16384", 1, 32, 8, 16384, 16384, 128, True, 4096),
     ("chunked_prefill_B1_H32_KV8_Nq2048_Nk16384", 1, 32, 8, 2048, 16384, 128, True, 0),
