@@ -94,6 +94,26 @@ int attn_fwd_fp16(const void* q, const void* k, const void* v, void* o, float* l
                   float scale, int causal, int window, attn_stream_t stream);
 
 /*
+ * attn_fwd_varlen — bf16 forward on a ragged batch (packed, token-major).
+ *   [ASK] "研究动机" (ragged batches on the feature surface).
+ *
+ *   q, o : bf16 [total_q, Hq, D]      k, v : bf16 [total_k, Hkv, D]
+ *   lse  : fp32 [Hq, total_q] (may be NULL)
+ *   cu_seqlens_q, cu_seqlens_k : int32 [B + 1] (device), non-decreasing, starting
+ *   at 0: sequence b owns query rows cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 and
+ *   key rows cu_seqlens_k[b] .. cu_seqlens_k[b+1]-1.  Masks and GQA act within a
+ *   sequence (causal is bottom-right aligned per sequence).  max_seqlen_q must
+ *   be >= every query length; an empty sequence is allowed.  A slice outside
+ *   [0, total) or longer than max_seqlen_q is skipped and reported as
+ *   ATTN_ERR_SEQLEN in the device error word.  D must be 64 or 128.
+ *   Errors: as attn_fwd.
+ */
+int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                    const int* cu_seqlens_q, const int* cu_seqlens_k,
+                    int B, int Hq, int Hkv, int max_seqlen_q, int total_q, int total_k, int D,
+                    float scale, int causal, int window, attn_stream_t stream);
+
+/*
  * attn_fwd_fp32 — fp32 fused attention forward on the FP32 SIMT pipes.
  *   [DEVLOG] 三 (fp32 [B,H,N,D] operator), 四 (tiled online softmax),
  *   五 (16-byte vector loads, padded shared-memory rows).

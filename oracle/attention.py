@@ -48,7 +48,7 @@ import numpy as np
 __all__ = [
     "visible_mask", "kv_head", "attention_forward", "attention_rows",
     "attention_probabilities", "decode_forward", "decode_split_partials",
-    "decode_combine", "paged_rows", "decode_forward_paged",
+    "decode_combine", "paged_rows", "decode_forward_paged", "attention_varlen",
 ]
 
 
@@ -162,6 +162,32 @@ def attention_probabilities(q, k, scale: float, causal: bool = False, window: in
             S[~visible_mask(np.arange(Nq), Nq, Nk, causal, window)] = -np.inf
             P[b, h] = _softmax_rows(S)[0]
     return P
+
+
+def attention_varlen(q, k, v, cu_q, cu_k, scale: float, causal: bool = False, window: int = 0):
+    """Ragged batch in packed token-major layout.
+
+    ``q``: ``[total_q, Hq, D]``, ``k``/``v``: ``[total_k, Hkv, D]``; sequence b owns
+    query rows ``cu_q[b]:cu_q[b+1]`` and key rows ``cu_k[b]:cu_k[b+1]``.  Each
+    sequence is an independent :func:`attention_forward` (masks per sequence).
+    Returns ``O [total_q, Hq, D]`` and ``LSE [Hq, total_q]``.
+    """
+    Q, K, V = _f64(q), _f64(k), _f64(v)
+    cq, ck = [int(x) for x in cu_q], [int(x) for x in cu_k]
+    O = np.zeros((Q.shape[0], Q.shape[1], V.shape[2]))
+    LSE = np.zeros((Q.shape[1], Q.shape[0]))
+    for b in range(len(cq) - 1):
+        q0, q1, k0, k1 = cq[b], cq[b + 1], ck[b], ck[b + 1]
+        if q1 == q0:
+            continue
+        if k1 == k0:   # no keys: every row sees nothing
+            LSE[:, q0:q1] = -np.inf
+            continue
+        Ob, Lb = attention_forward(Q[q0:q1].transpose(1, 0, 2)[None], K[k0:k1].transpose(1, 0, 2)[None],
+                                   V[k0:k1].transpose(1, 0, 2)[None], scale, causal, window)
+        O[q0:q1] = Ob[0].transpose(1, 0, 2)
+        LSE[:, q0:q1] = Lb[0]
+    return O, LSE
 
 
 # ---------------------------------------------------------------------------

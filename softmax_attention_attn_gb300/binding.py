@@ -26,6 +26,7 @@ SIGNATURES = {
     "attn_fwd": (_c_int, [_vp, _vp, _vp, _vp, _vp] + [_c_int] * 6 + [_c_float, _c_int, _c_int, _vp]),
     "attn_fwd_fp32": (_c_int, [_vp, _vp, _vp, _vp, _vp] + [_c_int] * 6 + [_c_float, _c_int, _c_int, _vp]),
     "attn_fwd_fp16": (_c_int, [_vp, _vp, _vp, _vp, _vp] + [_c_int] * 6 + [_c_float, _c_int, _c_int, _vp]),
+    "attn_fwd_varlen": (_c_int, [_vp] * 7 + [_c_int] * 7 + [_c_float, _c_int, _c_int, _vp]),
     "attn_decode_workspace_size": (ctypes.c_size_t, [_c_int] * 5),
     "attn_decode_splitkv": (_c_int, [_vp] * 5 + [_c_int] * 5 + [_c_float, _c_int, _vp]),
     "attn_decode_combine": (_c_int, [_vp] * 4 + [_c_int] * 5 + [_vp]),
@@ -117,6 +118,29 @@ def attn_fwd_fp16(q, k, v, o=None, lse=None, scale=None, causal=False, window=0,
     """fp16 forward: same layouts as :func:`attn_fwd`."""
     import torch
     return _fwd("attn_fwd_fp16", torch.float16, q, k, v, o, lse, scale, causal, window, stream)
+
+
+def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, o=None, lse=None, scale=None,
+                    causal=False, window=0, stream=None):
+    """Ragged bf16 forward: q ``[total_q,Hq,D]``, k/v ``[total_k,Hkv,D]`` -> (o, lse ``[Hq,total_q]``)."""
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _require(t, torch.bfloat16, n)
+    _require(cu_seqlens_q, torch.int32, "cu_seqlens_q")
+    _require(cu_seqlens_k, torch.int32, "cu_seqlens_k")
+    total_q, Hq, D = q.shape
+    total_k, Hkv, _ = k.shape
+    B = cu_seqlens_q.numel() - 1
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(Hq, total_q, device=q.device, dtype=torch.float32)
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    code = lib().attn_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(cu_seqlens_q),
+                                 _ptr(cu_seqlens_k), B, Hq, Hkv, int(max_seqlen_q), total_q, total_k, D,
+                                 scale, int(bool(causal)), int(window), _stream(stream))
+    _check(code, "attn_fwd_varlen")
+    return o, lse
 
 
 def attn_fwd_fp32(q, k, v, o=None, lse=None, scale=None, causal=False, window=0, stream=None):

@@ -146,6 +146,23 @@ int attn_fwd_fp16(const void* q, const void* k, const void* v, void* o, float* l
   return fwd_tc(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, 1, scale, causal, window, stream);
 }
 
+int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                    const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int Hq, int Hkv,
+                    int max_seqlen_q, int total_q, int total_k, int D, float scale, int causal,
+                    int window, attn_stream_t stream) {
+  if (!cu_seqlens_q || !cu_seqlens_k) return ATTN_ERR_NULL;
+  int rc = check_common(q, k, v, o, lse, B, Hq, Hkv, max_seqlen_q, total_k, D, scale);
+  if (rc != ATTN_OK) return rc;
+  if (total_q <= 0) return ATTN_ERR_DIM;
+  if (!aligned16(cu_seqlens_q) || !aligned16(cu_seqlens_k)) return ATTN_ERR_ALIGN;
+  if (D != 64 && D != 128) return ATTN_ERR_HEAD_DIM;
+  DeviceInfo* dev = nullptr;
+  if ((rc = device_info(&dev)) != ATTN_OK) return rc;
+  return launch_fwd_tc(q, k, v, o, lse, B, Hq, Hkv, max_seqlen_q, 0, D, 0, scale, causal, window,
+                       dev->num_sms, reinterpret_cast<cudaStream_t>(stream), dev->err,
+                       cu_seqlens_q, cu_seqlens_k, total_q, total_k);
+}
+
 int attn_fwd_fp32(const float* q, const float* k, const float* v, float* o, float* lse, int B,
                   int Hq, int Hkv, int Nq, int Nk, int D, float scale, int causal, int window,
                   attn_stream_t stream) {

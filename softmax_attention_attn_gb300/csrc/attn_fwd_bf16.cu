@@ -125,6 +125,8 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 // A work unit: 256 query rows (two Q tiles) of one (batch, head).
 struct Unit {
   int q0, b, h, kvh;
+  int Nq, Nk;              // this sequence's query / key counts
+  int q_tok, k_tok;        // ragged batches: first token row of the sequence
   int jb0, je0, jb1, je1;  // key-tile range [jb, je) of Q tile 0 / 1 (empty: jb == je)
   int j_begin, j_end;      // the union, streamed through the K/V ring
 };
@@ -144,15 +146,34 @@ __device__ __forceinline__ Unit make_unit(int w, const FwdParams& p, int n_qblk)
   u.h = bh % p.Hq;
   u.kvh = u.h / p.group;
   u.q0 = qblk * (BM * NQT);
-  const int off = p.Nk - p.Nq;  // bottom-right diagonal offset
+  if (p.varlen) {
+    const int qs = __ldg(p.cu_q + u.b), qe = __ldg(p.cu_q + u.b + 1);
+    const int ks = __ldg(p.cu_k + u.b), ke = __ldg(p.cu_k + u.b + 1);
+    u.q_tok = qs;
+    u.k_tok = ks;
+    u.Nq = qe - qs;
+    u.Nk = ke - ks;
+    // a slice outside the tensors, or longer than the unit list covers, is
+    // dropped (nothing read or written for it) and reported
+    if (qs < 0 || qe < qs || qe > p.total_q || ks < 0 || ke < ks || ke > p.total_k || u.Nq > p.Nq) {
+      if (qblk == 0 && u.h == 0) atomicCAS(p.err, 0, ATTN_ERR_SEQLEN);
+      u.Nq = 0;
+      u.Nk = 0;
+    }
+  } else {
+    u.q_tok = u.k_tok = 0;
+    u.Nq = p.Nq;
+    u.Nk = p.Nk;
+  }
+  const int off = u.Nk - u.Nq;  // bottom-right diagonal offset
   int jb[NQT], je[NQT];
 #pragma unroll
   for (int t = 0; t < NQT; ++t) {
     jb[t] = je[t] = 0;
     const int r0 = u.q0 + t * BM;
-    if (r0 >= p.Nq) continue;
-    const int r1 = min(r0 + BM - 1, p.Nq - 1);
-    int hi = p.Nk;
+    if (r0 >= u.Nq) continue;
+    const int r1 = min(r0 + BM - 1, u.Nq - 1);
+    int hi = u.Nk;
     if (p.causal) hi = min(hi, r1 + off + 1);
     int lo = 0;
     if (p.window > 0) lo = max(0, r0 + off - p.window + 1);
@@ -266,8 +287,12 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
         mbar_arrive_expect_tx(bar_q_full, NQT * TILE_BYTES);
         for (int t = 0; t < NQT; ++t)
           for (int kb = 0; kb < KBLKS; ++kb)
-            tma_load_3d(sb + SMEM_Q + t * TILE_BYTES + kb * KBLK_BYTES, &tm_q, bar_q_full, kb * 64,
-                        u.q0 + t * BM, u.b * p.Hq + u.h);
+            if (p.varlen)
+              tma_load_3d(sb + SMEM_Q + t * TILE_BYTES + kb * KBLK_BYTES, &tm_q, bar_q_full, kb * 64,
+                          u.h, u.q_tok + u.q0 + t * BM);
+            else
+              tma_load_3d(sb + SMEM_Q + t * TILE_BYTES + kb * KBLK_BYTES, &tm_q, bar_q_full, kb * 64,
+                          u.q0 + t * BM, u.b * p.Hq + u.h);
         ++nq;
         for (int j = u.j_begin; j < u.j_end && ok; ++j) {
           for (int kv = 0; kv < 2; ++kv, ++it) {
@@ -279,8 +304,12 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
             mbar_arrive_expect_tx(bar_kv_full(s), TILE_BYTES);
             const CUtensorMap* m = kv ? &tm_v : &tm_k;
             for (int kb = 0; kb < KBLKS; ++kb)
-              tma_load_3d(sb + SMEM_RING + s * TILE_BYTES + kb * KBLK_BYTES, m, bar_kv_full(s),
-                          kb * 64, j * BN, u.b * p.Hkv + u.kvh);
+              if (p.varlen)
+                tma_load_3d(sb + SMEM_RING + s * TILE_BYTES + kb * KBLK_BYTES, m, bar_kv_full(s),
+                            kb * 64, u.kvh, u.k_tok + j * BN);
+              else
+                tma_load_3d(sb + SMEM_RING + s * TILE_BYTES + kb * KBLK_BYTES, m, bar_kv_full(s),
+                            kb * 64, j * BN, u.b * p.Hkv + u.kvh);
           }
         }
       }
@@ -395,7 +424,6 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     const uint32_t s_addr = tmem + lane_sel + s_col(t);
     const uint32_t o_addr = tmem + lane_sel + o_col<HD>(t);
     const float c = p.scale_log2;
-    const int off = p.Nk - p.Nq;
     int n_own = 0;  // own key tiles so far (phase of s_full)
     int n_out = 0;  // units that produced O_t so far (phase of o_full)
     bool ok = true;
@@ -405,13 +433,14 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
       own_range(u, t, jb, je);
       const int n_tiles = max(0, je - jb);
       const int row = u.q0 + t * BM + quad * 32 + lane;
+      const int off = u.Nk - u.Nq;
       // visible keys of this row: lo_r <= key <= hi_r
       const int diag = row + off;
-      const int hi_r = p.causal ? min(diag, p.Nk - 1) : p.Nk - 1;
+      const int hi_r = p.causal ? min(diag, u.Nk - 1) : u.Nk - 1;
       const int lo_r = p.window > 0 ? diag - p.window + 1 : 0;
       // tile-uniform bounds: a K tile inside [tile_lo_max, tile_hi_min] needs no mask
       const int trow0 = u.q0 + t * BM;
-      const int tile_hi_min = p.causal ? min(trow0 + off, p.Nk - 1) : p.Nk - 1;
+      const int tile_hi_min = p.causal ? min(trow0 + off, u.Nk - 1) : u.Nk - 1;
       const int tile_lo_max = p.window > 0 ? trow0 + BM - 1 + off - p.window + 1 : 0;
 
       float m = -CUDART_INF_F;  // running max of scale*log2(e)*s (possibly stale)
@@ -531,10 +560,11 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
         for (int i = 0; i < HD; ++i) o[i] = 0u;
       }
-      if (row < p.Nq) {
+      if (row < u.Nq) {
         const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
-        uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) +
-                                               ((static_cast<size_t>(u.b) * p.Hq + u.h) * p.Nq + row) * HD);
+        const size_t orow_idx = p.varlen ? static_cast<size_t>(u.q_tok + row) * p.Hq + u.h
+                                         : (static_cast<size_t>(u.b) * p.Hq + u.h) * p.Nq + row;
+        uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + orow_idx * HD);
 #pragma unroll
         for (int i = 0; i < HD / 8; ++i) {
           const uint4 v4 = make_uint4(
@@ -546,7 +576,9 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
         }
         if (p.lse != nullptr) {
           const float lse = (l > 0.f) ? (m + log2f(l)) * 0.69314718055994531f : -CUDART_INF_F;
-          p.lse[(static_cast<size_t>(u.b) * p.Hq + u.h) * p.Nq + row] = lse;
+          const size_t li = p.varlen ? static_cast<size_t>(u.h) * p.total_q + u.q_tok + row
+                                     : (static_cast<size_t>(u.b) * p.Hq + u.h) * p.Nq + row;
+          p.lse[li] = lse;
         }
       }
     }
@@ -568,18 +600,25 @@ namespace fwd_bf16 {
 template <int HD, bool F16>
 int launch_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
                 int Hkv, int Nq, int Nk, float scale, int causal, int window, int num_sms,
-                cudaStream_t stream, int* err) {
+                cudaStream_t stream, int* err, const int* cu_q, const int* cu_k, int total_q,
+                int total_k) {
   using C = Cfg<HD, F16>;
   const CUtensorMapDataType dt = F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   CUtensorMap tq, tk, tv;
-  const uint32_t box[3] = {64, 128, 1};
-  if (!encode_tiled_3d(&tq, dt, q, HD, Nq, static_cast<uint64_t>(B) * Hq,
-                       2, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_tiled_3d(&tk, dt, k, HD, Nk, static_cast<uint64_t>(B) * Hkv,
-                       2, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_tiled_3d(&tv, dt, v, HD, Nk, static_cast<uint64_t>(B) * Hkv,
-                       2, box, CU_TENSOR_MAP_SWIZZLE_128B))
-    return ATTN_ERR_CUDA;
+  const bool varlen = cu_q != nullptr;
+  if (varlen) {  // packed [total, H, D]: 128 token rows of one head per box
+    const uint32_t box[3] = {64, 1, 128};
+    if (!encode_tiled_3d(&tq, dt, q, HD, Hq, total_q, 2, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tiled_3d(&tk, dt, k, HD, Hkv, total_k, 2, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tiled_3d(&tv, dt, v, HD, Hkv, total_k, 2, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return ATTN_ERR_CUDA;
+  } else {       // [B*H, N, D]: 128 rows of one (batch, head) per box
+    const uint32_t box[3] = {64, 128, 1};
+    if (!encode_tiled_3d(&tq, dt, q, HD, Nq, static_cast<uint64_t>(B) * Hq, 2, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tiled_3d(&tk, dt, k, HD, Nk, static_cast<uint64_t>(B) * Hkv, 2, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tiled_3d(&tv, dt, v, HD, Nk, static_cast<uint64_t>(B) * Hkv, 2, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return ATTN_ERR_CUDA;
+  }
   static int attr_set_dev = -1;
   int dev = 0;
   cudaGetDevice(&dev);
@@ -602,6 +641,11 @@ int launch_impl(const void* q, const void* k, const void* v, void* o, float* lse
   prm.causal = causal ? 1 : 0;
   prm.window = window > 0 ? window : 0;
   prm.err = err;
+  prm.varlen = varlen ? 1 : 0;
+  prm.cu_q = cu_q;
+  prm.cu_k = cu_k;
+  prm.total_q = total_q;
+  prm.total_k = total_k;
   // persistent: at most one CTA per SM, each walking units blockIdx.x, +gridDim.x, ...
   const long long n_qblk = (Nq + BM * NQT - 1) / (BM * NQT);
   const long long units = n_qblk * Hq * B;
@@ -615,16 +659,16 @@ int launch_impl(const void* q, const void* k, const void* v, void* o, float* lse
 
 int launch_fwd_tc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
                   int Hkv, int Nq, int Nk, int D, int f16, float scale, int causal, int window,
-                  int num_sms, cudaStream_t stream, int* err) {
+                  int num_sms, cudaStream_t stream, int* err, const int* cu_q, const int* cu_k,
+                  int total_q, int total_k) {
   using fwd_bf16::launch_impl;
-  if (D == 64 && !f16)
-    return launch_impl<64, false>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, window, num_sms, stream, err);
-  if (D == 128 && !f16)
-    return launch_impl<128, false>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, window, num_sms, stream, err);
-  if (D == 64 && f16)
-    return launch_impl<64, true>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, window, num_sms, stream, err);
-  if (D == 128 && f16)
-    return launch_impl<128, true>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, window, num_sms, stream, err);
+#define ATTN_TC_ARGS q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, window, num_sms, stream, err, \
+                     cu_q, cu_k, total_q, total_k
+  if (D == 64 && !f16) return launch_impl<64, false>(ATTN_TC_ARGS);
+  if (D == 128 && !f16) return launch_impl<128, false>(ATTN_TC_ARGS);
+  if (D == 64 && f16) return launch_impl<64, true>(ATTN_TC_ARGS);
+  if (D == 128 && f16) return launch_impl<128, true>(ATTN_TC_ARGS);
+#undef ATTN_TC_ARGS
   return ATTN_ERR_HEAD_DIM;
 }
 

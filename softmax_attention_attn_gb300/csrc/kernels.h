@@ -19,6 +19,13 @@ struct FwdParams {
   float scale_log2;  // scale * log2(e)
   int causal, window;
   int* err;          // device error word
+  // ragged batches: Q/O [total_q, Hq, D], K/V [total_k, Hkv, D]; sequence b owns
+  // rows cu_q[b] .. cu_q[b+1]-1 (queries) and cu_k[b] .. cu_k[b+1]-1 (keys); Nq is
+  // then the maximum query length (it sizes the unit list)
+  int varlen;
+  const int* cu_q;
+  const int* cu_k;
+  int total_q, total_k;
 };
 
 // Tensor maps (cuTensorMapEncodeTiled, fetched from the driver at run time).
@@ -31,9 +38,12 @@ bool encode_tiled_4d(CUtensorMap* map, CUtensorMapDataType dt, const void* base,
                      CUtensorMapSwizzle swz);
 
 // Tensor-core forward; f16 != 0 selects fp16 operands and output instead of bf16.
+// With cu_q != nullptr the batch is ragged (packed token-major layout, see FwdParams);
+// Nq is then the maximum query length and Nk is unused.
 int launch_fwd_tc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
                   int Hkv, int Nq, int Nk, int D, int f16, float scale, int causal, int window,
-                  int num_sms, cudaStream_t stream, int* err);
+                  int num_sms, cudaStream_t stream, int* err, const int* cu_q = nullptr,
+                  const int* cu_k = nullptr, int total_q = 0, int total_k = 0);
 
 int launch_fwd_fp32(const float* q, const float* k, const float* v, float* o, float* lse, int B,
                     int Hq, int Hkv, int Nq, int Nk, int D, float scale, int causal, int window,

@@ -48,6 +48,21 @@ def prefill_inputs(B: int, Hq: int, Hkv: int, Nq: int, Nk: int, D: int,
     return _cast(q, dtype), _cast(k, dtype), _cast(v, dtype)
 
 
+def varlen_inputs(lens_q, lens_k, Hq: int, Hkv: int, D: int, dtype: str = "bf16", seed: int = 0):
+    """Ragged batch, packed token-major: ``(q [Tq,Hq,D], k [Tk,Hkv,D], v, cu_q, cu_k)``.
+
+    One generator seeded with ``seed`` draws fp32 N(0, 1) Q, then K, then V for
+    the whole packed batch; ``cu_q`` / ``cu_k`` are int32 prefix sums of the lengths.
+    """
+    g = torch.Generator("cpu").manual_seed(seed)
+    tq, tk = int(sum(lens_q)), int(sum(lens_k))
+    q = torch.randn(tq, Hq, D, generator=g, dtype=torch.float32)
+    k = torch.randn(tk, Hkv, D, generator=g, dtype=torch.float32)
+    v = torch.randn(tk, Hkv, D, generator=g, dtype=torch.float32)
+    cu = lambda lens: torch.tensor([0] + list(torch.cumsum(torch.tensor(lens), 0).tolist()), dtype=torch.int32)  # noqa: E731
+    return _cast(q, dtype), _cast(k, dtype), _cast(v, dtype), cu(lens_q), cu(lens_k)
+
+
 def decode_row_seed(seed: int, b: int) -> int:
     """Seed of the generator that draws sequence ``b``'s K/V rows."""
     return seed * 1_000_003 + 1 + b

@@ -275,6 +275,32 @@ def pin_paged_decode(ora):
     assert abs(Lp[0, 0] - G[("dense", "LSE")][0][0]) < 1e-14
 
 
+def pin_varlen(ora):
+    """Ragged batch = each sequence on its own (brute force), empty sequences included."""
+    lens_q, lens_k = [3, 0, 5, 2], [3, 4, 7, 0]
+    Hq, Hkv, D = 4, 2, 3
+    r = np.random.default_rng(31)
+    q = r.standard_normal((sum(lens_q), Hq, D))
+    k = r.standard_normal((sum(lens_k), Hkv, D))
+    v = r.standard_normal((sum(lens_k), Hkv, D))
+    cq, ck = np.concatenate([[0], np.cumsum(lens_q)]), np.concatenate([[0], np.cumsum(lens_k)])
+    for causal, window in ((False, 0), (True, 0), (True, 2)):
+        O, L = ora.attention_varlen(q, k, v, cq, ck, 0.5, causal, window)
+        for b in range(4):
+            q0, q1, k0, k1 = cq[b], cq[b + 1], ck[b], ck[b + 1]
+            if q1 == q0:
+                continue
+            if k1 == k0:
+                assert np.all(O[q0:q1] == 0) and np.all(L[:, q0:q1] == -np.inf)
+                continue
+            Ob, Lb = brute_force(q[q0:q1].transpose(1, 0, 2)[None], k[k0:k1].transpose(1, 0, 2)[None],
+                                 v[k0:k1].transpose(1, 0, 2)[None], 0.5, causal, window)
+            assert np.allclose(O[q0:q1], Ob[0].transpose(1, 0, 2), atol=1e-12)
+            fin = np.isfinite(Lb[0])
+            assert np.array_equal(np.isfinite(L[:, q0:q1]), fin)
+            assert np.allclose(L[:, q0:q1][fin], Lb[0][fin], atol=1e-12)
+
+
 # ---------------------------------------------------------------- golden
 def _read_golden(name):
     env = {"ln": math.log}
@@ -311,7 +337,8 @@ def pin_golden(ora):
 
 
 PINS = [pin_brute_force, pin_sdpa, pin_zero_query, pin_single_key, pin_probability_rows,
-        pin_causal_first_row, pin_dominant_key, pin_invariants, pin_decode, pin_paged_decode, pin_golden]
+        pin_causal_first_row, pin_dominant_key, pin_invariants, pin_decode, pin_paged_decode, pin_varlen,
+        pin_golden]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)

@@ -181,6 +181,25 @@ def test_fp16_dense_workload_sampled(dev):
     check(o.cpu()[idx], lse.cpu()[idx], O, L, BF16_O_TOL, BF16_LSE_REL, True)
 
 
+VARLEN_CASES = [  # (lens_q, lens_k, Hq, Hkv, D, causal, window)
+    ([1, 300, 0, 1000, 129], [1, 300, 0, 1000, 129], 4, 2, 128, True, 0),
+    ([1, 300, 0, 1000, 129], [1, 300, 0, 1000, 129], 4, 2, 128, False, 0),
+    ([64, 200, 513], [700, 200, 1100], 4, 4, 128, True, 0),     # chunked prefill per sequence
+    ([257, 5, 800], [257, 0, 800], 2, 1, 64, True, 100),        # a sequence without keys
+]
+
+
+@pytest.mark.parametrize("case", VARLEN_CASES, ids=str)
+def test_bf16_varlen(dev, case):
+    lens_q, lens_k, Hq, Hkv, D, causal, window = case
+    q, k, v, cq, ck = inputs.varlen_inputs(lens_q, lens_k, Hq, Hkv, D, "bf16", seed=19)
+    o, lse = binding.attn_fwd_varlen(q.to(dev), k.to(dev), v.to(dev), cq.to(dev), ck.to(dev), max(lens_q),
+                                     causal=causal, window=window)
+    O, L = oracle.attention_varlen(q, k, v, cq, ck, 1 / math.sqrt(D), causal, window)
+    check(o, lse, O, L, BF16_O_TOL, BF16_LSE_REL, True)
+    assert binding.get_device_error() == 0
+
+
 @pytest.mark.parametrize("name,B,Hq,Hkv,Nq,Nk,D,causal,window", [
     ("sliding_window_4096_B1_H32_KV8_N16384", 1, 32, 8, 16384, 16384, 128, True, 4096),
     ("chunked_prefill_B1_H32_KV8_Nq2048_Nk16384", 1, 32, 8, 2048, 16384, 128, True, 0),
