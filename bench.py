@@ -49,6 +49,7 @@ FP32 = dict(B=2, Hq=8, Hkv=8, N=4096, D=128, causal=False)
 WINDOW = dict(B=1, Hq=32, Hkv=8, Nq=16384, Nk=16384, D=128, causal=True, window=4096)
 CHUNKED = dict(B=1, Hq=32, Hkv=8, Nq=2048, Nk=16384, D=128, causal=True, window=0)
 DENSE64 = dict(B=1, Hq=32, Hkv=32, N=8192, D=64, causal=False)
+VARLEN = dict(B=32, Hq=32, Hkv=8, D=128, n_lo=512, n_hi=8192, causal=True)
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FP32_SIMT_FLOP_PER_CLK_SM = 256.0   # 128 FP32 lanes x 2 (fused multiply-add)
 GB300_SMS = 152
@@ -83,7 +84,7 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--workload", choices=["dense", "causal", "decode", "fp32", "window", "chunked", "d64",
-                                           "paged", "fp16"],
+                                           "paged", "fp16", "varlen"],
                     default="dense",
                     help="workload of the timed loop (default: the dense bf16 prefill)")
     ap.add_argument("--no-extras", action="store_true", help="skip the other workloads")
@@ -265,6 +266,7 @@ WORKLOAD_NAMES = {
     "chunked": "bf16 chunked prefill (causal, bottom-right) B=1 Hq=32 Hkv=8 Nq=2048 Nk=16384 D=128",
     "d64": "bf16 dense prefill B=1 H=32 N=8192 D=64 (non-causal)",
     "fp16": "fp16 dense prefill B=1 H=32 N=8192 D=128 (non-causal)",
+    "varlen": "bf16 ragged causal prefill, 32 sequences of U[512,8192] tokens, Hq=32 Hkv=8 D=128",
     "paged": "bf16 split-KV decode on a paged cache (page 256) B=64 Hq=32 Hkv=8 D=128, Nk_b~U[512,32768], chunk 512",
 }
 
@@ -274,7 +276,23 @@ def make_workload(name, dev, seed, peaks, peak_src, sm_max_mhz, decode_batch=Non
     import torch
     from softmax_attention_attn_gb300 import binding, inputs
     w = {"name": name, "desc": WORKLOAD_NAMES[name]}
-    if name in ("dense", "causal", "fp32", "window", "chunked", "d64", "fp16"):
+    if name == "varlen":
+        c = VARLEN
+        g = torch.Generator("cpu").manual_seed(seed + 11)
+        lens = torch.randint(c["n_lo"], c["n_hi"] + 1, (c["B"],), generator=g).tolist()
+        host = inputs.varlen_inputs(lens, lens, c["Hq"], c["Hkv"], c["D"], "bf16", seed)
+        q, k, v, cq, ck = (x.to(dev) for x in host)
+        o = torch.empty_like(q)
+        lse = torch.empty(c["Hq"], q.shape[0], device=dev, dtype=torch.float32)
+        w["fn"] = lambda: binding.attn_fwd_varlen(q, k, v, cq, ck, max(lens), o, lse, causal=True)
+        w["work"] = sum(masked_flops(1, c["Hq"], n, n, c["D"], True, 0) for n in lens)
+        w["unit"], w["launches"], w["dtype"] = "TFLOP/s", 1, "bf16"
+        w["seq_len"], w["batch"] = max(lens), c["B"]
+        w["bound"], w["peak"] = "tensor", peaks["bf16_tflops"]
+        w["peak_source"] = f"{peak_src} dense bf16 (burst)"
+        w["e2e_in"] = [(x, t) for x, t in zip(host, (q, k, v, cq, ck))]
+        w["e2e_out"] = [o, lse]
+    elif name in ("dense", "causal", "fp32", "window", "chunked", "d64", "fp16"):
         c = {"dense": MAIN, "causal": CAUSAL, "fp32": FP32, "window": WINDOW, "chunked": CHUNKED,
              "d64": DENSE64, "fp16": MAIN}[name]
         Nq, Nk = c.get("Nq", c.get("N")), c.get("Nk", c.get("N"))
@@ -456,7 +474,7 @@ def run_gb300(args, rank, world, local_rank):
     workloads = {}
     if not args.no_extras:
         xs = max(5, min(args.steps // 10, 50))
-        for name in ("dense", "causal", "decode", "paged", "fp32", "window", "chunked", "d64", "fp16"):
+        for name in ("dense", "causal", "decode", "paged", "fp32", "window", "chunked", "d64", "fp16", "varlen"):
             if name == args.workload:
                 continue
             x = make_workload(name, dev, rank, peaks, peak_src, sm_max, args.decode_batch)
