@@ -90,6 +90,30 @@ __device__ __forceinline__ void bf16x8_to_float(const uint4& u, float (&f)[8]) {
   }
 }
 
+// acc[h][e] += sum over the 8 keys (ksub + 8 i) of one 64-key tile of
+// p[h][key] * v[key][g16 * 8 + e].  With MASK, keys >= valid contribute 0.
+template <int G, bool MASK>
+__device__ __forceinline__ void pv_tile(float (&acc)[G][8], const uint8_t* tile, const float* pt,
+                                        int chunk, int ksub, int g16, int valid) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int key = ksub + 8 * i;
+    const uint4 u = *reinterpret_cast<const uint4*>(tile + key * (HD * 2) + g16 * 16);
+    float vf[8];
+    bf16x8_to_float(u, vf);
+    if (MASK && key >= valid) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) vf[e] = 0.f;
+    }
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const float pw = pt[h * chunk + key];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[h][e] = fmaf(pw, vf[e], acc[h][e]);
+    }
+  }
+}
+
 struct Work {
   int b, c, kvh, n_valid, ntl;
 };
@@ -324,23 +348,15 @@ attn_decode_splitkv_kernel(const __grid_constant__ CUtensorMap tm_k,
       ok = ok && __all_sync(0xffffffffu, mbar_wait(bar_full(s), (it / STAGES) & 1, abort_flag, err));
       if (!ok) continue;
       const uint8_t* tile = smem + L.ring + s * TILE_BYTES;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int key = ksub + 8 * i;
-        const uint4 u = *reinterpret_cast<const uint4*>(tile + key * (HD * 2) + g16 * 16);
-        float vf[8];
-        bf16x8_to_float(u, vf);
-        if (tl * TILE + key >= wk.n_valid) {  // rows past the sequence: never let them in (p is 0,
-#pragma unroll                                // but 0 * NaN from an unused cache row is not)
-          for (int e = 0; e < 8; ++e) vf[e] = 0.f;
-        }
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          const float pw = work[h * chunk + tl * TILE + key];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) acc[h][e] = fmaf(pw, vf[e], acc[h][e]);
-        }
-      }
+      const float* pt = work + tl * TILE;
+      // Only a chunk's last tile can reach past the sequence: that tile takes the
+      // masked copy of the loop, which zeroes the extra rows (p is 0 there, but
+      // 0 * NaN from an unused cache row is not).
+      const int valid_here = wk.n_valid - tl * TILE;
+      if (valid_here >= TILE)
+        pv_tile<G, false>(acc, tile, pt, chunk, ksub, g16, TILE);
+      else
+        pv_tile<G, true>(acc, tile, pt, chunk, ksub, g16, valid_here);
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_empty(s));
     }
