@@ -15,11 +15,10 @@
 //     swizzle, mbarrier transaction counts).  Barriers and tensor memory are set
 //     up once; the next unit's Q, K/V and first S overlap the last unit's
 //     epilogue;
-//   * warps 9 and 10 (one elected thread each) issue tcgen05.mma for Q tile 0
-//     and 1: S_t = Q_t K^T into tensor memory (fp32, 128 columns per Q tile),
-//     then O_t += P_t V with P read from tensor memory (the TS form) and V from
-//     shared memory (MN-major operand); the issuers take strict turns, each
-//     waiting for its own inputs while the other one issues;
+//   * warp 9 (one elected thread) issues every tcgen05.mma of both Q tiles:
+//     S_t = Q_t K^T into tensor memory (fp32, 128 columns per Q tile), then
+//     O_t += P_t V with P read from tensor memory (the TS form) and V from
+//     shared memory (MN-major operand);
 //   * warps 0-3 and 4-7 are the softmax warpgroups of Q tile 0 and 1: thread r
 //     owns row r, loads its 128 scores from tensor memory, applies the mask,
 //     updates the running max / sum in the exp2 domain, rescales its O row in
@@ -50,8 +49,8 @@ constexpr int NQT = 2;                       // Q tiles per work unit
 constexpr int KBLK_BYTES = 128 * 64 * 2;     // 64-column (128-byte) slab of a 128-row tile
 constexpr int NUM_SOFTMAX_WARPS = 4 * NQT;
 constexpr int WARP_TMA = NUM_SOFTMAX_WARPS;
-constexpr int WARP_MMA = NUM_SOFTMAX_WARPS + 1;      // issuer of Q tile t is warp WARP_MMA + t
-constexpr int NTHREADS = (NUM_SOFTMAX_WARPS + 1 + NQT) * 32;
+constexpr int WARP_MMA = NUM_SOFTMAX_WARPS + 1;      // the MMA issuer
+constexpr int NTHREADS = (NUM_SOFTMAX_WARPS + 2) * 32;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float RESCALE_LOG2 = 8.0f;         // keep a stale max while the growth is <= 2^8
 
@@ -65,7 +64,7 @@ struct Cfg {
   static constexpr int SMEM_Q = 0;
   static constexpr int SMEM_RING = SMEM_Q + NQT * TILE_BYTES;
   static constexpr int SMEM_BAR = SMEM_RING + STAGES * TILE_BYTES;
-  static constexpr int NUM_BARS = 3 + 2 * STAGES + 6 * NQT;
+  static constexpr int NUM_BARS = 3 + 2 * STAGES + 5 * NQT;
   static constexpr int SMEM_MISC = SMEM_BAR + NUM_BARS * 8;
   static constexpr int SMEM_ALLOC = SMEM_MISC + 16 + 1024;  // + slack for 1024-byte alignment
   static constexpr uint32_t AB_FORMAT = F16 ? 0u : 1u;  // instruction-descriptor A/B format
@@ -86,32 +85,62 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   else return pack_bf16x2(lo, hi);
 }
 
-// S (tmem) = Q_tile (smem) x K_tile^T (smem); both K-major, 128-byte swizzle.
+// Shared-memory descriptors are linear in the start address (its field is
+// address >> 4 in the low 14 bits, and every shared-memory address here is
+// below 2^18), so a descriptor for base + offset is the base descriptor plus
+// offset >> 4 in its low word.
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t off16) {
+  uint32_t lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=r"(lo), "=r"(hi) : "l"(d));
+  lo += off16;
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+  return r;
+}
+
+// S (tmem) = Q_tile (smem) x K_tile^T (smem); both K-major, 128-byte swizzle,
+// given by the descriptors of their first byte.
 template <int HD, bool F16>
-__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t q_desc, uint64_t k_desc) {
 #pragma unroll
   for (int kk = 0; kk < HD / 16; ++kk) {
-    const uint32_t koff = static_cast<uint32_t>((kk >> 2) * KBLK_BYTES + (kk & 3) * 32);
-    const uint64_t a = smem_desc_sw128(q_smem + koff, 16, 1024);
-    const uint64_t b = smem_desc_sw128(k_smem + koff, 16, 1024);
-    mma_bf16_ss(d_tmem, a, b, Cfg<HD, F16>::IDESC_QK, kk > 0 ? 1u : 0u);
+    const uint32_t koff = static_cast<uint32_t>((kk >> 2) * KBLK_BYTES + (kk & 3) * 32) >> 4;
+    mma_bf16_ss(d_tmem, desc_add(q_desc, koff), desc_add(k_desc, koff), Cfg<HD, F16>::IDESC_QK,
+                kk > 0 ? 1u : 0u);
   }
 }
 
 // O (tmem) (+)= P (tmem, bf16) x V_tile (smem, MN-major: d contiguous), for the
 // 16-key steps kk in [kk0, kk0 + 4): one half of the tile's keys.  With HD =
 // 128 the two 64-column slabs of V are KBLK_BYTES apart (the leading byte
-// offset of the MN-major operand); with HD = 64 there is one slab.
+// offset of the MN-major operand, part of v_desc); with HD = 64 there is one slab.
 template <int HD, bool F16>
-__device__ __forceinline__ void issue_pv_half(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem,
+__device__ __forceinline__ void issue_pv_half(uint32_t d_tmem, uint32_t p_tmem, uint64_t v_desc,
                                               bool accumulate, int kk0) {
 #pragma unroll
   for (int kk = kk0; kk < kk0 + BN / 32; ++kk) {
-    const uint64_t b = smem_desc_sw128(v_smem + static_cast<uint32_t>(kk * 16 * 128),
-                                       KBLK_BYTES, 1024);
-    mma_bf16_ts(d_tmem, p_tmem + static_cast<uint32_t>(kk * 8), b, Cfg<HD, F16>::IDESC_PV,
+    mma_bf16_ts(d_tmem, p_tmem + static_cast<uint32_t>(kk * 8),
+                desc_add(v_desc, static_cast<uint32_t>(kk * 16 * 128) >> 4), Cfg<HD, F16>::IDESC_PV,
                 (accumulate || kk > 0) ? 1u : 0u);
   }
+}
+
+// A position in the K/V ring: slot and the parity of its fill / release phase.
+struct RingPos {
+  int slot;
+  uint32_t phase;
+};
+template <int STAGES>
+__device__ __forceinline__ RingPos ring_pos(int pos) {
+  return RingPos{pos % STAGES, static_cast<uint32_t>((pos / STAGES) & 1)};
+}
+template <int STAGES>
+__device__ __forceinline__ RingPos ring_next(RingPos r) {
+  if (++r.slot == STAGES) {
+    r.slot = 0;
+    r.phase ^= 1u;
+  }
+  return r;
 }
 
 // Wait bounded by time only (used to drain work already in flight).
@@ -225,8 +254,8 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
 
   // ---- barriers (phases run on across the units a CTA processes)
   const uint32_t bar_q_full = sb + SMEM_BAR;            // Q tiles of a unit landed
-  const uint32_t bar_q_empty = sb + SMEM_BAR + 8;       // both issuers' last S of a unit done
-  const uint32_t bar_mma_done = sb + SMEM_BAR + 16;     // every MMA of both issuers done
+  const uint32_t bar_q_empty = sb + SMEM_BAR + 8;       // the last S of both Q tiles of a unit done
+  const uint32_t bar_mma_done = sb + SMEM_BAR + 16;     // every MMA issued has completed
   auto bar_kv_full = [&](int s) { return sb + SMEM_BAR + 8u * (3 + s); };
   auto bar_kv_empty = [&](int s) { return sb + SMEM_BAR + 8u * (3 + STAGES + s); };
   auto bar_t = [&](int kind, int t) { return sb + SMEM_BAR + 8u * (3 + 2 * STAGES + kind * NQT + t); };
@@ -235,7 +264,6 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
   auto bar_p_hi = [&](int t) { return bar_t(2, t); };     // P_t keys 64-127 in TMEM
   auto bar_o_full = [&](int t) { return bar_t(3, t); };   // O_t of a unit complete
   auto bar_o_empty = [&](int t) { return bar_t(4, t); };  // epilogue has read O_t
-  auto bar_turn = [&](int t) { return bar_t(5, t); };     // issue turn handed to issuer t
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + SMEM_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SMEM_MISC + 4);
 
@@ -245,10 +273,10 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
   if (threadIdx.x == 0) {
     mbar_init(bar_q_full, 1);
     mbar_init(bar_q_empty, NQT);
-    mbar_init(bar_mma_done, NQT);
+    mbar_init(bar_mma_done, 1);
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(bar_kv_full(s), 1);
-      mbar_init(bar_kv_empty(s), NQT);   // released once both Q tiles are done with it
+      mbar_init(bar_kv_empty(s), 1);     // one release once both Q tiles are done with it
     }
     for (int t = 0; t < NQT; ++t) {
       mbar_init(bar_s_full(t), 1);
@@ -256,7 +284,6 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
       mbar_init(bar_p_hi(t), BM / 32);
       mbar_init(bar_o_full(t), 1);
       mbar_init(bar_o_empty(t), BM / 32);
-      mbar_init(bar_turn(t), 1);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -318,96 +345,99 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
         for (int i = max(0, it - STAGES); i < it; ++i) drain_wait(bar_kv_full(i % STAGES), (i / STAGES) & 1);
       }
     }
-  } else if (warp >= WARP_MMA) {
-    // ================================================================ MMA issuers
-    // One thread per Q tile issues that tile's S = Q K^T and O += P V.  The two
-    // issuers take turns, so the tensor pipe sees the order PV_0 S_0 PV_1 S_1
-    // ... as from a single issuer, but each issuer does its own waiting for
-    // inputs while the other one issues.  MMAs of one thread execute in issue
-    // order, which orders S_t(j+1) after PV_t(j) (P_t aliases S_t).
-    const int t = warp - WARP_MMA;
+  } else if (warp == WARP_MMA) {
+    // ================================================================ MMA issuer
+    // One thread issues every MMA of both Q tiles.  Per key tile j the order is
+    // PV_0(j) S_0(j+1) PV_1(j) S_1(j+1): while warpgroup 0 runs the softmax of
+    // S_0(j+1) the tensor core works through PV_1(j) and S_1(j+1), and vice
+    // versa.  The tensor core takes a 128 x 128 x 16 MMA about every 64 cycles
+    // and the issuing thread is held for most of that, so everything else on
+    // this thread (waits for inputs that are normally already there, one
+    // commit per barrier event, ring bookkeeping) is kept short: every cycle
+    // spent here beyond the MMAs leaves the tensor pipe idle.  MMAs of one
+    // thread execute in issue order, which orders S_t(j+1) after PV_t(j)
+    // (P_t aliases S_t).  A ring slot is released by one commit once every MMA
+    // reading it has been issued.
     if (lane == 0) {
-      const uint32_t q_sm = sb + SMEM_Q + t * TILE_BYTES;
-      auto slot_of = [](int pos) { return pos % STAGES; };
-      auto phase_of = [](int pos) { return static_cast<uint32_t>((pos / STAGES) & 1); };
-      int it_base = 0;  // ring position of the current unit's first K tile
-      int nq = 0;       // units with work so far
-      int gstep = 0;    // steps taken in turn order so far
-      int n_own = 0;    // own key tiles so far (phase of s_full / p_lo / p_hi)
-      int n_out = 0;    // units that produced O_t so far (phase of o_full / o_empty)
+      auto wait_full = [&](RingPos r) { return mbar_wait(bar_kv_full(r.slot), r.phase, abort_flag, p.err); };
+      const uint64_t q_desc0 = smem_desc_sw128(sb + SMEM_Q, 16, 1024);
+      const uint64_t k_desc0 = smem_desc_sw128(sb + SMEM_RING, 16, 1024);
+      const uint64_t v_desc0 = smem_desc_sw128(sb + SMEM_RING, KBLK_BYTES, 1024);
+      auto q_desc = [&](int t) { return desc_add(q_desc0, static_cast<uint32_t>(t * TILE_BYTES) >> 4); };
+      auto k_desc = [&](RingPos r) { return desc_add(k_desc0, static_cast<uint32_t>(r.slot * TILE_BYTES) >> 4); };
+      auto v_desc = [&](RingPos r) { return desc_add(v_desc0, static_cast<uint32_t>(r.slot * TILE_BYTES) >> 4); };
+      int it_base = 0;             // ring position of the current unit's first K tile
+      int nq = 0;                  // units with work so far
+      int n_own[NQT] = {0, 0};     // own key tiles so far (phase of s_full / p_lo / p_hi)
+      int n_out[NQT] = {0, 0};     // units that produced O_t so far (phase of o_full / o_empty)
       bool ok = true;
       for (int w = blockIdx.x; w < n_units && ok; w += gridDim.x) {
         const Unit u = make_unit(w, p, n_qblk);
         if (u.j_end <= u.j_begin) continue;
-        int jb, je;
-        own_range(u, t, jb, je);
-        if (je <= jb) jb = je = u.j_end;  // no own tiles: the slots are only released
-        auto kpos = [&](int j) { return it_base + 2 * (j - u.j_begin); };
-        // Tiles outside this Q tile's range: wait for the fill, then release the
-        // slot without using it (a release never runs ahead of its fill).
-        auto skip_tile = [&](int j) {
-          for (int kv = 0; kv < 2; ++kv) {
-            const int pos = kpos(j) + kv;
-            if (!mbar_wait(bar_kv_full(slot_of(pos)), phase_of(pos), abort_flag, p.err)) return false;
-            mbar_arrive(bar_kv_empty(slot_of(pos)));
-          }
-          return true;
-        };
+        int jb[NQT], je[NQT];
+        own_range(u, 0, jb[0], je[0]);
+        own_range(u, 1, jb[1], je[1]);
         if (!mbar_wait(bar_q_full, nq & 1, abort_flag, p.err)) { ok = false; break; }
-        if (jb < je) {  // first S of this unit (outside the turn order)
-          if (!mbar_wait(bar_kv_full(slot_of(kpos(jb))), phase_of(kpos(jb)), abort_flag, p.err)) { ok = false; break; }
-          tc_fence_after();
-          issue_qk<HD, F16>(tmem + s_col(t), q_sm, sb + SMEM_RING + slot_of(kpos(jb)) * TILE_BYTES);
-          mma_commit(bar_s_full(t));
-          mma_commit(bar_kv_empty(slot_of(kpos(jb))));
-          if (je - jb == 1) mma_commit(bar_q_empty);  // that was this unit's last S
-        } else {
-          mbar_arrive(bar_q_empty);
+        // first S of each Q tile
+#pragma unroll
+        for (int t = 0; t < NQT; ++t) {
+          if (jb[t] < je[t]) {
+            const RingPos r = ring_pos<STAGES>(it_base + 2 * (jb[t] - u.j_begin));
+            if (!wait_full(r)) { ok = false; break; }
+            tc_fence_after();
+            issue_qk<HD, F16>(tmem + s_col(t), q_desc(t), k_desc(r));
+            mma_commit(bar_s_full(t));
+            if (je[t] - jb[t] == 1) mma_commit(bar_q_empty);  // that was this tile's last S
+          } else {
+            mbar_arrive(bar_q_empty);
+          }
         }
-        for (int j = u.j_begin; j < u.j_end && ok; ++j, ++gstep) {
-          const bool own = (j >= jb && j < je);
-          const int lt = n_own + (j - jb);
-          const int vpos = kpos(j) + 1;
-          const uint32_t vsm = sb + SMEM_RING + slot_of(vpos) * TILE_BYTES;
-          if (own) {
-            if (!mbar_wait(bar_kv_full(slot_of(vpos)), phase_of(vpos), abort_flag, p.err)) { ok = false; break; }
-            if (!mbar_wait(bar_p_lo(t), lt & 1, abort_flag, p.err)) { ok = false; break; }
-            // PV overwrites O_t at the unit's first key tile: the epilogue of the
-            // previous unit must have read it out.
-            if (j == jb && n_out > 0 &&
-                !mbar_wait(bar_o_empty(t), (n_out - 1) & 1, abort_flag, p.err)) { ok = false; break; }
-          }
-          if (t == 1 || gstep > 0) {
-            const uint32_t par = static_cast<uint32_t>((t == 0 ? gstep - 1 : gstep) & 1);
-            if (!mbar_wait(bar_turn(t), par, abort_flag, p.err)) { ok = false; break; }
-          }
-          if (own) {
-            tc_fence_after();
-            issue_pv_half<HD, F16>(tmem + o_col<HD>(t), tmem + s_col(t), vsm, j > jb, 0);
-            if (!mbar_wait(bar_p_hi(t), lt & 1, abort_flag, p.err)) { ok = false; break; }
-            tc_fence_after();
-            issue_pv_half<HD, F16>(tmem + o_col<HD>(t), tmem + s_col(t), vsm, true, BN / 32);
-            mma_commit(bar_kv_empty(slot_of(vpos)));
-            if (j + 1 == je) {
-              mma_commit(bar_o_full(t));
-            } else {
-              const int npos = kpos(j + 1);
-              if (!mbar_wait(bar_kv_full(slot_of(npos)), phase_of(npos), abort_flag, p.err)) { ok = false; break; }
+        if (!ok) break;
+        RingPos kj = ring_pos<STAGES>(it_base);  // K of key tile j
+        mma_commit(bar_kv_empty(kj.slot));       // every S of the first key tile is issued
+        for (int j = u.j_begin; j < u.j_end && ok; ++j) {
+          const RingPos vj = ring_next<STAGES>(kj);  // V of key tile j
+          const RingPos kn = ring_next<STAGES>(vj);  // K of key tile j + 1
+          // the fills this key tile needs, checked once for both Q tiles
+          if (!wait_full(vj) || (j + 1 < u.j_end && !wait_full(kn))) { ok = false; break; }
+#pragma unroll
+          for (int t = 0; t < NQT; ++t) {
+            const bool own = j >= jb[t] && j < je[t];
+            if (own) {
+              const int lt = n_own[t] + (j - jb[t]);
+              // P_t complete (its second half handed over implies the first) is
+              // the usual case: one non-blocking test instead of two waits
+              const bool p_all = mbar_test_wait(bar_p_hi(t), lt & 1);
+              if (!p_all && !mbar_wait(bar_p_lo(t), lt & 1, abort_flag, p.err)) { ok = false; break; }
+              // PV overwrites O_t at the unit's first key tile: the epilogue of the
+              // previous unit must have read it out.
+              if (j == jb[t] && n_out[t] > 0 &&
+                  !mbar_wait(bar_o_empty(t), (n_out[t] - 1) & 1, abort_flag, p.err)) { ok = false; break; }
               tc_fence_after();
-              issue_qk<HD, F16>(tmem + s_col(t), q_sm, sb + SMEM_RING + slot_of(npos) * TILE_BYTES);
-              mma_commit(bar_s_full(t));
-              mma_commit(bar_kv_empty(slot_of(npos)));
-              if (j + 2 == je) mma_commit(bar_q_empty);  // this unit's last S
+              issue_pv_half<HD, F16>(tmem + o_col<HD>(t), tmem + s_col(t), v_desc(vj), j > jb[t], 0);
+              if (!p_all) {
+                if (!mbar_wait(bar_p_hi(t), lt & 1, abort_flag, p.err)) { ok = false; break; }
+                tc_fence_after();
+              }
+              issue_pv_half<HD, F16>(tmem + o_col<HD>(t), tmem + s_col(t), v_desc(vj), true, BN / 32);
+              if (j + 1 == je[t]) mma_commit(bar_o_full(t));
             }
-          } else if (!skip_tile(j)) {
-            ok = false;
-            break;
+            if (t == NQT - 1) mma_commit(bar_kv_empty(vj.slot));  // every P V of key tile j is issued
+            if (own && j + 1 < je[t]) {
+              issue_qk<HD, F16>(tmem + s_col(t), q_desc(t), k_desc(kn));
+              mma_commit(bar_s_full(t));
+              if (j + 2 == je[t]) mma_commit(bar_q_empty);  // this tile's last S
+            }
           }
-          mbar_arrive(bar_turn(1 - t));
+          if (j + 1 < u.j_end) mma_commit(bar_kv_empty(kn.slot));  // every S of key tile j+1 is issued
+          kj = kn;
         }
-        if (je > jb) {
-          n_own += je - jb;
-          ++n_out;
+#pragma unroll
+        for (int t = 0; t < NQT; ++t) {
+          if (je[t] > jb[t]) {
+            n_own[t] += je[t] - jb[t];
+            ++n_out[t];
+          }
         }
         it_base += 2 * (u.j_end - u.j_begin);
         ++nq;
