@@ -101,12 +101,13 @@ __device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t off16) {
 // S (tmem) = Q_tile (smem) x K_tile^T (smem); both K-major, 128-byte swizzle,
 // given by the descriptors of their first byte.
 template <int HD, bool F16>
-__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t q_desc, uint64_t k_desc) {
+__device__ __forceinline__ void issue_qk(uint32_t issue, uint32_t d_tmem, uint64_t q_desc,
+                                         uint64_t k_desc) {
 #pragma unroll
   for (int kk = 0; kk < HD / 16; ++kk) {
     const uint32_t koff = static_cast<uint32_t>((kk >> 2) * KBLK_BYTES + (kk & 3) * 32) >> 4;
-    mma_bf16_ss(d_tmem, desc_add(q_desc, koff), desc_add(k_desc, koff), Cfg<HD, F16>::IDESC_QK,
-                kk > 0 ? 1u : 0u);
+    mma_bf16_ss_if(issue, d_tmem, desc_add(q_desc, koff), desc_add(k_desc, koff),
+                   Cfg<HD, F16>::IDESC_QK, kk > 0 ? 1u : 0u);
   }
 }
 
@@ -115,11 +116,11 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t q_desc, uint6
 // 128 the two 64-column slabs of V are KBLK_BYTES apart (the leading byte
 // offset of the MN-major operand, part of v_desc); with HD = 64 there is one slab.
 template <int HD, bool F16>
-__device__ __forceinline__ void issue_pv_half(uint32_t d_tmem, uint32_t p_tmem, uint64_t v_desc,
-                                              bool accumulate, int kk0) {
+__device__ __forceinline__ void issue_pv_half(uint32_t issue, uint32_t d_tmem, uint32_t p_tmem,
+                                              uint64_t v_desc, bool accumulate, int kk0) {
 #pragma unroll
   for (int kk = kk0; kk < kk0 + BN / 32; ++kk) {
-    mma_bf16_ts(d_tmem, p_tmem + static_cast<uint32_t>(kk * 8),
+    mma_bf16_ts_if(issue, d_tmem, p_tmem + static_cast<uint32_t>(kk * 8),
                 desc_add(v_desc, static_cast<uint32_t>(kk * 16 * 128) >> 4), Cfg<HD, F16>::IDESC_PV,
                 (accumulate || kk > 0) ? 1u : 0u);
   }
@@ -358,7 +359,8 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     // thread execute in issue order, which orders S_t(j+1) after PV_t(j)
     // (P_t aliases S_t).  A ring slot is released by one commit once every MMA
     // reading it has been issued.
-    if (lane == 0) {
+    {
+      const uint32_t elect = lane == 0 ? 1u : 0u;  // the lane that issues
       auto wait_full = [&](RingPos r) { return mbar_wait(bar_kv_full(r.slot), r.phase, abort_flag, p.err); };
       const uint64_t q_desc0 = smem_desc_sw128(sb + SMEM_Q, 16, 1024);
       const uint64_t k_desc0 = smem_desc_sw128(sb + SMEM_RING, 16, 1024);
@@ -385,16 +387,16 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
             const RingPos r = ring_pos<STAGES>(it_base + 2 * (jb[t] - u.j_begin));
             if (!wait_full(r)) { ok = false; break; }
             tc_fence_after();
-            issue_qk<HD, F16>(tmem + s_col(t), q_desc(t), k_desc(r));
-            mma_commit(bar_s_full(t));
-            if (je[t] - jb[t] == 1) mma_commit(bar_q_empty);  // that was this tile's last S
+            issue_qk<HD, F16>(elect, tmem + s_col(t), q_desc(t), k_desc(r));
+            mma_commit_if(elect, bar_s_full(t));
+            if (je[t] - jb[t] == 1) mma_commit_if(elect, bar_q_empty);  // that was this tile's last S
           } else {
-            mbar_arrive(bar_q_empty);
+            mbar_arrive_if(elect, bar_q_empty);
           }
         }
         if (!ok) break;
         RingPos kj = ring_pos<STAGES>(it_base);  // K of key tile j
-        mma_commit(bar_kv_empty(kj.slot));       // every S of the first key tile is issued
+        mma_commit_if(elect, bar_kv_empty(kj.slot));       // every S of the first key tile is issued
         for (int j = u.j_begin; j < u.j_end && ok; ++j) {
           const RingPos vj = ring_next<STAGES>(kj);  // V of key tile j
           const RingPos kn = ring_next<STAGES>(vj);  // K of key tile j + 1
@@ -414,22 +416,22 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
               if (j == jb[t] && n_out[t] > 0 &&
                   !mbar_wait(bar_o_empty(t), (n_out[t] - 1) & 1, abort_flag, p.err)) { ok = false; break; }
               tc_fence_after();
-              issue_pv_half<HD, F16>(tmem + o_col<HD>(t), tmem + s_col(t), v_desc(vj), j > jb[t], 0);
+              issue_pv_half<HD, F16>(elect, tmem + o_col<HD>(t), tmem + s_col(t), v_desc(vj), j > jb[t], 0);
               if (!p_all) {
                 if (!mbar_wait(bar_p_hi(t), lt & 1, abort_flag, p.err)) { ok = false; break; }
                 tc_fence_after();
               }
-              issue_pv_half<HD, F16>(tmem + o_col<HD>(t), tmem + s_col(t), v_desc(vj), true, BN / 32);
-              if (j + 1 == je[t]) mma_commit(bar_o_full(t));
+              issue_pv_half<HD, F16>(elect, tmem + o_col<HD>(t), tmem + s_col(t), v_desc(vj), true, BN / 32);
+              if (j + 1 == je[t]) mma_commit_if(elect, bar_o_full(t));
             }
-            if (t == NQT - 1) mma_commit(bar_kv_empty(vj.slot));  // every P V of key tile j is issued
+            if (t == NQT - 1) mma_commit_if(elect, bar_kv_empty(vj.slot));  // every P V of key tile j is issued
             if (own && j + 1 < je[t]) {
-              issue_qk<HD, F16>(tmem + s_col(t), q_desc(t), k_desc(kn));
-              mma_commit(bar_s_full(t));
-              if (j + 2 == je[t]) mma_commit(bar_q_empty);  // this tile's last S
+              issue_qk<HD, F16>(elect, tmem + s_col(t), q_desc(t), k_desc(kn));
+              mma_commit_if(elect, bar_s_full(t));
+              if (j + 2 == je[t]) mma_commit_if(elect, bar_q_empty);  // this tile's last S
             }
           }
-          if (j + 1 < u.j_end) mma_commit(bar_kv_empty(kn.slot));  // every S of key tile j+1 is issued
+          if (j + 1 < u.j_end) mma_commit_if(elect, bar_kv_empty(kn.slot));  // every S of key tile j+1 is issued
           kj = kn;
         }
 #pragma unroll
@@ -443,7 +445,7 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
         ++nq;
       }
       // every MMA issued above must finish before tensor memory is released
-      mma_commit(bar_mma_done);
+      mma_commit_if(elect, bar_mma_done);
       drain_wait(bar_mma_done, 0);
     }
   } else {
