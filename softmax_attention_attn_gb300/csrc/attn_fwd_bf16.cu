@@ -49,8 +49,8 @@ constexpr int NQT = 2;                       // Q tiles per work unit
 constexpr int KBLK_BYTES = 128 * 64 * 2;     // 64-column (128-byte) slab of a 128-row tile
 constexpr int NUM_SOFTMAX_WARPS = 4 * NQT;
 constexpr int WARP_TMA = NUM_SOFTMAX_WARPS;
-constexpr int WARP_MMA = NUM_SOFTMAX_WARPS + 1;      // the MMA issuer
-constexpr int NTHREADS = (NUM_SOFTMAX_WARPS + 2) * 32;
+constexpr int WARP_MMA = NUM_SOFTMAX_WARPS + 1;      // issuer of Q tile t is warp WARP_MMA + t
+constexpr int NTHREADS = (NUM_SOFTMAX_WARPS + 1 + NQT) * 32;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float RESCALE_LOG2 = 8.0f;         // keep a stale max while the growth is <= 2^8
 
@@ -267,6 +267,7 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
   auto bar_o_empty = [&](int t) { return bar_t(4, t); };  // epilogue has read O_t
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + SMEM_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SMEM_MISC + 4);
+  volatile uint32_t* turn = reinterpret_cast<volatile uint32_t*>(smem + SMEM_MISC + 8);
 
   const int n_qblk = (p.Nq + BM * NQT - 1) / (BM * NQT);
   const int n_units = n_qblk * p.Hq * p.B;
@@ -274,10 +275,10 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
   if (threadIdx.x == 0) {
     mbar_init(bar_q_full, 1);
     mbar_init(bar_q_empty, NQT);
-    mbar_init(bar_mma_done, 1);
+    mbar_init(bar_mma_done, NQT);
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(bar_kv_full(s), 1);
-      mbar_init(bar_kv_empty(s), 1);     // one release once both Q tiles are done with it
+      mbar_init(bar_kv_empty(s), NQT);   // released once both Q tiles are done with it
     }
     for (int t = 0; t < NQT; ++t) {
       mbar_init(bar_s_full(t), 1);
@@ -287,6 +288,7 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
       mbar_init(bar_o_empty(t), BM / 32);
     }
     *abort_flag = 0;
+    *turn = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
   }
@@ -346,100 +348,124 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
         for (int i = max(0, it - STAGES); i < it; ++i) drain_wait(bar_kv_full(i % STAGES), (i / STAGES) & 1);
       }
     }
-  } else if (warp == WARP_MMA) {
-    // ================================================================ MMA issuer
-    // One thread issues every MMA of both Q tiles.  Per key tile j the order is
-    // PV_0(j) S_0(j+1) PV_1(j) S_1(j+1): while warpgroup 0 runs the softmax of
-    // S_0(j+1) the tensor core works through PV_1(j) and S_1(j+1), and vice
-    // versa.  The tensor core takes a 128 x 128 x 16 MMA about every 64 cycles
-    // and the issuing thread is held for most of that, so everything else on
-    // this thread (waits for inputs that are normally already there, one
-    // commit per barrier event, ring bookkeeping) is kept short: every cycle
-    // spent here beyond the MMAs leaves the tensor pipe idle.  MMAs of one
+  } else if (warp >= WARP_MMA) {
+    // ================================================================ MMA issuers
+    // Warp WARP_MMA + t issues the MMAs of Q tile t; per key tile j its step is
+    // PV_t(j) (P_t from tensor memory) then S_t(j+1).  The tensor core takes a
+    // 128 x 128 x 16 MMA about every 64 cycles and holds the issuing thread for
+    // most of that, so the two issuers take strict turns, step by step
+    // (t = 0, 1, 0, 1, ...), and do everything but the MMAs outside their turn:
+    // waits for P, for filled ring slots and for the epilogue before it, commits
+    // and slot releases after it.  One issuer's bookkeeping then overlaps the
+    // other's MMAs, and the tensor pipe sees the MMAs of one step together, so
+    // S_t(j+1) is not held back behind the other tile's MMAs.  The turn order
+    // only sets priority (the two Q tiles share no tensor memory and each issuer
+    // releases ring slots for its own uses); the turn passes through a
+    // shared-memory counter.  The whole warp runs the loop converged (its
+    // descriptors and addresses warp-uniform); lane 0 issues.  MMAs of one
     // thread execute in issue order, which orders S_t(j+1) after PV_t(j)
-    // (P_t aliases S_t).  A ring slot is released by one commit once every MMA
-    // reading it has been issued.
+    // (P_t aliases S_t).
+    const int t = warp - WARP_MMA;
     {
       const uint32_t elect = lane == 0 ? 1u : 0u;  // the lane that issues
       auto wait_full = [&](RingPos r) { return mbar_wait(bar_kv_full(r.slot), r.phase, abort_flag, p.err); };
-      const uint64_t q_desc0 = smem_desc_sw128(sb + SMEM_Q, 16, 1024);
+      // bounded spin until the turn counter reaches `seq`
+      auto wait_turn = [&](uint32_t seq) {
+        if (*turn == seq) return true;
+        const unsigned long long t0 = global_ns();
+        for (uint32_t it = 1;; ++it) {
+          if (*turn == seq) return true;
+          if ((it & 63u) == 0u) {
+            if (*abort_flag) return false;
+            if (global_ns() - t0 > kAttnWaitNs) {
+              *abort_flag = 1;
+              atomicCAS(p.err, 0, ATTN_ERR_TIMEOUT);
+              return false;
+            }
+          }
+        }
+      };
+      const uint64_t q_desc = smem_desc_sw128(sb + SMEM_Q + t * TILE_BYTES, 16, 1024);
       const uint64_t k_desc0 = smem_desc_sw128(sb + SMEM_RING, 16, 1024);
       const uint64_t v_desc0 = smem_desc_sw128(sb + SMEM_RING, KBLK_BYTES, 1024);
-      auto q_desc = [&](int t) { return desc_add(q_desc0, static_cast<uint32_t>(t * TILE_BYTES) >> 4); };
       auto k_desc = [&](RingPos r) { return desc_add(k_desc0, static_cast<uint32_t>(r.slot * TILE_BYTES) >> 4); };
       auto v_desc = [&](RingPos r) { return desc_add(v_desc0, static_cast<uint32_t>(r.slot * TILE_BYTES) >> 4); };
-      int it_base = 0;             // ring position of the current unit's first K tile
-      int nq = 0;                  // units with work so far
-      int n_own[NQT] = {0, 0};     // own key tiles so far (phase of s_full / p_lo / p_hi)
-      int n_out[NQT] = {0, 0};     // units that produced O_t so far (phase of o_full / o_empty)
+      int it_base = 0;                      // ring position of the current unit's first K tile
+      int nq = 0;                           // units with work so far
+      int n_own = 0;                        // own key tiles so far (phase of s_full / p_lo / p_hi)
+      int n_out = 0;                        // units that produced O_t so far (phase of o_full / o_empty)
+      uint32_t seq = static_cast<uint32_t>(t);  // this issuer's next turn
       bool ok = true;
       for (int w = blockIdx.x; w < n_units && ok; w += gridDim.x) {
         const Unit u = make_unit(w, p, n_qblk);
         if (u.j_end <= u.j_begin) continue;
-        int jb[NQT], je[NQT];
-        own_range(u, 0, jb[0], je[0]);
-        own_range(u, 1, jb[1], je[1]);
+        int jb, je;
+        own_range(u, t, jb, je);
+        if (je <= jb) jb = je = u.j_end;  // no own tiles: the slots are only released
         if (!mbar_wait(bar_q_full, nq & 1, abort_flag, p.err)) { ok = false; break; }
-        // first S of each Q tile
-#pragma unroll
-        for (int t = 0; t < NQT; ++t) {
-          if (jb[t] < je[t]) {
-            const RingPos r = ring_pos<STAGES>(it_base + 2 * (jb[t] - u.j_begin));
-            if (!wait_full(r)) { ok = false; break; }
-            tc_fence_after();
-            issue_qk<HD, F16>(elect, tmem + s_col(t), q_desc(t), k_desc(r));
-            mma_commit_if(elect, bar_s_full(t));
-            if (je[t] - jb[t] == 1) mma_commit_if(elect, bar_q_empty);  // that was this tile's last S
-          } else {
-            mbar_arrive_if(elect, bar_q_empty);
-          }
+        if (jb < je) {  // first S of this unit (outside the turn order)
+          const RingPos r = ring_pos<STAGES>(it_base + 2 * (jb - u.j_begin));
+          if (!wait_full(r)) { ok = false; break; }
+          tc_fence_after();
+          issue_qk<HD, F16>(elect, tmem + s_col(t), q_desc, k_desc(r));
+          mma_commit_if(elect, bar_s_full(t));
+          mma_commit_if(elect, bar_kv_empty(r.slot));
+          if (je - jb == 1) mma_commit_if(elect, bar_q_empty);  // that was this unit's last S
+        } else {
+          mbar_arrive_if(elect, bar_q_empty);
         }
-        if (!ok) break;
         RingPos kj = ring_pos<STAGES>(it_base);  // K of key tile j
-        mma_commit_if(elect, bar_kv_empty(kj.slot));       // every S of the first key tile is issued
         for (int j = u.j_begin; j < u.j_end && ok; ++j) {
           const RingPos vj = ring_next<STAGES>(kj);  // V of key tile j
           const RingPos kn = ring_next<STAGES>(vj);  // K of key tile j + 1
-          // the fills this key tile needs, checked once for both Q tiles
-          if (!wait_full(vj) || (j + 1 < u.j_end && !wait_full(kn))) { ok = false; break; }
-#pragma unroll
-          for (int t = 0; t < NQT; ++t) {
-            const bool own = j >= jb[t] && j < je[t];
-            if (own) {
-              const int lt = n_own[t] + (j - jb[t]);
-              // P_t complete (its second half handed over implies the first) is
-              // the usual case: one non-blocking test instead of two waits
-              const bool p_all = mbar_test_wait(bar_p_hi(t), lt & 1);
-              if (!p_all && !mbar_wait(bar_p_lo(t), lt & 1, abort_flag, p.err)) { ok = false; break; }
-              // PV overwrites O_t at the unit's first key tile: the epilogue of the
-              // previous unit must have read it out.
-              if (j == jb[t] && n_out[t] > 0 &&
-                  !mbar_wait(bar_o_empty(t), (n_out[t] - 1) & 1, abort_flag, p.err)) { ok = false; break; }
-              tc_fence_after();
-              issue_pv_half<HD, F16>(elect, tmem + o_col<HD>(t), tmem + s_col(t), v_desc(vj), j > jb[t], 0);
-              if (!p_all) {
-                if (!mbar_wait(bar_p_hi(t), lt & 1, abort_flag, p.err)) { ok = false; break; }
-                tc_fence_after();
-              }
-              issue_pv_half<HD, F16>(elect, tmem + o_col<HD>(t), tmem + s_col(t), v_desc(vj), true, BN / 32);
-              if (j + 1 == je[t]) mma_commit_if(elect, bar_o_full(t));
+          const bool own = j >= jb && j < je;
+          const int lt = n_own + (j - jb);
+          bool p_all = false;
+          if (own) {
+            // inputs of this step, before taking the turn
+            if (!wait_full(vj) || !mbar_wait(bar_p_lo(t), lt & 1, abort_flag, p.err)) { ok = false; break; }
+            // PV overwrites O_t at the unit's first key tile: the epilogue of the
+            // previous unit must have read it out.
+            if (j == jb && n_out > 0 && !mbar_wait(bar_o_empty(t), (n_out - 1) & 1, abort_flag, p.err)) {
+              ok = false;
+              break;
             }
-            if (t == NQT - 1) mma_commit_if(elect, bar_kv_empty(vj.slot));  // every P V of key tile j is issued
-            if (own && j + 1 < je[t]) {
-              issue_qk<HD, F16>(elect, tmem + s_col(t), q_desc(t), k_desc(kn));
-              mma_commit_if(elect, bar_s_full(t));
-              if (j + 2 == je[t]) mma_commit_if(elect, bar_q_empty);  // this tile's last S
-            }
+            if (j + 1 < je && !wait_full(kn)) { ok = false; break; }
+            p_all = mbar_test_wait(bar_p_hi(t), lt & 1);
           }
-          if (j + 1 < u.j_end) mma_commit_if(elect, bar_kv_empty(kn.slot));  // every S of key tile j+1 is issued
+          if (!wait_turn(seq)) { ok = false; break; }
+          if (own) {
+            tc_fence_after();
+            issue_pv_half<HD, F16>(elect, tmem + o_col<HD>(t), tmem + s_col(t), v_desc(vj), j > jb, 0);
+            if (!p_all) {
+              if (!mbar_wait(bar_p_hi(t), lt & 1, abort_flag, p.err)) { ok = false; break; }
+              tc_fence_after();
+            }
+            issue_pv_half<HD, F16>(elect, tmem + o_col<HD>(t), tmem + s_col(t), v_desc(vj), true, BN / 32);
+            if (j + 1 < je) issue_qk<HD, F16>(elect, tmem + s_col(t), q_desc, k_desc(kn));
+          }
+          *turn = seq + 1;  // the other issuer's turn
+          seq += 2;
+          if (own) {
+            mma_commit_if(elect, bar_kv_empty(vj.slot));
+            if (j + 1 == je) {
+              mma_commit_if(elect, bar_o_full(t));
+            } else {
+              mma_commit_if(elect, bar_s_full(t));
+              mma_commit_if(elect, bar_kv_empty(kn.slot));
+              if (j + 2 == je) mma_commit_if(elect, bar_q_empty);  // this unit's last S
+            }
+          } else {
+            // outside this Q tile's range: release both slots once they are filled
+            if (!wait_full(kj) || !wait_full(vj)) { ok = false; break; }
+            mbar_arrive_if(elect, bar_kv_empty(kj.slot));
+            mbar_arrive_if(elect, bar_kv_empty(vj.slot));
+          }
           kj = kn;
         }
-#pragma unroll
-        for (int t = 0; t < NQT; ++t) {
-          if (je[t] > jb[t]) {
-            n_own[t] += je[t] - jb[t];
-            ++n_out[t];
-          }
+        if (je > jb) {
+          n_own += je - jb;
+          ++n_out;
         }
         it_base += 2 * (u.j_end - u.j_begin);
         ++nq;
