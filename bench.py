@@ -111,8 +111,8 @@ def kernel_traffic():
     src_hash = hashlib.sha256(open(KERNEL_SRC, "rb").read()).hexdigest()[:16]
     fields = {}
     for line in open(TRAFFIC_FILE):
-        if ":" in line and line.startswith("- "):
-            k, v = line[2:].split(":", 1)
+        if ": " in line and line.startswith("- "):
+            k, v = line[2:].split(": ", 1)
             fields[k.strip()] = v.strip().strip("`")
     if fields.get("kernel source sha256[:16]") != src_hash:
         return None

@@ -15,16 +15,17 @@
 //     swizzle, mbarrier transaction counts).  Barriers and tensor memory are set
 //     up once; the next unit's Q, K/V and first S overlap the last unit's
 //     epilogue;
-//   * warp 9 (one elected thread) issues every tcgen05.mma of both Q tiles:
-//     S_t = Q_t K^T into tensor memory (fp32, 128 columns per Q tile), then
-//     O_t += P_t V with P read from tensor memory (the TS form) and V from
-//     shared memory (MN-major operand);
+//   * warps 9 and 10 issue the tcgen05.mma of Q tile 0 and 1 (lane 0 of a
+//     converged warp): S_t = Q_t K^T into tensor memory (fp32, 128 columns per
+//     Q tile), then O_t += P_t V with P read from tensor memory (the TS form)
+//     and V from shared memory (MN-major operand); the two take strict turns,
+//     one key tile at a time, and wait and commit outside their turn;
 //   * warps 0-3 and 4-7 are the softmax warpgroups of Q tile 0 and 1: thread r
 //     owns row r, loads its 128 scores from tensor memory, applies the mask,
 //     updates the running max / sum in the exp2 domain, rescales its O row in
 //     tensor memory when the max grew by more than 2^8 (otherwise the stale max
 //     is kept; the final normalisation is exact either way), writes P as bf16
-//     over its S columns and signals the MMA warp;
+//     over its S columns and signals its MMA issuer;
 //   * warp 8 (one elected thread) is the TMA producer;
 //   * the epilogue (same softmax threads) divides by the row sum, rounds O to
 //     bf16 and writes O and LSE.
@@ -551,7 +552,7 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
         l *= alpha;
         const float m_use = (m == -CUDART_INF_F) ? 0.f : m;
         // p = 2^(s*c - m), summed and packed to bf16 pairs; each half of the keys
-        // is handed to the MMA warp as soon as it is in tensor memory.
+        // is handed to the MMA issuer as soon as it is in tensor memory.
         const uint64_t c2 = f2_pack(c, c);
         const uint64_t nm2 = f2_pack(-m_use, -m_use);
         uint64_t sum2[2] = {0ull, 0ull};

@@ -83,3 +83,20 @@ def test_visible_pairs_matches_enumeration():
         brute = sum(1 for i in range(Nq) for j in range(Nk)
                     if (not causal or j <= i + Nk - Nq) and (window <= 0 or j > i + Nk - Nq - window))
         assert bench.visible_pairs(Nq, Nk, causal, window) == brute
+
+
+def test_kernel_traffic_reads_summary_only_for_matching_source(tmp_path, monkeypatch):
+    """roofline.traffic comes from the committed ncu summary only while the kernel source
+    it was captured from is unchanged (the field name itself contains a colon)."""
+    import hashlib
+    src = tmp_path / "kernel.cu"
+    src.write_text("__global__ void k() {}\n")
+    h = hashlib.sha256(src.read_bytes()).hexdigest()[:16]
+    summary = tmp_path / "summary.md"
+    summary.write_text(f"# k\n\n- kernel source sha256[:16]: `{h}`\n- dram bytes per launch: `1234`\n")
+    monkeypatch.setattr(bench, "KERNEL_SRC", str(src))
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(summary))
+    assert bench.kernel_traffic() == 1234.0
+    src.write_text("__global__ void k() { }\n")
+    assert bench.kernel_traffic() is None
+
