@@ -15,22 +15,26 @@
 //     swizzle, mbarrier transaction counts).  Barriers and tensor memory are set
 //     up once; the next unit's Q, K/V and first S overlap the last unit's
 //     epilogue;
-//   * warps 9 and 10 issue the tcgen05.mma of Q tile 0 and 1 (lane 0 of a
+//   * warps 0 and 1 issue the tcgen05.mma of Q tile 0 and 1 (lane 0 of a
 //     converged warp): S_t = Q_t K^T into tensor memory (fp32, 128 columns per
 //     Q tile), then O_t += P_t V with P read from tensor memory (the TS form)
 //     and V from shared memory (MN-major operand); the two take strict turns,
 //     one key tile at a time, and wait and commit outside their turn;
-//   * warps 0-3 and 4-7 are the softmax warpgroups of Q tile 0 and 1: thread r
-//     owns row r, loads its 128 scores from tensor memory, applies the mask,
+//   * warps 3-6 and 7-10 are the softmax warps of Q tile 0 and 1: warp w
+//     reaches tensor-memory lanes 32 (w % 4) .. + 31, so thread r of warp w
+//     owns row 32 (w % 4) + r; it loads its 128 scores, applies the mask,
 //     updates the running max / sum in the exp2 domain, rescales its O row in
 //     tensor memory when the max grew by more than 2^8 (otherwise the stale max
 //     is kept; the final normalisation is exact either way), writes P as bf16
 //     over its S columns and signals its MMA issuer;
-//   * warp 8 (one elected thread) is the TMA producer;
+//   * warp 2 (one elected thread) is the TMA producer;
+//   * the MMA issuers have the lowest warp numbers (measured about 1 % faster
+//     than the highest, where they share sub-partitions with the same softmax
+//     warps either way);
 //   * the epilogue (same softmax threads) divides by the row sum, rounds O to
 //     bf16 and writes O and LSE.
 //
-// The two Q tiles ping-pong: while warpgroup 0 runs the softmax of tile j the
+// The two Q tiles ping-pong: while the softmax warps of tile 0 work on tile j the
 // tensor core computes PV_1(j-1) and S_1(j), and vice versa.
 //
 // Tensor memory (512 columns): S_0 [0,128) S_1 [128,256) O_0 [256,384) O_1 [384,512);
@@ -49,8 +53,9 @@ constexpr int BN = 128;                      // keys per K/V tile
 constexpr int NQT = 2;                       // Q tiles per work unit
 constexpr int KBLK_BYTES = 128 * 64 * 2;     // 64-column (128-byte) slab of a 128-row tile
 constexpr int NUM_SOFTMAX_WARPS = 4 * NQT;
-constexpr int WARP_TMA = NUM_SOFTMAX_WARPS;
-constexpr int WARP_MMA = NUM_SOFTMAX_WARPS + 1;      // issuer of Q tile t is warp WARP_MMA + t
+constexpr int WARP_MMA = 0;                          // issuer of Q tile t is warp WARP_MMA + t
+constexpr int WARP_TMA = NQT;                        // TMA producer
+constexpr int WARP_SOFTMAX0 = NQT + 1;               // softmax warps of Q tile t: WARP_SOFTMAX0 + 4t ..
 constexpr int NTHREADS = (NUM_SOFTMAX_WARPS + 1 + NQT) * 32;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float RESCALE_LOG2 = 8.0f;         // keep a stale max while the growth is <= 2^8
@@ -349,7 +354,7 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
         for (int i = max(0, it - STAGES); i < it; ++i) drain_wait(bar_kv_full(i % STAGES), (i / STAGES) & 1);
       }
     }
-  } else if (warp >= WARP_MMA) {
+  } else if (warp < WARP_MMA + NQT) {
     // ================================================================ MMA issuers
     // Warp WARP_MMA + t issues the MMAs of Q tile t; per key tile j its step is
     // PV_t(j) (P_t from tensor memory) then S_t(j+1).  The tensor core takes a
@@ -477,7 +482,7 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     }
   } else {
     // ================================================================ softmax + epilogue
-    const int t = warp / 4;
+    const int t = (warp - WARP_SOFTMAX0) / 4;
     const int quad = warp % 4;
     const uint32_t lane_sel = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t s_addr = tmem + lane_sel + s_col(t);
