@@ -10,8 +10,9 @@
 // Agent 来优化"; here each stage is mapped onto Blackwell hardware:
 //
 //   * persistent CTAs (one per SM) walk a list of work units — two 128-row Q
-//     tiles of one (batch, head); causal lists put the longest units first —
-//     and stream 128-key K/V tiles through a 5-slot TMA ring (128-byte
+//     tiles of one (batch, head); causal lists put the longest units first and
+//     passes over the list alternate the direction in which units are dealt
+//     to the CTAs — and stream 128-key K/V tiles through a 5-slot TMA ring (128-byte
 //     swizzle, mbarrier transaction counts).  Barriers and tensor memory are set
 //     up once; the next unit's Q, K/V and first S overlap the last unit's
 //     epilogue;
@@ -233,6 +234,15 @@ __device__ __forceinline__ Unit make_unit(int w, const FwdParams& p, int n_qblk)
   return u;
 }
 
+// The unit a CTA takes in pass `pass` over the unit list: passes deal the units
+// to the CTAs alternately from the first and from the last CTA, which evens out
+// the work of longest-first (causal) lists.  Units grow with the pass, so a
+// CTA is done at its first unit past the end.
+__device__ __forceinline__ int unit_of_pass(int pass) {
+  const int c = (pass & 1) ? static_cast<int>(gridDim.x - 1 - blockIdx.x) : static_cast<int>(blockIdx.x);
+  return pass * static_cast<int>(gridDim.x) + c;
+}
+
 __device__ __forceinline__ void own_range(const Unit& u, int t, int& jb, int& je) {
   jb = t == 0 ? u.jb0 : u.jb1;
   je = t == 0 ? u.je0 : u.je1;
@@ -316,7 +326,7 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
       int it = 0;   // ring position (runs on across units)
       int nq = 0;   // units with work so far (phase of q_full / q_empty)
       bool ok = true;
-      for (int w = blockIdx.x; w < n_units && ok; w += gridDim.x) {
+      for (int pass = 0, w = unit_of_pass(0); w < n_units && ok; w = unit_of_pass(++pass)) {
         const Unit u = make_unit(w, p, n_qblk);
         if (u.j_end <= u.j_begin) continue;
         if (nq > 0 && !mbar_wait(bar_q_empty, (nq - 1) & 1, abort_flag, p.err)) { ok = false; break; }
@@ -402,7 +412,7 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
       int n_out = 0;                        // units that produced O_t so far (phase of o_full / o_empty)
       uint32_t seq = static_cast<uint32_t>(t);  // this issuer's next turn
       bool ok = true;
-      for (int w = blockIdx.x; w < n_units && ok; w += gridDim.x) {
+      for (int pass = 0, w = unit_of_pass(0); w < n_units && ok; w = unit_of_pass(++pass)) {
         const Unit u = make_unit(w, p, n_qblk);
         if (u.j_end <= u.j_begin) continue;
         int jb, je;
@@ -491,7 +501,7 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     int n_own = 0;  // own key tiles so far (phase of s_full)
     int n_out = 0;  // units that produced O_t so far (phase of o_full)
     bool ok = true;
-    for (int w = blockIdx.x; w < n_units && ok; w += gridDim.x) {
+    for (int pass = 0, w = unit_of_pass(0); w < n_units && ok; w = unit_of_pass(++pass)) {
       const Unit u = make_unit(w, p, n_qblk);
       int jb, je;
       own_range(u, t, jb, je);
