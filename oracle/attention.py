@@ -38,6 +38,12 @@ Sources (pages on softmax attention):
       block table ``[B, max_pages]`` names, for sequence b, the page of its
       logical page i, so key j of sequence b is row ``j % page_size`` of page
       ``block_table[b, j // page_size]``.
+    - an fp8 KV cache (fp8 e4m3 is on the list of data types) stores each K and
+      V element as one OCP FP8 E4M3 code; the value is the code's E4M3 value
+      times a per-tensor scale (``k_scale`` for K, ``v_scale`` for V).  E4M3:
+      bit 7 sign, bits 6-3 exponent (bias 7), bits 2-0 mantissa; exponent 0
+      encodes the subnormals ``m/8 * 2^-6``; exponent 15 with mantissa 7 is NaN;
+      there are no infinities.
 
 Every pin of this module lives in ``tests/test_oracle.py``.
 """
@@ -49,6 +55,7 @@ __all__ = [
     "visible_mask", "kv_head", "attention_forward", "attention_rows",
     "attention_probabilities", "decode_forward", "decode_split_partials",
     "decode_combine", "paged_rows", "decode_forward_paged", "attention_varlen",
+    "e4m3_to_float", "decode_forward_fp8", "decode_forward_paged_fp8",
 ]
 
 
@@ -298,6 +305,64 @@ def decode_forward_paged(q, k_pages, v_pages, block_table, seqlens, scale: float
     for b in (range(B) if batches is None else batches):
         Kb = paged_rows(k_pages, bt[b], lens[b])          # [Nk_b, Hkv, D]
         Vb = paged_rows(v_pages, bt[b], lens[b])
+        qb = _f64(q[b])
+        for h in range(Hq):
+            kh = kv_head(h, Hq, Hkv)
+            O[b, h], LSE[b, h] = _decode_one(qb[h], Kb[:, kh], Vb[:, kh], scale)
+    return O, LSE
+
+
+def e4m3_to_float(codes) -> np.ndarray:
+    """fp64 value of each OCP FP8 E4M3 code (uint8 array), from the format's
+    definition: sign bit 7, exponent bits 6-3 with bias 7, mantissa bits 2-0;
+    exponent 0 is subnormal (``m/8 * 2^-6``); code S.1111.111 is NaN."""
+    c = np.asarray(codes).astype(np.int64) & 0xFF
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = (c & 0x7).astype(np.float64)
+    mag = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2((e - 7).astype(np.float64)))
+    mag = np.where((e == 15) & (c & 0x7 == 7), np.nan, mag)
+    return sign * mag
+
+
+def decode_forward_fp8(q, k_codes, v_codes, k_scale: float, v_scale: float, seqlens, scale: float,
+                       batches=None):
+    """Decode against an fp8 (E4M3) cache ``[B,Nk_max,Hkv,D]`` of codes: the
+    plain decode of :func:`decode_forward` on the values ``code * k_scale`` /
+    ``code * v_scale`` (only each sequence's first ``Nk_b`` rows are decoded)."""
+    B, Hq, D = q.shape
+    Hkv = k_codes.shape[2]
+    lens = [int(x) for x in seqlens]
+    kc, vc = np.asarray(k_codes), np.asarray(v_codes)
+    O = np.zeros((B, Hq, vc.shape[3]))
+    LSE = np.zeros((B, Hq))
+    for b in (range(B) if batches is None else batches):
+        Kb = e4m3_to_float(kc[b, :lens[b]]) * float(k_scale)
+        Vb = e4m3_to_float(vc[b, :lens[b]]) * float(v_scale)
+        qb = _f64(q[b])
+        for h in range(Hq):
+            kh = kv_head(h, Hq, Hkv)
+            O[b, h], LSE[b, h] = _decode_one(qb[h], Kb[:, kh], Vb[:, kh], scale)
+    return O, LSE
+
+
+def decode_forward_paged_fp8(q, k_pages, v_pages, k_scale: float, v_scale: float, block_table,
+                             seqlens, scale: float, batches=None):
+    """:func:`decode_forward_paged` on a paged cache of E4M3 codes, values as in
+    :func:`decode_forward_fp8`."""
+    B, Hq, D = q.shape
+    kp, vp = np.asarray(k_pages), np.asarray(v_pages)
+    Hkv = kp.shape[2]
+    page_size = kp.shape[1]
+    bt = np.asarray(block_table)
+    lens = [int(x) for x in seqlens]
+    O = np.zeros((B, Hq, vp.shape[3]))
+    LSE = np.zeros((B, Hq))
+    for b in (range(B) if batches is None else batches):
+        j = np.arange(lens[b])
+        page = bt[b][j // page_size]
+        Kb = e4m3_to_float(kp[page, j % page_size]) * float(k_scale)
+        Vb = e4m3_to_float(vp[page, j % page_size]) * float(v_scale)
         qb = _f64(q[b])
         for h in range(Hq):
             kh = kv_head(h, Hq, Hkv)

@@ -336,9 +336,93 @@ def pin_golden(ora):
     assert abs(Lc[0, 0] - G[("split2", "combinedLSE")][0][0]) < 1e-14
 
 
+def _golden_e4m3():
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "e4m3_codes.txt")
+    out = []
+    for line in open(path):
+        if line.startswith("#") or not line.strip():
+            continue
+        code, expr = line.split()
+        out.append((int(code, 16), float("nan") if expr == "nan" else float(eval(expr, {"__builtins__": {}}))))
+    return out
+
+
+def pin_e4m3_codes(ora):
+    """E4M3 decoding against the hand-derived codes of tests/golden/e4m3_codes.txt
+    (format definition) and against torch's float8_e4m3fn conversion for all 256
+    codes (an independent implementation of the same format)."""
+    for code, want in _golden_e4m3():
+        got = float(ora.e4m3_to_float(np.array([code], dtype=np.uint8))[0])
+        if math.isnan(want):
+            assert math.isnan(got), (hex(code), got)
+        else:
+            assert got == want and math.copysign(1.0, got) == math.copysign(1.0, want), (hex(code), got, want)
+    codes = np.arange(256, dtype=np.uint8)
+    mine = ora.e4m3_to_float(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(np.isnan(mine), np.isnan(ref))
+    fin = ~np.isnan(ref)
+    assert np.array_equal(mine[fin], ref[fin])
+
+
+def pin_fp8_decode(ora):
+    """fp8-cache decode: brute force (math.fsum) on the decoded values for a tiny
+    case, the folding of k_scale into the score scale and of v_scale into O, and
+    paged == contiguous on pages laid out in a random order."""
+    rng = np.random.default_rng(5)
+    B, Hq, Hkv, D, nmax = 2, 4, 2, 8, 11
+    lens = [11, 5]
+    q = rng.standard_normal((B, Hq, D))
+    kc = rng.integers(0, 256, (B, nmax, Hkv, D), dtype=np.uint8)
+    vc = rng.integers(0, 256, (B, nmax, Hkv, D), dtype=np.uint8)
+    kc[(kc & 0x7F) == 0x7F] = 0x3A          # no NaN codes in the valid rows
+    vc[(vc & 0x7F) == 0x7F] = 0x41
+    kc[1, 5:] = 0x7F                         # NaN codes past sequence 1: never read
+    vc[1, 5:] = 0xFF
+    ks, vs, sc = 0.0625, 0.25, 0.3
+    O, L = ora.decode_forward_fp8(q, kc, vc, ks, vs, lens, sc)
+    # brute force from the format definition, one element at a time
+    def val(c):
+        c = int(c)
+        sgn = -1.0 if c & 0x80 else 1.0
+        e, m = (c >> 3) & 15, c & 7
+        return sgn * ((m / 8) * 2.0 ** -6 if e == 0 else (1 + m / 8) * 2.0 ** (e - 7))
+    for b in range(B):
+        for h in range(Hq):
+            kh = h // (Hq // Hkv)
+            s = [sc * math.fsum(q[b, h, d] * val(kc[b, j, kh, d]) * ks for d in range(D)) for j in range(lens[b])]
+            mx = max(s)
+            w = [math.exp(x - mx) for x in s]
+            den = math.fsum(w)
+            for d in range(D):
+                o = math.fsum(w[j] * val(vc[b, j, kh, d]) * vs for j in range(lens[b])) / den
+                assert abs(O[b, h, d] - o) < 1e-12 * max(1.0, abs(o)), (b, h, d)
+            assert abs(L[b, h] - (mx + math.log(den))) < 1e-12
+    O2, L2 = ora.decode_forward_fp8(q, kc, vc, 1.0, vs, lens, sc * ks)
+    assert np.allclose(O2, O, rtol=1e-13, atol=1e-13) and np.allclose(L2, L, rtol=1e-13, atol=1e-13)
+    O3, L3 = ora.decode_forward_fp8(q, kc, vc, ks, 3 * vs, lens, sc)
+    assert np.allclose(O3, 3 * O, rtol=1e-13, atol=1e-13) and np.allclose(L3, L, rtol=1e-13, atol=1e-13)
+    page = 4
+    need = [-(-n // page) for n in lens]
+    perm = rng.permutation(sum(need) + 2)
+    kp = np.full((len(perm), page, Hkv, D), 0x7F, dtype=np.uint8)
+    vp = np.full((len(perm), page, Hkv, D), 0xFF, dtype=np.uint8)
+    bt = np.zeros((B, max(need)), dtype=np.int32)
+    nxt = 0
+    for b in range(B):
+        for i in range(need[b]):
+            pg = int(perm[nxt]); nxt += 1
+            bt[b, i] = pg
+            rows = min(page, lens[b] - i * page)
+            kp[pg, :rows] = kc[b, i * page: i * page + rows]
+            vp[pg, :rows] = vc[b, i * page: i * page + rows]
+    O4, L4 = ora.decode_forward_paged_fp8(q, kp, vp, ks, vs, bt, lens, sc)
+    assert np.allclose(O4, O, rtol=1e-13, atol=1e-13) and np.allclose(L4, L, rtol=1e-13, atol=1e-13)
+
+
 PINS = [pin_brute_force, pin_sdpa, pin_zero_query, pin_single_key, pin_probability_rows,
         pin_causal_first_row, pin_dominant_key, pin_invariants, pin_decode, pin_paged_decode, pin_varlen,
-        pin_golden]
+        pin_golden, pin_e4m3_codes, pin_fp8_decode]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
@@ -431,6 +515,36 @@ def _mut_paged_rows_swapped(pages, block_table_b, n):
     return np.asarray(pages[page, j // page_size], dtype=np.float64) if n else np.zeros((0,) + tuple(pages.shape[2:]))
 
 
+def _mut_e4m3_bias8(codes):
+    c = np.asarray(codes).astype(np.int64) & 0xFF
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e, m = (c >> 3) & 0xF, (c & 0x7).astype(np.float64)
+    mag = np.where(e == 0, m / 8.0 * 2.0 ** -7, (1.0 + m / 8.0) * np.exp2((e - 8).astype(np.float64)))
+    return sign * np.where((e == 15) & (c & 0x7 == 7), np.nan, mag)
+
+
+def _mut_e4m3_no_subnormals(codes):
+    c = np.asarray(codes).astype(np.int64) & 0xFF
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e, m = (c >> 3) & 0xF, (c & 0x7).astype(np.float64)
+    mag = (1.0 + m / 8.0) * np.exp2((e - 7).astype(np.float64))
+    return sign * np.where((e == 15) & (c & 0x7 == 7), np.nan, mag)
+
+
+def _mut_fp8_paged_swapped(q, k_pages, v_pages, k_scale, v_scale, block_table, seqlens, scale, batches=None):
+    kp, vp = np.asarray(k_pages), np.asarray(v_pages)
+    page = kp.shape[1]
+    perm = [np.asarray(block_table)[b] for b in range(len(seqlens))]
+    B, Hq, D = q.shape
+    kc = np.zeros((B, int(max(seqlens)), kp.shape[2], kp.shape[3]), dtype=np.uint8)
+    vc = np.zeros_like(kc)
+    for b, n in enumerate(int(x) for x in seqlens):
+        j = np.arange(n)
+        kc[b, :n] = kp[perm[b][j % page] % kp.shape[0], j // page]
+        vc[b, :n] = vp[perm[b][j % page] % vp.shape[0], j // page]
+    return ORA.decode_forward_fp8(q, kc, vc, k_scale, v_scale, seqlens, scale, batches)
+
+
 MUTANTS = {
     "no_scale": ("_scores", _mut_no_scale),
     "sqrt_scale": ("_scores", _mut_sqrt_scale),
@@ -443,6 +557,9 @@ MUTANTS = {
     "softmax_over_queries": ("_softmax_rows", _wrap_softmax("key_axis_swapped")),
     "combine_unweighted": ("decode_combine", _mut_combine_unweighted),
     "paged_index_swapped": ("paged_rows", _mut_paged_rows_swapped),
+    "e4m3_bias_8": ("e4m3_to_float", _mut_e4m3_bias8),
+    "e4m3_no_subnormals": ("e4m3_to_float", _mut_e4m3_no_subnormals),
+    "fp8_paged_index_swapped": ("decode_forward_paged_fp8", _mut_fp8_paged_swapped),
 }
 
 
