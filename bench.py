@@ -44,6 +44,7 @@ METRIC = "attn-fwd TFLOP/s & % of BF16 tensor peak; split-KV decode HBM GB/s"
 MAIN = dict(B=1, Hq=32, Hkv=32, N=8192, D=128, causal=False)
 CAUSAL = dict(B=4, Hq=32, Hkv=8, N=4096, D=128, causal=True)
 DECODE = dict(B=64, Hq=32, Hkv=8, D=128, nk_lo=512, nk_hi=32768, chunk=512)
+DECODE_NAMES = ("decode", "paged", "decode_fp8")
 FP32 = dict(B=2, Hq=8, Hkv=8, N=4096, D=128, causal=False)
 # widened prefill workloads: sliding window, chunked prefill (Nq < Nk), head dim 64
 WINDOW = dict(B=1, Hq=32, Hkv=8, Nq=16384, Nk=16384, D=128, causal=True, window=4096)
@@ -84,7 +85,7 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--workload", choices=["dense", "causal", "decode", "fp32", "window", "chunked", "d64",
-                                           "paged", "fp16", "varlen"],
+                                           "paged", "fp16", "varlen", "decode_fp8"],
                     default="dense",
                     help="workload of the timed loop (default: the dense bf16 prefill)")
     ap.add_argument("--no-extras", action="store_true", help="skip the other workloads")
@@ -268,6 +269,8 @@ WORKLOAD_NAMES = {
     "fp16": "fp16 dense prefill B=1 H=32 N=8192 D=128 (non-causal)",
     "varlen": "bf16 ragged causal prefill, 32 sequences of U[512,8192] tokens, Hq=32 Hkv=8 D=128",
     "paged": "bf16 split-KV decode on a paged cache (page 256) B=64 Hq=32 Hkv=8 D=128, Nk_b~U[512,32768], chunk 512",
+    "decode_fp8": "split-KV decode on an fp8 E4M3 KV cache (bf16 Q) B=64 Hq=32 Hkv=8 D=128, Nk_b~U[512,32768], "
+                  "chunk 512",
 }
 
 
@@ -333,6 +336,21 @@ def make_workload(name, dev, seed, peaks, peak_src, sm_max_mhz, decode_batch=Non
             w["fn"] = lambda: binding.attn_decode(q, kc, vc, sl_d, ws, o, lse, chunk=d["chunk"])
             w["split_fn"] = lambda: binding.attn_decode_splitkv(q, kc, vc, sl_d, ws, chunk=d["chunk"])
             extra_in = [(sl, sl_d), (None, kc), (None, vc)]
+        elif name == "decode_fp8":
+            qh, kc, vc, sl = inputs.decode_inputs(d["B"], d["Hq"], d["Hkv"], d["D"], d["nk_lo"], d["nk_hi"],
+                                                  seed=seed, device=dev, kv_dtype="e4m3")
+            q, sl_d = qh.to(dev), sl.to(dev)
+            w["fn"] = lambda: binding.attn_decode_fp8(q, kc, vc, sl_d, 1.0, 1.0, ws, o, lse, chunk=d["chunk"])
+            lib = binding.lib()
+
+            def split_fp8():
+                rc = lib.attn_decode_splitkv_fp8(
+                    binding._ptr(q), binding._ptr(kc), binding._ptr(vc), 1.0, 1.0, binding._ptr(sl_d),
+                    binding._ptr(ws), d["B"], d["Hq"], d["Hkv"], d["nk_hi"], d["D"], 1 / math.sqrt(d["D"]),
+                    d["chunk"], binding._stream(None))
+                assert rc == 0
+            w["split_fn"] = split_fp8
+            extra_in = [(sl, sl_d), (None, kc), (None, vc)]
         else:
             qh, kc, vc, bt, sl = inputs.paged_decode_inputs(d["B"], d["Hq"], d["Hkv"], d["D"], d["nk_lo"],
                                                             d["nk_hi"], 256, seed=seed, device=dev)
@@ -348,12 +366,13 @@ def make_workload(name, dev, seed, peaks, peak_src, sm_max_mhz, decode_batch=Non
                 assert rc == 0
             w["split_fn"] = split_paged
             extra_in = [(sl, sl_d), (bt, bt_d), (None, kc), (None, vc)]
-        kv_bytes = int(sl.sum()) * d["Hkv"] * d["D"] * 2 * 2
+        kv_elem = 1 if name == "decode_fp8" else 2
+        kv_bytes = int(sl.sum()) * d["Hkv"] * d["D"] * kv_elem * 2
         w["kv_bytes"] = kv_bytes
         w["work"] = kv_bytes + q.numel() * 2 + o.numel() * 2 + lse.numel() * 4
         w["unit"] = "GB/s"
         w["launches"] = 2
-        w["dtype"] = "bf16"
+        w["dtype"] = "e4m3" if name == "decode_fp8" else "bf16"
         w["seq_len"], w["batch"] = d["nk_hi"], d["B"]
         w["bound"] = "hbm"
         w["peak"] = peaks["hbm_gbs"]
@@ -417,7 +436,7 @@ def run_gb300(args, rank, world, local_rank):
     clocks = clk.summary()
     ms_step = max_over_ranks(sum(ms) / len(ms))
     value = world * rate(w, ms_step)
-    if w["name"] in ("decode", "paged"):   # roofline of the dominant kernel: the split-KV partial step
+    if w["name"] in DECODE_NAMES:   # roofline of the dominant kernel: the split-KV partial step
         ms_k = max_over_ranks(statistics.mean(time_steps(torch, w["split_fn"], min(args.steps, 50), 3, flush, stream)))
         achieved = w["kv_bytes"] / (ms_k * 1e-3) / 1e9
         traffic = None
@@ -434,11 +453,11 @@ def run_gb300(args, rank, world, local_rank):
         pins = [(x.pin_memory() if x is not None else torch.empty(t.shape, dtype=t.dtype).pin_memory(), t)
                 for x, t in w["e2e_in"]]
         outs = [(torch.empty(t.shape, dtype=t.dtype).pin_memory(), t) for t in w["e2e_out"]]
-        if w["name"] in ("decode", "paged"):   # the host copy of the caches is the device draw
+        if w["name"] in DECODE_NAMES:   # the host copy of the caches is the device draw
             for (x, t), (hp, _) in zip(w["e2e_in"], pins):
                 if x is None:
                     hp.copy_(t)
-        e2e_steps = max(5, min(args.steps, 100 if w["name"] not in ("decode", "paged") else 10))
+        e2e_steps = max(5, min(args.steps, 100 if w["name"] not in DECODE_NAMES else 10))
 
         def e2e_step():
             for hp, t in pins:
@@ -474,7 +493,8 @@ def run_gb300(args, rank, world, local_rank):
     workloads = {}
     if not args.no_extras:
         xs = max(5, min(args.steps // 10, 50))
-        for name in ("dense", "causal", "decode", "paged", "fp32", "window", "chunked", "d64", "fp16", "varlen"):
+        for name in ("dense", "causal", "decode", "paged", "decode_fp8", "fp32", "window", "chunked", "d64", "fp16",
+                     "varlen"):
             if name == args.workload:
                 continue
             x = make_workload(name, dev, rank, peaks, peak_src, sm_max, args.decode_batch)
@@ -482,7 +502,7 @@ def run_gb300(args, rank, world, local_rank):
             r = rate(x, mx)
             entry = {"workload": x["desc"], "value": world * r, "unit": x["unit"], "ms_per_step": mx,
                      "bound": x["bound"], "frac": r / x["peak"], "peak": x["peak"], "peak_source": x["peak_source"]}
-            if name in ("decode", "paged"):
+            if name in DECODE_NAMES:
                 mk = max_over_ranks(statistics.mean(time_steps(torch, x["split_fn"], xs, 3, flush, stream)))
                 entry["splitkv_kernel_ms"] = mk
                 entry["splitkv_kernel_gbs"] = x["kv_bytes"] / (mk * 1e-3) / 1e9

@@ -180,6 +180,43 @@ int attn_decode_splitkv_paged(const void* q, const void* k_pages, const void* v_
                               int D, float scale, int chunk, attn_stream_t stream);
 
 /*
+ * attn_decode_splitkv_fp8 — split-KV decode, partial step, on an fp8 KV cache.
+ *   [ASK] "研究动机" (bf16/fp16/fp8 data types, fp8-KV decode shapes).
+ *
+ *   k_cache, v_cache : uint8 [B, Nk_max, Hkv, D] (device), one OCP FP8 E4M3 code
+ *                      per element (sign bit 7, exponent bits 6-3 with bias 7,
+ *                      mantissa bits 2-0; S.1111.111 is NaN).  The element's
+ *                      value is its E4M3 value times k_scale (K) or v_scale (V).
+ *   k_scale, v_scale : per-tensor dequantisation scales (host floats, finite, > 0)
+ *   q, seqlens, workspace and every other argument, the workspace layout and the
+ *   results are those of attn_decode_splitkv (q stays bf16; combine with
+ *   attn_decode_combine).  The arithmetic runs in fp32 on the exact decoded
+ *   values.  Cache rows at or past seqlens[b] are never weighted, whatever
+ *   codes they hold.
+ *   Errors: as attn_decode_splitkv; ATTN_ERR_SCALE also for a k_scale or v_scale
+ *   that is not finite or not > 0.
+ */
+int attn_decode_splitkv_fp8(const void* q, const void* k_cache, const void* v_cache,
+                            float k_scale, float v_scale, const int* seqlens, void* workspace,
+                            int B, int Hq, int Hkv, int Nk_max, int D, float scale, int chunk,
+                            attn_stream_t stream);
+
+/*
+ * attn_decode_splitkv_paged_fp8 — split-KV decode, partial step, on a paged fp8
+ * KV cache.   [ASK] "研究动机" (paged caches, fp8 data types).
+ *
+ *   k_pages, v_pages : uint8 [num_pages, page_size, Hkv, D] E4M3 codes, values
+ *                      as in attn_decode_splitkv_fp8
+ *   Every other argument, the block-table rules and the errors are those of
+ *   attn_decode_splitkv_paged plus the scale checks of attn_decode_splitkv_fp8.
+ */
+int attn_decode_splitkv_paged_fp8(const void* q, const void* k_pages, const void* v_pages,
+                                  float k_scale, float v_scale, const int* block_table,
+                                  const int* seqlens, void* workspace, int B, int Hq, int Hkv,
+                                  int num_pages, int page_size, int max_pages, int D, float scale,
+                                  int chunk, attn_stream_t stream);
+
+/*
  * attn_decode_combine — split-KV decode, combine step.  LSE-weighted merge of
  * the chunk results written by attn_decode_splitkv:
  *   M = max_c LSE_c,  w_c = exp(LSE_c - M),  O = sum_c w_c O_c / sum_c w_c,

@@ -32,6 +32,10 @@ SIGNATURES = {
     "attn_decode_combine": (_c_int, [_vp] * 4 + [_c_int] * 5 + [_vp]),
     "attn_decode_splitkv_paged": (_c_int, [_vp] * 6 + [_c_int] * 7 + [_c_float, _c_int, _vp]),
     "attn_decode_noalloc": (_c_int, [_vp] * 6 + [_c_int] * 5 + [_c_float, _c_int, _vp]),
+    "attn_decode_splitkv_fp8": (_c_int, [_vp] * 3 + [_c_float] * 2 + [_vp] * 2 + [_c_int] * 5
+                                + [_c_float, _c_int, _vp]),
+    "attn_decode_splitkv_paged_fp8": (_c_int, [_vp] * 3 + [_c_float] * 2 + [_vp] * 3 + [_c_int] * 7
+                                      + [_c_float, _c_int, _vp]),
     "attn_get_device_error": (_c_int, [_vp]),
     "attn_strerror": (ctypes.c_char_p, [_c_int]),
 }
@@ -226,6 +230,68 @@ def attn_decode_paged(q, k_pages, v_pages, block_table, seqlens, workspace=None,
                                            _ptr(seqlens), _ptr(workspace), B, Hq, Hkv, num_pages,
                                            page_size, max_pages, D, scale, int(chunk), _stream(stream))
     _check(code, "attn_decode_splitkv_paged")
+    return attn_decode_combine(workspace, seqlens, B, Hq, nk_max, D, o, lse, chunk, q.device, stream)
+
+
+def _require_fp8(t, name):
+    """fp8 E4M3 cache tensor: uint8 codes or torch.float8_e4m3fn, CUDA, contiguous."""
+    import torch
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype not in (torch.uint8, torch.float8_e4m3fn):
+        raise TypeError(f"{name} must hold E4M3 codes (uint8 or float8_e4m3fn), got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def attn_decode_fp8(q, k_cache, v_cache, seqlens, k_scale=1.0, v_scale=1.0, workspace=None, o=None,
+                    lse=None, scale=None, chunk=512, stream=None):
+    """Split-KV decode on an fp8 E4M3 cache ``[B,Nk_max,Hkv,D]`` (values = code * scale):
+    partial step, then combine step."""
+    import torch
+    _require(q, torch.bfloat16, "q")
+    _require_fp8(k_cache, "k_cache")
+    _require_fp8(v_cache, "v_cache")
+    _require(seqlens, torch.int32, "seqlens")
+    B, Hq, D = q.shape
+    _, Nk_max, Hkv, _ = k_cache.shape
+    need = attn_decode_workspace_size(B, Hq, D, Nk_max, chunk)
+    if workspace is None:
+        workspace = torch.empty(need, device=q.device, dtype=torch.uint8)
+    if workspace.numel() * workspace.element_size() < need:
+        raise ValueError(f"workspace holds fewer than {need} bytes")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    code = lib().attn_decode_splitkv_fp8(_ptr(q), _ptr(k_cache), _ptr(v_cache), float(k_scale),
+                                         float(v_scale), _ptr(seqlens), _ptr(workspace), B, Hq, Hkv,
+                                         Nk_max, D, scale, int(chunk), _stream(stream))
+    _check(code, "attn_decode_splitkv_fp8")
+    return attn_decode_combine(workspace, seqlens, B, Hq, Nk_max, D, o, lse, chunk, q.device, stream)
+
+
+def attn_decode_paged_fp8(q, k_pages, v_pages, block_table, seqlens, k_scale=1.0, v_scale=1.0,
+                          workspace=None, o=None, lse=None, scale=None, chunk=512, stream=None):
+    """Split-KV decode on a paged fp8 E4M3 cache ``[num_pages,page_size,Hkv,D]``."""
+    import torch
+    _require(q, torch.bfloat16, "q")
+    _require_fp8(k_pages, "k_pages")
+    _require_fp8(v_pages, "v_pages")
+    _require(block_table, torch.int32, "block_table")
+    _require(seqlens, torch.int32, "seqlens")
+    B, Hq, D = q.shape
+    num_pages, page_size, Hkv, _ = k_pages.shape
+    max_pages = block_table.shape[1]
+    nk_max = max_pages * page_size
+    need = attn_decode_workspace_size(B, Hq, D, nk_max, chunk)
+    if workspace is None:
+        workspace = torch.empty(need, device=q.device, dtype=torch.uint8)
+    if workspace.numel() * workspace.element_size() < need:
+        raise ValueError(f"workspace holds fewer than {need} bytes")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    code = lib().attn_decode_splitkv_paged_fp8(_ptr(q), _ptr(k_pages), _ptr(v_pages), float(k_scale),
+                                               float(v_scale), _ptr(block_table), _ptr(seqlens),
+                                               _ptr(workspace), B, Hq, Hkv, num_pages, page_size,
+                                               max_pages, D, scale, int(chunk), _stream(stream))
+    _check(code, "attn_decode_splitkv_paged_fp8")
     return attn_decode_combine(workspace, seqlens, B, Hq, nk_max, D, o, lse, chunk, q.device, stream)
 
 

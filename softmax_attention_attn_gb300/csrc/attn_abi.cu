@@ -232,6 +232,50 @@ int attn_decode_splitkv_paged(const void* q, const void* k_pages, const void* v_
                                      dev->num_sms, reinterpret_cast<cudaStream_t>(stream), dev->err);
 }
 
+int attn_decode_splitkv_fp8(const void* q, const void* k_cache, const void* v_cache, float k_scale,
+                            float v_scale, const int* seqlens, void* workspace, int B, int Hq,
+                            int Hkv, int Nk_max, int D, float scale, int chunk,
+                            attn_stream_t stream) {
+  if (!q || !k_cache || !v_cache || !seqlens || !workspace) return ATTN_ERR_NULL;
+  int rc = check_decode(B, Hq, Hkv, Nk_max, D, chunk);
+  if (rc != ATTN_OK) return rc;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(workspace) ||
+      !aligned16(seqlens))
+    return ATTN_ERR_ALIGN;
+  if (!std::isfinite(scale) || !(scale > 0.f) || !std::isfinite(k_scale) || !(k_scale > 0.f) ||
+      !std::isfinite(v_scale) || !(v_scale > 0.f))
+    return ATTN_ERR_SCALE;
+  DeviceInfo* dev = nullptr;
+  if ((rc = device_info(&dev)) != ATTN_OK) return rc;
+  return launch_decode_splitkv(q, k_cache, v_cache, seqlens, workspace, B, Hq, Hkv, Nk_max, scale,
+                               chunk, dev->num_sms, reinterpret_cast<cudaStream_t>(stream), dev->err,
+                               1, k_scale, v_scale);
+}
+
+int attn_decode_splitkv_paged_fp8(const void* q, const void* k_pages, const void* v_pages,
+                                  float k_scale, float v_scale, const int* block_table,
+                                  const int* seqlens, void* workspace, int B, int Hq, int Hkv,
+                                  int num_pages, int page_size, int max_pages, int D, float scale,
+                                  int chunk, attn_stream_t stream) {
+  if (!q || !k_pages || !v_pages || !block_table || !seqlens || !workspace) return ATTN_ERR_NULL;
+  if (num_pages <= 0 || max_pages <= 0 || page_size <= 0 || page_size % 64 != 0) return ATTN_ERR_DIM;
+  if (static_cast<long long>(max_pages) * page_size > 0x7fffffffLL) return ATTN_ERR_DIM;
+  int rc = check_decode(B, Hq, Hkv, max_pages * page_size, D, chunk);
+  if (rc != ATTN_OK) return rc;
+  if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(workspace) ||
+      !aligned16(seqlens) || !aligned16(block_table))
+    return ATTN_ERR_ALIGN;
+  if (!std::isfinite(scale) || !(scale > 0.f) || !std::isfinite(k_scale) || !(k_scale > 0.f) ||
+      !std::isfinite(v_scale) || !(v_scale > 0.f))
+    return ATTN_ERR_SCALE;
+  DeviceInfo* dev = nullptr;
+  if ((rc = device_info(&dev)) != ATTN_OK) return rc;
+  return launch_decode_splitkv_paged(q, k_pages, v_pages, block_table, seqlens, workspace, B, Hq,
+                                     Hkv, num_pages, page_size, max_pages, scale, chunk,
+                                     dev->num_sms, reinterpret_cast<cudaStream_t>(stream), dev->err,
+                                     1, k_scale, v_scale);
+}
+
 int attn_decode_combine(const void* workspace, const int* seqlens, void* o, float* lse, int B,
                         int Hq, int Nk_max, int D, int chunk, attn_stream_t stream) {
   if (!workspace || !seqlens || !o) return ATTN_ERR_NULL;

@@ -14,8 +14,13 @@
 //     round trip); the KV heads of one chunk are adjacent items, so
 //     neighbouring CTAs read neighbouring 256-byte rows of the cache;
 //   * one producer thread streams 64-key K and V tiles ([64 keys][128] bf16,
-//     16 KB) through a 5-slot TMA ring, so 80 KB per CTA (two CTAs per SM)
-//     are in flight;
+//     16 KB, through a 5-slot TMA ring; or [64 keys][128] fp8 E4M3 codes,
+//     8 KB, through a 10-slot ring), so 80 KB per CTA (two CTAs per SM) are in
+//     flight;
+//   * an fp8 cache holds E4M3 codes whose values are code * k_scale (K) and
+//     code * v_scale (V): codes convert exactly to fp32 (through f16, which
+//     holds every E4M3 value), k_scale folds into the softmax scale and v_scale
+//     scales each chunk's output;
 //   * four consumer warps: all G = Hq/Hkv query heads of the KV head share
 //     each K/V tile.  For the scores, a thread multiplies 16 bytes of 8 key
 //     rows by the G query slices it holds in registers and a 16-lane
@@ -23,6 +28,7 @@
 //     one shuffle per score.  The chunk's softmax runs in shared memory in the
 //     exp2 domain; P V accumulates per thread and is reduced across the eight
 //     key groups through shared memory.
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <math_constants.h>
 
@@ -34,8 +40,17 @@ namespace decode {
 
 constexpr int HD = 128;
 constexpr int TILE = 64;                      // keys per TMA tile
-constexpr int TILE_BYTES = TILE * HD * 2;     // 16 KB
-constexpr int STAGES = 5;
+constexpr int RING_BYTES = 5 * TILE * HD * 2; // 80 KB of K/V tiles in flight per CTA
+constexpr int MAX_STAGES = 10;
+
+// Ring geometry for a bf16 (KV8 = false) or fp8 E4M3 (KV8 = true) cache.
+template <bool KV8>
+struct Ring {
+  static constexpr int ROW_BYTES = KV8 ? HD : 2 * HD;  // one key row of one KV head
+  static constexpr int TILE_BYTES = TILE * ROW_BYTES;
+  static constexpr int STAGES = RING_BYTES / TILE_BYTES;
+  static_assert(STAGES <= MAX_STAGES, "ring slots");
+};
 constexpr int NCW = 4;                        // consumer warps
 constexpr int NC = NCW * 32;                  // consumer threads
 constexpr int NTHREADS = NC + 32;             // + producer warp
@@ -47,12 +62,12 @@ struct Layout {
 __host__ __device__ inline Layout layout(int G, int chunk, int B) {
   Layout L;
   L.ring = 0;
-  L.work = L.ring + STAGES * TILE_BYTES;
+  L.work = L.ring + RING_BYTES;
   const int scores = G * chunk * 4;
   const int red = 8 * G * HD * 4;
   L.stats = L.work + (scores > red ? scores : red);
   L.bars = L.stats + 2 * 8 * 4;                // m[8], l[8]
-  L.misc = L.bars + 2 * STAGES * 8;
+  L.misc = L.bars + 2 * MAX_STAGES * 8;
   L.split = L.misc + 16;                       // misc: abort flag, stop flag
   L.bytes = L.split + (B + 1) * 4;
   return L;
@@ -90,17 +105,48 @@ __device__ __forceinline__ void bf16x8_to_float(const uint4& u, float (&f)[8]) {
   }
 }
 
+// Eight E4M3 codes (the bytes of u, lowest first) to fp32.  Every E4M3 value
+// is exact in f16, so the conversion is exact.
+__device__ __forceinline__ void e4m3x8_to_float(const uint2& u, float (&f)[8]) {
+  const uint32_t w[2] = {u.x, u.y};
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    uint32_t h01, h23;
+    asm("{\n\t.reg .b16 lo, hi;\n\t"
+        "mov.b32 {lo, hi}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, lo;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
+        : "=r"(h01), "=r"(h23)
+        : "r"(w[i]));
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&h01));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&h23));
+    f[4 * i + 0] = a.x;
+    f[4 * i + 1] = a.y;
+    f[4 * i + 2] = b.x;
+    f[4 * i + 3] = b.y;
+  }
+}
+
+// The 8 elements [g16 * 8, g16 * 8 + 8) of key row `key` of a ring tile, as fp32.
+template <bool KV8>
+__device__ __forceinline__ void row_slice(const uint8_t* tile, int key, int g16, float (&f)[8]) {
+  if constexpr (KV8) {
+    e4m3x8_to_float(*reinterpret_cast<const uint2*>(tile + key * HD + g16 * 8), f);
+  } else {
+    bf16x8_to_float(*reinterpret_cast<const uint4*>(tile + key * (HD * 2) + g16 * 16), f);
+  }
+}
+
 // acc[h][e] += sum over the 8 keys (ksub + 8 i) of one 64-key tile of
 // p[h][key] * v[key][g16 * 8 + e].  With MASK, keys >= valid contribute 0.
-template <int G, bool MASK>
+template <int G, bool MASK, bool KV8>
 __device__ __forceinline__ void pv_tile(float (&acc)[G][8], const uint8_t* tile, const float* pt,
                                         int chunk, int ksub, int g16, int valid) {
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int key = ksub + 8 * i;
-    const uint4 u = *reinterpret_cast<const uint4*>(tile + key * (HD * 2) + g16 * 16);
     float vf[8];
-    bf16x8_to_float(u, vf);
+    row_slice<KV8>(tile, key, g16, vf);
     if (MASK && key >= valid) {
 #pragma unroll
       for (int e = 0; e < 8; ++e) vf[e] = 0.f;
@@ -145,14 +191,16 @@ struct Paging {
   int max_pages, page_size, num_pages;
 };
 
-template <int G, bool PAGED>
+template <int G, bool PAGED, bool KV8>
 __global__ void __launch_bounds__(NTHREADS, 2)
 attn_decode_splitkv_kernel(const __grid_constant__ CUtensorMap tm_k,
                            const __grid_constant__ CUtensorMap tm_v,
                            const __nv_bfloat16* __restrict__ q, const int* __restrict__ seqlens,
                            float* __restrict__ ws_o, float* __restrict__ ws_lse, int B, int Hq,
-                           int Hkv, int Nk_max, int chunk, int S_max, float c_log2, int* err,
-                           const Paging pg) {
+                           int Hkv, int Nk_max, int chunk, int S_max, float c_log2, float v_scale,
+                           int* err, const Paging pg) {
+  constexpr int STAGES = Ring<KV8>::STAGES;
+  constexpr int TILE_BYTES = Ring<KV8>::TILE_BYTES;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -289,9 +337,8 @@ attn_decode_splitkv_kernel(const __grid_constant__ CUtensorMap tm_k,
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int key = ksub + 8 * i;
-        const uint4 u = *reinterpret_cast<const uint4*>(tile + key * (HD * 2) + g16 * 16);
         float kf[8];
-        bf16x8_to_float(u, kf);
+        row_slice<KV8>(tile, key, g16, kf);
 #pragma unroll
         for (int h = 0; h < G; ++h) {
           float a = 0.f;
@@ -354,9 +401,9 @@ attn_decode_splitkv_kernel(const __grid_constant__ CUtensorMap tm_k,
       // 0 * NaN from an unused cache row is not).
       const int valid_here = wk.n_valid - tl * TILE;
       if (valid_here >= TILE)
-        pv_tile<G, false>(acc, tile, pt, chunk, ksub, g16, TILE);
+        pv_tile<G, false, KV8>(acc, tile, pt, chunk, ksub, g16, TILE);
       else
-        pv_tile<G, true>(acc, tile, pt, chunk, ksub, g16, valid_here);
+        pv_tile<G, true, KV8>(acc, tile, pt, chunk, ksub, g16, valid_here);
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_empty(s));
     }
@@ -377,7 +424,7 @@ attn_decode_splitkv_kernel(const __grid_constant__ CUtensorMap tm_k,
         float o = 0.f;
 #pragma unroll
         for (int k = 0; k < 8; ++k) o += red[(k * G + h) * HD + d];
-        ws_o[(base + static_cast<size_t>(h) * S_max) * HD + d] = o / st_l[h];
+        ws_o[(base + static_cast<size_t>(h) * S_max) * HD + d] = o / st_l[h] * v_scale;
       }
       if (tid < G) ws_lse[base + static_cast<size_t>(tid) * S_max] = (st_m[tid] + log2f(st_l[tid])) * 0.69314718055994531f;
       if (tid == 0) *stop = *abort_flag;
@@ -436,10 +483,11 @@ attn_decode_combine_kernel(const float* __restrict__ ws_o, const float* __restri
   if (lane == 0 && lse != nullptr) lse[bh] = M + logf(s);
 }
 
-template <int G, bool PAGED>
+template <int G, bool PAGED, bool KV8>
 int launch_split(const CUtensorMap& tk, const CUtensorMap& tv, const void* q, const int* seqlens,
                  float* ws_o, float* ws_lse, int B, int Hq, int Hkv, int Nk_max, float scale,
-                 int chunk, int S_max, int num_sms, cudaStream_t stream, int* err, const Paging& pg) {
+                 int chunk, int S_max, int num_sms, cudaStream_t stream, int* err, const Paging& pg,
+                 float k_scale, float v_scale) {
   const Layout L = layout(G, chunk, B);
   const int smem = L.bytes + 1024;
   static int attr_dev = -1;
@@ -447,33 +495,48 @@ int launch_split(const CUtensorMap& tk, const CUtensorMap& tv, const void* q, co
   int dev = 0;
   cudaGetDevice(&dev);
   if (attr_dev != dev || attr_bytes < smem) {
-    if (cudaFuncSetAttribute(attn_decode_splitkv_kernel<G, PAGED>,
+    if (cudaFuncSetAttribute(attn_decode_splitkv_kernel<G, PAGED, KV8>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
       return ATTN_ERR_CUDA;
     attr_dev = dev;
     attr_bytes = smem;
   }
   const int grid = 2 * num_sms;
-  attn_decode_splitkv_kernel<G, PAGED><<<grid, NTHREADS, smem, stream>>>(
+  attn_decode_splitkv_kernel<G, PAGED, KV8><<<grid, NTHREADS, smem, stream>>>(
       tk, tv, static_cast<const __nv_bfloat16*>(q), seqlens, ws_o, ws_lse, B, Hq, Hkv, Nk_max, chunk,
-      S_max, scale * 1.4426950408889634f, err, pg);
+      S_max, scale * k_scale * 1.4426950408889634f, v_scale, err, pg);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
-template <bool PAGED>
+template <bool PAGED, bool KV8>
 int launch_split_any(const CUtensorMap& tk, const CUtensorMap& tv, const void* q, const int* seqlens,
                      void* workspace, int B, int Hq, int Hkv, int Nk_max, float scale, int chunk,
-                     int num_sms, cudaStream_t stream, int* err, const Paging& pg) {
+                     int num_sms, cudaStream_t stream, int* err, const Paging& pg, float k_scale,
+                     float v_scale) {
   const int S_max = (Nk_max + chunk - 1) / chunk;
   float* ws_o = static_cast<float*>(workspace);
   float* ws_lse = ws_o + static_cast<size_t>(B) * Hq * S_max * HD;
+#define ATTN_SPLIT_ARGS tk, tv, q, seqlens, ws_o, ws_lse, B, Hq, Hkv, Nk_max, scale, chunk, S_max, \
+                        num_sms, stream, err, pg, k_scale, v_scale
   switch (Hq / Hkv) {
-    case 1: return launch_split<1, PAGED>(tk, tv, q, seqlens, ws_o, ws_lse, B, Hq, Hkv, Nk_max, scale, chunk, S_max, num_sms, stream, err, pg);
-    case 2: return launch_split<2, PAGED>(tk, tv, q, seqlens, ws_o, ws_lse, B, Hq, Hkv, Nk_max, scale, chunk, S_max, num_sms, stream, err, pg);
-    case 4: return launch_split<4, PAGED>(tk, tv, q, seqlens, ws_o, ws_lse, B, Hq, Hkv, Nk_max, scale, chunk, S_max, num_sms, stream, err, pg);
-    case 8: return launch_split<8, PAGED>(tk, tv, q, seqlens, ws_o, ws_lse, B, Hq, Hkv, Nk_max, scale, chunk, S_max, num_sms, stream, err, pg);
+    case 1: return launch_split<1, PAGED, KV8>(ATTN_SPLIT_ARGS);
+    case 2: return launch_split<2, PAGED, KV8>(ATTN_SPLIT_ARGS);
+    case 4: return launch_split<4, PAGED, KV8>(ATTN_SPLIT_ARGS);
+    case 8: return launch_split<8, PAGED, KV8>(ATTN_SPLIT_ARGS);
     default: return ATTN_ERR_GQA;
   }
+#undef ATTN_SPLIT_ARGS
+}
+
+// Tensor maps over a contiguous cache [B, Nk_max, Hkv, D] or a page pool
+// [num_pages, page_size, Hkv, D]: one box is 64 key rows of one KV head.
+inline bool cache_maps(CUtensorMap* tk, CUtensorMap* tv, const void* k, const void* v, int Hkv,
+                       int rows, int outer, bool kv8) {
+  const uint32_t box[4] = {HD, 1, TILE, 1};
+  const CUtensorMapDataType dt = kv8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const uint32_t es = kv8 ? 1 : 2;
+  return encode_tiled_4d(tk, dt, k, HD, Hkv, rows, outer, es, box, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+         encode_tiled_4d(tv, dt, v, HD, Hkv, rows, outer, es, box, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 }  // namespace decode
@@ -481,35 +544,32 @@ int launch_split_any(const CUtensorMap& tk, const CUtensorMap& tv, const void* q
 int launch_decode_splitkv(const void* q, const void* k_cache, const void* v_cache,
                           const int* seqlens, void* workspace, int B, int Hq, int Hkv,
                           int Nk_max, float scale, int chunk, int num_sms, cudaStream_t stream,
-                          int* err) {
+                          int* err, int kv8, float k_scale, float v_scale) {
   using namespace decode;
   CUtensorMap tk, tv;
-  const uint32_t box[4] = {HD, 1, TILE, 1};
-  if (!encode_tiled_4d(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, k_cache, HD, Hkv, Nk_max, B, 2, box,
-                       CU_TENSOR_MAP_SWIZZLE_NONE) ||
-      !encode_tiled_4d(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, v_cache, HD, Hkv, Nk_max, B, 2, box,
-                       CU_TENSOR_MAP_SWIZZLE_NONE))
-    return ATTN_ERR_CUDA;
+  if (!cache_maps(&tk, &tv, k_cache, v_cache, Hkv, Nk_max, B, kv8 != 0)) return ATTN_ERR_CUDA;
   const Paging none{nullptr, 0, 0, 0};
-  return launch_split_any<false>(tk, tv, q, seqlens, workspace, B, Hq, Hkv, Nk_max, scale, chunk,
-                                 num_sms, stream, err, none);
+  return kv8 ? launch_split_any<false, true>(tk, tv, q, seqlens, workspace, B, Hq, Hkv, Nk_max, scale,
+                                             chunk, num_sms, stream, err, none, k_scale, v_scale)
+             : launch_split_any<false, false>(tk, tv, q, seqlens, workspace, B, Hq, Hkv, Nk_max, scale,
+                                              chunk, num_sms, stream, err, none, 1.f, 1.f);
 }
 
 int launch_decode_splitkv_paged(const void* q, const void* k_pages, const void* v_pages,
                                 const int* block_table, const int* seqlens, void* workspace, int B,
                                 int Hq, int Hkv, int num_pages, int page_size, int max_pages,
-                                float scale, int chunk, int num_sms, cudaStream_t stream, int* err) {
+                                float scale, int chunk, int num_sms, cudaStream_t stream, int* err,
+                                int kv8, float k_scale, float v_scale) {
   using namespace decode;
   CUtensorMap tk, tv;
-  const uint32_t box[4] = {HD, 1, TILE, 1};
-  if (!encode_tiled_4d(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, k_pages, HD, Hkv, page_size, num_pages,
-                       2, box, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-      !encode_tiled_4d(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, v_pages, HD, Hkv, page_size, num_pages,
-                       2, box, CU_TENSOR_MAP_SWIZZLE_NONE))
-    return ATTN_ERR_CUDA;
+  if (!cache_maps(&tk, &tv, k_pages, v_pages, Hkv, page_size, num_pages, kv8 != 0)) return ATTN_ERR_CUDA;
   const Paging pg{block_table, max_pages, page_size, num_pages};
-  return launch_split_any<true>(tk, tv, q, seqlens, workspace, B, Hq, Hkv, max_pages * page_size,
-                                scale, chunk, num_sms, stream, err, pg);
+  return kv8 ? launch_split_any<true, true>(tk, tv, q, seqlens, workspace, B, Hq, Hkv,
+                                            max_pages * page_size, scale, chunk, num_sms, stream, err,
+                                            pg, k_scale, v_scale)
+             : launch_split_any<true, false>(tk, tv, q, seqlens, workspace, B, Hq, Hkv,
+                                             max_pages * page_size, scale, chunk, num_sms, stream, err,
+                                             pg, 1.f, 1.f);
 }
 
 int launch_decode_combine(const void* workspace, const int* seqlens, void* o, float* lse, int B,

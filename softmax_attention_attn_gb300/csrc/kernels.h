@@ -49,15 +49,19 @@ int launch_fwd_fp32(const float* q, const float* k, const float* v, float* o, fl
                     int Hq, int Hkv, int Nq, int Nk, int D, float scale, int causal, int window,
                     cudaStream_t stream, int* err);
 
+// Split-KV decode, partial step.  kv8 != 0: the cache holds fp8 E4M3 codes
+// whose values are code * k_scale (K) and code * v_scale (V); else bf16
+// (k_scale, v_scale unused).
 int launch_decode_splitkv(const void* q, const void* k_cache, const void* v_cache,
                           const int* seqlens, void* workspace, int B, int Hq, int Hkv,
                           int Nk_max, float scale, int chunk, int num_sms, cudaStream_t stream,
-                          int* err);
+                          int* err, int kv8 = 0, float k_scale = 1.f, float v_scale = 1.f);
 
 int launch_decode_splitkv_paged(const void* q, const void* k_pages, const void* v_pages,
                                 const int* block_table, const int* seqlens, void* workspace, int B,
                                 int Hq, int Hkv, int num_pages, int page_size, int max_pages,
-                                float scale, int chunk, int num_sms, cudaStream_t stream, int* err);
+                                float scale, int chunk, int num_sms, cudaStream_t stream, int* err,
+                                int kv8 = 0, float k_scale = 1.f, float v_scale = 1.f);
 
 int launch_decode_combine(const void* workspace, const int* seqlens, void* o, float* lse, int B,
                           int Hq, int Nk_max, int chunk, cudaStream_t stream, int* err);

@@ -17,6 +17,10 @@ Recipe (every draw uses ``torch.Generator("cpu")``):
   be regenerated without replaying the others.  Cache rows at or beyond
   ``Nk_b`` hold finite sentinels (K = 64, V = 1e4) so that a masking leak
   shows up as a large error instead of passing unnoticed.
+* an fp8 KV cache (``kv_dtype="e4m3"``) holds the same fp32 draws rounded to
+  the nearest OCP FP8 E4M3 value (torch's float8_e4m3fn conversion), stored as
+  uint8 codes; the tail sentinels are K = 64 and V = 448 (the largest finite
+  E4M3 value).  The value of a code is set by the caller's per-tensor scale.
 * large decode workloads may draw each sequence's K/V rows on a CUDA device
   instead (``device=...``): same per-sequence seeds and distribution, but a
   CUDA generator, so the values differ from the CPU draw; a check against the
@@ -28,6 +32,9 @@ import torch
 
 K_SENTINEL = 64.0
 V_SENTINEL = 1.0e4
+V_SENTINEL_FP8 = 448.0
+
+_KV_CODES = {"e4m3": torch.float8_e4m3fn}
 
 _DTYPES = {"fp32": torch.float32, "bf16": torch.bfloat16, "fp16": torch.float16}
 
@@ -77,18 +84,36 @@ def decode_seqlens_and_q(B: int, Hq: int, D: int, nk_lo: int, nk_hi: int,
     return seqlens.to(torch.int32), _cast(q, dtype)
 
 
+def _codes(t: torch.Tensor, kv_dtype: str) -> torch.Tensor:
+    """fp32 values -> uint8 codes of the fp8 format ``kv_dtype`` (nearest value)."""
+    if kv_dtype not in _KV_CODES:
+        raise ValueError(f"unknown fp8 cache type {kv_dtype!r}")
+    return t.to(_KV_CODES[kv_dtype]).view(torch.uint8)
+
+
 def decode_kv_rows(seed: int, b: int, nk: int, Hkv: int, D: int, dtype: str = "bf16",
-                   device="cpu"):
-    """The ``nk`` valid K and V rows ``[nk,Hkv,D]`` of sequence ``b``."""
+                   device="cpu", kv_dtype: str | None = None):
+    """The ``nk`` valid K and V rows ``[nk,Hkv,D]`` of sequence ``b`` (fp8 codes
+    when ``kv_dtype`` names an fp8 format)."""
     g = torch.Generator(device).manual_seed(decode_row_seed(seed, b))
     k = torch.randn(nk, Hkv, D, generator=g, dtype=torch.float32, device=device)
     v = torch.randn(nk, Hkv, D, generator=g, dtype=torch.float32, device=device)
+    if kv_dtype is not None:
+        return _codes(k, kv_dtype), _codes(v, kv_dtype)
     return _cast(k, dtype), _cast(v, dtype)
+
+
+def _sentinels(kv_dtype: str | None):
+    """(K, V) tail fill: values, or fp8 codes of K = 64 and V = 448."""
+    if kv_dtype is None:
+        return K_SENTINEL, V_SENTINEL
+    return (int(_codes(torch.tensor([K_SENTINEL]), kv_dtype)[0]),
+            int(_codes(torch.tensor([V_SENTINEL_FP8]), kv_dtype)[0]))
 
 
 def decode_inputs(B: int, Hq: int, Hkv: int, D: int, nk_lo: int, nk_hi: int,
                   seed: int = 0, nk_max: int | None = None, dtype: str = "bf16",
-                  pin_memory: bool = False, device="cpu"):
+                  pin_memory: bool = False, device="cpu", kv_dtype: str | None = None):
     """Full decode workload: ``(q, k_cache, v_cache, seqlens)``.
 
     ``k_cache``/``v_cache`` are ``[B,Nk_max,Hkv,D]`` with ``Nk_max`` defaulting to
@@ -100,23 +125,24 @@ def decode_inputs(B: int, Hq: int, Hkv: int, D: int, nk_lo: int, nk_hi: int,
     nk_max = nk_hi if nk_max is None else nk_max
     if int(seqlens.max()) > nk_max:
         raise ValueError("nk_max is below a drawn sequence length")
-    tdt = _DTYPES[dtype]
+    tdt = _DTYPES[dtype] if kv_dtype is None else torch.uint8
     on_cpu = torch.device(device).type == "cpu"
     k_cache = torch.empty(B, nk_max, Hkv, D, dtype=tdt, device=device, pin_memory=pin_memory and on_cpu)
     v_cache = torch.empty(B, nk_max, Hkv, D, dtype=tdt, device=device, pin_memory=pin_memory and on_cpu)
+    k_fill, v_fill = _sentinels(kv_dtype)
     for b in range(B):
         nk = int(seqlens[b])
-        kb, vb = decode_kv_rows(seed, b, nk, Hkv, D, dtype, device)
+        kb, vb = decode_kv_rows(seed, b, nk, Hkv, D, dtype, device, kv_dtype)
         k_cache[b, :nk] = kb
         v_cache[b, :nk] = vb
-        k_cache[b, nk:] = K_SENTINEL
-        v_cache[b, nk:] = V_SENTINEL
+        k_cache[b, nk:] = k_fill
+        v_cache[b, nk:] = v_fill
     return q, k_cache, v_cache, seqlens
 
 
 def paged_decode_inputs(B: int, Hq: int, Hkv: int, D: int, nk_lo: int, nk_hi: int,
                         page_size: int, seed: int = 0, dtype: str = "bf16", device="cpu",
-                        spare_pages: int = 0):
+                        spare_pages: int = 0, kv_dtype: str | None = None):
     """Paged decode workload: ``(q, k_pages, v_pages, block_table, seqlens)``.
 
     Sequence lengths, Q and every sequence's K/V rows are the draws of
@@ -133,12 +159,13 @@ def paged_decode_inputs(B: int, Hq: int, Hkv: int, D: int, nk_lo: int, nk_hi: in
     num_pages = sum(need) + spare_pages
     perm = torch.randperm(num_pages, generator=torch.Generator("cpu").manual_seed(seed + 7))
     block_table = torch.zeros(B, max_pages, dtype=torch.int32)
-    tdt = _DTYPES[dtype]
-    k_pages = torch.full((num_pages, page_size, Hkv, D), K_SENTINEL, dtype=tdt, device=device)
-    v_pages = torch.full((num_pages, page_size, Hkv, D), V_SENTINEL, dtype=tdt, device=device)
+    tdt = _DTYPES[dtype] if kv_dtype is None else torch.uint8
+    k_fill, v_fill = _sentinels(kv_dtype)
+    k_pages = torch.full((num_pages, page_size, Hkv, D), k_fill, dtype=tdt, device=device)
+    v_pages = torch.full((num_pages, page_size, Hkv, D), v_fill, dtype=tdt, device=device)
     nxt = 0
     for b in range(B):
-        kb, vb = decode_kv_rows(seed, b, lens[b], Hkv, D, dtype, device)
+        kb, vb = decode_kv_rows(seed, b, lens[b], Hkv, D, dtype, device, kv_dtype)
         for i in range(need[b]):
             page = int(perm[nxt])
             nxt += 1

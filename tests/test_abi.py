@@ -30,6 +30,7 @@ def declared_functions():
 def test_header_declares_entry_points():
     names = declared_functions()
     for must in ("attn_fwd", "attn_fwd_fp16", "attn_fwd_fp32", "attn_decode_splitkv", "attn_decode_combine",
+                 "attn_decode_splitkv_fp8", "attn_decode_splitkv_paged_fp8",
                  "attn_decode_workspace_size", "attn_get_device_error", "attn_strerror"):
         assert must in names
 
@@ -133,6 +134,31 @@ def test_paged_decode_argument_errors(L):
     assert paged(chunk=96) == -11
     assert paged(bt=MIS) == -5
     assert paged(scale=0.0) == -6
+
+
+def test_fp8_decode_argument_errors(L):
+    def fp8(q=P, kc=P, vc=P, ks=0.5, vs=2.0, sl=P, ws=P, B=4, Hq=32, Hkv=8, Nk=1024, D=128, scale=0.1,
+            chunk=512):
+        return L.attn_decode_splitkv_fp8(q, kc, vc, ks, vs, sl, ws, B, Hq, Hkv, Nk, D, scale, chunk, None)
+
+    def paged8(q=P, kp=P, vp=P, ks=0.5, vs=2.0, bt=P, sl=P, ws=P, B=4, Hq=32, Hkv=8, num_pages=100,
+               page_size=256, max_pages=8, D=128, scale=0.1, chunk=512):
+        return L.attn_decode_splitkv_paged_fp8(q, kp, vp, ks, vs, bt, sl, ws, B, Hq, Hkv, num_pages,
+                                               page_size, max_pages, D, scale, chunk, None)
+
+    for f in (fp8, paged8):
+        assert f(q=None) == -1
+        assert f(Hq=32, Hkv=3) == -3
+        assert f(D=64) == -4
+        assert f(chunk=96) == -11
+        assert f(sl=MIS) == -5
+        assert f(scale=0.0) == -6
+        assert f(ks=0.0) == -6
+        assert f(vs=-1.0) == -6
+        assert f(ks=float("nan")) == -6
+        assert f(vs=float("inf")) == -6
+    assert paged8(bt=None) == -1
+    assert paged8(page_size=100) == -2
 
 
 def test_workspace_size(L):

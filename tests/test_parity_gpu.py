@@ -350,3 +350,75 @@ def test_decode_bad_seqlen_reported(dev):
     check(o.cpu()[1:2], lse.cpu()[1:2], O[1:2], L[1:2], BF16_O_TOL, BF16_LSE_REL, True)
     assert torch.all(o.cpu()[[0, 2]].float() == 0) and torch.all(lse.cpu()[[0, 2]] == -math.inf)
     assert binding.get_device_error() == 0
+
+
+# ---------------------------------------------------------------- fp8 (E4M3) KV cache
+FP8_SCALES = (0.37, 1.9)   # k_scale, v_scale: values are code * scale
+
+
+@pytest.mark.parametrize("G,chunk", [(1, 512), (4, 512), (8, 64), (2, 1024)])
+def test_decode_fp8_small(dev, G, chunk):
+    """fp8 E4M3 cache: ragged lengths around the chunk and tile sizes."""
+    lens = [1, 63, 64, 511, 513, 1500, 2048]
+    B, Hkv = len(lens), 2
+    Hq = G * Hkv
+    ks, vs = FP8_SCALES
+    q, kc, vc, _ = inputs.decode_inputs(B, Hq, Hkv, 128, 1, 2, seed=G + chunk, nk_max=2048, kv_dtype="e4m3")
+    sl = torch.tensor(lens, dtype=torch.int32)
+    # regenerate rows for the chosen lengths (the drawn lengths are ignored)
+    for b, n in enumerate(lens):
+        kb, vb = inputs.decode_kv_rows(G + chunk, b, n, Hkv, 128, kv_dtype="e4m3")
+        kc[b, :n], vc[b, :n] = kb, vb
+    o, lse = binding.attn_decode_fp8(q.to(dev), kc.to(dev), vc.to(dev), sl.to(dev), ks, vs, chunk=chunk)
+    O, L = oracle.decode_forward_fp8(q, kc.numpy(), vc.numpy(), ks, vs, lens, 1 / math.sqrt(128))
+    check(o, lse, O, L, BF16_O_TOL, BF16_LSE_REL, True)
+    assert binding.get_device_error() == 0
+
+
+@pytest.mark.parametrize("page_size,chunk,G", [(64, 512, 4), (256, 512, 8), (128, 64, 2)])
+def test_decode_fp8_paged_small(dev, page_size, chunk, G):
+    """Paged fp8 cache, sequences scattered over the pool (and spare pages)."""
+    B, Hkv = 6, 2
+    Hq = G * Hkv
+    ks, vs = FP8_SCALES
+    q, kp, vp, bt, sl = inputs.paged_decode_inputs(B, Hq, Hkv, 128, 1, 3000, page_size, seed=page_size + G,
+                                                   spare_pages=5, kv_dtype="e4m3")
+    o, lse = binding.attn_decode_paged_fp8(q.to(dev), kp.to(dev), vp.to(dev), bt.to(dev), sl.to(dev), ks, vs,
+                                           chunk=chunk)
+    O, L = oracle.decode_forward_paged_fp8(q, kp.numpy(), vp.numpy(), ks, vs, bt, sl, 1 / math.sqrt(128))
+    check(o, lse, O, L, BF16_O_TOL, BF16_LSE_REL, True)
+    assert binding.get_device_error() == 0
+
+
+def test_decode_fp8_benchmark_workload_sampled(dev):
+    """B=64 Hq=32 Hkv=8, Nk_b ~ U[512, 32768], chunk 512, fp8 cache: sampled sequences."""
+    ks, vs = FP8_SCALES
+    q, kc, vc, seqlens = inputs.decode_inputs(64, 32, 8, 128, 512, 32768, seed=0, device=dev, kv_dtype="e4m3")
+    o, lse = binding.attn_decode_fp8(q.to(dev), kc, vc, seqlens.to(dev), ks, vs, chunk=512)
+    lens = seqlens.numpy()
+    batches = sorted({int(lens.argmax()), int(lens.argmin()), 0, 21, 63})
+    O = np.zeros((len(batches), 32, 128))
+    L = np.zeros((len(batches), 32))
+    for n, b in enumerate(batches):
+        nk = int(lens[b])
+        Ob, Lb = oracle.decode_forward_fp8(q[b:b + 1], kc[b:b + 1, :nk].cpu().numpy(),
+                                           vc[b:b + 1, :nk].cpu().numpy(), ks, vs, [nk], 1 / math.sqrt(128))
+        O[n], L[n] = Ob[0], Lb[0]
+    check(o.cpu()[batches], lse.cpu()[batches], O, L, BF16_O_TOL, BF16_LSE_REL, True)
+    assert binding.get_device_error() == 0
+
+
+def test_decode_fp8_nan_codes_in_unused_rows_do_not_leak(dev):
+    """Rows past a sequence's end hold NaN codes (0x7F, 0xFF): never weighted."""
+    lens = [5, 700, 1]
+    B, Hq, Hkv, nk_max = 3, 8, 2, 1024
+    _, q = inputs.decode_seqlens_and_q(B, Hq, 128, 1, 2, 6)
+    kc = torch.full((B, nk_max, Hkv, 128), 0x7F, dtype=torch.uint8)
+    vc = torch.full((B, nk_max, Hkv, 128), 0xFF, dtype=torch.uint8)
+    for b, n in enumerate(lens):
+        kb, vb = inputs.decode_kv_rows(6, b, n, Hkv, 128, kv_dtype="e4m3")
+        kc[b, :n], vc[b, :n] = kb, vb
+    o, lse = binding.attn_decode_fp8(q.to(dev), kc.to(dev), vc.to(dev), torch.tensor(lens, dtype=torch.int32).to(dev),
+                                     1.0, 1.0)
+    O, L = oracle.decode_forward_fp8(q, kc.numpy(), vc.numpy(), 1.0, 1.0, lens, 1 / math.sqrt(128))
+    check(o, lse, O, L, BF16_O_TOL, BF16_LSE_REL, True)
