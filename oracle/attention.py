@@ -38,6 +38,14 @@ Sources (pages on softmax attention):
       block table ``[B, max_pages]`` names, for sequence b, the page of its
       logical page i, so key j of sequence b is row ``j % page_size`` of page
       ``block_table[b, j // page_size]``.
+    - softcap and attention sinks (both on the list of masks, after vLLM's
+      feature surface, which the same section names): with a cap c > 0 each
+      scaled score becomes ``c * tanh(s / c)`` (masked scores stay -inf); a
+      sink is one logit per query head, ``sink[h]``, that joins the softmax
+      denominator of every row of head h but carries no value:
+      ``P_ij = exp(s_ij) / (sum_j exp(s_ij) + exp(sink[h]))``,
+      ``LSE_i = ln(sum_j exp(s_ij) + exp(sink[h]))``; a row with no visible key
+      then has O = 0 and LSE = sink[h];
     - an fp8 KV cache (fp8 e4m3 is on the list of data types) stores each K and
       V element as one OCP FP8 E4M3 code; the value is the code's E4M3 value
       times a per-tensor scale (``k_scale`` for K, ``v_scale`` for V).  E4M3:
@@ -56,6 +64,7 @@ __all__ = [
     "attention_probabilities", "decode_forward", "decode_split_partials",
     "decode_combine", "paged_rows", "decode_forward_paged", "attention_varlen",
     "e4m3_to_float", "decode_forward_fp8", "decode_forward_paged_fp8",
+    "softcap_scores", "attention_forward_ext", "attention_rows_ext",
 ]
 
 
@@ -367,4 +376,70 @@ def decode_forward_paged_fp8(q, k_pages, v_pages, k_scale: float, v_scale: float
         for h in range(Hq):
             kh = kv_head(h, Hq, Hkv)
             O[b, h], LSE[b, h] = _decode_one(qb[h], Kb[:, kh], Vb[:, kh], scale)
+    return O, LSE
+
+
+def softcap_scores(S: np.ndarray, cap: float) -> np.ndarray:
+    """``cap * tanh(S / cap)`` for ``cap > 0`` (masked -inf entries stay -inf);
+    ``S`` unchanged for ``cap <= 0``."""
+    if not cap > 0:
+        return S
+    with np.errstate(invalid="ignore"):
+        return np.where(np.isneginf(S), -np.inf, cap * np.tanh(S / cap))
+
+
+def _softmax_rows_sink(S: np.ndarray, sink: float):
+    """Two-pass row softmax with one extra denominator term ``exp(sink)`` (no
+    value attached).  ``sink = -inf`` is the plain softmax.  Returns ``(P, lse)``."""
+    M = np.maximum(S.max(axis=1), sink)                # pass 1: max over keys and the sink
+    empty = ~np.isfinite(M)                            # every key masked and no sink
+    M_safe = np.where(empty, 0.0, M)
+    E = np.exp(S - M_safe[:, None])                    # pass 2: exp (masked -> 0)
+    l = E.sum(axis=1) + np.exp(sink - M_safe)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        P = np.where(empty[:, None], 0.0, E / np.where(empty, 1.0, l)[:, None])
+        lse = np.where(empty, -np.inf, M_safe + np.log(np.where(empty, 1.0, l)))
+    return P, lse
+
+
+def _sink_of(sinks, h: int) -> float:
+    return -np.inf if sinks is None else float(np.asarray(sinks, dtype=np.float64)[h])
+
+
+def attention_forward_ext(q, k, v, scale: float, causal: bool = False, window: int = 0,
+                          softcap: float = 0.0, sinks=None, row_block: int = 512):
+    """:func:`attention_forward` with a softcap on the scaled scores and one sink
+    logit per query head (``sinks`` ``[Hq]``, or None for none)."""
+    Q, K, V = _f64(q), _f64(k), _f64(v)
+    B, Hq, Nq, D = Q.shape
+    Hkv, Nk = K.shape[1], K.shape[2]
+    O = np.zeros((B, Hq, Nq, V.shape[3]))
+    LSE = np.zeros((B, Hq, Nq))
+    for b in range(B):
+        for h in range(Hq):
+            kh = kv_head(h, Hq, Hkv)
+            for i0 in range(0, Nq, row_block):
+                rows = np.arange(i0, min(i0 + row_block, Nq))
+                S = _scores(Q[b, h, rows], K[b, kh], scale)
+                S[~visible_mask(rows, Nq, Nk, causal, window)] = -np.inf
+                P, lse = _softmax_rows_sink(softcap_scores(S, softcap), _sink_of(sinks, h))
+                O[b, h, rows] = P @ V[b, kh]
+                LSE[b, h, rows] = lse
+    return O, LSE
+
+
+def attention_rows_ext(q, k, v, scale: float, rows, causal: bool = False, window: int = 0,
+                       softcap: float = 0.0, sinks=None):
+    """:func:`attention_rows` with softcap and sinks, one ``(b, h, i)`` row at a time."""
+    B, Hq, Nq, _ = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    O = np.zeros((len(rows), v.shape[3]))
+    LSE = np.zeros(len(rows))
+    for n, (b, h, i) in enumerate(rows):
+        kh = kv_head(h, Hq, Hkv)
+        S = _scores(_f64(q[b, h, i])[None, :], _f64(k[b, kh]), scale)
+        S[~visible_mask(np.array([i]), Nq, Nk, causal, window)] = -np.inf
+        P, lse = _softmax_rows_sink(softcap_scores(S, softcap), _sink_of(sinks, h))
+        O[n] = (P @ _f64(v[b, kh]))[0]
+        LSE[n] = lse[0]
     return O, LSE

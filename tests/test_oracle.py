@@ -420,9 +420,65 @@ def pin_fp8_decode(ora):
     assert np.allclose(O4, O, rtol=1e-13, atol=1e-13) and np.allclose(L4, L, rtol=1e-13, atol=1e-13)
 
 
+def pin_softcap_sink(ora):
+    """Softcap and sinks: brute force (math.tanh, math.fsum) on tiny inputs with
+    causal / window masks and sinks from dominant to -inf, the Q = 0 closed form,
+    a row with no visible key, and the reductions to the plain forward."""
+    rng = np.random.default_rng(11)
+    B, Hq, Hkv, Nq, Nk, D = 1, 4, 2, 5, 7, 3
+    q = rng.standard_normal((B, Hq, Nq, D)) * 2.0
+    k = rng.standard_normal((B, Hkv, Nk, D)) * 2.0
+    v = rng.standard_normal((B, Hkv, Nk, D))
+    sinks = np.array([0.7, -2.0, 6.0, -np.inf])
+    sc, cap = 0.8, 2.5
+    for causal, window in ((False, 0), (True, 0), (True, 3), (False, 2)):
+        O, L = ora.attention_forward_ext(q, k, v, sc, causal, window, cap, sinks)
+        for h in range(Hq):
+            kh = h // (Hq // Hkv)
+            for i in range(Nq):
+                vis = [j for j in range(Nk) if (not causal or j <= i + Nk - Nq)
+                       and (window <= 0 or j > i + Nk - Nq - window)]
+                s = {j: cap * math.tanh(sc * math.fsum(q[0, h, i, d] * k[0, kh, j, d] for d in range(D)) / cap)
+                     for j in vis}
+                terms = [math.exp(x) for x in s.values()] + ([math.exp(sinks[h])] if np.isfinite(sinks[h]) else [])
+                den = math.fsum(terms)
+                for d in range(D):
+                    o = math.fsum(math.exp(s[j]) * v[0, kh, j, d] for j in vis) / den if vis else 0.0
+                    assert abs(O[0, h, i, d] - o) < 1e-12, (causal, window, h, i, d)
+                want = math.log(den) if terms else -math.inf
+                assert (L[0, h, i] == want) if not terms else abs(L[0, h, i] - want) < 1e-12
+    # Q = 0: every visible softcapped score is 0
+    z = np.zeros_like(q)
+    O0, L0 = ora.attention_forward_ext(z, k, v, sc, False, 0, cap, sinks)
+    for h in range(Hq):
+        kh = h // (Hq // Hkv)
+        extra = math.exp(sinks[h]) if np.isfinite(sinks[h]) else 0.0
+        assert np.allclose(O0[0, h], v[0, kh].sum(axis=0) / (Nk + extra), atol=1e-13)
+        assert np.allclose(L0[0, h], math.log(Nk + extra), atol=1e-13)
+    # no visible key (causal with Nq > Nk): O = 0, LSE = sink
+    q2 = rng.standard_normal((1, Hq, 6, D))
+    k2, v2 = rng.standard_normal((1, Hkv, 2, D)), rng.standard_normal((1, Hkv, 2, D))
+    O2, L2 = ora.attention_forward_ext(q2, k2, v2, sc, True, 0, cap, sinks)
+    for h in range(Hq):
+        assert np.all(O2[0, h, :4] == 0.0)
+        assert np.all(L2[0, h, :4] == sinks[h])
+    # reductions: no cap and no sinks is the plain forward; a huge cap is no cap
+    Op, Lp = ora.attention_forward(q, k, v, sc, True, 0)
+    Oe, Le = ora.attention_forward_ext(q, k, v, sc, True, 0, 0.0, None)
+    assert np.allclose(Oe, Op, atol=1e-14) and np.allclose(Le, Lp, atol=1e-14)
+    Oh, Lh = ora.attention_forward_ext(q, k, v, sc, True, 0, 1e9, np.full(Hq, -np.inf))
+    assert np.allclose(Oh, Op, atol=1e-9) and np.allclose(Lh, Lp, atol=1e-9)
+    # sampled rows agree with the full forward
+    rows = [(0, h, i) for h in range(Hq) for i in (0, 2, 4)]
+    Or, Lr = ora.attention_rows_ext(q, k, v, sc, rows, True, 3, cap, sinks)
+    Of, Lf = ora.attention_forward_ext(q, k, v, sc, True, 3, cap, sinks)
+    for n, (b, h, i) in enumerate(rows):
+        assert np.allclose(Or[n], Of[b, h, i], atol=1e-14) and abs(Lr[n] - Lf[b, h, i]) < 1e-14
+
+
 PINS = [pin_brute_force, pin_sdpa, pin_zero_query, pin_single_key, pin_probability_rows,
         pin_causal_first_row, pin_dominant_key, pin_invariants, pin_decode, pin_paged_decode, pin_varlen,
-        pin_golden, pin_e4m3_codes, pin_fp8_decode]
+        pin_golden, pin_e4m3_codes, pin_fp8_decode, pin_softcap_sink]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
@@ -545,6 +601,29 @@ def _mut_fp8_paged_swapped(q, k_pages, v_pages, k_scale, v_scale, block_table, s
     return ORA.decode_forward_fp8(q, kc, vc, k_scale, v_scale, seqlens, scale, batches)
 
 
+def _mut_softcap_no_divide(S, cap):
+    if not cap > 0:
+        return S
+    with np.errstate(invalid="ignore"):
+        return np.where(np.isneginf(S), -np.inf, cap * np.tanh(S))
+
+
+def _mut_sink_unshifted(S, sink):
+    M = S.max(axis=1)
+    empty = ~np.isfinite(M)
+    M_safe = np.where(empty, 0.0, M)
+    E = np.exp(S - M_safe[:, None])
+    l = E.sum(axis=1) + np.exp(sink)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        P = np.where(empty[:, None], 0.0, E / np.where(empty, 1.0, l)[:, None])
+        lse = np.where(empty, -np.inf, M_safe + np.log(np.where(empty, 1.0, l)))
+    return P, lse
+
+
+def _mut_sink_dropped(S, sink):
+    return ORA._softmax_rows(S)
+
+
 MUTANTS = {
     "no_scale": ("_scores", _mut_no_scale),
     "sqrt_scale": ("_scores", _mut_sqrt_scale),
@@ -560,6 +639,9 @@ MUTANTS = {
     "e4m3_bias_8": ("e4m3_to_float", _mut_e4m3_bias8),
     "e4m3_no_subnormals": ("e4m3_to_float", _mut_e4m3_no_subnormals),
     "fp8_paged_index_swapped": ("decode_forward_paged_fp8", _mut_fp8_paged_swapped),
+    "softcap_without_divide": ("softcap_scores", _mut_softcap_no_divide),
+    "sink_unshifted": ("_softmax_rows_sink", _mut_sink_unshifted),
+    "sink_dropped": ("_softmax_rows_sink", _mut_sink_dropped),
 }
 
 
