@@ -85,7 +85,7 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--workload", choices=["dense", "causal", "decode", "fp32", "window", "chunked", "d64",
-                                           "paged", "fp16", "varlen", "decode_fp8"],
+                                           "paged", "fp16", "varlen", "decode_fp8", "softcap"],
                     default="dense",
                     help="workload of the timed loop (default: the dense bf16 prefill)")
     ap.add_argument("--no-extras", action="store_true", help="skip the other workloads")
@@ -271,6 +271,7 @@ WORKLOAD_NAMES = {
     "paged": "bf16 split-KV decode on a paged cache (page 256) B=64 Hq=32 Hkv=8 D=128, Nk_b~U[512,32768], chunk 512",
     "decode_fp8": "split-KV decode on an fp8 E4M3 KV cache (bf16 Q) B=64 Hq=32 Hkv=8 D=128, Nk_b~U[512,32768], "
                   "chunk 512",
+    "softcap": "bf16 dense prefill B=1 H=32 N=8192 D=128 with softcap 50 and per-head attention sinks",
 }
 
 
@@ -295,9 +296,9 @@ def make_workload(name, dev, seed, peaks, peak_src, sm_max_mhz, decode_batch=Non
         w["peak_source"] = f"{peak_src} dense bf16 (burst)"
         w["e2e_in"] = [(x, t) for x, t in zip(host, (q, k, v, cq, ck))]
         w["e2e_out"] = [o, lse]
-    elif name in ("dense", "causal", "fp32", "window", "chunked", "d64", "fp16"):
+    elif name in ("dense", "causal", "fp32", "window", "chunked", "d64", "fp16", "softcap"):
         c = {"dense": MAIN, "causal": CAUSAL, "fp32": FP32, "window": WINDOW, "chunked": CHUNKED,
-             "d64": DENSE64, "fp16": MAIN}[name]
+             "d64": DENSE64, "fp16": MAIN, "softcap": MAIN}[name]
         Nq, Nk = c.get("Nq", c.get("N")), c.get("Nk", c.get("N"))
         dt = {"fp32": "fp32", "fp16": "fp16"}.get(name, "bf16")
         host = inputs.prefill_inputs(c["B"], c["Hq"], c["Hkv"], Nq, Nk, c["D"], dt, seed)
@@ -307,6 +308,10 @@ def make_workload(name, dev, seed, peaks, peak_src, sm_max_mhz, decode_batch=Non
         call = {"fp32": binding.attn_fwd_fp32, "fp16": binding.attn_fwd_fp16}.get(name, binding.attn_fwd)
         wnd = c.get("window", 0)
         w["fn"] = lambda: call(q, k, v, o, lse, causal=c["causal"], window=wnd)
+        if name == "softcap":
+            sinks = torch.randn(c["Hq"], generator=torch.Generator("cpu").manual_seed(seed + 5)).float().to(dev)
+            w["fn"] = lambda: binding.attn_fwd_softcap_sink(q, k, v, o, lse, causal=c["causal"], softcap=50.0,
+                                                            sinks=sinks)
         w["work"] = masked_flops(c["B"], c["Hq"], Nq, Nk, c["D"], c["causal"], wnd) if "Nq" in c else flops(**c)
         w["unit"] = "TFLOP/s"
         w["launches"] = 1
@@ -494,7 +499,7 @@ def run_gb300(args, rank, world, local_rank):
     if not args.no_extras:
         xs = max(5, min(args.steps // 10, 50))
         for name in ("dense", "causal", "decode", "paged", "decode_fp8", "fp32", "window", "chunked", "d64", "fp16",
-                     "varlen"):
+                     "varlen", "softcap"):
             if name == args.workload:
                 continue
             x = make_workload(name, dev, rank, peaks, peak_src, sm_max, args.decode_batch)

@@ -84,6 +84,27 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
              float scale, int causal, int window, attn_stream_t stream);
 
 /*
+ * attn_fwd_softcap_sink — attn_fwd with a softcap on the scores and one sink
+ * logit per query head.   [ASK] "研究动机" (softcap and attention-sink masks on
+ * the feature list; the pages give no formulas).
+ *
+ *   softcap : c > 0 maps each scaled score s = scale * q.k to c * tanh(s / c)
+ *             before the softmax (masked scores stay masked); c <= 0 disables
+ *   sinks   : device float32 [Hq] or NULL.  sinks[h] (natural-log units, may be
+ *             -inf) joins the softmax denominator of every row of query head h
+ *             without a value: P_ij = exp(s_ij) / (sum_j exp(s_ij) + exp(sinks[h]))
+ *             and LSE_i = ln(sum_j exp(s_ij) + exp(sinks[h])); a row with no
+ *             visible key gets O = 0 and LSE = sinks[h]
+ *   Every other argument, layout and result is that of attn_fwd (bf16; D 64 or
+ *   128; causal, window).
+ *   Errors: as attn_fwd, plus ATTN_ERR_SCALE for a softcap that is not finite
+ *   and ATTN_ERR_ALIGN for a sinks pointer that is not 4-byte aligned.
+ */
+int attn_fwd_softcap_sink(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                          int Hq, int Hkv, int Nq, int Nk, int D, float scale, int causal,
+                          int window, float softcap, const float* sinks, attn_stream_t stream);
+
+/*
  * attn_fwd_fp16 — fp16 variant of attn_fwd (same kernel, fp16 tensor-core
  * operands).  [ASK] "研究动机" (bf16 / fp16 / fp8 precisions on the feature
  * surface).  Same shapes, masks, D and error codes as attn_fwd with fp16 q, k,

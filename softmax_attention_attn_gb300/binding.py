@@ -27,6 +27,7 @@ SIGNATURES = {
     "attn_fwd_fp32": (_c_int, [_vp, _vp, _vp, _vp, _vp] + [_c_int] * 6 + [_c_float, _c_int, _c_int, _vp]),
     "attn_fwd_fp16": (_c_int, [_vp, _vp, _vp, _vp, _vp] + [_c_int] * 6 + [_c_float, _c_int, _c_int, _vp]),
     "attn_fwd_varlen": (_c_int, [_vp] * 7 + [_c_int] * 7 + [_c_float, _c_int, _c_int, _vp]),
+    "attn_fwd_softcap_sink": (_c_int, [_vp] * 5 + [_c_int] * 6 + [_c_float, _c_int, _c_int, _c_float, _vp, _vp]),
     "attn_decode_workspace_size": (ctypes.c_size_t, [_c_int] * 5),
     "attn_decode_splitkv": (_c_int, [_vp] * 5 + [_c_int] * 5 + [_c_float, _c_int, _vp]),
     "attn_decode_combine": (_c_int, [_vp] * 4 + [_c_int] * 5 + [_vp]),
@@ -116,6 +117,33 @@ def attn_fwd(q, k, v, o=None, lse=None, scale=None, causal=False, window=0, stre
     """bf16 forward: q ``[B,Hq,Nq,D]``, k/v ``[B,Hkv,Nk,D]`` -> (o, lse)."""
     import torch
     return _fwd("attn_fwd", torch.bfloat16, q, k, v, o, lse, scale, causal, window, stream)
+
+
+def attn_fwd_softcap_sink(q, k, v, o=None, lse=None, scale=None, causal=False, window=0, softcap=0.0,
+                          sinks=None, stream=None):
+    """bf16 forward with a softcap on the scaled scores (``softcap > 0``) and one
+    sink logit per query head (``sinks``: float32 CUDA tensor ``[Hq]``, or None)."""
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _require(t, torch.bfloat16, n)
+    B, Hq, Nq, D = q.shape
+    _, Hkv, Nk, _ = k.shape
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(B, Hq, Nq, device=q.device, dtype=torch.float32)
+    _require(o, torch.bfloat16, "o")
+    _require(lse, torch.float32, "lse")
+    if sinks is not None:
+        _require(sinks, torch.float32, "sinks")
+        if sinks.numel() != Hq:
+            raise ValueError(f"sinks must hold Hq = {Hq} values")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    code = lib().attn_fwd_softcap_sink(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Nq, Nk, D,
+                                       scale, int(bool(causal)), int(window), float(softcap),
+                                       _ptr(sinks) if sinks is not None else None, _stream(stream))
+    _check(code, "attn_fwd_softcap_sink")
+    return o, lse
 
 
 def attn_fwd_fp16(q, k, v, o=None, lse=None, scale=None, causal=False, window=0, stream=None):

@@ -139,6 +139,20 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
              attn_stream_t stream) {
   return fwd_tc(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, 0, scale, causal, window, stream);
 }
+int attn_fwd_softcap_sink(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                          int Hq, int Hkv, int Nq, int Nk, int D, float scale, int causal,
+                          int window, float softcap, const float* sinks, attn_stream_t stream) {
+  int rc = check_common(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, scale);
+  if (rc != ATTN_OK) return rc;
+  if (D != 64 && D != 128) return ATTN_ERR_HEAD_DIM;
+  if (!std::isfinite(softcap)) return ATTN_ERR_SCALE;
+  if (sinks != nullptr && (reinterpret_cast<uintptr_t>(sinks) & 3u) != 0) return ATTN_ERR_ALIGN;
+  DeviceInfo* dev = nullptr;
+  if ((rc = device_info(&dev)) != ATTN_OK) return rc;
+  return launch_fwd_tc(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, 0, scale, causal, window,
+                       dev->num_sms, reinterpret_cast<cudaStream_t>(stream), dev->err, nullptr,
+                       nullptr, 0, 0, softcap, sinks);
+}
 
 int attn_fwd_fp16(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
                   int Hkv, int Nq, int Nk, int D, float scale, int causal, int window,

@@ -92,6 +92,14 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   else return pack_bf16x2(lo, hi);
 }
 
+// tanh from the exponential: tanh|y| = 1 - 2 / (1 + e^(2|y|)), sign restored
+// (hardware 2^x and 1/x; e^(2|y|) = inf gives 1).  Its absolute error stays
+// near one fp32 ulp of 1, including for small |y|.
+__device__ __forceinline__ float tanh_exp(float y) {
+  const float e = ex2_approx(fabsf(y) * 2.8853900817779268f);  // 2^(2|y| log2 e)
+  return copysignf(fmaf(-2.f, rcp_approx(1.f + e), 1.f), y);
+}
+
 // Shared-memory descriptors are linear in the start address (its field is
 // address >> 4 in the low 14 bits, and every shared-memory address here is
 // below 2^18), so a descriptor for base + offset is the base descriptor plus
@@ -248,7 +256,7 @@ __device__ __forceinline__ void own_range(const Unit& u, int t, int& jb, int& je
   je = t == 0 ? u.je0 : u.je1;
 }
 
-template <int HD, bool F16>
+template <int HD, bool F16, bool CAP>
 __global__ void __launch_bounds__(NTHREADS, 1)
 attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
@@ -532,7 +540,8 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
         float s[BN];
 #pragma unroll
         for (int i = 0; i < BN; ++i) s[i] = __uint_as_float(sr[i >> 5][i & 31]);
-        if (k0 + BN - 1 > tile_hi_min || k0 < tile_lo_max) {
+        const bool need_mask = k0 + BN - 1 > tile_hi_min || k0 < tile_lo_max;
+        if (need_mask) {
 #pragma unroll
           for (int i = 0; i < BN; ++i) {
             const int key = k0 + i;
@@ -547,7 +556,12 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
           for (int g = 0; g < 8; ++g) mx[g] = fmax3(mx[g], s[i + g], s[i + 8 + g]);
         const float rmax = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
-        const float m_new = fmaxf(m, rmax * c);
+        float rmax_l2;  // the row maximum in exp2 units (after the softcap)
+        if constexpr (CAP)
+          rmax_l2 = rmax == -CUDART_INF_F ? -CUDART_INF_F : p.cap_post * tanh_exp(p.cap_pre * rmax);
+        else
+          rmax_l2 = rmax * c;
+        const float m_new = fmaxf(m, rmax_l2);
         float alpha = 1.f;
         bool grow = false;
         if (jj == 0) {
@@ -579,9 +593,19 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
             uint32_t pk[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-              const uint64_t x2 = f2_fma(f2_pack(s[c0 + 2 * i], s[c0 + 2 * i + 1]), c2, nm2);
               float x0, x1;
-              f2_unpack(x2, x0, x1);
+              if constexpr (CAP) {
+                // capped score in exp2 units; masked scores stay -inf
+                x0 = fmaf(p.cap_post, tanh_exp(p.cap_pre * s[c0 + 2 * i]), -m_use);
+                x1 = fmaf(p.cap_post, tanh_exp(p.cap_pre * s[c0 + 2 * i + 1]), -m_use);
+                if (need_mask) {
+                  if (s[c0 + 2 * i] == -CUDART_INF_F) x0 = -CUDART_INF_F;
+                  if (s[c0 + 2 * i + 1] == -CUDART_INF_F) x1 = -CUDART_INF_F;
+                }
+              } else {
+                const uint64_t x2 = f2_fma(f2_pack(s[c0 + 2 * i], s[c0 + 2 * i + 1]), c2, nm2);
+                f2_unpack(x2, x0, x1);
+              }
               const float p0 = ex2_approx(x0);
               const float p1 = ex2_approx(x1);
               sum2[i & 1] = f2_add(sum2[i & 1], f2_pack(p0, p1));
@@ -635,7 +659,24 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
         for (int i = 0; i < HD; ++i) o[i] = 0u;
       }
       if (row < u.Nq) {
-        const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+        // normaliser and LSE; a sink adds 2^(sink - m) to the row sum (in the
+        // common maximum M = max(m, sink)); a row with no visible key has O = 0
+        // and LSE = sink
+        float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+        float lse_val = (l > 0.f) ? (m + log2f(l)) * 0.69314718055994531f : -CUDART_INF_F;
+        if (p.sinks != nullptr) {
+          const float sink = __ldg(p.sinks + u.h);
+          if (l > 0.f) {
+            const float M = fmaxf(m, sink * 1.4426950408889634f);
+            const float w = ex2_approx(m - M);
+            const float lt = fmaf(l, w, ex2_approx(sink * 1.4426950408889634f - M));
+            inv_l = w / lt;
+            lse_val = (M + log2f(lt)) * 0.69314718055994531f;
+          } else {
+            inv_l = 0.f;
+            lse_val = sink;
+          }
+        }
         const size_t orow_idx = p.varlen ? static_cast<size_t>(u.q_tok + row) * p.Hq + u.h
                                          : (static_cast<size_t>(u.b) * p.Hq + u.h) * p.Nq + row;
         uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + orow_idx * HD);
@@ -649,7 +690,7 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
           orow[i] = v4;
         }
         if (p.lse != nullptr) {
-          const float lse = (l > 0.f) ? (m + log2f(l)) * 0.69314718055994531f : -CUDART_INF_F;
+          const float lse = lse_val;
           const size_t li = p.varlen ? static_cast<size_t>(u.h) * p.total_q + u.q_tok + row
                                      : (static_cast<size_t>(u.b) * p.Hq + u.h) * p.Nq + row;
           p.lse[li] = lse;
@@ -671,11 +712,11 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
 // --------------------------------------------------------------------- host
 namespace fwd_bf16 {
 
-template <int HD, bool F16>
+template <int HD, bool F16, bool CAP>
 int launch_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
                 int Hkv, int Nq, int Nk, float scale, int causal, int window, int num_sms,
                 cudaStream_t stream, int* err, const int* cu_q, const int* cu_k, int total_q,
-                int total_k) {
+                int total_k, float softcap, const float* sinks) {
   using C = Cfg<HD, F16>;
   const CUtensorMapDataType dt = F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   CUtensorMap tq, tk, tv;
@@ -697,7 +738,7 @@ int launch_impl(const void* q, const void* k, const void* v, void* o, float* lse
   int dev = 0;
   cudaGetDevice(&dev);
   if (attr_set_dev != dev) {
-    if (cudaFuncSetAttribute(attn_fwd_bf16_kernel<HD, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(attn_fwd_bf16_kernel<HD, F16, CAP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::SMEM_ALLOC) != cudaSuccess)
       return ATTN_ERR_CUDA;
     attr_set_dev = dev;
@@ -720,12 +761,15 @@ int launch_impl(const void* q, const void* k, const void* v, void* o, float* lse
   prm.cu_k = cu_k;
   prm.total_q = total_q;
   prm.total_k = total_k;
+  prm.cap_pre = CAP ? scale / softcap : 0.f;
+  prm.cap_post = CAP ? softcap * 1.4426950408889634f : 0.f;
+  prm.sinks = sinks;
   // persistent: at most one CTA per SM, each walking units blockIdx.x, +gridDim.x, ...
   const long long n_qblk = (Nq + BM * NQT - 1) / (BM * NQT);
   const long long units = n_qblk * Hq * B;
   if (units > 0x7fffffffLL) return ATTN_ERR_DIM;
   const int grid = static_cast<int>(units < num_sms ? units : num_sms);
-  attn_fwd_bf16_kernel<HD, F16><<<grid, NTHREADS, C::SMEM_ALLOC, stream>>>(tq, tk, tv, prm);
+  attn_fwd_bf16_kernel<HD, F16, CAP><<<grid, NTHREADS, C::SMEM_ALLOC, stream>>>(tq, tk, tv, prm);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -734,14 +778,16 @@ int launch_impl(const void* q, const void* k, const void* v, void* o, float* lse
 int launch_fwd_tc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
                   int Hkv, int Nq, int Nk, int D, int f16, float scale, int causal, int window,
                   int num_sms, cudaStream_t stream, int* err, const int* cu_q, const int* cu_k,
-                  int total_q, int total_k) {
+                  int total_q, int total_k, float softcap, const float* sinks) {
   using fwd_bf16::launch_impl;
 #define ATTN_TC_ARGS q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, window, num_sms, stream, err, \
-                     cu_q, cu_k, total_q, total_k
-  if (D == 64 && !f16) return launch_impl<64, false>(ATTN_TC_ARGS);
-  if (D == 128 && !f16) return launch_impl<128, false>(ATTN_TC_ARGS);
-  if (D == 64 && f16) return launch_impl<64, true>(ATTN_TC_ARGS);
-  if (D == 128 && f16) return launch_impl<128, true>(ATTN_TC_ARGS);
+                     cu_q, cu_k, total_q, total_k, softcap, sinks
+  const bool cap = softcap > 0.f;
+  if (cap && f16) return ATTN_ERR_HEAD_DIM;  // the softcap instances are bf16 only
+  if (D == 64 && !f16) return cap ? launch_impl<64, false, true>(ATTN_TC_ARGS) : launch_impl<64, false, false>(ATTN_TC_ARGS);
+  if (D == 128 && !f16) return cap ? launch_impl<128, false, true>(ATTN_TC_ARGS) : launch_impl<128, false, false>(ATTN_TC_ARGS);
+  if (D == 64 && f16) return launch_impl<64, true, false>(ATTN_TC_ARGS);
+  if (D == 128 && f16) return launch_impl<128, true, false>(ATTN_TC_ARGS);
 #undef ATTN_TC_ARGS
   return ATTN_ERR_HEAD_DIM;
 }

@@ -26,6 +26,11 @@ struct FwdParams {
   const int* cu_q;
   const int* cu_k;
   int total_q, total_k;
+  // softcap c > 0: score s -> c * tanh(scale * s / c); cap_pre = scale / c,
+  // cap_post = c * log2(e).  sinks: one logit per query head (natural-log
+  // units) in every row's softmax denominator, or null.
+  float cap_pre, cap_post;
+  const float* sinks;
 };
 
 // Tensor maps (cuTensorMapEncodeTiled, fetched from the driver at run time).
@@ -40,10 +45,13 @@ bool encode_tiled_4d(CUtensorMap* map, CUtensorMapDataType dt, const void* base,
 // Tensor-core forward; f16 != 0 selects fp16 operands and output instead of bf16.
 // With cu_q != nullptr the batch is ragged (packed token-major layout, see FwdParams);
 // Nq is then the maximum query length and Nk is unused.
+// softcap > 0 (bf16 only) caps the scaled scores; sinks (device, [Hq]) adds
+// one logit per query head to every row's softmax denominator.
 int launch_fwd_tc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
                   int Hkv, int Nq, int Nk, int D, int f16, float scale, int causal, int window,
                   int num_sms, cudaStream_t stream, int* err, const int* cu_q = nullptr,
-                  const int* cu_k = nullptr, int total_q = 0, int total_k = 0);
+                  const int* cu_k = nullptr, int total_q = 0, int total_k = 0,
+                  float softcap = 0.f, const float* sinks = nullptr);
 
 int launch_fwd_fp32(const float* q, const float* k, const float* v, float* o, float* lse, int B,
                     int Hq, int Hkv, int Nq, int Nk, int D, float scale, int causal, int window,

@@ -308,6 +308,13 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// 1/x on the special-function unit (approximate, flush-to-zero); 1/inf = 0.
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // max(a, b, c) in one instruction (three-input max of sm_100+).
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;

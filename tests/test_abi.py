@@ -161,6 +161,21 @@ def test_fp8_decode_argument_errors(L):
     assert paged8(page_size=100) == -2
 
 
+def test_softcap_sink_argument_errors(L):
+    def f(q=P, k=P, v=P, o=P, lse=P, B=2, Hq=8, Hkv=2, Nq=128, Nk=128, D=128, scale=0.1, causal=0,
+          window=0, cap=30.0, sinks=P):
+        return L.attn_fwd_softcap_sink(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, scale, causal, window, cap,
+                                       sinks, None)
+
+    assert f(q=None) == -1
+    assert f(D=96) == -4
+    assert f(Hq=8, Hkv=3) == -3
+    assert f(scale=0.0) == -6
+    assert f(cap=float("nan")) == -6
+    assert f(cap=float("inf")) == -6
+    assert f(sinks=ctypes.c_void_p(258)) == -5   # not 4-byte aligned
+
+
 def test_workspace_size(L):
     # O_part [B,Hq,S_max,D] + LSE_part [B,Hq,S_max], fp32, rounded up to 256 bytes
     n = L.attn_decode_workspace_size(64, 32, 128, 32768, 512)

@@ -422,3 +422,56 @@ def test_decode_fp8_nan_codes_in_unused_rows_do_not_leak(dev):
                                      1.0, 1.0)
     O, L = oracle.decode_forward_fp8(q, kc.numpy(), vc.numpy(), 1.0, 1.0, lens, 1 / math.sqrt(128))
     check(o, lse, O, L, BF16_O_TOL, BF16_LSE_REL, True)
+
+
+# ---------------------------------------------------------------- softcap and attention sinks
+def _sinks(Hq, kind, seed):
+    g = torch.Generator("cpu").manual_seed(seed)
+    if kind is None:
+        return None
+    s = torch.randn(Hq, generator=g) * 2.0
+    if kind == "extreme":          # one head never attends (sink dominates), one has no sink
+        s[0] = 30.0
+        s[-1] = -math.inf
+    return s.float()
+
+
+SOFTCAP_CASES = [
+    # B, Hq, Hkv, Nq, Nk, D, causal, window, cap, sinks
+    (1, 4, 4, 300, 300, 128, False, 0, 20.0, "normal"),
+    (2, 8, 2, 257, 257, 128, True, 0, 5.0, "extreme"),
+    (1, 4, 2, 300, 130, 128, True, 0, 10.0, "normal"),    # rows 0..169 see no key
+    (1, 4, 1, 384, 384, 128, True, 64, 0.0, "normal"),    # sinks only
+    (2, 4, 2, 200, 333, 64, False, 0, 30.0, None),        # cap only, D = 64
+    (1, 8, 8, 129, 1000, 128, True, 0, 50.0, "extreme"),  # chunked-prefill shape
+]
+
+
+@pytest.mark.parametrize("case", SOFTCAP_CASES, ids=lambda c: "-".join(map(str, c)))
+def test_softcap_sink(dev, case):
+    B, Hq, Hkv, Nq, Nk, D, causal, window, cap, kind = case
+    q, k, v = inputs.prefill_inputs(B, Hq, Hkv, Nq, Nk, D, "bf16", seed=Nq + Nk)
+    sinks = _sinks(Hq, kind, Nq)
+    o, lse = binding.attn_fwd_softcap_sink(q.to(dev), k.to(dev), v.to(dev), causal=causal, window=window,
+                                           softcap=cap, sinks=None if sinks is None else sinks.to(dev))
+    O, L = oracle.attention_forward_ext(q, k, v, 1 / math.sqrt(D), causal, window, cap,
+                                        None if sinks is None else sinks.numpy())
+    check(o, lse, O, L, BF16_O_TOL, BF16_LSE_REL, True)
+    if causal and Nq > Nk and sinks is not None:   # rows with no visible key: O = 0, LSE = sink
+        lo = lse.cpu()[:, :, : Nq - Nk]
+        assert torch.all(o.cpu()[:, :, : Nq - Nk].float() == 0)
+        assert torch.equal(lo, sinks.view(1, Hq, 1).expand_as(lo))
+    assert binding.get_device_error() == 0
+
+
+def test_softcap_sink_full_size_sampled(dev):
+    """Dense B=1 H=32 N=8192 D=128, softcap 50 and per-head sinks: sampled rows."""
+    q, k, v = inputs.prefill_inputs(1, 32, 32, 8192, 8192, 128, "bf16", seed=0)
+    sinks = _sinks(32, "extreme", 9)
+    o, lse = binding.attn_fwd_softcap_sink(q.to(dev), k.to(dev), v.to(dev), softcap=50.0, sinks=sinks.to(dev))
+    rows = sample_rows(1, 32, 8192, 24, seed=3)
+    O, L = oracle.attention_rows_ext(q, k, v, 1 / math.sqrt(128), rows, False, 0, 50.0, sinks.numpy())
+    og = torch.stack([o[b, h, i] for b, h, i in rows]).cpu()
+    lg = torch.stack([lse[b, h, i] for b, h, i in rows]).cpu()
+    check(og, lg, O, L, BF16_O_TOL, BF16_LSE_REL, True)
+    assert binding.get_device_error() == 0
