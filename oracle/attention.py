@@ -38,6 +38,11 @@ Sources (pages on softmax attention):
       block table ``[B, max_pages]`` names, for sequence b, the page of its
       logical page i, so key j of sequence b is row ``j % page_size`` of page
       ``block_table[b, j // page_size]``.
+    - the backward pass (named as missing work, "then the backward pass"): the
+      gradients of O with respect to Q, K and V for an upstream gradient dO,
+      by the chain rule through S = scale Q K^T (masked entries constant),
+      P = softmax(S) and O = P V; a KV head's K and V gradients sum over the
+      query heads that read it;
     - softcap and attention sinks (both on the list of masks, after vLLM's
       feature surface, which the same section names): with a cap c > 0 each
       scaled score becomes ``c * tanh(s / c)`` (masked scores stay -inf); a
@@ -65,6 +70,7 @@ __all__ = [
     "decode_combine", "paged_rows", "decode_forward_paged", "attention_varlen",
     "e4m3_to_float", "decode_forward_fp8", "decode_forward_paged_fp8",
     "softcap_scores", "attention_forward_ext", "attention_rows_ext",
+    "attention_backward",
 ]
 
 
@@ -443,3 +449,36 @@ def attention_rows_ext(q, k, v, scale: float, rows, causal: bool = False, window
         O[n] = (P @ _f64(v[b, kh]))[0]
         LSE[n] = lse[0]
     return O, LSE
+
+
+def _backward_head(Qh, Kh, Vh, dOh, scale: float, vis):
+    """One query head against its KV head: ``(dQ_h, dK_h, dV_h)``.
+
+    dV = P^T dO;  dP = dO V^T;  dS = P * (dP - rowsum(P * dP));
+    dQ = scale dS K;  dK = scale dS^T Q."""
+    S = _scores(Qh, Kh, scale)
+    S[~vis] = -np.inf
+    P, _ = _softmax_rows(S)
+    dV = P.T @ dOh
+    dP = dOh @ Vh.T
+    dS = P * (dP - (P * dP).sum(axis=1, keepdims=True))
+    return scale * (dS @ Kh), scale * (dS.T @ Qh), dV
+
+
+def attention_backward(q, k, v, do, scale: float, causal: bool = False, window: int = 0):
+    """Gradients of :func:`attention_forward`'s O for the upstream gradient
+    ``do`` ``[B,Hq,Nq,D]``: ``(dQ [B,Hq,Nq,D], dK [B,Hkv,Nk,D], dV [B,Hkv,Nk,D])``
+    in fp64."""
+    Q, K, V, dO = _f64(q), _f64(k), _f64(v), _f64(do)
+    B, Hq, Nq, D = Q.shape
+    Hkv, Nk = K.shape[1], K.shape[2]
+    vis = visible_mask(np.arange(Nq), Nq, Nk, causal, window)
+    dQ, dK, dV = np.zeros_like(Q), np.zeros_like(K), np.zeros_like(V)
+    for b in range(B):
+        for h in range(Hq):
+            kh = kv_head(h, Hq, Hkv)
+            gq, gk, gv = _backward_head(Q[b, h], K[b, kh], V[b, kh], dO[b, h], scale, vis)
+            dQ[b, h] = gq
+            dK[b, kh] += gk
+            dV[b, kh] += gv
+    return dQ, dK, dV

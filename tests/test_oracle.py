@@ -476,9 +476,46 @@ def pin_softcap_sink(ora):
         assert np.allclose(Or[n], Of[b, h, i], atol=1e-14) and abs(Lr[n] - Lf[b, h, i]) < 1e-14
 
 
+def pin_backward(ora):
+    """Backward: central finite differences of the loss sum(dO * O) through the
+    oracle's own forward, and float64 autograd through torch's SDPA (GQA by
+    repeated K/V heads), causal, windowed and dense."""
+    rng = np.random.default_rng(21)
+    B, Hq, Hkv, Nq, Nk, D = 1, 4, 2, 5, 6, 3
+    q, k, v = (rng.standard_normal(sh) for sh in ((B, Hq, Nq, D), (B, Hkv, Nk, D), (B, Hkv, Nk, D)))
+    do = rng.standard_normal((B, Hq, Nq, D))
+    sc, eps = 0.6, 1e-6
+    for causal, window in ((False, 0), (True, 0), (True, 3)):
+        dQ, dK, dV = ora.attention_backward(q, k, v, do, sc, causal, window)
+        loss = lambda qq, kk, vv: float((ora.attention_forward(qq, kk, vv, sc, causal, window)[0] * do).sum())  # noqa: E731
+        for name, x, g in (("q", q, dQ), ("k", k, dK), ("v", v, dV)):
+            for idx in [(0, 0, 0, 0), (0, 1, 2, 1), (0, Hkv - 1, 4, 2), (0, 0, 3, 2)]:
+                if idx[1] >= x.shape[1] or idx[2] >= x.shape[2]:
+                    continue
+                xp, xm = x.copy(), x.copy()
+                xp[idx] += eps
+                xm[idx] -= eps
+                args_p = {"q": (xp, k, v), "k": (q, xp, v), "v": (q, k, xp)}[name]
+                args_m = {"q": (xm, k, v), "k": (q, xm, v), "v": (q, k, xm)}[name]
+                fd = (loss(*args_p) - loss(*args_m)) / (2 * eps)
+                assert abs(fd - g[idx]) < 1e-7 * max(1.0, abs(fd)), (causal, window, name, idx, fd, g[idx])
+    for causal in (False, True):
+        B, Hq, Hkv, N, D = 2, 4, 2, 9, 8
+        q, k, v, do = (rng.standard_normal(sh) for sh in ((B, Hq, N, D), (B, Hkv, N, D), (B, Hkv, N, D), (B, Hq, N, D)))
+        tq = torch.tensor(q, requires_grad=True)
+        tk = torch.tensor(k, requires_grad=True)
+        tv = torch.tensor(v, requires_grad=True)
+        out = torch.nn.functional.scaled_dot_product_attention(
+            tq, tk.repeat_interleave(2, dim=1), tv.repeat_interleave(2, dim=1), is_causal=causal, scale=0.4)
+        out.backward(torch.tensor(do))
+        dQ, dK, dV = ora.attention_backward(q, k, v, do, 0.4, causal, 0)
+        for mine, ref in ((dQ, tq.grad), (dK, tk.grad), (dV, tv.grad)):
+            assert np.allclose(mine, ref.numpy(), rtol=0, atol=1e-12)
+
+
 PINS = [pin_brute_force, pin_sdpa, pin_zero_query, pin_single_key, pin_probability_rows,
         pin_causal_first_row, pin_dominant_key, pin_invariants, pin_decode, pin_paged_decode, pin_varlen,
-        pin_golden, pin_e4m3_codes, pin_fp8_decode, pin_softcap_sink]
+        pin_golden, pin_e4m3_codes, pin_fp8_decode, pin_softcap_sink, pin_backward]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
@@ -624,6 +661,36 @@ def _mut_sink_dropped(S, sink):
     return ORA._softmax_rows(S)
 
 
+def _mut_bwd_no_dsum(Qh, Kh, Vh, dOh, scale, vis):
+    S = ORA._scores(Qh, Kh, scale)
+    S[~vis] = -np.inf
+    P, _ = ORA._softmax_rows(S)
+    dS = P * (dOh @ Vh.T)
+    return scale * (dS @ Kh), scale * (dS.T @ Qh), P.T @ dOh
+
+
+def _mut_bwd_dk_unscaled(Qh, Kh, Vh, dOh, scale, vis):
+    S = ORA._scores(Qh, Kh, scale)
+    S[~vis] = -np.inf
+    P, _ = ORA._softmax_rows(S)
+    dP = dOh @ Vh.T
+    dS = P * (dP - (P * dP).sum(axis=1, keepdims=True))
+    return scale * (dS @ Kh), dS.T @ Qh, P.T @ dOh
+
+
+def _mut_bwd_dv_untransposed(Qh, Kh, Vh, dOh, scale, vis):
+    gq, gk, gv = _GOOD_BWD(Qh, Kh, Vh, dOh, scale, vis)
+    S = ORA._scores(Qh, Kh, scale)
+    S[~vis] = -np.inf
+    P, _ = ORA._softmax_rows(S)
+    if P.shape[0] == P.shape[1]:
+        return gq, gk, P @ dOh
+    return gq, gk, (P.T @ dOh)[::-1]
+
+
+_GOOD_BWD = ORA._backward_head
+
+
 MUTANTS = {
     "no_scale": ("_scores", _mut_no_scale),
     "sqrt_scale": ("_scores", _mut_sqrt_scale),
@@ -642,6 +709,9 @@ MUTANTS = {
     "softcap_without_divide": ("softcap_scores", _mut_softcap_no_divide),
     "sink_unshifted": ("_softmax_rows_sink", _mut_sink_unshifted),
     "sink_dropped": ("_softmax_rows_sink", _mut_sink_dropped),
+    "bwd_missing_rowsum_term": ("_backward_head", _mut_bwd_no_dsum),
+    "bwd_dk_unscaled": ("_backward_head", _mut_bwd_dk_unscaled),
+    "bwd_dv_untransposed": ("_backward_head", _mut_bwd_dv_untransposed),
 }
 
 
