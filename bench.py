@@ -85,7 +85,7 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--workload", choices=["dense", "causal", "decode", "fp32", "window", "chunked", "d64",
-                                           "paged", "fp16", "varlen", "decode_fp8", "softcap"],
+                                           "paged", "fp16", "varlen", "decode_fp8", "softcap", "bwd"],
                     default="dense",
                     help="workload of the timed loop (default: the dense bf16 prefill)")
     ap.add_argument("--no-extras", action="store_true", help="skip the other workloads")
@@ -272,6 +272,7 @@ WORKLOAD_NAMES = {
     "decode_fp8": "split-KV decode on an fp8 E4M3 KV cache (bf16 Q) B=64 Hq=32 Hkv=8 D=128, Nk_b~U[512,32768], "
                   "chunk 512",
     "softcap": "bf16 dense prefill B=1 H=32 N=8192 D=128 with softcap 50 and per-head attention sinks",
+    "bwd": "bf16 backward (dQ, dK, dV) B=1 H=32 N=8192 D=128 (non-causal); FLOPs = 2.5 x forward",
 }
 
 
@@ -280,7 +281,26 @@ def make_workload(name, dev, seed, peaks, peak_src, sm_max_mhz, decode_batch=Non
     import torch
     from softmax_attention_attn_gb300 import binding, inputs
     w = {"name": name, "desc": WORKLOAD_NAMES[name]}
-    if name == "varlen":
+    if name == "bwd":
+        c = MAIN
+        host = inputs.prefill_inputs(c["B"], c["Hq"], c["Hkv"], c["N"], c["N"], c["D"], "bf16", seed)
+        q, k, v = (x.to(dev) for x in host)
+        do = torch.randn(c["B"], c["Hq"], c["N"], c["D"], generator=torch.Generator("cpu").manual_seed(seed + 9))
+        do = do.to(torch.bfloat16).to(dev)
+        o, lse = binding.attn_fwd(q, k, v)
+        dq = torch.empty(q.shape, device=dev, dtype=torch.float32)
+        dk, dv = torch.empty_like(k), torch.empty_like(v)
+        ws = torch.empty(binding.lib().attn_bwd_workspace_size(c["B"], c["Hq"], c["N"]), device=dev,
+                         dtype=torch.uint8)
+        w["fn"] = lambda: binding.attn_bwd(q, k, v, o, do, lse, dq, dk, dv, ws)
+        w["work"] = 2.5 * flops(**c)
+        w["unit"], w["launches"], w["dtype"] = "TFLOP/s", 2, "bf16"
+        w["seq_len"], w["batch"] = c["N"], c["B"]
+        w["bound"], w["peak"] = "tensor", peaks["bf16_tflops"]
+        w["peak_source"] = f"{peak_src} dense bf16 (burst)"
+        w["e2e_in"] = [(x, t) for x, t in zip(host, (q, k, v))]
+        w["e2e_out"] = [dq, dk, dv]
+    elif name == "varlen":
         c = VARLEN
         g = torch.Generator("cpu").manual_seed(seed + 11)
         lens = torch.randint(c["n_lo"], c["n_hi"] + 1, (c["B"],), generator=g).tolist()
@@ -499,7 +519,7 @@ def run_gb300(args, rank, world, local_rank):
     if not args.no_extras:
         xs = max(5, min(args.steps // 10, 50))
         for name in ("dense", "causal", "decode", "paged", "decode_fp8", "fp32", "window", "chunked", "d64", "fp16",
-                     "varlen", "softcap"):
+                     "varlen", "softcap", "bwd"):
             if name == args.workload:
                 continue
             x = make_workload(name, dev, rank, peaks, peak_src, sm_max, args.decode_batch)

@@ -201,6 +201,36 @@ int attn_decode_splitkv_paged(const void* q, const void* k_pages, const void* v_
                               int D, float scale, int chunk, attn_stream_t stream);
 
 /*
+ * attn_bwd_workspace_size — bytes of device workspace attn_bwd needs:
+ *   2 * B * Hq * ceil(Nq / 64) * 64 * 4 (per query: LSE * log2(e) and D).
+ */
+size_t attn_bwd_workspace_size(int B, int Hq, int Nq);
+
+/*
+ * attn_bwd — attention backward: the gradients of attn_fwd's O with respect to
+ * Q, K and V for an upstream gradient dO.   [DEVLOG] 二 (the forward
+ * O = softmax(scale Q K^T) V); [ASK] "研究动机" (forward only there; the
+ * backward pass is named as the next piece of work).
+ *
+ *   q, o, dout : bf16 [B, Hq, Nq, D]; k, v : bf16 [B, Hkv, Nk, D]
+ *   lse        : float32 [B, Hq, Nq], the forward's LSE (natural log; -inf for
+ *                rows with no visible key) for the same q, k, v, scale, causal
+ *   dq         : float32 [B, Hq, Nq, D] (output; zeroed, then accumulated)
+ *   dk, dv     : bf16 [B, Hkv, Nk, D] (outputs; K/V gradients of a KV head sum
+ *                over the query heads that read it)
+ *   workspace  : device buffer of attn_bwd_workspace_size(B, Hq, Nq) bytes
+ *   causal     : bottom-right aligned as in attn_fwd; no sliding window
+ *   D must be 128.  All device pointers 16-byte aligned, contiguous; the
+ *   caller owns every buffer.  Asynchronous on `stream`.
+ *   Errors: ATTN_ERR_NULL, ATTN_ERR_DIM, ATTN_ERR_GQA, ATTN_ERR_HEAD_DIM,
+ *   ATTN_ERR_ALIGN, ATTN_ERR_SCALE, ATTN_ERR_CUDA; a bounded wait that runs
+ *   out sets ATTN_ERR_TIMEOUT in the device error word.
+ */
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+             const float* lse, float* dq, void* dk, void* dv, void* workspace, int B, int Hq,
+             int Hkv, int Nq, int Nk, int D, float scale, int causal, attn_stream_t stream);
+
+/*
  * attn_decode_splitkv_fp8 — split-KV decode, partial step, on an fp8 KV cache.
  *   [ASK] "研究动机" (bf16/fp16/fp8 data types, fp8-KV decode shapes).
  *

@@ -37,6 +37,8 @@ SIGNATURES = {
                                 + [_c_float, _c_int, _vp]),
     "attn_decode_splitkv_paged_fp8": (_c_int, [_vp] * 3 + [_c_float] * 2 + [_vp] * 3 + [_c_int] * 7
                                       + [_c_float, _c_int, _vp]),
+    "attn_bwd_workspace_size": (ctypes.c_size_t, [_c_int] * 3),
+    "attn_bwd": (_c_int, [_vp] * 10 + [_c_int] * 6 + [_c_float, _c_int, _vp]),
     "attn_get_device_error": (_c_int, [_vp]),
     "attn_strerror": (ctypes.c_char_p, [_c_int]),
 }
@@ -144,6 +146,37 @@ def attn_fwd_softcap_sink(q, k, v, o=None, lse=None, scale=None, causal=False, w
                                        _ptr(sinks) if sinks is not None else None, _stream(stream))
     _check(code, "attn_fwd_softcap_sink")
     return o, lse
+
+
+def attn_bwd(q, k, v, o, do, lse, dq=None, dk=None, dv=None, workspace=None, scale=None, causal=False,
+             stream=None):
+    """bf16 backward: (dq fp32 ``[B,Hq,Nq,D]``, dk, dv bf16 ``[B,Hkv,Nk,D]``) for the
+    upstream gradient ``do``, from the forward's ``o`` and ``lse``."""
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (do, "do")):
+        _require(t, torch.bfloat16, n)
+    _require(lse, torch.float32, "lse")
+    B, Hq, Nq, D = q.shape
+    _, Hkv, Nk, _ = k.shape
+    if dq is None:
+        dq = torch.empty(B, Hq, Nq, D, device=q.device, dtype=torch.float32)
+    if dk is None:
+        dk = torch.empty_like(k)
+    if dv is None:
+        dv = torch.empty_like(v)
+    need = int(lib().attn_bwd_workspace_size(B, Hq, Nq))
+    if workspace is None:
+        workspace = torch.empty(need, device=q.device, dtype=torch.uint8)
+    if workspace.numel() * workspace.element_size() < need:
+        raise ValueError(f"workspace holds fewer than {need} bytes")
+    _require(dq, torch.float32, "dq")
+    _require(dk, torch.bfloat16, "dk")
+    _require(dv, torch.bfloat16, "dv")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    code = lib().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
+                          _ptr(workspace), B, Hq, Hkv, Nq, Nk, D, scale, int(bool(causal)), _stream(stream))
+    _check(code, "attn_bwd")
+    return dq, dk, dv
 
 
 def attn_fwd_fp16(q, k, v, o=None, lse=None, scale=None, causal=False, window=0, stream=None):

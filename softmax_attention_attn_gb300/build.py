@@ -21,7 +21,7 @@ LIB_NAME = "libattn.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
 
 SOURCES = ["attn_abi.cu", "attn_fwd_bf16.cu", "attn_fwd_fp32.cu", "attn_decode.cu",
-           "attn_decode_noalloc.cu"]
+           "attn_decode_noalloc.cu", "attn_bwd.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                      "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]

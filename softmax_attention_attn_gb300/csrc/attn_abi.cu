@@ -246,6 +246,32 @@ int attn_decode_splitkv_paged(const void* q, const void* k_pages, const void* v_
                                      dev->num_sms, reinterpret_cast<cudaStream_t>(stream), dev->err);
 }
 
+size_t attn_bwd_workspace_size(int B, int Hq, int Nq) {
+  if (B <= 0 || Hq <= 0 || Nq <= 0) return 0;
+  return bwd_workspace_bytes(B, Hq, Nq);
+}
+
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+             const float* lse, float* dq, void* dk, void* dv, void* workspace, int B, int Hq,
+             int Hkv, int Nq, int Nk, int D, float scale, int causal, attn_stream_t stream) {
+  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || !workspace) return ATTN_ERR_NULL;
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Nq <= 0 || Nk <= 0 || D <= 0) return ATTN_ERR_DIM;
+  if (Hq % Hkv != 0) return ATTN_ERR_GQA;
+  if (D != 128) return ATTN_ERR_HEAD_DIM;
+  if (static_cast<long long>(B) * Hq * Nq > (1ll << 31) || static_cast<long long>(B) * Hkv > 65535 ||
+      B > 65535)
+    return ATTN_ERR_DIM;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) ||
+      !aligned16(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(workspace))
+    return ATTN_ERR_ALIGN;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_SCALE;
+  DeviceInfo* dev = nullptr;
+  int rc = device_info(&dev);
+  if (rc != ATTN_OK) return rc;
+  return launch_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, B, Hq, Hkv, Nq, Nk, scale, causal,
+                    reinterpret_cast<cudaStream_t>(stream), dev->err);
+}
+
 int attn_decode_splitkv_fp8(const void* q, const void* k_cache, const void* v_cache, float k_scale,
                             float v_scale, const int* seqlens, void* workspace, int B, int Hq,
                             int Hkv, int Nk_max, int D, float scale, int chunk,

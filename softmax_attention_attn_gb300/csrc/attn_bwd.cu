@@ -1,0 +1,476 @@
+// attn_bwd.cu — bf16 attention backward (dQ, dK, dV) for sm_103a on tcgen05.
+//
+// The gradients of the forward of "Agent 帮我写 CUDA：一个 Softmax Attention
+// 算子的开发全记录" (section 二: O = softmax(scale Q K^T) V) for an upstream
+// gradient dO, the backward pass named as missing work in "Ask, Don't Equip:
+// ..." (section "研究动机", forward only; "then the backward pass"):
+//
+//   P = exp(scale Q K^T - LSE)   (LSE from the forward; masked entries 0)
+//   dV = P^T dO      dP = dO V^T      D = rowsum(dO * O) = rowsum(P * dP)
+//   dS = P * (dP - D)      dQ = scale dS K      dK = scale dS^T Q
+//   (K and V gradients of a KV head sum over the query heads that read it).
+//
+// Design: one CTA per (batch, KV head, 128-key tile j); it keeps K_j and V_j
+// in shared memory and dK_j, dV_j in tensor memory while it walks every query
+// head of the KV head's group and every 64-query tile i that sees the key
+// tile.  With the keys on the tensor-memory lanes:
+//   * S^T = K_j Q_i^T and dP^T = V_j dO_i^T (M = 128 keys, N = 64 queries);
+//   * four row warps (thread r owns key r) form P^T and dS^T = scale P^T (dP^T - D)
+//     in fp32, write both as bf16 into the S^T / dP^T columns they read, and
+//     dS^T also into shared memory;
+//   * dV_j += P^T dO_i and dK_j += dS^T Q_i (A from tensor memory, the TS form);
+//   * dQ_i^T = K_j^T dS^T (M = 128 head dims, N = 64 queries; both operands
+//     MN-major in shared memory); the row warps read it (thread r owns head
+//     dim r) and add it to the fp32 dQ with global atomics;
+//   * one TMA warp streams Q_i, dO_i (and the per-query LSE*log2(e) and D
+//     vectors, prepared by attn_bwd_prep_kernel) through a 3-stage ring; one
+//     thread issues every MMA.
+// Tensor memory (512 columns): S^T [0,64) dP^T [64,128) dV [128,256)
+// dK [256,384) dQ^T [384,448).  Every wait is bounded (see ptx.cuh).
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math_constants.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace attn {
+namespace bwd {
+
+constexpr int HD = 128;
+constexpr int BK = 128;                          // keys per CTA
+constexpr int BQ = 64;                           // queries per step
+constexpr int NS = 3;                            // Q / dO ring stages
+constexpr int KSLAB = BK * 128;                  // 64-column slab of a 128-row tile (16 KB)
+constexpr int QSLAB = BQ * 128;                  // 64-column slab of a 64-row tile (8 KB)
+constexpr int SM_K = 0;
+constexpr int SM_V = SM_K + 2 * KSLAB;
+constexpr int SM_STAGE = SM_V + 2 * KSLAB;
+constexpr int STAGE_BYTES = 4 * QSLAB;           // Q_i (2 slabs) + dO_i (2 slabs)
+constexpr int SM_DS = SM_STAGE + NS * STAGE_BYTES;  // dS^T [128 keys][64 queries] bf16, one slab
+constexpr int VEC_BYTES = 2 * BQ * 4;            // LSE*log2(e)[64], D[64]
+constexpr int SM_VEC = SM_DS + KSLAB;
+constexpr int SM_BAR = SM_VEC + NS * VEC_BYTES;
+constexpr int NUM_BARS = 1 + 2 * NS + 6;
+constexpr int SM_MISC = SM_BAR + NUM_BARS * 8;
+constexpr int SMEM_ALLOC = SM_MISC + 16 + 1024;  // + slack for 1024-byte alignment
+static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
+constexpr int WARP_TMA = 4;
+constexpr int WARP_MMA = 5;
+constexpr int NTHREADS = 6 * 32;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t COL_S = 0, COL_DP = 64, COL_DV = 128, COL_DK = 256, COL_DQ = 384;
+
+// Instruction descriptor, kind::f16 with bf16 A/B and fp32 D; bit 15 / 16 set
+// the A / B operand MN-major.
+constexpr uint32_t idesc(uint32_t M, uint32_t N, uint32_t a_mn, uint32_t b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (a_mn << 15) | (b_mn << 16) | ((N >> 3) << 17) |
+         ((M >> 4) << 24);
+}
+constexpr uint32_t ID_ST = idesc(BK, BQ, 0, 0);   // S^T, dP^T: K / V and Q / dO, both K-major
+constexpr uint32_t ID_GRAD = idesc(BK, HD, 0, 1); // dV, dK: P^T / dS^T in TMEM, dO / Q MN-major
+constexpr uint32_t ID_DQ = idesc(HD, BQ, 1, 1);   // dQ^T: K^T and dS^T, both MN-major
+
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t off16) {
+  uint32_t lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=r"(lo), "=r"(hi) : "l"(d));
+  lo += off16;
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+  return r;
+}
+
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  const unsigned long long t0 = global_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_ns() - t0 > kAttnWaitNs) break;
+  }
+}
+
+struct BwdParams {
+  const float* lse2;   // [B*Hq][Nq_pad]: LSE * log2(e); +inf on padding and on rows with no key
+  const float* delta;  // [B*Hq][Nq_pad]: rowsum(dO * O); 0 on padding
+  float* dq;           // [B, Hq, Nq, D] fp32, accumulated (zeroed before the launch)
+  __nv_bfloat16* dk;   // [B, Hkv, Nk, D]
+  __nv_bfloat16* dv;
+  int B, Hq, Hkv, Nq, Nk, Nq_pad, group;
+  float c_log2;        // scale * log2(e)
+  float scale;
+  int causal;
+  int* err;
+};
+
+// D = rowsum(dO * O) and LSE * log2(e) per query row, padded to 64 rows per head.
+__global__ void __launch_bounds__(256)
+attn_bwd_prep_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
+                     const float* __restrict__ lse, float* __restrict__ lse2, float* __restrict__ delta,
+                     long long rows_pad, int Nq, int Nq_pad) {
+  const long long r = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int lane = static_cast<int>(threadIdx.x & 31);
+  if (r >= rows_pad) return;
+  const long long bh = r / Nq_pad;
+  const int i = static_cast<int>(r - bh * Nq_pad);
+  if (i >= Nq) {
+    if (lane == 0) {
+      delta[r] = 0.f;
+      lse2[r] = CUDART_INF_F;
+    }
+    return;
+  }
+  const long long src = (bh * Nq + i) * HD + lane * 4;
+  const uint2 uo = *reinterpret_cast<const uint2*>(o + src);
+  const uint2 ud = *reinterpret_cast<const uint2*>(dout + src);
+  const float o4[4] = {__uint_as_float(uo.x << 16), __uint_as_float(uo.x & 0xFFFF0000u),
+                       __uint_as_float(uo.y << 16), __uint_as_float(uo.y & 0xFFFF0000u)};
+  const float d4[4] = {__uint_as_float(ud.x << 16), __uint_as_float(ud.x & 0xFFFF0000u),
+                       __uint_as_float(ud.y << 16), __uint_as_float(ud.y & 0xFFFF0000u)};
+  float s = (o4[0] * d4[0] + o4[1] * d4[1]) + (o4[2] * d4[2] + o4[3] * d4[3]);
+#pragma unroll
+  for (int k = 16; k >= 1; k >>= 1) s += __shfl_xor_sync(0xffffffffu, s, k);
+  if (lane == 0) {
+    delta[r] = s;
+    const float l = lse[bh * Nq + i];
+    lse2[r] = l == -CUDART_INF_F ? CUDART_INF_F : l * 1.4426950408889634f;
+  }
+}
+
+__global__ void __launch_bounds__(NTHREADS, 1)
+attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                const BwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  const uint32_t sb = smem_u32(smem);
+  const int warp = warp_id_uniform();
+  const int lane = static_cast<int>(lane_id());
+
+  const uint32_t bar_kv_full = sb + SM_BAR;                                 // K_j, V_j landed
+  auto bar_q_full = [&](int s) { return sb + SM_BAR + 8u * (1 + s); };       // stage s landed
+  auto bar_q_empty = [&](int s) { return sb + SM_BAR + 8u * (1 + NS + s); }; // stage s read by every MMA
+  const uint32_t bar_s_full = sb + SM_BAR + 8u * (1 + 2 * NS);              // S^T, dP^T in TMEM
+  const uint32_t bar_p_ready = bar_s_full + 8;                              // P^T, dS^T written
+  const uint32_t bar_dq_full = bar_s_full + 16;                             // dQ^T in TMEM
+  const uint32_t bar_dq_empty = bar_s_full + 24;                            // dQ^T read out
+  const uint32_t bar_kv_done = bar_s_full + 32;                             // dK, dV complete
+  const uint32_t bar_mma_done = bar_s_full + 40;                            // every MMA complete
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + SM_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SM_MISC + 4);
+
+  const int j0 = static_cast<int>(blockIdx.x) * BK;
+  const int kvh = static_cast<int>(blockIdx.y);
+  const int b = static_cast<int>(blockIdx.z);
+  const int off = p.Nk - p.Nq;  // bottom-right causal: key k visible to query q iff k <= q + off
+  const int n_qt = (p.Nq + BQ - 1) / BQ;
+  int it0 = 0;  // first query tile with a query that sees a key of this tile
+  if (p.causal && j0 - off > 0) it0 = (j0 - off) / BQ;
+  const int per_head = max(0, n_qt - it0);
+  const int n_steps = per_head * p.group;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar_kv_full, 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(bar_q_full(s), 1);
+      mbar_init(bar_q_empty(s), 1);
+    }
+    mbar_init(bar_s_full, 1);
+    mbar_init(bar_p_ready, 4);
+    mbar_init(bar_dq_full, 1);
+    mbar_init(bar_dq_empty, 4);
+    mbar_init(bar_kv_done, 1);
+    mbar_init(bar_mma_done, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == WARP_MMA) {
+    tmem_alloc(smem_u32(tmem_holder), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  auto step_head = [&](int step) { return kvh * p.group + step / max(per_head, 1); };
+  auto step_q0 = [&](int step) { return (it0 + step % max(per_head, 1)) * BQ; };
+
+  if (warp == WARP_TMA) {
+    // ================================================================ producer
+    if (lane == 0 && n_steps > 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      tma_prefetch_desc(&tm_do);
+      mbar_arrive_expect_tx(bar_kv_full, 4 * KSLAB);
+      for (int kb = 0; kb < 2; ++kb) {
+        tma_load_3d(sb + SM_K + kb * KSLAB, &tm_k, bar_kv_full, kb * 64, j0, b * p.Hkv + kvh);
+        tma_load_3d(sb + SM_V + kb * KSLAB, &tm_v, bar_kv_full, kb * 64, j0, b * p.Hkv + kvh);
+      }
+      int step = 0;
+      bool ok = true;
+      for (; step < n_steps && ok; ++step) {
+        const int s = step % NS, use = step / NS;
+        if (use > 0 && !mbar_wait(bar_q_empty(s), (use - 1) & 1, abort_flag, p.err)) {
+          ok = false;
+          break;
+        }
+        const int h = step_head(step), i0 = step_q0(step);
+        const uint32_t st = sb + SM_STAGE + s * STAGE_BYTES;
+        const uint32_t vec = sb + SM_VEC + s * VEC_BYTES;
+        mbar_arrive_expect_tx(bar_q_full(s), STAGE_BYTES + VEC_BYTES);
+        for (int kb = 0; kb < 2; ++kb) {
+          tma_load_3d(st + kb * QSLAB, &tm_q, bar_q_full(s), kb * 64, i0, b * p.Hq + h);
+          tma_load_3d(st + 2 * QSLAB + kb * QSLAB, &tm_do, bar_q_full(s), kb * 64, i0, b * p.Hq + h);
+        }
+        const size_t vrow = (static_cast<size_t>(b) * p.Hq + h) * p.Nq_pad + i0;
+        bulk_load(vec, p.lse2 + vrow, BQ * 4, bar_q_full(s));
+        bulk_load(vec + BQ * 4, p.delta + vrow, BQ * 4, bar_q_full(s));
+      }
+      if (!ok) {  // let the copies already issued land before the CTA exits
+        drain_wait(bar_kv_full, 0);
+        for (int i = max(0, step - NS); i < step; ++i) drain_wait(bar_q_full(i % NS), (i / NS) & 1);
+      }
+    }
+  } else if (warp == WARP_MMA) {
+    // ================================================================ MMA issuer
+    if (lane == 0 && n_steps > 0) {
+      const uint64_t k_kmaj = smem_desc_sw128(sb + SM_K, 16, 1024);   // K as A, K-major
+      const uint64_t v_kmaj = smem_desc_sw128(sb + SM_V, 16, 1024);
+      const uint64_t k_mn = smem_desc_sw128(sb + SM_K, KSLAB, 1024);  // K^T as A, MN-major
+      const uint64_t ds_mn = smem_desc_sw128(sb + SM_DS, KSLAB, 1024); // dS^T as B, MN-major
+      bool ok = mbar_wait(bar_kv_full, 0, abort_flag, p.err);
+      for (int step = 0; step < n_steps && ok; ++step) {
+        const int s = step % NS;
+        const uint32_t st = sb + SM_STAGE + s * STAGE_BYTES;
+        const uint64_t q_kmaj = smem_desc_sw128(st, 16, 1024);
+        const uint64_t do_kmaj = smem_desc_sw128(st + 2 * QSLAB, 16, 1024);
+        const uint64_t q_mn = smem_desc_sw128(st, QSLAB, 1024);
+        const uint64_t do_mn = smem_desc_sw128(st + 2 * QSLAB, QSLAB, 1024);
+        if (!mbar_wait(bar_q_full(s), (step / NS) & 1, abort_flag, p.err)) { ok = false; break; }
+        tc_fence_after();
+        // S^T = K_j Q_i^T, dP^T = V_j dO_i^T
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          const uint32_t a_off = static_cast<uint32_t>((kk >> 2) * KSLAB + (kk & 3) * 32) >> 4;
+          const uint32_t b_off = static_cast<uint32_t>((kk >> 2) * QSLAB + (kk & 3) * 32) >> 4;
+          mma_bf16_ss(tmem + COL_S, desc_add(k_kmaj, a_off), desc_add(q_kmaj, b_off), ID_ST, kk > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          const uint32_t a_off = static_cast<uint32_t>((kk >> 2) * KSLAB + (kk & 3) * 32) >> 4;
+          const uint32_t b_off = static_cast<uint32_t>((kk >> 2) * QSLAB + (kk & 3) * 32) >> 4;
+          mma_bf16_ss(tmem + COL_DP, desc_add(v_kmaj, a_off), desc_add(do_kmaj, b_off), ID_ST, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar_s_full);
+        if (!mbar_wait(bar_p_ready, step & 1, abort_flag, p.err)) { ok = false; break; }
+        tc_fence_after();
+        // dV_j += P^T dO_i, dK_j += dS^T Q_i  (16 queries per K step)
+#pragma unroll
+        for (int kk = 0; kk < BQ / 16; ++kk) {
+          const uint32_t boff = static_cast<uint32_t>(kk * 16 * 128) >> 4;
+          mma_bf16_ts(tmem + COL_DV, tmem + COL_S + kk * 8, desc_add(do_mn, boff), ID_GRAD,
+                      (step > 0 || kk > 0) ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < BQ / 16; ++kk) {
+          const uint32_t boff = static_cast<uint32_t>(kk * 16 * 128) >> 4;
+          mma_bf16_ts(tmem + COL_DK, tmem + COL_DP + kk * 8, desc_add(q_mn, boff), ID_GRAD,
+                      (step > 0 || kk > 0) ? 1u : 0u);
+        }
+        // dQ_i^T = K_j^T dS^T (16 keys per K step); the previous dQ^T must be read out
+        if (step > 0 && !mbar_wait(bar_dq_empty, (step - 1) & 1, abort_flag, p.err)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk) {
+          const uint32_t off16 = static_cast<uint32_t>(kk * 16 * 128) >> 4;
+          mma_bf16_ss(tmem + COL_DQ, desc_add(k_mn, off16), desc_add(ds_mn, off16), ID_DQ, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar_dq_full);
+        mma_commit(bar_q_empty(s));
+      }
+      if (ok) mma_commit(bar_kv_done);
+      mma_commit(bar_mma_done);
+      drain_wait(bar_mma_done, 0);
+    }
+  } else if (warp < 4) {
+    // ================================================================ row warps
+    const int quad = warp;
+    const uint32_t lane_sel = static_cast<uint32_t>(quad * 32) << 16;
+    const int r = quad * 32 + lane;  // key row (S^T, dP^T, dV, dK) / head dim (dQ^T) of this thread
+    const int key = j0 + r;
+    const bool key_ok = key < p.Nk;
+    bool ok = true;
+    for (int step = 0; step < n_steps && ok; ++step) {
+      const int s = step % NS;
+      const int h = step_head(step), i0 = step_q0(step);
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_q_full(s), (step / NS) & 1, abort_flag, p.err) &&
+                                       mbar_wait(bar_s_full, step & 1, abort_flag, p.err));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t sr[2][32], dr[2][32];
+      tmem_ld32(tmem + lane_sel + COL_S, sr[0]);
+      tmem_ld32(tmem + lane_sel + COL_S + 32, sr[1]);
+      tmem_ld32(tmem + lane_sel + COL_DP, dr[0]);
+      tmem_ld32(tmem + lane_sel + COL_DP + 32, dr[1]);
+      tmem_wait_ld();
+      const float* lse2v = reinterpret_cast<const float*>(smem + SM_VEC + s * VEC_BYTES);
+      const float* deltav = lse2v + BQ;
+      // causal: query c of this step sees this key iff key <= i0 + c + off
+      const int c_min = p.causal ? key - off - i0 : 0;  // first visible query index (may be < 0)
+      uint32_t pk[32], dk[32];
+#pragma unroll
+      for (int c = 0; c < BQ; c += 2) {
+        float pv[2], dsv[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int cc = c + e;
+          const float sv = __uint_as_float(sr[cc >> 5][cc & 31]);
+          const float dpv = __uint_as_float(dr[cc >> 5][cc & 31]);
+          const bool vis = key_ok && cc >= c_min;
+          const float pr = vis ? ex2_approx(fmaf(sv, p.c_log2, -lse2v[cc])) : 0.f;
+          pv[e] = pr;
+          dsv[e] = pr * (dpv - deltav[cc]) * p.scale;
+        }
+        pk[c >> 1] = pack_bf16x2(pv[0], pv[1]);
+        dk[c >> 1] = pack_bf16x2(dsv[0], dsv[1]);
+      }
+      // P^T over S^T columns [0, 32), dS^T over dP^T columns [64, 96)
+      tmem_st16(tmem + lane_sel + COL_S, *reinterpret_cast<const uint32_t(*)[16]>(pk));
+      tmem_st16(tmem + lane_sel + COL_S + 16, *reinterpret_cast<const uint32_t(*)[16]>(pk + 16));
+      tmem_st16(tmem + lane_sel + COL_DP, *reinterpret_cast<const uint32_t(*)[16]>(dk));
+      tmem_st16(tmem + lane_sel + COL_DP + 16, *reinterpret_cast<const uint32_t(*)[16]>(dk + 16));
+      // dS^T row r into shared memory (128-byte rows, 128-byte swizzle: 16-byte
+      // chunk c of row r sits at chunk c ^ (r % 8)); the previous step's dQ MMA
+      // has read the tile (its completion was waited on before that read-out)
+      uint8_t* ds_row = smem + SM_DS + r * 128;
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4*>(ds_row + ((c ^ (r & 7)) * 16)) =
+            make_uint4(dk[4 * c], dk[4 * c + 1], dk[4 * c + 2], dk[4 * c + 3]);
+      fence_proxy_async_smem();
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_p_ready);
+      // dQ_i^T read-out: this thread holds head dim r of the 64 queries
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_dq_full, step & 1, abort_flag, p.err));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t qr[2][32];
+      tmem_ld32(tmem + lane_sel + COL_DQ, qr[0]);
+      tmem_ld32(tmem + lane_sel + COL_DQ + 32, qr[1]);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_dq_empty);
+      float* dq = p.dq + (static_cast<size_t>(b) * p.Hq + h) * p.Nq * HD + static_cast<size_t>(i0) * HD + r;
+      const int nq = min(BQ, p.Nq - i0);
+#pragma unroll
+      for (int c = 0; c < BQ; ++c)
+        if (c < nq) atomicAdd(dq + static_cast<size_t>(c) * HD, __uint_as_float(qr[c >> 5][c & 31]));
+    }
+    // dK_j, dV_j: this thread's key row
+    if (ok) {
+      if (n_steps > 0) ok = __all_sync(0xffffffffu, mbar_wait(bar_kv_done, 0, abort_flag, p.err));
+      if (ok) {
+        tc_fence_after();
+        const size_t orow = (static_cast<size_t>(b) * p.Hkv + kvh) * p.Nk + key;
+#pragma unroll
+        for (int which = 0; which < 2; ++which) {
+          uint32_t g[HD];
+          if (n_steps > 0) {
+#pragma unroll
+            for (int ch = 0; ch < HD / 32; ++ch) {
+              uint32_t (&gc)[32] = *reinterpret_cast<uint32_t(*)[32]>(g + 32 * ch);
+              tmem_ld32(tmem + lane_sel + (which ? COL_DK : COL_DV) + ch * 32, gc);
+            }
+            tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int i = 0; i < HD; ++i) g[i] = 0u;
+          }
+          if (key_ok) {
+            uint4* dst = reinterpret_cast<uint4*>((which ? p.dk : p.dv) + orow * HD);
+#pragma unroll
+            for (int i = 0; i < HD / 8; ++i)
+              dst[i] = make_uint4(pack_bf16x2(__uint_as_float(g[8 * i + 0]), __uint_as_float(g[8 * i + 1])),
+                                  pack_bf16x2(__uint_as_float(g[8 * i + 2]), __uint_as_float(g[8 * i + 3])),
+                                  pack_bf16x2(__uint_as_float(g[8 * i + 4]), __uint_as_float(g[8 * i + 5])),
+                                  pack_bf16x2(__uint_as_float(g[8 * i + 6]), __uint_as_float(g[8 * i + 7])));
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == WARP_MMA) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+}  // namespace bwd
+
+size_t bwd_workspace_bytes(int B, int Hq, int Nq) {
+  const size_t nq_pad = static_cast<size_t>((Nq + bwd::BQ - 1) / bwd::BQ) * bwd::BQ;
+  return 2 * static_cast<size_t>(B) * Hq * nq_pad * sizeof(float);
+}
+
+int launch_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+               const float* lse, float* dq, void* dk, void* dv, void* workspace, int B, int Hq,
+               int Hkv, int Nq, int Nk, float scale, int causal, cudaStream_t stream, int* err) {
+  using namespace bwd;
+  const int nq_pad = (Nq + BQ - 1) / BQ * BQ;
+  const long long rows_pad = static_cast<long long>(B) * Hq * nq_pad;
+  float* lse2 = static_cast<float*>(workspace);
+  float* delta = lse2 + rows_pad;
+  if (cudaMemsetAsync(dq, 0, static_cast<size_t>(B) * Hq * Nq * HD * sizeof(float), stream) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  attn_bwd_prep_kernel<<<static_cast<unsigned>((rows_pad + 7) / 8), 256, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), lse, lse2, delta,
+      rows_pad, Nq, nq_pad);
+  if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+  CUtensorMap tq, tk, tv, tdo;
+  const uint32_t box_q[3] = {64, BQ, 1};
+  const uint32_t box_k[3] = {64, BK, 1};
+  const CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  if (!encode_tiled_3d(&tq, dt, q, HD, Nq, static_cast<uint64_t>(B) * Hq, 2, box_q, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_tiled_3d(&tdo, dt, dout, HD, Nq, static_cast<uint64_t>(B) * Hq, 2, box_q, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_tiled_3d(&tk, dt, k, HD, Nk, static_cast<uint64_t>(B) * Hkv, 2, box_k, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_tiled_3d(&tv, dt, v, HD, Nk, static_cast<uint64_t>(B) * Hkv, 2, box_k, CU_TENSOR_MAP_SWIZZLE_128B))
+    return ATTN_ERR_CUDA;
+  static int attr_dev = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (attr_dev != dev) {
+    if (cudaFuncSetAttribute(attn_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC) !=
+        cudaSuccess)
+      return ATTN_ERR_CUDA;
+    attr_dev = dev;
+  }
+  BwdParams prm;
+  prm.lse2 = lse2;
+  prm.delta = delta;
+  prm.dq = dq;
+  prm.dk = static_cast<__nv_bfloat16*>(dk);
+  prm.dv = static_cast<__nv_bfloat16*>(dv);
+  prm.B = B;
+  prm.Hq = Hq;
+  prm.Hkv = Hkv;
+  prm.Nq = Nq;
+  prm.Nk = Nk;
+  prm.Nq_pad = nq_pad;
+  prm.group = Hq / Hkv;
+  prm.c_log2 = scale * 1.4426950408889634f;
+  prm.scale = scale;
+  prm.causal = causal ? 1 : 0;
+  prm.err = err;
+  const dim3 grid((Nk + BK - 1) / BK, Hkv, B);
+  attn_bwd_kernel<<<grid, NTHREADS, SMEM_ALLOC, stream>>>(tq, tk, tv, tdo, prm);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // namespace attn

@@ -176,6 +176,21 @@ def test_softcap_sink_argument_errors(L):
     assert f(sinks=ctypes.c_void_p(258)) == -5   # not 4-byte aligned
 
 
+def test_backward_argument_errors(L):
+    def f(q=P, k=P, v=P, o=P, do=P, lse=P, dq=P, dk=P, dv=P, ws=P, B=2, Hq=8, Hkv=2, Nq=128, Nk=128, D=128,
+          scale=0.1, causal=0):
+        return L.attn_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, B, Hq, Hkv, Nq, Nk, D, scale, causal, None)
+
+    assert f(do=None) == -1
+    assert f(ws=None) == -1
+    assert f(Nq=0) == -2
+    assert f(Hq=8, Hkv=3) == -3
+    assert f(D=64) == -4
+    assert f(dq=MIS) == -5
+    assert f(scale=-1.0) == -6
+    assert L.attn_bwd_workspace_size(2, 8, 100) == 2 * 2 * 8 * 128 * 4
+
+
 def test_workspace_size(L):
     # O_part [B,Hq,S_max,D] + LSE_part [B,Hq,S_max], fp32, rounded up to 256 bytes
     n = L.attn_decode_workspace_size(64, 32, 128, 32768, 512)

@@ -475,3 +475,55 @@ def test_softcap_sink_full_size_sampled(dev):
     lg = torch.stack([lse[b, h, i] for b, h, i in rows]).cpu()
     check(og, lg, O, L, BF16_O_TOL, BF16_LSE_REL, True)
     assert binding.get_device_error() == 0
+
+
+# ---------------------------------------------------------------- backward
+BWD_CASES = [
+    # B, Hq, Hkv, Nq, Nk, causal
+    (1, 2, 2, 200, 200, False),
+    (2, 4, 2, 257, 257, True),      # GQA, ragged tiles
+    (1, 4, 1, 130, 300, True),      # bottom-right causal, Nq < Nk
+    (1, 2, 2, 300, 130, True),      # Nq > Nk: rows 0..169 see no key
+    (1, 2, 1, 64, 1000, False),     # one query tile, many key tiles
+]
+
+
+def _bwd_check(got, want, name):
+    """Each gradient against 2 % of its tensor's largest magnitude (P, dS and O are
+    rounded to bf16, relative 2^-9, before the fp32 sums)."""
+    g = got.float().cpu().numpy()
+    assert np.isfinite(g).all(), f"{name}: non-finite values"
+    err = float(np.abs(g - want).max())
+    tol = 2e-2 * max(1.0, float(np.abs(want).max()))
+    assert err <= tol, f"{name}: max-abs err {err:.3e} (tol {tol:.3e})"
+    return err
+
+
+@pytest.mark.parametrize("case", BWD_CASES, ids=lambda c: "-".join(map(str, c)))
+def test_backward(dev, case):
+    B, Hq, Hkv, Nq, Nk, causal = case
+    q, k, v = inputs.prefill_inputs(B, Hq, Hkv, Nq, Nk, 128, "bf16", seed=Nq * 7 + Nk)
+    g = torch.Generator("cpu").manual_seed(Nq + 3)
+    do = torch.randn(B, Hq, Nq, 128, generator=g).to(torch.bfloat16)
+    qd, kd, vd, dod = q.to(dev), k.to(dev), v.to(dev), do.to(dev)
+    o, lse = binding.attn_fwd(qd, kd, vd, causal=causal)
+    dq, dk, dv = binding.attn_bwd(qd, kd, vd, o, dod, lse, causal=causal)
+    dQ, dK, dV = oracle.attention_backward(q, k, v, do, 1 / math.sqrt(128), causal, 0)
+    _bwd_check(dq, dQ, "dQ")
+    _bwd_check(dk, dK, "dK")
+    _bwd_check(dv, dV, "dV")
+    assert binding.get_device_error() == 0
+
+
+def test_backward_multi_tile(dev):
+    """B=1 Hq=4 Hkv=2 N=2048 causal: 16 key tiles x 32 query tiles per head."""
+    q, k, v = inputs.prefill_inputs(1, 4, 2, 2048, 2048, 128, "bf16", seed=5)
+    do = torch.randn(1, 4, 2048, 128, generator=torch.Generator("cpu").manual_seed(6)).to(torch.bfloat16)
+    qd, kd, vd, dod = q.to(dev), k.to(dev), v.to(dev), do.to(dev)
+    o, lse = binding.attn_fwd(qd, kd, vd, causal=True)
+    dq, dk, dv = binding.attn_bwd(qd, kd, vd, o, dod, lse, causal=True)
+    dQ, dK, dV = oracle.attention_backward(q, k, v, do, 1 / math.sqrt(128), True, 0)
+    _bwd_check(dq, dQ, "dQ")
+    _bwd_check(dk, dK, "dK")
+    _bwd_check(dv, dV, "dV")
+    assert binding.get_device_error() == 0
