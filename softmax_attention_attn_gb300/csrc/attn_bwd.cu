@@ -12,21 +12,35 @@
 //
 // Design: one CTA per (batch, KV head, 128-key tile j); it keeps K_j and V_j
 // in shared memory and dK_j, dV_j in tensor memory while it walks every query
-// head of the KV head's group and every 64-query tile i that sees the key
+// head of the KV head's group and every 128-query tile i that sees the key
 // tile.  With the keys on the tensor-memory lanes:
-//   * S^T = K_j Q_i^T and dP^T = V_j dO_i^T (M = 128 keys, N = 64 queries);
-//   * four row warps (thread r owns key r) form P^T and dS^T = scale P^T (dP^T - D)
-//     in fp32, write both as bf16 into the S^T / dP^T columns they read, and
-//     dS^T also into shared memory;
+//   * S^T = K_j Q_i^T and dP^T = V_j dO_i^T (M = 128 keys, N = 128 queries);
+//   * four row warps (thread r owns key r) form P^T as soon as S^T is done
+//     (while the dP^T MMAs run) and dS^T = scale P^T (dP^T - D) as soon as
+//     dP^T is done (while the dV MMAs run), in fp32, and write each as bf16
+//     into the columns they read; dS^T also goes to shared memory;
 //   * dV_j += P^T dO_i and dK_j += dS^T Q_i (A from tensor memory, the TS form);
-//   * dQ_i^T = K_j^T dS^T (M = 128 head dims, N = 64 queries; both operands
-//     MN-major in shared memory); the row warps read it (thread r owns head
-//     dim r) and add it to the fp32 dQ with global atomics;
+//   * dQ_i = dS K_j (M = 128 queries, N = 128 head dims; both operands
+//     MN-major in shared memory: dS^T and K_j as they lie) over the dP^T
+//     columns (the dK MMA that reads dS^T from them runs first: MMAs of one
+//     thread execute in order); four more warps read it (thread r owns query
+//     r), free the columns for the next dP^T, stage it as fp32 in the Q/dO
+//     stage the step has finished with (128-byte swizzled 32 x 32 boxes) and
+//     add it to the fp32 dQ with TMA reduce-add copies while the next step
+//     runs.  (Per-thread global atomics here would fill the load/store queue
+//     that the row warps' shared-memory loads share.)  The stage is handed
+//     back to the TMA warp once the copies have read it;
 //   * one TMA warp streams Q_i, dO_i (and the per-query LSE*log2(e) and D
-//     vectors, prepared by attn_bwd_prep_kernel) through a 3-stage ring; one
-//     thread issues every MMA.
-// Tensor memory (512 columns): S^T [0,64) dP^T [64,128) dV [128,256)
-// dK [256,384) dQ^T [384,448).  Every wait is bounded (see ptx.cuh).
+//     vectors, prepared by attn_bwd_prep_kernel) through a 2-stage ring; one
+//     thread issues every MMA.  128-query steps keep every MMA at N = 128 or
+//     K = 128: a 128 x 64 x 16 MMA takes almost as long to issue and run as a
+//     128 x 128 x 16 one.
+// Tensor memory (512 columns): S^T / P^T [0,128), dP^T / dS^T / dQ [128,256),
+// dV [256,384), dK [384,512).  Shared memory: the 1024-byte aligned operand
+// block (K_j, V_j, two Q/dO stages, dS^T) fills all but 3 KB of the 227 KB, so
+// the barriers sit in front of it when the alignment padding has room and
+// behind it otherwise, next to the per-stage vectors.  Every wait is bounded
+// (see ptx.cuh).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math_constants.h>
@@ -39,27 +53,29 @@ namespace bwd {
 
 constexpr int HD = 128;
 constexpr int BK = 128;                          // keys per CTA
-constexpr int BQ = 64;                           // queries per step
-constexpr int NS = 3;                            // Q / dO ring stages
+constexpr int BQ = 128;                          // queries per step
+constexpr int NS = 2;                            // Q / dO ring stages
 constexpr int KSLAB = BK * 128;                  // 64-column slab of a 128-row tile (16 KB)
-constexpr int QSLAB = BQ * 128;                  // 64-column slab of a 64-row tile (8 KB)
+constexpr int QSLAB = BQ * 128;                  // 64-column slab of a 128-row tile (16 KB)
 constexpr int SM_K = 0;
 constexpr int SM_V = SM_K + 2 * KSLAB;
 constexpr int SM_STAGE = SM_V + 2 * KSLAB;
 constexpr int STAGE_BYTES = 4 * QSLAB;           // Q_i (2 slabs) + dO_i (2 slabs)
-constexpr int SM_DS = SM_STAGE + NS * STAGE_BYTES;  // dS^T [128 keys][64 queries] bf16, one slab
-constexpr int VEC_BYTES = 2 * BQ * 4;            // LSE*log2(e)[64], D[64]
-constexpr int SM_VEC = SM_DS + KSLAB;
-constexpr int SM_BAR = SM_VEC + NS * VEC_BYTES;
-constexpr int NUM_BARS = 1 + 2 * NS + 6;
-constexpr int SM_MISC = SM_BAR + NUM_BARS * 8;
-constexpr int SMEM_ALLOC = SM_MISC + 16 + 1024;  // + slack for 1024-byte alignment
-static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
+constexpr int SM_DS = SM_STAGE + NS * STAGE_BYTES;  // dS^T [128 keys][128 queries] bf16, 2 slabs
+constexpr int SM_BIG = SM_DS + 2 * KSLAB;        // end of the operand block
+constexpr int VEC_BYTES = 2 * BQ * 4;            // LSE*log2(e)[128], D[128]
+constexpr int NUM_BARS = 1 + 2 * NS + 8;
+constexpr int SMALL_BYTES = 128;                 // barriers + misc words
+static_assert(NUM_BARS * 8 + 16 <= SMALL_BYTES, "small block");
+constexpr int SMEM_ALLOC = 227 * 1024;
+static_assert(SM_BIG + 1023 + NS * VEC_BYTES <= SMEM_ALLOC, "operand block + vectors, small block in front");
+static_assert(SM_BIG + SMALL_BYTES - 1 + SMALL_BYTES + NS * VEC_BYTES <= SMEM_ALLOC, "everything behind");
 constexpr int WARP_TMA = 4;
 constexpr int WARP_MMA = 5;
-constexpr int NTHREADS = 6 * 32;
+constexpr int WARP_DQ0 = 6;                      // warps 6..9 read dQ out (lane quad = warp % 4)
+constexpr int NTHREADS = 10 * 32;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t COL_S = 0, COL_DP = 64, COL_DV = 128, COL_DK = 256, COL_DQ = 384;
+constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DV = 256, COL_DK = 384, COL_DQ = COL_DP;
 
 // Instruction descriptor, kind::f16 with bf16 A/B and fp32 D; bit 15 / 16 set
 // the A / B operand MN-major.
@@ -69,7 +85,8 @@ constexpr uint32_t idesc(uint32_t M, uint32_t N, uint32_t a_mn, uint32_t b_mn) {
 }
 constexpr uint32_t ID_ST = idesc(BK, BQ, 0, 0);   // S^T, dP^T: K / V and Q / dO, both K-major
 constexpr uint32_t ID_GRAD = idesc(BK, HD, 0, 1); // dV, dK: P^T / dS^T in TMEM, dO / Q MN-major
-constexpr uint32_t ID_DQ = idesc(HD, BQ, 1, 1);   // dQ^T: K^T and dS^T, both MN-major
+constexpr uint32_t ID_DQ = idesc(BQ, HD, 1, 1);   // dQ: dS (from dS^T) and K, both MN-major
+static_assert(BQ == 128 && BK == 128 && HD == 128, "tile shapes");
 
 __device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t off16) {
   uint32_t lo, hi;
@@ -89,6 +106,7 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 
 struct BwdParams {
   const float* lse2;   // [B*Hq][Nq_pad]: LSE * log2(e); +inf on padding and on rows with no key
+                       // (Nq_pad: Nq rounded up to 128)
   const float* delta;  // [B*Hq][Nq_pad]: rowsum(dO * O); 0 on padding
   float* dq;           // [B, Hq, Nq, D] fp32, accumulated (zeroed before the launch)
   __nv_bfloat16* dk;   // [B, Hkv, Nk, D]
@@ -100,7 +118,7 @@ struct BwdParams {
   int* err;
 };
 
-// D = rowsum(dO * O) and LSE * log2(e) per query row, padded to 64 rows per head.
+// D = rowsum(dO * O) and LSE * log2(e) per query row, padded to 128 rows per head.
 __global__ void __launch_bounds__(256)
 attn_bwd_prep_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
                      const float* __restrict__ lse, float* __restrict__ lse2, float* __restrict__ delta,
@@ -137,25 +155,34 @@ attn_bwd_prep_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* _
 __global__ void __launch_bounds__(NTHREADS, 1)
 attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                const BwdParams p) {
+                const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
-  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
+  uint8_t* smem = smem_raw + pad;
   const uint32_t sb = smem_u32(smem);
+  const bool small_front = pad >= static_cast<uint32_t>(SMALL_BYTES);
+  uint8_t* small = small_front ? smem_raw : smem + SM_BIG;
+  const uint32_t sbar = smem_u32(small);
+  uint8_t* vecs = smem + SM_BIG + (small_front ? 0 : SMALL_BYTES);  // per stage: LSE*log2(e), D
+  const uint32_t svec = smem_u32(vecs);
   const int warp = warp_id_uniform();
   const int lane = static_cast<int>(lane_id());
 
-  const uint32_t bar_kv_full = sb + SM_BAR;                                 // K_j, V_j landed
-  auto bar_q_full = [&](int s) { return sb + SM_BAR + 8u * (1 + s); };       // stage s landed
-  auto bar_q_empty = [&](int s) { return sb + SM_BAR + 8u * (1 + NS + s); }; // stage s read by every MMA
-  const uint32_t bar_s_full = sb + SM_BAR + 8u * (1 + 2 * NS);              // S^T, dP^T in TMEM
-  const uint32_t bar_p_ready = bar_s_full + 8;                              // P^T, dS^T written
-  const uint32_t bar_dq_full = bar_s_full + 16;                             // dQ^T in TMEM
-  const uint32_t bar_dq_empty = bar_s_full + 24;                            // dQ^T read out
-  const uint32_t bar_kv_done = bar_s_full + 32;                             // dK, dV complete
-  const uint32_t bar_mma_done = bar_s_full + 40;                            // every MMA complete
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + SM_MISC);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SM_MISC + 4);
+  const uint32_t bar_kv_full = sbar;                                        // K_j, V_j landed
+  auto bar_q_full = [&](int s) { return sbar + 8u * (1 + s); };              // stage s landed
+  auto bar_q_empty = [&](int s) { return sbar + 8u * (1 + NS + s); };        // stage s read by every MMA and
+                                                                            // by the dQ reduce copies
+  const uint32_t bar_s_full = sbar + 8u * (1 + 2 * NS);                     // S^T in TMEM
+  const uint32_t bar_p_ready = bar_s_full + 8;                              // P^T written
+  const uint32_t bar_dp_full = bar_s_full + 16;                             // dP^T in TMEM
+  const uint32_t bar_ds_ready = bar_s_full + 24;                            // dS^T written
+  const uint32_t bar_dq_full = bar_s_full + 32;                             // dQ in TMEM
+  const uint32_t bar_dq_empty = bar_s_full + 40;                            // dQ read out
+  const uint32_t bar_kv_done = bar_s_full + 48;                             // dK, dV complete
+  const uint32_t bar_mma_done = bar_s_full + 56;                            // every MMA complete
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(small + NUM_BARS * 8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(small + NUM_BARS * 8 + 4);
 
   const int j0 = static_cast<int>(blockIdx.x) * BK;
   const int kvh = static_cast<int>(blockIdx.y);
@@ -171,10 +198,12 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     mbar_init(bar_kv_full, 1);
     for (int s = 0; s < NS; ++s) {
       mbar_init(bar_q_full(s), 1);
-      mbar_init(bar_q_empty(s), 1);
+      mbar_init(bar_q_empty(s), 1 + 4);
     }
     mbar_init(bar_s_full, 1);
     mbar_init(bar_p_ready, 4);
+    mbar_init(bar_dp_full, 1);
+    mbar_init(bar_ds_ready, 4);
     mbar_init(bar_dq_full, 1);
     mbar_init(bar_dq_empty, 4);
     mbar_init(bar_kv_done, 1);
@@ -217,7 +246,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
         const int h = step_head(step), i0 = step_q0(step);
         const uint32_t st = sb + SM_STAGE + s * STAGE_BYTES;
-        const uint32_t vec = sb + SM_VEC + s * VEC_BYTES;
+        const uint32_t vec = svec + s * VEC_BYTES;
         mbar_arrive_expect_tx(bar_q_full(s), STAGE_BYTES + VEC_BYTES);
         for (int kb = 0; kb < 2; ++kb) {
           tma_load_3d(st + kb * QSLAB, &tm_q, bar_q_full(s), kb * 64, i0, b * p.Hq + h);
@@ -237,8 +266,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     if (lane == 0 && n_steps > 0) {
       const uint64_t k_kmaj = smem_desc_sw128(sb + SM_K, 16, 1024);   // K as A, K-major
       const uint64_t v_kmaj = smem_desc_sw128(sb + SM_V, 16, 1024);
-      const uint64_t k_mn = smem_desc_sw128(sb + SM_K, KSLAB, 1024);  // K^T as A, MN-major
-      const uint64_t ds_mn = smem_desc_sw128(sb + SM_DS, KSLAB, 1024); // dS^T as B, MN-major
+      const uint64_t k_mn = smem_desc_sw128(sb + SM_K, KSLAB, 1024);  // K as B, MN-major
+      const uint64_t ds_mn = smem_desc_sw128(sb + SM_DS, KSLAB, 1024); // dS (stored as dS^T) as A, MN-major
       bool ok = mbar_wait(bar_kv_full, 0, abort_flag, p.err);
       for (int step = 0; step < n_steps && ok; ++step) {
         const int s = step % NS;
@@ -249,42 +278,47 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const uint64_t do_mn = smem_desc_sw128(st + 2 * QSLAB, QSLAB, 1024);
         if (!mbar_wait(bar_q_full(s), (step / NS) & 1, abort_flag, p.err)) { ok = false; break; }
         tc_fence_after();
-        // S^T = K_j Q_i^T, dP^T = V_j dO_i^T
+        // S^T = K_j Q_i^T (over P^T of the previous step: the dV MMA that read it came first)
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
           const uint32_t a_off = static_cast<uint32_t>((kk >> 2) * KSLAB + (kk & 3) * 32) >> 4;
           const uint32_t b_off = static_cast<uint32_t>((kk >> 2) * QSLAB + (kk & 3) * 32) >> 4;
           mma_bf16_ss(tmem + COL_S, desc_add(k_kmaj, a_off), desc_add(q_kmaj, b_off), ID_ST, kk > 0 ? 1u : 0u);
         }
+        mma_commit(bar_s_full);
+        // dP^T = V_j dO_i^T over the previous step's dQ: it must have been read out
+        if (step > 0 && !mbar_wait(bar_dq_empty, (step - 1) & 1, abort_flag, p.err)) { ok = false; break; }
+        tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
           const uint32_t a_off = static_cast<uint32_t>((kk >> 2) * KSLAB + (kk & 3) * 32) >> 4;
           const uint32_t b_off = static_cast<uint32_t>((kk >> 2) * QSLAB + (kk & 3) * 32) >> 4;
           mma_bf16_ss(tmem + COL_DP, desc_add(v_kmaj, a_off), desc_add(do_kmaj, b_off), ID_ST, kk > 0 ? 1u : 0u);
         }
-        mma_commit(bar_s_full);
+        mma_commit(bar_dp_full);
+        // dV_j += P^T dO_i (16 queries per K step)
         if (!mbar_wait(bar_p_ready, step & 1, abort_flag, p.err)) { ok = false; break; }
         tc_fence_after();
-        // dV_j += P^T dO_i, dK_j += dS^T Q_i  (16 queries per K step)
 #pragma unroll
         for (int kk = 0; kk < BQ / 16; ++kk) {
           const uint32_t boff = static_cast<uint32_t>(kk * 16 * 128) >> 4;
           mma_bf16_ts(tmem + COL_DV, tmem + COL_S + kk * 8, desc_add(do_mn, boff), ID_GRAD,
                       (step > 0 || kk > 0) ? 1u : 0u);
         }
+        // dK_j += dS^T Q_i
+        if (!mbar_wait(bar_ds_ready, step & 1, abort_flag, p.err)) { ok = false; break; }
+        tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < BQ / 16; ++kk) {
           const uint32_t boff = static_cast<uint32_t>(kk * 16 * 128) >> 4;
           mma_bf16_ts(tmem + COL_DK, tmem + COL_DP + kk * 8, desc_add(q_mn, boff), ID_GRAD,
                       (step > 0 || kk > 0) ? 1u : 0u);
         }
-        // dQ_i^T = K_j^T dS^T (16 keys per K step); the previous dQ^T must be read out
-        if (step > 0 && !mbar_wait(bar_dq_empty, (step - 1) & 1, abort_flag, p.err)) { ok = false; break; }
-        tc_fence_after();
+        // dQ_i = dS K_j (16 keys per K step), over dP^T / dS^T (read by the dK MMAs above)
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk) {
           const uint32_t off16 = static_cast<uint32_t>(kk * 16 * 128) >> 4;
-          mma_bf16_ss(tmem + COL_DQ, desc_add(k_mn, off16), desc_add(ds_mn, off16), ID_DQ, kk > 0 ? 1u : 0u);
+          mma_bf16_ss(tmem + COL_DQ, desc_add(ds_mn, off16), desc_add(k_mn, off16), ID_DQ, kk > 0 ? 1u : 0u);
         }
         mma_commit(bar_dq_full);
         mma_commit(bar_q_empty(s));
@@ -293,112 +327,164 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       mma_commit(bar_mma_done);
       drain_wait(bar_mma_done, 0);
     }
-  } else if (warp < 4) {
-    // ================================================================ row warps
-    const int quad = warp;
+  } else {
+    // ================================================================ row warps (0..3), dQ warps (6..9)
+    const bool dq_warp = warp >= WARP_DQ0;
+    const int quad = warp & 3;
     const uint32_t lane_sel = static_cast<uint32_t>(quad * 32) << 16;
-    const int r = quad * 32 + lane;  // key row (S^T, dP^T, dV, dK) / head dim (dQ^T) of this thread
+    const int r = quad * 32 + lane;  // key row (S^T, dP^T, dV, dK) / query row (dQ) of this thread
     const int key = j0 + r;
     const bool key_ok = key < p.Nk;
     bool ok = true;
     for (int step = 0; step < n_steps && ok; ++step) {
       const int s = step % NS;
       const int h = step_head(step), i0 = step_q0(step);
+      if (dq_warp) {
+        // dQ_i: this thread holds query r of the step, all 128 head dims
+        ok = __all_sync(0xffffffffu, mbar_wait(bar_dq_full, step & 1, abort_flag, p.err));
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t qr[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_sel + COL_DQ + 32 * c, qr[c]);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_dq_empty);  // the columns are free for the next dP^T
+        // Stage rows [32 quad, +32) in the finished Q/dO stage (its MMAs are
+        // complete: dq_full follows them) as four 32-query x 32-dim boxes,
+        // 128-byte rows with the 128-byte swizzle (16-byte chunk c of row l at
+        // chunk c ^ (l % 8)).
+        uint8_t* box0 = smem + SM_STAGE + s * STAGE_BYTES + quad * (4 * 32 * 128);
+#pragma unroll
+        for (int bx = 0; bx < 4; ++bx)
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4*>(box0 + bx * (32 * 128) + lane * 128 + ((c ^ (lane & 7)) * 16)) =
+                make_uint4(qr[bx][4 * c], qr[bx][4 * c + 1], qr[bx][4 * c + 2], qr[bx][4 * c + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          // rows past the sequence end fall outside the map and are skipped
+          if (i0 + quad * 32 < p.Nq) {
+#pragma unroll
+            for (int bx = 0; bx < 4; ++bx)
+              tma_reduce_add_3d(&tm_dq, smem_u32(box0 + bx * (32 * 128)), bx * 32, i0 + quad * 32, b * p.Hq + h);
+          }
+          bulk_commit_group();
+          bulk_wait_group_read0();
+          mbar_arrive(bar_q_empty(s));  // the stage may be refilled
+        }
+        __syncwarp();
+        continue;
+      }
       ok = __all_sync(0xffffffffu, mbar_wait(bar_q_full(s), (step / NS) & 1, abort_flag, p.err) &&
                                        mbar_wait(bar_s_full, step & 1, abort_flag, p.err));
       if (!ok) break;
       tc_fence_after();
-      uint32_t sr[2][32], dr[2][32];
-      tmem_ld32(tmem + lane_sel + COL_S, sr[0]);
-      tmem_ld32(tmem + lane_sel + COL_S + 32, sr[1]);
-      tmem_ld32(tmem + lane_sel + COL_DP, dr[0]);
-      tmem_ld32(tmem + lane_sel + COL_DP + 32, dr[1]);
-      tmem_wait_ld();
-      const float* lse2v = reinterpret_cast<const float*>(smem + SM_VEC + s * VEC_BYTES);
+      const float* lse2v = reinterpret_cast<const float*>(vecs + s * VEC_BYTES);
       const float* deltav = lse2v + BQ;
       // causal: query c of this step sees this key iff key <= i0 + c + off
       const int c_min = p.causal ? key - off - i0 : 0;  // first visible query index (may be < 0)
-      uint32_t pk[32], dk[32];
+      // P^T, 64 queries at a time, packed as bf16 pairs into S^T columns
+      // [32 hq, +32) (already read)
 #pragma unroll
-      for (int c = 0; c < BQ; c += 2) {
-        float pv[2], dsv[2];
+      for (int hq = 0; hq < 2; ++hq) {
+        uint32_t sr[2][32];
+        tmem_ld32(tmem + lane_sel + COL_S + 64 * hq, sr[0]);
+        tmem_ld32(tmem + lane_sel + COL_S + 64 * hq + 32, sr[1]);
+        tmem_wait_ld();
+        uint32_t pk[32];
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int cc = c + e;
-          const float sv = __uint_as_float(sr[cc >> 5][cc & 31]);
-          const float dpv = __uint_as_float(dr[cc >> 5][cc & 31]);
-          const bool vis = key_ok && cc >= c_min;
-          const float pr = vis ? ex2_approx(fmaf(sv, p.c_log2, -lse2v[cc])) : 0.f;
-          pv[e] = pr;
-          dsv[e] = pr * (dpv - deltav[cc]) * p.scale;
+        for (int c = 0; c < 64; c += 4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(lse2v + 64 * hq + c);  // one broadcast load
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+          float pv[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int cc = 64 * hq + c + e;
+            const bool vis = key_ok && cc >= c_min;
+            pv[e] = vis ? ex2_approx(fmaf(__uint_as_float(sr[(c + e) >> 5][(c + e) & 31]), p.c_log2, -lv[e])) : 0.f;
+          }
+          pk[c >> 1] = pack_bf16x2(pv[0], pv[1]);
+          pk[(c >> 1) + 1] = pack_bf16x2(pv[2], pv[3]);
         }
-        pk[c >> 1] = pack_bf16x2(pv[0], pv[1]);
-        dk[c >> 1] = pack_bf16x2(dsv[0], dsv[1]);
+        tmem_st32(tmem + lane_sel + COL_S + 32 * hq, pk);
       }
-      // P^T over S^T columns [0, 32), dS^T over dP^T columns [64, 96)
-      tmem_st16(tmem + lane_sel + COL_S, *reinterpret_cast<const uint32_t(*)[16]>(pk));
-      tmem_st16(tmem + lane_sel + COL_S + 16, *reinterpret_cast<const uint32_t(*)[16]>(pk + 16));
-      tmem_st16(tmem + lane_sel + COL_DP, *reinterpret_cast<const uint32_t(*)[16]>(dk));
-      tmem_st16(tmem + lane_sel + COL_DP + 16, *reinterpret_cast<const uint32_t(*)[16]>(dk + 16));
-      // dS^T row r into shared memory (128-byte rows, 128-byte swizzle: 16-byte
-      // chunk c of row r sits at chunk c ^ (r % 8)); the previous step's dQ MMA
-      // has read the tile (its completion was waited on before that read-out)
-      uint8_t* ds_row = smem + SM_DS + r * 128;
-#pragma unroll
-      for (int c = 0; c < 8; ++c)
-        *reinterpret_cast<uint4*>(ds_row + ((c ^ (r & 7)) * 16)) =
-            make_uint4(dk[4 * c], dk[4 * c + 1], dk[4 * c + 2], dk[4 * c + 3]);
-      fence_proxy_async_smem();
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_p_ready);
-      // dQ_i^T read-out: this thread holds head dim r of the 64 queries
-      ok = __all_sync(0xffffffffu, mbar_wait(bar_dq_full, step & 1, abort_flag, p.err));
+      // dS^T = scale P^T (dP^T - D), 64 queries at a time, from the packed P^T;
+      // bf16 pairs into dP^T columns [32 hq, +32) (already read) and into row r
+      // of the shared-memory tile (two 64-query slabs, 128-byte rows, 128-byte
+      // swizzle: 16-byte chunk c of a row sits at chunk c ^ (r % 8)).  The
+      // previous step's dQ MMA has read that tile: it completed before dP^T.
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_dp_full, step & 1, abort_flag, p.err));
       if (!ok) break;
       tc_fence_after();
-      uint32_t qr[2][32];
-      tmem_ld32(tmem + lane_sel + COL_DQ, qr[0]);
-      tmem_ld32(tmem + lane_sel + COL_DQ + 32, qr[1]);
-      tmem_wait_ld();
+#pragma unroll
+      for (int hq = 0; hq < 2; ++hq) {
+        uint32_t dr[2][32], pp[32];
+        tmem_ld32(tmem + lane_sel + COL_DP + 64 * hq, dr[0]);
+        tmem_ld32(tmem + lane_sel + COL_DP + 64 * hq + 32, dr[1]);
+        tmem_ld32(tmem + lane_sel + COL_S + 32 * hq, pp);
+        tmem_wait_ld();
+        uint32_t dk[32];
+#pragma unroll
+        for (int c = 0; c < 64; c += 4) {
+          const float4 d4 = *reinterpret_cast<const float4*>(deltav + 64 * hq + c);  // one broadcast load
+          const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+          for (int e = 0; e < 4; e += 2) {
+            const int cl = c + e;
+            const float p0 = __uint_as_float(pp[cl >> 1] << 16);
+            const float p1 = __uint_as_float(pp[cl >> 1] & 0xFFFF0000u);
+            const float d0 = p0 * (__uint_as_float(dr[cl >> 5][cl & 31]) - dv[e]) * p.scale;
+            const float d1 = p1 * (__uint_as_float(dr[(cl + 1) >> 5][(cl + 1) & 31]) - dv[e + 1]) * p.scale;
+            dk[cl >> 1] = pack_bf16x2(d0, d1);
+          }
+        }
+        tmem_st32(tmem + lane_sel + COL_DP + 32 * hq, dk);
+        uint8_t* ds_row = smem + SM_DS + hq * KSLAB + r * 128;
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8)
+          *reinterpret_cast<uint4*>(ds_row + ((c8 ^ (r & 7)) * 16)) =
+              make_uint4(dk[4 * c8], dk[4 * c8 + 1], dk[4 * c8 + 2], dk[4 * c8 + 3]);
+      }
+      fence_proxy_async_smem();
+      tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_dq_empty);
-      float* dq = p.dq + (static_cast<size_t>(b) * p.Hq + h) * p.Nq * HD + static_cast<size_t>(i0) * HD + r;
-      const int nq = min(BQ, p.Nq - i0);
-#pragma unroll
-      for (int c = 0; c < BQ; ++c)
-        if (c < nq) atomicAdd(dq + static_cast<size_t>(c) * HD, __uint_as_float(qr[c >> 5][c & 31]));
+      if (lane == 0) mbar_arrive(bar_ds_ready);
     }
-    // dK_j, dV_j: this thread's key row
+    if (dq_warp && lane == 0) bulk_wait_group0();  // the dQ adds are complete before the CTA exits
+    // dV_j (row warps) or dK_j (dQ warps): this thread's key row
     if (ok) {
       if (n_steps > 0) ok = __all_sync(0xffffffffu, mbar_wait(bar_kv_done, 0, abort_flag, p.err));
       if (ok) {
         tc_fence_after();
         const size_t orow = (static_cast<size_t>(b) * p.Hkv + kvh) * p.Nk + key;
+        uint32_t g[HD];
+        if (n_steps > 0) {
 #pragma unroll
-        for (int which = 0; which < 2; ++which) {
-          uint32_t g[HD];
-          if (n_steps > 0) {
-#pragma unroll
-            for (int ch = 0; ch < HD / 32; ++ch) {
-              uint32_t (&gc)[32] = *reinterpret_cast<uint32_t(*)[32]>(g + 32 * ch);
-              tmem_ld32(tmem + lane_sel + (which ? COL_DK : COL_DV) + ch * 32, gc);
-            }
-            tmem_wait_ld();
-          } else {
-#pragma unroll
-            for (int i = 0; i < HD; ++i) g[i] = 0u;
+          for (int ch = 0; ch < HD / 32; ++ch) {
+            uint32_t (&gc)[32] = *reinterpret_cast<uint32_t(*)[32]>(g + 32 * ch);
+            tmem_ld32(tmem + lane_sel + (dq_warp ? COL_DK : COL_DV) + ch * 32, gc);
           }
-          if (key_ok) {
-            uint4* dst = reinterpret_cast<uint4*>((which ? p.dk : p.dv) + orow * HD);
+          tmem_wait_ld();
+        } else {
 #pragma unroll
-            for (int i = 0; i < HD / 8; ++i)
-              dst[i] = make_uint4(pack_bf16x2(__uint_as_float(g[8 * i + 0]), __uint_as_float(g[8 * i + 1])),
-                                  pack_bf16x2(__uint_as_float(g[8 * i + 2]), __uint_as_float(g[8 * i + 3])),
-                                  pack_bf16x2(__uint_as_float(g[8 * i + 4]), __uint_as_float(g[8 * i + 5])),
-                                  pack_bf16x2(__uint_as_float(g[8 * i + 6]), __uint_as_float(g[8 * i + 7])));
-          }
+          for (int i = 0; i < HD; ++i) g[i] = 0u;
+        }
+        if (key_ok) {
+          uint4* dst = reinterpret_cast<uint4*>((dq_warp ? p.dk : p.dv) + orow * HD);
+#pragma unroll
+          for (int i = 0; i < HD / 8; ++i)
+            dst[i] = make_uint4(pack_bf16x2(__uint_as_float(g[8 * i + 0]), __uint_as_float(g[8 * i + 1])),
+                                pack_bf16x2(__uint_as_float(g[8 * i + 2]), __uint_as_float(g[8 * i + 3])),
+                                pack_bf16x2(__uint_as_float(g[8 * i + 4]), __uint_as_float(g[8 * i + 5])),
+                                pack_bf16x2(__uint_as_float(g[8 * i + 6]), __uint_as_float(g[8 * i + 7])));
         }
       }
     }
@@ -433,14 +519,17 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
       static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), lse, lse2, delta,
       rows_pad, Nq, nq_pad);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
-  CUtensorMap tq, tk, tv, tdo;
+  CUtensorMap tq, tk, tv, tdo, tdq;
   const uint32_t box_q[3] = {64, BQ, 1};
   const uint32_t box_k[3] = {64, BK, 1};
+  const uint32_t box_dq[3] = {32, 32, 1};
   const CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   if (!encode_tiled_3d(&tq, dt, q, HD, Nq, static_cast<uint64_t>(B) * Hq, 2, box_q, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_tiled_3d(&tdo, dt, dout, HD, Nq, static_cast<uint64_t>(B) * Hq, 2, box_q, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_tiled_3d(&tk, dt, k, HD, Nk, static_cast<uint64_t>(B) * Hkv, 2, box_k, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_tiled_3d(&tv, dt, v, HD, Nk, static_cast<uint64_t>(B) * Hkv, 2, box_k, CU_TENSOR_MAP_SWIZZLE_128B))
+      !encode_tiled_3d(&tv, dt, v, HD, Nk, static_cast<uint64_t>(B) * Hkv, 2, box_k, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_tiled_3d(&tdq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dq, HD, Nq, static_cast<uint64_t>(B) * Hq, 4, box_dq,
+                       CU_TENSOR_MAP_SWIZZLE_128B))
     return ATTN_ERR_CUDA;
   static int attr_dev = -1;
   int dev = 0;
@@ -469,7 +558,7 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
   prm.causal = causal ? 1 : 0;
   prm.err = err;
   const dim3 grid((Nk + BK - 1) / BK, Hkv, B);
-  attn_bwd_kernel<<<grid, NTHREADS, SMEM_ALLOC, stream>>>(tq, tk, tv, tdo, prm);
+  attn_bwd_kernel<<<grid, NTHREADS, SMEM_ALLOC, stream>>>(tq, tk, tv, tdo, tdq, prm);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

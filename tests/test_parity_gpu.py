@@ -485,6 +485,7 @@ BWD_CASES = [
     (1, 4, 1, 130, 300, True),      # bottom-right causal, Nq < Nk
     (1, 2, 2, 300, 130, True),      # Nq > Nk: rows 0..169 see no key
     (1, 2, 1, 64, 1000, False),     # one query tile, many key tiles
+    (1, 4, 2, 384, 384, True),      # whole tiles only, two query heads per KV head
 ]
 
 
