@@ -105,9 +105,9 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 }
 
 struct BwdParams {
-  const float* lse2;   // [B*Hq][Nq_pad]: LSE * log2(e); +inf on padding and on rows with no key
+  const float* nlse2;  // [B*Hq][Nq_pad]: -LSE * log2(e); -inf on padding and on rows with no key
                        // (Nq_pad: Nq rounded up to 128)
-  const float* delta;  // [B*Hq][Nq_pad]: rowsum(dO * O); 0 on padding
+  const float* ndelta; // [B*Hq][Nq_pad]: -scale * rowsum(dO * O); 0 on padding
   float* dq;           // [B, Hq, Nq, D] fp32, accumulated (zeroed before the launch)
   __nv_bfloat16* dk;   // [B, Hkv, Nk, D]
   __nv_bfloat16* dv;
@@ -118,11 +118,13 @@ struct BwdParams {
   int* err;
 };
 
-// D = rowsum(dO * O) and LSE * log2(e) per query row, padded to 128 rows per head.
+// -scale * D (D = rowsum(dO * O)) and -LSE * log2(e) per query row, padded to
+// 128 rows per head, negated so that the main kernel needs one fused
+// multiply-add per score.
 __global__ void __launch_bounds__(256)
 attn_bwd_prep_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
-                     const float* __restrict__ lse, float* __restrict__ lse2, float* __restrict__ delta,
-                     long long rows_pad, int Nq, int Nq_pad) {
+                     const float* __restrict__ lse, float* __restrict__ nlse2, float* __restrict__ ndelta,
+                     long long rows_pad, int Nq, int Nq_pad, float scale) {
   const long long r = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   const int lane = static_cast<int>(threadIdx.x & 31);
   if (r >= rows_pad) return;
@@ -130,8 +132,8 @@ attn_bwd_prep_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* _
   const int i = static_cast<int>(r - bh * Nq_pad);
   if (i >= Nq) {
     if (lane == 0) {
-      delta[r] = 0.f;
-      lse2[r] = CUDART_INF_F;
+      ndelta[r] = 0.f;
+      nlse2[r] = -CUDART_INF_F;
     }
     return;
   }
@@ -146,9 +148,9 @@ attn_bwd_prep_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* _
 #pragma unroll
   for (int k = 16; k >= 1; k >>= 1) s += __shfl_xor_sync(0xffffffffu, s, k);
   if (lane == 0) {
-    delta[r] = s;
+    ndelta[r] = -scale * s;
     const float l = lse[bh * Nq + i];
-    lse2[r] = l == -CUDART_INF_F ? CUDART_INF_F : l * 1.4426950408889634f;
+    nlse2[r] = l == -CUDART_INF_F ? -CUDART_INF_F : -l * 1.4426950408889634f;
   }
 }
 
@@ -164,7 +166,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   const bool small_front = pad >= static_cast<uint32_t>(SMALL_BYTES);
   uint8_t* small = small_front ? smem_raw : smem + SM_BIG;
   const uint32_t sbar = smem_u32(small);
-  uint8_t* vecs = smem + SM_BIG + (small_front ? 0 : SMALL_BYTES);  // per stage: LSE*log2(e), D
+  uint8_t* vecs = smem + SM_BIG + (small_front ? 0 : SMALL_BYTES);  // per stage: -LSE*log2(e), -scale*D
   const uint32_t svec = smem_u32(vecs);
   const int warp = warp_id_uniform();
   const int lane = static_cast<int>(lane_id());
@@ -253,8 +255,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           tma_load_3d(st + 2 * QSLAB + kb * QSLAB, &tm_do, bar_q_full(s), kb * 64, i0, b * p.Hq + h);
         }
         const size_t vrow = (static_cast<size_t>(b) * p.Hq + h) * p.Nq_pad + i0;
-        bulk_load(vec, p.lse2 + vrow, BQ * 4, bar_q_full(s));
-        bulk_load(vec + BQ * 4, p.delta + vrow, BQ * 4, bar_q_full(s));
+        bulk_load(vec, p.nlse2 + vrow, BQ * 4, bar_q_full(s));
+        bulk_load(vec + BQ * 4, p.ndelta + vrow, BQ * 4, bar_q_full(s));
       }
       if (!ok) {  // let the copies already issued land before the CTA exits
         drain_wait(bar_kv_full, 0);
@@ -382,12 +384,13 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                                        mbar_wait(bar_s_full, step & 1, abort_flag, p.err));
       if (!ok) break;
       tc_fence_after();
-      const float* lse2v = reinterpret_cast<const float*>(vecs + s * VEC_BYTES);
-      const float* deltav = lse2v + BQ;
+      const float* nlse2v = reinterpret_cast<const float*>(vecs + s * VEC_BYTES);
+      const float* ndeltav = nlse2v + BQ;
       // causal: query c of this step sees this key iff key <= i0 + c + off
       const int c_min = p.causal ? key - off - i0 : 0;  // first visible query index (may be < 0)
-      // P^T, 64 queries at a time, packed as bf16 pairs into S^T columns
-      // [32 hq, +32) (already read)
+      const uint64_t c_log2_2 = f2_pack(p.c_log2, p.c_log2);
+      // P^T = 2^(S^T scale log2(e) - LSE log2(e)), 64 queries at a time, packed
+      // as bf16 pairs into S^T columns [32 hq, +32) (already read)
 #pragma unroll
       for (int hq = 0; hq < 2; ++hq) {
         uint32_t sr[2][32];
@@ -397,17 +400,25 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         uint32_t pk[32];
 #pragma unroll
         for (int c = 0; c < 64; c += 4) {
-          const float4 l4 = *reinterpret_cast<const float4*>(lse2v + 64 * hq + c);  // one broadcast load
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-          float pv[4];
+          const float4 l4 = *reinterpret_cast<const float4*>(nlse2v + 64 * hq + c);  // one broadcast load
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int cc = 64 * hq + c + e;
-            const bool vis = key_ok && cc >= c_min;
-            pv[e] = vis ? ex2_approx(fmaf(__uint_as_float(sr[(c + e) >> 5][(c + e) & 31]), p.c_log2, -lv[e])) : 0.f;
+          for (int e = 0; e < 4; e += 2) {
+            const int cl = c + e;
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[cl >> 5][cl & 31]), __uint_as_float(sr[cl >> 5][(cl & 31) + 1])),
+                             c_log2_2, e == 0 ? f2_pack(l4.x, l4.y) : f2_pack(l4.z, l4.w)),
+                      x0, x1);
+            pk[cl >> 1] = pack_bf16x2(ex2_approx(x0), ex2_approx(x1));
           }
-          pk[c >> 1] = pack_bf16x2(pv[0], pv[1]);
-          pk[(c >> 1) + 1] = pack_bf16x2(pv[2], pv[3]);
+        }
+        // masked entries (padding keys, causal) to 0: only warps that have some
+        if (!__all_sync(0xffffffffu, key_ok && c_min <= 64 * hq)) {
+#pragma unroll
+          for (int c = 0; c < 64; c += 2) {
+            const int cc = 64 * hq + c;
+            const bool v0 = key_ok && cc >= c_min, v1 = key_ok && cc + 1 >= c_min;
+            pk[c >> 1] &= (v0 ? 0x0000FFFFu : 0u) | (v1 ? 0xFFFF0000u : 0u);
+          }
         }
         tmem_st32(tmem + lane_sel + COL_S + 32 * hq, pk);
       }
@@ -415,14 +426,15 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_p_ready);
-      // dS^T = scale P^T (dP^T - D), 64 queries at a time, from the packed P^T;
-      // bf16 pairs into dP^T columns [32 hq, +32) (already read) and into row r
-      // of the shared-memory tile (two 64-query slabs, 128-byte rows, 128-byte
-      // swizzle: 16-byte chunk c of a row sits at chunk c ^ (r % 8)).  The
-      // previous step's dQ MMA has read that tile: it completed before dP^T.
+      // dS^T = P^T (scale dP^T - scale D), 64 queries at a time, from the packed
+      // P^T; bf16 pairs into dP^T columns [32 hq, +32) (already read) and into
+      // row r of the shared-memory tile (two 64-query slabs, 128-byte rows,
+      // 128-byte swizzle: 16-byte chunk c of a row sits at chunk c ^ (r % 8)).
+      // The previous step's dQ MMA has read that tile: it completed before dP^T.
       ok = __all_sync(0xffffffffu, mbar_wait(bar_dp_full, step & 1, abort_flag, p.err));
       if (!ok) break;
       tc_fence_after();
+      const uint64_t scale2 = f2_pack(p.scale, p.scale);
 #pragma unroll
       for (int hq = 0; hq < 2; ++hq) {
         uint32_t dr[2][32], pp[32];
@@ -433,15 +445,14 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         uint32_t dk[32];
 #pragma unroll
         for (int c = 0; c < 64; c += 4) {
-          const float4 d4 = *reinterpret_cast<const float4*>(deltav + 64 * hq + c);  // one broadcast load
-          const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+          const float4 d4 = *reinterpret_cast<const float4*>(ndeltav + 64 * hq + c);  // one broadcast load
 #pragma unroll
           for (int e = 0; e < 4; e += 2) {
             const int cl = c + e;
-            const float p0 = __uint_as_float(pp[cl >> 1] << 16);
-            const float p1 = __uint_as_float(pp[cl >> 1] & 0xFFFF0000u);
-            const float d0 = p0 * (__uint_as_float(dr[cl >> 5][cl & 31]) - dv[e]) * p.scale;
-            const float d1 = p1 * (__uint_as_float(dr[(cl + 1) >> 5][(cl + 1) & 31]) - dv[e + 1]) * p.scale;
+            const uint64_t p2 = f2_pack(__uint_as_float(pp[cl >> 1] << 16), __uint_as_float(pp[cl >> 1] & 0xFFFF0000u));
+            const uint64_t dp2 = f2_pack(__uint_as_float(dr[cl >> 5][cl & 31]), __uint_as_float(dr[cl >> 5][(cl & 31) + 1]));
+            float d0, d1;
+            f2_unpack(f2_mul(p2, f2_fma(dp2, scale2, e == 0 ? f2_pack(d4.x, d4.y) : f2_pack(d4.z, d4.w))), d0, d1);
             dk[cl >> 1] = pack_bf16x2(d0, d1);
           }
         }
@@ -511,13 +522,13 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
   using namespace bwd;
   const int nq_pad = (Nq + BQ - 1) / BQ * BQ;
   const long long rows_pad = static_cast<long long>(B) * Hq * nq_pad;
-  float* lse2 = static_cast<float*>(workspace);
-  float* delta = lse2 + rows_pad;
+  float* nlse2 = static_cast<float*>(workspace);
+  float* ndelta = nlse2 + rows_pad;
   if (cudaMemsetAsync(dq, 0, static_cast<size_t>(B) * Hq * Nq * HD * sizeof(float), stream) != cudaSuccess)
     return ATTN_ERR_CUDA;
   attn_bwd_prep_kernel<<<static_cast<unsigned>((rows_pad + 7) / 8), 256, 0, stream>>>(
-      static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), lse, lse2, delta,
-      rows_pad, Nq, nq_pad);
+      static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), lse, nlse2, ndelta,
+      rows_pad, Nq, nq_pad, scale);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
   CUtensorMap tq, tk, tv, tdo, tdq;
   const uint32_t box_q[3] = {64, BQ, 1};
@@ -541,8 +552,8 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
     attr_dev = dev;
   }
   BwdParams prm;
-  prm.lse2 = lse2;
-  prm.delta = delta;
+  prm.nlse2 = nlse2;
+  prm.ndelta = ndelta;
   prm.dq = dq;
   prm.dk = static_cast<__nv_bfloat16*>(dk);
   prm.dv = static_cast<__nv_bfloat16*>(dv);
