@@ -223,8 +223,16 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
 
+  // Each CTA walks its query tiles from a different start (rotated by its key
+  // tile): the CTAs of one head then add into different dQ rows at any moment
+  // instead of all into the same ones, which the L2 would serialise.
+  const int rot = per_head > 0 ? static_cast<int>(blockIdx.x) % per_head : 0;
   auto step_head = [&](int step) { return kvh * p.group + step / max(per_head, 1); };
-  auto step_q0 = [&](int step) { return (it0 + step % max(per_head, 1)) * BQ; };
+  auto step_q0 = [&](int step) {
+    int t = step % max(per_head, 1) + rot;
+    if (t >= per_head) t -= per_head;
+    return (it0 + t) * BQ;
+  };
 
   if (warp == WARP_TMA) {
     // ================================================================ producer
