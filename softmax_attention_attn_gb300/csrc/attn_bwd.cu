@@ -15,11 +15,14 @@
 // head of the KV head's group and every 128-query tile i that sees the key
 // tile.  With the keys on the tensor-memory lanes:
 //   * S^T = K_j Q_i^T and dP^T = V_j dO_i^T (M = 128 keys, N = 128 queries);
-//   * four row warps (thread r owns key r) form P^T as soon as S^T is done
-//     (while the dP^T MMAs run) and dS^T = scale P^T (dP^T - D) as soon as
-//     dP^T is done (while the dV MMAs run), in fp32, and write each as bf16
-//     into the columns they read; dS^T also goes to shared memory;
-//   * dV_j += P^T dO_i and dK_j += dS^T Q_i (A from tensor memory, the TS form);
+//   * eight row warps, two per lane quarter (thread r owns key r; the two
+//     warps of a quarter take queries [0,64) and [64,128)), form P^T as soon
+//     as S^T is done (while the dP^T MMAs run) and dS^T = scale P^T (dP^T - D)
+//     as soon as dP^T is done (while the dV MMAs run), in fp32; P^T goes as
+//     bf16 pairs into the first half of the S^T columns each warp read, dS^T
+//     as bf16 into shared memory;
+//   * dV_j += P^T dO_i (A from tensor memory, the TS form) and dK_j += dS^T Q_i
+//     (A from shared memory);
 //   * dQ_i = dS K_j (M = 128 queries, N = 128 head dims; both operands
 //     MN-major in shared memory: dS^T and K_j as they lie) over the dP^T
 //     columns (the dK MMA that reads dS^T from them runs first: MMAs of one
@@ -70,10 +73,11 @@ static_assert(NUM_BARS * 8 + 16 <= SMALL_BYTES, "small block");
 constexpr int SMEM_ALLOC = 227 * 1024;
 static_assert(SM_BIG + 1023 + NS * VEC_BYTES <= SMEM_ALLOC, "operand block + vectors, small block in front");
 static_assert(SM_BIG + SMALL_BYTES - 1 + SMALL_BYTES + NS * VEC_BYTES <= SMEM_ALLOC, "everything behind");
-constexpr int WARP_TMA = 4;
-constexpr int WARP_MMA = 5;
-constexpr int WARP_DQ0 = 6;                      // warps 6..9 read dQ out (lane quad = warp % 4)
-constexpr int NTHREADS = 10 * 32;
+constexpr int NROW = 8;                          // row warps 0..7: lane quad = warp % 4, query half = warp / 4
+constexpr int WARP_TMA = 8;
+constexpr int WARP_MMA = 9;
+constexpr int WARP_DQ0 = 10;                     // warps 10..13 read dQ out (lane quad = warp % 4)
+constexpr int NTHREADS = 14 * 32;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DV = 256, COL_DK = 384, COL_DQ = COL_DP;
 
@@ -203,9 +207,9 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       mbar_init(bar_q_empty(s), 1 + 4);
     }
     mbar_init(bar_s_full, 1);
-    mbar_init(bar_p_ready, 4);
+    mbar_init(bar_p_ready, NROW);
     mbar_init(bar_dp_full, 1);
-    mbar_init(bar_ds_ready, 4);
+    mbar_init(bar_ds_ready, NROW);
     mbar_init(bar_dq_full, 1);
     mbar_init(bar_dq_empty, 4);
     mbar_init(bar_kv_done, 1);
@@ -278,6 +282,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       const uint64_t v_kmaj = smem_desc_sw128(sb + SM_V, 16, 1024);
       const uint64_t k_mn = smem_desc_sw128(sb + SM_K, KSLAB, 1024);  // K as B, MN-major
       const uint64_t ds_mn = smem_desc_sw128(sb + SM_DS, KSLAB, 1024); // dS (stored as dS^T) as A, MN-major
+      const uint64_t ds_kmaj = smem_desc_sw128(sb + SM_DS, 16, 1024);  // dS^T as A, K-major
       bool ok = mbar_wait(bar_kv_full, 0, abort_flag, p.err);
       for (int step = 0; step < n_steps && ok; ++step) {
         const int s = step % NS;
@@ -311,20 +316,22 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < BQ / 16; ++kk) {
+          // P^T of queries [64 hf, +64) sits in columns [64 hf, +32) (bf16 pairs)
+          const uint32_t a_col = COL_S + (kk >> 2) * 64 + (kk & 3) * 8;
           const uint32_t boff = static_cast<uint32_t>(kk * 16 * 128) >> 4;
-          mma_bf16_ts(tmem + COL_DV, tmem + COL_S + kk * 8, desc_add(do_mn, boff), ID_GRAD,
-                      (step > 0 || kk > 0) ? 1u : 0u);
+          mma_bf16_ts(tmem + COL_DV, tmem + a_col, desc_add(do_mn, boff), ID_GRAD, (step > 0 || kk > 0) ? 1u : 0u);
         }
         // dK_j += dS^T Q_i
         if (!mbar_wait(bar_ds_ready, step & 1, abort_flag, p.err)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < BQ / 16; ++kk) {
+          const uint32_t a_off = static_cast<uint32_t>((kk >> 2) * KSLAB + (kk & 3) * 32) >> 4;
           const uint32_t boff = static_cast<uint32_t>(kk * 16 * 128) >> 4;
-          mma_bf16_ts(tmem + COL_DK, tmem + COL_DP + kk * 8, desc_add(q_mn, boff), ID_GRAD,
+          mma_bf16_ss(tmem + COL_DK, desc_add(ds_kmaj, a_off), desc_add(q_mn, boff), ID_GRAD,
                       (step > 0 || kk > 0) ? 1u : 0u);
         }
-        // dQ_i = dS K_j (16 keys per K step), over dP^T / dS^T (read by the dK MMAs above)
+        // dQ_i = dS K_j (16 keys per K step), over dP^T (read by the row warps before ds_ready)
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk) {
           const uint32_t off16 = static_cast<uint32_t>(kk * 16 * 128) >> 4;
@@ -338,9 +345,10 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       drain_wait(bar_mma_done, 0);
     }
   } else {
-    // ================================================================ row warps (0..3), dQ warps (6..9)
+    // ================================================================ row warps (0..7), dQ warps (10..13)
     const bool dq_warp = warp >= WARP_DQ0;
     const int quad = warp & 3;
+    const int hf = dq_warp ? 0 : warp >> 2;  // query half of a row warp
     const uint32_t lane_sel = static_cast<uint32_t>(quad * 32) << 16;
     const int r = quad * 32 + lane;  // key row (S^T, dP^T, dV, dK) / query row (dQ) of this thread
     const int key = j0 + r;
@@ -350,28 +358,32 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       const int s = step % NS;
       const int h = step_head(step), i0 = step_q0(step);
       if (dq_warp) {
-        // dQ_i: this thread holds query r of the step, all 128 head dims
+        // dQ_i: this thread holds query r of the step.  Stage it in the
+        // finished Q/dO stage (its MMAs are complete: dq_full follows them) as
+        // four 32-query x 32-dim boxes per warp, 128-byte rows with the
+        // 128-byte swizzle (16-byte chunk c of row l at chunk c ^ (l % 8)).
         ok = __all_sync(0xffffffffu, mbar_wait(bar_dq_full, step & 1, abort_flag, p.err));
         if (!ok) break;
         tc_fence_after();
-        uint32_t qr[4][32];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_sel + COL_DQ + 32 * c, qr[c]);
-        tmem_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_dq_empty);  // the columns are free for the next dP^T
-        // Stage rows [32 quad, +32) in the finished Q/dO stage (its MMAs are
-        // complete: dq_full follows them) as four 32-query x 32-dim boxes,
-        // 128-byte rows with the 128-byte swizzle (16-byte chunk c of row l at
-        // chunk c ^ (l % 8)).
         uint8_t* box0 = smem + SM_STAGE + s * STAGE_BYTES + quad * (4 * 32 * 128);
 #pragma unroll
-        for (int bx = 0; bx < 4; ++bx)
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t qr[2][32];
+          tmem_ld32(tmem + lane_sel + COL_DQ + 64 * hh, qr[0]);
+          tmem_ld32(tmem + lane_sel + COL_DQ + 64 * hh + 32, qr[1]);
+          tmem_wait_ld();
+          if (hh == 1) {  // the columns are free for the next dP^T
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_dq_empty);
+          }
 #pragma unroll
-          for (int c = 0; c < 8; ++c)
-            *reinterpret_cast<uint4*>(box0 + bx * (32 * 128) + lane * 128 + ((c ^ (lane & 7)) * 16)) =
-                make_uint4(qr[bx][4 * c], qr[bx][4 * c + 1], qr[bx][4 * c + 2], qr[bx][4 * c + 3]);
+          for (int bx = 0; bx < 2; ++bx)
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              *reinterpret_cast<uint4*>(box0 + (2 * hh + bx) * (32 * 128) + lane * 128 + ((c ^ (lane & 7)) * 16)) =
+                  make_uint4(qr[bx][4 * c], qr[bx][4 * c + 1], qr[bx][4 * c + 2], qr[bx][4 * c + 3]);
+        }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
@@ -392,23 +404,22 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                                        mbar_wait(bar_s_full, step & 1, abort_flag, p.err));
       if (!ok) break;
       tc_fence_after();
-      const float* nlse2v = reinterpret_cast<const float*>(vecs + s * VEC_BYTES);
-      const float* ndeltav = nlse2v + BQ;
+      const float* nlse2v = reinterpret_cast<const float*>(vecs + s * VEC_BYTES) + 64 * hf;
+      const float* ndeltav = reinterpret_cast<const float*>(vecs + s * VEC_BYTES) + BQ + 64 * hf;
       // causal: query c of this step sees this key iff key <= i0 + c + off
-      const int c_min = p.causal ? key - off - i0 : 0;  // first visible query index (may be < 0)
-      const uint64_t c_log2_2 = f2_pack(p.c_log2, p.c_log2);
-      // P^T = 2^(S^T scale log2(e) - LSE log2(e)), 64 queries at a time, packed
-      // as bf16 pairs into S^T columns [32 hq, +32) (already read)
-#pragma unroll
-      for (int hq = 0; hq < 2; ++hq) {
+      const int c_min = p.causal ? key - off - i0 - 64 * hf : 0;  // first visible query of this half
+      // P^T = 2^(S^T scale log2(e) - LSE log2(e)) for queries [64 hf, +64),
+      // packed as bf16 pairs into S^T columns [64 hf, +32) (read by this warp only)
+      {
         uint32_t sr[2][32];
-        tmem_ld32(tmem + lane_sel + COL_S + 64 * hq, sr[0]);
-        tmem_ld32(tmem + lane_sel + COL_S + 64 * hq + 32, sr[1]);
+        tmem_ld32(tmem + lane_sel + COL_S + 64 * hf, sr[0]);
+        tmem_ld32(tmem + lane_sel + COL_S + 64 * hf + 32, sr[1]);
         tmem_wait_ld();
+        const uint64_t c_log2_2 = f2_pack(p.c_log2, p.c_log2);
         uint32_t pk[32];
 #pragma unroll
         for (int c = 0; c < 64; c += 4) {
-          const float4 l4 = *reinterpret_cast<const float4*>(nlse2v + 64 * hq + c);  // one broadcast load
+          const float4 l4 = *reinterpret_cast<const float4*>(nlse2v + c);  // one broadcast load
 #pragma unroll
           for (int e = 0; e < 4; e += 2) {
             const int cl = c + e;
@@ -420,90 +431,88 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           }
         }
         // masked entries (padding keys, causal) to 0: only warps that have some
-        if (!__all_sync(0xffffffffu, key_ok && c_min <= 64 * hq)) {
+        if (!__all_sync(0xffffffffu, key_ok && c_min <= 0)) {
 #pragma unroll
           for (int c = 0; c < 64; c += 2) {
-            const int cc = 64 * hq + c;
-            const bool v0 = key_ok && cc >= c_min, v1 = key_ok && cc + 1 >= c_min;
+            const bool v0 = key_ok && c >= c_min, v1 = key_ok && c + 1 >= c_min;
             pk[c >> 1] &= (v0 ? 0x0000FFFFu : 0u) | (v1 ? 0xFFFF0000u : 0u);
           }
         }
-        tmem_st32(tmem + lane_sel + COL_S + 32 * hq, pk);
+        tmem_st32(tmem + lane_sel + COL_S + 64 * hf, pk);
+        tmem_wait_st();
       }
-      tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_p_ready);
-      // dS^T = P^T (scale dP^T - scale D), 64 queries at a time, from the packed
-      // P^T; bf16 pairs into dP^T columns [32 hq, +32) (already read) and into
-      // row r of the shared-memory tile (two 64-query slabs, 128-byte rows,
-      // 128-byte swizzle: 16-byte chunk c of a row sits at chunk c ^ (r % 8)).
-      // The previous step's dQ MMA has read that tile: it completed before dP^T.
+      // dS^T = P^T (scale dP^T - scale D) for queries [64 hf, +64), 32 at a
+      // time, from the packed P^T, as bf16 into row r of shared-memory slab hf
+      // (128-byte rows, 128-byte swizzle: 16-byte chunk c of a row sits at
+      // chunk c ^ (r % 8)).  The previous step's dK and dQ MMAs have read that
+      // tile: they completed before dP^T.
       ok = __all_sync(0xffffffffu, mbar_wait(bar_dp_full, step & 1, abort_flag, p.err));
       if (!ok) break;
       tc_fence_after();
-      const uint64_t scale2 = f2_pack(p.scale, p.scale);
+      {
+        const uint64_t scale2 = f2_pack(p.scale, p.scale);
+        uint8_t* ds_row = smem + SM_DS + hf * KSLAB + r * 128;
 #pragma unroll
-      for (int hq = 0; hq < 2; ++hq) {
-        uint32_t dr[2][32], pp[32];
-        tmem_ld32(tmem + lane_sel + COL_DP + 64 * hq, dr[0]);
-        tmem_ld32(tmem + lane_sel + COL_DP + 64 * hq + 32, dr[1]);
-        tmem_ld32(tmem + lane_sel + COL_S + 32 * hq, pp);
-        tmem_wait_ld();
-        uint32_t dk[32];
+        for (int qc = 0; qc < 2; ++qc) {
+          uint32_t dr[32], pp[16];
+          tmem_ld32(tmem + lane_sel + COL_DP + 64 * hf + 32 * qc, dr);
+          tmem_ld16(tmem + lane_sel + COL_S + 64 * hf + 16 * qc, pp);
+          tmem_wait_ld();
+          uint32_t dk[16];
 #pragma unroll
-        for (int c = 0; c < 64; c += 4) {
-          const float4 d4 = *reinterpret_cast<const float4*>(ndeltav + 64 * hq + c);  // one broadcast load
+          for (int c = 0; c < 32; c += 4) {
+            const float4 d4 = *reinterpret_cast<const float4*>(ndeltav + 32 * qc + c);  // one broadcast load
 #pragma unroll
-          for (int e = 0; e < 4; e += 2) {
-            const int cl = c + e;
-            const uint64_t p2 = f2_pack(__uint_as_float(pp[cl >> 1] << 16), __uint_as_float(pp[cl >> 1] & 0xFFFF0000u));
-            const uint64_t dp2 = f2_pack(__uint_as_float(dr[cl >> 5][cl & 31]), __uint_as_float(dr[cl >> 5][(cl & 31) + 1]));
-            float d0, d1;
-            f2_unpack(f2_mul(p2, f2_fma(dp2, scale2, e == 0 ? f2_pack(d4.x, d4.y) : f2_pack(d4.z, d4.w))), d0, d1);
-            dk[cl >> 1] = pack_bf16x2(d0, d1);
+            for (int e = 0; e < 4; e += 2) {
+              const int cl = c + e;
+              const uint64_t p2 =
+                  f2_pack(__uint_as_float(pp[cl >> 1] << 16), __uint_as_float(pp[cl >> 1] & 0xFFFF0000u));
+              const uint64_t dp2 = f2_pack(__uint_as_float(dr[cl]), __uint_as_float(dr[cl + 1]));
+              float d0, d1;
+              f2_unpack(f2_mul(p2, f2_fma(dp2, scale2, e == 0 ? f2_pack(d4.x, d4.y) : f2_pack(d4.z, d4.w))), d0, d1);
+              dk[cl >> 1] = pack_bf16x2(d0, d1);
+            }
           }
-        }
-        tmem_st32(tmem + lane_sel + COL_DP + 32 * hq, dk);
-        uint8_t* ds_row = smem + SM_DS + hq * KSLAB + r * 128;
 #pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8)
-          *reinterpret_cast<uint4*>(ds_row + ((c8 ^ (r & 7)) * 16)) =
-              make_uint4(dk[4 * c8], dk[4 * c8 + 1], dk[4 * c8 + 2], dk[4 * c8 + 3]);
+          for (int c4 = 0; c4 < 4; ++c4)
+            *reinterpret_cast<uint4*>(ds_row + (((4 * qc + c4) ^ (r & 7)) * 16)) =
+                make_uint4(dk[4 * c4], dk[4 * c4 + 1], dk[4 * c4 + 2], dk[4 * c4 + 3]);
+        }
       }
       fence_proxy_async_smem();
-      tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_ds_ready);
     }
     if (dq_warp && lane == 0) bulk_wait_group0();  // the dQ adds are complete before the CTA exits
-    // dV_j (row warps) or dK_j (dQ warps): this thread's key row
-    if (ok) {
+    // dV_j (row warps of query half 0) or dK_j (row warps of query half 1): this thread's key row
+    if (ok && !dq_warp) {
       if (n_steps > 0) ok = __all_sync(0xffffffffu, mbar_wait(bar_kv_done, 0, abort_flag, p.err));
       if (ok) {
         tc_fence_after();
         const size_t orow = (static_cast<size_t>(b) * p.Hkv + kvh) * p.Nk + key;
-        uint32_t g[HD];
-        if (n_steps > 0) {
+        uint4* dst = reinterpret_cast<uint4*>((hf ? p.dk : p.dv) + orow * HD);
 #pragma unroll
-          for (int ch = 0; ch < HD / 32; ++ch) {
-            uint32_t (&gc)[32] = *reinterpret_cast<uint32_t(*)[32]>(g + 32 * ch);
-            tmem_ld32(tmem + lane_sel + (dq_warp ? COL_DK : COL_DV) + ch * 32, gc);
+        for (int ch = 0; ch < HD / 32; ++ch) {
+          uint32_t g[32];
+          if (n_steps > 0) {
+            tmem_ld32(tmem + lane_sel + (hf ? COL_DK : COL_DV) + ch * 32, g);
+            tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) g[i] = 0u;
           }
-          tmem_wait_ld();
-        } else {
+          if (key_ok) {
 #pragma unroll
-          for (int i = 0; i < HD; ++i) g[i] = 0u;
-        }
-        if (key_ok) {
-          uint4* dst = reinterpret_cast<uint4*>((dq_warp ? p.dk : p.dv) + orow * HD);
-#pragma unroll
-          for (int i = 0; i < HD / 8; ++i)
-            dst[i] = make_uint4(pack_bf16x2(__uint_as_float(g[8 * i + 0]), __uint_as_float(g[8 * i + 1])),
-                                pack_bf16x2(__uint_as_float(g[8 * i + 2]), __uint_as_float(g[8 * i + 3])),
-                                pack_bf16x2(__uint_as_float(g[8 * i + 4]), __uint_as_float(g[8 * i + 5])),
-                                pack_bf16x2(__uint_as_float(g[8 * i + 6]), __uint_as_float(g[8 * i + 7])));
+            for (int i = 0; i < 4; ++i)
+              dst[4 * ch + i] = make_uint4(pack_bf16x2(__uint_as_float(g[8 * i + 0]), __uint_as_float(g[8 * i + 1])),
+                                           pack_bf16x2(__uint_as_float(g[8 * i + 2]), __uint_as_float(g[8 * i + 3])),
+                                           pack_bf16x2(__uint_as_float(g[8 * i + 4]), __uint_as_float(g[8 * i + 5])),
+                                           pack_bf16x2(__uint_as_float(g[8 * i + 6]), __uint_as_float(g[8 * i + 7])));
+          }
         }
       }
     }
