@@ -584,6 +584,12 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
         // is handed to the MMA issuer as soon as it is in tensor memory.
         const uint64_t c2 = f2_pack(c, c);
         const uint64_t nm2 = f2_pack(-m_use, -m_use);
+        // softcap in exp2 units: cap_post tanh(y) - m = (cap_post - m) - 2 cap_post / (1 + 2^(2 y log2 e)),
+        // y = cap_pre s (the identity holds for either sign of y and saturates through inf and 0)
+        const uint64_t k2 = f2_pack(p.cap_pre * 2.8853900817779268f, p.cap_pre * 2.8853900817779268f);
+        const uint64_t one2 = f2_pack(1.f, 1.f);
+        const uint64_t ncp2 = f2_pack(-2.f * p.cap_post, -2.f * p.cap_post);
+        const uint64_t cpm2 = f2_pack(p.cap_post - m_use, p.cap_post - m_use);
         uint64_t sum2[2] = {0ull, 0ull};
 #pragma unroll
         for (int half = 0; half < 2; ++half) {  // P columns [32*half, +32) = keys [64*half, +64)
@@ -596,8 +602,10 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
               float x0, x1;
               if constexpr (CAP) {
                 // capped score in exp2 units; masked scores stay -inf
-                x0 = fmaf(p.cap_post, tanh_exp(p.cap_pre * s[c0 + 2 * i]), -m_use);
-                x1 = fmaf(p.cap_post, tanh_exp(p.cap_pre * s[c0 + 2 * i + 1]), -m_use);
+                float e0, e1, d0, d1;
+                f2_unpack(f2_mul(f2_pack(s[c0 + 2 * i], s[c0 + 2 * i + 1]), k2), e0, e1);
+                f2_unpack(f2_add(f2_pack(ex2_approx(e0), ex2_approx(e1)), one2), d0, d1);
+                f2_unpack(f2_fma(f2_pack(rcp_approx(d0), rcp_approx(d1)), ncp2, cpm2), x0, x1);
                 if (need_mask) {
                   if (s[c0 + 2 * i] == -CUDART_INF_F) x0 = -CUDART_INF_F;
                   if (s[c0 + 2 * i + 1] == -CUDART_INF_F) x1 = -CUDART_INF_F;
