@@ -14,9 +14,11 @@
 //     round trip); the KV heads of one chunk are adjacent items, so
 //     neighbouring CTAs read neighbouring 256-byte rows of the cache;
 //   * one producer thread streams 64-key K and V tiles ([64 keys][128] bf16,
-//     16 KB, through a 5-slot TMA ring; or [64 keys][128] fp8 E4M3 codes,
-//     8 KB, through a 10-slot ring), so 80 KB per CTA (two CTAs per SM) are in
-//     flight;
+//     16 KB, through a 3-slot TMA ring; or [64 keys][128] fp8 E4M3 codes,
+//     8 KB, through a 6-slot ring), so 48 KB per CTA and, with three CTAs per
+//     SM, 144 KB per SM are in flight (three CTAs rather than two with larger
+//     rings: the consumers, not the copies, set the pace, and more resident
+//     warps hide their latencies better);
 //   * an fp8 cache holds E4M3 codes whose values are code * k_scale (K) and
 //     code * v_scale (V): codes convert exactly to fp32 (through f16, which
 //     holds every E4M3 value), k_scale folds into the softmax scale and v_scale
@@ -40,7 +42,8 @@ namespace decode {
 
 constexpr int HD = 128;
 constexpr int TILE = 64;                      // keys per TMA tile
-constexpr int RING_BYTES = 5 * TILE * HD * 2; // 80 KB of K/V tiles in flight per CTA
+constexpr int RING_BYTES = 3 * TILE * HD * 2; // 48 KB of K/V tiles in flight per CTA
+constexpr int CTAS_PER_SM = 3;                 // 144 KB in flight per SM
 constexpr int MAX_STAGES = 10;
 
 // Ring geometry for a bf16 (KV8 = false) or fp8 E4M3 (KV8 = true) cache.
@@ -192,7 +195,7 @@ struct Paging {
 };
 
 template <int G, bool PAGED, bool KV8>
-__global__ void __launch_bounds__(NTHREADS, 2)
+__global__ void __launch_bounds__(NTHREADS, CTAS_PER_SM)
 attn_decode_splitkv_kernel(const __grid_constant__ CUtensorMap tm_k,
                            const __grid_constant__ CUtensorMap tm_v,
                            const __nv_bfloat16* __restrict__ q, const int* __restrict__ seqlens,
@@ -492,6 +495,8 @@ int launch_split(const CUtensorMap& tk, const CUtensorMap& tv, const void* q, co
   const int smem = L.bytes + 1024;
   static int attr_dev = -1;
   static int attr_bytes = 0;
+  static int attr_smem = -1;   // shared-memory size the resident count below is for
+  static int resident = 1;     // CTAs of this instance that fit on one SM
   int dev = 0;
   cudaGetDevice(&dev);
   if (attr_dev != dev || attr_bytes < smem) {
@@ -500,8 +505,19 @@ int launch_split(const CUtensorMap& tk, const CUtensorMap& tv, const void* q, co
       return ATTN_ERR_CUDA;
     attr_dev = dev;
     attr_bytes = smem;
+    attr_smem = -1;
   }
-  const int grid = 2 * num_sms;
+  if (attr_smem != smem) {
+    // the persistent grid is as many CTAs as are resident at once: up to three
+    // per SM, fewer when a large chunk or head group enlarges the score area
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_decode_splitkv_kernel<G, PAGED, KV8>, NTHREADS,
+                                                      smem) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    resident = n < 1 ? 1 : (n > CTAS_PER_SM ? CTAS_PER_SM : n);
+    attr_smem = smem;
+  }
+  const int grid = resident * num_sms;
   attn_decode_splitkv_kernel<G, PAGED, KV8><<<grid, NTHREADS, smem, stream>>>(
       tk, tv, static_cast<const __nv_bfloat16*>(q), seqlens, ws_o, ws_lse, B, Hq, Hkv, Nk_max, chunk,
       S_max, scale * k_scale * 1.4426950408889634f, v_scale, err, pg);
