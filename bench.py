@@ -460,6 +460,8 @@ def run_gb300(args, rank, world, local_rank):
         wall1 = time.perf_counter()
     clocks = clk.summary()
     ms_step = max_over_ranks(sum(ms) / len(ms))
+    ms_median = max_over_ranks(statistics.median(ms))
+    ms_min = max_over_ranks(min(ms))
     value = world * rate(w, ms_step)
     if w["name"] in DECODE_NAMES:   # roofline of the dominant kernel: the split-KV partial step
         ms_k = max_over_ranks(statistics.mean(time_steps(torch, w["split_fn"], min(args.steps, 50), 3, flush, stream)))
@@ -471,6 +473,27 @@ def run_gb300(args, rank, world, local_rank):
     rc = binding.get_device_error()
     if rc != 0:
         raise RuntimeError(f"device error word {rc} after the timed region")
+
+    # ---------------- launch floor: the smallest valid forward call (one 128-query tile), timed
+    # back to back, against which the timed steps above are long enough to ignore launch costs
+    lq = torch.randn(1, 1, 128, 128, device=dev).to(torch.bfloat16)
+    lo = torch.empty_like(lq)
+    ll = torch.empty(1, 1, 128, device=dev)
+    for _ in range(10):
+        binding.attn_fwd(lq, lq, lq, lo, ll)
+    torch.cuda.synchronize()
+    n_floor = 200
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    ev0.record(stream)
+    for _ in range(n_floor):
+        binding.attn_fwd(lq, lq, lq, lo, ll)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    launch_floor = {"us_per_call_device": ev0.elapsed_time(ev1) * 1e3 / n_floor,
+                    "us_per_call_host": (time.perf_counter() - t0) * 1e6 / n_floor,
+                    "call": "attn_fwd B=1 H=1 N=128 D=128 bf16, 200 calls back to back"}
+    del lq, lo, ll
 
     # ---------------- end to end: pinned host inputs copied in, results copied out, every step
     e2e = None
@@ -544,7 +567,8 @@ def run_gb300(args, rank, world, local_rank):
 
     line = {
         "metric": METRIC, "value": value, "unit": main["unit"], "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": ms_step, "ms_per_step_median": ms_median, "ms_per_step_min": ms_min,
+        "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": main["dtype"], "data": "synthetic",
         "config": {"workload": main_work_desc, "global_batch": world * main["batch"], "seq_len": main["seq_len"],
                    "parallelism": "replicas" if world > 1 else "single",
@@ -554,6 +578,7 @@ def run_gb300(args, rank, world, local_rank):
         "e2e": e2e,
         "gpu_launches": args.steps * main["launches"],
         "wall_s_timed_region": wall1 - wall0,
+        "launch_floor": launch_floor,
         "clocks": clocks,
         "workloads": workloads,
         "cpu_baseline": cpu,
