@@ -202,7 +202,8 @@ int attn_decode_splitkv_paged(const void* q, const void* k_pages, const void* v_
 
 /*
  * attn_bwd_workspace_size — bytes of device workspace attn_bwd needs:
- *   2 * B * Hq * ceil(Nq / 64) * 64 * 4 (per query: LSE * log2(e) and D).
+ *   2 * B * Hq * ceil(Nq / 128) * 128 * 4 (per query, padded to 128 rows per
+ *   head: -LSE * log2(e) and -scale * D with D = rowsum(dO * O)).
  */
 size_t attn_bwd_workspace_size(int B, int Hq, int Nq);
 
