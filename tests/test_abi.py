@@ -189,6 +189,7 @@ def test_backward_argument_errors(L):
     assert f(dq=MIS) == -5
     assert f(scale=-1.0) == -6
     assert L.attn_bwd_workspace_size(2, 8, 100) == 2 * 2 * 8 * 128 * 4
+    assert L.attn_bwd_workspace_size(1, 3, 130) == 2 * 1 * 3 * 256 * 4   # 128 rows per head
 
 
 def test_workspace_size(L):
