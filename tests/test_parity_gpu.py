@@ -516,6 +516,26 @@ def test_backward(dev, case):
     assert binding.get_device_error() == 0
 
 
+def test_backward_full_size_two_heads(dev):
+    """The benchmarked backward (B=1 H=32 N=8192 D=128, non-causal, the bench's inputs and dO
+    draw and the same launch): every dQ, dK and dV row of heads 0 and 17 against the oracle,
+    whose per-head fp64 backward fits this size (about 86 GFLOP and 2.6 GB per head)."""
+    B, H, N, D, seed = 1, 32, 8192, 128, 0
+    q, k, v = inputs.prefill_inputs(B, H, H, N, N, D, "bf16", seed)
+    do = torch.randn(B, H, N, D, generator=torch.Generator("cpu").manual_seed(seed + 9)).to(torch.bfloat16)
+    qd, kd, vd, dod = q.to(dev), k.to(dev), v.to(dev), do.to(dev)
+    o, lse = binding.attn_fwd(qd, kd, vd)
+    dq, dk, dv = binding.attn_bwd(qd, kd, vd, o, dod, lse)
+    torch.cuda.synchronize()
+    assert binding.get_device_error() == 0
+    for h in (0, 17):
+        sl = slice(h, h + 1)
+        dQ, dK, dV = oracle.attention_backward(q[:, sl], k[:, sl], v[:, sl], do[:, sl], 1 / math.sqrt(D), False, 0)
+        _bwd_check(dq[:, sl], dQ, f"dQ head {h}")
+        _bwd_check(dk[:, sl], dK, f"dK head {h}")
+        _bwd_check(dv[:, sl], dV, f"dV head {h}")
+
+
 def test_backward_multi_tile(dev):
     """B=1 Hq=4 Hkv=2 N=2048 causal: 16 key tiles x 32 query tiles per head."""
     q, k, v = inputs.prefill_inputs(1, 4, 2, 2048, 2048, 128, "bf16", seed=5)
