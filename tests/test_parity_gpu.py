@@ -200,6 +200,29 @@ def test_bf16_varlen(dev, case):
     assert binding.get_device_error() == 0
 
 
+def test_bf16_varlen_benchmark_workload_sampled(dev):
+    """The benchmark's ragged batch (32 causal sequences, lengths ~U[512, 8192], Hq=32 Hkv=8,
+    the bench's draws and launch): sampled rows of every sequence, including its first and
+    last, against the oracle on that sequence alone."""
+    Hq, Hkv, D = 32, 8, 128
+    lens = torch.randint(512, 8192 + 1, (32,), generator=torch.Generator("cpu").manual_seed(11)).tolist()
+    q, k, v, cq, ck = inputs.varlen_inputs(lens, lens, Hq, Hkv, D, "bf16", 0)
+    o, lse = binding.attn_fwd_varlen(q.to(dev), k.to(dev), v.to(dev), cq.to(dev), ck.to(dev), max(lens),
+                                     causal=True)
+    o, lse = o.cpu(), lse.cpu()
+    assert binding.get_device_error() == 0
+    rng = np.random.default_rng(3)
+    for b, n in enumerate(lens):
+        t0 = int(cq[b])
+        seq = lambda x: x[t0:t0 + n].permute(1, 0, 2).unsqueeze(0)  # noqa: E731  [1, H, n, D]
+        rows = sorted({(0, int(rng.integers(Hq)), i)
+                       for i in (0, n - 1, int(rng.integers(n)), int(rng.integers(n)), int(rng.integers(n)))})
+        O, L = oracle.attention_rows(seq(q), seq(k), seq(v), 1 / math.sqrt(D), rows, True)
+        hs = [h for _, h, _ in rows]
+        ts = [t0 + i for _, _, i in rows]
+        check(o[ts, hs], lse[hs, ts], O, L, BF16_O_TOL, BF16_LSE_REL, True)
+
+
 @pytest.mark.parametrize("name,B,Hq,Hkv,Nq,Nk,D,causal,window", [
     ("sliding_window_4096_B1_H32_KV8_N16384", 1, 32, 8, 16384, 16384, 128, True, 4096),
     ("chunked_prefill_B1_H32_KV8_Nq2048_Nk16384", 1, 32, 8, 2048, 16384, 128, True, 0),
