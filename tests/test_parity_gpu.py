@@ -509,6 +509,7 @@ BWD_CASES = [
     (1, 2, 2, 300, 130, True),      # Nq > Nk: rows 0..169 see no key
     (1, 2, 1, 64, 1000, False),     # one query tile, many key tiles
     (1, 4, 2, 384, 384, True),      # whole tiles only, two query heads per KV head
+    (2, 2, 1, 5, 37, True),         # fewer queries than one 32-row dQ box
 ]
 
 
