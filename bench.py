@@ -328,10 +328,15 @@ def make_workload(name, dev, seed, peaks, peak_src, sm_max_mhz, decode_batch=Non
         call = {"fp32": binding.attn_fwd_fp32, "fp16": binding.attn_fwd_fp16}.get(name, binding.attn_fwd)
         wnd = c.get("window", 0)
         w["fn"] = lambda: call(q, k, v, o, lse, causal=c["causal"], window=wnd)
+        # the same step on other buffers (the pipelined end-to-end loop alternates two sets)
+        w["make_fn"] = lambda ins, outs: (lambda: call(ins[0], ins[1], ins[2], outs[0], outs[1],
+                                                       causal=c["causal"], window=wnd))
         if name == "softcap":
             sinks = torch.randn(c["Hq"], generator=torch.Generator("cpu").manual_seed(seed + 5)).float().to(dev)
             w["fn"] = lambda: binding.attn_fwd_softcap_sink(q, k, v, o, lse, causal=c["causal"], softcap=50.0,
                                                             sinks=sinks)
+            w["make_fn"] = lambda ins, outs: (lambda: binding.attn_fwd_softcap_sink(
+                ins[0], ins[1], ins[2], outs[0], outs[1], causal=c["causal"], softcap=50.0, sinks=sinks))
         w["work"] = masked_flops(c["B"], c["Hq"], Nq, Nk, c["D"], c["causal"], wnd) if "Nq" in c else flops(**c)
         w["unit"] = "TFLOP/s"
         w["launches"] = 1
@@ -530,7 +535,59 @@ def run_gb300(args, rank, world, local_rank):
         e2e = {"value": world * rate(w, e2e_ms), "unit": w["unit"],
                "h2d_bytes_per_step": sum(hp.numel() * hp.element_size() for hp, _ in pins),
                "d2h_bytes_per_step": sum(hp.numel() * hp.element_size() for hp, _ in outs),
-               "ms_per_step": e2e_ms}
+               "ms_per_step": e2e_ms, "pipelined": False}
+        if "make_fn" in w:
+            # Pipelined: the same steps (each copies its inputs in from pinned host memory and
+            # its results out to pinned host memory) with step i+1's copy in and step i-1's
+            # copy out running on their own streams while step i computes.  Two sets of device
+            # buffers alternate so that no copy touches a buffer a kernel still uses.
+            sets_in = [[t for _, t in pins], [torch.empty_like(t) for _, t in pins]]
+            sets_out = [[t for _, t in outs], [torch.empty_like(t) for _, t in outs]]
+            host_out = [[hp for hp, _ in outs], [torch.empty(t.shape, dtype=t.dtype).pin_memory() for _, t in outs]]
+            fns = [w["make_fn"](sets_in[j], sets_out[j]) for j in range(2)]
+            s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+            ev_in = [torch.cuda.Event() for _ in range(2)]
+            ev_comp = [torch.cuda.Event() for _ in range(2)]
+            ev_out = [torch.cuda.Event() for _ in range(2)]
+
+            def pipelined(n):
+                s_in.wait_stream(stream)
+                s_out.wait_stream(stream)
+                for i in range(n):
+                    j = i % 2
+                    with torch.cuda.stream(s_in):
+                        if i >= 2:
+                            s_in.wait_event(ev_comp[j])      # step i-2's kernel has read set j
+                        for (hp, _), t in zip(pins, sets_in[j]):
+                            t.copy_(hp, non_blocking=True)
+                        ev_in[j].record(s_in)
+                    stream.wait_event(ev_in[j])
+                    if i >= 2:
+                        stream.wait_event(ev_out[j])         # step i-2's results are out
+                    fns[j]()
+                    ev_comp[j].record(stream)
+                    with torch.cuda.stream(s_out):
+                        s_out.wait_event(ev_comp[j])
+                        for hp, t in zip(host_out[j], sets_out[j]):
+                            hp.copy_(t, non_blocking=True)
+                        ev_out[j].record(s_out)
+                stream.wait_stream(s_out)
+
+            pipelined(3)
+            torch.cuda.synchronize()
+            barrier()
+            t0 = time.perf_counter()
+            ev0.record(stream)
+            pipelined(e2e_steps)
+            ev1.record(stream)
+            torch.cuda.synchronize()
+            barrier()
+            p_ms = max_over_ranks(max(ev0.elapsed_time(ev1), (time.perf_counter() - t0) * 1e3) / e2e_steps)
+            e2e.update({"serial_value": e2e["value"], "serial_ms_per_step": e2e_ms,
+                        "value": world * rate(w, p_ms), "ms_per_step": p_ms, "pipelined": True,
+                        "pipelining": "step i+1's copy in and step i-1's copy out overlap step i "
+                                      "(two device buffer sets, three streams)"})
+            del sets_in, sets_out, host_out, fns
         del pins, outs
     main_work_desc = w["desc"]
     main = {k: w[k] for k in ("name", "unit", "bound", "peak", "peak_source", "dtype", "seq_len", "batch", "launches")}
