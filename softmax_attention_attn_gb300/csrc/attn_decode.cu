@@ -469,13 +469,25 @@ attn_decode_combine_kernel(const float* __restrict__ ws_o, const float* __restri
     const float wc = (c0 + lane < n) ? ex2_approx((lp[c0 + lane] - M) * LOG2E) : 0.f;
     s += wc;
     const int cnt = min(32, n - c0);
-    for (int j = 0; j < cnt; ++j) {
-      const float w = __shfl_sync(0xffffffffu, wc, j);
-      const float4 x = *reinterpret_cast<const float4*>(op + static_cast<size_t>(c0 + j) * HD);
-      acc.x = fmaf(w, x.x, acc.x);
-      acc.y = fmaf(w, x.y, acc.y);
-      acc.z = fmaf(w, x.z, acc.z);
-      acc.w = fmaf(w, x.w, acc.w);
+    // eight chunks at a time, all eight loads in flight before the sums (chunks past the
+    // count load zeros and add nothing: their weights are finite)
+    for (int j0 = 0; j0 < cnt; j0 += 8) {
+      float4 x[8];
+      float w[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int j = j0 + u;
+        w[u] = __shfl_sync(0xffffffffu, wc, j & 31);
+        x[u] = j < cnt ? *reinterpret_cast<const float4*>(op + static_cast<size_t>(c0 + j) * HD)
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        acc.x = fmaf(w[u], x[u].x, acc.x);
+        acc.y = fmaf(w[u], x[u].y, acc.y);
+        acc.z = fmaf(w[u], x[u].z, acc.z);
+        acc.w = fmaf(w[u], x[u].w, acc.w);
+      }
     }
   }
 #pragma unroll
