@@ -25,20 +25,20 @@
 //     (A from shared memory);
 //   * dQ_i = dS K_j (M = 128 queries, N = 128 head dims; both operands
 //     MN-major in shared memory: dS^T and K_j as they lie) over the dP^T
-//     columns (the dK MMA that reads dS^T from them runs first: MMAs of one
-//     thread execute in order); four more warps read it (thread r owns query
+//     columns, which the row warps have read before handing dS^T over; four
+//     more warps read it (thread r owns query
 //     r), free the columns for the next dP^T, stage it as fp32 in the Q/dO
 //     stage the step has finished with (128-byte swizzled 32 x 32 boxes) and
 //     add it to the fp32 dQ with TMA reduce-add copies while the next step
 //     runs.  (Per-thread global atomics here would fill the load/store queue
 //     that the row warps' shared-memory loads share.)  The stage is handed
 //     back to the TMA warp once the copies have read it;
-//   * one TMA warp streams Q_i, dO_i (and the per-query LSE*log2(e) and D
-//     vectors, prepared by attn_bwd_prep_kernel) through a 2-stage ring; one
+//   * one TMA warp streams Q_i, dO_i (and the per-query -LSE*log2(e) and
+//     -scale*D vectors, prepared by attn_bwd_prep_kernel) through a 2-stage ring; one
 //     thread issues every MMA.  128-query steps keep every MMA at N = 128 or
 //     K = 128: a 128 x 64 x 16 MMA takes almost as long to issue and run as a
 //     128 x 128 x 16 one.
-// Tensor memory (512 columns): S^T / P^T [0,128), dP^T / dS^T / dQ [128,256),
+// Tensor memory (512 columns): S^T / P^T [0,128), dP^T / dQ [128,256),
 // dV [256,384), dK [384,512).  Shared memory: the 1024-byte aligned operand
 // block (K_j, V_j, two Q/dO stages, dS^T) fills all but 3 KB of the 227 KB, so
 // the barriers sit in front of it when the alignment padding has room and
@@ -66,7 +66,7 @@ constexpr int SM_STAGE = SM_V + 2 * KSLAB;
 constexpr int STAGE_BYTES = 4 * QSLAB;           // Q_i (2 slabs) + dO_i (2 slabs)
 constexpr int SM_DS = SM_STAGE + NS * STAGE_BYTES;  // dS^T [128 keys][128 queries] bf16, 2 slabs
 constexpr int SM_BIG = SM_DS + 2 * KSLAB;        // end of the operand block
-constexpr int VEC_BYTES = 2 * BQ * 4;            // LSE*log2(e)[128], D[128]
+constexpr int VEC_BYTES = 2 * BQ * 4;            // -LSE*log2(e)[128], -scale*D[128]
 constexpr int NUM_BARS = 1 + 2 * NS + 8;
 constexpr int SMALL_BYTES = 128;                 // barriers + misc words
 static_assert(NUM_BARS * 8 + 16 <= SMALL_BYTES, "small block");
@@ -88,7 +88,7 @@ constexpr uint32_t idesc(uint32_t M, uint32_t N, uint32_t a_mn, uint32_t b_mn) {
          ((M >> 4) << 24);
 }
 constexpr uint32_t ID_ST = idesc(BK, BQ, 0, 0);   // S^T, dP^T: K / V and Q / dO, both K-major
-constexpr uint32_t ID_GRAD = idesc(BK, HD, 0, 1); // dV, dK: P^T / dS^T in TMEM, dO / Q MN-major
+constexpr uint32_t ID_GRAD = idesc(BK, HD, 0, 1); // dV, dK: P^T (TMEM) / dS^T (smem, K-major), dO / Q MN-major
 constexpr uint32_t ID_DQ = idesc(BQ, HD, 1, 1);   // dQ: dS (from dS^T) and K, both MN-major
 static_assert(BQ == 128 && BK == 128 && HD == 128, "tile shapes");
 
