@@ -42,13 +42,16 @@ namespace decode {
 
 constexpr int HD = 128;
 constexpr int TILE = 64;                      // keys per TMA tile
-constexpr int RING_BYTES = 3 * TILE * HD * 2; // 48 KB of K/V tiles in flight per CTA
-constexpr int CTAS_PER_SM = 3;                 // 144 KB in flight per SM
 constexpr int MAX_STAGES = 10;
 
-// Ring geometry for a bf16 (KV8 = false) or fp8 E4M3 (KV8 = true) cache.
-template <bool KV8>
+// Residency and ring geometry for a bf16 (KV8 = false) or fp8 E4M3 (KV8 = true)
+// cache: three CTAs per SM with 48 KB rings (144 KB in flight per SM); four with
+// 32 KB rings (128 KB) for the fp8 cache with up to four query heads per KV
+// head, whose consumers need the extra warps most and fit in the registers.
+template <int G, bool KV8>
 struct Ring {
+  static constexpr int CTAS_PER_SM = (KV8 && G <= 4) ? 4 : 3;
+  static constexpr int RING_BYTES = (CTAS_PER_SM == 4 ? 2 : 3) * TILE * HD * 2;
   static constexpr int ROW_BYTES = KV8 ? HD : 2 * HD;  // one key row of one KV head
   static constexpr int TILE_BYTES = TILE * ROW_BYTES;
   static constexpr int STAGES = RING_BYTES / TILE_BYTES;
@@ -62,10 +65,10 @@ struct Layout {
   int ring, work, stats, bars, misc, split, bytes;
 };
 
-__host__ __device__ inline Layout layout(int G, int chunk, int B) {
+__host__ __device__ inline Layout layout(int G, int chunk, int B, int ring_bytes) {
   Layout L;
   L.ring = 0;
-  L.work = L.ring + RING_BYTES;
+  L.work = L.ring + ring_bytes;
   const int scores = G * chunk * 4;
   const int red = 8 * G * HD * 4;
   L.stats = L.work + (scores > red ? scores : red);
@@ -195,20 +198,20 @@ struct Paging {
 };
 
 template <int G, bool PAGED, bool KV8>
-__global__ void __launch_bounds__(NTHREADS, CTAS_PER_SM)
+__global__ void __launch_bounds__(NTHREADS, (Ring<G, KV8>::CTAS_PER_SM))
 attn_decode_splitkv_kernel(const __grid_constant__ CUtensorMap tm_k,
                            const __grid_constant__ CUtensorMap tm_v,
                            const __nv_bfloat16* __restrict__ q, const int* __restrict__ seqlens,
                            float* __restrict__ ws_o, float* __restrict__ ws_lse, int B, int Hq,
                            int Hkv, int Nk_max, int chunk, int S_max, float c_log2, float v_scale,
                            int* err, const Paging pg) {
-  constexpr int STAGES = Ring<KV8>::STAGES;
-  constexpr int TILE_BYTES = Ring<KV8>::TILE_BYTES;
+  constexpr int STAGES = Ring<G, KV8>::STAGES;
+  constexpr int TILE_BYTES = Ring<G, KV8>::TILE_BYTES;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
   const uint32_t sb = smem_u32(smem);
-  const Layout L = layout(G, chunk, B);
+  const Layout L = layout(G, chunk, B, Ring<G, KV8>::RING_BYTES);
   float* work = reinterpret_cast<float*>(smem + L.work);   // scores / p, then reduction buffer
   float* st_m = reinterpret_cast<float*>(smem + L.stats);
   float* st_l = st_m + 8;
@@ -503,7 +506,7 @@ int launch_split(const CUtensorMap& tk, const CUtensorMap& tv, const void* q, co
                  float* ws_o, float* ws_lse, int B, int Hq, int Hkv, int Nk_max, float scale,
                  int chunk, int S_max, int num_sms, cudaStream_t stream, int* err, const Paging& pg,
                  float k_scale, float v_scale) {
-  const Layout L = layout(G, chunk, B);
+  const Layout L = layout(G, chunk, B, Ring<G, KV8>::RING_BYTES);
   const int smem = L.bytes + 1024;
   static int attr_dev = -1;
   static int attr_bytes = 0;
@@ -521,12 +524,14 @@ int launch_split(const CUtensorMap& tk, const CUtensorMap& tv, const void* q, co
   }
   if (attr_smem != smem) {
     // the persistent grid is as many CTAs as are resident at once: up to three
-    // per SM, fewer when a large chunk or head group enlarges the score area
+    // (fp8 cache, G <= 4: four) per SM, fewer when a large chunk or head group
+    // enlarges the score area
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_decode_splitkv_kernel<G, PAGED, KV8>, NTHREADS,
                                                       smem) != cudaSuccess)
       return ATTN_ERR_CUDA;
-    resident = n < 1 ? 1 : (n > CTAS_PER_SM ? CTAS_PER_SM : n);
+    constexpr int cap = Ring<G, KV8>::CTAS_PER_SM;
+    resident = n < 1 ? 1 : (n > cap ? cap : n);
     attr_smem = smem;
   }
   const int grid = resident * num_sms;
