@@ -6,22 +6,29 @@ loads, S = Q K^T, mask, online softmax, O correction, O += P V, epilogue) over
 the dense workload B=1 H=32 N=8192 D=128, inputs resident in HBM, L2 flushed
 before every step (a 256 MiB write), each step timed with CUDA events on the
 launching stream.  ``value`` is attention-forward TFLOP/s counted as
-4*B*Hq*Nq*Nk*D (halved for causal).  The same JSON line also carries:
+4*B*Hq*Nq*Nk*D (halved for causal).  The one JSON line printed on stdout is
+kept short (every figure rounded to four significant digits) and carries:
 
-* ``e2e``: the same metric through the C ABI with the inputs copied from pinned
-  host memory and O / LSE copied back inside every timed step;
 * ``roofline``: achieved TFLOP/s of the kernel against the measured dense bf16
   peak, plus the DRAM traffic of one ncu capture of the same kernel;
-* ``workloads``: the causal GQA prefill (B=4 Hq=32 Hkv=8 N=4096), the split-KV
-  decode (B=64 Hq=32 Hkv=8, Nk_b ~ U[512, 32768], chunk 512, HBM GB/s against
-  the measured copy bandwidth) and the fp32 prefill (B=2 H=8 N=4096 D=128);
-* ``cpu_baseline``: the fp64 CPU oracle timed on this host on a bounded
-  sample of the same workload;
+* ``decode``: the split-KV decode (B=64 Hq=32 Hkv=8, Nk_b ~ U[512, 32768],
+  chunk 512) in HBM GB/s against the measured copy bandwidth, for the whole
+  step and for the partial-step kernel alone;
+* ``causal``: the causal GQA prefill (B=4 Hq=32 Hkv=8 N=4096) in TFLOP/s;
+* ``e2e``: the same metric through the C ABI with the inputs copied from pinned
+  host memory and O / LSE copied back inside every timed step;
+* ``cpu_baseline``: the fp64 CPU oracle timed on this host on whole heads of
+  the dense workload, on one thread and on every core;
+* ``w``: every other workload as ``[value, fraction of its roofline]``;
+* ``fp32``: the fp32 configurations (B=2 H=4 N=64 D=32 and the B=2 H=8 sweep
+  over N x D) in TFLOP/s against the derived FP32 SIMT peak;
 * ``clocks``: SM clocks and throttle reasons sampled during the timed region.
 
-``--impl reference`` times the CPU oracle instead (rank 0 only).  Under
-torchrun every rank runs its own replica of the workload (weak scaling, no
-collective on the data path); timing is the maximum over ranks.
+``--details PATH`` also writes every workload's full record (descriptions,
+step times, peaks) as JSON to PATH.  ``--impl reference`` times the CPU oracle
+instead (rank 0 only).  Under torchrun every rank runs its own replica of the
+workload (weak scaling, no collective on the data path); timing is the maximum
+over ranks.
 """
 from __future__ import annotations
 
@@ -44,13 +51,21 @@ METRIC = "attn-fwd TFLOP/s & % of BF16 tensor peak; split-KV decode HBM GB/s"
 MAIN = dict(B=1, Hq=32, Hkv=32, N=8192, D=128, causal=False)
 CAUSAL = dict(B=4, Hq=32, Hkv=8, N=4096, D=128, causal=True)
 DECODE = dict(B=64, Hq=32, Hkv=8, D=128, nk_lo=512, nk_hi=32768, chunk=512)
-DECODE_NAMES = ("decode", "paged", "decode_fp8")
+DECODE_NAMES = ("decode", "paged", "decode_fp8", "decode_mqa", "decode_d64")
+# widened decode workloads: multi-query (32 query heads on one KV head) and head dimension 64
+DECODE_MQA = dict(DECODE, B=128, Hkv=1)
+DECODE_D64 = dict(DECODE, D=64)
 FP32 = dict(B=2, Hq=8, Hkv=8, N=4096, D=128, causal=False)
 # widened prefill workloads: sliding window, chunked prefill (Nq < Nk), head dim 64
 WINDOW = dict(B=1, Hq=32, Hkv=8, Nq=16384, Nk=16384, D=128, causal=True, window=4096)
 CHUNKED = dict(B=1, Hq=32, Hkv=8, Nq=2048, Nk=16384, D=128, causal=True, window=0)
 DENSE64 = dict(B=1, Hq=32, Hkv=32, N=8192, D=64, causal=False)
 VARLEN = dict(B=32, Hq=32, Hkv=8, D=128, n_lo=512, n_hi=8192, causal=True)
+# fp32 configurations: B=2 H=4 N=64 D=32, then the B=2 H=8 sweep over N x D
+FP32_POINTS = [(2, 4, 64, 32)] + [(2, 8, n, d) for n in (64, 256, 1024, 4096) for d in (32, 64, 128)]
+SHORT = {"paged": "paged_dec", "decode_fp8": "fp8kv_dec", "decode_mqa": "mqa_dec", "decode_d64": "d64_dec", "window": "window4k", "chunked": "chunked",
+         "d64": "d64", "fp16": "fp16", "varlen": "varlen", "softcap": "softcap", "bwd": "bwd",
+         "fp32": "fp32", "dense": "dense"}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FP32_SIMT_FLOP_PER_CLK_SM = 256.0   # 128 FP32 lanes x 2 (fused multiply-add)
 GB300_SMS = 152
@@ -85,13 +100,16 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--workload", choices=["dense", "causal", "decode", "fp32", "window", "chunked", "d64",
-                                           "paged", "fp16", "varlen", "decode_fp8", "softcap", "bwd"],
+                                           "paged", "fp16", "varlen", "decode_fp8", "softcap", "bwd",
+                                           "decode_mqa", "decode_d64"],
                     default="dense",
                     help="workload of the timed loop (default: the dense bf16 prefill)")
     ap.add_argument("--no-extras", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffers) measurement")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-oracle sample budget")
-    ap.add_argument("--decode-batch", type=int, default=DECODE["B"],
+    ap.add_argument("--details", default=None, help="also write every workload's full record to this JSON file")
+    ap.add_argument("--cpu-worker", type=int, default=0, help=argparse.SUPPRESS)
+    ap.add_argument("--decode-batch", type=int, default=None,
                     help="sequences in the decode workload (smaller for profiler captures)")
     return ap.parse_args()
 
@@ -194,64 +212,138 @@ def time_steps(torch, fn, steps, warmup, flush, stream):
     return [s.elapsed_time(e) for s, e in zip(starts, ends)]
 
 
-def cpu_oracle_sample(budget_s, seed=0):
-    """fp64 oracle on whole heads of the dense workload until ``budget_s`` elapses."""
-    import numpy as np  # noqa: F401
+MAIN_CONFIG = {"workload": "bf16 dense prefill B=1 H=32 N=8192 D=128 (non-causal)", "global_batch": 1,
+               "seq_len": MAIN["N"], "parallelism": "single"}
+
+
+def host_cores():
+    return len(os.sched_getaffinity(0))
+
+
+def cpu_oracle_heads(threads, budget_s, seed=0):
+    """Whole heads of the dense workload through the fp64 oracle on ``threads`` threads.
+
+    Heads are handed out one at a time until ``budget_s`` has elapsed (heads in
+    flight finish).  Input generation is not timed.  Returns (heads, seconds).
+    Run in a process whose BLAS is limited to one thread (``--cpu-worker``), so
+    that ``threads`` is the number of cores actually used.
+    """
+    import threading
+    from concurrent.futures import ThreadPoolExecutor
     import oracle
     from softmax_attention_attn_gb300 import inputs
     q, k, v = inputs.prefill_inputs(1, MAIN["Hq"], MAIN["Hkv"], MAIN["N"], MAIN["N"], MAIN["D"], "bf16", seed)
     scale = 1 / math.sqrt(MAIN["D"])
-    heads, t0 = 0, time.perf_counter()
-    while heads < MAIN["Hq"] and (time.perf_counter() - t0) < budget_s:
-        h = heads
-        oracle.attention_forward(q[:, h:h + 1], k[:, h:h + 1], v[:, h:h + 1], scale)
-        heads += 1
-    dt = time.perf_counter() - t0
-    f = flops(1, heads, MAIN["N"], MAIN["D"], False)
-    return {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": len(os.sched_getaffinity(0)),
-            "kind": "oracle",
-            "sample": f"{heads} of 32 heads of the dense workload (B=1 N=8192 D=128), fp64 numpy, "
-                      f"{dt:.1f} s; matmul on numpy's BLAS threads, the rest single-threaded"}
+    lock = threading.Lock()
+    state = {"next": 0, "done": 0}
+    t0 = time.perf_counter()
+
+    def worker():
+        while True:
+            with lock:
+                h = state["next"]
+                if h >= MAIN["Hq"] or time.perf_counter() - t0 >= budget_s:
+                    return
+                state["next"] = h + 1
+            oracle.attention_forward(q[:, h:h + 1], k[:, h:h + 1], v[:, h:h + 1], scale)
+            with lock:
+                state["done"] += 1
+
+    with ThreadPoolExecutor(threads) as ex:
+        for f in [ex.submit(worker) for _ in range(threads)]:
+            f.result()
+    return state["done"], time.perf_counter() - t0
+
+
+def cpu_worker_main(threads, budget_s):
+    """``bench.py --cpu-worker N``: print one JSON object with the oracle's heads and seconds."""
+    heads, dt = cpu_oracle_heads(threads, budget_s)
+    print(json.dumps({"threads": threads, "heads": heads, "seconds": dt}), flush=True)
+
+
+def cpu_oracle_run(threads, budget_s):
+    """The oracle on ``threads`` threads in a child process with one BLAS thread per call."""
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    for key in ("RANK", "WORLD_SIZE", "LOCAL_RANK"):
+        env.pop(key, None)
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-worker", str(threads),
+                        "--cpu-seconds", str(budget_s)], capture_output=True, text=True, env=env,
+                       timeout=budget_s * 6 + 300)
+    if r.returncode != 0:
+        raise RuntimeError(f"CPU oracle worker failed: {r.stderr[-2000:]}")
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def cpu_baseline(budget_s):
+    """fp64 oracle on whole heads of the dense workload: one thread, then every core."""
+    f_head = flops(1, 1, MAIN["N"], MAIN["D"], False)
+    n = host_cores()
+    one = cpu_oracle_run(1, budget_s)
+    alln = cpu_oracle_run(n, budget_s)
+    v1 = one["heads"] * f_head / one["seconds"] / 1e12
+    vn = alln["heads"] * f_head / alln["seconds"] / 1e12
+    return {"value": sig(vn), "unit": "TFLOP/s", "cores": n, "kind": "oracle", "value_1_core": sig(v1),
+            "sample": f"fp64 oracle, whole heads of the dense workload: {alln['heads']} heads in "
+                      f"{alln['seconds']:.1f} s on {n} threads, {one['heads']} in {one['seconds']:.1f} s on 1"}
+
+
+def sig(x, n=4):
+    """``x`` rounded to ``n`` significant digits (None stays None)."""
+    if x is None or not math.isfinite(x) or x == 0:
+        return x
+    return round(x, n - 1 - int(math.floor(math.log10(abs(x)))))
 
 
 # ------------------------------------------------------------------ reference arm
 def run_reference(args, rank, world):
-    """The CPU oracle, as it stands, on a bounded sample of the dense workload per step."""
+    """The CPU oracle, as it stands, on a bounded sample of the dense workload per step.
+
+    A step is R query rows (against all 8192 keys) of one head, split over every
+    core in blocks of 256 rows; R is set from one calibration step so that the
+    whole run takes about a minute.
+    """
     if rank != 0:
         return
+    os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
     import numpy as np
+    from concurrent.futures import ThreadPoolExecutor
     import oracle
     from softmax_attention_attn_gb300 import inputs
     q, k, v = inputs.prefill_inputs(1, MAIN["Hq"], MAIN["Hkv"], MAIN["N"], MAIN["N"], MAIN["D"], "bf16", 0)
-    # input preparation (untimed): the oracle's fp64 view of the bf16 values
-    q64, k64, v64 = (x.to(dtype=__import__("torch").float64).numpy() for x in (q, k, v))
     scale = 1 / math.sqrt(MAIN["D"])
-    rows_per_step = 64
+    n = host_cores()
+    blk = 256
     rng = np.random.default_rng(0)
+    ex = ThreadPoolExecutor(n)
 
-    def step():
+    def step(rows):
         h = int(rng.integers(MAIN["Hq"]))
-        i0 = int(rng.integers(0, MAIN["N"] - rows_per_step))
-        oracle.attention_forward(q64[:, h:h + 1, i0:i0 + rows_per_step], k64[:, h:h + 1], v64[:, h:h + 1], scale)
+        i0 = int(rng.integers(0, MAIN["N"] - rows + 1))
+        parts = [(i, min(i + blk, i0 + rows)) for i in range(i0, i0 + rows, blk)]
+        list(ex.map(lambda p: oracle.attention_forward(q[:, h:h + 1, p[0]:p[1]], k[:, h:h + 1],
+                                                       v[:, h:h + 1], scale), parts))
 
+    t0 = time.perf_counter()
+    step(n * blk)
+    per_row = (time.perf_counter() - t0) / (n * blk)
+    target = min(2.0, 60.0 / (args.steps + args.warmup))
+    rows = int(max(blk, min(MAIN["N"], target / per_row)) // blk * blk)
     for _ in range(args.warmup):
-        step()
+        step(rows)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        step()
+        step(rows)
     dt = time.perf_counter() - t0
-    f = 4.0 * rows_per_step * MAIN["N"] * MAIN["D"] * args.steps
-    value = f / dt / 1e12
-    sample = (f"{rows_per_step} query rows x all 8192 keys of one head of the dense workload "
-              "(B=1 H=32 N=8192 D=128) per step, fp64 numpy oracle; matmul on numpy's BLAS threads")
+    ex.shutdown()
+    f = 4.0 * rows * MAIN["N"] * MAIN["D"] * args.steps
+    value = sig(f / dt / 1e12)
+    sample = (f"{rows} query rows x all 8192 keys of one head of the dense workload per step, fp64 oracle "
+              f"on {n} threads (blocks of {blk} rows, one BLAS thread each)")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": sig(dt / args.steps * 1e3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic",
-            "config": {"workload": "bf16 dense prefill B=1 H=32 N=8192 D=128 (oracle on sampled rows)",
-                       "global_batch": 1, "seq_len": MAIN["N"], "parallelism": "single"},
-            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": len(os.sched_getaffinity(0)),
-                             "kind": "oracle", "sample": sample},
+            "data": "synthetic", "config": dict(MAIN_CONFIG),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": n, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
     print(json.dumps(line), flush=True)
@@ -272,6 +364,8 @@ WORKLOAD_NAMES = {
     "decode_fp8": "split-KV decode on an fp8 E4M3 KV cache (bf16 Q) B=64 Hq=32 Hkv=8 D=128, Nk_b~U[512,32768], "
                   "chunk 512",
     "softcap": "bf16 dense prefill B=1 H=32 N=8192 D=128 with softcap 50 and per-head attention sinks",
+    "decode_mqa": "bf16 multi-query split-KV decode B=128 Hq=32 Hkv=1 D=128, Nk_b~U[512,32768], chunk 512",
+    "decode_d64": "bf16 split-KV decode B=64 Hq=32 Hkv=8 D=64, Nk_b~U[512,32768], chunk 512",
     "bwd": "bf16 backward (dQ, dK, dV) B=1 H=32 N=8192 D=128 (non-causal); FLOPs = 2.5 x forward",
 }
 
@@ -353,13 +447,14 @@ def make_workload(name, dev, seed, peaks, peak_src, sm_max_mhz, decode_batch=Non
         w["e2e_in"] = [(x, t) for x, t in zip(host, (q, k, v))]
         w["e2e_out"] = [o, lse]
     else:
-        d = dict(DECODE, B=decode_batch or DECODE["B"])
-        w["desc"] = WORKLOAD_NAMES[name].replace("B=64", f"B={d['B']}")
+        base = {"decode_mqa": DECODE_MQA, "decode_d64": DECODE_D64}.get(name, DECODE)
+        d = dict(base, B=decode_batch) if decode_batch else dict(base)
+        w["desc"] = WORKLOAD_NAMES[name].replace(f"B={base['B']}", f"B={d['B']}")
         ws = torch.empty(binding.attn_decode_workspace_size(d["B"], d["Hq"], d["D"], d["nk_hi"], d["chunk"]),
                          device=dev, dtype=torch.uint8)
         o = torch.empty(d["B"], d["Hq"], d["D"], device=dev, dtype=torch.bfloat16)
         lse = torch.empty(d["B"], d["Hq"], device=dev)
-        if name == "decode":
+        if name in ("decode", "decode_mqa", "decode_d64"):
             qh, kc, vc, sl = inputs.decode_inputs(d["B"], d["Hq"], d["Hkv"], d["D"], d["nk_lo"], d["nk_hi"],
                                                   seed=seed, device=dev)
             q, sl_d = qh.to(dev), sl.to(dev)
@@ -412,6 +507,19 @@ def make_workload(name, dev, seed, peaks, peak_src, sm_max_mhz, decode_batch=Non
     return w
 
 
+def make_fp32_point(dev, seed, B, H, N, D, sm_max_mhz):
+    """One fp32 configuration (dense, non-causal, Hq = Hkv = H) resident on ``dev``."""
+    import torch
+    from softmax_attention_attn_gb300 import binding, inputs
+    q, k, v = (x.to(dev) for x in inputs.prefill_inputs(B, H, H, N, N, D, "fp32", seed))
+    o = torch.empty_like(q)
+    lse = torch.empty(B, H, N, device=dev, dtype=torch.float32)
+    return {"desc": f"fp32 dense prefill B={B} H={H} N={N} D={D}",
+            "fn": lambda: binding.attn_fwd_fp32(q, k, v, o, lse), "work": flops(B, H, N, D, False),
+            "unit": "TFLOP/s", "peak": GB300_SMS * FP32_SIMT_FLOP_PER_CLK_SM * sm_max_mhz * 1e6 / 1e12,
+            "peak_source": f"152 SMs x 256 FP32 FLOP/clk x {sm_max_mhz:.0f} MHz"}
+
+
 def max_over_ranks_of(x, world, device):
     """Maximum of a per-rank float over all ranks (the step time of the slowest rank)."""
     if world == 1:
@@ -426,6 +534,60 @@ def max_over_ranks_of(x, world, device):
 def rate(w, ms):
     scale = 1e12 if w["unit"] == "TFLOP/s" else 1e9
     return w["work"] / (ms * 1e-3) / scale
+
+
+def build_line(args, world, main, main_work_desc, value, ms_step, ms_median, ms_min, achieved, traffic, e2e,
+               clocks, workloads, cpu, launch_floor, wall_s):
+    """The short stdout JSON line and the full details record of a GB300-arm run."""
+    details = {
+        "main": {"workload": main_work_desc, "ms_per_step": ms_step, "ms_per_step_median": ms_median,
+                 "ms_per_step_min": ms_min, "peak_source": main["peak_source"]},
+        "wall_s_timed_region": wall_s, "launch_floor": launch_floor, "e2e": e2e, "workloads": workloads,
+        "cpu_baseline": cpu, "clocks": clocks,
+    }
+    line = {
+        "metric": METRIC, "value": sig(value), "unit": main["unit"], "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": sig(ms_step), "ms_med": sig(ms_median), "ms_min": sig(ms_min),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": main["dtype"],
+        "data": "synthetic", "gpu_launches": args.steps * main["launches"],
+        "config": dict(MAIN_CONFIG, global_batch=world * main["batch"],
+                       parallelism="replicas" if world > 1 else "single")
+        if main["name"] == "dense" else {"workload": main_work_desc, "global_batch": world * main["batch"],
+                                         "seq_len": main["seq_len"],
+                                         "parallelism": "replicas" if world > 1 else "single"},
+        "timing": "CUDA events per step; L2 flushed (256 MiB write) before every step",
+        "roofline": {"bound": main["bound"], "achieved": sig(achieved), "peak": main["peak"], "unit": main["unit"],
+                     "frac": sig(achieved / main["peak"]), "traffic": traffic,
+                     "peak_source": main["peak_source"]},
+    }
+    if "decode" in workloads:
+        d = workloads["decode"]
+        line["decode"] = {"GB/s": sig(d["value"]), "frac": sig(d["frac"]), "split_GB/s": sig(d["splitkv_kernel_gbs"]),
+                          "split_frac": sig(d["splitkv_frac"]), "peak_GB/s": d["peak"],
+                          "workload": "bf16 split-KV decode B=64 Hq=32 Hkv=8 D=128 Nk~U[512,32768] chunk 512"}
+    if "causal" in workloads:
+        c = workloads["causal"]
+        line["causal"] = {"TFLOP/s": sig(c["value"]), "frac": sig(c["frac"]),
+                          "workload": "bf16 causal GQA B=4 Hq=32 Hkv=8 N=4096 D=128"}
+    if e2e is not None:
+        line["e2e"] = {"value": sig(e2e["value"]), "unit": e2e["unit"], "h2d_bytes_per_step": e2e["h2d_bytes_per_step"],
+                       "d2h_bytes_per_step": e2e["d2h_bytes_per_step"], "ms_per_step": sig(e2e["ms_per_step"]),
+                       "pipelined": e2e["pipelined"]}
+        if "serial_value" in e2e:
+            line["e2e"]["serial_value"] = sig(e2e["serial_value"])
+    line["clocks"] = None if clocks is None else {k: (sig(v) if isinstance(v, float) else v) for k, v in clocks.items()}
+    line["cpu_baseline"] = cpu
+    line["w"] = {SHORT.get(n, n): [sig(e["value"]), sig(e["frac"])] for n, e in workloads.items()
+                 if n not in ("decode", "causal") and not n.startswith("fp32_B")}
+    for n in ("paged", "decode_fp8", "decode_mqa", "decode_d64"):
+        if n in workloads:
+            line["w"][SHORT[n]].append(sig(workloads[n]["splitkv_frac"]))
+    fp32 = {n[5:].replace("_", ""): [sig(e["value"]), sig(e["frac"])] for n, e in workloads.items()
+            if n.startswith("fp32_B")}
+    if fp32:
+        line["fp32"] = fp32
+    line["keys"] = "w/fp32: [value, frac of roofline(, split-kernel frac)]; units: TFLOP/s, decode GB/s"
+    return details, line
 
 
 def run_gb300(args, rank, world, local_rank):
@@ -598,8 +760,8 @@ def run_gb300(args, rank, world, local_rank):
     workloads = {}
     if not args.no_extras:
         xs = max(5, min(args.steps // 10, 50))
-        for name in ("dense", "causal", "decode", "paged", "decode_fp8", "fp32", "window", "chunked", "d64", "fp16",
-                     "varlen", "softcap", "bwd"):
+        for name in ("dense", "causal", "decode", "paged", "decode_fp8", "decode_mqa", "decode_d64", "window",
+                     "chunked", "d64", "fp16", "varlen", "softcap", "bwd"):
             if name == args.workload:
                 continue
             x = make_workload(name, dev, rank, peaks, peak_src, sm_max, args.decode_batch)
@@ -615,33 +777,30 @@ def run_gb300(args, rank, world, local_rank):
             workloads[name] = entry
             del x
             torch.cuda.empty_cache()
+        # the fp32 configurations: B=2 H=4 N=64 D=32 and the B=2 H=8 sweep over N x D
+        for (B, H, N, D) in FP32_POINTS:
+            x = make_fp32_point(dev, rank, B, H, N, D, sm_max)
+            mx = max_over_ranks(statistics.mean(time_steps(torch, x["fn"], xs, 3, flush, stream)))
+            r = rate(x, mx)
+            workloads[f"fp32_B{B}_H{H}_N{N}_D{D}"] = {
+                "workload": x["desc"], "value": world * r, "unit": "TFLOP/s", "ms_per_step": mx, "bound": "alu",
+                "frac": r / x["peak"], "peak": x["peak"], "peak_source": x["peak_source"]}
+            del x
+        torch.cuda.empty_cache()
         if binding.get_device_error() != 0:
             raise RuntimeError("device error word set by a secondary workload")
 
     cpu = None
     if rank == 0 and world == 1 and args.cpu_seconds > 0:
-        cpu = cpu_oracle_sample(args.cpu_seconds)
+        cpu = cpu_baseline(args.cpu_seconds)
 
-    line = {
-        "metric": METRIC, "value": value, "unit": main["unit"], "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_step, "ms_per_step_median": ms_median, "ms_per_step_min": ms_min,
-        "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": main["dtype"], "data": "synthetic",
-        "config": {"workload": main_work_desc, "global_batch": world * main["batch"], "seq_len": main["seq_len"],
-                   "parallelism": "replicas" if world > 1 else "single",
-                   "l2": "flushed (256 MiB write) before every step", "timing": "CUDA events per step"},
-        "roofline": {"bound": main["bound"], "achieved": achieved, "peak": main["peak"], "unit": main["unit"],
-                     "frac": achieved / main["peak"], "traffic": traffic, "peak_source": main["peak_source"]},
-        "e2e": e2e,
-        "gpu_launches": args.steps * main["launches"],
-        "wall_s_timed_region": wall1 - wall0,
-        "launch_floor": launch_floor,
-        "clocks": clocks,
-        "workloads": workloads,
-        "cpu_baseline": cpu,
-    }
+    details, line = build_line(args, world, main, main_work_desc, value, ms_step, ms_median, ms_min,
+                               achieved, traffic, e2e, clocks, workloads, cpu, launch_floor, wall1 - wall0)
+    if args.details:
+        with open(args.details, "w") as f:
+            json.dump({"line": line, "details": details}, f, indent=1)
     if rank == 0:
-        print(json.dumps(line), flush=True)
+        print(json.dumps(line, separators=(",", ":")), flush=True)
 
 
 def main():
@@ -649,6 +808,9 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.cpu_worker > 0:      # child process of cpu_baseline(): the oracle on N threads
+        cpu_worker_main(args.cpu_worker, args.cpu_seconds)
+        return
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
     if args.impl == "reference":
