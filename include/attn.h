@@ -167,8 +167,11 @@ size_t attn_decode_workspace_size(int B, int Hq, int D, int Nk_max, int chunk);
  *              (keys c*chunk .. min((c+1)*chunk, seqlens[b]) - 1) it receives the
  *              chunk's normalised output O_c and its LSE_c; other entries are
  *              left untouched.
- *   D must be 128; Hq / Hkv must be 1, 2, 4 or 8; chunk must be a multiple of
- *   64 in [64, 1024].  A seqlens[b] outside [1, Nk_max] sets ATTN_ERR_SEQLEN in
+ *   D must be 64 or 128; Hq / Hkv must be 1, 2, 4, 8, 16 or 32 (32 with Hkv = 1
+ *   is multi-query decode); chunk must be a multiple of 64 in [64, 1024].  The
+ *   chunk's scores for all query heads of a KV head are held in shared memory,
+ *   so a combination whose shared memory would exceed the per-block limit
+ *   returns ATTN_ERR_CAPACITY (D = 128, Hq / Hkv = 32 fits every chunk size).  A seqlens[b] outside [1, Nk_max] sets ATTN_ERR_SEQLEN in
  *   the device error word and that sequence is skipped.
  *   Errors: ATTN_ERR_NULL, _DIM, _GQA, _HEAD_DIM, _ALIGN, _SCALE, _CHUNK,
  *   _DEVICE, _CUDA.
@@ -269,8 +272,9 @@ int attn_decode_splitkv_paged_fp8(const void* q, const void* k_pages, const void
                                   int chunk, attn_stream_t stream);
 
 /*
- * attn_decode_combine — split-KV decode, combine step.  LSE-weighted merge of
- * the chunk results written by attn_decode_splitkv:
+ * attn_decode_combine — split-KV decode, combine step.   [ASK] "研究动机"
+ * (split-KV decode: the chunks' partial results are merged into one output).
+ * LSE-weighted merge of the chunk results written by attn_decode_splitkv:
  *   M = max_c LSE_c,  w_c = exp(LSE_c - M),  O = sum_c w_c O_c / sum_c w_c,
  *   LSE = M + ln sum_c w_c,   over c < ceil(seqlens[b] / chunk).
  *   o : bf16 [B, Hq, D] (out)        lse : fp32 [B, Hq] (out; may be NULL)
@@ -296,11 +300,16 @@ int attn_decode_combine(const void* workspace, const int* seqlens, void* o, floa
  *   loads this part of the library keeps it until the process exits.  Sizes
  *   needing more scratch than that, i.e.
  *   attn_decode_workspace_size(B, Hq, D, Nk_max, chunk) > 16 MiB, are rejected
- *   with ATTN_ERR_CAPACITY before anything is queued (this capacity check comes
- *   before the other argument checks).
+ *   with ATTN_ERR_CAPACITY before anything is queued.  Checks run in this
+ *   order: NULL pointers (ATTN_ERR_NULL), sizes for which no workspace size
+ *   exists (ATTN_ERR_DIM), the capacity (ATTN_ERR_CAPACITY), then the checks
+ *   of attn_decode_splitkv and attn_decode_combine.
  *   The first call on a device looks up the scratch array's device address
- *   (cudaGetSymbolAddress, once per device): make that first call before any
- *   stream capture.  All calls share the one array, so calls whose kernels
+ *   (cudaGetSymbolAddress, once per device) and keeps it for the rest of the
+ *   process: make that first call before any stream capture, and do not call
+ *   this entry point again on a device after cudaDeviceReset() or any other
+ *   teardown of its primary context (the kept address then no longer names
+ *   the scratch array; the library's device error word is cached the same way).  All calls share the one array, so calls whose kernels
  *   overlap on the GPU (different streams without ordering) race and corrupt
  *   each other's results; calls on one stream are ordered and safe.  Nothing in
  *   the scratch needs to start at zero: every entry the combine step reads is

@@ -23,8 +23,6 @@ __device__ int g_device_error;
 
 namespace {
 
-constexpr int kMaxDevices = 64;
-
 struct DeviceInfo {
   bool ready = false;
   int status = ATTN_OK;
@@ -201,8 +199,8 @@ static int check_decode(int B, int Hq, int Hkv, int Nk_max, int D, int chunk) {
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || Nk_max <= 0 || D <= 0 || chunk <= 0) return ATTN_ERR_DIM;
   if (Hq % Hkv != 0) return ATTN_ERR_GQA;
   const int g = Hq / Hkv;
-  if (g != 1 && g != 2 && g != 4 && g != 8) return ATTN_ERR_GQA;
-  if (D != 128) return ATTN_ERR_HEAD_DIM;
+  if (g != 1 && g != 2 && g != 4 && g != 8 && g != 16 && g != 32) return ATTN_ERR_GQA;
+  if (D != 64 && D != 128) return ATTN_ERR_HEAD_DIM;
   if (chunk % 64 != 0 || chunk > 1024) return ATTN_ERR_CHUNK;
   if (B > 4096) return ATTN_ERR_CAPACITY;
   if (static_cast<long long>(B) * Hq > (1ll << 30)) return ATTN_ERR_DIM;
@@ -221,7 +219,7 @@ int attn_decode_splitkv(const void* q, const void* k_cache, const void* v_cache,
   if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_SCALE;
   DeviceInfo* dev = nullptr;
   if ((rc = device_info(&dev)) != ATTN_OK) return rc;
-  return (launch_decode_splitkv(q, k_cache, v_cache, seqlens, workspace, B, Hq, Hkv, Nk_max,
+  return (launch_decode_splitkv(q, k_cache, v_cache, seqlens, workspace, B, Hq, Hkv, Nk_max, D,
                                       scale, chunk, dev->num_sms,
                                       reinterpret_cast<cudaStream_t>(stream), dev->err));
 }
@@ -242,7 +240,7 @@ int attn_decode_splitkv_paged(const void* q, const void* k_pages, const void* v_
   DeviceInfo* dev = nullptr;
   if ((rc = device_info(&dev)) != ATTN_OK) return rc;
   return launch_decode_splitkv_paged(q, k_pages, v_pages, block_table, seqlens, workspace, B, Hq,
-                                     Hkv, num_pages, page_size, max_pages, scale, chunk,
+                                     Hkv, num_pages, page_size, max_pages, D, scale, chunk,
                                      dev->num_sms, reinterpret_cast<cudaStream_t>(stream), dev->err);
 }
 
@@ -287,7 +285,7 @@ int attn_decode_splitkv_fp8(const void* q, const void* k_cache, const void* v_ca
     return ATTN_ERR_SCALE;
   DeviceInfo* dev = nullptr;
   if ((rc = device_info(&dev)) != ATTN_OK) return rc;
-  return launch_decode_splitkv(q, k_cache, v_cache, seqlens, workspace, B, Hq, Hkv, Nk_max, scale,
+  return launch_decode_splitkv(q, k_cache, v_cache, seqlens, workspace, B, Hq, Hkv, Nk_max, D, scale,
                                chunk, dev->num_sms, reinterpret_cast<cudaStream_t>(stream), dev->err,
                                1, k_scale, v_scale);
 }
@@ -311,7 +309,7 @@ int attn_decode_splitkv_paged_fp8(const void* q, const void* k_pages, const void
   DeviceInfo* dev = nullptr;
   if ((rc = device_info(&dev)) != ATTN_OK) return rc;
   return launch_decode_splitkv_paged(q, k_pages, v_pages, block_table, seqlens, workspace, B, Hq,
-                                     Hkv, num_pages, page_size, max_pages, scale, chunk,
+                                     Hkv, num_pages, page_size, max_pages, D, scale, chunk,
                                      dev->num_sms, reinterpret_cast<cudaStream_t>(stream), dev->err,
                                      1, k_scale, v_scale);
 }
@@ -325,7 +323,7 @@ int attn_decode_combine(const void* workspace, const int* seqlens, void* o, floa
     return ATTN_ERR_ALIGN;
   DeviceInfo* dev = nullptr;
   if ((rc = device_info(&dev)) != ATTN_OK) return rc;
-  return (launch_decode_combine(workspace, seqlens, o, lse, B, Hq, Nk_max, chunk,
+  return (launch_decode_combine(workspace, seqlens, o, lse, B, Hq, Nk_max, D, chunk,
                                       reinterpret_cast<cudaStream_t>(stream), dev->err));
 }
 

@@ -559,15 +559,8 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
       !encode_tiled_3d(&tdq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dq, HD, Nq, static_cast<uint64_t>(B) * Hq, 4, box_dq,
                        CU_TENSOR_MAP_SWIZZLE_128B))
     return ATTN_ERR_CUDA;
-  static int attr_dev = -1;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (attr_dev != dev) {
-    if (cudaFuncSetAttribute(attn_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC) !=
-        cudaSuccess)
-      return ATTN_ERR_CUDA;
-    attr_dev = dev;
-  }
+  static KernelSetup setup;
+  if (const int rc = prepare_kernel(setup, attn_bwd_kernel, SMEM_ALLOC); rc != ATTN_OK) return rc;
   BwdParams prm;
   prm.nlse2 = nlse2;
   prm.ndelta = ndelta;

@@ -7,22 +7,19 @@
 // restricted to the chunk's keys.  Chunks cover keys [c*chunk, (c+1)*chunk) of
 // each sequence; the combine step weights chunk c by exp(LSE_c - max LSE).
 //
-// The partial step is bound by HBM bandwidth (about 2 flops per byte), so it
-// uses no tensor cores.  Design:
+// The partial step should be bound by HBM bandwidth.  Two consumers serve it:
+//
+// SIMT consumer (bf16 cache, head dimension 128, up to 8 query heads per KV
+// head: about 2-8 FLOP per byte, within what the FP32 pipes do at HBM speed):
 //   * persistent CTAs walk a work list of (sequence b, chunk c, KV head) items,
 //     built in shared memory from the device-side sequence lengths (no host
 //     round trip); the KV heads of one chunk are adjacent items, so
 //     neighbouring CTAs read neighbouring 256-byte rows of the cache;
 //   * one producer thread streams 64-key K and V tiles ([64 keys][128] bf16,
-//     16 KB, through a 3-slot TMA ring; or [64 keys][128] fp8 E4M3 codes,
-//     8 KB, through a 6-slot ring), so 48 KB per CTA and, with three CTAs per
-//     SM, 144 KB per SM are in flight (three CTAs rather than two with larger
-//     rings: the consumers, not the copies, set the pace, and more resident
-//     warps hide their latencies better);
-//   * an fp8 cache holds E4M3 codes whose values are code * k_scale (K) and
-//     code * v_scale (V): codes convert exactly to fp32 (through f16, which
-//     holds every E4M3 value), k_scale folds into the softmax scale and v_scale
-//     scales each chunk's output;
+//     16 KB) through a 3-slot TMA ring, so 48 KB per CTA and, with three CTAs
+//     per SM, 144 KB per SM are in flight (three CTAs rather than two with
+//     larger rings: the consumers, not the copies, set the pace, and more
+//     resident warps hide their latencies better);
 //   * four consumer warps: all G = Hq/Hkv query heads of the KV head share
 //     each K/V tile.  For the scores, a thread multiplies 16 bytes of 8 key
 //     rows by the G query slices it holds in registers and a 16-lane
@@ -30,6 +27,10 @@
 //     one shuffle per score.  The chunk's softmax runs in shared memory in the
 //     exp2 domain; P V accumulates per thread and is reduced across the eight
 //     key groups through shared memory.
+//
+// Tensor-core consumer (fp8 E4M3 cache, head dimension 64, 16 or 32 query heads
+// per KV head): the same work list, producer and chunk softmax, with the two
+// products on warp-level MMAs; see the section "tensor-core partial step".
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <math_constants.h>
@@ -44,15 +45,13 @@ constexpr int HD = 128;
 constexpr int TILE = 64;                      // keys per TMA tile
 constexpr int MAX_STAGES = 10;
 
-// Residency and ring geometry for a bf16 (KV8 = false) or fp8 E4M3 (KV8 = true)
-// cache: three CTAs per SM with 48 KB rings (144 KB in flight per SM); four with
-// 32 KB rings (128 KB) for the fp8 cache with up to four query heads per KV
-// head, whose consumers need the extra warps most and fit in the registers.
-template <int G, bool KV8>
+// Residency and ring geometry of the SIMT consumer (bf16 cache): three CTAs per
+// SM with 48 KB rings (144 KB in flight per SM).
+template <int G>
 struct Ring {
-  static constexpr int CTAS_PER_SM = (KV8 && G <= 4) ? 4 : 3;
-  static constexpr int RING_BYTES = (CTAS_PER_SM == 4 ? 2 : 3) * TILE * HD * 2;
-  static constexpr int ROW_BYTES = KV8 ? HD : 2 * HD;  // one key row of one KV head
+  static constexpr int CTAS_PER_SM = 3;
+  static constexpr int RING_BYTES = 3 * TILE * HD * 2;
+  static constexpr int ROW_BYTES = 2 * HD;             // one key row of one KV head
   static constexpr int TILE_BYTES = TILE * ROW_BYTES;
   static constexpr int STAGES = RING_BYTES / TILE_BYTES;
   static_assert(STAGES <= MAX_STAGES, "ring slots");
@@ -111,48 +110,21 @@ __device__ __forceinline__ void bf16x8_to_float(const uint4& u, float (&f)[8]) {
   }
 }
 
-// Eight E4M3 codes (the bytes of u, lowest first) to fp32.  Every E4M3 value
-// is exact in f16, so the conversion is exact.
-__device__ __forceinline__ void e4m3x8_to_float(const uint2& u, float (&f)[8]) {
-  const uint32_t w[2] = {u.x, u.y};
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    uint32_t h01, h23;
-    asm("{\n\t.reg .b16 lo, hi;\n\t"
-        "mov.b32 {lo, hi}, %2;\n\t"
-        "cvt.rn.f16x2.e4m3x2 %0, lo;\n\t"
-        "cvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
-        : "=r"(h01), "=r"(h23)
-        : "r"(w[i]));
-    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&h01));
-    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&h23));
-    f[4 * i + 0] = a.x;
-    f[4 * i + 1] = a.y;
-    f[4 * i + 2] = b.x;
-    f[4 * i + 3] = b.y;
-  }
-}
-
 // The 8 elements [g16 * 8, g16 * 8 + 8) of key row `key` of a ring tile, as fp32.
-template <bool KV8>
 __device__ __forceinline__ void row_slice(const uint8_t* tile, int key, int g16, float (&f)[8]) {
-  if constexpr (KV8) {
-    e4m3x8_to_float(*reinterpret_cast<const uint2*>(tile + key * HD + g16 * 8), f);
-  } else {
-    bf16x8_to_float(*reinterpret_cast<const uint4*>(tile + key * (HD * 2) + g16 * 16), f);
-  }
+  bf16x8_to_float(*reinterpret_cast<const uint4*>(tile + key * (HD * 2) + g16 * 16), f);
 }
 
 // acc[h][e] += sum over the 8 keys (ksub + 8 i) of one 64-key tile of
 // p[h][key] * v[key][g16 * 8 + e].  With MASK, keys >= valid contribute 0.
-template <int G, bool MASK, bool KV8>
+template <int G, bool MASK>
 __device__ __forceinline__ void pv_tile(float (&acc)[G][8], const uint8_t* tile, const float* pt,
                                         int chunk, int ksub, int g16, int valid) {
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int key = ksub + 8 * i;
     float vf[8];
-    row_slice<KV8>(tile, key, g16, vf);
+    row_slice(tile, key, g16, vf);
     if (MASK && key >= valid) {
 #pragma unroll
       for (int e = 0; e < 8; ++e) vf[e] = 0.f;
@@ -197,21 +169,21 @@ struct Paging {
   int max_pages, page_size, num_pages;
 };
 
-template <int G, bool PAGED, bool KV8>
-__global__ void __launch_bounds__(NTHREADS, (Ring<G, KV8>::CTAS_PER_SM))
+template <int G, bool PAGED>
+__global__ void __launch_bounds__(NTHREADS, (Ring<G>::CTAS_PER_SM))
 attn_decode_splitkv_kernel(const __grid_constant__ CUtensorMap tm_k,
                            const __grid_constant__ CUtensorMap tm_v,
                            const __nv_bfloat16* __restrict__ q, const int* __restrict__ seqlens,
                            float* __restrict__ ws_o, float* __restrict__ ws_lse, int B, int Hq,
-                           int Hkv, int Nk_max, int chunk, int S_max, float c_log2, float v_scale,
-                           int* err, const Paging pg) {
-  constexpr int STAGES = Ring<G, KV8>::STAGES;
-  constexpr int TILE_BYTES = Ring<G, KV8>::TILE_BYTES;
+                           int Hkv, int Nk_max, int chunk, int S_max, float c_log2, int* err,
+                           const Paging pg) {
+  constexpr int STAGES = Ring<G>::STAGES;
+  constexpr int TILE_BYTES = Ring<G>::TILE_BYTES;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
   const uint32_t sb = smem_u32(smem);
-  const Layout L = layout(G, chunk, B, Ring<G, KV8>::RING_BYTES);
+  const Layout L = layout(G, chunk, B, Ring<G>::RING_BYTES);
   float* work = reinterpret_cast<float*>(smem + L.work);   // scores / p, then reduction buffer
   float* st_m = reinterpret_cast<float*>(smem + L.stats);
   float* st_l = st_m + 8;
@@ -344,7 +316,7 @@ attn_decode_splitkv_kernel(const __grid_constant__ CUtensorMap tm_k,
       for (int i = 0; i < 8; ++i) {
         const int key = ksub + 8 * i;
         float kf[8];
-        row_slice<KV8>(tile, key, g16, kf);
+        row_slice(tile, key, g16, kf);
 #pragma unroll
         for (int h = 0; h < G; ++h) {
           float a = 0.f;
@@ -407,9 +379,9 @@ attn_decode_splitkv_kernel(const __grid_constant__ CUtensorMap tm_k,
       // 0 * NaN from an unused cache row is not).
       const int valid_here = wk.n_valid - tl * TILE;
       if (valid_here >= TILE)
-        pv_tile<G, false, KV8>(acc, tile, pt, chunk, ksub, g16, TILE);
+        pv_tile<G, false>(acc, tile, pt, chunk, ksub, g16, TILE);
       else
-        pv_tile<G, true, KV8>(acc, tile, pt, chunk, ksub, g16, valid_here);
+        pv_tile<G, true>(acc, tile, pt, chunk, ksub, g16, valid_here);
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_empty(s));
     }
@@ -430,7 +402,7 @@ attn_decode_splitkv_kernel(const __grid_constant__ CUtensorMap tm_k,
         float o = 0.f;
 #pragma unroll
         for (int k = 0; k < 8; ++k) o += red[(k * G + h) * HD + d];
-        ws_o[(base + static_cast<size_t>(h) * S_max) * HD + d] = o / st_l[h] * v_scale;
+        ws_o[(base + static_cast<size_t>(h) * S_max) * HD + d] = o / st_l[h];
       }
       if (tid < G) ws_lse[base + static_cast<size_t>(tid) * S_max] = (st_m[tid] + log2f(st_l[tid])) * 0.69314718055994531f;
       if (tid == 0) *stop = *abort_flag;
@@ -440,34 +412,537 @@ attn_decode_splitkv_kernel(const __grid_constant__ CUtensorMap tm_k,
   }
 }
 
-// One warp per (b, h): LSE-weighted merge of the chunk results.
+// ====================================================================== tensor-core partial step
+// The same partial step for an fp8 (E4M3) cache, for head dimension 64, and for
+// 16 or 32 query heads per KV head.  There the SIMT consumers above cannot keep
+// up with HBM: an fp8 byte needs its conversion plus G multiply-adds for Q K and
+// again for P V (about 16 FLOP per byte at G = 4), and G = 16 or 32 query heads
+// per KV head need 16-32 FLOP per byte of a bf16 cache, both above what the FP32
+// pipes deliver per byte of HBM bandwidth.  Both products of a chunk are small
+// dense contractions (G x D x 64 keys per tile), so the consumer warps run them
+// as warp-level tensor-core MMAs (m16n8k16, fp32 accumulation):
+//   * Q K^T: a warp takes 16 keys of a tile; the A operand is the K rows,
+//     read from the 128-byte (64-byte for 64-byte rows) swizzled TMA tile and,
+//     for fp8, converted in registers (cvt.rn.f16x2.e4m3x2, exact: every E4M3
+//     value is an f16 value); the B operand is Q^T in registers (8 query heads per
+//     MMA column block).  Thread (g, c) of a warp supplies the head-dimension
+//     slice [c D/4, (c+1) D/4) in every K step (the sum over d may visit d in
+//     any order, so the MMA's K index is permuted to make that slice contiguous).
+//   * For an fp8 cache the MMAs run on f16 operands: each query head is scaled
+//     by a power of two into f16 range (exact) and its scores are scaled back.
+//   * P V: O^T = V^T P^T; warp w owns the head-dimension rows [w D/4, (w+1) D/4)
+//     and reads V^T fragments from the tile (pairs of keys at one d are gathered
+//     with byte permutes); P is read from the chunk's score rows in shared
+//     memory and rounded to the MMA operand type (f16 for fp8, else bf16).  No
+//     reduction across warps is needed.
+// Keys past a sequence's end get score -inf and V = 0 (an unused cache row may
+// hold NaN, and 0 * NaN is NaN).
+namespace decode_mma {
+
+constexpr int TILE = 64;                 // keys per TMA tile
+constexpr int NCW = 4;                   // consumer warps
+constexpr int NC = NCW * 32;
+constexpr int NTHREADS = NC + 32;        // + producer warp
+constexpr int SPAD = 8;                  // floats of padding per score row (row stride chunk + SPAD)
+constexpr int MAX_STAGES = 16;
+
+template <int HD, bool KV8>
+struct Geo {
+  static constexpr int ESZ = KV8 ? 1 : 2;
+  static constexpr int ROW = HD * ESZ;                  // bytes of one key row of one KV head
+  static constexpr int SROW = ROW > 128 ? 128 : ROW;    // bytes of that row inside one swizzled slab
+  static constexpr int SLABS = ROW / SROW;              // 2 for bf16 D = 128, else 1
+  static constexpr int SLAB_BYTES = TILE * SROW;
+  static constexpr int TILE_BYTES = TILE * ROW;
+};
+
+// Residency: up to 8 query heads per KV head, three CTAs per SM with 48 KB rings;
+// with 16 or 32 the chunk's scores take 32-64 KB (chunk 512), so one CTA per SM
+// runs with as large a ring as the shared memory leaves (up to 16 tiles).
+template <int HD, int G, bool KV8>
+struct Cfg {
+  static constexpr int NT = (G + 7) / 8;                // MMA column blocks of 8 query heads
+  static constexpr int CTAS_PER_SM = G <= 8 ? 3 : 1;
+  static constexpr int SMALL_RING_BYTES = 48 * 1024;    // G <= 8
+};
+
+struct Layout {
+  int work, stats, bars, misc, split, bytes;
+};
+
+__host__ __device__ inline Layout layout(int G, int chunk, int B, int ring_bytes) {
+  Layout L;
+  L.work = ring_bytes;                                  // scores, then p: [G][chunk + SPAD] fp32
+  L.stats = L.work + G * (chunk + SPAD) * 4;
+  L.bars = L.stats + 2 * 32 * 4;                        // m[32], l[32]
+  L.misc = L.bars + 2 * MAX_STAGES * 8;
+  L.split = L.misc + 16;                                // misc: abort flag, stop flag
+  L.bytes = L.split + (B + 1) * 4;
+  return L;
+}
+
+// Byte offset inside a ring tile of byte `b` of key row `row`: the row is split
+// into slabs of SROW bytes, each slab a [64][SROW] block written by one TMA box
+// with the 128-byte (SROW = 128) or 64-byte (SROW = 64) swizzle: the 16-byte
+// chunk index is XORed with row & 7, respectively (row >> 1) & 3.
+template <int HD, bool KV8>
+__device__ __forceinline__ uint32_t tile_off(int row, int b) {
+  using GE = Geo<HD, KV8>;
+  const int slab = b / GE::SROW;
+  const int bb = b % GE::SROW;
+  int ch = bb >> 4;
+  if constexpr (GE::SROW == 128) ch ^= row & 7;
+  else ch ^= (row >> 1) & 3;
+  return static_cast<uint32_t>(slab * GE::SLAB_BYTES + row * GE::SROW + (ch << 4) + (bb & 15));
+}
+
+// Two E4M3 codes (bits 0-15 of `w` if !HI, else bits 16-31) -> f16x2 (exact).
+template <bool HI>
+__device__ __forceinline__ uint32_t e4m3x2_f16x2(uint32_t w) {
+  uint32_t h;
+  if constexpr (HI)
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, hi;\n\t}" : "=r"(h) : "r"(w));
+  else
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, lo;\n\t}" : "=r"(h) : "r"(w));
+  return h;
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
+}
+
+// D (16x8 fp32) += A (16x16) B (16x8): f16 operands if F16, else bf16.
+template <bool F16>
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  if constexpr (F16)
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  else
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+template <int HD, int G, bool PAGED, bool KV8>
+__global__ void __launch_bounds__(NTHREADS, 1)
+attn_decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                       const __nv_bfloat16* __restrict__ q, const int* __restrict__ seqlens,
+                       float* __restrict__ ws_o, float* __restrict__ ws_lse, int B, int Hq, int Hkv,
+                       int Nk_max, int chunk, int S_max, float c_log2, float v_scale, int* err,
+                       const decode::Paging pg, int STAGES) {
+  using GE = Geo<HD, KV8>;
+  using C = Cfg<HD, G, KV8>;
+  constexpr int NT = C::NT;
+  constexpr int TILE_BYTES = GE::TILE_BYTES;
+  constexpr int KK = HD / 16;             // K steps of Q K^T
+  constexpr int DQ = HD / 4;              // head-dimension elements per thread in Q K^T
+  constexpr int QW = DQ / 2;              // 32-bit words of 16-bit values per thread and head
+  constexpr int KW = DQ * GE::ESZ / 4;    // 32-bit words of one K row slice per thread
+  constexpr int MT = HD / 64;             // 16-row blocks of the head dimension per warp in P V
+  constexpr int DV = HD == 128 ? 4 : 2;   // head-dimension elements per thread in P V
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  const uint32_t sb = smem_u32(smem);
+  const Layout L = layout(G, chunk, B, STAGES * TILE_BYTES);
+  const int wstride = chunk + SPAD;
+  float* work = reinterpret_cast<float*>(smem + L.work);
+  float* st_m = reinterpret_cast<float*>(smem + L.stats);
+  float* st_l = st_m + 32;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc);
+  int* split = reinterpret_cast<int*>(smem + L.split);
+  auto bar_full = [&](int s) { return sb + L.bars + 8u * s; };
+  auto bar_empty = [&](int s) { return sb + L.bars + 8u * (STAGES + s); };
+
+  const int warp = warp_id_uniform();
+  const int lane = static_cast<int>(lane_id());
+  const int tid = static_cast<int>(threadIdx.x);
+
+  if (tid == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(bar_full(s), 1);
+      mbar_init(bar_empty(s), NCW);
+    }
+    abort_flag[0] = 0;
+    abort_flag[1] = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  // ---- work list: split[b] = number of chunks of sequences 0..b-1 (one warp)
+  if (warp == 0) {
+    const int per = (B + 31) / 32;
+    const int b0 = min(B, lane * per), b1 = min(B, b0 + per);
+    int local = 0;
+    for (int b = b0; b < b1; ++b) {
+      const int Lb = seqlens[b];
+      if (Lb < 1 || Lb > Nk_max) {
+        atomicCAS(err, 0, ATTN_ERR_SEQLEN);
+        continue;
+      }
+      local += (Lb + chunk - 1) / chunk;
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    int run = incl - local;
+    for (int b = b0; b < b1; ++b) {
+      split[b] = run;
+      const int Lb = seqlens[b];
+      if (Lb >= 1 && Lb <= Nk_max) run += (Lb + chunk - 1) / chunk;
+    }
+    if (lane == 31) split[B] = incl;
+  }
+  __syncthreads();
+  const int total = split[B] * Hkv;
+
+  if (warp == NCW) {
+    // ================================================================ producer
+    if (lane == 0) {
+      int it = 0;
+      int cached_lp = -1, cached_b = -1, cached_page = 0;
+      bool ok = true;
+      for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+        const decode::Work wk = decode::decode_work(w, split, B, Hkv, chunk, seqlens);
+        for (int kv = 0; kv < 2 && ok; ++kv) {
+          const CUtensorMap* m = kv ? &tm_v : &tm_k;
+          for (int tl = 0; tl < wk.ntl; ++tl, ++it) {
+            const int s = it % STAGES, u = it / STAGES;
+            if (u > 0 && !mbar_wait(bar_empty(s), (u - 1) & 1, abort_flag, err)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(bar_full(s), TILE_BYTES);
+            const int key0 = wk.c * chunk + tl * TILE;
+            int row = key0, outer = wk.b;
+            if constexpr (PAGED) {
+              const int lp = key0 / pg.page_size;
+              if (lp != cached_lp || wk.b != cached_b) {  // one block-table read per page
+                cached_page = __ldg(pg.block_table + static_cast<size_t>(wk.b) * pg.max_pages + lp);
+                cached_lp = lp;
+                cached_b = wk.b;
+              }
+              int page = cached_page;
+              if (page < 0 || page >= pg.num_pages) {  // reported; the copy reads zeros instead
+                atomicCAS(err, 0, ATTN_ERR_PAGE);
+                page = pg.num_pages;
+              }
+              row = key0 - lp * pg.page_size;
+              outer = page;
+            }
+#pragma unroll
+            for (int sl = 0; sl < GE::SLABS; ++sl)
+              tma_load_4d(sb + s * TILE_BYTES + sl * GE::SLAB_BYTES, m, bar_full(s), sl * (GE::SROW / GE::ESZ),
+                          wk.kvh, row, outer);
+          }
+        }
+      }
+      if (!ok) {
+        for (int i = max(0, it - STAGES); i < it; ++i) {
+          const unsigned long long t0 = global_ns();
+          while (!mbar_try_wait(bar_full(i % STAGES), (i / STAGES) & 1))
+            if (global_ns() - t0 > kAttnWaitNs) break;
+        }
+      }
+    }
+    return;
+  }
+
+  // ==================================================================== consumers
+  // As in the SIMT consumer: a failed wait never leaves an item early; every
+  // consumer reaches the same named barriers and the stop decision is taken at
+  // the end of the item from one shared copy of the abort flag.
+  volatile int* stop = abort_flag + 1;
+  const int g = lane >> 2;        // MMA row group
+  const int c = lane & 3;         // thread in group
+  int it = 0;
+  for (int w = blockIdx.x; w < total; w += gridDim.x) {
+    const decode::Work wk = decode::decode_work(w, split, B, Hkv, chunk, seqlens);
+    const int h0 = wk.kvh * G;
+    // bf16 D = 128: threads c >= 2 visit the 16-byte chunks of their slice in the
+    // order 2, 3, 0, 1 (for K and, identically, for Q), so that the K loads of
+    // threads c and c + 2, which read different slabs, fall into different banks
+    const int rot = (GE::ROW == 256) ? 2 * (c >> 1) : 0;
+    // ---- Q^T fragments: thread (g, c) holds head 8 nt + g, elements [c DQ, (c+1) DQ)
+    uint32_t qf[NT][QW];
+    float qsc[NT][2];             // fp8 cache: the score scales of heads 8 nt + 2c, + 1
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int h = 8 * nt + g;
+      uint32_t raw[QW];
+      if (h < G) {
+        const uint4* src = reinterpret_cast<const uint4*>(q + (static_cast<size_t>(wk.b) * Hq + h0 + h) * HD + c * DQ);
+#pragma unroll
+        for (int i = 0; i < QW / 4; ++i) {
+          const uint4 u = __ldg(src + (i ^ rot));
+          raw[4 * i + 0] = u.x;
+          raw[4 * i + 1] = u.y;
+          raw[4 * i + 2] = u.z;
+          raw[4 * i + 3] = u.w;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < QW; ++i) raw[i] = 0u;
+      }
+      if constexpr (KV8) {
+        // f16 operands: scale head h by 2^-e with e = floor(log2 max|q_h|) - 14, so that
+        // the largest |q| lies in [2^14, 2^15) (exact: a power of two; bf16 values then
+        // fit f16's 11-bit significand); the head's scores are multiplied by 2^e.
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < QW; ++i)
+          amax = fmax3(amax, fabsf(__uint_as_float(raw[i] << 16)), fabsf(__uint_as_float(raw[i] & 0xFFFF0000u)));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        int e = 0;
+        if (amax > 0.f) e = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFF) - 127 - 14;
+        e = max(-100, min(100, e));
+        const float down = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+        const float up = __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
+#pragma unroll
+        for (int i = 0; i < QW; ++i)
+          qf[nt][i] = pack_f16x2(__uint_as_float(raw[i] << 16) * down, __uint_as_float(raw[i] & 0xFFFF0000u) * down);
+        qsc[nt][0] = __shfl_sync(0xffffffffu, up, 8 * c);
+        qsc[nt][1] = __shfl_sync(0xffffffffu, up, 8 * c + 4);
+      } else {
+#pragma unroll
+        for (int i = 0; i < QW; ++i) qf[nt][i] = raw[i];
+        qsc[nt][0] = qsc[nt][1] = 1.f;
+      }
+    }
+    // ---- phase 1: scores of the chunk, s[h][key] = q_h . k_key
+    bool ok = true;
+    for (int tl = 0; tl < wk.ntl; ++tl, ++it) {
+      const int s = it % STAGES;
+      ok = ok && __all_sync(0xffffffffu, mbar_wait(bar_full(s), (it / STAGES) & 1, abort_flag, err));
+      if (!ok) continue;
+      const uint8_t* tile = smem + s * TILE_BYTES;
+      // K rows 16 warp + g and + 8: this thread's slice [c DQ, (c+1) DQ) of each
+      uint32_t ka[2][KW];
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int row = 16 * warp + g + 8 * r;
+#pragma unroll
+        for (int j = 0; j < KW / 4; ++j) {
+          const uint4 u = *reinterpret_cast<const uint4*>(tile + tile_off<HD, KV8>(row, c * DQ * GE::ESZ + 16 * (j ^ rot)));
+          ka[r][4 * j + 0] = u.x;
+          ka[r][4 * j + 1] = u.y;
+          ka[r][4 * j + 2] = u.z;
+          ka[r][4 * j + 3] = u.w;
+        }
+      }
+      float acc[NT][4];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < KK; ++kk) {
+        // MMA K index 2c + {0, 1} -> d = c DQ + 4 kk + {0, 1}; 2c + 8 + {0, 1} -> + {2, 3}
+        uint32_t a0, a1, a2, a3;
+        if constexpr (KV8) {
+          a0 = e4m3x2_f16x2<false>(ka[0][kk]);
+          a1 = e4m3x2_f16x2<false>(ka[1][kk]);
+          a2 = e4m3x2_f16x2<true>(ka[0][kk]);
+          a3 = e4m3x2_f16x2<true>(ka[1][kk]);
+        } else {
+          a0 = ka[0][2 * kk];
+          a1 = ka[1][2 * kk];
+          a2 = ka[0][2 * kk + 1];
+          a3 = ka[1][2 * kk + 1];
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma16816<KV8>(acc[nt], a0, a1, a2, a3, qf[nt][2 * kk], qf[nt][2 * kk + 1]);
+      }
+      // the MMAs above have consumed every value this warp read from the slot
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_empty(s));
+      // acc[nt] = S^T: rows keys 16 warp + g (+8), columns heads 8 nt + 2c (+1)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int h = 8 * nt + 2 * c + (e & 1);
+          const int key = tl * TILE + 16 * warp + g + 8 * (e >> 1);
+          if (h < G) work[h * wstride + key] = key < wk.n_valid ? acc[nt][e] * qsc[nt][e & 1] : -CUDART_INF_F;
+        }
+      }
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(NC) : "memory");
+    // ---- phase 2: chunk softmax per head (exp2 domain), p written in place
+    const int nk_pad = wk.ntl * TILE;
+    for (int h = warp; h < G; h += NCW) {
+      float* sh = work + h * wstride;
+      float mx = -CUDART_INF_F;
+      for (int j = lane; j < nk_pad; j += 32) mx = fmaxf(mx, sh[j]);
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      const float m = (mx == -CUDART_INF_F) ? 0.f : mx * c_log2;
+      float sum = 0.f;
+      for (int j = lane; j < nk_pad; j += 32) {
+        const float pv = ex2_approx(fmaf(sh[j], c_log2, -m));
+        sh[j] = pv;
+        sum += pv;
+      }
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      if (lane == 0) {
+        st_m[h] = m;
+        st_l[h] = sum;
+      }
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(NC) : "memory");
+    // ---- phase 3: O^T = V^T P^T for head-dimension rows [warp DQ, (warp+1) DQ)
+    float oacc[MT][NT][4];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) oacc[mt][nt][0] = oacc[mt][nt][1] = oacc[mt][nt][2] = oacc[mt][nt][3] = 0.f;
+    const int dbase = warp * DQ + DV * g;   // this thread's head-dimension elements dbase .. + DV - 1
+    for (int tl = 0; tl < wk.ntl; ++tl, ++it) {
+      const int s = it % STAGES;
+      ok = ok && __all_sync(0xffffffffu, mbar_wait(bar_full(s), (it / STAGES) & 1, abort_flag, err));
+      if (!ok) continue;
+      const uint8_t* tile = smem + s * TILE_BYTES;
+      const int valid_here = wk.n_valid - tl * TILE;   // keys of this tile inside the sequence
+#pragma unroll
+      for (int ks = 0; ks < TILE / 16; ++ks) {
+        // the MMA K index 2c + {0, 1, 8, 9} is key 16 ks + 2c + {0, 1, 8, 9}
+        uint32_t vw[4][DV * GE::ESZ / 4 > 0 ? DV * GE::ESZ / 4 : 1];   // V[key][dbase .. + DV) per key
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int key = 16 * ks + 2 * c + (i & 1) + 8 * (i >> 1);
+          const uint32_t off = tile_off<HD, KV8>(key, dbase * GE::ESZ);
+          const bool in = key < valid_here;
+          if constexpr (DV * GE::ESZ == 8) {
+            const uint2 u = *reinterpret_cast<const uint2*>(tile + off);
+            vw[i][0] = in ? u.x : 0u;
+            vw[i][1] = in ? u.y : 0u;
+          } else if constexpr (DV * GE::ESZ == 4) {
+            const uint32_t u = *reinterpret_cast<const uint32_t*>(tile + off);
+            vw[i][0] = in ? u : 0u;
+          } else {   // fp8, D = 64: two codes
+            const uint32_t u = *reinterpret_cast<const uint16_t*>(tile + off);
+            vw[i][0] = in ? u : 0u;
+          }
+        }
+        // A fragments: block mt covers d = dbase + 2 mt (MMA row g) and + 1 (row g + 8)
+        uint32_t af[MT][4];
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+          for (int pr = 0; pr < 2; ++pr) {   // pr 0: keys (2c, 2c+1); pr 1: keys (2c+8, 2c+9)
+            const int i0 = 2 * pr, i1 = 2 * pr + 1;
+            uint32_t lo, hi;   // (key i0, key i1) at d = dbase + 2mt, and at + 1
+            if constexpr (KV8) {
+              const uint32_t x = prmt(vw[i0][0], vw[i1][0], mt == 0 ? 0x5140u : 0x7362u);
+              lo = e4m3x2_f16x2<false>(x);
+              hi = e4m3x2_f16x2<true>(x);
+            } else {
+              lo = prmt(vw[i0][mt], vw[i1][mt], 0x5410u);
+              hi = prmt(vw[i0][mt], vw[i1][mt], 0x7632u);
+            }
+            af[mt][2 * pr + 0] = lo;
+            af[mt][2 * pr + 1] = hi;
+          }
+        }
+        // B fragments: P^T, keys (2c, 2c+1) and (2c+8, 2c+9) of head 8 nt + g
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const int h = 8 * nt + g;
+          uint32_t b0 = 0u, b1 = 0u;
+          if (h < G) {
+            const float* ph = work + h * wstride + tl * TILE + 16 * ks + 2 * c;
+            const float2 p01 = *reinterpret_cast<const float2*>(ph);
+            const float2 p89 = *reinterpret_cast<const float2*>(ph + 8);
+            if constexpr (KV8) {
+              b0 = pack_f16x2(p01.x, p01.y);
+              b1 = pack_f16x2(p89.x, p89.y);
+            } else {
+              b0 = pack_bf16x2(p01.x, p01.y);
+              b1 = pack_bf16x2(p89.x, p89.y);
+            }
+          }
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt)
+            mma16816<KV8>(oacc[mt][nt], af[mt][0], af[mt][1], af[mt][2], af[mt][3], b0, b1);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_empty(s));
+    }
+    // ---- write the chunk's O_c (normalised, times v_scale) and LSE_c
+    {
+      const size_t base = (static_cast<size_t>(wk.b) * Hq + h0) * S_max + wk.c;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int h = 8 * nt + 2 * c + e;
+          if (h >= G) continue;
+          const float sc = v_scale / st_l[h];
+          float* dst = ws_o + (base + static_cast<size_t>(h) * S_max) * HD + dbase;
+          if constexpr (DV == 4) {
+            // elements dbase + {0, 1, 2, 3} = (mt 0 row g, mt 0 row g+8, mt 1 row g, mt 1 row g+8)
+            *reinterpret_cast<float4*>(dst) = make_float4(oacc[0][nt][e] * sc, oacc[0][nt][2 + e] * sc,
+                                                          oacc[MT - 1][nt][e] * sc, oacc[MT - 1][nt][2 + e] * sc);
+          } else {
+            *reinterpret_cast<float2*>(dst) = make_float2(oacc[0][nt][e] * sc, oacc[0][nt][2 + e] * sc);
+          }
+        }
+      }
+      if (tid < G) ws_lse[base + static_cast<size_t>(tid) * S_max] = (st_m[tid] + log2f(st_l[tid])) * 0.69314718055994531f;
+      if (tid == 0) *stop = *abort_flag;
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(NC) : "memory");  // scores and stats free for the next item
+    if (*stop) break;
+  }
+}
+
+}  // namespace decode_mma
+
+// One warp per (b, h): LSE-weighted merge of the chunk results; lane l holds
+// head-dimension elements [l HD/32, (l+1) HD/32).
+template <int HDIM>
 __global__ void __launch_bounds__(128)
 attn_decode_combine_kernel(const float* __restrict__ ws_o, const float* __restrict__ ws_lse,
                            const int* __restrict__ seqlens, __nv_bfloat16* __restrict__ o,
                            float* __restrict__ lse, int B, int Hq, int Nk_max, int chunk, int S_max,
                            int* err) {
+  constexpr int E = HDIM / 32;   // elements per lane: 4 or 2
   const int lane = static_cast<int>(lane_id());
   const int bh = static_cast<int>(blockIdx.x) * 4 + static_cast<int>(threadIdx.x >> 5);
   if (bh >= B * Hq) return;
   const int b = bh / Hq;
   const int Lb = __ldg(seqlens + b);
-  __nv_bfloat16* orow = o + static_cast<size_t>(bh) * HD + lane * 4;
+  __nv_bfloat16* orow = o + static_cast<size_t>(bh) * HDIM + lane * E;
   if (Lb < 1 || Lb > Nk_max) {
     if (lane == 0) atomicCAS(err, 0, ATTN_ERR_SEQLEN);
-    *reinterpret_cast<uint2*>(orow) = make_uint2(0u, 0u);
+    if constexpr (E == 4) *reinterpret_cast<uint2*>(orow) = make_uint2(0u, 0u);
+    else *reinterpret_cast<uint32_t*>(orow) = 0u;
     if (lane == 0 && lse != nullptr) lse[bh] = -CUDART_INF_F;
     return;
   }
   const int n = (Lb + chunk - 1) / chunk;
   const float* lp = ws_lse + static_cast<size_t>(bh) * S_max;
-  const float* op = ws_o + static_cast<size_t>(bh) * S_max * HD + lane * 4;
+  const float* op = ws_o + static_cast<size_t>(bh) * S_max * HDIM + lane * E;
   float M = -CUDART_INF_F;
   for (int c = lane; c < n; c += 32) M = fmaxf(M, lp[c]);
 #pragma unroll
   for (int k = 16; k >= 1; k >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, k));
   constexpr float LOG2E = 1.4426950408889634f;
   float s = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float acc[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
   for (int c0 = 0; c0 < n; c0 += 32) {
     const float wc = (c0 + lane < n) ? ex2_approx((lp[c0 + lane] - M) * LOG2E) : 0.f;
     s += wc;
@@ -475,146 +950,217 @@ attn_decode_combine_kernel(const float* __restrict__ ws_o, const float* __restri
     // eight chunks at a time, all eight loads in flight before the sums (chunks past the
     // count load zeros and add nothing: their weights are finite)
     for (int j0 = 0; j0 < cnt; j0 += 8) {
-      float4 x[8];
+      float x[8][E];
       float w[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const int j = j0 + u;
         w[u] = __shfl_sync(0xffffffffu, wc, j & 31);
-        x[u] = j < cnt ? *reinterpret_cast<const float4*>(op + static_cast<size_t>(c0 + j) * HD)
-                       : make_float4(0.f, 0.f, 0.f, 0.f);
+        if constexpr (E == 4) {
+          const float4 v = j < cnt ? *reinterpret_cast<const float4*>(op + static_cast<size_t>(c0 + j) * HDIM)
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+          x[u][0] = v.x;
+          x[u][1] = v.y;
+          x[u][2] = v.z;
+          x[u][3] = v.w;
+        } else {
+          const float2 v = j < cnt ? *reinterpret_cast<const float2*>(op + static_cast<size_t>(c0 + j) * HDIM)
+                                   : make_float2(0.f, 0.f);
+          x[u][0] = v.x;
+          x[u][1] = v.y;
+        }
       }
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        acc.x = fmaf(w[u], x[u].x, acc.x);
-        acc.y = fmaf(w[u], x[u].y, acc.y);
-        acc.z = fmaf(w[u], x[u].z, acc.z);
-        acc.w = fmaf(w[u], x[u].w, acc.w);
-      }
+      for (int u = 0; u < 8; ++u)
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[e] = fmaf(w[u], x[u][e], acc[e]);
     }
   }
 #pragma unroll
   for (int k = 16; k >= 1; k >>= 1) s += __shfl_xor_sync(0xffffffffu, s, k);
   const float inv = 1.f / s;
-  *reinterpret_cast<uint2*>(orow) =
-      make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+  if constexpr (E == 4)
+    *reinterpret_cast<uint2*>(orow) =
+        make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv), pack_bf16x2(acc[2] * inv, acc[3] * inv));
+  else
+    *reinterpret_cast<uint32_t*>(orow) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
   if (lane == 0 && lse != nullptr) lse[bh] = M + logf(s);
 }
 
-template <int G, bool PAGED, bool KV8>
+template <int G, bool PAGED>
 int launch_split(const CUtensorMap& tk, const CUtensorMap& tv, const void* q, const int* seqlens,
                  float* ws_o, float* ws_lse, int B, int Hq, int Hkv, int Nk_max, float scale,
                  int chunk, int S_max, int num_sms, cudaStream_t stream, int* err, const Paging& pg,
                  float k_scale, float v_scale) {
-  const Layout L = layout(G, chunk, B, Ring<G, KV8>::RING_BYTES);
+  const Layout L = layout(G, chunk, B, Ring<G>::RING_BYTES);
   const int smem = L.bytes + 1024;
-  static int attr_dev = -1;
-  static int attr_bytes = 0;
-  static int attr_smem = -1;   // shared-memory size the resident count below is for
-  static int resident = 1;     // CTAs of this instance that fit on one SM
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (attr_dev != dev || attr_bytes < smem) {
-    if (cudaFuncSetAttribute(attn_decode_splitkv_kernel<G, PAGED, KV8>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-      return ATTN_ERR_CUDA;
-    attr_dev = dev;
-    attr_bytes = smem;
-    attr_smem = -1;
-  }
-  if (attr_smem != smem) {
-    // the persistent grid is as many CTAs as are resident at once: up to three
-    // (fp8 cache, G <= 4: four) per SM, fewer when a large chunk or head group
-    // enlarges the score area
-    int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_decode_splitkv_kernel<G, PAGED, KV8>, NTHREADS,
-                                                      smem) != cudaSuccess)
-      return ATTN_ERR_CUDA;
-    constexpr int cap = Ring<G, KV8>::CTAS_PER_SM;
-    resident = n < 1 ? 1 : (n > cap ? cap : n);
-    attr_smem = smem;
-  }
+  // the persistent grid is as many CTAs as are resident at once: up to three
+  // per SM, fewer when a large chunk or head group enlarges the score area
+  static KernelSetup setup;
+  int n = 0;
+  if (const int rc = prepare_kernel(setup, attn_decode_splitkv_kernel<G, PAGED>, smem, NTHREADS, &n);
+      rc != ATTN_OK)
+    return rc;
+  constexpr int cap = Ring<G>::CTAS_PER_SM;
+  const int resident = n < 1 ? 1 : (n > cap ? cap : n);
   const int grid = resident * num_sms;
-  attn_decode_splitkv_kernel<G, PAGED, KV8><<<grid, NTHREADS, smem, stream>>>(
+  attn_decode_splitkv_kernel<G, PAGED><<<grid, NTHREADS, smem, stream>>>(
       tk, tv, static_cast<const __nv_bfloat16*>(q), seqlens, ws_o, ws_lse, B, Hq, Hkv, Nk_max, chunk,
-      S_max, scale * k_scale * 1.4426950408889634f, v_scale, err, pg);
+      S_max, scale * 1.4426950408889634f, err, pg);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
-template <bool PAGED, bool KV8>
-int launch_split_any(const CUtensorMap& tk, const CUtensorMap& tv, const void* q, const int* seqlens,
-                     void* workspace, int B, int Hq, int Hkv, int Nk_max, float scale, int chunk,
-                     int num_sms, cudaStream_t stream, int* err, const Paging& pg, float k_scale,
-                     float v_scale) {
-  const int S_max = (Nk_max + chunk - 1) / chunk;
-  float* ws_o = static_cast<float*>(workspace);
-  float* ws_lse = ws_o + static_cast<size_t>(B) * Hq * S_max * HD;
-#define ATTN_SPLIT_ARGS tk, tv, q, seqlens, ws_o, ws_lse, B, Hq, Hkv, Nk_max, scale, chunk, S_max, \
-                        num_sms, stream, err, pg, k_scale, v_scale
-  switch (Hq / Hkv) {
-    case 1: return launch_split<1, PAGED, KV8>(ATTN_SPLIT_ARGS);
-    case 2: return launch_split<2, PAGED, KV8>(ATTN_SPLIT_ARGS);
-    case 4: return launch_split<4, PAGED, KV8>(ATTN_SPLIT_ARGS);
-    case 8: return launch_split<8, PAGED, KV8>(ATTN_SPLIT_ARGS);
-    default: return ATTN_ERR_GQA;
+template <int HDIM, int G, bool PAGED, bool KV8>
+int launch_mma(const CUtensorMap& tk, const CUtensorMap& tv, const void* q, const int* seqlens, float* ws_o,
+               float* ws_lse, int B, int Hq, int Hkv, int Nk_max, float scale, int chunk, int S_max,
+               int num_sms, cudaStream_t stream, int* err, const Paging& pg, float k_scale, float v_scale) {
+  using C = decode_mma::Cfg<HDIM, G, KV8>;
+  constexpr int tile = decode_mma::Geo<HDIM, KV8>::TILE_BYTES;
+  constexpr int kMaxSmem = 227 * 1024;
+  int stages = C::SMALL_RING_BYTES / tile;
+  if (G > 8) {   // as many ring slots as fit next to the scores (at most MAX_STAGES)
+    const int rest = decode_mma::layout(G, chunk, B, 0).bytes + 1024;
+    stages = (kMaxSmem - rest) / tile;
+    if (stages > decode_mma::MAX_STAGES) stages = decode_mma::MAX_STAGES;
   }
-#undef ATTN_SPLIT_ARGS
+  if (stages < 2) return ATTN_ERR_CAPACITY;
+  const decode_mma::Layout L = decode_mma::layout(G, chunk, B, stages * tile);
+  const int smem = L.bytes + 1024;
+  if (smem > kMaxSmem) return ATTN_ERR_CAPACITY;
+  static KernelSetup setup;
+  int n = 0;
+  if (const int rc = prepare_kernel(setup, decode_mma::attn_decode_mma_kernel<HDIM, G, PAGED, KV8>, smem,
+                                    decode_mma::NTHREADS, &n);
+      rc != ATTN_OK)
+    return rc;
+  const int resident = n < 1 ? 1 : (n > C::CTAS_PER_SM ? C::CTAS_PER_SM : n);
+  decode_mma::attn_decode_mma_kernel<HDIM, G, PAGED, KV8><<<resident * num_sms, decode_mma::NTHREADS, smem, stream>>>(
+      tk, tv, static_cast<const __nv_bfloat16*>(q), seqlens, ws_o, ws_lse, B, Hq, Hkv, Nk_max, chunk, S_max,
+      scale * k_scale * 1.4426950408889634f, v_scale, err, pg, stages);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 // Tensor maps over a contiguous cache [B, Nk_max, Hkv, D] or a page pool
-// [num_pages, page_size, Hkv, D]: one box is 64 key rows of one KV head.
-inline bool cache_maps(CUtensorMap* tk, CUtensorMap* tv, const void* k, const void* v, int Hkv,
-                       int rows, int outer, bool kv8) {
-  const uint32_t box[4] = {HD, 1, TILE, 1};
+// [num_pages, page_size, Hkv, D].  SIMT kernel: one box is 64 key rows of one
+// KV head, unswizzled.  Tensor-core kernel: one box is one swizzled slab (64
+// key rows x at most 128 bytes of one KV head).
+inline bool cache_maps(CUtensorMap* tk, CUtensorMap* tv, const void* k, const void* v, int D, int Hkv,
+                       int rows, int outer, bool kv8, bool mma) {
   const CUtensorMapDataType dt = kv8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const uint32_t es = kv8 ? 1 : 2;
-  return encode_tiled_4d(tk, dt, k, HD, Hkv, rows, outer, es, box, CU_TENSOR_MAP_SWIZZLE_NONE) &&
-         encode_tiled_4d(tv, dt, v, HD, Hkv, rows, outer, es, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+  uint32_t box[4] = {static_cast<uint32_t>(D), 1, TILE, 1};
+  CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_NONE;
+  if (mma) {
+    const uint32_t row = static_cast<uint32_t>(D) * es;
+    const uint32_t srow = row > 128 ? 128 : row;
+    box[0] = srow / es;
+    swz = srow == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  }
+  return encode_tiled_4d(tk, dt, k, D, Hkv, rows, outer, es, box, swz) &&
+         encode_tiled_4d(tv, dt, v, D, Hkv, rows, outer, es, box, swz);
+}
+
+// The SIMT kernel serves the bf16 cache with D = 128 and up to 8 query heads
+// per KV head (it keeps up with HBM there); every other case takes the
+// tensor-core kernel.
+inline bool use_simt(int D, int G, bool kv8) { return !kv8 && D == 128 && G <= 8; }
+
+template <bool PAGED, bool KV8>
+int launch_split_any(const void* k, const void* v, int map_rows, int map_outer, const void* q,
+                     const int* seqlens, void* workspace, int B, int Hq, int Hkv, int Nk_max, int D,
+                     float scale, int chunk, int num_sms, cudaStream_t stream, int* err, const Paging& pg,
+                     float k_scale, float v_scale) {
+  const int S_max = (Nk_max + chunk - 1) / chunk;
+  float* ws_o = static_cast<float*>(workspace);
+  float* ws_lse = ws_o + static_cast<size_t>(B) * Hq * S_max * D;
+  const int G = Hq / Hkv;
+  const bool simt = use_simt(D, G, KV8);
+  CUtensorMap tk, tv;
+  if (!cache_maps(&tk, &tv, k, v, D, Hkv, map_rows, map_outer, KV8, !simt)) return ATTN_ERR_CUDA;
+#define ATTN_SPLIT_ARGS tk, tv, q, seqlens, ws_o, ws_lse, B, Hq, Hkv, Nk_max, scale, chunk, S_max, \
+                        num_sms, stream, err, pg, k_scale, v_scale
+  if (simt) {
+    if constexpr (!KV8) {
+      switch (G) {
+        case 1: return launch_split<1, PAGED>(ATTN_SPLIT_ARGS);
+        case 2: return launch_split<2, PAGED>(ATTN_SPLIT_ARGS);
+        case 4: return launch_split<4, PAGED>(ATTN_SPLIT_ARGS);
+        case 8: return launch_split<8, PAGED>(ATTN_SPLIT_ARGS);
+        default: return ATTN_ERR_GQA;
+      }
+    }
+    return ATTN_ERR_GQA;
+  }
+  if (D == 128) {
+    switch (G) {
+      case 1: return launch_mma<128, 1, PAGED, KV8>(ATTN_SPLIT_ARGS);
+      case 2: return launch_mma<128, 2, PAGED, KV8>(ATTN_SPLIT_ARGS);
+      case 4: return launch_mma<128, 4, PAGED, KV8>(ATTN_SPLIT_ARGS);
+      case 8: return launch_mma<128, 8, PAGED, KV8>(ATTN_SPLIT_ARGS);
+      case 16: return launch_mma<128, 16, PAGED, KV8>(ATTN_SPLIT_ARGS);
+      case 32: return launch_mma<128, 32, PAGED, KV8>(ATTN_SPLIT_ARGS);
+      default: return ATTN_ERR_GQA;
+    }
+  }
+  if (D == 64) {
+    switch (G) {
+      case 1: return launch_mma<64, 1, PAGED, KV8>(ATTN_SPLIT_ARGS);
+      case 2: return launch_mma<64, 2, PAGED, KV8>(ATTN_SPLIT_ARGS);
+      case 4: return launch_mma<64, 4, PAGED, KV8>(ATTN_SPLIT_ARGS);
+      case 8: return launch_mma<64, 8, PAGED, KV8>(ATTN_SPLIT_ARGS);
+      case 16: return launch_mma<64, 16, PAGED, KV8>(ATTN_SPLIT_ARGS);
+      case 32: return launch_mma<64, 32, PAGED, KV8>(ATTN_SPLIT_ARGS);
+      default: return ATTN_ERR_GQA;
+    }
+  }
+#undef ATTN_SPLIT_ARGS
+  return ATTN_ERR_HEAD_DIM;
 }
 
 }  // namespace decode
 
 int launch_decode_splitkv(const void* q, const void* k_cache, const void* v_cache,
                           const int* seqlens, void* workspace, int B, int Hq, int Hkv,
-                          int Nk_max, float scale, int chunk, int num_sms, cudaStream_t stream,
+                          int Nk_max, int D, float scale, int chunk, int num_sms, cudaStream_t stream,
                           int* err, int kv8, float k_scale, float v_scale) {
   using namespace decode;
-  CUtensorMap tk, tv;
-  if (!cache_maps(&tk, &tv, k_cache, v_cache, Hkv, Nk_max, B, kv8 != 0)) return ATTN_ERR_CUDA;
   const Paging none{nullptr, 0, 0, 0};
-  return kv8 ? launch_split_any<false, true>(tk, tv, q, seqlens, workspace, B, Hq, Hkv, Nk_max, scale,
-                                             chunk, num_sms, stream, err, none, k_scale, v_scale)
-             : launch_split_any<false, false>(tk, tv, q, seqlens, workspace, B, Hq, Hkv, Nk_max, scale,
-                                              chunk, num_sms, stream, err, none, 1.f, 1.f);
+  return kv8 ? launch_split_any<false, true>(k_cache, v_cache, Nk_max, B, q, seqlens, workspace, B, Hq, Hkv,
+                                             Nk_max, D, scale, chunk, num_sms, stream, err, none, k_scale, v_scale)
+             : launch_split_any<false, false>(k_cache, v_cache, Nk_max, B, q, seqlens, workspace, B, Hq, Hkv,
+                                              Nk_max, D, scale, chunk, num_sms, stream, err, none, 1.f, 1.f);
 }
 
 int launch_decode_splitkv_paged(const void* q, const void* k_pages, const void* v_pages,
                                 const int* block_table, const int* seqlens, void* workspace, int B,
-                                int Hq, int Hkv, int num_pages, int page_size, int max_pages,
+                                int Hq, int Hkv, int num_pages, int page_size, int max_pages, int D,
                                 float scale, int chunk, int num_sms, cudaStream_t stream, int* err,
                                 int kv8, float k_scale, float v_scale) {
   using namespace decode;
-  CUtensorMap tk, tv;
-  if (!cache_maps(&tk, &tv, k_pages, v_pages, Hkv, page_size, num_pages, kv8 != 0)) return ATTN_ERR_CUDA;
   const Paging pg{block_table, max_pages, page_size, num_pages};
-  return kv8 ? launch_split_any<true, true>(tk, tv, q, seqlens, workspace, B, Hq, Hkv,
-                                            max_pages * page_size, scale, chunk, num_sms, stream, err,
-                                            pg, k_scale, v_scale)
-             : launch_split_any<true, false>(tk, tv, q, seqlens, workspace, B, Hq, Hkv,
-                                             max_pages * page_size, scale, chunk, num_sms, stream, err,
-                                             pg, 1.f, 1.f);
+  return kv8 ? launch_split_any<true, true>(k_pages, v_pages, page_size, num_pages, q, seqlens, workspace, B,
+                                            Hq, Hkv, max_pages * page_size, D, scale, chunk, num_sms, stream,
+                                            err, pg, k_scale, v_scale)
+             : launch_split_any<true, false>(k_pages, v_pages, page_size, num_pages, q, seqlens, workspace, B,
+                                             Hq, Hkv, max_pages * page_size, D, scale, chunk, num_sms, stream,
+                                             err, pg, 1.f, 1.f);
 }
 
 int launch_decode_combine(const void* workspace, const int* seqlens, void* o, float* lse, int B,
-                          int Hq, int Nk_max, int chunk, cudaStream_t stream, int* err) {
+                          int Hq, int Nk_max, int D, int chunk, cudaStream_t stream, int* err) {
   using namespace decode;
   const int S_max = (Nk_max + chunk - 1) / chunk;
   const float* ws_o = static_cast<const float*>(workspace);
-  const float* ws_lse = ws_o + static_cast<size_t>(B) * Hq * S_max * HD;
+  const float* ws_lse = ws_o + static_cast<size_t>(B) * Hq * S_max * D;
   const int grid = (B * Hq + 3) / 4;
-  attn_decode_combine_kernel<<<grid, 128, 0, stream>>>(ws_o, ws_lse, seqlens,
-                                                        static_cast<__nv_bfloat16*>(o), lse, B, Hq,
-                                                        Nk_max, chunk, S_max, err);
+  if (D == 128)
+    attn_decode_combine_kernel<128><<<grid, 128, 0, stream>>>(ws_o, ws_lse, seqlens, static_cast<__nv_bfloat16*>(o),
+                                                              lse, B, Hq, Nk_max, chunk, S_max, err);
+  else if (D == 64)
+    attn_decode_combine_kernel<64><<<grid, 128, 0, stream>>>(ws_o, ws_lse, seqlens, static_cast<__nv_bfloat16*>(o),
+                                                             lse, B, Hq, Nk_max, chunk, S_max, err);
+  else
+    return ATTN_ERR_HEAD_DIM;
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

@@ -43,6 +43,8 @@
 #include <cuda_runtime.h>
 #include <math_constants.h>
 
+#include <cmath>
+
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -80,6 +82,13 @@ struct Cfg {
   static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
   static_assert(2 * BN + 2 * HD <= TMEM_COLS, "tensor memory budget");
 };
+
+// Softcap fast path: tanh(y) ~= y * sum_k kTanhPoly[k] y^(2k) for |y| <= kTanhPolyYMax,
+// the minimax polynomial (largest relative error 5.9e-7; 6.7e-7 evaluated in fp32
+// by Horner's rule) found by the Remez exchange in softmax_attention_attn_gb300/tanh_fit.py.
+constexpr double kTanhPoly[6] = {0.99999941359925792, -0.33329042378530915, 0.13281433880740096,
+                                 -0.051605674002214393, 0.016743115063837057, -0.003067060326585761};
+constexpr double kTanhPolyYMax = 1.0;
 
 __device__ __forceinline__ uint32_t s_col(int t) { return static_cast<uint32_t>(t * BN); }
 template <int HD>
@@ -541,26 +550,82 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
         for (int i = 0; i < BN; ++i) s[i] = __uint_as_float(sr[i >> 5][i & 31]);
         const bool need_mask = k0 + BN - 1 > tile_hi_min || k0 < tile_lo_max;
-        if (need_mask) {
-#pragma unroll
-          for (int i = 0; i < BN; ++i) {
-            const int key = k0 + i;
-            if (key > hi_r || key < lo_r) s[i] = -CUDART_INF_F;
-          }
-        }
         float mx[8];
+        float rmax;   // the row maximum: of s * c (exp2 units), or of the capped scores
+        if constexpr (CAP) {
+          // Softcap: the warp takes the polynomial path for this tile when every raw
+          // score of its 32 rows (masked ones included: they are finite here and are
+          // set to -inf after the cap) lies in [-smax, smax].
+          float mn[8];
 #pragma unroll
-        for (int g = 0; g < 8; ++g) mx[g] = fmaxf(s[g], s[8 + g]);
+          for (int g = 0; g < 8; ++g) {
+            mx[g] = fmaxf(s[g], s[8 + g]);
+            mn[g] = fminf(s[g], s[8 + g]);
+          }
 #pragma unroll
-        for (int i = 16; i < BN; i += 16)
+          for (int i = 16; i < BN; i += 16)
 #pragma unroll
-          for (int g = 0; g < 8; ++g) mx[g] = fmax3(mx[g], s[i + g], s[i + 8 + g]);
-        const float rmax = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
-        float rmax_l2;  // the row maximum in exp2 units (after the softcap)
-        if constexpr (CAP)
-          rmax_l2 = rmax == -CUDART_INF_F ? -CUDART_INF_F : p.cap_post * tanh_exp(p.cap_pre * rmax);
-        else
-          rmax_l2 = rmax * c;
+            for (int g = 0; g < 8; ++g) {
+              mx[g] = fmax3(mx[g], s[i + g], s[i + 8 + g]);
+              mn[g] = fmin3(mn[g], s[i + g], s[i + 8 + g]);
+            }
+          const float rmax_raw = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+          const float rmin_raw = fmin3(fmin3(mn[0], mn[1], mn[2]), fmin3(mn[3], mn[4], mn[5]), fminf(mn[6], mn[7]));
+          const bool poly = __all_sync(0xffffffffu, rmax_raw <= p.cap_poly_smax && rmin_raw >= -p.cap_poly_smax);
+          // s <- cap_post tanh(cap_pre s): the capped score in exp2 units, in place
+          if (poly) {  // cap_post tanh(cap_pre s) = s P(s^2), Horner's rule on pairs
+            auto cap_pair = [&](float a0, float a1, float& x0, float& x1) {
+              const uint64_t s2 = f2_pack(a0, a1);
+              const uint64_t w2 = f2_mul(s2, s2);
+              uint64_t q2 = f2_fma(f2_pack(p.cap_poly[5], p.cap_poly[5]), w2, f2_pack(p.cap_poly[4], p.cap_poly[4]));
+              q2 = f2_fma(q2, w2, f2_pack(p.cap_poly[3], p.cap_poly[3]));
+              q2 = f2_fma(q2, w2, f2_pack(p.cap_poly[2], p.cap_poly[2]));
+              q2 = f2_fma(q2, w2, f2_pack(p.cap_poly[1], p.cap_poly[1]));
+              q2 = f2_fma(q2, w2, f2_pack(p.cap_poly[0], p.cap_poly[0]));
+              f2_unpack(f2_mul(s2, q2), x0, x1);
+            };
+#pragma unroll
+            for (int i = 0; i < BN; i += 2) cap_pair(s[i], s[i + 1], s[i], s[i + 1]);
+            float unused;
+            cap_pair(rmax_raw, rmax_raw, rmax, unused);   // tanh is increasing: the max of the capped scores
+          } else {     // through the exponential identity (two special-function operations)
+#pragma unroll
+            for (int i = 0; i < BN; ++i) s[i] = p.cap_post * tanh_exp(p.cap_pre * s[i]);
+            rmax = p.cap_post * tanh_exp(p.cap_pre * rmax_raw);
+          }
+          if (need_mask) {
+#pragma unroll
+            for (int i = 0; i < BN; ++i) {
+              const int key = k0 + i;
+              if (key > hi_r || key < lo_r) s[i] = -CUDART_INF_F;
+            }
+#pragma unroll
+            for (int g = 0; g < 8; ++g) mx[g] = fmaxf(s[g], s[8 + g]);
+#pragma unroll
+            for (int i = 16; i < BN; i += 16)
+#pragma unroll
+              for (int g = 0; g < 8; ++g) mx[g] = fmax3(mx[g], s[i + g], s[i + 8 + g]);
+            rmax = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+          }
+        } else {
+          if (need_mask) {
+#pragma unroll
+            for (int i = 0; i < BN; ++i) {
+              const int key = k0 + i;
+              if (key > hi_r || key < lo_r) s[i] = -CUDART_INF_F;
+            }
+          }
+#pragma unroll
+          for (int g = 0; g < 8; ++g) mx[g] = fmaxf(s[g], s[8 + g]);
+#pragma unroll
+          for (int i = 16; i < BN; i += 16)
+#pragma unroll
+            for (int g = 0; g < 8; ++g) mx[g] = fmax3(mx[g], s[i + g], s[i + 8 + g]);
+          rmax = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+        }
+        // the row maximum in exp2 units (the capped scores are in exp2 units already)
+        const float cs = CAP ? 1.f : c;
+        const float rmax_l2 = rmax * cs;
         const float m_new = fmaxf(m, rmax_l2);
         float alpha = 1.f;
         bool grow = false;
@@ -580,16 +645,10 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
         const bool rescale = __any_sync(0xffffffffu, grow);
         l *= alpha;
         const float m_use = (m == -CUDART_INF_F) ? 0.f : m;
-        // p = 2^(s*c - m), summed and packed to bf16 pairs; each half of the keys
+        // p = 2^(s cs - m), summed and packed to bf16 pairs; each half of the keys
         // is handed to the MMA issuer as soon as it is in tensor memory.
-        const uint64_t c2 = f2_pack(c, c);
+        const uint64_t c2 = f2_pack(cs, cs);
         const uint64_t nm2 = f2_pack(-m_use, -m_use);
-        // softcap in exp2 units: cap_post tanh(y) - m = (cap_post - m) - 2 cap_post / (1 + 2^(2 y log2 e)),
-        // y = cap_pre s (the identity holds for either sign of y and saturates through inf and 0)
-        const uint64_t k2 = f2_pack(p.cap_pre * 2.8853900817779268f, p.cap_pre * 2.8853900817779268f);
-        const uint64_t one2 = f2_pack(1.f, 1.f);
-        const uint64_t ncp2 = f2_pack(-2.f * p.cap_post, -2.f * p.cap_post);
-        const uint64_t cpm2 = f2_pack(p.cap_post - m_use, p.cap_post - m_use);
         uint64_t sum2[2] = {0ull, 0ull};
 #pragma unroll
         for (int half = 0; half < 2; ++half) {  // P columns [32*half, +32) = keys [64*half, +64)
@@ -600,20 +659,7 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               float x0, x1;
-              if constexpr (CAP) {
-                // capped score in exp2 units; masked scores stay -inf
-                float e0, e1, d0, d1;
-                f2_unpack(f2_mul(f2_pack(s[c0 + 2 * i], s[c0 + 2 * i + 1]), k2), e0, e1);
-                f2_unpack(f2_add(f2_pack(ex2_approx(e0), ex2_approx(e1)), one2), d0, d1);
-                f2_unpack(f2_fma(f2_pack(rcp_approx(d0), rcp_approx(d1)), ncp2, cpm2), x0, x1);
-                if (need_mask) {
-                  if (s[c0 + 2 * i] == -CUDART_INF_F) x0 = -CUDART_INF_F;
-                  if (s[c0 + 2 * i + 1] == -CUDART_INF_F) x1 = -CUDART_INF_F;
-                }
-              } else {
-                const uint64_t x2 = f2_fma(f2_pack(s[c0 + 2 * i], s[c0 + 2 * i + 1]), c2, nm2);
-                f2_unpack(x2, x0, x1);
-              }
+              f2_unpack(f2_fma(f2_pack(s[c0 + 2 * i], s[c0 + 2 * i + 1]), c2, nm2), x0, x1);
               const float p0 = ex2_approx(x0);
               const float p1 = ex2_approx(x1);
               sum2[i & 1] = f2_add(sum2[i & 1], f2_pack(p0, p1));
@@ -742,15 +788,9 @@ int launch_impl(const void* q, const void* k, const void* v, void* o, float* lse
         !encode_tiled_3d(&tv, dt, v, HD, Nk, static_cast<uint64_t>(B) * Hkv, 2, box, CU_TENSOR_MAP_SWIZZLE_128B))
       return ATTN_ERR_CUDA;
   }
-  static int attr_set_dev = -1;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (attr_set_dev != dev) {
-    if (cudaFuncSetAttribute(attn_fwd_bf16_kernel<HD, F16, CAP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::SMEM_ALLOC) != cudaSuccess)
-      return ATTN_ERR_CUDA;
-    attr_set_dev = dev;
-  }
+  static KernelSetup setup;
+  if (const int rc = prepare_kernel(setup, attn_fwd_bf16_kernel<HD, F16, CAP>, C::SMEM_ALLOC); rc != ATTN_OK)
+    return rc;
   FwdParams prm;
   prm.o = o;
   prm.lse = lse;
@@ -771,6 +811,25 @@ int launch_impl(const void* q, const void* k, const void* v, void* o, float* lse
   prm.total_k = total_k;
   prm.cap_pre = CAP ? scale / softcap : 0.f;
   prm.cap_post = CAP ? softcap * 1.4426950408889634f : 0.f;
+  // Softcap fast path: cap_post tanh(a s) = s * sum_k (scale log2(e) t_k a^(2k)) (s^2)^k with
+  // a = scale / softcap, valid while |a s| <= kTanhPolyYMax.  Coefficients that are not
+  // normal floats (an extreme scale / softcap ratio) leave the path disabled.
+  prm.cap_poly_smax = -1.f;
+  for (int i = 0; i < 6; ++i) prm.cap_poly[i] = 0.f;
+  if (CAP) {
+    const double a = static_cast<double>(scale) / softcap;
+    const double c2 = static_cast<double>(scale) * 1.4426950408889634;
+    bool ok = true;
+    double ak = 1.0;
+    for (int i = 0; i < 6; ++i) {
+      const double u = c2 * kTanhPoly[i] * ak;
+      ok = ok && std::isfinite(u) && std::fabs(u) >= 1e-36 && std::fabs(u) <= 1e36;  // normal floats
+      prm.cap_poly[i] = static_cast<float>(u);
+      ak *= a * a;
+    }
+    const double smax = kTanhPolyYMax / a;
+    if (ok && std::isfinite(smax) && smax < 1e15) prm.cap_poly_smax = static_cast<float>(smax);
+  }
   prm.sinks = sinks;
   // persistent: at most one CTA per SM, each walking units blockIdx.x, +gridDim.x, ...
   const long long n_qblk = (Nq + BM * NQT - 1) / (BM * NQT);

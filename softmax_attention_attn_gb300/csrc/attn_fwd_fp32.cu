@@ -246,15 +246,8 @@ __global__ void __launch_bounds__(NT) attn_fwd_fp32_kernel(const float* __restri
 template <int D>
 int launch(const float* q, const float* k, const float* v, float* o, float* lse, int B, int Hq,
            int Hkv, int Nq, int Nk, float scale, int causal, int window, cudaStream_t stream) {
-  static int attr_dev = -1;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (attr_dev != dev) {
-    if (cudaFuncSetAttribute(attn_fwd_fp32_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Smem<D>::BYTES) != cudaSuccess)
-      return ATTN_ERR_CUDA;
-    attr_dev = dev;
-  }
+  static KernelSetup setup;
+  if (const int rc = prepare_kernel(setup, attn_fwd_fp32_kernel<D>, Smem<D>::BYTES); rc != ATTN_OK) return rc;
   const dim3 grid((Nq + BM - 1) / BM, Hq, B);
   attn_fwd_fp32_kernel<D><<<grid, NT, Smem<D>::BYTES, stream>>>(
       q, k, v, o, lse, Hq, Hkv, Nq, Nk, scale * 1.4426950408889634f, causal, window > 0 ? window : 0);

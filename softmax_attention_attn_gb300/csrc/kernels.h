@@ -3,6 +3,8 @@
 #pragma once
 
 #include <cstdint>
+#include <mutex>
+
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -10,6 +12,46 @@
 #include "attn.h"
 
 namespace attn {
+
+constexpr int kMaxDevices = 64;
+
+// Per-device launch set-up of one kernel: the dynamic shared-memory limit it
+// was raised to and the CTAs per SM resident at the last size asked for.
+// One object per kernel instance (a function-local static); every access holds
+// its mutex, so concurrent callers on any devices are safe.
+struct KernelSetup {
+  std::mutex mu;
+  int smem_limit[kMaxDevices] = {};   // 0: attribute not raised on that device yet
+  int occ_smem[kMaxDevices] = {};     // shared-memory size resident[] was computed for
+  int resident[kMaxDevices] = {};
+};
+
+// Raises `kernel`'s dynamic shared-memory limit on the current device to at
+// least `smem` bytes (once per device) and, when `resident` is given, stores
+// the number of CTAs of `threads` threads and `smem` bytes that fit on one SM.
+template <typename Kernel>
+int prepare_kernel(KernelSetup& st, Kernel kernel, int smem, int threads = 0, int* resident = nullptr) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_DEVICE;
+  std::lock_guard<std::mutex> lock(st.mu);
+  if (st.smem_limit[dev] < smem) {
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    st.smem_limit[dev] = smem;
+  }
+  if (resident != nullptr) {
+    if (st.occ_smem[dev] != smem) {
+      int n = 0;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+      st.resident[dev] = n;
+      st.occ_smem[dev] = smem;
+    }
+    *resident = st.resident[dev];
+  }
+  return ATTN_OK;
+}
 
 struct FwdParams {
   void* o;           // bf16 or fp16 output
@@ -30,6 +72,11 @@ struct FwdParams {
   // cap_post = c * log2(e).  sinks: one logit per query head (natural-log
   // units) in every row's softmax denominator, or null.
   float cap_pre, cap_post;
+  // Softcap fast path: on a tile whose raw scores all satisfy |s| <= cap_poly_smax
+  // the capped exponent is s * P(s^2) - m with P(w) = sum_k cap_poly[k] w^k
+  // (tanh as an odd minimax polynomial; cap_poly_smax < 0 disables the path).
+  float cap_poly[6];
+  float cap_poly_smax;
   const float* sinks;
 };
 
@@ -69,16 +116,16 @@ int launch_fwd_fp32(const float* q, const float* k, const float* v, float* o, fl
 // (k_scale, v_scale unused).
 int launch_decode_splitkv(const void* q, const void* k_cache, const void* v_cache,
                           const int* seqlens, void* workspace, int B, int Hq, int Hkv,
-                          int Nk_max, float scale, int chunk, int num_sms, cudaStream_t stream,
+                          int Nk_max, int D, float scale, int chunk, int num_sms, cudaStream_t stream,
                           int* err, int kv8 = 0, float k_scale = 1.f, float v_scale = 1.f);
 
 int launch_decode_splitkv_paged(const void* q, const void* k_pages, const void* v_pages,
                                 const int* block_table, const int* seqlens, void* workspace, int B,
-                                int Hq, int Hkv, int num_pages, int page_size, int max_pages,
+                                int Hq, int Hkv, int num_pages, int page_size, int max_pages, int D,
                                 float scale, int chunk, int num_sms, cudaStream_t stream, int* err,
                                 int kv8 = 0, float k_scale = 1.f, float v_scale = 1.f);
 
 int launch_decode_combine(const void* workspace, const int* seqlens, void* o, float* lse, int B,
-                          int Hq, int Nk_max, int chunk, cudaStream_t stream, int* err);
+                          int Hq, int Nk_max, int D, int chunk, cudaStream_t stream, int* err);
 
 }  // namespace attn

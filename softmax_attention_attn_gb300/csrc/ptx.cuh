@@ -364,6 +364,13 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return d;
 }
 
+// min(a, b, c) in one instruction (three-input min of sm_100+).
+__device__ __forceinline__ float fmin3(float a, float b, float c) {
+  float d;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // Packed pair of fp32 values for the paired FP32 instructions of sm_100+.
 __device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
   uint64_t r;

@@ -1,7 +1,13 @@
 import os
 import sys
 
-import pytest
+# The oracle's fp64 products run one BLAS thread per call: the full-size checks
+# spread (batch, head) slices over every host core with a thread pool instead.
+# Set before numpy is first imported.
+os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+os.environ.setdefault("OMP_NUM_THREADS", "1")
+
+import pytest  # noqa: E402
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 if ROOT not in sys.path:

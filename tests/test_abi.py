@@ -101,8 +101,10 @@ def test_decode_argument_errors(L):
     assert split(ws=None) == -1
     assert split(B=0) == -2
     assert split(Hq=12, Hkv=8) == -3
-    assert split(Hq=32, Hkv=2) == -3          # group of 16 not supported
-    assert split(D=64) == -4
+    assert split(Hq=64, Hkv=1) == -3          # group of 64 not supported
+    assert split(Hq=24, Hkv=2) == -3          # group of 12 not supported
+    assert split(D=96) == -4
+    assert split(D=256) == -4
     assert split(chunk=500) == -11
     assert split(chunk=2048) == -11
     assert split(B=5000) == -12
@@ -130,7 +132,7 @@ def test_paged_decode_argument_errors(L):
     assert paged(num_pages=0) == -2
     assert paged(max_pages=-1) == -2
     assert paged(Hq=32, Hkv=3) == -3
-    assert paged(D=64) == -4
+    assert paged(D=32) == -4
     assert paged(chunk=96) == -11
     assert paged(bt=MIS) == -5
     assert paged(scale=0.0) == -6
@@ -149,7 +151,7 @@ def test_fp8_decode_argument_errors(L):
     for f in (fp8, paged8):
         assert f(q=None) == -1
         assert f(Hq=32, Hkv=3) == -3
-        assert f(D=64) == -4
+        assert f(D=256) == -4
         assert f(chunk=96) == -11
         assert f(sl=MIS) == -5
         assert f(scale=0.0) == -6

@@ -5,8 +5,12 @@ Tolerances (fixed by the attention-forward target):
   * bf16 inputs (fp32 accumulation): max-abs error <= 2e-2 on O and
     |dLSE| <= 1e-2 * max(1, |LSE|) on LSE.
 Rows that see no key must give O = 0 and LSE = -inf on both sides.
-Small and ragged shapes are compared element by element; the full benchmark
-workloads are compared on sampled rows that the oracle computes one by one.
+Small and ragged shapes are compared element by element.  The benchmark's
+dense, causal GQA and split-KV decode workloads are compared element by element
+on every output (the oracle runs over (batch, head) slices on every host core);
+the other full-size workloads on sampled rows that the oracle computes one by one.
+Every output and workspace the library writes sits between canary-filled guard
+regions (``helpers.Guarded``) that are checked after the call.
 """
 import math
 
@@ -15,6 +19,7 @@ import pytest
 import torch
 
 import oracle
+from helpers import check_guards, compare_rows, guarded, parallel_map
 from softmax_attention_attn_gb300 import binding, inputs
 
 pytestmark = pytest.mark.gpu
@@ -59,7 +64,9 @@ def sample_rows(B, H, N, n, seed, tile=128):
 # ---------------------------------------------------------------- fp32 path
 def run_fp32(dev, B, Hq, Hkv, Nq, Nk, D, causal=False, window=0, seed=0):
     q, k, v = inputs.prefill_inputs(B, Hq, Hkv, Nq, Nk, D, "fp32", seed)
-    o, lse = binding.attn_fwd_fp32(q.to(dev), k.to(dev), v.to(dev), causal=causal, window=window)
+    go, gl = guarded(q.shape, torch.float32, dev), guarded((B, Hq, Nq), torch.float32, dev)
+    o, lse = binding.attn_fwd_fp32(q.to(dev), k.to(dev), v.to(dev), go.t, gl.t, causal=causal, window=window)
+    check_guards(go, gl)
     return q, k, v, o, lse
 
 
@@ -108,7 +115,9 @@ def test_fp32_edge_cases(dev, case):
 # ---------------------------------------------------------------- bf16 path
 def run_bf16(dev, B, Hq, Hkv, Nq, Nk, causal=False, window=0, seed=0, D=128):
     q, k, v = inputs.prefill_inputs(B, Hq, Hkv, Nq, Nk, D, "bf16", seed)
-    o, lse = binding.attn_fwd(q.to(dev), k.to(dev), v.to(dev), causal=causal, window=window)
+    go, gl = guarded(q.shape, torch.bfloat16, dev), guarded((B, Hq, Nq), torch.float32, dev)
+    o, lse = binding.attn_fwd(q.to(dev), k.to(dev), v.to(dev), go.t, gl.t, causal=causal, window=window)
+    check_guards(go, gl)
     return q, k, v, o, lse
 
 
@@ -167,7 +176,9 @@ FP16_CASES = [  # (B, Hq, Hkv, Nq, Nk, D, causal, window)
 def test_fp16_forward(dev, case):
     B, Hq, Hkv, Nq, Nk, D, causal, window = case
     q, k, v = inputs.prefill_inputs(B, Hq, Hkv, Nq, Nk, D, "fp16", seed=17)
-    o, lse = binding.attn_fwd_fp16(q.to(dev), k.to(dev), v.to(dev), causal=causal, window=window)
+    go, gl = guarded(q.shape, torch.float16, dev), guarded((B, Hq, Nq), torch.float32, dev)
+    o, lse = binding.attn_fwd_fp16(q.to(dev), k.to(dev), v.to(dev), go.t, gl.t, causal=causal, window=window)
+    check_guards(go, gl)
     O, L = oracle.attention_forward(q, k, v, 1 / math.sqrt(D), causal, window)
     check(o, lse, O, L, BF16_O_TOL, BF16_LSE_REL, True)
 
@@ -193,8 +204,10 @@ VARLEN_CASES = [  # (lens_q, lens_k, Hq, Hkv, D, causal, window)
 def test_bf16_varlen(dev, case):
     lens_q, lens_k, Hq, Hkv, D, causal, window = case
     q, k, v, cq, ck = inputs.varlen_inputs(lens_q, lens_k, Hq, Hkv, D, "bf16", seed=19)
+    go, gl = guarded(q.shape, torch.bfloat16, dev), guarded((Hq, q.shape[0]), torch.float32, dev)
     o, lse = binding.attn_fwd_varlen(q.to(dev), k.to(dev), v.to(dev), cq.to(dev), ck.to(dev), max(lens_q),
-                                     causal=causal, window=window)
+                                     go.t, gl.t, causal=causal, window=window)
+    check_guards(go, gl)
     O, L = oracle.attention_varlen(q, k, v, cq, ck, 1 / math.sqrt(D), causal, window)
     check(o, lse, O, L, BF16_O_TOL, BF16_LSE_REL, True)
     assert binding.get_device_error() == 0
@@ -242,47 +255,65 @@ def test_bf16_widened_workloads_sampled(dev, name, B, Hq, Hkv, Nq, Nk, D, causal
     ("dense_B1_H32_N8192", 1, 32, 32, 8192, False),
     ("causal_gqa_B4_H32_KV8_N4096", 4, 32, 8, 4096, True),
 ])
-def test_bf16_benchmark_workloads_sampled(dev, name, B, Hq, Hkv, N, causal):
-    """The benchmark's prefill workloads, checked on sampled rows."""
+def test_bf16_benchmark_workloads_full(dev, name, B, Hq, Hkv, N, causal):
+    """The benchmark's prefill workloads (its draws and launch), every O and LSE element
+    against the oracle, one (batch, head) slice per task on every host core."""
     q, k, v, o, lse = run_bf16(dev, B, Hq, Hkv, N, N, causal, 0, seed=0)
-    assert torch.isfinite(o.float()).all().item() and torch.isfinite(lse).all().item()
-    rows = sample_rows(B, Hq, N, 96, seed=5)
-    O, L = oracle.attention_rows(q, k, v, 1 / math.sqrt(128), rows, causal)
-    idx = tuple(np.array(rows).T)
-    check(o.cpu()[idx], lse.cpu()[idx], O, L, BF16_O_TOL, BF16_LSE_REL, True)
+    o, lse = o.float().cpu().numpy(), lse.cpu().numpy()
+    g = Hq // Hkv
+
+    def one(bh):
+        b, h = divmod(bh, Hq)
+        O, L = oracle.attention_forward(q[b:b + 1, h:h + 1], k[b:b + 1, h // g:h // g + 1],
+                                        v[b:b + 1, h // g:h // g + 1], 1 / math.sqrt(128), causal)
+        return compare_rows(o[b, h], lse[b, h], O[0, 0], L[0, 0])
+
+    res = parallel_map(one, range(B * Hq))
+    err_o = max(r[0] for r in res)
+    err_l = max(r[1] for r in res)
+    print(f"[achieved] {name} full: O err {err_o:.3e}, LSE err {err_l:.3e}")
+    assert all(r[2] for r in res), "non-finite output or LSE finiteness mismatch"
+    assert err_o <= BF16_O_TOL and err_l <= BF16_LSE_REL, f"O err {err_o:.3e}, LSE err {err_l:.3e}"
 
 
 # ---------------------------------------------------------------- decode
-def run_decode(dev, B, Hq, Hkv, lens, nk_max, chunk, seed=0):
-    _, q = inputs.decode_seqlens_and_q(B, Hq, 128, 1, 2, seed)
+def run_decode(dev, B, Hq, Hkv, lens, nk_max, chunk, seed=0, D=128, fill=None):
+    _, q = inputs.decode_seqlens_and_q(B, Hq, D, 1, 2, seed)
     seqlens = torch.tensor(lens, dtype=torch.int32)
-    kc = torch.full((B, nk_max, Hkv, 128), inputs.K_SENTINEL, dtype=torch.bfloat16)
-    vc = torch.full((B, nk_max, Hkv, 128), inputs.V_SENTINEL, dtype=torch.bfloat16)
+    kfill, vfill = (inputs.K_SENTINEL, inputs.V_SENTINEL) if fill is None else (fill, fill)
+    kc = torch.full((B, nk_max, Hkv, D), kfill, dtype=torch.bfloat16)
+    vc = torch.full((B, nk_max, Hkv, D), vfill, dtype=torch.bfloat16)
     for b, n in enumerate(lens):
-        kb, vb = inputs.decode_kv_rows(seed, b, n, Hkv, 128)
+        kb, vb = inputs.decode_kv_rows(seed, b, n, Hkv, D)
         kc[b, :n], vc[b, :n] = kb, vb
-    ws = torch.empty(binding.attn_decode_workspace_size(B, Hq, 128, nk_max, chunk), device=dev,
-                     dtype=torch.uint8)
-    o, lse = binding.attn_decode(q.to(dev), kc.to(dev), vc.to(dev), seqlens.to(dev), ws, chunk=chunk)
+    gw = guarded((binding.attn_decode_workspace_size(B, Hq, D, nk_max, chunk),), torch.uint8, dev)
+    go, gl = guarded((B, Hq, D), torch.bfloat16, dev), guarded((B, Hq), torch.float32, dev)
+    ws = gw.t
+    o, lse = binding.attn_decode(q.to(dev), kc.to(dev), vc.to(dev), seqlens.to(dev), ws, go.t, gl.t, chunk=chunk)
+    check_guards(gw, go, gl)
     return q, kc, vc, seqlens, ws, o, lse
 
 
-@pytest.mark.parametrize("G", [1, 2, 4, 8])
+@pytest.mark.parametrize("D,G", [(128, 1), (128, 2), (128, 4), (128, 8), (128, 16), (128, 32),
+                                 (64, 1), (64, 4), (64, 8), (64, 32)])
 @pytest.mark.parametrize("chunk", [64, 512, 1024])
-def test_decode_small(dev, G, chunk):
+def test_decode_small(dev, D, G, chunk):
+    """bf16 cache: D = 128 with up to 8 query heads per KV head runs the SIMT consumer,
+    16 or 32 heads (MQA with Hkv = 1) and D = 64 the tensor-core consumer."""
     lens = [1, 64, 511, 512, 513, 1500, 2048]
-    B, Hkv = len(lens), 2
+    B = len(lens)
+    Hkv = 2 if G < 32 else 1
     Hq = G * Hkv
-    q, kc, vc, seqlens, ws, o, lse = run_decode(dev, B, Hq, Hkv, lens, 2048, chunk, seed=G + chunk)
-    scale = 1 / math.sqrt(128)
+    q, kc, vc, seqlens, ws, o, lse = run_decode(dev, B, Hq, Hkv, lens, 2048, chunk, seed=G + chunk, D=D)
+    scale = 1 / math.sqrt(D)
     O, L = oracle.decode_forward(q, kc, vc, seqlens, scale)
     check(o, lse, O, L, BF16_O_TOL, BF16_LSE_REL, True)
     # the partial step on its own, valid chunks only
     Op, Lp, ns = oracle.decode_split_partials(q, kc, vc, seqlens, scale, chunk)
     S_max = Op.shape[2]
     wsf = ws.view(torch.float32).cpu().numpy()
-    go = wsf[: B * Hq * S_max * 128].reshape(B, Hq, S_max, 128)
-    gl = wsf[B * Hq * S_max * 128: B * Hq * S_max * 129].reshape(B, Hq, S_max)
+    go = wsf[: B * Hq * S_max * D].reshape(B, Hq, S_max, D)
+    gl = wsf[B * Hq * S_max * D: B * Hq * S_max * (D + 1)].reshape(B, Hq, S_max)
     for b in range(B):
         n = int(ns[b])
         assert np.abs(go[b, :, :n] - Op[b, :, :n]).max() <= BF16_O_TOL
@@ -290,36 +321,81 @@ def test_decode_small(dev, G, chunk):
     assert binding.get_device_error() == 0
 
 
-def test_decode_benchmark_workload_sampled(dev):
-    """B=64 Hq=32 Hkv=8, Nk_b ~ U[512, 32768], chunk 512: sampled sequences.
+def test_decode_benchmark_workload_full(dev):
+    """B=64 Hq=32 Hkv=8, Nk_b ~ U[512, 32768], chunk 512 (the benchmark's draws and launch):
+    every O and LSE element of every sequence against the oracle.
 
-    The 8.6 GB cache is drawn on the device; the sampled sequences' rows are
-    copied back for the oracle.
+    The 8.6 GB cache is drawn on the device; each sequence's rows are copied back
+    for the oracle, which runs one sequence per task on every host core.
     """
     q, kc, vc, seqlens = inputs.decode_inputs(64, 32, 8, 128, 512, 32768, seed=0, device=dev)
-    o, lse = binding.attn_decode(q.to(dev), kc, vc, seqlens.to(dev), chunk=512)
-    lens = seqlens.numpy()
-    batches = sorted({int(lens.argmax()), int(lens.argmin()), 0, 17, 40, 63})
-    O = np.zeros((len(batches), 32, 128))
-    L = np.zeros((len(batches), 32))
-    for n, b in enumerate(batches):
-        nk = int(lens[b])
-        Ob, Lb = oracle.decode_forward(q[b:b + 1], kc[b:b + 1, :nk].cpu(), vc[b:b + 1, :nk].cpu(),
-                                       [nk], 1 / math.sqrt(128))
-        O[n], L[n] = Ob[0], Lb[0]
-    check(o.cpu()[batches], lse.cpu()[batches], O, L, BF16_O_TOL, BF16_LSE_REL, True)
+    B, Hq = 64, 32
+    gw = guarded((binding.attn_decode_workspace_size(B, Hq, 128, 32768, 512),), torch.uint8, dev)
+    go, gl = guarded((B, Hq, 128), torch.bfloat16, dev), guarded((B, Hq), torch.float32, dev)
+    o, lse = binding.attn_decode(q.to(dev), kc, vc, seqlens.to(dev), gw.t, go.t, gl.t, chunk=512)
+    check_guards(gw, go, gl)
     assert binding.get_device_error() == 0
+    o, lse = o.float().cpu().numpy(), lse.cpu().numpy()
+    lens = seqlens.numpy()
+
+    def one(b):
+        nk = int(lens[b])
+        Ob, Lb = oracle.decode_forward(q[b:b + 1], kc[b:b + 1, :nk].cpu(), vc[b:b + 1, :nk].cpu(), [nk],
+                                       1 / math.sqrt(128))
+        return compare_rows(o[b], lse[b], Ob[0], Lb[0])
+
+    res = parallel_map(one, range(B), threads=8)   # at most 8 sequences' fp64 caches in memory
+    err_o = max(r[0] for r in res)
+    err_l = max(r[1] for r in res)
+    print(f"[achieved] decode B=64 full: O err {err_o:.3e}, LSE err {err_l:.3e}")
+    assert all(r[2] for r in res), "non-finite output or LSE finiteness mismatch"
+    assert err_o <= BF16_O_TOL and err_l <= BF16_LSE_REL, f"O err {err_o:.3e}, LSE err {err_l:.3e}"
 
 
-@pytest.mark.parametrize("page_size,chunk,G", [(64, 512, 4), (256, 512, 4), (128, 64, 2), (512, 1024, 8)])
-def test_decode_paged_small(dev, page_size, chunk, G):
+@pytest.mark.parametrize("name,B,Hq,Hkv,D", [
+    ("mqa_B128_Hq32_Hkv1_D128", 128, 32, 1, 128),
+    ("d64_B64_Hq32_Hkv8", 64, 32, 8, 64),
+])
+def test_decode_widened_workloads_full(dev, name, B, Hq, Hkv, D):
+    """Multi-query decode and head dimension 64 (the benchmark's draws: Nk_b ~ U[512, 32768],
+    chunk 512): every O and LSE element against the oracle."""
+    q, kc, vc, seqlens = inputs.decode_inputs(B, Hq, Hkv, D, 512, 32768, seed=0, device=dev)
+    gw = guarded((binding.attn_decode_workspace_size(B, Hq, D, 32768, 512),), torch.uint8, dev)
+    go, gl = guarded((B, Hq, D), torch.bfloat16, dev), guarded((B, Hq), torch.float32, dev)
+    o, lse = binding.attn_decode(q.to(dev), kc, vc, seqlens.to(dev), gw.t, go.t, gl.t, chunk=512)
+    check_guards(gw, go, gl)
+    assert binding.get_device_error() == 0
+    o, lse = o.float().cpu().numpy(), lse.cpu().numpy()
+    lens = seqlens.numpy()
+
+    def one(b):
+        nk = int(lens[b])
+        Ob, Lb = oracle.decode_forward(q[b:b + 1], kc[b:b + 1, :nk].cpu(), vc[b:b + 1, :nk].cpu(), [nk],
+                                       1 / math.sqrt(D))
+        return compare_rows(o[b], lse[b], Ob[0], Lb[0])
+
+    res = parallel_map(one, range(B), threads=8)
+    err_o = max(r[0] for r in res)
+    err_l = max(r[1] for r in res)
+    print(f"[achieved] decode {name} full: O err {err_o:.3e}, LSE err {err_l:.3e}")
+    assert all(r[2] for r in res), "non-finite output or LSE finiteness mismatch"
+    assert err_o <= BF16_O_TOL and err_l <= BF16_LSE_REL, f"O err {err_o:.3e}, LSE err {err_l:.3e}"
+
+
+@pytest.mark.parametrize("page_size,chunk,G,D", [(64, 512, 4, 128), (256, 512, 4, 128), (128, 64, 2, 128),
+                                                 (512, 1024, 8, 128), (64, 512, 16, 128), (128, 512, 4, 64)])
+def test_decode_paged_small(dev, page_size, chunk, G, D):
     """Paged cache with sequences scattered over the pool (and spare pages)."""
     B, Hkv = 7, 2
     Hq = G * Hkv
-    q, kp, vp, bt, sl = inputs.paged_decode_inputs(B, Hq, Hkv, 128, 1, 3000, page_size, seed=page_size + G,
+    q, kp, vp, bt, sl = inputs.paged_decode_inputs(B, Hq, Hkv, D, 1, 3000, page_size, seed=page_size + G,
                                                    spare_pages=5)
-    o, lse = binding.attn_decode_paged(q.to(dev), kp.to(dev), vp.to(dev), bt.to(dev), sl.to(dev), chunk=chunk)
-    O, L = oracle.decode_forward_paged(q, kp, vp, bt, sl, 1 / math.sqrt(128))
+    gw = guarded((binding.attn_decode_workspace_size(B, Hq, D, bt.shape[1] * page_size, chunk),), torch.uint8, dev)
+    go, gl = guarded((B, Hq, D), torch.bfloat16, dev), guarded((B, Hq), torch.float32, dev)
+    o, lse = binding.attn_decode_paged(q.to(dev), kp.to(dev), vp.to(dev), bt.to(dev), sl.to(dev), gw.t, go.t, gl.t,
+                                       chunk=chunk)
+    check_guards(gw, go, gl)
+    O, L = oracle.decode_forward_paged(q, kp, vp, bt, sl, 1 / math.sqrt(D))
     check(o, lse, O, L, BF16_O_TOL, BF16_LSE_REL, True)
     assert binding.get_device_error() == 0
 
@@ -342,18 +418,12 @@ def test_decode_paged_benchmark_workload_sampled(dev):
     assert binding.get_device_error() == 0
 
 
-def test_decode_nan_in_unused_cache_rows_does_not_leak(dev):
-    """Rows past a sequence's end may hold anything, NaN included."""
+@pytest.mark.parametrize("D,Hq,Hkv", [(128, 8, 2), (128, 32, 2), (64, 8, 2), (128, 32, 1)])
+def test_decode_nan_in_unused_cache_rows_does_not_leak(dev, D, Hq, Hkv):
+    """Rows past a sequence's end may hold anything, NaN included (SIMT and tensor-core consumers)."""
     lens = [5, 700, 1]
-    B, Hq, Hkv, nk_max = 3, 8, 2, 1024
-    _, q = inputs.decode_seqlens_and_q(B, Hq, 128, 1, 2, 6)
-    kc = torch.full((B, nk_max, Hkv, 128), float("nan"), dtype=torch.bfloat16)
-    vc = torch.full((B, nk_max, Hkv, 128), float("nan"), dtype=torch.bfloat16)
-    for b, n in enumerate(lens):
-        kb, vb = inputs.decode_kv_rows(6, b, n, Hkv, 128)
-        kc[b, :n], vc[b, :n] = kb, vb
-    o, lse = binding.attn_decode(q.to(dev), kc.to(dev), vc.to(dev), torch.tensor(lens, dtype=torch.int32).to(dev))
-    O, L = oracle.decode_forward(q, kc, vc, lens, 1 / math.sqrt(128))
+    q, kc, vc, seqlens, ws, o, lse = run_decode(dev, 3, Hq, Hkv, lens, 1024, 512, seed=6, D=D, fill=float("nan"))
+    O, L = oracle.decode_forward(q, kc, vc, lens, 1 / math.sqrt(D))
     check(o, lse, O, L, BF16_O_TOL, BF16_LSE_REL, True)
 
 
@@ -379,21 +449,27 @@ def test_decode_bad_seqlen_reported(dev):
 FP8_SCALES = (0.37, 1.9)   # k_scale, v_scale: values are code * scale
 
 
-@pytest.mark.parametrize("G,chunk", [(1, 512), (4, 512), (8, 64), (2, 1024)])
-def test_decode_fp8_small(dev, G, chunk):
+@pytest.mark.parametrize("G,chunk,D", [(1, 512, 128), (4, 512, 128), (8, 64, 128), (2, 1024, 128),
+                                       (16, 512, 128), (32, 512, 128), (4, 512, 64), (32, 64, 64)])
+def test_decode_fp8_small(dev, G, chunk, D):
     """fp8 E4M3 cache: ragged lengths around the chunk and tile sizes."""
     lens = [1, 63, 64, 511, 513, 1500, 2048]
-    B, Hkv = len(lens), 2
+    B = len(lens)
+    Hkv = 2 if G < 32 else 1
     Hq = G * Hkv
     ks, vs = FP8_SCALES
-    q, kc, vc, _ = inputs.decode_inputs(B, Hq, Hkv, 128, 1, 2, seed=G + chunk, nk_max=2048, kv_dtype="e4m3")
+    q, kc, vc, _ = inputs.decode_inputs(B, Hq, Hkv, D, 1, 2, seed=G + chunk, nk_max=2048, kv_dtype="e4m3")
     sl = torch.tensor(lens, dtype=torch.int32)
     # regenerate rows for the chosen lengths (the drawn lengths are ignored)
     for b, n in enumerate(lens):
-        kb, vb = inputs.decode_kv_rows(G + chunk, b, n, Hkv, 128, kv_dtype="e4m3")
+        kb, vb = inputs.decode_kv_rows(G + chunk, b, n, Hkv, D, kv_dtype="e4m3")
         kc[b, :n], vc[b, :n] = kb, vb
-    o, lse = binding.attn_decode_fp8(q.to(dev), kc.to(dev), vc.to(dev), sl.to(dev), ks, vs, chunk=chunk)
-    O, L = oracle.decode_forward_fp8(q, kc.numpy(), vc.numpy(), ks, vs, lens, 1 / math.sqrt(128))
+    gw = guarded((binding.attn_decode_workspace_size(B, Hq, D, 2048, chunk),), torch.uint8, dev)
+    go, gl = guarded((B, Hq, D), torch.bfloat16, dev), guarded((B, Hq), torch.float32, dev)
+    o, lse = binding.attn_decode_fp8(q.to(dev), kc.to(dev), vc.to(dev), sl.to(dev), ks, vs, gw.t, go.t, gl.t,
+                                     chunk=chunk)
+    check_guards(gw, go, gl)
+    O, L = oracle.decode_forward_fp8(q, kc.numpy(), vc.numpy(), ks, vs, lens, 1 / math.sqrt(D))
     check(o, lse, O, L, BF16_O_TOL, BF16_LSE_REL, True)
     assert binding.get_device_error() == 0
 
@@ -406,8 +482,11 @@ def test_decode_fp8_paged_small(dev, page_size, chunk, G):
     ks, vs = FP8_SCALES
     q, kp, vp, bt, sl = inputs.paged_decode_inputs(B, Hq, Hkv, 128, 1, 3000, page_size, seed=page_size + G,
                                                    spare_pages=5, kv_dtype="e4m3")
+    gw = guarded((binding.attn_decode_workspace_size(B, Hq, 128, bt.shape[1] * page_size, chunk),), torch.uint8, dev)
+    go, gl = guarded((B, Hq, 128), torch.bfloat16, dev), guarded((B, Hq), torch.float32, dev)
     o, lse = binding.attn_decode_paged_fp8(q.to(dev), kp.to(dev), vp.to(dev), bt.to(dev), sl.to(dev), ks, vs,
-                                           chunk=chunk)
+                                           gw.t, go.t, gl.t, chunk=chunk)
+    check_guards(gw, go, gl)
     O, L = oracle.decode_forward_paged_fp8(q, kp.numpy(), vp.numpy(), ks, vs, bt, sl, 1 / math.sqrt(128))
     check(o, lse, O, L, BF16_O_TOL, BF16_LSE_REL, True)
     assert binding.get_device_error() == 0
@@ -428,6 +507,28 @@ def test_decode_fp8_benchmark_workload_sampled(dev):
                                            vc[b:b + 1, :nk].cpu().numpy(), ks, vs, [nk], 1 / math.sqrt(128))
         O[n], L[n] = Ob[0], Lb[0]
     check(o.cpu()[batches], lse.cpu()[batches], O, L, BF16_O_TOL, BF16_LSE_REL, True)
+    assert binding.get_device_error() == 0
+
+
+def test_decode_fp8_query_magnitudes_outside_f16_range(dev):
+    """The fp8 consumer runs its MMAs on f16 operands: each query head is scaled by a power of two
+    into f16 range first.  A head with |q| up to about 1e5 (beyond f16's 65504), one near 1e-6
+    (f16 subnormal range) and a zero head must still match the oracle."""
+    lens = [700, 1500, 64]
+    B, Hq, Hkv = 3, 8, 2
+    q, kc, vc, _ = inputs.decode_inputs(B, Hq, Hkv, 128, 1, 2, seed=41, nk_max=2048, kv_dtype="e4m3")
+    for b, n in enumerate(lens):
+        kb, vb = inputs.decode_kv_rows(41, b, n, Hkv, 128, kv_dtype="e4m3")
+        kc[b, :n], vc[b, :n] = kb, vb
+    q = q.float()
+    q[:, 1] *= 3e4                # |q| up to ~1e5, beyond f16's 65504; softmax close to one-hot
+    q[:, 2] *= 1e-6
+    q[:, 5] = 0.0
+    q = q.to(torch.bfloat16)
+    sl = torch.tensor(lens, dtype=torch.int32)
+    o, lse = binding.attn_decode_fp8(q.to(dev), kc.to(dev), vc.to(dev), sl.to(dev), 1.0, 1.0)
+    O, L = oracle.decode_forward_fp8(q, kc.numpy(), vc.numpy(), 1.0, 1.0, lens, 1 / math.sqrt(128))
+    check(o, lse, O, L, BF16_O_TOL, BF16_LSE_REL, True)
     assert binding.get_device_error() == 0
 
 
@@ -467,16 +568,26 @@ SOFTCAP_CASES = [
     (1, 4, 1, 384, 384, 128, True, 64, 0.0, "normal"),    # sinks only
     (2, 4, 2, 200, 333, 64, False, 0, 30.0, None),        # cap only, D = 64
     (1, 8, 8, 129, 1000, 128, True, 0, 50.0, "extreme"),  # chunked-prefill shape
+    # Q scaled by 3 (scaled scores ~ N(0, 9)) against cap 5: in one launch some warps'
+    # tiles stay within the polynomial range |score / cap| <= 1 and others leave it
+    (1, 4, 4, 384, 1024, 128, False, 0, 5.0, "normal", 3.0),
+    (1, 4, 2, 256, 2048, 64, False, 0, 50.0, None, 1.0),  # every tile on the polynomial path, D = 64
+    (2, 4, 1, 640, 640, 128, True, 0, 2.0, "normal", 1.5),  # causal, cap 2: unmasked tiles on both paths
 ]
 
 
 @pytest.mark.parametrize("case", SOFTCAP_CASES, ids=lambda c: "-".join(map(str, c)))
 def test_softcap_sink(dev, case):
-    B, Hq, Hkv, Nq, Nk, D, causal, window, cap, kind = case
+    B, Hq, Hkv, Nq, Nk, D, causal, window, cap, kind = case[:10]
     q, k, v = inputs.prefill_inputs(B, Hq, Hkv, Nq, Nk, D, "bf16", seed=Nq + Nk)
+    if len(case) > 10:
+        q = (q.float() * case[10]).to(torch.bfloat16)
     sinks = _sinks(Hq, kind, Nq)
-    o, lse = binding.attn_fwd_softcap_sink(q.to(dev), k.to(dev), v.to(dev), causal=causal, window=window,
-                                           softcap=cap, sinks=None if sinks is None else sinks.to(dev))
+    go, gl = guarded(q.shape, torch.bfloat16, dev), guarded((B, Hq, Nq), torch.float32, dev)
+    o, lse = binding.attn_fwd_softcap_sink(q.to(dev), k.to(dev), v.to(dev), go.t, gl.t, causal=causal,
+                                           window=window, softcap=cap,
+                                           sinks=None if sinks is None else sinks.to(dev))
+    check_guards(go, gl)
     O, L = oracle.attention_forward_ext(q, k, v, 1 / math.sqrt(D), causal, window, cap,
                                         None if sinks is None else sinks.numpy())
     check(o, lse, O, L, BF16_O_TOL, BF16_LSE_REL, True)
@@ -520,6 +631,7 @@ def _bwd_check(got, want, name):
     assert np.isfinite(g).all(), f"{name}: non-finite values"
     err = float(np.abs(g - want).max())
     tol = 2e-2 * max(1.0, float(np.abs(want).max()))
+    print(f"[achieved] backward {name}: max-abs err {err:.3e}, tol {tol:.3e}, max |grad| {np.abs(want).max():.3e}")
     assert err <= tol, f"{name}: max-abs err {err:.3e} (tol {tol:.3e})"
     return err
 
@@ -532,7 +644,11 @@ def test_backward(dev, case):
     do = torch.randn(B, Hq, Nq, 128, generator=g).to(torch.bfloat16)
     qd, kd, vd, dod = q.to(dev), k.to(dev), v.to(dev), do.to(dev)
     o, lse = binding.attn_fwd(qd, kd, vd, causal=causal)
-    dq, dk, dv = binding.attn_bwd(qd, kd, vd, o, dod, lse, causal=causal)
+    gq, gk, gv = (guarded(q.shape, torch.float32, dev), guarded(k.shape, torch.bfloat16, dev),
+                  guarded(v.shape, torch.bfloat16, dev))
+    gw = guarded((binding.lib().attn_bwd_workspace_size(B, Hq, Nq),), torch.uint8, dev)
+    dq, dk, dv = binding.attn_bwd(qd, kd, vd, o, dod, lse, gq.t, gk.t, gv.t, gw.t, causal=causal)
+    check_guards(gq, gk, gv, gw)
     dQ, dK, dV = oracle.attention_backward(q, k, v, do, 1 / math.sqrt(128), causal, 0)
     _bwd_check(dq, dQ, "dQ")
     _bwd_check(dk, dK, "dK")
@@ -552,9 +668,12 @@ def test_backward_full_size_two_heads(dev):
     dq, dk, dv = binding.attn_bwd(qd, kd, vd, o, dod, lse)
     torch.cuda.synchronize()
     assert binding.get_device_error() == 0
-    for h in (0, 17):
+    def one(h):
         sl = slice(h, h + 1)
-        dQ, dK, dV = oracle.attention_backward(q[:, sl], k[:, sl], v[:, sl], do[:, sl], 1 / math.sqrt(D), False, 0)
+        return h, oracle.attention_backward(q[:, sl], k[:, sl], v[:, sl], do[:, sl], 1 / math.sqrt(D), False, 0)
+
+    for h, (dQ, dK, dV) in parallel_map(one, (0, 17), threads=2):
+        sl = slice(h, h + 1)
         _bwd_check(dq[:, sl], dQ, f"dQ head {h}")
         _bwd_check(dk[:, sl], dK, f"dK head {h}")
         _bwd_check(dv[:, sl], dV, f"dV head {h}")

@@ -4,9 +4,10 @@ It is meant for callers that cannot allocate device memory (for example a
 plugin inside a host runtime that owns the device memory pool), so it keeps its
 per-chunk partials in a scratch array inside the library instead of a
 caller-provided workspace.  Two calls in a row, with different inputs and
-sizes, must match the workspace-based entry points (attn_decode_splitkv +
-attn_decode_combine) within the bf16 tolerances of the other parity tests; a
-size beyond the scratch capacity must be rejected on the host.
+sizes, must match the fp64 oracle's decode and the workspace-based entry points
+(attn_decode_splitkv + attn_decode_combine) within the bf16 tolerances of the
+other parity tests; a call without an LSE output must give the same O; a size
+beyond the scratch capacity must be rejected on the host.
 
 This file is named so that pytest collects it last.
 """
@@ -17,6 +18,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from softmax_attention_attn_gb300 import binding, inputs
 
 pytestmark = pytest.mark.gpu
@@ -38,10 +40,17 @@ def make_case(seed, lens, nk_max, dev):
 
 
 def call_noalloc(L, q, kc, vc, sl, o, lse, B, nk_max):
-    p = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    p = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())  # noqa: E731
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     return L.attn_decode_noalloc(p(q), p(kc), p(vc), p(sl), p(o), p(lse), B, HQ, HKV, nk_max, D,
                                  1 / math.sqrt(D), CHUNK, stream)
+
+
+def _close(o, lse, ref_o, ref_lse):
+    """max-abs O error and relative LSE error (|dLSE| / max(1, |LSE|)) against a reference."""
+    err_o = float(np.abs(o - ref_o).max())
+    err_l = 0.0 if lse is None else float((np.abs(lse - ref_lse) / np.maximum(1.0, np.abs(ref_lse))).max())
+    return err_o, err_l
 
 
 def test_noalloc_matches_workspace_entry_points(cuda_lib):
@@ -62,8 +71,19 @@ def test_noalloc_matches_workspace_entry_points(cuda_lib):
         oo, ro = o.float().cpu().numpy(), ref_o.float().cpu().numpy()
         ll, rl = lse.cpu().numpy(), ref_lse.cpu().numpy()
         assert np.isfinite(oo).all() and np.isfinite(ll).all()
-        assert np.abs(oo - ro).max() <= BF16_O_TOL
-        assert (np.abs(ll - rl) / np.maximum(1.0, np.abs(rl))).max() <= BF16_LSE_REL
+        # against the workspace-based entry points
+        err_o, err_l = _close(oo, ll, ro, rl)
+        assert err_o <= BF16_O_TOL and err_l <= BF16_LSE_REL, (err_o, err_l)
+        # against the fp64 oracle on the same inputs
+        O, Lse = oracle.decode_forward(q.cpu(), kc.cpu(), vc.cpu(), lens, 1 / math.sqrt(D))
+        err_o, err_l = _close(oo, ll, O, Lse)
+        assert err_o <= BF16_O_TOL and err_l <= BF16_LSE_REL, (err_o, err_l)
+        # the LSE output is optional: without it, O is unchanged
+        o2 = torch.full((B, HQ, D), float("nan"), device=dev, dtype=torch.bfloat16)
+        assert call_noalloc(L, q, kc, vc, sl, o2, None, B, nk_max) == 0
+        torch.cuda.synchronize()
+        assert binding.get_device_error() == 0
+        assert torch.equal(o2, o)
 
 
 def test_noalloc_rejects_sizes_beyond_capacity(cuda_lib):
