@@ -83,12 +83,39 @@ struct Cfg {
   static_assert(2 * BN + 2 * HD <= TMEM_COLS, "tensor memory budget");
 };
 
-// Softcap fast path: tanh(y) ~= y * sum_k kTanhPoly[k] y^(2k) for |y| <= kTanhPolyYMax,
-// the minimax polynomial (largest relative error 5.9e-7; 6.7e-7 evaluated in fp32
-// by Horner's rule) found by the Remez exchange in softmax_attention_attn_gb300/tanh_fit.py.
-constexpr double kTanhPoly[6] = {0.99999941359925792, -0.33329042378530915, 0.13281433880740096,
-                                 -0.051605674002214393, 0.016743115063837057, -0.003067060326585761};
-constexpr double kTanhPolyYMax = 1.0;
+// Softcap fast paths: tanh(y) ~= y * sum_k t_k y^(2k), minimax polynomials of the same
+// accuracy (largest relative error 5.4e-7 / 5.9e-7; 5.9e-7 / 6.7e-7 evaluated in fp32 by
+// Horner's rule) on |y| <= 0.5 (short) and |y| <= 1 (long), found by the Remez exchange in
+// softmax_attention_attn_gb300/tanh_fit.py.
+constexpr double kTanhPolyShort[4] = {0.99999945577093852, -0.3332631793594138, 0.1319029660321,
+                                      -0.044402226127707133};
+constexpr double kTanhPolyShortYMax = 0.5;
+constexpr double kTanhPolyLong[6] = {0.99999941359925792, -0.33329042378530915, 0.13281433880740096,
+                                     -0.051605674002214393, 0.016743115063837057, -0.003067060326585761};
+constexpr double kTanhPolyLongYMax = 1.0;
+
+// In place: s[i] <- s[i] * P(s[i]^2) with P(w) = sum_k coef[k] w^k (Horner's rule on
+// f32x2 pairs); *rmax <- the same for the scalar *rmax.
+template <int TERMS, int N>
+__device__ __forceinline__ void cap_polynomial(float (&s)[N], float* rmax, const float* coef) {
+  uint64_t cf[TERMS];
+#pragma unroll
+  for (int k = 0; k < TERMS; ++k) cf[k] = f2_pack(coef[k], coef[k]);
+#pragma unroll
+  for (int i = 0; i < N; i += 2) {
+    const uint64_t s2 = f2_pack(s[i], s[i + 1]);
+    const uint64_t w2 = f2_mul(s2, s2);
+    uint64_t q2 = f2_fma(cf[TERMS - 1], w2, cf[TERMS - 2]);
+#pragma unroll
+    for (int k = TERMS - 3; k >= 0; --k) q2 = f2_fma(q2, w2, cf[k]);
+    f2_unpack(f2_mul(s2, q2), s[i], s[i + 1]);
+  }
+  const float w = *rmax * *rmax;
+  float q = fmaf(coef[TERMS - 1], w, coef[TERMS - 2]);
+#pragma unroll
+  for (int k = TERMS - 3; k >= 0; --k) q = fmaf(q, w, coef[k]);
+  *rmax *= q;
+}
 
 __device__ __forceinline__ uint32_t s_col(int t) { return static_cast<uint32_t>(t * BN); }
 template <int HD>
@@ -553,9 +580,9 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
         float mx[8];
         float rmax;   // the row maximum: of s * c (exp2 units), or of the capped scores
         if constexpr (CAP) {
-          // Softcap: the warp takes the polynomial path for this tile when every raw
+          // Softcap: the warp caps this tile's scores with a polynomial when every raw
           // score of its 32 rows (masked ones included: they are finite here and are
-          // set to -inf after the cap) lies in [-smax, smax].
+          // set to -inf after the cap) lies in that polynomial's range.
           float mn[8];
 #pragma unroll
           for (int g = 0; g < 8; ++g) {
@@ -571,23 +598,18 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
             }
           const float rmax_raw = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
           const float rmin_raw = fmin3(fmin3(mn[0], mn[1], mn[2]), fmin3(mn[3], mn[4], mn[5]), fminf(mn[6], mn[7]));
-          const bool poly = __all_sync(0xffffffffu, rmax_raw <= p.cap_poly_smax && rmin_raw >= -p.cap_poly_smax);
-          // s <- cap_post tanh(cap_pre s): the capped score in exp2 units, in place
-          if (poly) {  // cap_post tanh(cap_pre s) = s P(s^2), Horner's rule on pairs
-            auto cap_pair = [&](float a0, float a1, float& x0, float& x1) {
-              const uint64_t s2 = f2_pack(a0, a1);
-              const uint64_t w2 = f2_mul(s2, s2);
-              uint64_t q2 = f2_fma(f2_pack(p.cap_poly[5], p.cap_poly[5]), w2, f2_pack(p.cap_poly[4], p.cap_poly[4]));
-              q2 = f2_fma(q2, w2, f2_pack(p.cap_poly[3], p.cap_poly[3]));
-              q2 = f2_fma(q2, w2, f2_pack(p.cap_poly[2], p.cap_poly[2]));
-              q2 = f2_fma(q2, w2, f2_pack(p.cap_poly[1], p.cap_poly[1]));
-              q2 = f2_fma(q2, w2, f2_pack(p.cap_poly[0], p.cap_poly[0]));
-              f2_unpack(f2_mul(s2, q2), x0, x1);
-            };
-#pragma unroll
-            for (int i = 0; i < BN; i += 2) cap_pair(s[i], s[i + 1], s[i], s[i + 1]);
-            float unused;
-            cap_pair(rmax_raw, rmax_raw, rmax, unused);   // tanh is increasing: the max of the capped scores
+          // the shortest polynomial every score of the warp's rows allows
+          const bool fits_short =
+              __all_sync(0xffffffffu, rmax_raw <= p.cap_smax_short && rmin_raw >= -p.cap_smax_short);
+          const bool fits_long =
+              __all_sync(0xffffffffu, rmax_raw <= p.cap_smax_long && rmin_raw >= -p.cap_smax_long);
+          // s <- cap_post tanh(cap_pre s): the capped score in exp2 units, in place;
+          // tanh is increasing, so rmax (the cap of the raw maximum) is the capped maximum
+          rmax = rmax_raw;
+          if (fits_short) {
+            cap_polynomial<4>(s, &rmax, p.cap_short);
+          } else if (fits_long) {
+            cap_polynomial<6>(s, &rmax, p.cap_long);
           } else {     // through the exponential identity (two special-function operations)
 #pragma unroll
             for (int i = 0; i < BN; ++i) s[i] = p.cap_post * tanh_exp(p.cap_pre * s[i]);
@@ -811,25 +833,28 @@ int launch_impl(const void* q, const void* k, const void* v, void* o, float* lse
   prm.total_k = total_k;
   prm.cap_pre = CAP ? scale / softcap : 0.f;
   prm.cap_post = CAP ? softcap * 1.4426950408889634f : 0.f;
-  // Softcap fast path: cap_post tanh(a s) = s * sum_k (scale log2(e) t_k a^(2k)) (s^2)^k with
-  // a = scale / softcap, valid while |a s| <= kTanhPolyYMax.  Coefficients that are not
-  // normal floats (an extreme scale / softcap ratio) leave the path disabled.
-  prm.cap_poly_smax = -1.f;
-  for (int i = 0; i < 6; ++i) prm.cap_poly[i] = 0.f;
-  if (CAP) {
+  // Softcap fast paths: cap_post tanh(a s) = s * sum_k (scale log2(e) t_k a^(2k)) (s^2)^k with
+  // a = scale / softcap, valid while |a s| <= the fit's y_max.  A fit whose prescaled
+  // coefficients are not all normal floats (an extreme scale / softcap ratio) stays disabled.
+  auto prescale = [&](const double* t, int terms, double ymax, float* out, float* smax_out) {
+    *smax_out = -1.f;
+    for (int i = 0; i < terms; ++i) out[i] = 0.f;
+    if (!CAP) return;
     const double a = static_cast<double>(scale) / softcap;
     const double c2 = static_cast<double>(scale) * 1.4426950408889634;
     bool ok = true;
     double ak = 1.0;
-    for (int i = 0; i < 6; ++i) {
-      const double u = c2 * kTanhPoly[i] * ak;
+    for (int i = 0; i < terms; ++i) {
+      const double u = c2 * t[i] * ak;
       ok = ok && std::isfinite(u) && std::fabs(u) >= 1e-36 && std::fabs(u) <= 1e36;  // normal floats
-      prm.cap_poly[i] = static_cast<float>(u);
+      out[i] = static_cast<float>(u);
       ak *= a * a;
     }
-    const double smax = kTanhPolyYMax / a;
-    if (ok && std::isfinite(smax) && smax < 1e15) prm.cap_poly_smax = static_cast<float>(smax);
-  }
+    const double smax = ymax / a;
+    if (ok && std::isfinite(smax) && smax < 1e15) *smax_out = static_cast<float>(smax);
+  };
+  prescale(kTanhPolyShort, 4, kTanhPolyShortYMax, prm.cap_short, &prm.cap_smax_short);
+  prescale(kTanhPolyLong, 6, kTanhPolyLongYMax, prm.cap_long, &prm.cap_smax_long);
   prm.sinks = sinks;
   // persistent: at most one CTA per SM, each walking units blockIdx.x, +gridDim.x, ...
   const long long n_qblk = (Nq + BM * NQT - 1) / (BM * NQT);

@@ -72,11 +72,13 @@ struct FwdParams {
   // cap_post = c * log2(e).  sinks: one logit per query head (natural-log
   // units) in every row's softmax denominator, or null.
   float cap_pre, cap_post;
-  // Softcap fast path: on a tile whose raw scores all satisfy |s| <= cap_poly_smax
-  // the capped exponent is s * P(s^2) - m with P(w) = sum_k cap_poly[k] w^k
-  // (tanh as an odd minimax polynomial; cap_poly_smax < 0 disables the path).
-  float cap_poly[6];
-  float cap_poly_smax;
+  // Softcap fast paths: on a tile whose raw scores all satisfy |s| <= cap_smax_short
+  // (cap_smax_long) the capped score in exp2 units is s * P(s^2) with
+  // P(w) = sum_k cap_short[k] w^k (cap_long[k] w^k): tanh as an odd minimax
+  // polynomial.  A negative bound disables that path.
+  float cap_short[4];
+  float cap_long[6];
+  float cap_smax_short, cap_smax_long;
   const float* sinks;
 };
 

@@ -1,21 +1,23 @@
 """Minimax polynomial for tanh used by the softcap path of the bf16 forward kernel.
 
 The softcap maps a scaled score to ``cap * tanh(y)`` with ``y = scale * s / cap``.
-On tiles where every ``|y| <= Y_MAX`` the kernel evaluates tanh as the odd
+On tiles where every ``|y|`` is small the kernel evaluates tanh as the odd
 polynomial ``tanh(y) ~= y * T(y^2)`` with
 
-    T(z) ~= sum_k t_k z^k,   k = 0 .. DEGREE,   z in [0, Y_MAX^2],
+    T(z) ~= sum_k t_k z^k,   k = 0 .. degree,   z in [0, y_max^2],
 
 on the FMA pipes instead of through the exponential identity (two special-
-function operations per score).  The coefficients ``t_k`` minimise the largest
+function operations per score).  Two fits of the same accuracy are used: a
+short one for ``|y| <= 0.5`` and a longer one for ``|y| <= 1``; a tile takes the
+shortest fit its scores allow.  The coefficients ``t_k`` minimise the largest
 relative error ``|T_fit(z) / T(z) - 1|`` with ``T(z) = tanh(sqrt z) / sqrt z``,
 which is also the relative error of the approximated tanh.  They are found by
 the Remez exchange algorithm (E. Ya. Remez, 1934): solve for the polynomial
 whose error equioscillates with height E on DEGREE + 2 reference points, move
 the references to the extrema of the new error curve, repeat.
 
-This module is the generator of the constants ``kTanhPoly`` in
-``csrc/attn_fwd_bf16.cu``; ``python -m softmax_attention_attn_gb300.tanh_fit``
+This module is the generator of the constants ``kTanhPolyShort`` and
+``kTanhPolyLong`` in ``csrc/attn_fwd_bf16.cu``; ``python -m softmax_attention_attn_gb300.tanh_fit``
 prints them, and a CPU test checks that the source holds these values and that
 the fp32 Horner evaluation meets ``MAX_REL_ERR``.  Nothing in the library's
 run-time path imports it.
@@ -24,8 +26,9 @@ from __future__ import annotations
 
 import numpy as np
 
-DEGREE = 5            # polynomial degree in z = y^2 (an odd degree-11 polynomial in y)
-Y_MAX = 1.0           # the fast path covers |y| <= Y_MAX
+# (degree in z = y^2, y_max): an odd degree-7 polynomial in y on |y| <= 0.5 and an odd
+# degree-11 polynomial on |y| <= 1
+FITS = {"short": (3, 0.5), "long": (5, 1.0)}
 MAX_REL_ERR = 8e-7    # bound on the relative error of y * T(y^2) evaluated in fp32 (Horner)
 
 
@@ -39,7 +42,7 @@ def tanh_over_y(z):
     return out
 
 
-def remez(degree: int = DEGREE, y_max: float = Y_MAX, iters: int = 60, grid_points: int = 400001):
+def remez(degree: int, y_max: float, iters: int = 60, grid_points: int = 400001):
     """Coefficients t_0..t_degree (float64) and the minimax relative error on [0, y_max^2]."""
     zmax = y_max * y_max
     n = degree
@@ -70,7 +73,7 @@ def remez(degree: int = DEGREE, y_max: float = Y_MAX, iters: int = 60, grid_poin
     return coef, float(np.abs(err).max())
 
 
-def fp32_horner_rel_err(coef, y_max: float = Y_MAX, points: int = 200001) -> float:
+def fp32_horner_rel_err(coef, y_max: float, points: int = 200001) -> float:
     """Largest relative error of y * T(y^2) against tanh(y) when evaluated in fp32 by Horner's rule."""
     y = np.linspace(-y_max, y_max, points).astype(np.float32)
     z = (y * y).astype(np.float32)
@@ -85,7 +88,8 @@ def fp32_horner_rel_err(coef, y_max: float = Y_MAX, points: int = 200001) -> flo
 
 
 if __name__ == "__main__":
-    c, e = remez()
-    print(f"// degree {DEGREE} in y^2 on |y| <= {Y_MAX}: minimax relative error {e:.3e}, "
-          f"fp32 Horner {fp32_horner_rel_err(c):.3e}")
-    print("constexpr double kTanhPoly[] = {" + ", ".join(f"{x:.17g}" for x in c) + "};")
+    for name, (deg, ym) in FITS.items():
+        c, e = remez(deg, ym)
+        print(f"// {name}: degree {deg} in y^2 on |y| <= {ym}: minimax relative error {e:.3e}, "
+              f"fp32 Horner {fp32_horner_rel_err(c, ym):.3e}")
+        print(f"constexpr double kTanhPoly{name.capitalize()}[] = {{" + ", ".join(f"{x:.17g}" for x in c) + "};")

@@ -573,6 +573,10 @@ SOFTCAP_CASES = [
     (1, 4, 4, 384, 1024, 128, False, 0, 5.0, "normal", 3.0),
     (1, 4, 2, 256, 2048, 64, False, 0, 50.0, None, 1.0),  # every tile on the polynomial path, D = 64
     (2, 4, 1, 640, 640, 128, True, 0, 2.0, "normal", 1.5),  # causal, cap 2: unmasked tiles on both paths
+    # per-head Q scales 0.3 / 0.7 / 1.3 against cap 4: the largest |score / cap| of a warp's tile
+    # is about 0.3 / 0.7 / 1.4, so warps of one launch take the short polynomial (|y| <= 0.5),
+    # the long one (|y| <= 1) and the exponential identity
+    (1, 8, 8, 512, 2048, 128, False, 0, 4.0, "normal", (0.3, 0.3, 0.7, 0.7, 1.3, 1.3, 1.3, 1.3)),
 ]
 
 
@@ -581,7 +585,9 @@ def test_softcap_sink(dev, case):
     B, Hq, Hkv, Nq, Nk, D, causal, window, cap, kind = case[:10]
     q, k, v = inputs.prefill_inputs(B, Hq, Hkv, Nq, Nk, D, "bf16", seed=Nq + Nk)
     if len(case) > 10:
-        q = (q.float() * case[10]).to(torch.bfloat16)
+        mul = torch.tensor(case[10], dtype=torch.float32).view(1, -1, 1, 1) if isinstance(case[10], tuple) \
+            else case[10]
+        q = (q.float() * mul).to(torch.bfloat16)
     sinks = _sinks(Hq, kind, Nq)
     go, gl = guarded(q.shape, torch.bfloat16, dev), guarded((B, Hq, Nq), torch.float32, dev)
     o, lse = binding.attn_fwd_softcap_sink(q.to(dev), k.to(dev), v.to(dev), go.t, gl.t, causal=causal,
