@@ -223,7 +223,8 @@ size_t attn_bwd_workspace_size(int B, int Hq, int Nq);
  *   dk, dv     : bf16 [B, Hkv, Nk, D] (outputs; K/V gradients of a KV head sum
  *                over the query heads that read it)
  *   workspace  : device buffer of attn_bwd_workspace_size(B, Hq, Nq) bytes
- *   causal     : bottom-right aligned as in attn_fwd; no sliding window
+ *   causal, window : the forward's masks, as in attn_fwd (bottom-right causal;
+ *                window > 0 keeps the last `window` keys up to the diagonal)
  *   D must be 128.  All device pointers 16-byte aligned, contiguous; the
  *   caller owns every buffer.  Asynchronous on `stream`.
  *   Errors: ATTN_ERR_NULL, ATTN_ERR_DIM, ATTN_ERR_GQA, ATTN_ERR_HEAD_DIM,
@@ -232,7 +233,8 @@ size_t attn_bwd_workspace_size(int B, int Hq, int Nq);
  */
 int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
              const float* lse, float* dq, void* dk, void* dv, void* workspace, int B, int Hq,
-             int Hkv, int Nq, int Nk, int D, float scale, int causal, attn_stream_t stream);
+             int Hkv, int Nq, int Nk, int D, float scale, int causal, int window,
+             attn_stream_t stream);
 
 /*
  * attn_decode_splitkv_fp8 — split-KV decode, partial step, on an fp8 KV cache.

@@ -38,7 +38,7 @@ SIGNATURES = {
     "attn_decode_splitkv_paged_fp8": (_c_int, [_vp] * 3 + [_c_float] * 2 + [_vp] * 3 + [_c_int] * 7
                                       + [_c_float, _c_int, _vp]),
     "attn_bwd_workspace_size": (ctypes.c_size_t, [_c_int] * 3),
-    "attn_bwd": (_c_int, [_vp] * 10 + [_c_int] * 6 + [_c_float, _c_int, _vp]),
+    "attn_bwd": (_c_int, [_vp] * 10 + [_c_int] * 6 + [_c_float, _c_int, _c_int, _vp]),
     "attn_get_device_error": (_c_int, [_vp]),
     "attn_strerror": (ctypes.c_char_p, [_c_int]),
 }
@@ -149,7 +149,7 @@ def attn_fwd_softcap_sink(q, k, v, o=None, lse=None, scale=None, causal=False, w
 
 
 def attn_bwd(q, k, v, o, do, lse, dq=None, dk=None, dv=None, workspace=None, scale=None, causal=False,
-             stream=None):
+             window=0, stream=None):
     """bf16 backward: (dq fp32 ``[B,Hq,Nq,D]``, dk, dv bf16 ``[B,Hkv,Nk,D]``) for the
     upstream gradient ``do``, from the forward's ``o`` and ``lse``."""
     import torch
@@ -174,7 +174,8 @@ def attn_bwd(q, k, v, o, do, lse, dq=None, dk=None, dv=None, workspace=None, sca
     _require(dv, torch.bfloat16, "dv")
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
     code = lib().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
-                          _ptr(workspace), B, Hq, Hkv, Nq, Nk, D, scale, int(bool(causal)), _stream(stream))
+                          _ptr(workspace), B, Hq, Hkv, Nq, Nk, D, scale, int(bool(causal)), int(window),
+                          _stream(stream))
     _check(code, "attn_bwd")
     return dq, dk, dv
 

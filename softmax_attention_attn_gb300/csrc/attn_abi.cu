@@ -251,7 +251,8 @@ size_t attn_bwd_workspace_size(int B, int Hq, int Nq) {
 
 int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
              const float* lse, float* dq, void* dk, void* dv, void* workspace, int B, int Hq,
-             int Hkv, int Nq, int Nk, int D, float scale, int causal, attn_stream_t stream) {
+             int Hkv, int Nq, int Nk, int D, float scale, int causal, int window,
+             attn_stream_t stream) {
   if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || !workspace) return ATTN_ERR_NULL;
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || Nq <= 0 || Nk <= 0 || D <= 0) return ATTN_ERR_DIM;
   if (Hq % Hkv != 0) return ATTN_ERR_GQA;
@@ -266,7 +267,7 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
   DeviceInfo* dev = nullptr;
   int rc = device_info(&dev);
   if (rc != ATTN_OK) return rc;
-  return launch_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, B, Hq, Hkv, Nq, Nk, scale, causal,
+  return launch_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, B, Hq, Hkv, Nq, Nk, scale, causal, window,
                     reinterpret_cast<cudaStream_t>(stream), dev->err);
 }
 

@@ -119,6 +119,7 @@ struct BwdParams {
   float c_log2;        // scale * log2(e)
   float scale;
   int causal;
+  int window;          // > 0: key k visible to query q only if k > q + Nk - Nq - window
   int* err;
 };
 
@@ -197,7 +198,14 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   const int n_qt = (p.Nq + BQ - 1) / BQ;
   int it0 = 0;  // first query tile with a query that sees a key of this tile
   if (p.causal && j0 - off > 0) it0 = (j0 - off) / BQ;
-  const int per_head = max(0, n_qt - it0);
+  // sliding window: key k is visible to query q only if q < k - off + window, so the
+  // tile's last key (j0 + BK - 1) bounds the last query tile
+  int it_end = n_qt;
+  if (p.window > 0) {
+    const long long q_last = static_cast<long long>(j0) + BK - 1 - off + p.window - 1;
+    it_end = q_last < 0 ? 0 : static_cast<int>(min(static_cast<long long>(n_qt), q_last / BQ + 1));
+  }
+  const int per_head = max(0, it_end - it0);
   const int n_steps = per_head * p.group;
 
   if (threadIdx.x == 0) {
@@ -406,8 +414,10 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       tc_fence_after();
       const float* nlse2v = reinterpret_cast<const float*>(vecs + s * VEC_BYTES) + 64 * hf;
       const float* ndeltav = reinterpret_cast<const float*>(vecs + s * VEC_BYTES) + BQ + 64 * hf;
-      // causal: query c of this step sees this key iff key <= i0 + c + off
+      // causal: query c of this step sees this key iff key <= i0 + c + off; window: iff
+      // i0 + c < key - off + window
       const int c_min = p.causal ? key - off - i0 - 64 * hf : 0;  // first visible query of this half
+      const int c_max = p.window > 0 ? key - off + p.window - 1 - i0 - 64 * hf : 63;  // last visible
       // P^T = 2^(S^T scale log2(e) - LSE log2(e)) for queries [64 hf, +64),
       // packed as bf16 pairs into S^T columns [64 hf, +32) (read by this warp only)
       {
@@ -430,11 +440,11 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             pk[cl >> 1] = pack_bf16x2(ex2_approx(x0), ex2_approx(x1));
           }
         }
-        // masked entries (padding keys, causal) to 0: only warps that have some
-        if (!__all_sync(0xffffffffu, key_ok && c_min <= 0)) {
+        // masked entries (padding keys, causal, window) to 0: only warps that have some
+        if (!__all_sync(0xffffffffu, key_ok && c_min <= 0 && c_max >= 63)) {
 #pragma unroll
           for (int c = 0; c < 64; c += 2) {
-            const bool v0 = key_ok && c >= c_min, v1 = key_ok && c + 1 >= c_min;
+            const bool v0 = key_ok && c >= c_min && c <= c_max, v1 = key_ok && c + 1 >= c_min && c + 1 <= c_max;
             pk[c >> 1] &= (v0 ? 0x0000FFFFu : 0u) | (v1 ? 0xFFFF0000u : 0u);
           }
         }
@@ -535,7 +545,8 @@ size_t bwd_workspace_bytes(int B, int Hq, int Nq) {
 
 int launch_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
                const float* lse, float* dq, void* dk, void* dv, void* workspace, int B, int Hq,
-               int Hkv, int Nq, int Nk, float scale, int causal, cudaStream_t stream, int* err) {
+               int Hkv, int Nq, int Nk, float scale, int causal, int window, cudaStream_t stream,
+               int* err) {
   using namespace bwd;
   const int nq_pad = (Nq + BQ - 1) / BQ * BQ;
   const long long rows_pad = static_cast<long long>(B) * Hq * nq_pad;
@@ -577,6 +588,7 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
   prm.c_log2 = scale * 1.4426950408889634f;
   prm.scale = scale;
   prm.causal = causal ? 1 : 0;
+  prm.window = window > 0 ? window : 0;
   prm.err = err;
   const dim3 grid((Nk + BK - 1) / BK, Hkv, B);
   attn_bwd_kernel<<<grid, NTHREADS, SMEM_ALLOC, stream>>>(tq, tk, tv, tdo, tdq, prm);

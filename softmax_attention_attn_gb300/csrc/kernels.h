@@ -107,7 +107,8 @@ int launch_fwd_tc(const void* q, const void* k, const void* v, void* o, float* l
 size_t bwd_workspace_bytes(int B, int Hq, int Nq);
 int launch_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
                const float* lse, float* dq, void* dk, void* dv, void* workspace, int B, int Hq,
-               int Hkv, int Nq, int Nk, float scale, int causal, cudaStream_t stream, int* err);
+               int Hkv, int Nq, int Nk, float scale, int causal, int window, cudaStream_t stream,
+               int* err);
 
 int launch_fwd_fp32(const float* q, const float* k, const float* v, float* o, float* lse, int B,
                     int Hq, int Hkv, int Nq, int Nk, int D, float scale, int causal, int window,

@@ -181,7 +181,7 @@ def test_softcap_sink_argument_errors(L):
 def test_backward_argument_errors(L):
     def f(q=P, k=P, v=P, o=P, do=P, lse=P, dq=P, dk=P, dv=P, ws=P, B=2, Hq=8, Hkv=2, Nq=128, Nk=128, D=128,
           scale=0.1, causal=0):
-        return L.attn_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, B, Hq, Hkv, Nq, Nk, D, scale, causal, None)
+        return L.attn_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, B, Hq, Hkv, Nq, Nk, D, scale, causal, 0, None)
 
     assert f(do=None) == -1
     assert f(ws=None) == -1

@@ -619,14 +619,18 @@ def test_softcap_sink_full_size_sampled(dev):
 
 # ---------------------------------------------------------------- backward
 BWD_CASES = [
-    # B, Hq, Hkv, Nq, Nk, causal
-    (1, 2, 2, 200, 200, False),
-    (2, 4, 2, 257, 257, True),      # GQA, ragged tiles
-    (1, 4, 1, 130, 300, True),      # bottom-right causal, Nq < Nk
-    (1, 2, 2, 300, 130, True),      # Nq > Nk: rows 0..169 see no key
-    (1, 2, 1, 64, 1000, False),     # one query tile, many key tiles
-    (1, 4, 2, 384, 384, True),      # whole tiles only, two query heads per KV head
-    (2, 2, 1, 5, 37, True),         # fewer queries than one 32-row dQ box
+    # B, Hq, Hkv, Nq, Nk, causal, window
+    (1, 2, 2, 200, 200, False, 0),
+    (2, 4, 2, 257, 257, True, 0),       # GQA, ragged tiles
+    (1, 4, 1, 130, 300, True, 0),       # bottom-right causal, Nq < Nk
+    (1, 2, 2, 300, 130, True, 0),       # Nq > Nk: rows 0..169 see no key
+    (1, 2, 1, 64, 1000, False, 0),      # one query tile, many key tiles
+    (1, 4, 2, 384, 384, True, 0),       # whole tiles only, two query heads per KV head
+    (2, 2, 1, 5, 37, True, 0),          # fewer queries than one 32-row dQ box
+    (1, 2, 2, 300, 300, True, 64),      # causal sliding window
+    (1, 4, 2, 257, 257, False, 100),    # window without causal
+    (1, 2, 1, 130, 700, True, 50),      # chunked prefill + window: key tiles no query sees (dK = dV = 0)
+    (1, 2, 2, 512, 512, True, 128),     # window of exactly one tile, whole tiles
 ]
 
 
@@ -644,18 +648,18 @@ def _bwd_check(got, want, name):
 
 @pytest.mark.parametrize("case", BWD_CASES, ids=lambda c: "-".join(map(str, c)))
 def test_backward(dev, case):
-    B, Hq, Hkv, Nq, Nk, causal = case
+    B, Hq, Hkv, Nq, Nk, causal, window = case
     q, k, v = inputs.prefill_inputs(B, Hq, Hkv, Nq, Nk, 128, "bf16", seed=Nq * 7 + Nk)
     g = torch.Generator("cpu").manual_seed(Nq + 3)
     do = torch.randn(B, Hq, Nq, 128, generator=g).to(torch.bfloat16)
     qd, kd, vd, dod = q.to(dev), k.to(dev), v.to(dev), do.to(dev)
-    o, lse = binding.attn_fwd(qd, kd, vd, causal=causal)
+    o, lse = binding.attn_fwd(qd, kd, vd, causal=causal, window=window)
     gq, gk, gv = (guarded(q.shape, torch.float32, dev), guarded(k.shape, torch.bfloat16, dev),
                   guarded(v.shape, torch.bfloat16, dev))
     gw = guarded((binding.lib().attn_bwd_workspace_size(B, Hq, Nq),), torch.uint8, dev)
-    dq, dk, dv = binding.attn_bwd(qd, kd, vd, o, dod, lse, gq.t, gk.t, gv.t, gw.t, causal=causal)
+    dq, dk, dv = binding.attn_bwd(qd, kd, vd, o, dod, lse, gq.t, gk.t, gv.t, gw.t, causal=causal, window=window)
     check_guards(gq, gk, gv, gw)
-    dQ, dK, dV = oracle.attention_backward(q, k, v, do, 1 / math.sqrt(128), causal, 0)
+    dQ, dK, dV = oracle.attention_backward(q, k, v, do, 1 / math.sqrt(128), causal, window)
     _bwd_check(dq, dQ, "dQ")
     _bwd_check(dk, dK, "dK")
     _bwd_check(dv, dV, "dV")
