@@ -440,9 +440,6 @@ attn_decode_splitkv_kernel(const __grid_constant__ CUtensorMap tm_k,
 namespace decode_mma {
 
 constexpr int TILE = 64;                 // keys per TMA tile
-constexpr int NCW = 4;                   // consumer warps
-constexpr int NC = NCW * 32;
-constexpr int NTHREADS = NC + 32;        // + producer warp
 constexpr int SPAD = 8;                  // floats of padding per score row (row stride chunk + SPAD)
 constexpr int MAX_STAGES = 16;
 
@@ -459,11 +456,28 @@ struct Geo {
 // Residency: up to 8 query heads per KV head, three CTAs per SM with 48 KB rings;
 // with 16 or 32 the chunk's scores take 32-64 KB (chunk 512), so one CTA per SM
 // runs with as large a ring as the shared memory leaves (up to 16 tiles).
+// Consumer warps: four (warp w: keys [16w, 16w+16) of a tile in Q K^T, head-dimension rows
+// [w D/4, (w+1) D/4) in P V) up to 8 query heads per KV head; eight with 16 or 32, where the
+// products are long enough per item that a CTA alone on its SM needs more warps in flight
+// (warp w then takes keys [16 (w % 4), +16) and half of the heads' MMA column blocks in Q K^T,
+// and its share of the (head-dimension block, head column block) pairs in P V).
 template <int HD, int G, bool KV8>
 struct Cfg {
   static constexpr int NT = (G + 7) / 8;                // MMA column blocks of 8 query heads
   static constexpr int CTAS_PER_SM = G <= 8 ? 3 : 1;
   static constexpr int SMALL_RING_BYTES = 48 * 1024;    // G <= 8
+  static constexpr int NCW = G >= 16 ? 8 : 4;           // consumer warps
+  static constexpr int NC = NCW * 32;
+  static constexpr int NTHREADS = NC + 32;              // + producer warp
+  // Q K^T: warp w takes key block w % 4 and column blocks [(w / 4) NTW, + NTW)
+  static constexpr int NTW = NT / (NCW / 4);
+  // P V: MB blocks of 16 head-dimension rows; a warp takes MTW consecutive blocks and
+  // NTP column blocks
+  static constexpr int MB = HD / 16;
+  static constexpr int MTW = MB > NCW ? MB / NCW : 1;
+  static constexpr int WPM = NCW > MB ? NCW / MB : 1;   // warps per block of rows
+  static constexpr int NTP = NT / WPM;
+  static_assert(NTW >= 1 && NTP >= 1 && NTW * (NCW / 4) == NT && NTP * WPM == NT, "warp split");
 };
 
 struct Layout {
@@ -532,7 +546,7 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
 }
 
 template <int HD, int G, bool PAGED, bool KV8>
-__global__ void __launch_bounds__(NTHREADS, 1)
+__global__ void __launch_bounds__(Cfg<HD, G, KV8>::NTHREADS, 1)
 attn_decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                        const __nv_bfloat16* __restrict__ q, const int* __restrict__ seqlens,
                        float* __restrict__ ws_o, float* __restrict__ ws_lse, int B, int Hq, int Hkv,
@@ -540,14 +554,17 @@ attn_decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_co
                        const decode::Paging pg, int STAGES) {
   using GE = Geo<HD, KV8>;
   using C = Cfg<HD, G, KV8>;
-  constexpr int NT = C::NT;
+  constexpr int NCW = C::NCW;
+  constexpr int NC = C::NC;
+  constexpr int NTW = C::NTW;
+  constexpr int NTP = C::NTP;
   constexpr int TILE_BYTES = GE::TILE_BYTES;
   constexpr int KK = HD / 16;             // K steps of Q K^T
   constexpr int DQ = HD / 4;              // head-dimension elements per thread in Q K^T
   constexpr int QW = DQ / 2;              // 32-bit words of 16-bit values per thread and head
   constexpr int KW = DQ * GE::ESZ / 4;    // 32-bit words of one K row slice per thread
-  constexpr int MT = HD / 64;             // 16-row blocks of the head dimension per warp in P V
-  constexpr int DV = HD == 128 ? 4 : 2;   // head-dimension elements per thread in P V
+  constexpr int MT = C::MTW;              // 16-row blocks of the head dimension per warp in P V
+  constexpr int DV = 2 * MT;              // head-dimension elements per thread in P V
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -665,6 +682,10 @@ attn_decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_co
   volatile int* stop = abort_flag + 1;
   const int g = lane >> 2;        // MMA row group
   const int c = lane & 3;         // thread in group
+  const int kblk = warp & 3;      // Q K^T: key block of the tile
+  const int nt0 = (warp >> 2) * NTW;                         // Q K^T: first column block
+  const int mblk = warp % (C::MB / MT);                      // P V: first row block (of MT)
+  const int pt0 = (warp / (C::MB / MT)) * NTP;               // P V: first column block
   int it = 0;
   for (int w = blockIdx.x; w < total; w += gridDim.x) {
     const decode::Work wk = decode::decode_work(w, split, B, Hkv, chunk, seqlens);
@@ -673,12 +694,12 @@ attn_decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_co
     // order 2, 3, 0, 1 (for K and, identically, for Q), so that the K loads of
     // threads c and c + 2, which read different slabs, fall into different banks
     const int rot = (GE::ROW == 256) ? 2 * (c >> 1) : 0;
-    // ---- Q^T fragments: thread (g, c) holds head 8 nt + g, elements [c DQ, (c+1) DQ)
-    uint32_t qf[NT][QW];
-    float qsc[NT][2];             // fp8 cache: the score scales of heads 8 nt + 2c, + 1
+    // ---- Q^T fragments: thread (g, c) holds head 8 (nt0 + nt) + g, elements [c DQ, (c+1) DQ)
+    uint32_t qf[NTW][QW];
+    float qsc[NTW][2];            // fp8 cache: the score scales of heads 8 (nt0 + nt) + 2c, + 1
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const int h = 8 * nt + g;
+    for (int nt = 0; nt < NTW; ++nt) {
+      const int h = 8 * (nt0 + nt) + g;
       uint32_t raw[QW];
       if (h < G) {
         const uint4* src = reinterpret_cast<const uint4*>(q + (static_cast<size_t>(wk.b) * Hq + h0 + h) * HD + c * DQ);
@@ -731,7 +752,7 @@ attn_decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_co
       uint32_t ka[2][KW];
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
-        const int row = 16 * warp + g + 8 * r;
+        const int row = 16 * kblk + g + 8 * r;
 #pragma unroll
         for (int j = 0; j < KW / 4; ++j) {
           const uint4 u = *reinterpret_cast<const uint4*>(tile + tile_off<HD, KV8>(row, c * DQ * GE::ESZ + 16 * (j ^ rot)));
@@ -741,9 +762,9 @@ attn_decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_co
           ka[r][4 * j + 3] = u.w;
         }
       }
-      float acc[NT][4];
+      float acc[NTW][4];
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+      for (int nt = 0; nt < NTW; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
 #pragma unroll
       for (int kk = 0; kk < KK; ++kk) {
         // MMA K index 2c + {0, 1} -> d = c DQ + 4 kk + {0, 1}; 2c + 8 + {0, 1} -> + {2, 3}
@@ -760,18 +781,18 @@ attn_decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_co
           a3 = ka[1][2 * kk + 1];
         }
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma16816<KV8>(acc[nt], a0, a1, a2, a3, qf[nt][2 * kk], qf[nt][2 * kk + 1]);
+        for (int nt = 0; nt < NTW; ++nt) mma16816<KV8>(acc[nt], a0, a1, a2, a3, qf[nt][2 * kk], qf[nt][2 * kk + 1]);
       }
       // the MMAs above have consumed every value this warp read from the slot
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_empty(s));
-      // acc[nt] = S^T: rows keys 16 warp + g (+8), columns heads 8 nt + 2c (+1)
+      // acc[nt] = S^T: rows keys 16 kblk + g (+8), columns heads 8 (nt0 + nt) + 2c (+1)
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
+      for (int nt = 0; nt < NTW; ++nt) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int h = 8 * nt + 2 * c + (e & 1);
-          const int key = tl * TILE + 16 * warp + g + 8 * (e >> 1);
+          const int h = 8 * (nt0 + nt) + 2 * c + (e & 1);
+          const int key = tl * TILE + 16 * kblk + g + 8 * (e >> 1);
           if (h < G) work[h * wstride + key] = key < wk.n_valid ? acc[nt][e] * qsc[nt][e & 1] : -CUDART_INF_F;
         }
       }
@@ -800,13 +821,14 @@ attn_decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_co
       }
     }
     asm volatile("bar.sync 1, %0;" ::"n"(NC) : "memory");
-    // ---- phase 3: O^T = V^T P^T for head-dimension rows [warp DQ, (warp+1) DQ)
-    float oacc[MT][NT][4];
+    // ---- phase 3: O^T = V^T P^T for head-dimension rows [16 MT mblk, +16 MT) and column
+    // blocks [pt0, pt0 + NTP)
+    float oacc[MT][NTP][4];
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) oacc[mt][nt][0] = oacc[mt][nt][1] = oacc[mt][nt][2] = oacc[mt][nt][3] = 0.f;
-    const int dbase = warp * DQ + DV * g;   // this thread's head-dimension elements dbase .. + DV - 1
+      for (int nt = 0; nt < NTP; ++nt) oacc[mt][nt][0] = oacc[mt][nt][1] = oacc[mt][nt][2] = oacc[mt][nt][3] = 0.f;
+    const int dbase = mblk * 16 * MT + DV * g;   // this thread's head-dimension elements dbase .. + DV - 1
     for (int tl = 0; tl < wk.ntl; ++tl, ++it) {
       const int s = it % STAGES;
       ok = ok && __all_sync(0xffffffffu, mbar_wait(bar_full(s), (it / STAGES) & 1, abort_flag, err));
@@ -854,10 +876,10 @@ attn_decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_co
             af[mt][2 * pr + 1] = hi;
           }
         }
-        // B fragments: P^T, keys (2c, 2c+1) and (2c+8, 2c+9) of head 8 nt + g
+        // B fragments: P^T, keys (2c, 2c+1) and (2c+8, 2c+9) of head 8 (pt0 + nt) + g
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          const int h = 8 * nt + g;
+        for (int nt = 0; nt < NTP; ++nt) {
+          const int h = 8 * (pt0 + nt) + g;
           uint32_t b0 = 0u, b1 = 0u;
           if (h < G) {
             const float* ph = work + h * wstride + tl * TILE + 16 * ks + 2 * c;
@@ -883,10 +905,10 @@ attn_decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_co
     {
       const size_t base = (static_cast<size_t>(wk.b) * Hq + h0) * S_max + wk.c;
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
+      for (int nt = 0; nt < NTP; ++nt) {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const int h = 8 * nt + 2 * c + e;
+          const int h = 8 * (pt0 + nt) + 2 * c + e;
           if (h >= G) continue;
           const float sc = v_scale / st_l[h];
           float* dst = ws_o + (base + static_cast<size_t>(h) * S_max) * HD + dbase;
@@ -1030,11 +1052,11 @@ int launch_mma(const CUtensorMap& tk, const CUtensorMap& tv, const void* q, cons
   static KernelSetup setup;
   int n = 0;
   if (const int rc = prepare_kernel(setup, decode_mma::attn_decode_mma_kernel<HDIM, G, PAGED, KV8>, smem,
-                                    decode_mma::NTHREADS, &n);
+                                    C::NTHREADS, &n);
       rc != ATTN_OK)
     return rc;
   const int resident = n < 1 ? 1 : (n > C::CTAS_PER_SM ? C::CTAS_PER_SM : n);
-  decode_mma::attn_decode_mma_kernel<HDIM, G, PAGED, KV8><<<resident * num_sms, decode_mma::NTHREADS, smem, stream>>>(
+  decode_mma::attn_decode_mma_kernel<HDIM, G, PAGED, KV8><<<resident * num_sms, C::NTHREADS, smem, stream>>>(
       tk, tv, static_cast<const __nv_bfloat16*>(q), seqlens, ws_o, ws_lse, B, Hq, Hkv, Nk_max, chunk, S_max,
       scale * k_scale * 1.4426950408889634f, v_scale, err, pg, stages);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
