@@ -3,14 +3,20 @@
 // Follows "Agent 帮我写 CUDA：一个 Softmax Attention 算子的开发全记录": the tiled
 // kernel of section 四 (a block owns a tile of query rows, loops over K/V tiles
 // held in shared memory and merges the online-softmax state across tiles), the
-// 16-byte vector loads and padded shared-memory rows of section 五, and the
-// head-dimension-specific compilation of section 六 (one instantiation per D).
-// Differences for sm_103a: K/V tiles are double-buffered with cp.async so the
-// next tile streams in while the current one is used, each thread computes a
-// 4x4 block of scores (register tiling instead of one warp per row), and the
-// softmax statistics are reduced with half-warp shuffles.  Exponentials use the
-// exp2 form: 2^(s*scale*log2 e - m).  No TF32 or other reduced-precision
-// arithmetic is used.
+// 16-byte vector loads of section 五, and the head-dimension-specific
+// compilation of section 六 (one instantiation per D).  Differences for sm_103a:
+//   * each thread computes a 4x4 block of scores and a 4 x D/16 block of O
+//     (register tiling instead of one warp per row); the softmax statistics are
+//     reduced with half-warp shuffles;
+//   * two CTAs share an SM (16 warps), so each keeps its shared memory to 112 KB
+//     at D = 128: one K and one V buffer, filled by cp.async one phase ahead
+//     (K of the next tile streams in during the softmax and P V of this tile, V
+//     of the next tile during the next Q K^T), no padding.  Instead of the padded
+//     rows of section 五, the 16-byte chunks of each K row are XOR-swizzled by the
+//     row index, so the 16 K rows that a half-warp reads at one column fall into
+//     different banks; Q, V and P reads are broadcasts or contiguous;
+//   * exponentials use the exp2 form 2^(s*scale*log2 e - m).
+// No TF32 or other reduced-precision arithmetic is used.
 #include <cuda_runtime.h>
 #include <math_constants.h>
 
@@ -26,15 +32,21 @@ constexpr int NT = 256;  // threads: 16 row groups x 16 column groups
 
 template <int D>
 struct Smem {
-  static constexpr int LD = D + 4;  // padded row (floats) — conflict-free 16-byte reads
-  static constexpr int PLD = BN + 4;
-  static constexpr int Q = 0;
-  static constexpr int K = Q + BM * LD;           // two buffers
-  static constexpr int V = K + 2 * BN * LD;       // two buffers
-  static constexpr int P = V + 2 * BN * LD;
-  static constexpr int FLOATS = P + BM * PLD;
+  static constexpr int Q = 0;                    // [BM][D]
+  static constexpr int K = Q + BM * D;           // [BN][D], 16-byte chunks swizzled
+  static constexpr int V = K + BN * D;           // [BN][D]
+  static constexpr int P = V + BN * D;           // [BM][BN]
+  static constexpr int FLOATS = P + BM * BN;
   static constexpr int BYTES = FLOATS * 4;
+  static constexpr int CHUNKS = D / 4;           // 16-byte chunks per row
+  static constexpr int SWZ = CHUNKS < 16 ? CHUNKS - 1 : 15;
 };
+
+// Float offset of the 16-byte chunk `c` of K row `r` (swizzled by the row).
+template <int D>
+__device__ __forceinline__ int k_off(int r, int c) {
+  return r * D + ((c ^ (r & Smem<D>::SWZ)) << 2);
+}
 
 __device__ __forceinline__ void cp_async16(float* dst, const float* src, bool valid) {
   const uint32_t d = smem_u32(dst);
@@ -42,35 +54,37 @@ __device__ __forceinline__ void cp_async16(float* dst, const float* src, bool va
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src), "r"(n) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-// rows [row0, row0+64) of a [N, D] head into smem with leading dimension LD
-template <int D>
+// rows [row0, row0+64) of a [N, D] head into shared memory ([64][D]; K rows swizzled)
+template <int D, bool SWIZZLE>
 __device__ __forceinline__ void load_rows(float* dst, const float* head, int row0, int N) {
-  constexpr int LD = Smem<D>::LD;
   constexpr int VEC = D / 4;  // float4 per row
   for (int i = threadIdx.x; i < 64 * VEC; i += NT) {
-    const int r = i / VEC, c = (i % VEC) * 4;
+    const int r = i / VEC, c = i % VEC;
     const int gr = row0 + r;
     const bool valid = gr < N;
-    cp_async16(dst + r * LD + c, head + static_cast<size_t>(valid ? gr : 0) * D + c, valid);
+    float* d = SWIZZLE ? dst + k_off<D>(r, c) : dst + r * D + c * 4;
+    cp_async16(d, head + static_cast<size_t>(valid ? gr : 0) * D + c * 4, valid);
   }
 }
 
 template <int D>
-__global__ void __launch_bounds__(NT) attn_fwd_fp32_kernel(const float* __restrict__ Q,
-                                                          const float* __restrict__ K,
-                                                          const float* __restrict__ V,
-                                                          float* __restrict__ O,
-                                                          float* __restrict__ LSE, int Hq, int Hkv,
-                                                          int Nq, int Nk, float c, int causal,
-                                                          int window) {
+__global__ void __launch_bounds__(NT, 2) attn_fwd_fp32_kernel(const float* __restrict__ Q,
+                                                             const float* __restrict__ K,
+                                                             const float* __restrict__ V,
+                                                             float* __restrict__ O,
+                                                             float* __restrict__ LSE, int Hq, int Hkv,
+                                                             int Nq, int Nk, float c, int causal,
+                                                             int window) {
   using S = Smem<D>;
-  constexpr int LD = S::LD, PLD = S::PLD;
   constexpr int DC = D / 16;  // output columns per thread
   extern __shared__ float4 smem4[];
   float* sm = reinterpret_cast<float*>(smem4);
   float* Qs = sm + S::Q;
+  float* Ks = sm + S::K;
+  float* Vs = sm + S::V;
   float* Ps = sm + S::P;
 
   const int tid = threadIdx.x, ty = tid / 16, tx = tid % 16;
@@ -95,11 +109,15 @@ __global__ void __launch_bounds__(NT) attn_fwd_fp32_kernel(const float* __restri
   const int tile_hi_min = causal ? min(q0 + off, Nk - 1) : Nk - 1;
   const int tile_lo_max = window > 0 ? q0 + BM - 1 + off - window + 1 : 0;
 
+  // cp.async groups in issue order: {Q, K_0}, {V_0}, then per tile j: {K_j+1} after
+  // Q K^T_j and {V_j+1} after P V_j.  Waiting for all but the newest group therefore
+  // always completes the buffer about to be read.
   if (n_tiles > 0) {
-    load_rows<D>(Qs, Qh, q0, Nq);
-    load_rows<D>(sm + S::K, Kh, j_begin * BN, Nk);
-    load_rows<D>(sm + S::V, Vh, j_begin * BN, Nk);
+    load_rows<D, false>(Qs, Qh, q0, Nq);
+    load_rows<D, true>(Ks, Kh, j_begin * BN, Nk);
   }
+  cp_async_commit();
+  if (n_tiles > 0) load_rows<D, false>(Vs, Vh, j_begin * BN, Nk);
   cp_async_commit();
 
   float m[4], l[4], acc[4][DC];
@@ -112,16 +130,8 @@ __global__ void __launch_bounds__(NT) attn_fwd_fp32_kernel(const float* __restri
   }
 
   for (int jj = 0; jj < n_tiles; ++jj) {
-    const int buf = jj & 1;
-    const float* Ks = sm + S::K + buf * BN * LD;
-    const float* Vs = sm + S::V + buf * BN * LD;
-    cp_async_wait_all();
-    __syncthreads();  // tile jj visible; everyone is done with tile jj-1
-    if (jj + 1 < n_tiles) {
-      load_rows<D>(sm + S::K + (buf ^ 1) * BN * LD, Kh, (j_begin + jj + 1) * BN, Nk);
-      load_rows<D>(sm + S::V + (buf ^ 1) * BN * LD, Vh, (j_begin + jj + 1) * BN, Nk);
-    }
-    cp_async_commit();
+    cp_async_wait<1>();
+    __syncthreads();  // K_j (and Q) visible; everyone is done with P V_j-1 (P buffer free)
 
     // ---- scores: rows ty*4+i, keys tx+16*n
     float s[4][4];
@@ -133,9 +143,9 @@ __global__ void __launch_bounds__(NT) attn_fwd_fp32_kernel(const float* __restri
     for (int d = 0; d < D; d += 4) {
       float4 qv[4], kv[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) qv[i] = *reinterpret_cast<const float4*>(Qs + (ty * 4 + i) * LD + d);
+      for (int i = 0; i < 4; ++i) qv[i] = *reinterpret_cast<const float4*>(Qs + (ty * 4 + i) * D + d);
 #pragma unroll
-      for (int n = 0; n < 4; ++n) kv[n] = *reinterpret_cast<const float4*>(Ks + (tx + 16 * n) * LD + d);
+      for (int n = 0; n < 4; ++n) kv[n] = *reinterpret_cast<const float4*>(Ks + k_off<D>(tx + 16 * n, d >> 2));
 #pragma unroll
       for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -146,6 +156,10 @@ __global__ void __launch_bounds__(NT) attn_fwd_fp32_kernel(const float* __restri
           s[i][n] = fmaf(qv[i].w, kv[n].w, s[i][n]);
         }
     }
+    __syncthreads();  // everyone is done with K_j: stream K_j+1 in during the softmax and P V
+    if (jj + 1 < n_tiles) load_rows<D, true>(Ks, Kh, (j_begin + jj + 1) * BN, Nk);
+    cp_async_commit();
+
     const int k0 = (j_begin + jj) * BN;
     const bool need_mask = (k0 + BN - 1 > tile_hi_min) || (k0 < tile_lo_max);
 #pragma unroll
@@ -176,7 +190,7 @@ __global__ void __launch_bounds__(NT) attn_fwd_fp32_kernel(const float* __restri
       for (int n = 0; n < 4; ++n) {
         const float pv = ex2_approx(s[i][n] - m_use);
         sum += pv;
-        Ps[(ty * 4 + i) * PLD + tx + 16 * n] = pv;
+        Ps[(ty * 4 + i) * BN + tx + 16 * n] = pv;
       }
 #pragma unroll
       for (int o = 8; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
@@ -184,17 +198,18 @@ __global__ void __launch_bounds__(NT) attn_fwd_fp32_kernel(const float* __restri
 #pragma unroll
       for (int d = 0; d < DC; ++d) acc[i][d] *= alpha;
     }
-    __syncthreads();  // P tile complete
+    cp_async_wait<1>();
+    __syncthreads();  // P tile complete; V_j visible
 
-    // ---- O += P V: rows ty*4+i, columns (see col())
+    // ---- O += P V: rows ty*4+i, columns tx*4.. (+64 for D = 128), or tx*2.. for D = 32
 #pragma unroll 2
     for (int kk = 0; kk < BN; kk += 4) {
       float4 pr[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) pr[i] = *reinterpret_cast<const float4*>(Ps + (ty * 4 + i) * PLD + kk);
+      for (int i = 0; i < 4; ++i) pr[i] = *reinterpret_cast<const float4*>(Ps + (ty * 4 + i) * BN + kk);
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const float* vrow = Vs + (kk + u) * LD;
+        const float* vrow = Vs + (kk + u) * D;
         float vv[DC];
         if constexpr (DC == 8) {
           const float4 a = *reinterpret_cast<const float4*>(vrow + tx * 4);
@@ -216,8 +231,11 @@ __global__ void __launch_bounds__(NT) attn_fwd_fp32_kernel(const float* __restri
         }
       }
     }
+    __syncthreads();  // everyone is done with V_j: stream V_j+1 in during the next Q K^T
+    if (jj + 1 < n_tiles) load_rows<D, false>(Vs, Vh, (j_begin + jj + 1) * BN, Nk);
+    cp_async_commit();
   }
-  cp_async_wait_all();
+  cp_async_wait<0>();
 
   // ---- epilogue
 #pragma unroll
