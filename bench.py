@@ -64,7 +64,7 @@ VARLEN = dict(B=32, Hq=32, Hkv=8, D=128, n_lo=512, n_hi=8192, causal=True)
 # fp32 configurations: B=2 H=4 N=64 D=32, then the B=2 H=8 sweep over N x D
 FP32_POINTS = [(2, 4, 64, 32)] + [(2, 8, n, d) for n in (64, 256, 1024, 4096) for d in (32, 64, 128)]
 SHORT = {"paged": "paged_dec", "decode_fp8": "fp8kv_dec", "decode_mqa": "mqa_dec", "decode_d64": "d64_dec", "window": "window4k", "chunked": "chunked",
-         "d64": "d64", "fp16": "fp16", "varlen": "varlen", "softcap": "softcap", "bwd": "bwd",
+         "d64": "d64", "fp16": "fp16", "varlen": "varlen", "softcap": "softcap", "bwd": "bwd", "bwd_d64": "bwd_d64",
          "fp32": "fp32", "dense": "dense"}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FP32_SIMT_FLOP_PER_CLK_SM = 256.0   # 128 FP32 lanes x 2 (fused multiply-add)
@@ -101,7 +101,7 @@ def parse_args():
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--workload", choices=["dense", "causal", "decode", "fp32", "window", "chunked", "d64",
                                            "paged", "fp16", "varlen", "decode_fp8", "softcap", "bwd",
-                                           "decode_mqa", "decode_d64"],
+                                           "decode_mqa", "decode_d64", "bwd_d64"],
                     default="dense",
                     help="workload of the timed loop (default: the dense bf16 prefill)")
     ap.add_argument("--no-extras", action="store_true", help="skip the other workloads")
@@ -367,6 +367,7 @@ WORKLOAD_NAMES = {
     "decode_mqa": "bf16 multi-query split-KV decode B=128 Hq=32 Hkv=1 D=128, Nk_b~U[512,32768], chunk 512",
     "decode_d64": "bf16 split-KV decode B=64 Hq=32 Hkv=8 D=64, Nk_b~U[512,32768], chunk 512",
     "bwd": "bf16 backward (dQ, dK, dV) B=1 H=32 N=8192 D=128 (non-causal); FLOPs = 2.5 x forward",
+    "bwd_d64": "bf16 backward (dQ, dK, dV) B=1 H=32 N=8192 D=64 (non-causal); FLOPs = 2.5 x forward",
 }
 
 
@@ -375,8 +376,8 @@ def make_workload(name, dev, seed, peaks, peak_src, sm_max_mhz, decode_batch=Non
     import torch
     from softmax_attention_attn_gb300 import binding, inputs
     w = {"name": name, "desc": WORKLOAD_NAMES[name]}
-    if name == "bwd":
-        c = MAIN
+    if name in ("bwd", "bwd_d64"):
+        c = MAIN if name == "bwd" else DENSE64
         host = inputs.prefill_inputs(c["B"], c["Hq"], c["Hkv"], c["N"], c["N"], c["D"], "bf16", seed)
         q, k, v = (x.to(dev) for x in host)
         do = torch.randn(c["B"], c["Hq"], c["N"], c["D"], generator=torch.Generator("cpu").manual_seed(seed + 9))
@@ -761,7 +762,7 @@ def run_gb300(args, rank, world, local_rank):
     if not args.no_extras:
         xs = max(5, min(args.steps // 10, 50))
         for name in ("dense", "causal", "decode", "paged", "decode_fp8", "decode_mqa", "decode_d64", "window",
-                     "chunked", "d64", "fp16", "varlen", "softcap", "bwd"):
+                     "chunked", "d64", "fp16", "varlen", "softcap", "bwd", "bwd_d64"):
             if name == args.workload:
                 continue
             x = make_workload(name, dev, rank, peaks, peak_src, sm_max, args.decode_batch)

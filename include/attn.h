@@ -225,7 +225,7 @@ size_t attn_bwd_workspace_size(int B, int Hq, int Nq);
  *   workspace  : device buffer of attn_bwd_workspace_size(B, Hq, Nq) bytes
  *   causal, window : the forward's masks, as in attn_fwd (bottom-right causal;
  *                window > 0 keeps the last `window` keys up to the diagonal)
- *   D must be 128.  All device pointers 16-byte aligned, contiguous; the
+ *   D must be 64 or 128.  All device pointers 16-byte aligned, contiguous; the
  *   caller owns every buffer.  Asynchronous on `stream`.
  *   Errors: ATTN_ERR_NULL, ATTN_ERR_DIM, ATTN_ERR_GQA, ATTN_ERR_HEAD_DIM,
  *   ATTN_ERR_ALIGN, ATTN_ERR_SCALE, ATTN_ERR_CUDA; a bounded wait that runs

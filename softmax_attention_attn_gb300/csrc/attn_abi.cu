@@ -256,7 +256,7 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
   if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || !workspace) return ATTN_ERR_NULL;
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || Nq <= 0 || Nk <= 0 || D <= 0) return ATTN_ERR_DIM;
   if (Hq % Hkv != 0) return ATTN_ERR_GQA;
-  if (D != 128) return ATTN_ERR_HEAD_DIM;
+  if (D != 64 && D != 128) return ATTN_ERR_HEAD_DIM;
   if (static_cast<long long>(B) * Hq * Nq > (1ll << 31) || static_cast<long long>(B) * Hkv > 65535 ||
       B > 65535)
     return ATTN_ERR_DIM;
@@ -267,8 +267,8 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
   DeviceInfo* dev = nullptr;
   int rc = device_info(&dev);
   if (rc != ATTN_OK) return rc;
-  return launch_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, B, Hq, Hkv, Nq, Nk, scale, causal, window,
-                    reinterpret_cast<cudaStream_t>(stream), dev->err);
+  return launch_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, B, Hq, Hkv, Nq, Nk, D, scale, causal,
+                    window, reinterpret_cast<cudaStream_t>(stream), dev->err);
 }
 
 int attn_decode_splitkv_fp8(const void* q, const void* k_cache, const void* v_cache, float k_scale,

@@ -54,25 +54,16 @@
 namespace attn {
 namespace bwd {
 
-constexpr int HD = 128;
 constexpr int BK = 128;                          // keys per CTA
 constexpr int BQ = 128;                          // queries per step
 constexpr int NS = 2;                            // Q / dO ring stages
 constexpr int KSLAB = BK * 128;                  // 64-column slab of a 128-row tile (16 KB)
 constexpr int QSLAB = BQ * 128;                  // 64-column slab of a 128-row tile (16 KB)
-constexpr int SM_K = 0;
-constexpr int SM_V = SM_K + 2 * KSLAB;
-constexpr int SM_STAGE = SM_V + 2 * KSLAB;
-constexpr int STAGE_BYTES = 4 * QSLAB;           // Q_i (2 slabs) + dO_i (2 slabs)
-constexpr int SM_DS = SM_STAGE + NS * STAGE_BYTES;  // dS^T [128 keys][128 queries] bf16, 2 slabs
-constexpr int SM_BIG = SM_DS + 2 * KSLAB;        // end of the operand block
 constexpr int VEC_BYTES = 2 * BQ * 4;            // -LSE*log2(e)[128], -scale*D[128]
 constexpr int NUM_BARS = 1 + 2 * NS + 8;
 constexpr int SMALL_BYTES = 128;                 // barriers + misc words
 static_assert(NUM_BARS * 8 + 16 <= SMALL_BYTES, "small block");
 constexpr int SMEM_ALLOC = 227 * 1024;
-static_assert(SM_BIG + 1023 + NS * VEC_BYTES <= SMEM_ALLOC, "operand block + vectors, small block in front");
-static_assert(SM_BIG + SMALL_BYTES - 1 + SMALL_BYTES + NS * VEC_BYTES <= SMEM_ALLOC, "everything behind");
 constexpr int NROW = 8;                          // row warps 0..7: lane quad = warp % 4, query half = warp / 4
 constexpr int WARP_TMA = 8;
 constexpr int WARP_MMA = 9;
@@ -88,9 +79,27 @@ constexpr uint32_t idesc(uint32_t M, uint32_t N, uint32_t a_mn, uint32_t b_mn) {
          ((M >> 4) << 24);
 }
 constexpr uint32_t ID_ST = idesc(BK, BQ, 0, 0);   // S^T, dP^T: K / V and Q / dO, both K-major
-constexpr uint32_t ID_GRAD = idesc(BK, HD, 0, 1); // dV, dK: P^T (TMEM) / dS^T (smem, K-major), dO / Q MN-major
-constexpr uint32_t ID_DQ = idesc(BQ, HD, 1, 1);   // dQ: dS (from dS^T) and K, both MN-major
-static_assert(BQ == 128 && BK == 128 && HD == 128, "tile shapes");
+static_assert(BQ == 128 && BK == 128, "tile shapes");
+
+// Shared-memory layout and head-dimension-dependent MMA shapes for head dimension HD
+// (64 or 128): K_j, V_j and each stage's Q_i, dO_i are HD / 64 slabs of 64 columns.
+template <int HD>
+struct Lay {
+  static_assert(HD == 64 || HD == 128, "head dimension");
+  static constexpr int SLABS = HD / 64;
+  static constexpr int SM_K = 0;
+  static constexpr int SM_V = SM_K + SLABS * KSLAB;
+  static constexpr int SM_STAGE = SM_V + SLABS * KSLAB;
+  static constexpr int STAGE_BYTES = 2 * SLABS * QSLAB;     // Q_i + dO_i
+  static constexpr int SM_DS = SM_STAGE + NS * STAGE_BYTES; // dS^T [128 keys][128 queries] bf16, 2 slabs
+  static constexpr int SM_BIG = SM_DS + 2 * KSLAB;          // end of the operand block
+  static constexpr uint32_t ID_GRAD = idesc(BK, HD, 0, 1);  // dV, dK: P^T (TMEM) / dS^T (smem, K-major), dO / Q MN-major
+  static constexpr uint32_t ID_DQ = idesc(BQ, HD, 1, 1);    // dQ: dS (from dS^T) and K, both MN-major
+  static_assert(SM_BIG + 1023 + NS * VEC_BYTES <= SMEM_ALLOC, "operand block + vectors, small block in front");
+  static_assert(SM_BIG + SMALL_BYTES - 1 + SMALL_BYTES + NS * VEC_BYTES <= SMEM_ALLOC, "everything behind");
+  // the dQ of a step, staged as fp32 32 x 32 boxes (HD / 32 per lane quarter), fits a finished stage
+  static_assert(4 * (HD / 32) * 32 * 128 <= STAGE_BYTES, "dQ staging");
+};
 
 __device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t off16) {
   uint32_t lo, hi;
@@ -126,6 +135,7 @@ struct BwdParams {
 // -scale * D (D = rowsum(dO * O)) and -LSE * log2(e) per query row, padded to
 // 128 rows per head, negated so that the main kernel needs one fused
 // multiply-add per score.
+template <int HD>
 __global__ void __launch_bounds__(256)
 attn_bwd_prep_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
                      const float* __restrict__ lse, float* __restrict__ nlse2, float* __restrict__ ndelta,
@@ -142,14 +152,23 @@ attn_bwd_prep_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* _
     }
     return;
   }
-  const long long src = (bh * Nq + i) * HD + lane * 4;
-  const uint2 uo = *reinterpret_cast<const uint2*>(o + src);
-  const uint2 ud = *reinterpret_cast<const uint2*>(dout + src);
-  const float o4[4] = {__uint_as_float(uo.x << 16), __uint_as_float(uo.x & 0xFFFF0000u),
-                       __uint_as_float(uo.y << 16), __uint_as_float(uo.y & 0xFFFF0000u)};
-  const float d4[4] = {__uint_as_float(ud.x << 16), __uint_as_float(ud.x & 0xFFFF0000u),
-                       __uint_as_float(ud.y << 16), __uint_as_float(ud.y & 0xFFFF0000u)};
-  float s = (o4[0] * d4[0] + o4[1] * d4[1]) + (o4[2] * d4[2] + o4[3] * d4[3]);
+  float s;
+  if constexpr (HD == 128) {   // four elements per lane
+    const long long src = (bh * Nq + i) * HD + lane * 4;
+    const uint2 uo = *reinterpret_cast<const uint2*>(o + src);
+    const uint2 ud = *reinterpret_cast<const uint2*>(dout + src);
+    const float o4[4] = {__uint_as_float(uo.x << 16), __uint_as_float(uo.x & 0xFFFF0000u),
+                         __uint_as_float(uo.y << 16), __uint_as_float(uo.y & 0xFFFF0000u)};
+    const float d4[4] = {__uint_as_float(ud.x << 16), __uint_as_float(ud.x & 0xFFFF0000u),
+                         __uint_as_float(ud.y << 16), __uint_as_float(ud.y & 0xFFFF0000u)};
+    s = (o4[0] * d4[0] + o4[1] * d4[1]) + (o4[2] * d4[2] + o4[3] * d4[3]);
+  } else {                     // two elements per lane
+    const long long src = (bh * Nq + i) * HD + lane * 2;
+    const uint32_t uo = *reinterpret_cast<const uint32_t*>(o + src);
+    const uint32_t ud = *reinterpret_cast<const uint32_t*>(dout + src);
+    s = __uint_as_float(uo << 16) * __uint_as_float(ud << 16) +
+        __uint_as_float(uo & 0xFFFF0000u) * __uint_as_float(ud & 0xFFFF0000u);
+  }
 #pragma unroll
   for (int k = 16; k >= 1; k >>= 1) s += __shfl_xor_sync(0xffffffffu, s, k);
   if (lane == 0) {
@@ -159,10 +178,16 @@ attn_bwd_prep_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* _
   }
 }
 
+template <int HD>
 __global__ void __launch_bounds__(NTHREADS, 1)
 attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                 const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
+  using LY = Lay<HD>;
+  constexpr int SLABS = LY::SLABS;
+  constexpr int SM_K = LY::SM_K, SM_V = LY::SM_V, SM_STAGE = LY::SM_STAGE, STAGE_BYTES = LY::STAGE_BYTES;
+  constexpr int SM_DS = LY::SM_DS, SM_BIG = LY::SM_BIG;
+  constexpr uint32_t ID_GRAD = LY::ID_GRAD, ID_DQ = LY::ID_DQ;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
@@ -253,8 +278,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       tma_prefetch_desc(&tm_do);
-      mbar_arrive_expect_tx(bar_kv_full, 4 * KSLAB);
-      for (int kb = 0; kb < 2; ++kb) {
+      mbar_arrive_expect_tx(bar_kv_full, 2 * SLABS * KSLAB);
+      for (int kb = 0; kb < SLABS; ++kb) {
         tma_load_3d(sb + SM_K + kb * KSLAB, &tm_k, bar_kv_full, kb * 64, j0, b * p.Hkv + kvh);
         tma_load_3d(sb + SM_V + kb * KSLAB, &tm_v, bar_kv_full, kb * 64, j0, b * p.Hkv + kvh);
       }
@@ -270,9 +295,9 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const uint32_t st = sb + SM_STAGE + s * STAGE_BYTES;
         const uint32_t vec = svec + s * VEC_BYTES;
         mbar_arrive_expect_tx(bar_q_full(s), STAGE_BYTES + VEC_BYTES);
-        for (int kb = 0; kb < 2; ++kb) {
+        for (int kb = 0; kb < SLABS; ++kb) {
           tma_load_3d(st + kb * QSLAB, &tm_q, bar_q_full(s), kb * 64, i0, b * p.Hq + h);
-          tma_load_3d(st + 2 * QSLAB + kb * QSLAB, &tm_do, bar_q_full(s), kb * 64, i0, b * p.Hq + h);
+          tma_load_3d(st + SLABS * QSLAB + kb * QSLAB, &tm_do, bar_q_full(s), kb * 64, i0, b * p.Hq + h);
         }
         const size_t vrow = (static_cast<size_t>(b) * p.Hq + h) * p.Nq_pad + i0;
         bulk_load(vec, p.nlse2 + vrow, BQ * 4, bar_q_full(s));
@@ -296,9 +321,9 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const int s = step % NS;
         const uint32_t st = sb + SM_STAGE + s * STAGE_BYTES;
         const uint64_t q_kmaj = smem_desc_sw128(st, 16, 1024);
-        const uint64_t do_kmaj = smem_desc_sw128(st + 2 * QSLAB, 16, 1024);
+        const uint64_t do_kmaj = smem_desc_sw128(st + SLABS * QSLAB, 16, 1024);
         const uint64_t q_mn = smem_desc_sw128(st, QSLAB, 1024);
-        const uint64_t do_mn = smem_desc_sw128(st + 2 * QSLAB, QSLAB, 1024);
+        const uint64_t do_mn = smem_desc_sw128(st + SLABS * QSLAB, QSLAB, 1024);
         if (!mbar_wait(bar_q_full(s), (step / NS) & 1, abort_flag, p.err)) { ok = false; break; }
         tc_fence_after();
         // S^T = K_j Q_i^T (over P^T of the previous step: the dV MMA that read it came first)
@@ -373,14 +398,14 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         ok = __all_sync(0xffffffffu, mbar_wait(bar_dq_full, step & 1, abort_flag, p.err));
         if (!ok) break;
         tc_fence_after();
-        uint8_t* box0 = smem + SM_STAGE + s * STAGE_BYTES + quad * (4 * 32 * 128);
+        uint8_t* box0 = smem + SM_STAGE + s * STAGE_BYTES + quad * ((HD / 32) * 32 * 128);
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
+        for (int hh = 0; hh < HD / 64; ++hh) {
           uint32_t qr[2][32];
           tmem_ld32(tmem + lane_sel + COL_DQ + 64 * hh, qr[0]);
           tmem_ld32(tmem + lane_sel + COL_DQ + 64 * hh + 32, qr[1]);
           tmem_wait_ld();
-          if (hh == 1) {  // the columns are free for the next dP^T
+          if (hh == HD / 64 - 1) {  // the columns are free for the next dP^T
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_dq_empty);
@@ -398,7 +423,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           // rows past the sequence end fall outside the map and are skipped
           if (i0 + quad * 32 < p.Nq) {
 #pragma unroll
-            for (int bx = 0; bx < 4; ++bx)
+            for (int bx = 0; bx < HD / 32; ++bx)
               tma_reduce_add_3d(&tm_dq, smem_u32(box0 + bx * (32 * 128)), bx * 32, i0 + quad * 32, b * p.Hq + h);
           }
           bulk_commit_group();
@@ -543,18 +568,20 @@ size_t bwd_workspace_bytes(int B, int Hq, int Nq) {
   return 2 * static_cast<size_t>(B) * Hq * nq_pad * sizeof(float);
 }
 
-int launch_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
-               const float* lse, float* dq, void* dk, void* dv, void* workspace, int B, int Hq,
-               int Hkv, int Nq, int Nk, float scale, int causal, int window, cudaStream_t stream,
-               int* err) {
-  using namespace bwd;
+namespace bwd {
+
+template <int HD>
+int launch_bwd_hd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                  const float* lse, float* dq, void* dk, void* dv, void* workspace, int B, int Hq,
+                  int Hkv, int Nq, int Nk, float scale, int causal, int window, cudaStream_t stream,
+                  int* err) {
   const int nq_pad = (Nq + BQ - 1) / BQ * BQ;
   const long long rows_pad = static_cast<long long>(B) * Hq * nq_pad;
   float* nlse2 = static_cast<float*>(workspace);
   float* ndelta = nlse2 + rows_pad;
   if (cudaMemsetAsync(dq, 0, static_cast<size_t>(B) * Hq * Nq * HD * sizeof(float), stream) != cudaSuccess)
     return ATTN_ERR_CUDA;
-  attn_bwd_prep_kernel<<<static_cast<unsigned>((rows_pad + 7) / 8), 256, 0, stream>>>(
+  attn_bwd_prep_kernel<HD><<<static_cast<unsigned>((rows_pad + 7) / 8), 256, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), lse, nlse2, ndelta,
       rows_pad, Nq, nq_pad, scale);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
@@ -571,7 +598,7 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
                        CU_TENSOR_MAP_SWIZZLE_128B))
     return ATTN_ERR_CUDA;
   static KernelSetup setup;
-  if (const int rc = prepare_kernel(setup, attn_bwd_kernel, SMEM_ALLOC); rc != ATTN_OK) return rc;
+  if (const int rc = prepare_kernel(setup, attn_bwd_kernel<HD>, SMEM_ALLOC); rc != ATTN_OK) return rc;
   BwdParams prm;
   prm.nlse2 = nlse2;
   prm.ndelta = ndelta;
@@ -591,8 +618,23 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
   prm.window = window > 0 ? window : 0;
   prm.err = err;
   const dim3 grid((Nk + BK - 1) / BK, Hkv, B);
-  attn_bwd_kernel<<<grid, NTHREADS, SMEM_ALLOC, stream>>>(tq, tk, tv, tdo, tdq, prm);
+  attn_bwd_kernel<HD><<<grid, NTHREADS, SMEM_ALLOC, stream>>>(tq, tk, tv, tdo, tdq, prm);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // namespace bwd
+
+int launch_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+               const float* lse, float* dq, void* dk, void* dv, void* workspace, int B, int Hq,
+               int Hkv, int Nq, int Nk, int D, float scale, int causal, int window, cudaStream_t stream,
+               int* err) {
+  if (D == 128)
+    return bwd::launch_bwd_hd<128>(q, k, v, o, dout, lse, dq, dk, dv, workspace, B, Hq, Hkv, Nq, Nk, scale,
+                                   causal, window, stream, err);
+  if (D == 64)
+    return bwd::launch_bwd_hd<64>(q, k, v, o, dout, lse, dq, dk, dv, workspace, B, Hq, Hkv, Nq, Nk, scale,
+                                  causal, window, stream, err);
+  return ATTN_ERR_HEAD_DIM;
 }
 
 }  // namespace attn

@@ -103,11 +103,12 @@ int launch_fwd_tc(const void* q, const void* k, const void* v, void* o, float* l
                   float softcap = 0.f, const float* sinks = nullptr);
 
 // Backward: D and LSE*log2(e) into the workspace (bwd_workspace_bytes), dQ
-// zeroed and accumulated in fp32, dK and dV written in bf16.  D = 128.
+// zeroed and accumulated in fp32, dK and dV written in bf16.  Head dimension
+// D = 64 or 128.
 size_t bwd_workspace_bytes(int B, int Hq, int Nq);
 int launch_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
                const float* lse, float* dq, void* dk, void* dv, void* workspace, int B, int Hq,
-               int Hkv, int Nq, int Nk, float scale, int causal, int window, cudaStream_t stream,
+               int Hkv, int Nq, int Nk, int D, float scale, int causal, int window, cudaStream_t stream,
                int* err);
 
 int launch_fwd_fp32(const float* q, const float* k, const float* v, float* o, float* lse, int B,

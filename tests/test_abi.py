@@ -187,7 +187,8 @@ def test_backward_argument_errors(L):
     assert f(ws=None) == -1
     assert f(Nq=0) == -2
     assert f(Hq=8, Hkv=3) == -3
-    assert f(D=64) == -4
+    assert f(D=96) == -4
+    assert f(D=256) == -4
     assert f(dq=MIS) == -5
     assert f(scale=-1.0) == -6
     assert L.attn_bwd_workspace_size(2, 8, 100) == 2 * 2 * 8 * 128 * 4

@@ -631,6 +631,12 @@ BWD_CASES = [
     (1, 4, 2, 257, 257, False, 100),    # window without causal
     (1, 2, 1, 130, 700, True, 50),      # chunked prefill + window: key tiles no query sees (dK = dV = 0)
     (1, 2, 2, 512, 512, True, 128),     # window of exactly one tile, whole tiles
+    # head dimension 64
+    (1, 2, 2, 200, 200, False, 0, 64),
+    (2, 4, 2, 257, 257, True, 0, 64),
+    (1, 4, 1, 130, 300, True, 0, 64),
+    (1, 2, 1, 130, 700, True, 50, 64),
+    (1, 4, 2, 384, 384, True, 0, 64),
 ]
 
 
@@ -648,10 +654,11 @@ def _bwd_check(got, want, name):
 
 @pytest.mark.parametrize("case", BWD_CASES, ids=lambda c: "-".join(map(str, c)))
 def test_backward(dev, case):
-    B, Hq, Hkv, Nq, Nk, causal, window = case
-    q, k, v = inputs.prefill_inputs(B, Hq, Hkv, Nq, Nk, 128, "bf16", seed=Nq * 7 + Nk)
+    B, Hq, Hkv, Nq, Nk, causal, window = case[:7]
+    D = case[7] if len(case) > 7 else 128
+    q, k, v = inputs.prefill_inputs(B, Hq, Hkv, Nq, Nk, D, "bf16", seed=Nq * 7 + Nk)
     g = torch.Generator("cpu").manual_seed(Nq + 3)
-    do = torch.randn(B, Hq, Nq, 128, generator=g).to(torch.bfloat16)
+    do = torch.randn(B, Hq, Nq, D, generator=g).to(torch.bfloat16)
     qd, kd, vd, dod = q.to(dev), k.to(dev), v.to(dev), do.to(dev)
     o, lse = binding.attn_fwd(qd, kd, vd, causal=causal, window=window)
     gq, gk, gv = (guarded(q.shape, torch.float32, dev), guarded(k.shape, torch.bfloat16, dev),
@@ -659,7 +666,7 @@ def test_backward(dev, case):
     gw = guarded((binding.lib().attn_bwd_workspace_size(B, Hq, Nq),), torch.uint8, dev)
     dq, dk, dv = binding.attn_bwd(qd, kd, vd, o, dod, lse, gq.t, gk.t, gv.t, gw.t, causal=causal, window=window)
     check_guards(gq, gk, gv, gw)
-    dQ, dK, dV = oracle.attention_backward(q, k, v, do, 1 / math.sqrt(128), causal, window)
+    dQ, dK, dV = oracle.attention_backward(q, k, v, do, 1 / math.sqrt(D), causal, window)
     _bwd_check(dq, dQ, "dQ")
     _bwd_check(dk, dK, "dK")
     _bwd_check(dv, dV, "dV")
