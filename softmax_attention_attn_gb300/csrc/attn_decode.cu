@@ -762,9 +762,13 @@ attn_decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_co
           ka[r][4 * j + 3] = u.w;
         }
       }
-      float acc[NTW][4];
+      // two partial sums per column block (even and odd K steps): twice the independent
+      // MMAs in flight against the MMA latency
+      float acc[NTW][4], acc2[NTW][4];
 #pragma unroll
-      for (int nt = 0; nt < NTW; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+      for (int nt = 0; nt < NTW; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[nt][e] = acc2[nt][e] = 0.f;
 #pragma unroll
       for (int kk = 0; kk < KK; ++kk) {
         // MMA K index 2c + {0, 1} -> d = c DQ + 4 kk + {0, 1}; 2c + 8 + {0, 1} -> + {2, 3}
@@ -781,8 +785,13 @@ attn_decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_co
           a3 = ka[1][2 * kk + 1];
         }
 #pragma unroll
-        for (int nt = 0; nt < NTW; ++nt) mma16816<KV8>(acc[nt], a0, a1, a2, a3, qf[nt][2 * kk], qf[nt][2 * kk + 1]);
+        for (int nt = 0; nt < NTW; ++nt)
+          mma16816<KV8>((kk & 1) ? acc2[nt] : acc[nt], a0, a1, a2, a3, qf[nt][2 * kk], qf[nt][2 * kk + 1]);
       }
+#pragma unroll
+      for (int nt = 0; nt < NTW; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[nt][e] += acc2[nt][e];
       // the MMAs above have consumed every value this warp read from the slot
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_empty(s));
