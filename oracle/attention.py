@@ -57,6 +57,11 @@ Sources (pages on softmax attention):
       bit 7 sign, bits 6-3 exponent (bias 7), bits 2-0 mantissa; exponent 0
       encodes the subnormals ``m/8 * 2^-6``; exponent 15 with mantissa 7 is NaN;
       there are no infinities.
+    - fp8 e4m3 Q, K and V (the "fp8 dense prefill" scenario that the same page's
+      section "局限与改进" lists among the weakest, and its section "未来方向" among
+      the work still open): each tensor holds E4M3 codes with its own per-tensor
+      scale (``q_scale``, ``k_scale``, ``v_scale``); the values are code times
+      scale and everything else is the plain forward.
 
 Every pin of this module lives in ``tests/test_oracle.py``.
 """
@@ -70,7 +75,7 @@ __all__ = [
     "decode_combine", "paged_rows", "decode_forward_paged", "attention_varlen",
     "e4m3_to_float", "decode_forward_fp8", "decode_forward_paged_fp8",
     "softcap_scores", "attention_forward_ext", "attention_rows_ext",
-    "attention_backward",
+    "attention_backward", "attention_forward_fp8", "attention_rows_fp8",
 ]
 
 
@@ -382,6 +387,35 @@ def decode_forward_paged_fp8(q, k_pages, v_pages, k_scale: float, v_scale: float
         for h in range(Hq):
             kh = kv_head(h, Hq, Hkv)
             O[b, h], LSE[b, h] = _decode_one(qb[h], Kb[:, kh], Vb[:, kh], scale)
+    return O, LSE
+
+
+def attention_forward_fp8(q_codes, k_codes, v_codes, q_scale: float, k_scale: float,
+                          v_scale: float, scale: float, causal: bool = False, window: int = 0):
+    """Forward on fp8 (E4M3) Q, K and V ``[B,H,N,D]`` of codes: the plain forward of
+    :func:`attention_forward` on the values ``code * q_scale``, ``code * k_scale``
+    and ``code * v_scale``."""
+    Q = e4m3_to_float(q_codes) * float(q_scale)
+    K = e4m3_to_float(k_codes) * float(k_scale)
+    V = e4m3_to_float(v_codes) * float(v_scale)
+    return attention_forward(Q, K, V, scale, causal, window)
+
+
+def attention_rows_fp8(q_codes, k_codes, v_codes, q_scale: float, k_scale: float, v_scale: float,
+                       scale: float, rows, causal: bool = False, window: int = 0):
+    """:func:`attention_rows` (selected ``(b, h, i)`` rows) on E4M3 codes, values as in
+    :func:`attention_forward_fp8`; only the K/V heads the rows read are decoded."""
+    rows = list(rows)
+    Hq, Hkv = q_codes.shape[1], k_codes.shape[1]
+    O = np.zeros((len(rows), v_codes.shape[3]))
+    LSE = np.zeros(len(rows))
+    for n, (b, h, i) in enumerate(rows):
+        kh = kv_head(h, Hq, Hkv)
+        q1 = e4m3_to_float(q_codes[b:b + 1, h:h + 1]) * float(q_scale)
+        k1 = e4m3_to_float(k_codes[b:b + 1, kh:kh + 1]) * float(k_scale)
+        v1 = e4m3_to_float(v_codes[b:b + 1, kh:kh + 1]) * float(v_scale)
+        o, lse = attention_rows(q1, k1, v1, scale, [(0, 0, i)], causal, window)
+        O[n], LSE[n] = o[0], lse[0]
     return O, LSE
 
 

@@ -420,6 +420,51 @@ def pin_fp8_decode(ora):
     assert np.allclose(O4, O, rtol=1e-13, atol=1e-13) and np.allclose(L4, L, rtol=1e-13, atol=1e-13)
 
 
+def pin_fp8_prefill(ora):
+    """fp8 Q/K/V prefill: brute force (math.fsum) on the values decoded from the
+    format definition for a tiny GQA case under causal and window masks, the
+    folding of q_scale * k_scale into the score scale and of v_scale into O, and
+    sampled rows == the full forward."""
+    rng = np.random.default_rng(17)
+    B, Hq, Hkv, Nq, Nk, D = 1, 4, 2, 5, 7, 6
+    qc = rng.integers(0, 256, (B, Hq, Nq, D), dtype=np.uint8)
+    kc = rng.integers(0, 256, (B, Hkv, Nk, D), dtype=np.uint8)
+    vc = rng.integers(0, 256, (B, Hkv, Nk, D), dtype=np.uint8)
+    for c in (qc, kc, vc):
+        c[(c & 0x7F) == 0x7F] = 0x38         # no NaN codes
+    qs, ks, vs, sc = 0.125, 0.03125, 0.5, 0.2
+
+    def val(c):
+        c = int(c)
+        sgn = -1.0 if c & 0x80 else 1.0
+        e, m = (c >> 3) & 15, c & 7
+        return sgn * ((m / 8) * 2.0 ** -6 if e == 0 else (1 + m / 8) * 2.0 ** (e - 7))
+    for causal, window in ((False, 0), (True, 0), (True, 3), (False, 2)):
+        O, L = ora.attention_forward_fp8(qc, kc, vc, qs, ks, vs, sc, causal, window)
+        for h in range(Hq):
+            kh = h // (Hq // Hkv)
+            for i in range(Nq):
+                vis = [j for j in range(Nk)
+                       if (not causal or j <= i + Nk - Nq) and (window <= 0 or j > i + Nk - Nq - window)]
+                s = {j: sc * math.fsum(val(qc[0, h, i, d]) * qs * val(kc[0, kh, j, d]) * ks for d in range(D))
+                     for j in vis}
+                mx = max(s.values())
+                w = {j: math.exp(s[j] - mx) for j in vis}
+                den = math.fsum(w.values())
+                for d in range(D):
+                    o = math.fsum(w[j] * val(vc[0, kh, j, d]) * vs for j in vis) / den
+                    assert abs(O[0, h, i, d] - o) < 1e-12 * max(1.0, abs(o)), (causal, window, h, i, d)
+                assert abs(L[0, h, i] - (mx + math.log(den))) < 1e-12
+        O2, L2 = ora.attention_forward_fp8(qc, kc, vc, 1.0, 1.0, vs, sc * qs * ks, causal, window)
+        assert np.allclose(O2, O, rtol=1e-13, atol=1e-13) and np.allclose(L2, L, rtol=1e-13, atol=1e-13)
+        O3, L3 = ora.attention_forward_fp8(qc, kc, vc, qs, ks, 3 * vs, sc, causal, window)
+        assert np.allclose(O3, 3 * O, rtol=1e-13, atol=1e-13) and np.allclose(L3, L, rtol=1e-13, atol=1e-13)
+        rows = [(0, 3, 4), (0, 0, 0), (0, 1, 2)]
+        Or, Lr = ora.attention_rows_fp8(qc, kc, vc, qs, ks, vs, sc, rows, causal, window)
+        for n, (b, h, i) in enumerate(rows):
+            assert np.allclose(Or[n], O[b, h, i], rtol=1e-13, atol=1e-13) and abs(Lr[n] - L[b, h, i]) < 1e-12
+
+
 def pin_softcap_sink(ora):
     """Softcap and sinks: brute force (math.tanh, math.fsum) on tiny inputs with
     causal / window masks and sinks from dominant to -inf, the Q = 0 closed form,
@@ -515,7 +560,7 @@ def pin_backward(ora):
 
 PINS = [pin_brute_force, pin_sdpa, pin_zero_query, pin_single_key, pin_probability_rows,
         pin_causal_first_row, pin_dominant_key, pin_invariants, pin_decode, pin_paged_decode, pin_varlen,
-        pin_golden, pin_e4m3_codes, pin_fp8_decode, pin_softcap_sink, pin_backward]
+        pin_golden, pin_e4m3_codes, pin_fp8_decode, pin_fp8_prefill, pin_softcap_sink, pin_backward]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
@@ -638,6 +683,11 @@ def _mut_fp8_paged_swapped(q, k_pages, v_pages, k_scale, v_scale, block_table, s
     return ORA.decode_forward_fp8(q, kc, vc, k_scale, v_scale, seqlens, scale, batches)
 
 
+def _mut_fp8_prefill_scales_swapped(q_codes, k_codes, v_codes, q_scale, k_scale, v_scale, scale,
+                                    causal=False, window=0):
+    return _GOOD_FP8_PREFILL(q_codes, k_codes, v_codes, q_scale, v_scale, k_scale, scale, causal, window)
+
+
 def _mut_softcap_no_divide(S, cap):
     if not cap > 0:
         return S
@@ -689,6 +739,7 @@ def _mut_bwd_dv_untransposed(Qh, Kh, Vh, dOh, scale, vis):
 
 
 _GOOD_BWD = ORA._backward_head
+_GOOD_FP8_PREFILL = ORA.attention_forward_fp8
 
 
 MUTANTS = {
@@ -706,6 +757,7 @@ MUTANTS = {
     "e4m3_bias_8": ("e4m3_to_float", _mut_e4m3_bias8),
     "e4m3_no_subnormals": ("e4m3_to_float", _mut_e4m3_no_subnormals),
     "fp8_paged_index_swapped": ("decode_forward_paged_fp8", _mut_fp8_paged_swapped),
+    "fp8_prefill_k_v_scales_swapped": ("attention_forward_fp8", _mut_fp8_prefill_scales_swapped),
     "softcap_without_divide": ("softcap_scores", _mut_softcap_no_divide),
     "sink_unshifted": ("_softmax_rows_sink", _mut_sink_unshifted),
     "sink_dropped": ("_softmax_rows_sink", _mut_sink_dropped),
