@@ -65,7 +65,7 @@ VARLEN = dict(B=32, Hq=32, Hkv=8, D=128, n_lo=512, n_hi=8192, causal=True)
 FP32_POINTS = [(2, 4, 64, 32)] + [(2, 8, n, d) for n in (64, 256, 1024, 4096) for d in (32, 64, 128)]
 SHORT = {"paged": "paged_dec", "decode_fp8": "fp8kv_dec", "decode_mqa": "mqa_dec", "decode_d64": "d64_dec", "window": "window4k", "chunked": "chunked",
          "d64": "d64", "fp16": "fp16", "varlen": "varlen", "softcap": "softcap", "bwd": "bwd", "bwd_d64": "bwd_d64",
-         "fp32": "fp32", "dense": "dense"}
+         "fp32": "fp32", "dense": "dense", "fp8": "fp8"}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FP32_SIMT_FLOP_PER_CLK_SM = 256.0   # 128 FP32 lanes x 2 (fused multiply-add)
 GB300_SMS = 152
@@ -101,7 +101,7 @@ def parse_args():
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--workload", choices=["dense", "causal", "decode", "fp32", "window", "chunked", "d64",
                                            "paged", "fp16", "varlen", "decode_fp8", "softcap", "bwd",
-                                           "decode_mqa", "decode_d64", "bwd_d64"],
+                                           "decode_mqa", "decode_d64", "bwd_d64", "fp8"],
                     default="dense",
                     help="workload of the timed loop (default: the dense bf16 prefill)")
     ap.add_argument("--no-extras", action="store_true", help="skip the other workloads")
@@ -368,6 +368,8 @@ WORKLOAD_NAMES = {
     "decode_d64": "bf16 split-KV decode B=64 Hq=32 Hkv=8 D=64, Nk_b~U[512,32768], chunk 512",
     "bwd": "bf16 backward (dQ, dK, dV) B=1 H=32 N=8192 D=128 (non-causal); FLOPs = 2.5 x forward",
     "bwd_d64": "bf16 backward (dQ, dK, dV) B=1 H=32 N=8192 D=64 (non-causal); FLOPs = 2.5 x forward",
+    "fp8": "fp8 E4M3 Q/K/V dense prefill B=1 H=32 N=8192 D=128 (non-causal): Q K^T on E4M3 tensor cores, "
+           "P V in bf16 after V is widened (2 launches)",
 }
 
 
@@ -395,6 +397,26 @@ def make_workload(name, dev, seed, peaks, peak_src, sm_max_mhz, decode_batch=Non
         w["peak_source"] = f"{peak_src} dense bf16 (burst)"
         w["e2e_in"] = [(x, t) for x, t in zip(host, (q, k, v))]
         w["e2e_out"] = [dq, dk, dv]
+    elif name == "fp8":
+        c = MAIN
+        host = inputs.prefill_inputs_fp8(c["B"], c["Hq"], c["Hkv"], c["N"], c["N"], c["D"], seed)
+        q, k, v = (x.to(dev) for x in host)
+        o = torch.empty(q.shape, device=dev, dtype=torch.bfloat16)
+        lse = torch.empty(c["B"], c["Hq"], c["N"], device=dev, dtype=torch.float32)
+        ws = torch.empty(binding.attn_fwd_fp8_workspace_size(c["B"], c["Hkv"], c["N"], c["D"]), device=dev,
+                         dtype=torch.uint8)
+        w["fn"] = lambda: binding.attn_fwd_fp8(q, k, v, 1.0, 1.0, 1.0, o, lse, ws)
+        w["make_fn"] = lambda ins, outs: (lambda: binding.attn_fwd_fp8(ins[0], ins[1], ins[2], 1.0, 1.0, 1.0,
+                                                                       outs[0], outs[1], ws))
+        w["work"] = flops(**c)
+        w["unit"], w["launches"], w["dtype"] = "TFLOP/s", 2, "e4m3"
+        w["seq_len"], w["batch"] = c["N"], c["B"]
+        # half the FLOPs (Q K^T) at the fp8 rate (twice bf16: the nominal 4.5 / 2.25 PFLOP/s
+        # ratio), half (P V) at the bf16 rate: 1 / (0.5 / 2P + 0.5 / P) = 4P / 3
+        w["bound"], w["peak"] = "tensor", peaks["bf16_tflops"] * 4.0 / 3.0
+        w["peak_source"] = f"4/3 x {peak_src} dense bf16 (burst): Q K^T at 2x (fp8), P V at 1x (bf16)"
+        w["e2e_in"] = [(x, t) for x, t in zip(host, (q, k, v))]
+        w["e2e_out"] = [o, lse]
     elif name == "varlen":
         c = VARLEN
         g = torch.Generator("cpu").manual_seed(seed + 11)
@@ -762,7 +784,7 @@ def run_gb300(args, rank, world, local_rank):
     if not args.no_extras:
         xs = max(5, min(args.steps // 10, 50))
         for name in ("dense", "causal", "decode", "paged", "decode_fp8", "decode_mqa", "decode_d64", "window",
-                     "chunked", "d64", "fp16", "varlen", "softcap", "bwd", "bwd_d64"):
+                     "chunked", "d64", "fp16", "varlen", "softcap", "bwd", "bwd_d64", "fp8"):
             if name == args.workload:
                 continue
             x = make_workload(name, dev, rank, peaks, peak_src, sm_max, args.decode_batch)

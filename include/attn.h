@@ -115,6 +115,38 @@ int attn_fwd_fp16(const void* q, const void* k, const void* v, void* o, float* l
                   float scale, int causal, int window, attn_stream_t stream);
 
 /*
+ * attn_fwd_fp8_workspace_size — bytes of device workspace attn_fwd_fp8 needs:
+ * a bf16 copy of V, B * Hkv * Nk * D * 2.  Returns 0 for invalid sizes.
+ */
+size_t attn_fwd_fp8_workspace_size(int B, int Hkv, int Nk, int D);
+
+/*
+ * attn_fwd_fp8 — fused attention forward on fp8 (E4M3) Q, K and V.
+ *   [ASK] "局限与改进" (fp8 dense prefill among the weakest scenarios) and
+ *   "未来方向" (fp8 among the work still open); the operator is that of attn_fwd.
+ *
+ *   q    : uint8 [B, Hq,  Nq, D]  k, v : uint8 [B, Hkv, Nk, D], one OCP FP8
+ *          E4M3 code per element (sign bit 7, exponent bits 6-3 with bias 7,
+ *          mantissa bits 2-0; S.1111.111 is NaN).  An element's value is its
+ *          E4M3 value times q_scale, k_scale or v_scale (per-tensor, host floats).
+ *   o    : bf16 [B, Hq, Nq, D] (out)   lse : fp32 [B, Hq, Nq] (out; may be NULL)
+ *   workspace : device, attn_fwd_fp8_workspace_size(B, Hkv, Nk, D) bytes, owned
+ *          by the caller; overwritten (it receives V widened to bf16).
+ *   D must be 128.  S = Q K^T runs on the E4M3 codes (tensor cores, fp32
+ *   accumulation) and is scaled by scale * q_scale * k_scale; P is rounded to
+ *   bf16 and multiplied by the exact bf16 copy of V; O is multiplied by v_scale
+ *   and rounded to bf16.  Masks, GQA and LSE are those of attn_fwd.
+ *   Errors: as attn_fwd; ATTN_ERR_NULL / _ALIGN also for the workspace;
+ *   ATTN_ERR_SCALE also for a q_scale, k_scale or v_scale that is not finite or
+ *   not > 0, or a product scale * q_scale * k_scale that is not a finite
+ *   positive float.
+ */
+int attn_fwd_fp8(const void* q, const void* k, const void* v, float q_scale, float k_scale,
+                 float v_scale, void* o, float* lse, void* workspace,
+                 int B, int Hq, int Hkv, int Nq, int Nk, int D,
+                 float scale, int causal, int window, attn_stream_t stream);
+
+/*
  * attn_fwd_varlen — bf16 forward on a ragged batch (packed, token-major).
  *   [ASK] "研究动机" (ragged batches on the feature surface).
  *

@@ -37,6 +37,9 @@ SIGNATURES = {
                                 + [_c_float, _c_int, _vp]),
     "attn_decode_splitkv_paged_fp8": (_c_int, [_vp] * 3 + [_c_float] * 2 + [_vp] * 3 + [_c_int] * 7
                                       + [_c_float, _c_int, _vp]),
+    "attn_fwd_fp8_workspace_size": (ctypes.c_size_t, [_c_int] * 4),
+    "attn_fwd_fp8": (_c_int, [_vp] * 3 + [_c_float] * 3 + [_vp] * 3 + [_c_int] * 6
+                     + [_c_float, _c_int, _c_int, _vp]),
     "attn_bwd_workspace_size": (ctypes.c_size_t, [_c_int] * 3),
     "attn_bwd": (_c_int, [_vp] * 10 + [_c_int] * 6 + [_c_float, _c_int, _c_int, _vp]),
     "attn_get_device_error": (_c_int, [_vp]),
@@ -304,6 +307,39 @@ def _require_fp8(t, name):
         raise TypeError(f"{name} must hold E4M3 codes (uint8 or float8_e4m3fn), got {t.dtype}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
+
+
+def attn_fwd_fp8_workspace_size(B, Hkv, Nk, D) -> int:
+    return int(lib().attn_fwd_fp8_workspace_size(int(B), int(Hkv), int(Nk), int(D)))
+
+
+def attn_fwd_fp8(q, k, v, q_scale=1.0, k_scale=1.0, v_scale=1.0, o=None, lse=None, workspace=None,
+                 scale=None, causal=False, window=0, stream=None):
+    """Forward on fp8 E4M3 q ``[B,Hq,Nq,D]`` and k/v ``[B,Hkv,Nk,D]`` (values = code *
+    per-tensor scale) -> (o bf16, lse fp32).  ``workspace`` (uint8, at least
+    :func:`attn_fwd_fp8_workspace_size` bytes) is allocated when None."""
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _require_fp8(t, n)
+    B, Hq, Nq, D = q.shape
+    _, Hkv, Nk, _ = k.shape
+    need = attn_fwd_fp8_workspace_size(B, Hkv, Nk, D)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), device=q.device, dtype=torch.uint8)
+    if workspace.numel() * workspace.element_size() < need:
+        raise ValueError(f"workspace holds fewer than {need} bytes")
+    if o is None:
+        o = torch.empty(B, Hq, Nq, D, device=q.device, dtype=torch.bfloat16)
+    if lse is None:
+        lse = torch.empty(B, Hq, Nq, device=q.device, dtype=torch.float32)
+    _require(o, torch.bfloat16, "o")
+    _require(lse, torch.float32, "lse")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    code = lib().attn_fwd_fp8(_ptr(q), _ptr(k), _ptr(v), float(q_scale), float(k_scale), float(v_scale),
+                              _ptr(o), _ptr(lse), _ptr(workspace), B, Hq, Hkv, Nq, Nk, D, scale,
+                              int(bool(causal)), int(window), _stream(stream))
+    _check(code, "attn_fwd_fp8")
+    return o, lse
 
 
 def attn_decode_fp8(q, k_cache, v_cache, seqlens, k_scale=1.0, v_scale=1.0, workspace=None, o=None,

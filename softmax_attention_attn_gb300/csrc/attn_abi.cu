@@ -158,6 +158,30 @@ int attn_fwd_fp16(const void* q, const void* k, const void* v, void* o, float* l
   return fwd_tc(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, 1, scale, causal, window, stream);
 }
 
+size_t attn_fwd_fp8_workspace_size(int B, int Hkv, int Nk, int D) {
+  if (B <= 0 || Hkv <= 0 || Nk <= 0 || D <= 0) return 0;
+  return fwd_fp8_workspace_bytes(B, Hkv, Nk, D);
+}
+
+int attn_fwd_fp8(const void* q, const void* k, const void* v, float q_scale, float k_scale,
+                 float v_scale, void* o, float* lse, void* workspace, int B, int Hq, int Hkv,
+                 int Nq, int Nk, int D, float scale, int causal, int window, attn_stream_t stream) {
+  int rc = check_common(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, scale);
+  if (rc != ATTN_OK) return rc;
+  if (!workspace) return ATTN_ERR_NULL;
+  if (!aligned16(workspace)) return ATTN_ERR_ALIGN;
+  if (D != 128) return ATTN_ERR_HEAD_DIM;
+  for (const float x : {q_scale, k_scale, v_scale})
+    if (!std::isfinite(x) || !(x > 0.f)) return ATTN_ERR_SCALE;
+  const float s_all = scale * q_scale * k_scale;  // the score scale the kernel applies
+  if (!std::isfinite(s_all) || !(s_all > 0.f)) return ATTN_ERR_SCALE;
+  DeviceInfo* dev = nullptr;
+  if ((rc = device_info(&dev)) != ATTN_OK) return rc;
+  return launch_fwd_fp8(q, k, v, q_scale, k_scale, v_scale, o, lse, workspace, B, Hq, Hkv, Nq, Nk,
+                        D, scale, causal, window, dev->num_sms,
+                        reinterpret_cast<cudaStream_t>(stream), dev->err);
+}
+
 int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
                     const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int Hq, int Hkv,
                     int max_seqlen_q, int total_q, int total_k, int D, float scale, int causal,

@@ -64,23 +64,29 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr float RESCALE_LOG2 = 8.0f;         // keep a stale max while the growth is <= 2^8
 
 // Shape constants for head dimension HD (64 or 128); F16 selects fp16 instead
-// of bf16 operands.
-template <int HD, bool F16 = false>
+// of bf16 operands; QK8 selects E4M3 Q and K (S = Q K^T on kind::f8f6f4; V, P
+// and O stay bf16).
+template <int HD, bool F16 = false, bool QK8 = false>
 struct Cfg {
-  static constexpr int KBLKS = HD / 64;                 // 128-byte slabs per tile row
-  static constexpr int TILE_BYTES = KBLKS * KBLK_BYTES; // one 128-row Q, K or V tile
-  static constexpr int STAGES = HD == 128 ? 5 : 10;     // K/V ring slots (one K or V tile each)
+  static constexpr int KBLKS = HD / 64;                 // 128-byte slabs per 16-bit tile row
+  static constexpr int TILE_BYTES = KBLKS * KBLK_BYTES; // one 128-row 16-bit tile (a ring slot)
+  static constexpr int QK_BOX = QK8 ? 128 : 64;         // Q/K elements per 128-byte slab row
+  static constexpr int QK_SLABS = HD / QK_BOX;          // 128-byte slabs per Q/K tile row
+  static constexpr int QK_TILE_BYTES = QK_SLABS * KBLK_BYTES;  // one 128-row Q or K tile
+  static constexpr int QK_STEPS = QK8 ? HD / 32 : HD / 16;     // MMAs of one Q K^T (32 bytes of K each)
+  static constexpr int STAGES = HD == 128 ? (QK8 ? 6 : 5) : 10;  // K/V ring slots (one K or V tile each)
   static constexpr int SMEM_Q = 0;
-  static constexpr int SMEM_RING = SMEM_Q + NQT * TILE_BYTES;
+  static constexpr int SMEM_RING = SMEM_Q + NQT * QK_TILE_BYTES;
   static constexpr int SMEM_BAR = SMEM_RING + STAGES * TILE_BYTES;
   static constexpr int NUM_BARS = 3 + 2 * STAGES + 5 * NQT;
   static constexpr int SMEM_MISC = SMEM_BAR + NUM_BARS * 8;
   static constexpr int SMEM_ALLOC = SMEM_MISC + 16 + 1024;  // + slack for 1024-byte alignment
   static constexpr uint32_t AB_FORMAT = F16 ? 0u : 1u;  // instruction-descriptor A/B format
-  static constexpr uint32_t IDESC_QK = idesc_f16kind_f32(128, BN, 0, AB_FORMAT);
+  static constexpr uint32_t IDESC_QK = QK8 ? idesc_e4m3_f32(128, BN) : idesc_f16kind_f32(128, BN, 0, AB_FORMAT);
   static constexpr uint32_t IDESC_PV = idesc_f16kind_f32(128, HD, 1, AB_FORMAT);
   static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
   static_assert(2 * BN + 2 * HD <= TMEM_COLS, "tensor memory budget");
+  static_assert(!QK8 || (HD == 128 && !F16), "E4M3 Q/K: bf16 V/O and HD = 128 only");
 };
 
 // Softcap fast paths: tanh(y) ~= y * sum_k t_k y^(2k), minimax polynomials of the same
@@ -150,15 +156,21 @@ __device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t off16) {
 }
 
 // S (tmem) = Q_tile (smem) x K_tile^T (smem); both K-major, 128-byte swizzle,
-// given by the descriptors of their first byte.
-template <int HD, bool F16>
+// given by the descriptors of their first byte.  Every MMA takes 32 bytes of
+// each row (16 bf16 / fp16 or 32 E4M3 elements), four per 128-byte slab.
+template <int HD, bool F16, bool QK8>
 __device__ __forceinline__ void issue_qk(uint32_t issue, uint32_t d_tmem, uint64_t q_desc,
                                          uint64_t k_desc) {
+  using C = Cfg<HD, F16, QK8>;
 #pragma unroll
-  for (int kk = 0; kk < HD / 16; ++kk) {
+  for (int kk = 0; kk < C::QK_STEPS; ++kk) {
     const uint32_t koff = static_cast<uint32_t>((kk >> 2) * KBLK_BYTES + (kk & 3) * 32) >> 4;
-    mma_bf16_ss_if(issue, d_tmem, desc_add(q_desc, koff), desc_add(k_desc, koff),
-                   Cfg<HD, F16>::IDESC_QK, kk > 0 ? 1u : 0u);
+    if constexpr (QK8)
+      mma_f8_ss_if(issue, d_tmem, desc_add(q_desc, koff), desc_add(k_desc, koff), C::IDESC_QK,
+                   kk > 0 ? 1u : 0u);
+    else
+      mma_bf16_ss_if(issue, d_tmem, desc_add(q_desc, koff), desc_add(k_desc, koff), C::IDESC_QK,
+                     kk > 0 ? 1u : 0u);
   }
 }
 
@@ -292,14 +304,17 @@ __device__ __forceinline__ void own_range(const Unit& u, int t, int& jb, int& je
   je = t == 0 ? u.je0 : u.je1;
 }
 
-template <int HD, bool F16, bool CAP>
+template <int HD, bool F16, bool CAP, bool QK8>
 __global__ void __launch_bounds__(NTHREADS, 1)
 attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
-  using C = Cfg<HD, F16>;
+  using C = Cfg<HD, F16, QK8>;
   constexpr int KBLKS = C::KBLKS;
   constexpr int TILE_BYTES = C::TILE_BYTES;
+  constexpr int QK_SLABS = C::QK_SLABS;
+  constexpr int QK_BOX = C::QK_BOX;
+  constexpr int QK_TILE_BYTES = C::QK_TILE_BYTES;
   constexpr int STAGES = C::STAGES;
   constexpr int SMEM_Q = C::SMEM_Q;
   constexpr int SMEM_RING = C::SMEM_RING;
@@ -374,15 +389,15 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
         const Unit u = make_unit(w, p, n_qblk);
         if (u.j_end <= u.j_begin) continue;
         if (nq > 0 && !mbar_wait(bar_q_empty, (nq - 1) & 1, abort_flag, p.err)) { ok = false; break; }
-        mbar_arrive_expect_tx(bar_q_full, NQT * TILE_BYTES);
+        mbar_arrive_expect_tx(bar_q_full, NQT * QK_TILE_BYTES);
         for (int t = 0; t < NQT; ++t)
-          for (int kb = 0; kb < KBLKS; ++kb)
+          for (int kb = 0; kb < QK_SLABS; ++kb)
             if (p.varlen)
-              tma_load_3d(sb + SMEM_Q + t * TILE_BYTES + kb * KBLK_BYTES, &tm_q, bar_q_full, kb * 64,
-                          u.h, u.q_tok + u.q0 + t * BM);
+              tma_load_3d(sb + SMEM_Q + t * QK_TILE_BYTES + kb * KBLK_BYTES, &tm_q, bar_q_full,
+                          kb * QK_BOX, u.h, u.q_tok + u.q0 + t * BM);
             else
-              tma_load_3d(sb + SMEM_Q + t * TILE_BYTES + kb * KBLK_BYTES, &tm_q, bar_q_full, kb * 64,
-                          u.q0 + t * BM, u.b * p.Hq + u.h);
+              tma_load_3d(sb + SMEM_Q + t * QK_TILE_BYTES + kb * KBLK_BYTES, &tm_q, bar_q_full,
+                          kb * QK_BOX, u.q0 + t * BM, u.b * p.Hq + u.h);
         ++nq;
         for (int j = u.j_begin; j < u.j_end && ok; ++j) {
           for (int kv = 0; kv < 2; ++kv, ++it) {
@@ -391,15 +406,18 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
               ok = false;
               break;
             }
-            mbar_arrive_expect_tx(bar_kv_full(s), TILE_BYTES);
+            // K: QK_SLABS slabs of QK_BOX elements (E4M3 K fills half a slot); V: KBLKS bf16 slabs
+            const int slabs = kv ? KBLKS : QK_SLABS;
+            const int box_x = kv ? 64 : QK_BOX;
+            mbar_arrive_expect_tx(bar_kv_full(s), kv ? TILE_BYTES : QK_TILE_BYTES);
             const CUtensorMap* m = kv ? &tm_v : &tm_k;
-            for (int kb = 0; kb < KBLKS; ++kb)
+            for (int kb = 0; kb < slabs; ++kb)
               if (p.varlen)
                 tma_load_3d(sb + SMEM_RING + s * TILE_BYTES + kb * KBLK_BYTES, m, bar_kv_full(s),
-                            kb * 64, u.kvh, u.k_tok + j * BN);
+                            kb * box_x, u.kvh, u.k_tok + j * BN);
               else
                 tma_load_3d(sb + SMEM_RING + s * TILE_BYTES + kb * KBLK_BYTES, m, bar_kv_full(s),
-                            kb * 64, j * BN, u.b * p.Hkv + u.kvh);
+                            kb * box_x, j * BN, u.b * p.Hkv + u.kvh);
           }
         }
       }
@@ -445,7 +463,7 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
           }
         }
       };
-      const uint64_t q_desc = smem_desc_sw128(sb + SMEM_Q + t * TILE_BYTES, 16, 1024);
+      const uint64_t q_desc = smem_desc_sw128(sb + SMEM_Q + t * QK_TILE_BYTES, 16, 1024);
       const uint64_t k_desc0 = smem_desc_sw128(sb + SMEM_RING, 16, 1024);
       const uint64_t v_desc0 = smem_desc_sw128(sb + SMEM_RING, KBLK_BYTES, 1024);
       auto k_desc = [&](RingPos r) { return desc_add(k_desc0, static_cast<uint32_t>(r.slot * TILE_BYTES) >> 4); };
@@ -467,7 +485,7 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
           const RingPos r = ring_pos<STAGES>(it_base + 2 * (jb - u.j_begin));
           if (!wait_full(r)) { ok = false; break; }
           tc_fence_after();
-          issue_qk<HD, F16>(elect, tmem + s_col(t), q_desc, k_desc(r));
+          issue_qk<HD, F16, QK8>(elect, tmem + s_col(t), q_desc, k_desc(r));
           mma_commit_if(elect, bar_s_full(t));
           mma_commit_if(elect, bar_kv_empty(r.slot));
           if (je - jb == 1) mma_commit_if(elect, bar_q_empty);  // that was this unit's last S
@@ -502,7 +520,7 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
               tc_fence_after();
             }
             issue_pv_half<HD, F16>(elect, tmem + o_col<HD>(t), tmem + s_col(t), v_desc(vj), true, BN / 32);
-            if (j + 1 < je) issue_qk<HD, F16>(elect, tmem + s_col(t), q_desc, k_desc(kn));
+            if (j + 1 < je) issue_qk<HD, F16, QK8>(elect, tmem + s_col(t), q_desc, k_desc(kn));
           }
           *turn = seq + 1;  // the other issuer's turn
           seq += 2;
@@ -753,6 +771,7 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
             lse_val = sink;
           }
         }
+        inv_l *= p.o_scale;
         const size_t orow_idx = p.varlen ? static_cast<size_t>(u.q_tok + row) * p.Hq + u.h
                                          : (static_cast<size_t>(u.b) * p.Hq + u.h) * p.Nq + row;
         uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + orow_idx * HD);
@@ -788,30 +807,35 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
 // --------------------------------------------------------------------- host
 namespace fwd_bf16 {
 
-template <int HD, bool F16, bool CAP>
+template <int HD, bool F16, bool CAP, bool QK8 = false>
 int launch_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
                 int Hkv, int Nq, int Nk, float scale, int causal, int window, int num_sms,
                 cudaStream_t stream, int* err, const int* cu_q, const int* cu_k, int total_q,
-                int total_k, float softcap, const float* sinks) {
-  using C = Cfg<HD, F16>;
+                int total_k, float softcap, const float* sinks, float o_scale = 1.f) {
+  using C = Cfg<HD, F16, QK8>;
   const CUtensorMapDataType dt = F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  // Q and K: 16-bit, or E4M3 codes (one byte, 128 per 128-byte box row)
+  const CUtensorMapDataType dt_qk = QK8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : dt;
+  const uint32_t es_qk = QK8 ? 1u : 2u;
   CUtensorMap tq, tk, tv;
   const bool varlen = cu_q != nullptr;
   if (varlen) {  // packed [total, H, D]: 128 token rows of one head per box
     const uint32_t box[3] = {64, 1, 128};
-    if (!encode_tiled_3d(&tq, dt, q, HD, Hq, total_q, 2, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_tiled_3d(&tk, dt, k, HD, Hkv, total_k, 2, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
+    const uint32_t box_qk[3] = {static_cast<uint32_t>(C::QK_BOX), 1, 128};
+    if (!encode_tiled_3d(&tq, dt_qk, q, HD, Hq, total_q, es_qk, box_qk, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tiled_3d(&tk, dt_qk, k, HD, Hkv, total_k, es_qk, box_qk, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_tiled_3d(&tv, dt, v, HD, Hkv, total_k, 2, box, CU_TENSOR_MAP_SWIZZLE_128B))
       return ATTN_ERR_CUDA;
   } else {       // [B*H, N, D]: 128 rows of one (batch, head) per box
     const uint32_t box[3] = {64, 128, 1};
-    if (!encode_tiled_3d(&tq, dt, q, HD, Nq, static_cast<uint64_t>(B) * Hq, 2, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_tiled_3d(&tk, dt, k, HD, Nk, static_cast<uint64_t>(B) * Hkv, 2, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
+    const uint32_t box_qk[3] = {static_cast<uint32_t>(C::QK_BOX), 128, 1};
+    if (!encode_tiled_3d(&tq, dt_qk, q, HD, Nq, static_cast<uint64_t>(B) * Hq, es_qk, box_qk, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tiled_3d(&tk, dt_qk, k, HD, Nk, static_cast<uint64_t>(B) * Hkv, es_qk, box_qk, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_tiled_3d(&tv, dt, v, HD, Nk, static_cast<uint64_t>(B) * Hkv, 2, box, CU_TENSOR_MAP_SWIZZLE_128B))
       return ATTN_ERR_CUDA;
   }
   static KernelSetup setup;
-  if (const int rc = prepare_kernel(setup, attn_fwd_bf16_kernel<HD, F16, CAP>, C::SMEM_ALLOC); rc != ATTN_OK)
+  if (const int rc = prepare_kernel(setup, attn_fwd_bf16_kernel<HD, F16, CAP, QK8>, C::SMEM_ALLOC); rc != ATTN_OK)
     return rc;
   FwdParams prm;
   prm.o = o;
@@ -856,12 +880,13 @@ int launch_impl(const void* q, const void* k, const void* v, void* o, float* lse
   prescale(kTanhPolyShort, 4, kTanhPolyShortYMax, prm.cap_short, &prm.cap_smax_short);
   prescale(kTanhPolyLong, 6, kTanhPolyLongYMax, prm.cap_long, &prm.cap_smax_long);
   prm.sinks = sinks;
+  prm.o_scale = o_scale;
   // persistent: at most one CTA per SM, each walking units blockIdx.x, +gridDim.x, ...
   const long long n_qblk = (Nq + BM * NQT - 1) / (BM * NQT);
   const long long units = n_qblk * Hq * B;
   if (units > 0x7fffffffLL) return ATTN_ERR_DIM;
   const int grid = static_cast<int>(units < num_sms ? units : num_sms);
-  attn_fwd_bf16_kernel<HD, F16, CAP><<<grid, NTHREADS, C::SMEM_ALLOC, stream>>>(tq, tk, tv, prm);
+  attn_fwd_bf16_kernel<HD, F16, CAP, QK8><<<grid, NTHREADS, C::SMEM_ALLOC, stream>>>(tq, tk, tv, prm);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -882,6 +907,63 @@ int launch_fwd_tc(const void* q, const void* k, const void* v, void* o, float* l
   if (D == 128 && f16) return launch_impl<128, true, false>(ATTN_TC_ARGS);
 #undef ATTN_TC_ARGS
   return ATTN_ERR_HEAD_DIM;
+}
+
+// ---------------------------------------------------------------- fp8 prefill
+namespace fwd_bf16 {
+
+// E4M3 codes -> bf16 values, 16 codes per thread and step (one 16-byte load, two
+// 16-byte stores).  Exact: every E4M3 value (NaN included) is a bf16 value, and
+// the conversion goes through f16, which also holds every E4M3 value exactly.
+__global__ void __launch_bounds__(256) e4m3_to_bf16_kernel(const uint4* __restrict__ in,
+                                                           uint4* __restrict__ out, size_t n16) {
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n16;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const uint4 c = __ldcs(in + i);  // read once
+    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+    uint32_t r[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        // two codes (bytes 2*half, 2*half + 1 of w[k]) -> f16x2 -> two floats -> bf16x2
+        const uint16_t pair = static_cast<uint16_t>(w[k] >> (16 * half));
+        uint32_t h2;
+        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(pair));
+        float lo, hi;
+        asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
+            : "=f"(lo), "=f"(hi) : "r"(h2));
+        r[2 * k + half] = pack_bf16x2(lo, hi);
+      }
+    }
+    out[2 * i] = make_uint4(r[0], r[1], r[2], r[3]);
+    out[2 * i + 1] = make_uint4(r[4], r[5], r[6], r[7]);
+  }
+}
+
+}  // namespace fwd_bf16
+
+size_t fwd_fp8_workspace_bytes(int B, int Hkv, int Nk, int D) {
+  return static_cast<size_t>(B) * Hkv * Nk * D * 2;
+}
+
+int launch_fwd_fp8(const void* q, const void* k, const void* v, float q_scale, float k_scale,
+                   float v_scale, void* o, float* lse, void* workspace, int B, int Hq, int Hkv,
+                   int Nq, int Nk, int D, float scale, int causal, int window, int num_sms,
+                   cudaStream_t stream, int* err) {
+  if (D != 128) return ATTN_ERR_HEAD_DIM;
+  // V widened to bf16 in the workspace, then the forward with S on E4M3 Q/K; the
+  // Q and K scales fold into the score scale, the V scale into the normaliser.
+  const size_t n16 = static_cast<size_t>(B) * Hkv * Nk * D / 16;
+  const long long want = static_cast<long long>((n16 + 255) / 256);
+  const int grid = static_cast<int>(want < 4LL * num_sms ? (want > 0 ? want : 1) : 4LL * num_sms);
+  fwd_bf16::e4m3_to_bf16_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint4*>(v),
+                                                         static_cast<uint4*>(workspace), n16);
+  if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+  return fwd_bf16::launch_impl<128, false, false, true>(q, k, workspace, o, lse, B, Hq, Hkv, Nq, Nk,
+                                                       scale * q_scale * k_scale, causal, window,
+                                                       num_sms, stream, err, nullptr, nullptr, 0, 0,
+                                                       0.f, nullptr, v_scale);
 }
 
 }  // namespace attn

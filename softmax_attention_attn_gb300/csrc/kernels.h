@@ -80,6 +80,7 @@ struct FwdParams {
   float cap_long[6];
   float cap_smax_short, cap_smax_long;
   const float* sinks;
+  float o_scale;     // multiplies O (the V dequantisation scale of E4M3 inputs; else 1)
 };
 
 // Tensor maps (cuTensorMapEncodeTiled, fetched from the driver at run time).
@@ -106,6 +107,13 @@ int launch_fwd_tc(const void* q, const void* k, const void* v, void* o, float* l
 // zeroed and accumulated in fp32, dK and dV written in bf16.  Head dimension
 // D = 64 or 128.
 size_t bwd_workspace_bytes(int B, int Hq, int Nq);
+// fp8 prefill: E4M3 q [B,Hq,Nq,128], k / v [B,Hkv,Nk,128] (codes, per-tensor
+// scales); V is widened to bf16 into `workspace` (fwd_fp8_workspace_bytes) first.
+size_t fwd_fp8_workspace_bytes(int B, int Hkv, int Nk, int D);
+int launch_fwd_fp8(const void* q, const void* k, const void* v, float q_scale, float k_scale,
+                   float v_scale, void* o, float* lse, void* workspace, int B, int Hq, int Hkv,
+                   int Nq, int Nk, int D, float scale, int causal, int window, int num_sms,
+                   cudaStream_t stream, int* err);
 int launch_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
                const float* lse, float* dq, void* dk, void* dv, void* workspace, int B, int Hq,
                int Hkv, int Nq, int Nk, int D, float scale, int causal, int window, cudaStream_t stream,

@@ -224,6 +224,19 @@ __device__ __forceinline__ void mma_bf16_ss_if(uint32_t issue, uint32_t d_tmem, 
       : "memory");
 }
 
+// S (tmem, fp32) (+)= A (smem) x B (smem)^T with 8-bit A/B (kind::f8f6f4; the
+// formats are in the instruction descriptor): one K = 32 step of 32 bytes per row.
+__device__ __forceinline__ void mma_f8_ss_if(uint32_t issue, uint32_t d_tmem, uint64_t a_desc,
+                                             uint64_t b_desc, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "setp.ne.b32 q, %5, 0;\n\t"
+      "@q tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(issue)
+      : "memory");
+}
+
 __device__ __forceinline__ void mma_bf16_ts_if(uint32_t issue, uint32_t d_tmem, uint32_t a_tmem,
                                                uint64_t b_desc, uint32_t idesc, uint32_t accumulate) {
   asm volatile(
@@ -337,6 +350,11 @@ __host__ __device__ constexpr uint32_t idesc_f16kind_f32(uint32_t M, uint32_t N,
                                                          uint32_t ab_format) {
   return (1u << 4) | (ab_format << 7) | (ab_format << 10) | (b_mn_major << 16) | ((N >> 3) << 17) |
          ((M >> 4) << 24);
+}
+// Instruction descriptor for kind::f8f6f4 with E4M3 A and B (format code 0 in
+// bits 7-9 and 10-12), both K-major, fp32 D; the other fields as above.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(uint32_t M, uint32_t N) {
+  return (1u << 4) | (0u << 7) | (0u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N, uint32_t b_mn_major) {
   return idesc_f16kind_f32(M, N, b_mn_major, 1u);

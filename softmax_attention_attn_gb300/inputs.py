@@ -10,6 +10,9 @@ Recipe (every draw uses ``torch.Generator("cpu")``):
 * prefill workloads: one generator seeded with ``seed`` draws fp32 N(0, 1)
   tensors in the order Q ``[B,Hq,Nq,D]``, K ``[B,Hkv,Nk,D]``, V ``[B,Hkv,Nk,D]``;
   bf16 / fp16 workloads cast those fp32 values with round-to-nearest-even.
+* fp8 prefill workloads (``prefill_inputs_fp8``): the same fp32 draws rounded
+  to the nearest OCP FP8 E4M3 value (torch's float8_e4m3fn conversion) and
+  stored as uint8 codes; the per-tensor scales are the caller's.
 * decode workloads: a generator seeded with ``seed`` draws the per-sequence
   key counts ``Nk_b ~ U{nk_lo..nk_hi}`` first and then Q ``[B,Hq,D]``.  Sequence
   ``b`` then draws its own K and V rows ``[Nk_b,Hkv,D]`` (K first) from a
@@ -53,6 +56,14 @@ def prefill_inputs(B: int, Hq: int, Hkv: int, Nq: int, Nk: int, D: int,
     k = torch.randn(B, Hkv, Nk, D, generator=g, dtype=torch.float32)
     v = torch.randn(B, Hkv, Nk, D, generator=g, dtype=torch.float32)
     return _cast(q, dtype), _cast(k, dtype), _cast(v, dtype)
+
+
+def prefill_inputs_fp8(B: int, Hq: int, Hkv: int, Nq: int, Nk: int, D: int, seed: int = 0,
+                       fmt: str = "e4m3"):
+    """The fp32 draws of :func:`prefill_inputs` rounded to the nearest value of the
+    fp8 format ``fmt`` and returned as its uint8 codes (Q, K, V)."""
+    q, k, v = prefill_inputs(B, Hq, Hkv, Nq, Nk, D, "fp32", seed)
+    return _codes(q, fmt), _codes(k, fmt), _codes(v, fmt)
 
 
 def varlen_inputs(lens_q, lens_k, Hq: int, Hkv: int, D: int, dtype: str = "bf16", seed: int = 0):

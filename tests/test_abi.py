@@ -30,7 +30,7 @@ def declared_functions():
 def test_header_declares_entry_points():
     names = declared_functions()
     for must in ("attn_fwd", "attn_fwd_fp16", "attn_fwd_fp32", "attn_decode_splitkv", "attn_decode_combine",
-                 "attn_decode_splitkv_fp8", "attn_decode_splitkv_paged_fp8",
+                 "attn_decode_splitkv_fp8", "attn_decode_splitkv_paged_fp8", "attn_fwd_fp8",
                  "attn_decode_workspace_size", "attn_get_device_error", "attn_strerror"):
         assert must in names
 
@@ -176,6 +176,30 @@ def test_softcap_sink_argument_errors(L):
     assert f(cap=float("nan")) == -6
     assert f(cap=float("inf")) == -6
     assert f(sinks=ctypes.c_void_p(258)) == -5   # not 4-byte aligned
+
+
+def test_fp8_forward_argument_errors(L):
+    def f(q=P, k=P, v=P, qs=1.0, ks=1.0, vs=1.0, o=P, lse=P, ws=P, B=1, Hq=4, Hkv=2, Nq=8, Nk=8, D=128,
+          scale=0.1, causal=0, window=0):
+        return L.attn_fwd_fp8(q, k, v, qs, ks, vs, o, lse, ws, B, Hq, Hkv, Nq, Nk, D, scale, causal, window,
+                              None)
+
+    assert f(v=None) == -1
+    assert f(ws=None) == -1
+    assert f(Nq=0) == -2
+    assert f(Hq=6, Hkv=4) == -3
+    assert f(D=64) == -4
+    assert f(D=256) == -4
+    assert f(ws=MIS) == -5
+    assert f(q=MIS) == -5
+    assert f(qs=0.0) == -6
+    assert f(ks=float("nan")) == -6
+    assert f(vs=-1.0) == -6
+    assert f(vs=float("inf")) == -6
+    assert f(scale=1e-30, qs=1e-10, ks=1e-10) == -6      # product underflows to 0
+    assert f(scale=1e30, qs=1e10, ks=1e10) == -6         # product overflows
+    assert L.attn_fwd_fp8_workspace_size(2, 8, 1000, 128) == 2 * 8 * 1000 * 128 * 2
+    assert L.attn_fwd_fp8_workspace_size(0, 8, 1000, 128) == 0
 
 
 def test_backward_argument_errors(L):

@@ -276,6 +276,87 @@ def test_bf16_benchmark_workloads_full(dev, name, B, Hq, Hkv, N, causal):
     assert err_o <= BF16_O_TOL and err_l <= BF16_LSE_REL, f"O err {err_o:.3e}, LSE err {err_l:.3e}"
 
 
+# ---------------------------------------------------------------- fp8 (E4M3) Q/K/V prefill
+def run_fp8(dev, B, Hq, Hkv, Nq, Nk, causal=False, window=0, seed=0, scales=(1.0, 1.0, 1.0)):
+    q, k, v = inputs.prefill_inputs_fp8(B, Hq, Hkv, Nq, Nk, 128, seed)
+    gw = guarded((binding.attn_fwd_fp8_workspace_size(B, Hkv, Nk, 128),), torch.uint8, dev)
+    go, gl = guarded((B, Hq, Nq, 128), torch.bfloat16, dev), guarded((B, Hq, Nq), torch.float32, dev)
+    o, lse = binding.attn_fwd_fp8(q.to(dev), k.to(dev), v.to(dev), *scales, go.t, gl.t, gw.t,
+                                  causal=causal, window=window)
+    check_guards(gw, go, gl)
+    return q.numpy(), k.numpy(), v.numpy(), o, lse
+
+
+FP8_CASES = [  # (B, Hq, Hkv, Nq, Nk, causal, window, (q_scale, k_scale, v_scale))
+    (1, 2, 2, 128, 128, False, 0, (1.0, 1.0, 1.0)),      # one tile
+    (1, 2, 2, 300, 300, False, 0, (2.0, 0.5, 0.75)),     # ragged tail, scales folded
+    (2, 4, 2, 513, 513, True, 0, (1.0, 1.0, 1.0)),       # GQA, causal, ragged
+    (1, 2, 1, 256, 1000, True, 0, (0.25, 4.0, 3.0)),     # Nq < Nk
+    (1, 2, 2, 700, 300, True, 0, (1.0, 1.0, 1.0)),       # Nq > Nk: fully masked rows
+    (1, 2, 2, 1000, 1000, True, 100, (1.0, 1.0, 1.0)),   # causal + window
+    (1, 2, 2, 600, 600, False, 64, (1.0, 1.0, 1.0)),     # window only
+    (1, 1, 1, 1, 1, False, 0, (1.0, 1.0, 1.0)),
+    (1, 3, 1, 257, 129, False, 0, (1.0, 1.0, 1.0)),
+    (1, 4, 4, 1024, 1024, False, 0, (0.5, 0.5, 1.0)),    # several full K/V tiles
+]
+
+
+@pytest.mark.parametrize("case", FP8_CASES, ids=str)
+def test_fp8_prefill_cases(dev, case):
+    B, Hq, Hkv, Nq, Nk, causal, window, scales = case
+    q, k, v, o, lse = run_fp8(dev, B, Hq, Hkv, Nq, Nk, causal, window, seed=23, scales=scales)
+    O, L = oracle.attention_forward_fp8(q, k, v, *scales, 1 / math.sqrt(128), causal, window)
+    err = check(o, lse, O, L, BF16_O_TOL, BF16_LSE_REL, True)
+    print(f"[achieved] fp8 prefill {case}: O err {err:.3e}")
+    assert binding.get_device_error() == 0
+
+
+def test_fp8_prefill_benchmark_workload_full(dev):
+    """The benchmark's fp8 prefill workload (B=1 H=32 N=8192 D=128 dense, its draws and
+    launch): every O and LSE element against the oracle, one head per task."""
+    B, H, N = 1, 32, 8192
+    q, k, v, o, lse = run_fp8(dev, B, H, H, N, N, seed=0)
+    o, lse = o.float().cpu().numpy(), lse.cpu().numpy()
+
+    def one(h):
+        O, L = oracle.attention_forward_fp8(q[:, h:h + 1], k[:, h:h + 1], v[:, h:h + 1], 1.0, 1.0, 1.0,
+                                            1 / math.sqrt(128))
+        return compare_rows(o[0, h], lse[0, h], O[0, 0], L[0, 0])
+
+    res = parallel_map(one, range(H))
+    err_o = max(r[0] for r in res)
+    err_l = max(r[1] for r in res)
+    print(f"[achieved] fp8 prefill B1 H32 N8192 full: O err {err_o:.3e}, LSE err {err_l:.3e}")
+    assert all(r[2] for r in res), "non-finite output or LSE finiteness mismatch"
+    assert err_o <= BF16_O_TOL and err_l <= BF16_LSE_REL, f"O err {err_o:.3e}, LSE err {err_l:.3e}"
+
+
+def test_fp8_prefill_extreme_codes(dev):
+    """Q and K at the largest E4M3 magnitude (448) and V with subnormal and maximal codes,
+    with scales that keep the scaled scores moderate: the fp32 accumulation of 448^2
+    products and the exact widening of every V code."""
+    B, H, N = 1, 2, 384
+    g = torch.Generator("cpu").manual_seed(29)
+    q = torch.randint(0, 256, (B, H, N, 128), generator=g, dtype=torch.uint8)
+    k = torch.randint(0, 256, (B, H, N, 128), generator=g, dtype=torch.uint8)
+    v = torch.randint(0, 256, (B, H, N, 128), generator=g, dtype=torch.uint8)
+    for t in (q, k, v):
+        t[(t & 0x7F) == 0x7F] = 0x7E         # +-448 instead of NaN
+    q[0, 0, :64] = 0x7E                      # rows of +448
+    k[0, 0, 5::7] = 0x7E
+    v[0, 1, ::3] = 0x01                      # smallest subnormal
+    scales = (1.0 / 448, 1.0 / 448, 0.01)
+    gw = guarded((binding.attn_fwd_fp8_workspace_size(B, H, N, 128),), torch.uint8, dev)
+    go, gl = guarded((B, H, N, 128), torch.bfloat16, dev), guarded((B, H, N), torch.float32, dev)
+    o, lse = binding.attn_fwd_fp8(q.to(dev), k.to(dev), v.to(dev), *scales, go.t, gl.t, gw.t, causal=True)
+    check_guards(gw, go, gl)
+    O, L = oracle.attention_forward_fp8(q.numpy(), k.numpy(), v.numpy(), *scales, 1 / math.sqrt(128), True)
+    check(o, lse, O, L, BF16_O_TOL, BF16_LSE_REL, True)
+    # the widened V in the workspace is the exact bf16 value of every code
+    wide = gw.t.view(torch.bfloat16).view(B, H, N, 128).float().cpu().numpy()
+    assert np.array_equal(wide, oracle.e4m3_to_float(v.numpy()).astype(np.float32))
+
+
 # ---------------------------------------------------------------- decode
 def run_decode(dev, B, Hq, Hkv, lens, nk_max, chunk, seed=0, D=128, fill=None):
     _, q = inputs.decode_seqlens_and_q(B, Hq, D, 1, 2, seed)
