@@ -15,7 +15,10 @@
 //     rows of section 五, the 16-byte chunks of each K row are XOR-swizzled by the
 //     row index, so the 16 K rows that a half-warp reads at one column fall into
 //     different banks; Q, V and P reads are broadcasts or contiguous;
-//   * exponentials use the exp2 form 2^(s*scale*log2 e - m).
+//   * exponentials use the exp2 form 2^(s*scale*log2 e - m);
+//   * the Q K^T and P V products run as packed pairs (fma.rn.f32x2: two IEEE fp32
+//     FMAs per instruction, so the FMA pipe is kept busy with half the issue slots
+//     and the shared-memory loads issue in between).
 // No TF32 or other reduced-precision arithmetic is used.
 #include <cuda_runtime.h>
 #include <math_constants.h>
@@ -120,42 +123,54 @@ __global__ void __launch_bounds__(NT, 2) attn_fwd_fp32_kernel(const float* __res
   if (n_tiles > 0) load_rows<D, false>(Vs, Vh, j_begin * BN, Nk);
   cp_async_commit();
 
-  float m[4], l[4], acc[4][DC];
+  // O accumulators as packed pairs of adjacent output columns (fma.rn.f32x2)
+  constexpr int DP = DC / 2;
+  float m[4], l[4];
+  uint64_t acc[4][DP];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     m[i] = -CUDART_INF_F;
     l[i] = 0.f;
 #pragma unroll
-    for (int d = 0; d < DC; ++d) acc[i][d] = 0.f;
+    for (int d = 0; d < DP; ++d) acc[i][d] = 0ull;
   }
 
   for (int jj = 0; jj < n_tiles; ++jj) {
     cp_async_wait<1>();
     __syncthreads();  // K_j (and Q) visible; everyone is done with P V_j-1 (P buffer free)
 
-    // ---- scores: rows ty*4+i, keys tx+16*n
-    float s[4][4];
+    // ---- scores: rows ty*4+i, keys tx+16*n.  Packed fp32 pairs (fma.rn.f32x2, two
+    // IEEE fp32 FMAs per instruction): s2 holds the partial sums over even and odd d,
+    // added at the end; a 16-byte load gives the pairs (d, d+1) and (d+2, d+3).
+    uint64_t s2[4][4];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
-      for (int n = 0; n < 4; ++n) s[i][n] = 0.f;
+      for (int n = 0; n < 4; ++n) s2[i][n] = 0ull;
 #pragma unroll 4
     for (int d = 0; d < D; d += 4) {
-      float4 qv[4], kv[4];
+      ulonglong2 qv[4], kv[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) qv[i] = *reinterpret_cast<const float4*>(Qs + (ty * 4 + i) * D + d);
+      for (int i = 0; i < 4; ++i) qv[i] = *reinterpret_cast<const ulonglong2*>(Qs + (ty * 4 + i) * D + d);
 #pragma unroll
-      for (int n = 0; n < 4; ++n) kv[n] = *reinterpret_cast<const float4*>(Ks + k_off<D>(tx + 16 * n, d >> 2));
+      for (int n = 0; n < 4; ++n) kv[n] = *reinterpret_cast<const ulonglong2*>(Ks + k_off<D>(tx + 16 * n, d >> 2));
 #pragma unroll
       for (int i = 0; i < 4; ++i)
 #pragma unroll
         for (int n = 0; n < 4; ++n) {
-          s[i][n] = fmaf(qv[i].x, kv[n].x, s[i][n]);
-          s[i][n] = fmaf(qv[i].y, kv[n].y, s[i][n]);
-          s[i][n] = fmaf(qv[i].z, kv[n].z, s[i][n]);
-          s[i][n] = fmaf(qv[i].w, kv[n].w, s[i][n]);
+          s2[i][n] = f2_fma(qv[i].x, kv[n].x, s2[i][n]);
+          s2[i][n] = f2_fma(qv[i].y, kv[n].y, s2[i][n]);
         }
     }
+    float s[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int n = 0; n < 4; ++n) {
+        float e, o;
+        f2_unpack(s2[i][n], e, o);
+        s[i][n] = e + o;
+      }
     __syncthreads();  // everyone is done with K_j: stream K_j+1 in during the softmax and P V
     if (jj + 1 < n_tiles) load_rows<D, true>(Ks, Kh, (j_begin + jj + 1) * BN, Nk);
     cp_async_commit();
@@ -195,8 +210,9 @@ __global__ void __launch_bounds__(NT, 2) attn_fwd_fp32_kernel(const float* __res
 #pragma unroll
       for (int o = 8; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
       l[i] = l[i] * alpha + sum;
+      const uint64_t alpha2 = f2_pack(alpha, alpha);
 #pragma unroll
-      for (int d = 0; d < DC; ++d) acc[i][d] *= alpha;
+      for (int d = 0; d < DP; ++d) acc[i][d] = f2_mul(acc[i][d], alpha2);
     }
     cp_async_wait<1>();
     __syncthreads();  // P tile complete; V_j visible
@@ -210,24 +226,23 @@ __global__ void __launch_bounds__(NT, 2) attn_fwd_fp32_kernel(const float* __res
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const float* vrow = Vs + (kk + u) * D;
-        float vv[DC];
+        uint64_t vv[DP];   // pairs of adjacent columns
         if constexpr (DC == 8) {
-          const float4 a = *reinterpret_cast<const float4*>(vrow + tx * 4);
-          const float4 bb = *reinterpret_cast<const float4*>(vrow + 64 + tx * 4);
-          vv[0] = a.x; vv[1] = a.y; vv[2] = a.z; vv[3] = a.w;
-          vv[4] = bb.x; vv[5] = bb.y; vv[6] = bb.z; vv[7] = bb.w;
+          const ulonglong2 a = *reinterpret_cast<const ulonglong2*>(vrow + tx * 4);
+          const ulonglong2 bb = *reinterpret_cast<const ulonglong2*>(vrow + 64 + tx * 4);
+          vv[0] = a.x; vv[1] = a.y; vv[2] = bb.x; vv[3] = bb.y;
         } else if constexpr (DC == 4) {
-          const float4 a = *reinterpret_cast<const float4*>(vrow + tx * 4);
-          vv[0] = a.x; vv[1] = a.y; vv[2] = a.z; vv[3] = a.w;
-        } else {
-          const float2 a = *reinterpret_cast<const float2*>(vrow + tx * 2);
+          const ulonglong2 a = *reinterpret_cast<const ulonglong2*>(vrow + tx * 4);
           vv[0] = a.x; vv[1] = a.y;
+        } else {
+          vv[0] = *reinterpret_cast<const unsigned long long*>(vrow + tx * 2);
         }
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const float pw = u == 0 ? pr[i].x : u == 1 ? pr[i].y : u == 2 ? pr[i].z : pr[i].w;
+          const uint64_t pw2 = f2_pack(pw, pw);
 #pragma unroll
-          for (int d = 0; d < DC; ++d) acc[i][d] = fmaf(pw, vv[d], acc[i][d]);
+          for (int d = 0; d < DP; ++d) acc[i][d] = f2_fma(pw2, vv[d], acc[i][d]);
         }
       }
     }
@@ -244,16 +259,20 @@ __global__ void __launch_bounds__(NT, 2) attn_fwd_fp32_kernel(const float* __res
     if (row >= Nq) continue;
     const float inv_l = l[i] > 0.f ? 1.f / l[i] : 0.f;
     float* orow = O + ((static_cast<size_t>(b) * Hq + h) * Nq + row) * D;
+    float a[DC];
+#pragma unroll
+    for (int d = 0; d < DP; ++d) {
+      f2_unpack(acc[i][d], a[2 * d], a[2 * d + 1]);
+      a[2 * d] *= inv_l;
+      a[2 * d + 1] *= inv_l;
+    }
     if constexpr (DC == 8) {
-      *reinterpret_cast<float4*>(orow + tx * 4) =
-          make_float4(acc[i][0] * inv_l, acc[i][1] * inv_l, acc[i][2] * inv_l, acc[i][3] * inv_l);
-      *reinterpret_cast<float4*>(orow + 64 + tx * 4) =
-          make_float4(acc[i][4] * inv_l, acc[i][5] * inv_l, acc[i][6] * inv_l, acc[i][7] * inv_l);
+      *reinterpret_cast<float4*>(orow + tx * 4) = make_float4(a[0], a[1], a[2], a[3]);
+      *reinterpret_cast<float4*>(orow + 64 + tx * 4) = make_float4(a[4], a[5], a[6], a[7]);
     } else if constexpr (DC == 4) {
-      *reinterpret_cast<float4*>(orow + tx * 4) =
-          make_float4(acc[i][0] * inv_l, acc[i][1] * inv_l, acc[i][2] * inv_l, acc[i][3] * inv_l);
+      *reinterpret_cast<float4*>(orow + tx * 4) = make_float4(a[0], a[1], a[2], a[3]);
     } else {
-      *reinterpret_cast<float2*>(orow + tx * 2) = make_float2(acc[i][0] * inv_l, acc[i][1] * inv_l);
+      *reinterpret_cast<float2*>(orow + tx * 2) = make_float2(a[0], a[1]);
     }
     if (tx == 0 && LSE != nullptr)
       LSE[(static_cast<size_t>(b) * Hq + h) * Nq + row] =
