@@ -74,11 +74,15 @@ struct Cfg {
   static constexpr int QK_SLABS = HD / QK_BOX;          // 128-byte slabs per Q/K tile row
   static constexpr int QK_TILE_BYTES = QK_SLABS * KBLK_BYTES;  // one 128-row Q or K tile
   static constexpr int QK_STEPS = QK8 ? HD / 32 : HD / 16;     // MMAs of one Q K^T (32 bytes of K each)
-  static constexpr int STAGES = HD == 128 ? (QK8 ? 6 : 5) : 10;  // K/V ring slots (one K or V tile each)
+  static constexpr int STAGES = HD == 128 ? (QK8 ? 5 : 4) : 10;  // K/V ring slots (one K or V tile each)
+  // Q tile buffers: three rotate over the Q tiles of successive units (tile t of the
+  // n-th unit with work in buffer (2n + t) % 3), so the next unit's Q tile 0 loads
+  // while the current unit runs and its Q tile 1 as soon as the current tile 0 is done
+  static constexpr int NQB = 3;
   static constexpr int SMEM_Q = 0;
-  static constexpr int SMEM_RING = SMEM_Q + NQT * QK_TILE_BYTES;
+  static constexpr int SMEM_RING = SMEM_Q + NQB * QK_TILE_BYTES;
   static constexpr int SMEM_BAR = SMEM_RING + STAGES * TILE_BYTES;
-  static constexpr int NUM_BARS = 3 + 2 * STAGES + 5 * NQT;
+  static constexpr int NUM_BARS = 2 * NQB + 1 + 2 * STAGES + 5 * NQT;
   static constexpr int SMEM_MISC = SMEM_BAR + NUM_BARS * 8;
   static constexpr int SMEM_ALLOC = SMEM_MISC + 16 + 1024;  // + slack for 1024-byte alignment
   static constexpr uint32_t AB_FORMAT = F16 ? 0u : 1u;  // instruction-descriptor A/B format
@@ -329,12 +333,14 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
   const int lane = static_cast<int>(lane_id());
 
   // ---- barriers (phases run on across the units a CTA processes)
-  const uint32_t bar_q_full = sb + SMEM_BAR;            // Q tiles of a unit landed
-  const uint32_t bar_q_empty = sb + SMEM_BAR + 8;       // the last S of both Q tiles of a unit done
-  const uint32_t bar_mma_done = sb + SMEM_BAR + 16;     // every MMA issued has completed
-  auto bar_kv_full = [&](int s) { return sb + SMEM_BAR + 8u * (3 + s); };
-  auto bar_kv_empty = [&](int s) { return sb + SMEM_BAR + 8u * (3 + STAGES + s); };
-  auto bar_t = [&](int kind, int t) { return sb + SMEM_BAR + 8u * (3 + 2 * STAGES + kind * NQT + t); };
+  constexpr int NQB = C::NQB;
+  constexpr int B0 = 2 * NQB + 1;                       // first barrier after the Q and done barriers
+  auto bar_q_full = [&](int qb) { return sb + SMEM_BAR + 8u * qb; };          // Q tile in buffer qb landed
+  auto bar_q_empty = [&](int qb) { return sb + SMEM_BAR + 8u * (NQB + qb); }; // its last S done
+  const uint32_t bar_mma_done = sb + SMEM_BAR + 8u * (2 * NQB);               // every MMA issued has completed
+  auto bar_kv_full = [&](int s) { return sb + SMEM_BAR + 8u * (B0 + s); };
+  auto bar_kv_empty = [&](int s) { return sb + SMEM_BAR + 8u * (B0 + STAGES + s); };
+  auto bar_t = [&](int kind, int t) { return sb + SMEM_BAR + 8u * (B0 + 2 * STAGES + kind * NQT + t); };
   auto bar_s_full = [&](int t) { return bar_t(0, t); };   // S_t of a key tile in TMEM
   auto bar_p_lo = [&](int t) { return bar_t(1, t); };     // P_t keys 0-63 in TMEM (+ O_t rescaled)
   auto bar_p_hi = [&](int t) { return bar_t(2, t); };     // P_t keys 64-127 in TMEM
@@ -348,8 +354,10 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
   const int n_units = n_qblk * p.Hq * p.B;
 
   if (threadIdx.x == 0) {
-    mbar_init(bar_q_full, 1);
-    mbar_init(bar_q_empty, NQT);
+    for (int qb = 0; qb < NQB; ++qb) {
+      mbar_init(bar_q_full(qb), 1);
+      mbar_init(bar_q_empty(qb), 1);   // released by the issuer of the tile it holds
+    }
     mbar_init(bar_mma_done, NQT);
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(bar_kv_full(s), 1);
@@ -383,23 +391,33 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       int it = 0;   // ring position (runs on across units)
-      int nq = 0;   // units with work so far (phase of q_full / q_empty)
+      int nq = 0;   // units with work so far
+      int nql = 0;  // Q tiles loaded so far (tile t of unit n is load 2n + t)
       bool ok = true;
+      // Q tile t of the current unit into buffer nql % NQB, once the tile it held is done
+      auto load_q = [&](const Unit& u, int t) -> bool {
+        const int qb = nql % NQB, use = nql / NQB;
+        if (use > 0 && !mbar_wait(bar_q_empty(qb), (use - 1) & 1, abort_flag, p.err)) return false;
+        mbar_arrive_expect_tx(bar_q_full(qb), QK_TILE_BYTES);
+        for (int kb = 0; kb < QK_SLABS; ++kb)
+          if (p.varlen)
+            tma_load_3d(sb + SMEM_Q + qb * QK_TILE_BYTES + kb * KBLK_BYTES, &tm_q, bar_q_full(qb),
+                        kb * QK_BOX, u.h, u.q_tok + u.q0 + t * BM);
+          else
+            tma_load_3d(sb + SMEM_Q + qb * QK_TILE_BYTES + kb * KBLK_BYTES, &tm_q, bar_q_full(qb),
+                        kb * QK_BOX, u.q0 + t * BM, u.b * p.Hq + u.h);
+        ++nql;
+        return true;
+      };
       for (int pass = 0, w = unit_of_pass(0); w < n_units && ok; w = unit_of_pass(++pass)) {
         const Unit u = make_unit(w, p, n_qblk);
         if (u.j_end <= u.j_begin) continue;
-        if (nq > 0 && !mbar_wait(bar_q_empty, (nq - 1) & 1, abort_flag, p.err)) { ok = false; break; }
-        mbar_arrive_expect_tx(bar_q_full, NQT * QK_TILE_BYTES);
-        for (int t = 0; t < NQT; ++t)
-          for (int kb = 0; kb < QK_SLABS; ++kb)
-            if (p.varlen)
-              tma_load_3d(sb + SMEM_Q + t * QK_TILE_BYTES + kb * KBLK_BYTES, &tm_q, bar_q_full,
-                          kb * QK_BOX, u.h, u.q_tok + u.q0 + t * BM);
-            else
-              tma_load_3d(sb + SMEM_Q + t * QK_TILE_BYTES + kb * KBLK_BYTES, &tm_q, bar_q_full,
-                          kb * QK_BOX, u.q0 + t * BM, u.b * p.Hq + u.h);
+        // Q tile 0 (its buffer freed a unit ago), the first K/V pair, then Q tile 1 (its
+        // buffer is the previous unit's tile 0), so that tile 0 can start while tile 1 waits
+        if (!load_q(u, 0)) { ok = false; break; }
         ++nq;
         for (int j = u.j_begin; j < u.j_end && ok; ++j) {
+          if (j == u.j_begin + 1 && !load_q(u, 1)) { ok = false; break; }
           for (int kv = 0; kv < 2; ++kv, ++it) {
             const int s = it % STAGES, use = it / STAGES;
             if (use > 0 && !mbar_wait(bar_kv_empty(s), (use - 1) & 1, abort_flag, p.err)) {
@@ -420,9 +438,10 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
                             kb * box_x, j * BN, u.b * p.Hkv + u.kvh);
           }
         }
+        if (ok && u.j_end == u.j_begin + 1 && !load_q(u, 1)) { ok = false; break; }  // one-tile unit
       }
       if (!ok) {  // give up: let the copies already issued land before the CTA exits
-        if (nq > 0) drain_wait(bar_q_full, (nq - 1) & 1);
+        for (int i = max(0, nql - 2); i < nql; ++i) drain_wait(bar_q_full(i % NQB), (i / NQB) & 1);
         for (int i = max(0, it - STAGES); i < it; ++i) drain_wait(bar_kv_full(i % STAGES), (i / STAGES) & 1);
       }
     }
@@ -463,7 +482,6 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
           }
         }
       };
-      const uint64_t q_desc = smem_desc_sw128(sb + SMEM_Q + t * QK_TILE_BYTES, 16, 1024);
       const uint64_t k_desc0 = smem_desc_sw128(sb + SMEM_RING, 16, 1024);
       const uint64_t v_desc0 = smem_desc_sw128(sb + SMEM_RING, KBLK_BYTES, 1024);
       auto k_desc = [&](RingPos r) { return desc_add(k_desc0, static_cast<uint32_t>(r.slot * TILE_BYTES) >> 4); };
@@ -480,7 +498,10 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
         int jb, je;
         own_range(u, t, jb, je);
         if (je <= jb) jb = je = u.j_end;  // no own tiles: the slots are only released
-        if (!mbar_wait(bar_q_full, nq & 1, abort_flag, p.err)) { ok = false; break; }
+        // this unit's Q tile t: load 2 nq + t
+        const int qb = (2 * nq + t) % NQB;
+        if (!mbar_wait(bar_q_full(qb), ((2 * nq + t) / NQB) & 1, abort_flag, p.err)) { ok = false; break; }
+        const uint64_t q_desc = smem_desc_sw128(sb + SMEM_Q + qb * QK_TILE_BYTES, 16, 1024);
         if (jb < je) {  // first S of this unit (outside the turn order)
           const RingPos r = ring_pos<STAGES>(it_base + 2 * (jb - u.j_begin));
           if (!wait_full(r)) { ok = false; break; }
@@ -488,9 +509,9 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
           issue_qk<HD, F16, QK8>(elect, tmem + s_col(t), q_desc, k_desc(r));
           mma_commit_if(elect, bar_s_full(t));
           mma_commit_if(elect, bar_kv_empty(r.slot));
-          if (je - jb == 1) mma_commit_if(elect, bar_q_empty);  // that was this unit's last S
+          if (je - jb == 1) mma_commit_if(elect, bar_q_empty(qb));  // that was this unit's last S
         } else {
-          mbar_arrive_if(elect, bar_q_empty);
+          mbar_arrive_if(elect, bar_q_empty(qb));
         }
         RingPos kj = ring_pos<STAGES>(it_base);  // K of key tile j
         for (int j = u.j_begin; j < u.j_end && ok; ++j) {
@@ -531,7 +552,7 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
             } else {
               mma_commit_if(elect, bar_s_full(t));
               mma_commit_if(elect, bar_kv_empty(kn.slot));
-              if (j + 2 == je) mma_commit_if(elect, bar_q_empty);  // this unit's last S
+              if (j + 2 == je) mma_commit_if(elect, bar_q_empty(qb));  // this unit's last S
             }
           } else {
             // outside this Q tile's range: release both slots once they are filled
@@ -774,15 +795,21 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
         inv_l *= p.o_scale;
         const size_t orow_idx = p.varlen ? static_cast<size_t>(u.q_tok + row) * p.Hq + u.h
                                          : (static_cast<size_t>(u.b) * p.Hq + u.h) * p.Nq + row;
-        uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + orow_idx * HD);
+        uint16_t* orow = static_cast<uint16_t*>(p.o) + orow_idx * HD;
+        // the row's HD outputs, normalised and packed: word k holds outputs 2k, 2k + 1
+        uint32_t w[HD / 2];
 #pragma unroll
-        for (int i = 0; i < HD / 8; ++i) {
-          const uint4 v4 = make_uint4(
-              pack2<F16>(__uint_as_float(o[8 * i + 0]) * inv_l, __uint_as_float(o[8 * i + 1]) * inv_l),
-              pack2<F16>(__uint_as_float(o[8 * i + 2]) * inv_l, __uint_as_float(o[8 * i + 3]) * inv_l),
-              pack2<F16>(__uint_as_float(o[8 * i + 4]) * inv_l, __uint_as_float(o[8 * i + 5]) * inv_l),
-              pack2<F16>(__uint_as_float(o[8 * i + 6]) * inv_l, __uint_as_float(o[8 * i + 7]) * inv_l));
-          orow[i] = v4;
+        for (int k = 0; k < HD / 2; ++k)
+          w[k] = pack2<F16>(__uint_as_float(o[2 * k]) * inv_l, __uint_as_float(o[2 * k + 1]) * inv_l);
+        if (p.o_align32) {
+          // 32-byte stores: each thread writes its own row, so a warp's store touches 32
+          // rows; whole 32-byte sectors halve the write requests of 16-byte stores
+#pragma unroll
+          for (int i = 0; i < HD / 16; ++i) st_global_v8(orow + 16 * i, &w[8 * i]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < HD / 8; ++i)
+            reinterpret_cast<uint4*>(orow)[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
         }
         if (p.lse != nullptr) {
           const float lse = lse_val;
@@ -881,6 +908,7 @@ int launch_impl(const void* q, const void* k, const void* v, void* o, float* lse
   prescale(kTanhPolyLong, 6, kTanhPolyLongYMax, prm.cap_long, &prm.cap_smax_long);
   prm.sinks = sinks;
   prm.o_scale = o_scale;
+  prm.o_align32 = (reinterpret_cast<uintptr_t>(o) & 31u) == 0 ? 1 : 0;
   // persistent: at most one CTA per SM, each walking units blockIdx.x, +gridDim.x, ...
   const long long n_qblk = (Nq + BM * NQT - 1) / (BM * NQT);
   const long long units = n_qblk * Hq * B;

@@ -81,6 +81,7 @@ struct FwdParams {
   float cap_smax_short, cap_smax_long;
   const float* sinks;
   float o_scale;     // multiplies O (the V dequantisation scale of E4M3 inputs; else 1)
+  int o_align32;     // O is 32-byte aligned (rows are then written with 32-byte stores)
 };
 
 // Tensor maps (cuTensorMapEncodeTiled, fetched from the driver at run time).

@@ -360,6 +360,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N, ui
   return idesc_f16kind_f32(M, N, b_mn_major, 1u);
 }
 
+// 32-byte global store of eight 32-bit words (the address must be 32-byte aligned).
+__device__ __forceinline__ void st_global_v8(void* ptr, const uint32_t* w) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(w[0]), "r"(w[1]),
+               "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+
 // ------------------------------------------------------------------ math
 // 2^x on the special-function unit (hardware ex2, approximate, flush-to-zero).
 __device__ __forceinline__ float ex2_approx(float x) {

@@ -163,6 +163,23 @@ def test_bf16_head_dim_64(dev, case):
     check(o, lse, O, L, BF16_O_TOL, BF16_LSE_REL, True)
 
 
+@pytest.mark.parametrize("D", [64, 128])
+def test_bf16_output_only_16_byte_aligned(dev, D):
+    """O at an address that is 16- but not 32-byte aligned takes the 16-byte store path of
+    the epilogue; the result must equal the 32-byte-aligned call bit for bit."""
+    B, Hq, Hkv, N = 1, 2, 2, 300
+    q, k, v = (x.to(dev) for x in inputs.prefill_inputs(B, Hq, Hkv, N, N, D, "bf16", seed=21))
+    o_ref, lse_ref = binding.attn_fwd(q, k, v, causal=True)
+    n = B * Hq * N * D * 2
+    buf = torch.full((n + 16 + 4096,), 0xA5, dtype=torch.uint8, device=dev)
+    o16 = buf[16:16 + n].view(torch.bfloat16).view(B, Hq, N, D)
+    assert o16.data_ptr() % 32 == 16
+    binding.attn_fwd(q, k, v, o16, causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o16, o_ref)
+    assert int((buf[:16] != 0xA5).sum()) == 0 and int((buf[16 + n:] != 0xA5).sum()) == 0
+
+
 FP16_CASES = [  # (B, Hq, Hkv, Nq, Nk, D, causal, window)
     (1, 2, 2, 300, 300, 128, False, 0),
     (2, 4, 2, 513, 513, 128, True, 0),
