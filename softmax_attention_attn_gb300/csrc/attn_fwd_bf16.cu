@@ -211,6 +211,22 @@ __device__ __forceinline__ RingPos ring_next(RingPos r) {
   return r;
 }
 
+// Masks the scores of keys outside [lo, hi] (tile-relative: element i is key k0 + i):
+// one compare with a constant and one select per score without a window, an
+// unsigned range check with a window.
+__device__ __forceinline__ void apply_mask(float (&s)[BN], int hi, int lo, bool window) {
+  if (window) {
+    const uint32_t span = static_cast<uint32_t>(hi - lo);
+#pragma unroll
+    for (int i = 0; i < BN; ++i)
+      if (static_cast<uint32_t>(i - lo) > span) s[i] = -CUDART_INF_F;
+  } else {
+#pragma unroll
+    for (int i = 0; i < BN; ++i)
+      if (i > hi) s[i] = -CUDART_INF_F;
+  }
+}
+
 // Wait bounded by time only (used to drain work already in flight).
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   const unsigned long long t0 = global_ns();
@@ -655,11 +671,7 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
             rmax = p.cap_post * tanh_exp(p.cap_pre * rmax_raw);
           }
           if (need_mask) {
-#pragma unroll
-            for (int i = 0; i < BN; ++i) {
-              const int key = k0 + i;
-              if (key > hi_r || key < lo_r) s[i] = -CUDART_INF_F;
-            }
+            apply_mask(s, hi_r - k0, lo_r - k0, p.window > 0);
 #pragma unroll
             for (int g = 0; g < 8; ++g) mx[g] = fmaxf(s[g], s[8 + g]);
 #pragma unroll
@@ -670,11 +682,7 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
           }
         } else {
           if (need_mask) {
-#pragma unroll
-            for (int i = 0; i < BN; ++i) {
-              const int key = k0 + i;
-              if (key > hi_r || key < lo_r) s[i] = -CUDART_INF_F;
-            }
+            apply_mask(s, hi_r - k0, lo_r - k0, p.window > 0);
           }
 #pragma unroll
           for (int g = 0; g < 8; ++g) mx[g] = fmaxf(s[g], s[8 + g]);
