@@ -12,10 +12,11 @@
 //   * persistent CTAs (one per SM) walk a list of work units — two 128-row Q
 //     tiles of one (batch, head); causal lists put the longest units first and
 //     passes over the list alternate the direction in which units are dealt
-//     to the CTAs — and stream 128-key K/V tiles through a 5-slot TMA ring (128-byte
-//     swizzle, mbarrier transaction counts).  Barriers and tensor memory are set
-//     up once; the next unit's Q, K/V and first S overlap the last unit's
-//     epilogue;
+//     to the CTAs — and stream 128-key K/V tiles through a TMA ring (4 slots at
+//     D = 128; 128-byte swizzle, mbarrier transaction counts).  Three Q tile
+//     buffers rotate over the units' Q tiles, so the next unit's Q lands while
+//     the current one runs.  Barriers and tensor memory are set up once; the
+//     next unit's Q, K/V and first S overlap the last unit's epilogue;
 //   * warps 0 and 1 issue the tcgen05.mma of Q tile 0 and 1 (lane 0 of a
 //     converged warp): S_t = Q_t K^T into tensor memory (fp32, 128 columns per
 //     Q tile), then O_t += P_t V with P read from tensor memory (the TS form)
@@ -33,7 +34,9 @@
 //     than the highest, where they share sub-partitions with the same softmax
 //     warps either way);
 //   * the epilogue (same softmax threads) divides by the row sum, rounds O to
-//     bf16 and writes O and LSE.
+//     bf16 and writes O (32-byte stores when O is 32-byte aligned) and LSE;
+//   * with QK8, Q and K are E4M3 codes and S = Q K^T runs on kind::f8f6f4
+//     (the fp8 prefill; V arrives widened to bf16).
 //
 // The two Q tiles ping-pong: while the softmax warps of tile 0 work on tile j the
 // tensor core computes PV_1(j-1) and S_1(j), and vice versa.
