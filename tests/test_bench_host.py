@@ -105,8 +105,8 @@ def test_kernel_traffic_reads_summary_only_for_matching_source(tmp_path, monkeyp
 def _fake_run():
     """Workload records of a full run with plausible magnitudes (no GPU involved)."""
     wl = {}
-    for name in ("causal", "decode", "paged", "decode_fp8", "window", "chunked", "d64", "fp16", "varlen",
-                 "softcap", "bwd"):
+    for name in ("causal", "decode", "paged", "decode_fp8", "decode_mqa", "decode_d64", "window", "chunked",
+                 "d64", "fp16", "varlen", "softcap", "bwd", "bwd_d64", "fp8"):
         dec = name in bench.DECODE_NAMES
         e = {"workload": bench.WORKLOAD_NAMES[name], "value": 6543.21987 if dec else 1234.56789,
              "unit": "GB/s" if dec else "TFLOP/s", "ms_per_step": 0.61234567, "bound": "hbm" if dec else "tensor",
