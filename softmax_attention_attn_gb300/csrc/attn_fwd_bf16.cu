@@ -410,8 +410,7 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       int it = 0;   // ring position (runs on across units)
-      int nq = 0;   // units with work so far
-      int nql = 0;  // Q tiles loaded so far (tile t of unit n is load 2n + t)
+      int nql = 0;  // Q tiles loaded so far (tile t of the n-th unit with work is load 2n + t)
       bool ok = true;
       // Q tile t of the current unit into buffer nql % NQB, once the tile it held is done
       auto load_q = [&](const Unit& u, int t) -> bool {
@@ -434,7 +433,6 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
         // Q tile 0 (its buffer freed a unit ago), the first K/V pair, then Q tile 1 (its
         // buffer is the previous unit's tile 0), so that tile 0 can start while tile 1 waits
         if (!load_q(u, 0)) { ok = false; break; }
-        ++nq;
         for (int j = u.j_begin; j < u.j_end && ok; ++j) {
           if (j == u.j_begin + 1 && !load_q(u, 1)) { ok = false; break; }
           for (int kv = 0; kv < 2; ++kv, ++it) {
@@ -460,7 +458,7 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
         if (ok && u.j_end == u.j_begin + 1 && !load_q(u, 1)) { ok = false; break; }  // one-tile unit
       }
       if (!ok) {  // give up: let the copies already issued land before the CTA exits
-        for (int i = max(0, nql - 2); i < nql; ++i) drain_wait(bar_q_full(i % NQB), (i / NQB) & 1);
+        for (int i = max(0, nql - NQB); i < nql; ++i) drain_wait(bar_q_full(i % NQB), (i / NQB) & 1);
         for (int i = max(0, it - STAGES); i < it; ++i) drain_wait(bar_kv_full(i % STAGES), (i / STAGES) & 1);
       }
     }
