@@ -464,7 +464,7 @@ struct Geo {
 template <int HD, int G, bool KV8>
 struct Cfg {
   static constexpr int NT = (G + 7) / 8;                // MMA column blocks of 8 query heads
-  static constexpr int CTAS_PER_SM = G <= 8 ? 3 : 1;
+  static constexpr int CTAS_PER_SM = G <= 8 ? 3 : 2;
   static constexpr int SMALL_RING_BYTES = 48 * 1024;    // G <= 8
   static constexpr int NCW = G >= 16 ? 8 : 4;           // consumer warps
   static constexpr int NC = NCW * 32;
@@ -546,7 +546,7 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
 }
 
 template <int HD, int G, bool PAGED, bool KV8>
-__global__ void __launch_bounds__(Cfg<HD, G, KV8>::NTHREADS, 1)
+__global__ void __launch_bounds__(Cfg<HD, G, KV8>::NTHREADS, Cfg<HD, G, KV8>::CTAS_PER_SM > 2 ? 1 : Cfg<HD, G, KV8>::CTAS_PER_SM)
 attn_decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                        const __nv_bfloat16* __restrict__ q, const int* __restrict__ seqlens,
                        float* __restrict__ ws_o, float* __restrict__ ws_lse, int B, int Hq, int Hkv,
@@ -1049,9 +1049,12 @@ int launch_mma(const CUtensorMap& tk, const CUtensorMap& tv, const void* q, cons
   constexpr int tile = decode_mma::Geo<HDIM, KV8>::TILE_BYTES;
   constexpr int kMaxSmem = 227 * 1024;
   int stages = C::SMALL_RING_BYTES / tile;
-  if (G > 8) {   // as many ring slots as fit next to the scores (at most MAX_STAGES)
+  if (G > 8) {
+    // as many ring slots as fit next to the scores with two CTAs per SM, else with one
+    // (long chunks), at most MAX_STAGES
     const int rest = decode_mma::layout(G, chunk, B, 0).bytes + 1024;
-    stages = (kMaxSmem - rest) / tile;
+    stages = (kMaxSmem / 2 - 1024 - rest) / tile;
+    if (stages < 2) stages = (kMaxSmem - rest) / tile;
     if (stages > decode_mma::MAX_STAGES) stages = decode_mma::MAX_STAGES;
   }
   if (stages < 2) return ATTN_ERR_CAPACITY;
