@@ -453,9 +453,11 @@ struct Geo {
   static constexpr int TILE_BYTES = TILE * ROW;
 };
 
-// Residency: up to 8 query heads per KV head, three CTAs per SM with 48 KB rings;
-// with 16 or 32 the chunk's scores take 32-64 KB (chunk 512), so one CTA per SM
-// runs with as large a ring as the shared memory leaves (up to 16 tiles).
+// Residency: up to 8 query heads per KV head, three (bf16) or four (fp8) CTAs per SM
+// with 48 / 40 KB rings; with 16 or 32 the chunk's scores take 32-64 KB (chunk 512),
+// so two CTAs share an SM with the ring slots the rest of half the shared memory holds
+// (one CTA with up to 16 tiles when two do not fit).  The launch bound lets the
+// compiler keep the registers within that residency.
 // Consumer warps: four (warp w: keys [16w, 16w+16) of a tile in Q K^T, head-dimension rows
 // [w D/4, (w+1) D/4) in P V) up to 8 query heads per KV head; eight with 16 or 32, where the
 // products are long enough per item that a CTA alone on its SM needs more warps in flight
@@ -464,8 +466,11 @@ struct Geo {
 template <int HD, int G, bool KV8>
 struct Cfg {
   static constexpr int NT = (G + 7) / 8;                // MMA column blocks of 8 query heads
-  static constexpr int CTAS_PER_SM = G <= 8 ? 3 : 2;
-  static constexpr int SMALL_RING_BYTES = 48 * 1024;    // G <= 8
+  // up to 8 heads: four CTAs per SM with 40 KB rings for fp8 caches (the consumers' per-byte
+  // work needs the warps), three with 48 KB rings for bf16 (measured: fp8 5422 -> 5560 GB/s with
+  // four; bf16 D = 64 6030 -> 5560 with four); 16 or 32 heads: two
+  static constexpr int CTAS_PER_SM = G <= 8 ? (KV8 ? 4 : 3) : 2;
+  static constexpr int SMALL_RING_BYTES = (KV8 ? 40 : 48) * 1024;    // G <= 8
   static constexpr int NCW = G >= 16 ? 8 : 4;           // consumer warps
   static constexpr int NC = NCW * 32;
   static constexpr int NTHREADS = NC + 32;              // + producer warp
@@ -546,7 +551,7 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
 }
 
 template <int HD, int G, bool PAGED, bool KV8>
-__global__ void __launch_bounds__(Cfg<HD, G, KV8>::NTHREADS, Cfg<HD, G, KV8>::CTAS_PER_SM > 2 ? 1 : Cfg<HD, G, KV8>::CTAS_PER_SM)
+__global__ void __launch_bounds__(Cfg<HD, G, KV8>::NTHREADS, Cfg<HD, G, KV8>::CTAS_PER_SM)
 attn_decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                        const __nv_bfloat16* __restrict__ q, const int* __restrict__ seqlens,
                        float* __restrict__ ws_o, float* __restrict__ ws_lse, int B, int Hq, int Hkv,
