@@ -241,6 +241,7 @@ attn_decode_splitkv_kernel(const __grid_constant__ CUtensorMap tm_k,
     if (lane == 0) {
       int it = 0;
       int cached_lp = -1, cached_b = -1, cached_page = 0;
+      const uint64_t stream_policy = l2_policy_evict_first();   // the cache is read once
       bool ok = true;
       for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
         const Work wk = decode_work(w, split, B, Hkv, chunk, seqlens);
@@ -266,10 +267,10 @@ attn_decode_splitkv_kernel(const __grid_constant__ CUtensorMap tm_k,
                 atomicCAS(err, 0, ATTN_ERR_PAGE);
                 page = pg.num_pages;
               }
-              tma_load_4d(sb + L.ring + s * TILE_BYTES, m, bar_full(s), 0, wk.kvh,
-                          key0 - lp * pg.page_size, page);
+              tma_load_4d_hint(sb + L.ring + s * TILE_BYTES, m, bar_full(s), 0, wk.kvh,
+                               key0 - lp * pg.page_size, page, stream_policy);
             } else {
-              tma_load_4d(sb + L.ring + s * TILE_BYTES, m, bar_full(s), 0, wk.kvh, key0, wk.b);
+              tma_load_4d_hint(sb + L.ring + s * TILE_BYTES, m, bar_full(s), 0, wk.kvh, key0, wk.b, stream_policy);
             }
           }
         }
@@ -290,6 +291,8 @@ attn_decode_splitkv_kernel(const __grid_constant__ CUtensorMap tm_k,
   // consumer keeps reaching the same named barriers, and the decision to stop
   // is taken at the end of the item from one shared copy of the abort flag.
   volatile int* stop = abort_flag + 1;
+  // chunk results: kept in L2 for the combine step, which reads them right after this kernel
+  const uint64_t keep_policy = l2_policy_evict_last();
   const int g16 = tid & 15;       // 16-byte column slice of a 256-byte row
   const int ksub = tid >> 4;      // key sub-group 0..7
   constexpr int V = 8 * G;        // partial sums per thread per tile
@@ -402,9 +405,11 @@ attn_decode_splitkv_kernel(const __grid_constant__ CUtensorMap tm_k,
         float o = 0.f;
 #pragma unroll
         for (int k = 0; k < 8; ++k) o += red[(k * G + h) * HD + d];
-        ws_o[(base + static_cast<size_t>(h) * S_max) * HD + d] = o / st_l[h];
+        st_global_hint(ws_o + (base + static_cast<size_t>(h) * S_max) * HD + d, o / st_l[h], keep_policy);
       }
-      if (tid < G) ws_lse[base + static_cast<size_t>(tid) * S_max] = (st_m[tid] + log2f(st_l[tid])) * 0.69314718055994531f;
+      if (tid < G)
+        st_global_hint(ws_lse + base + static_cast<size_t>(tid) * S_max,
+                       (st_m[tid] + log2f(st_l[tid])) * 0.69314718055994531f, keep_policy);
       if (tid == 0) *stop = *abort_flag;
     }
     asm volatile("bar.sync 1, %0;" ::"n"(NC) : "memory");  // red free for the next item
@@ -633,6 +638,9 @@ attn_decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_co
     if (lane == 0) {
       int it = 0;
       int cached_lp = -1, cached_b = -1, cached_page = 0;
+      // the cache is read once; 128-byte rows keep the default policy (neighbouring KV heads'
+      // rows share DRAM bursts that L2 serves to the CTAs reading them)
+      const uint64_t stream_policy = GE::ROW >= 256 ? l2_policy_evict_first() : l2_policy_evict_normal();
       bool ok = true;
       for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
         const decode::Work wk = decode::decode_work(w, split, B, Hkv, chunk, seqlens);
@@ -664,8 +672,8 @@ attn_decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_co
             }
 #pragma unroll
             for (int sl = 0; sl < GE::SLABS; ++sl)
-              tma_load_4d(sb + s * TILE_BYTES + sl * GE::SLAB_BYTES, m, bar_full(s), sl * (GE::SROW / GE::ESZ),
-                          wk.kvh, row, outer);
+              tma_load_4d_hint(sb + s * TILE_BYTES + sl * GE::SLAB_BYTES, m, bar_full(s),
+                               sl * (GE::SROW / GE::ESZ), wk.kvh, row, outer, stream_policy);
           }
         }
       }
@@ -685,6 +693,8 @@ attn_decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_co
   // consumer reaches the same named barriers and the stop decision is taken at
   // the end of the item from one shared copy of the abort flag.
   volatile int* stop = abort_flag + 1;
+  // chunk results: kept in L2 for the combine step, which reads them right after this kernel
+  const uint64_t keep_policy = l2_policy_evict_last();
   const int g = lane >> 2;        // MMA row group
   const int c = lane & 3;         // thread in group
   const int kblk = warp & 3;      // Q K^T: key block of the tile
@@ -928,14 +938,16 @@ attn_decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_co
           float* dst = ws_o + (base + static_cast<size_t>(h) * S_max) * HD + dbase;
           if constexpr (DV == 4) {
             // elements dbase + {0, 1, 2, 3} = (mt 0 row g, mt 0 row g+8, mt 1 row g, mt 1 row g+8)
-            *reinterpret_cast<float4*>(dst) = make_float4(oacc[0][nt][e] * sc, oacc[0][nt][2 + e] * sc,
-                                                          oacc[MT - 1][nt][e] * sc, oacc[MT - 1][nt][2 + e] * sc);
+            st_global_hint(dst, oacc[0][nt][e] * sc, oacc[0][nt][2 + e] * sc, oacc[MT - 1][nt][e] * sc,
+                           oacc[MT - 1][nt][2 + e] * sc, keep_policy);
           } else {
-            *reinterpret_cast<float2*>(dst) = make_float2(oacc[0][nt][e] * sc, oacc[0][nt][2 + e] * sc);
+            st_global_hint(dst, oacc[0][nt][e] * sc, oacc[0][nt][2 + e] * sc, keep_policy);
           }
         }
       }
-      if (tid < G) ws_lse[base + static_cast<size_t>(tid) * S_max] = (st_m[tid] + log2f(st_l[tid])) * 0.69314718055994531f;
+      if (tid < G)
+        st_global_hint(ws_lse + base + static_cast<size_t>(tid) * S_max,
+                       (st_m[tid] + log2f(st_l[tid])) * 0.69314718055994531f, keep_policy);
       if (tid == 0) *stop = *abort_flag;
     }
     asm volatile("bar.sync 1, %0;" ::"n"(NC) : "memory");  // scores and stats free for the next item
@@ -945,8 +957,13 @@ attn_decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_co
 
 }  // namespace decode_mma
 
-// One warp per (b, h): LSE-weighted merge of the chunk results; lane l holds
-// head-dimension elements [l HD/32, (l+1) HD/32).
+// One CTA per (b, h): LSE-weighted merge of the chunk results.  The four warps
+// take chunks w, w + 4, w + 8, ... and issue up to 16 chunk loads (lane l:
+// head-dimension elements [l HD/32, (l+1) HD/32)) before any arithmetic, so a
+// sequence of up to 64 chunks is read in one round of memory latency; each warp
+// keeps a running (max, sum, weighted O) over its chunks, and warp 0 merges the
+// four through shared memory.  (One warp walking all chunks of its (b, h) made
+// the longest sequences' warps wait for one round per 8-16 chunks.)
 template <int HDIM>
 __global__ void __launch_bounds__(128)
 attn_decode_combine_kernel(const float* __restrict__ ws_o, const float* __restrict__ ws_lse,
@@ -954,73 +971,100 @@ attn_decode_combine_kernel(const float* __restrict__ ws_o, const float* __restri
                            float* __restrict__ lse, int B, int Hq, int Nk_max, int chunk, int S_max,
                            int* err) {
   constexpr int E = HDIM / 32;   // elements per lane: 4 or 2
+  constexpr int NW = 4;          // warps
+  constexpr int DEPTH = 16;      // chunks per warp per round
+  constexpr float LOG2E = 1.4426950408889634f;
+  __shared__ float s_m[NW], s_s[NW];
+  __shared__ __align__(16) float s_acc[NW][HDIM];
+  const int warp = static_cast<int>(threadIdx.x >> 5);
   const int lane = static_cast<int>(lane_id());
-  const int bh = static_cast<int>(blockIdx.x) * 4 + static_cast<int>(threadIdx.x >> 5);
-  if (bh >= B * Hq) return;
+  const int bh = static_cast<int>(blockIdx.x);
   const int b = bh / Hq;
   const int Lb = __ldg(seqlens + b);
   __nv_bfloat16* orow = o + static_cast<size_t>(bh) * HDIM + lane * E;
-  if (Lb < 1 || Lb > Nk_max) {
-    if (lane == 0) atomicCAS(err, 0, ATTN_ERR_SEQLEN);
-    if constexpr (E == 4) *reinterpret_cast<uint2*>(orow) = make_uint2(0u, 0u);
-    else *reinterpret_cast<uint32_t*>(orow) = 0u;
-    if (lane == 0 && lse != nullptr) lse[bh] = -CUDART_INF_F;
+  if (Lb < 1 || Lb > Nk_max) {   // the whole CTA leaves together
+    if (warp == 0) {
+      if (lane == 0) atomicCAS(err, 0, ATTN_ERR_SEQLEN);
+      if constexpr (E == 4) *reinterpret_cast<uint2*>(orow) = make_uint2(0u, 0u);
+      else *reinterpret_cast<uint32_t*>(orow) = 0u;
+      if (lane == 0 && lse != nullptr) lse[bh] = -CUDART_INF_F;
+    }
     return;
   }
   const int n = (Lb + chunk - 1) / chunk;
   const float* lp = ws_lse + static_cast<size_t>(bh) * S_max;
   const float* op = ws_o + static_cast<size_t>(bh) * S_max * HDIM + lane * E;
-  float M = -CUDART_INF_F;
-  for (int c = lane; c < n; c += 32) M = fmaxf(M, lp[c]);
-#pragma unroll
-  for (int k = 16; k >= 1; k >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, k));
-  constexpr float LOG2E = 1.4426950408889634f;
-  float s = 0.f;
+  float m = -CUDART_INF_F, s = 0.f;
   float acc[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
-  for (int c0 = 0; c0 < n; c0 += 32) {
-    const float wc = (c0 + lane < n) ? ex2_approx((lp[c0 + lane] - M) * LOG2E) : 0.f;
-    s += wc;
-    const int cnt = min(32, n - c0);
-    // eight chunks at a time, all eight loads in flight before the sums (chunks past the
-    // count load zeros and add nothing: their weights are finite)
-    for (int j0 = 0; j0 < cnt; j0 += 8) {
-      float x[8][E];
-      float w[8];
+  for (int c0 = warp; c0 < n; c0 += NW * DEPTH) {   // c0 < n: lv[0] is finite
+    float lv[DEPTH];
+    float x[DEPTH][E];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int j = j0 + u;
-        w[u] = __shfl_sync(0xffffffffu, wc, j & 31);
-        if constexpr (E == 4) {
-          const float4 v = j < cnt ? *reinterpret_cast<const float4*>(op + static_cast<size_t>(c0 + j) * HDIM)
-                                   : make_float4(0.f, 0.f, 0.f, 0.f);
-          x[u][0] = v.x;
-          x[u][1] = v.y;
-          x[u][2] = v.z;
-          x[u][3] = v.w;
-        } else {
-          const float2 v = j < cnt ? *reinterpret_cast<const float2*>(op + static_cast<size_t>(c0 + j) * HDIM)
-                                   : make_float2(0.f, 0.f);
-          x[u][0] = v.x;
-          x[u][1] = v.y;
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-#pragma unroll
-        for (int e = 0; e < E; ++e) acc[e] = fmaf(w[u], x[u][e], acc[e]);
+    for (int u = 0; u < DEPTH; ++u) {
+      // chunks past n re-read chunk n - 1 (no branch, so every load can issue at once)
+      // and get LSE -inf, i.e. weight 0
+      // (volatile asm loads keep the compiler from spreading them over several rounds)
+      const int c = c0 + NW * u;
+      const int cc = min(c, n - 1);
+      float l;
+      asm volatile("ld.global.f32 %0, [%1];" : "=f"(l) : "l"(lp + cc));
+      lv[u] = c < n ? l : -CUDART_INF_F;
+      const float* src = op + static_cast<size_t>(cc) * HDIM;
+      if constexpr (E == 4)
+        asm volatile("ld.global.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(x[u][0]), "=f"(x[u][1]), "=f"(x[u][2]), "=f"(x[u][3]) : "l"(src));
+      else
+        asm volatile("ld.global.v2.f32 {%0, %1}, [%2];" : "=f"(x[u][0]), "=f"(x[u][1]) : "l"(src));
     }
+    float mr = lv[0];
+#pragma unroll
+    for (int u = 1; u < DEPTH; ++u) mr = fmaxf(mr, lv[u]);
+    const float mn = fmaxf(m, mr);
+    const float corr = ex2_approx((m - mn) * LOG2E);   // 0 on the first round (m = -inf)
+    s *= corr;
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] *= corr;
+#pragma unroll
+    for (int u = 0; u < DEPTH; ++u) {
+      const float w = ex2_approx((lv[u] - mn) * LOG2E);
+      s += w;
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[e] = fmaf(w, x[u][e], acc[e]);
+    }
+    m = mn;
+  }
+  // warps without chunks (n < 4) keep m = -inf, s = 0, acc = 0
+  if (lane == 0) {
+    s_m[warp] = m;
+    s_s[warp] = s;
   }
 #pragma unroll
-  for (int k = 16; k >= 1; k >>= 1) s += __shfl_xor_sync(0xffffffffu, s, k);
-  const float inv = 1.f / s;
+  for (int e = 0; e < E; ++e) s_acc[warp][lane * E + e] = acc[e];
+  __syncthreads();
+  if (warp != 0) return;
+  float M = s_m[0];
+#pragma unroll
+  for (int w = 1; w < NW; ++w) M = fmaxf(M, s_m[w]);
+  float S = 0.f;
+  float out[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) out[e] = 0.f;
+#pragma unroll
+  for (int w = 0; w < NW; ++w) {
+    const float f = s_m[w] == -CUDART_INF_F ? 0.f : ex2_approx((s_m[w] - M) * LOG2E);
+    S = fmaf(f, s_s[w], S);
+#pragma unroll
+    for (int e = 0; e < E; ++e) out[e] = fmaf(f, s_acc[w][lane * E + e], out[e]);
+  }
+  const float inv = 1.f / S;
   if constexpr (E == 4)
     *reinterpret_cast<uint2*>(orow) =
-        make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv), pack_bf16x2(acc[2] * inv, acc[3] * inv));
+        make_uint2(pack_bf16x2(out[0] * inv, out[1] * inv), pack_bf16x2(out[2] * inv, out[3] * inv));
   else
-    *reinterpret_cast<uint32_t*>(orow) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-  if (lane == 0 && lse != nullptr) lse[bh] = M + logf(s);
+    *reinterpret_cast<uint32_t*>(orow) = pack_bf16x2(out[0] * inv, out[1] * inv);
+  if (lane == 0 && lse != nullptr) lse[bh] = M + logf(S);
 }
 
 template <int G, bool PAGED>
@@ -1191,7 +1235,7 @@ int launch_decode_combine(const void* workspace, const int* seqlens, void* o, fl
   const int S_max = (Nk_max + chunk - 1) / chunk;
   const float* ws_o = static_cast<const float*>(workspace);
   const float* ws_lse = ws_o + static_cast<size_t>(B) * Hq * S_max * D;
-  const int grid = (B * Hq + 3) / 4;
+  const int grid = B * Hq;
   if (D == 128)
     attn_decode_combine_kernel<128><<<grid, 128, 0, stream>>>(ws_o, ws_lse, seqlens, static_cast<__nv_bfloat16*>(o),
                                                               lse, B, Hq, Nk_max, chunk, S_max, err);
