@@ -729,7 +729,10 @@ BWD_CASES = [
     (1, 4, 2, 257, 257, False, 100),    # window without causal
     (1, 2, 1, 130, 700, True, 50),      # chunked prefill + window: key tiles no query sees (dK = dV = 0)
     (1, 2, 2, 512, 512, True, 128),     # window of exactly one tile, whole tiles
+    (1, 4, 2, 300, 300, False, 0),      # key-tile pairs, odd tile count (a CTA past the last key)
+    (2, 4, 2, 257, 520, False, 0),      # key-tile pairs, GQA, ragged query and key tiles
     # head dimension 64
+    (1, 2, 1, 130, 300, False, 0, 64),  # key-tile pairs, odd tile count
     (1, 2, 2, 200, 200, False, 0, 64),
     (2, 4, 2, 257, 257, True, 0, 64),
     (1, 4, 1, 130, 300, True, 0, 64),
