@@ -35,6 +35,8 @@
 #include <cuda_runtime.h>
 #include <math_constants.h>
 
+#include <type_traits>
+
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -832,9 +834,14 @@ attn_decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_co
       for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
       const float m = (mx == -CUDART_INF_F) ? 0.f : mx * c_log2;
       float sum = 0.f;
+      // p in the P V operand type (f16 for fp8 caches, else bf16), written in place over the
+      // scores: p_j lands in the bytes of score j / 2, which the warp has already read (in an
+      // earlier pass, or, for j < 32, by the load of this pass)
+      const uint32_t sh16 = smem_u32(sh);
       for (int j = lane; j < nk_pad; j += 32) {
         const float pv = ex2_approx(fmaf(sh[j], c_log2, -m));
-        sh[j] = pv;
+        st_shared_u16(sh16 + 2 * j, KV8 ? __half_as_ushort(__float2half_rn(pv))
+                                        : __bfloat16_as_ushort(__float2bfloat16_rn(pv)));
         sum += pv;
       }
 #pragma unroll
@@ -859,6 +866,10 @@ attn_decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_co
       if (!ok) continue;
       const uint8_t* tile = smem + s * TILE_BYTES;
       const int valid_here = wk.n_valid - tl * TILE;   // keys of this tile inside the sequence
+      // a full tile takes the copy of the loop without the per-key check (only a chunk's
+      // last tile can reach past the sequence)
+      auto tile_pv = [&](auto mask_tag) {
+      constexpr bool MASK = decltype(mask_tag)::value;
 #pragma unroll
       for (int ks = 0; ks < TILE / 16; ++ks) {
         // the MMA K index 2c + {0, 1, 8, 9} is key 16 ks + 2c + {0, 1, 8, 9}
@@ -867,7 +878,7 @@ attn_decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_co
         for (int i = 0; i < 4; ++i) {
           const int key = 16 * ks + 2 * c + (i & 1) + 8 * (i >> 1);
           const uint32_t off = tile_off<HD, KV8>(key, dbase * GE::ESZ);
-          const bool in = key < valid_here;
+          const bool in = !MASK || key < valid_here;
           if constexpr (DV * GE::ESZ == 8) {
             const uint2 u = *reinterpret_cast<const uint2*>(tile + off);
             vw[i][0] = in ? u.x : 0u;
@@ -905,23 +916,19 @@ attn_decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_co
         for (int nt = 0; nt < NTP; ++nt) {
           const int h = 8 * (pt0 + nt) + g;
           uint32_t b0 = 0u, b1 = 0u;
-          if (h < G) {
-            const float* ph = work + h * wstride + tl * TILE + 16 * ks + 2 * c;
-            const float2 p01 = *reinterpret_cast<const float2*>(ph);
-            const float2 p89 = *reinterpret_cast<const float2*>(ph + 8);
-            if constexpr (KV8) {
-              b0 = pack_f16x2(p01.x, p01.y);
-              b1 = pack_f16x2(p89.x, p89.y);
-            } else {
-              b0 = pack_bf16x2(p01.x, p01.y);
-              b1 = pack_bf16x2(p89.x, p89.y);
-            }
+          if (h < G) {   // p of keys (2c, 2c+1) and (2c+8, 2c+9), already in the operand type
+            const uint16_t* ph = reinterpret_cast<const uint16_t*>(work + h * wstride) + tl * TILE + 16 * ks + 2 * c;
+            b0 = *reinterpret_cast<const uint32_t*>(ph);
+            b1 = *reinterpret_cast<const uint32_t*>(ph + 8);
           }
 #pragma unroll
           for (int mt = 0; mt < MT; ++mt)
             mma16816<KV8>(oacc[mt][nt], af[mt][0], af[mt][1], af[mt][2], af[mt][3], b0, b1);
         }
       }
+      };
+      if (valid_here >= TILE) tile_pv(std::false_type{});
+      else tile_pv(std::true_type{});
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_empty(s));
     }

@@ -409,6 +409,11 @@ __device__ __forceinline__ void st_global_v8(void* ptr, const uint32_t* w) {
                : "memory");
 }
 
+// 16-bit shared-memory store (volatile: never moved across other memory accesses).
+__device__ __forceinline__ void st_shared_u16(uint32_t addr, unsigned short v) {
+  asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
+
 // ------------------------------------------------------------------ math
 // 2^x on the special-function unit (hardware ex2, approximate, flush-to-zero).
 __device__ __forceinline__ float ex2_approx(float x) {
