@@ -447,7 +447,10 @@ attn_decode_splitkv_kernel(const __grid_constant__ CUtensorMap tm_k,
 namespace decode_mma {
 
 constexpr int TILE = 64;                 // keys per TMA tile
-constexpr int SPAD = 8;                  // floats of padding per score row (row stride chunk + SPAD)
+// floats of padding per score row (row stride chunk + SPAD, chunk a multiple of 64): a
+// stride of 4 mod 32 words puts the score stores of Q K^T (heads 2c + e, keys g) and the
+// 32-bit p loads of P V (heads g, key pairs c) on 32 different banks
+constexpr int SPAD = 4;
 constexpr int MAX_STAGES = 16;
 
 template <int HD, bool KV8>
