@@ -536,27 +536,25 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
           const RingPos kn = ring_next<STAGES>(vj);  // K of key tile j + 1
           const bool own = j >= jb && j < je;
           const int lt = n_own + (j - jb);
-          bool p_all = false;
           if (own) {
-            // inputs of this step, before taking the turn
-            if (!wait_full(vj) || !mbar_wait(bar_p_lo(t), lt & 1, abort_flag, p.err)) { ok = false; break; }
+            // inputs of this step, before taking the turn: the ring slots (filled
+            // long before in the steady state) first, P_t's first half last, so that
+            // the turn follows the softmax's hand-over with as little delay as possible
+            if (!wait_full(vj) || (j + 1 < je && !wait_full(kn))) { ok = false; break; }
             // PV overwrites O_t at the unit's first key tile: the epilogue of the
             // previous unit must have read it out.
             if (j == jb && n_out > 0 && !mbar_wait(bar_o_empty(t), (n_out - 1) & 1, abort_flag, p.err)) {
               ok = false;
               break;
             }
-            if (j + 1 < je && !wait_full(kn)) { ok = false; break; }
-            p_all = mbar_test_wait(bar_p_hi(t), lt & 1);
+            if (!mbar_wait(bar_p_lo(t), lt & 1, abort_flag, p.err)) { ok = false; break; }
           }
           if (!wait_turn(seq)) { ok = false; break; }
           if (own) {
             tc_fence_after();
             issue_pv_half<HD, F16>(elect, tmem + o_col<HD>(t), tmem + s_col(t), v_desc(vj), j > jb, 0);
-            if (!p_all) {
-              if (!mbar_wait(bar_p_hi(t), lt & 1, abort_flag, p.err)) { ok = false; break; }
-              tc_fence_after();
-            }
+            if (!mbar_wait(bar_p_hi(t), lt & 1, abort_flag, p.err)) { ok = false; break; }
+            tc_fence_after();
             issue_pv_half<HD, F16>(elect, tmem + o_col<HD>(t), tmem + s_col(t), v_desc(vj), true, BN / 32);
             if (j + 1 < je) issue_qk<HD, F16, QK8>(elect, tmem + s_col(t), q_desc, k_desc(kn));
           }
