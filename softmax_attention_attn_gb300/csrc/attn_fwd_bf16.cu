@@ -469,8 +469,8 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     // 128 x 128 x 16 MMA about every 64 cycles and holds the issuing thread for
     // most of that, so the two issuers take strict turns, step by step
     // (t = 0, 1, 0, 1, ...), and do everything but the MMAs outside their turn:
-    // waits for P, for filled ring slots and for the epilogue before it, commits
-    // and slot releases after it.  One issuer's bookkeeping then overlaps the
+    // waits for ring slots, the epilogue and P's first half before it (its second
+    // half inside), commits and slot releases after.  One issuer's bookkeeping then overlaps the
     // other's MMAs, and the tensor pipe sees the MMAs of one step together, so
     // S_t(j+1) is not held back behind the other tile's MMAs.  The turn order
     // only sets priority (the two Q tiles share no tensor memory and each issuer
