@@ -409,6 +409,8 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
+      const uint64_t once_policy = l2_policy_evict_first();   // Q: read once
+      const uint64_t keep_policy = l2_policy_evict_last();    // K/V: read by every q-block of a head
       int it = 0;   // ring position (runs on across units)
       int nql = 0;  // Q tiles loaded so far (tile t of the n-th unit with work is load 2n + t)
       bool ok = true;
@@ -419,11 +421,11 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
         mbar_arrive_expect_tx(bar_q_full(qb), QK_TILE_BYTES);
         for (int kb = 0; kb < QK_SLABS; ++kb)
           if (p.varlen)
-            tma_load_3d(sb + SMEM_Q + qb * QK_TILE_BYTES + kb * KBLK_BYTES, &tm_q, bar_q_full(qb),
-                        kb * QK_BOX, u.h, u.q_tok + u.q0 + t * BM);
+            tma_load_3d_hint(sb + SMEM_Q + qb * QK_TILE_BYTES + kb * KBLK_BYTES, &tm_q, bar_q_full(qb),
+                             kb * QK_BOX, u.h, u.q_tok + u.q0 + t * BM, once_policy);
           else
-            tma_load_3d(sb + SMEM_Q + qb * QK_TILE_BYTES + kb * KBLK_BYTES, &tm_q, bar_q_full(qb),
-                        kb * QK_BOX, u.q0 + t * BM, u.b * p.Hq + u.h);
+            tma_load_3d_hint(sb + SMEM_Q + qb * QK_TILE_BYTES + kb * KBLK_BYTES, &tm_q, bar_q_full(qb),
+                             kb * QK_BOX, u.q0 + t * BM, u.b * p.Hq + u.h, once_policy);
         ++nql;
         return true;
       };
@@ -448,11 +450,11 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
             const CUtensorMap* m = kv ? &tm_v : &tm_k;
             for (int kb = 0; kb < slabs; ++kb)
               if (p.varlen)
-                tma_load_3d(sb + SMEM_RING + s * TILE_BYTES + kb * KBLK_BYTES, m, bar_kv_full(s),
-                            kb * box_x, u.kvh, u.k_tok + j * BN);
+                tma_load_3d_hint(sb + SMEM_RING + s * TILE_BYTES + kb * KBLK_BYTES, m, bar_kv_full(s),
+                                 kb * box_x, u.kvh, u.k_tok + j * BN, keep_policy);
               else
-                tma_load_3d(sb + SMEM_RING + s * TILE_BYTES + kb * KBLK_BYTES, m, bar_kv_full(s),
-                            kb * box_x, j * BN, u.b * p.Hkv + u.kvh);
+                tma_load_3d_hint(sb + SMEM_RING + s * TILE_BYTES + kb * KBLK_BYTES, m, bar_kv_full(s),
+                                 kb * box_x, j * BN, u.b * p.Hkv + u.kvh, keep_policy);
           }
         }
         if (ok && u.j_end == u.j_begin + 1 && !load_q(u, 1)) { ok = false; break; }  // one-tile unit
@@ -596,6 +598,7 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
     const uint32_t s_addr = tmem + lane_sel + s_col(t);
     const uint32_t o_addr = tmem + lane_sel + o_col<HD>(t);
     const float c = p.scale_log2;
+    const uint64_t out_policy = l2_policy_evict_first();   // O is written once
     int n_own = 0;  // own key tiles so far (phase of s_full)
     int n_out = 0;  // units that produced O_t so far (phase of o_full)
     bool ok = true;
@@ -812,7 +815,7 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
           // 32-byte stores: each thread writes its own row, so a warp's store touches 32
           // rows; whole 32-byte sectors halve the write requests of 16-byte stores
 #pragma unroll
-          for (int i = 0; i < HD / 16; ++i) st_global_v8(orow + 16 * i, &w[8 * i]);
+          for (int i = 0; i < HD / 16; ++i) st_global_v8_hint(orow + 16 * i, &w[8 * i], out_policy);
         } else {
 #pragma unroll
           for (int i = 0; i < HD / 8; ++i)
