@@ -17,24 +17,28 @@
 //     buffers rotate over the units' Q tiles, so the next unit's Q lands while
 //     the current one runs.  Barriers and tensor memory are set up once; the
 //     next unit's Q, K/V and first S overlap the last unit's epilogue;
-//   * warps 0 and 1 issue the tcgen05.mma of Q tile 0 and 1 (lane 0 of a
-//     converged warp): S_t = Q_t K^T into tensor memory (fp32, 128 columns per
-//     Q tile), then O_t += P_t V with P read from tensor memory (the TS form)
-//     and V from shared memory (MN-major operand); the two take strict turns,
-//     one key tile at a time, and wait and commit outside their turn;
-//   * warps 3-6 and 7-10 are the softmax warps of Q tile 0 and 1: warp w
+//   * 512 threads in four warpgroups, each given its register share by setmaxnreg
+//     (the softmax warpgroups take more than the 128 a thread is launched with);
+//   * warps 0-3 and 4-7 are the softmax warps of Q tile 0 and 1: warp w
 //     reaches tensor-memory lanes 32 (w % 4) .. + 31, so thread r of warp w
 //     owns row 32 (w % 4) + r; it loads its 128 scores, applies the mask,
 //     updates the running max / sum in the exp2 domain, rescales its O row in
 //     tensor memory when the max grew by more than 2^8 (otherwise the stale max
 //     is kept; the final normalisation is exact either way), writes P as bf16
-//     over its S columns and signals its MMA issuer;
-//   * warp 2 (one elected thread) is the TMA producer;
-//   * the MMA issuers have the lowest warp numbers (measured about 1 % faster
-//     than the highest, where they share sub-partitions with the same softmax
-//     warps either way);
-//   * the epilogue (same softmax threads) divides by the row sum, rounds O to
-//     bf16 and writes O (32-byte stores when O is 32-byte aligned) and LSE;
+//     over its S columns and signals its MMA issuer; at the end of a unit it
+//     writes LSE and hands 1 / l to the epilogue warps through shared memory;
+//   * warps 8-11 are the epilogue: once a unit's last P V has completed they
+//     read O out of tensor memory, hand it back to the MMA issuer, divide by
+//     the row sum, round to bf16 and write O (32-byte stores when O is 32-byte
+//     aligned), while the softmax warps already run the next unit;
+//   * warps 12 and 13 issue the tcgen05.mma of Q tile 0 and 1 (lane 0 of a
+//     converged warp): S_t = Q_t K^T into tensor memory (fp32, 128 columns per
+//     Q tile), then O_t += P_t V with P read from tensor memory (the TS form)
+//     and V from shared memory (MN-major operand); the two take strict turns,
+//     one key tile at a time, and wait and commit outside their turn;
+//   * warp 14 (one elected thread) is the TMA producer, with L2 policies: Q
+//     evict-first (read once), K/V evict-last (read by every q-block of a head);
+//     warp 15 only completes the last warpgroup;
 //   * with QK8, Q and K are E4M3 codes and S = Q K^T runs on kind::f8f6f4
 //     (the fp8 prefill; V arrives widened to bf16).
 //
@@ -46,6 +50,7 @@
 #include <cuda_runtime.h>
 #include <math_constants.h>
 
+#include <atomic>
 #include <cmath>
 
 #include "kernels.h"
@@ -59,10 +64,24 @@ constexpr int BN = 128;                      // keys per K/V tile
 constexpr int NQT = 2;                       // Q tiles per work unit
 constexpr int KBLK_BYTES = 128 * 64 * 2;     // 64-column (128-byte) slab of a 128-row tile
 constexpr int NUM_SOFTMAX_WARPS = 4 * NQT;
-constexpr int WARP_MMA = 0;                          // issuer of Q tile t is warp WARP_MMA + t
-constexpr int WARP_TMA = NQT;                        // TMA producer
-constexpr int WARP_SOFTMAX0 = NQT + 1;               // softmax warps of Q tile t: WARP_SOFTMAX0 + 4t ..
-constexpr int NTHREADS = (NUM_SOFTMAX_WARPS + 1 + NQT) * 32;
+constexpr int WARP_SOFTMAX0 = 0;                     // softmax warps of Q tile t: WARP_SOFTMAX0 + 4t ..
+constexpr int WARP_EPI = NUM_SOFTMAX_WARPS;          // epilogue warps: WARP_EPI + q reads TMEM lanes 32q ..
+constexpr int WARP_MMA = WARP_EPI + 4;               // issuer of Q tile t is warp WARP_MMA + t
+constexpr int WARP_TMA = WARP_MMA + NQT;             // TMA producer (the warp after it idles)
+constexpr int NTHREADS = (WARP_TMA + 2) * 32;        // four warpgroups
+// Registers per thread after each warpgroup's setmaxnreg: the block is launched with
+// 65536 / NTHREADS = 128 each; the two softmax warpgroups take more, the epilogue and
+// control (issuers, TMA) warpgroups give theirs up, and the shares add up to the block's
+// (an `inc` beyond the pool would wait forever).  The epilogue holds a packed output
+// row (HD / 2 words) and one 32-column piece of O.
+template <int HD, bool CAP>
+struct Regs {
+  static constexpr int SOFTMAX = (HD == 64 || CAP) ? 176 : 168;
+  static constexpr int CTRL = CAP ? 56 : 72;
+  static constexpr int EPI = (65536 - 2 * 128 * SOFTMAX - 128 * CTRL) / 128;
+  static_assert(2 * 128 * SOFTMAX + 128 * EPI + 128 * CTRL == 65536 && EPI % 8 == 0, "register shares");
+};
+static_assert(NTHREADS == 512 && NUM_SOFTMAX_WARPS == 8, "four warpgroups: softmax x2, epilogue, control");
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float RESCALE_LOG2 = 8.0f;         // keep a stale max while the growth is <= 2^8
 
@@ -85,9 +104,10 @@ struct Cfg {
   static constexpr int SMEM_Q = 0;
   static constexpr int SMEM_RING = SMEM_Q + NQB * QK_TILE_BYTES;
   static constexpr int SMEM_BAR = SMEM_RING + STAGES * TILE_BYTES;
-  static constexpr int NUM_BARS = 2 * NQB + 1 + 2 * STAGES + 5 * NQT;
+  static constexpr int NUM_BARS = 2 * NQB + 1 + 2 * STAGES + 7 * NQT;
   static constexpr int SMEM_MISC = SMEM_BAR + NUM_BARS * 8;
-  static constexpr int SMEM_ALLOC = SMEM_MISC + 16 + 1024;  // + slack for 1024-byte alignment
+  static constexpr int SMEM_STATS = SMEM_MISC + 16;     // per Q tile row: 1 / l for the epilogue warps
+  static constexpr int SMEM_ALLOC = SMEM_STATS + NQT * BM * 4 + 1024;  // + slack for 1024-byte alignment
   static constexpr uint32_t AB_FORMAT = F16 ? 0u : 1u;  // instruction-descriptor A/B format
   static constexpr uint32_t IDESC_QK = QK8 ? idesc_e4m3_f32(128, BN) : idesc_f16kind_f32(128, BN, 0, AB_FORMAT);
   static constexpr uint32_t IDESC_PV = idesc_f16kind_f32(128, HD, 1, AB_FORMAT);
@@ -365,6 +385,8 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
   auto bar_p_hi = [&](int t) { return bar_t(2, t); };     // P_t keys 64-127 in TMEM
   auto bar_o_full = [&](int t) { return bar_t(3, t); };   // O_t of a unit complete
   auto bar_o_empty = [&](int t) { return bar_t(4, t); };  // epilogue has read O_t
+  auto bar_stats_full = [&](int t) { return bar_t(5, t); };   // a unit's 1 / l of Q tile t in smem
+  auto bar_stats_empty = [&](int t) { return bar_t(6, t); };  // the epilogue warps have read them
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + SMEM_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SMEM_MISC + 4);
   volatile uint32_t* turn = reinterpret_cast<volatile uint32_t*>(smem + SMEM_MISC + 8);
@@ -387,7 +409,9 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
       mbar_init(bar_p_lo(t), BM / 32);   // one arrival per softmax warp
       mbar_init(bar_p_hi(t), BM / 32);
       mbar_init(bar_o_full(t), 1);
-      mbar_init(bar_o_empty(t), BM / 32);
+      mbar_init(bar_o_empty(t), BM / 32);      // one arrival per epilogue warp
+      mbar_init(bar_stats_full(t), BM / 32);   // one arrival per softmax warp
+      mbar_init(bar_stats_empty(t), BM / 32);  // one arrival per epilogue warp
     }
     *abort_flag = 0;
     *turn = 0;
@@ -403,204 +427,277 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
 
-  if (warp == WARP_TMA) {
-    // ================================================================ producer
-    if (lane == 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
-      const uint64_t once_policy = l2_policy_evict_first();   // Q: read once
-      const uint64_t keep_policy = l2_policy_evict_last();    // K/V: read by every q-block of a head
-      int it = 0;   // ring position (runs on across units)
-      int nql = 0;  // Q tiles loaded so far (tile t of the n-th unit with work is load 2n + t)
-      bool ok = true;
-      // Q tile t of the current unit into buffer nql % NQB, once the tile it held is done
-      auto load_q = [&](const Unit& u, int t) -> bool {
-        const int qb = nql % NQB, use = nql / NQB;
-        if (use > 0 && !mbar_wait(bar_q_empty(qb), (use - 1) & 1, abort_flag, p.err)) return false;
-        mbar_arrive_expect_tx(bar_q_full(qb), QK_TILE_BYTES);
-        for (int kb = 0; kb < QK_SLABS; ++kb)
-          if (p.varlen)
-            tma_load_3d_hint(sb + SMEM_Q + qb * QK_TILE_BYTES + kb * KBLK_BYTES, &tm_q, bar_q_full(qb),
-                             kb * QK_BOX, u.h, u.q_tok + u.q0 + t * BM, once_policy);
-          else
-            tma_load_3d_hint(sb + SMEM_Q + qb * QK_TILE_BYTES + kb * KBLK_BYTES, &tm_q, bar_q_full(qb),
-                             kb * QK_BOX, u.q0 + t * BM, u.b * p.Hq + u.h, once_policy);
-        ++nql;
-        return true;
-      };
-      for (int pass = 0, w = unit_of_pass(0); w < n_units && ok; w = unit_of_pass(++pass)) {
-        const Unit u = make_unit(w, p, n_qblk);
-        if (u.j_end <= u.j_begin) continue;
-        // Q tile 0 (its buffer freed a unit ago), the first K/V pair, then Q tile 1 (its
-        // buffer is the previous unit's tile 0), so that tile 0 can start while tile 1 waits
-        if (!load_q(u, 0)) { ok = false; break; }
-        for (int j = u.j_begin; j < u.j_end && ok; ++j) {
-          if (j == u.j_begin + 1 && !load_q(u, 1)) { ok = false; break; }
-          for (int kv = 0; kv < 2; ++kv, ++it) {
-            const int s = it % STAGES, use = it / STAGES;
-            if (use > 0 && !mbar_wait(bar_kv_empty(s), (use - 1) & 1, abort_flag, p.err)) {
-              ok = false;
-              break;
+  if (warp >= WARP_MMA) {
+    setmaxnreg_dec<Regs<HD, CAP>::CTRL>();
+    if (warp == WARP_TMA) {
+      // ================================================================ producer
+      if (lane == 0) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+        const uint64_t once_policy = l2_policy_evict_first();   // Q: read once
+        const uint64_t keep_policy = l2_policy_evict_last();    // K/V: read by every q-block of a head
+        int it = 0;   // ring position (runs on across units)
+        int nql = 0;  // Q tiles loaded so far (tile t of the n-th unit with work is load 2n + t)
+        bool ok = true;
+        // Q tile t of the current unit into buffer nql % NQB, once the tile it held is done
+        auto load_q = [&](const Unit& u, int t) -> bool {
+          const int qb = nql % NQB, use = nql / NQB;
+          if (use > 0 && !mbar_wait(bar_q_empty(qb), (use - 1) & 1, abort_flag, p.err)) return false;
+          mbar_arrive_expect_tx(bar_q_full(qb), QK_TILE_BYTES);
+          for (int kb = 0; kb < QK_SLABS; ++kb)
+            if (p.varlen)
+              tma_load_3d_hint(sb + SMEM_Q + qb * QK_TILE_BYTES + kb * KBLK_BYTES, &tm_q, bar_q_full(qb),
+                               kb * QK_BOX, u.h, u.q_tok + u.q0 + t * BM, once_policy);
+            else
+              tma_load_3d_hint(sb + SMEM_Q + qb * QK_TILE_BYTES + kb * KBLK_BYTES, &tm_q, bar_q_full(qb),
+                               kb * QK_BOX, u.q0 + t * BM, u.b * p.Hq + u.h, once_policy);
+          ++nql;
+          return true;
+        };
+        for (int pass = 0, w = unit_of_pass(0); w < n_units && ok; w = unit_of_pass(++pass)) {
+          const Unit u = make_unit(w, p, n_qblk);
+          if (u.j_end <= u.j_begin) continue;
+          // Q tile 0 (its buffer freed a unit ago), the first K/V pair, then Q tile 1 (its
+          // buffer is the previous unit's tile 0), so that tile 0 can start while tile 1 waits
+          if (!load_q(u, 0)) { ok = false; break; }
+          for (int j = u.j_begin; j < u.j_end && ok; ++j) {
+            if (j == u.j_begin + 1 && !load_q(u, 1)) { ok = false; break; }
+            for (int kv = 0; kv < 2; ++kv, ++it) {
+              const int s = it % STAGES, use = it / STAGES;
+              if (use > 0 && !mbar_wait(bar_kv_empty(s), (use - 1) & 1, abort_flag, p.err)) {
+                ok = false;
+                break;
+              }
+              // K: QK_SLABS slabs of QK_BOX elements (E4M3 K fills half a slot); V: KBLKS bf16 slabs
+              const int slabs = kv ? KBLKS : QK_SLABS;
+              const int box_x = kv ? 64 : QK_BOX;
+              mbar_arrive_expect_tx(bar_kv_full(s), kv ? TILE_BYTES : QK_TILE_BYTES);
+              const CUtensorMap* m = kv ? &tm_v : &tm_k;
+              for (int kb = 0; kb < slabs; ++kb)
+                if (p.varlen)
+                  tma_load_3d_hint(sb + SMEM_RING + s * TILE_BYTES + kb * KBLK_BYTES, m, bar_kv_full(s),
+                                   kb * box_x, u.kvh, u.k_tok + j * BN, keep_policy);
+                else
+                  tma_load_3d_hint(sb + SMEM_RING + s * TILE_BYTES + kb * KBLK_BYTES, m, bar_kv_full(s),
+                                   kb * box_x, j * BN, u.b * p.Hkv + u.kvh, keep_policy);
             }
-            // K: QK_SLABS slabs of QK_BOX elements (E4M3 K fills half a slot); V: KBLKS bf16 slabs
-            const int slabs = kv ? KBLKS : QK_SLABS;
-            const int box_x = kv ? 64 : QK_BOX;
-            mbar_arrive_expect_tx(bar_kv_full(s), kv ? TILE_BYTES : QK_TILE_BYTES);
-            const CUtensorMap* m = kv ? &tm_v : &tm_k;
-            for (int kb = 0; kb < slabs; ++kb)
-              if (p.varlen)
-                tma_load_3d_hint(sb + SMEM_RING + s * TILE_BYTES + kb * KBLK_BYTES, m, bar_kv_full(s),
-                                 kb * box_x, u.kvh, u.k_tok + j * BN, keep_policy);
-              else
-                tma_load_3d_hint(sb + SMEM_RING + s * TILE_BYTES + kb * KBLK_BYTES, m, bar_kv_full(s),
-                                 kb * box_x, j * BN, u.b * p.Hkv + u.kvh, keep_policy);
           }
+          if (ok && u.j_end == u.j_begin + 1 && !load_q(u, 1)) { ok = false; break; }  // one-tile unit
         }
-        if (ok && u.j_end == u.j_begin + 1 && !load_q(u, 1)) { ok = false; break; }  // one-tile unit
+        if (!ok) {  // give up: let the copies already issued land before the CTA exits
+          for (int i = max(0, nql - NQB); i < nql; ++i) drain_wait(bar_q_full(i % NQB), (i / NQB) & 1);
+          for (int i = max(0, it - STAGES); i < it; ++i) drain_wait(bar_kv_full(i % STAGES), (i / STAGES) & 1);
+        }
       }
-      if (!ok) {  // give up: let the copies already issued land before the CTA exits
-        for (int i = max(0, nql - NQB); i < nql; ++i) drain_wait(bar_q_full(i % NQB), (i / NQB) & 1);
-        for (int i = max(0, it - STAGES); i < it; ++i) drain_wait(bar_kv_full(i % STAGES), (i / STAGES) & 1);
+    } else if (warp < WARP_MMA + NQT) {
+      // ================================================================ MMA issuers
+      // Warp WARP_MMA + t issues the MMAs of Q tile t; per key tile j its step is
+      // PV_t(j) (P_t from tensor memory) then S_t(j+1).  The tensor core takes a
+      // 128 x 128 x 16 MMA about every 64 cycles and holds the issuing thread for
+      // most of that, so the two issuers take strict turns, step by step
+      // (t = 0, 1, 0, 1, ...), and do everything but the MMAs outside their turn:
+      // waits for ring slots, the epilogue and P's first half before it (its second
+      // half inside), commits and slot releases after.  One issuer's bookkeeping then overlaps the
+      // other's MMAs, and the tensor pipe sees the MMAs of one step together, so
+      // S_t(j+1) is not held back behind the other tile's MMAs.  The turn order
+      // only sets priority (the two Q tiles share no tensor memory and each issuer
+      // releases ring slots for its own uses); the turn passes through a
+      // shared-memory counter.  The whole warp runs the loop converged (its
+      // descriptors and addresses warp-uniform); lane 0 issues.  MMAs of one
+      // thread execute in issue order, which orders S_t(j+1) after PV_t(j)
+      // (P_t aliases S_t).
+      const int t = warp - WARP_MMA;
+      {
+        const uint32_t elect = lane == 0 ? 1u : 0u;  // the lane that issues
+        auto wait_full = [&](RingPos r) { return mbar_wait(bar_kv_full(r.slot), r.phase, abort_flag, p.err); };
+        // bounded spin until the turn counter reaches `seq`
+        auto wait_turn = [&](uint32_t seq) {
+          if (*turn == seq) return true;
+          const unsigned long long t0 = global_ns();
+          for (uint32_t it = 1;; ++it) {
+            if (*turn == seq) return true;
+            if ((it & 63u) == 0u) {
+              if (*abort_flag) return false;
+              if (global_ns() - t0 > kAttnWaitNs) {
+                *abort_flag = 1;
+                atomicCAS(p.err, 0, ATTN_ERR_TIMEOUT);
+                return false;
+              }
+            }
+          }
+        };
+        const uint64_t k_desc0 = smem_desc_sw128(sb + SMEM_RING, 16, 1024);
+        const uint64_t v_desc0 = smem_desc_sw128(sb + SMEM_RING, KBLK_BYTES, 1024);
+        auto k_desc = [&](RingPos r) { return desc_add(k_desc0, static_cast<uint32_t>(r.slot * TILE_BYTES) >> 4); };
+        auto v_desc = [&](RingPos r) { return desc_add(v_desc0, static_cast<uint32_t>(r.slot * TILE_BYTES) >> 4); };
+        int it_base = 0;                      // ring position of the current unit's first K tile
+        int nq = 0;                           // units with work so far
+        int n_own = 0;                        // own key tiles so far (phase of s_full / p_lo / p_hi)
+        int n_out = 0;                        // units that produced O_t so far (phase of o_full / o_empty)
+        uint32_t seq = static_cast<uint32_t>(t);  // this issuer's next turn
+        bool ok = true;
+        for (int pass = 0, w = unit_of_pass(0); w < n_units && ok; w = unit_of_pass(++pass)) {
+          const Unit u = make_unit(w, p, n_qblk);
+          if (u.j_end <= u.j_begin) continue;
+          int jb, je;
+          own_range(u, t, jb, je);
+          if (je <= jb) jb = je = u.j_end;  // no own tiles: the slots are only released
+          // this unit's Q tile t: load 2 nq + t
+          const int qb = (2 * nq + t) % NQB;
+          if (!mbar_wait(bar_q_full(qb), ((2 * nq + t) / NQB) & 1, abort_flag, p.err)) { ok = false; break; }
+          const uint64_t q_desc = smem_desc_sw128(sb + SMEM_Q + qb * QK_TILE_BYTES, 16, 1024);
+          if (jb < je) {  // first S of this unit (outside the turn order)
+            const RingPos r = ring_pos<STAGES>(it_base + 2 * (jb - u.j_begin));
+            if (!wait_full(r)) { ok = false; break; }
+            tc_fence_after();
+            issue_qk<HD, F16, QK8>(elect, tmem + s_col(t), q_desc, k_desc(r));
+            mma_commit_if(elect, bar_s_full(t));
+            mma_commit_if(elect, bar_kv_empty(r.slot));
+            if (je - jb == 1) mma_commit_if(elect, bar_q_empty(qb));  // that was this unit's last S
+          } else {
+            mbar_arrive_if(elect, bar_q_empty(qb));
+          }
+          RingPos kj = ring_pos<STAGES>(it_base);  // K of key tile j
+          for (int j = u.j_begin; j < u.j_end && ok; ++j) {
+            const RingPos vj = ring_next<STAGES>(kj);  // V of key tile j
+            const RingPos kn = ring_next<STAGES>(vj);  // K of key tile j + 1
+            const bool own = j >= jb && j < je;
+            const int lt = n_own + (j - jb);
+            if (own) {
+              // inputs of this step, before taking the turn: the ring slots (filled
+              // long before in the steady state) first, P_t's first half last, so that
+              // the turn follows the softmax's hand-over with as little delay as possible
+              if (!wait_full(vj) || (j + 1 < je && !wait_full(kn))) { ok = false; break; }
+              // PV overwrites O_t at the unit's first key tile: the epilogue of the
+              // previous unit must have read it out.
+              if (j == jb && n_out > 0 && !mbar_wait(bar_o_empty(t), (n_out - 1) & 1, abort_flag, p.err)) {
+                ok = false;
+                break;
+              }
+              if (!mbar_wait(bar_p_lo(t), lt & 1, abort_flag, p.err)) { ok = false; break; }
+            }
+            if (!wait_turn(seq)) { ok = false; break; }
+            if (own) {
+              tc_fence_after();
+              issue_pv_half<HD, F16>(elect, tmem + o_col<HD>(t), tmem + s_col(t), v_desc(vj), j > jb, 0);
+              if (!mbar_wait(bar_p_hi(t), lt & 1, abort_flag, p.err)) { ok = false; break; }
+              tc_fence_after();
+              issue_pv_half<HD, F16>(elect, tmem + o_col<HD>(t), tmem + s_col(t), v_desc(vj), true, BN / 32);
+              if (j + 1 < je) issue_qk<HD, F16, QK8>(elect, tmem + s_col(t), q_desc, k_desc(kn));
+            }
+            *turn = seq + 1;  // the other issuer's turn
+            seq += 2;
+            if (own) {
+              mma_commit_if(elect, bar_kv_empty(vj.slot));
+              if (j + 1 == je) {
+                mma_commit_if(elect, bar_o_full(t));
+              } else {
+                mma_commit_if(elect, bar_s_full(t));
+                mma_commit_if(elect, bar_kv_empty(kn.slot));
+                if (j + 2 == je) mma_commit_if(elect, bar_q_empty(qb));  // this unit's last S
+              }
+            } else {
+              // outside this Q tile's range: release both slots once they are filled
+              if (!wait_full(kj) || !wait_full(vj)) { ok = false; break; }
+              mbar_arrive_if(elect, bar_kv_empty(kj.slot));
+              mbar_arrive_if(elect, bar_kv_empty(vj.slot));
+            }
+            kj = kn;
+          }
+          if (je > jb) {
+            n_own += je - jb;
+            ++n_out;
+          }
+          it_base += 2 * (u.j_end - u.j_begin);
+          ++nq;
+        }
+        // every MMA issued above must finish before tensor memory is released
+        mma_commit_if(elect, bar_mma_done);
+        drain_wait(bar_mma_done, 0);
       }
     }
-  } else if (warp < WARP_MMA + NQT) {
-    // ================================================================ MMA issuers
-    // Warp WARP_MMA + t issues the MMAs of Q tile t; per key tile j its step is
-    // PV_t(j) (P_t from tensor memory) then S_t(j+1).  The tensor core takes a
-    // 128 x 128 x 16 MMA about every 64 cycles and holds the issuing thread for
-    // most of that, so the two issuers take strict turns, step by step
-    // (t = 0, 1, 0, 1, ...), and do everything but the MMAs outside their turn:
-    // waits for ring slots, the epilogue and P's first half before it (its second
-    // half inside), commits and slot releases after.  One issuer's bookkeeping then overlaps the
-    // other's MMAs, and the tensor pipe sees the MMAs of one step together, so
-    // S_t(j+1) is not held back behind the other tile's MMAs.  The turn order
-    // only sets priority (the two Q tiles share no tensor memory and each issuer
-    // releases ring slots for its own uses); the turn passes through a
-    // shared-memory counter.  The whole warp runs the loop converged (its
-    // descriptors and addresses warp-uniform); lane 0 issues.  MMAs of one
-    // thread execute in issue order, which orders S_t(j+1) after PV_t(j)
-    // (P_t aliases S_t).
-    const int t = warp - WARP_MMA;
-    {
-      const uint32_t elect = lane == 0 ? 1u : 0u;  // the lane that issues
-      auto wait_full = [&](RingPos r) { return mbar_wait(bar_kv_full(r.slot), r.phase, abort_flag, p.err); };
-      // bounded spin until the turn counter reaches `seq`
-      auto wait_turn = [&](uint32_t seq) {
-        if (*turn == seq) return true;
-        const unsigned long long t0 = global_ns();
-        for (uint32_t it = 1;; ++it) {
-          if (*turn == seq) return true;
-          if ((it & 63u) == 0u) {
-            if (*abort_flag) return false;
-            if (global_ns() - t0 > kAttnWaitNs) {
-              *abort_flag = 1;
-              atomicCAS(p.err, 0, ATTN_ERR_TIMEOUT);
-              return false;
-            }
-          }
-        }
-      };
-      const uint64_t k_desc0 = smem_desc_sw128(sb + SMEM_RING, 16, 1024);
-      const uint64_t v_desc0 = smem_desc_sw128(sb + SMEM_RING, KBLK_BYTES, 1024);
-      auto k_desc = [&](RingPos r) { return desc_add(k_desc0, static_cast<uint32_t>(r.slot * TILE_BYTES) >> 4); };
-      auto v_desc = [&](RingPos r) { return desc_add(v_desc0, static_cast<uint32_t>(r.slot * TILE_BYTES) >> 4); };
-      int it_base = 0;                      // ring position of the current unit's first K tile
-      int nq = 0;                           // units with work so far
-      int n_own = 0;                        // own key tiles so far (phase of s_full / p_lo / p_hi)
-      int n_out = 0;                        // units that produced O_t so far (phase of o_full / o_empty)
-      uint32_t seq = static_cast<uint32_t>(t);  // this issuer's next turn
-      bool ok = true;
-      for (int pass = 0, w = unit_of_pass(0); w < n_units && ok; w = unit_of_pass(++pass)) {
-        const Unit u = make_unit(w, p, n_qblk);
-        if (u.j_end <= u.j_begin) continue;
+  } else if (warp >= WARP_EPI) {
+    setmaxnreg_dec<Regs<HD, CAP>::EPI>();
+    // ================================================================ epilogue
+    // Warp WARP_EPI + q takes rows [32q, 32q + 32) of each Q tile: once a unit's
+    // last P V into O_t has completed it reads O_t out of tensor memory, hands
+    // it back to the MMA issuer and writes O_t / l in the output type, while
+    // the softmax warps already run the next unit.  Q tile 0, then Q tile 1, unit
+    // by unit (the order in which they finish).
+    const int quad = warp % 4;
+    const uint32_t lane_sel = static_cast<uint32_t>(quad * 32) << 16;
+    const float* stats = reinterpret_cast<const float*>(smem + C::SMEM_STATS);
+    const uint64_t out_policy = l2_policy_evict_first();   // O is written once
+    int n_unit = 0;          // units so far (phase of stats_full / stats_empty)
+    int n_out[NQT] = {};     // units that produced O_t so far (phase of o_full / o_empty)
+    bool ok = true;
+    for (int pass = 0, w = unit_of_pass(0); w < n_units && ok; w = unit_of_pass(++pass)) {
+      const Unit u = make_unit(w, p, n_qblk);
+#pragma unroll
+      for (int t = 0; t < NQT; ++t) {
         int jb, je;
         own_range(u, t, jb, je);
-        if (je <= jb) jb = je = u.j_end;  // no own tiles: the slots are only released
-        // this unit's Q tile t: load 2 nq + t
-        const int qb = (2 * nq + t) % NQB;
-        if (!mbar_wait(bar_q_full(qb), ((2 * nq + t) / NQB) & 1, abort_flag, p.err)) { ok = false; break; }
-        const uint64_t q_desc = smem_desc_sw128(sb + SMEM_Q + qb * QK_TILE_BYTES, 16, 1024);
-        if (jb < je) {  // first S of this unit (outside the turn order)
-          const RingPos r = ring_pos<STAGES>(it_base + 2 * (jb - u.j_begin));
-          if (!wait_full(r)) { ok = false; break; }
-          tc_fence_after();
-          issue_qk<HD, F16, QK8>(elect, tmem + s_col(t), q_desc, k_desc(r));
-          mma_commit_if(elect, bar_s_full(t));
-          mma_commit_if(elect, bar_kv_empty(r.slot));
-          if (je - jb == 1) mma_commit_if(elect, bar_q_empty(qb));  // that was this unit's last S
-        } else {
-          mbar_arrive_if(elect, bar_q_empty(qb));
-        }
-        RingPos kj = ring_pos<STAGES>(it_base);  // K of key tile j
-        for (int j = u.j_begin; j < u.j_end && ok; ++j) {
-          const RingPos vj = ring_next<STAGES>(kj);  // V of key tile j
-          const RingPos kn = ring_next<STAGES>(vj);  // K of key tile j + 1
-          const bool own = j >= jb && j < je;
-          const int lt = n_own + (j - jb);
-          if (own) {
-            // inputs of this step, before taking the turn: the ring slots (filled
-            // long before in the steady state) first, P_t's first half last, so that
-            // the turn follows the softmax's hand-over with as little delay as possible
-            if (!wait_full(vj) || (j + 1 < je && !wait_full(kn))) { ok = false; break; }
-            // PV overwrites O_t at the unit's first key tile: the epilogue of the
-            // previous unit must have read it out.
-            if (j == jb && n_out > 0 && !mbar_wait(bar_o_empty(t), (n_out - 1) & 1, abort_flag, p.err)) {
-              ok = false;
-              break;
-            }
-            if (!mbar_wait(bar_p_lo(t), lt & 1, abort_flag, p.err)) { ok = false; break; }
-          }
-          if (!wait_turn(seq)) { ok = false; break; }
-          if (own) {
-            tc_fence_after();
-            issue_pv_half<HD, F16>(elect, tmem + o_col<HD>(t), tmem + s_col(t), v_desc(vj), j > jb, 0);
-            if (!mbar_wait(bar_p_hi(t), lt & 1, abort_flag, p.err)) { ok = false; break; }
-            tc_fence_after();
-            issue_pv_half<HD, F16>(elect, tmem + o_col<HD>(t), tmem + s_col(t), v_desc(vj), true, BN / 32);
-            if (j + 1 < je) issue_qk<HD, F16, QK8>(elect, tmem + s_col(t), q_desc, k_desc(kn));
-          }
-          *turn = seq + 1;  // the other issuer's turn
-          seq += 2;
-          if (own) {
-            mma_commit_if(elect, bar_kv_empty(vj.slot));
-            if (j + 1 == je) {
-              mma_commit_if(elect, bar_o_full(t));
-            } else {
-              mma_commit_if(elect, bar_s_full(t));
-              mma_commit_if(elect, bar_kv_empty(kn.slot));
-              if (j + 2 == je) mma_commit_if(elect, bar_q_empty(qb));  // this unit's last S
-            }
-          } else {
-            // outside this Q tile's range: release both slots once they are filled
-            if (!wait_full(kj) || !wait_full(vj)) { ok = false; break; }
-            mbar_arrive_if(elect, bar_kv_empty(kj.slot));
-            mbar_arrive_if(elect, bar_kv_empty(vj.slot));
-          }
-          kj = kn;
-        }
+        ok = __all_sync(0xffffffffu, mbar_wait(bar_stats_full(t), n_unit & 1, abort_flag, p.err));
+        if (!ok) break;
+        const float inv_l = stats[t * BM + quad * 32 + lane];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_stats_empty(t));
+        // the row's HD outputs, normalised and packed: word k holds outputs 2k, 2k + 1
+        uint32_t wd[HD / 2];
         if (je > jb) {
-          n_own += je - jb;
-          ++n_out;
+          ok = __all_sync(0xffffffffu, mbar_wait(bar_o_full(t), n_out[t] & 1, abort_flag, p.err));
+          if (!ok) break;
+          ++n_out[t];
+          tc_fence_after();
+          const uint32_t o_addr = tmem + lane_sel + o_col<HD>(t);
+#pragma unroll
+          for (int ch = 0; ch < HD / 32; ++ch) {
+            uint32_t o[32];
+            tmem_ld32(o_addr + ch * 32, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int k = 0; k < 16; ++k)
+              wd[16 * ch + k] = pack2<F16>(__uint_as_float(o[2 * k]) * inv_l, __uint_as_float(o[2 * k + 1]) * inv_l);
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_o_empty(t));
+        } else {
+#pragma unroll
+          for (int k = 0; k < HD / 2; ++k) wd[k] = 0u;   // no visible key: O = 0
         }
-        it_base += 2 * (u.j_end - u.j_begin);
-        ++nq;
+        const int row = u.q0 + t * BM + quad * 32 + lane;
+        if (row < u.Nq) {
+          const size_t orow_idx = p.varlen ? static_cast<size_t>(u.q_tok + row) * p.Hq + u.h
+                                           : (static_cast<size_t>(u.b) * p.Hq + u.h) * p.Nq + row;
+          uint16_t* orow = static_cast<uint16_t*>(p.o) + orow_idx * HD;
+          if (p.o_align32) {
+            // 32-byte stores: each thread writes its own row, so a warp's store touches 32
+            // rows; whole 32-byte sectors halve the write requests of 16-byte stores
+#pragma unroll
+            for (int i = 0; i < HD / 16; ++i) st_global_v8_hint(orow + 16 * i, &wd[8 * i], out_policy);
+          } else {
+#pragma unroll
+            for (int i = 0; i < HD / 8; ++i)
+              reinterpret_cast<uint4*>(orow)[i] = make_uint4(wd[4 * i], wd[4 * i + 1], wd[4 * i + 2], wd[4 * i + 3]);
+          }
+        }
       }
-      // every MMA issued above must finish before tensor memory is released
-      mma_commit_if(elect, bar_mma_done);
-      drain_wait(bar_mma_done, 0);
+      ++n_unit;
     }
   } else {
-    // ================================================================ softmax + epilogue
+    setmaxnreg_inc<Regs<HD, CAP>::SOFTMAX>();
+    // ================================================================ softmax
     const int t = (warp - WARP_SOFTMAX0) / 4;
     const int quad = warp % 4;
     const uint32_t lane_sel = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t s_addr = tmem + lane_sel + s_col(t);
     const uint32_t o_addr = tmem + lane_sel + o_col<HD>(t);
     const float c = p.scale_log2;
-    const uint64_t out_policy = l2_policy_evict_first();   // O is written once
     int n_own = 0;  // own key tiles so far (phase of s_full)
-    int n_out = 0;  // units that produced O_t so far (phase of o_full)
+    int n_unit = 0; // units so far (phase of stats_full / stats_empty)
+    float* stats = reinterpret_cast<float*>(smem + C::SMEM_STATS);
     bool ok = true;
     for (int pass = 0, w = unit_of_pass(0); w < n_units && ok; w = unit_of_pass(++pass)) {
       const Unit u = make_unit(w, p, n_qblk);
@@ -762,71 +859,38 @@ attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
       if (!ok) break;
       n_own += n_tiles;
 
-      // ---- epilogue: read O_t out of tensor memory (then hand it back to the
-      // MMA issuer), O / l -> bf16, LSE
-      uint32_t o[HD];
-      if (n_tiles > 0) {
-        ok = __all_sync(0xffffffffu, mbar_wait(bar_o_full(t), n_out & 1, abort_flag, p.err));
-        if (!ok) break;
-        ++n_out;
-        tc_fence_after();
-#pragma unroll
-        for (int ch = 0; ch < HD / 32; ++ch) {
-          uint32_t (&oc)[32] = *reinterpret_cast<uint32_t(*)[32]>(o + 32 * ch);
-          tmem_ld32(o_addr + ch * 32, oc);
-        }
-        tmem_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_o_empty(t));
-      } else {
-#pragma unroll
-        for (int i = 0; i < HD; ++i) o[i] = 0u;
-      }
-      if (row < u.Nq) {
-        // normaliser and LSE; a sink adds 2^(sink - m) to the row sum (in the
-        // common maximum M = max(m, sink)); a row with no visible key has O = 0
-        // and LSE = sink
-        float inv_l = (l > 0.f) ? 1.f / l : 0.f;
-        float lse_val = (l > 0.f) ? (m + log2f(l)) * 0.69314718055994531f : -CUDART_INF_F;
-        if (p.sinks != nullptr) {
-          const float sink = __ldg(p.sinks + u.h);
-          if (l > 0.f) {
-            const float M = fmaxf(m, sink * 1.4426950408889634f);
-            const float w = ex2_approx(m - M);
-            const float lt = fmaf(l, w, ex2_approx(sink * 1.4426950408889634f - M));
-            inv_l = w / lt;
-            lse_val = (M + log2f(lt)) * 0.69314718055994531f;
-          } else {
-            inv_l = 0.f;
-            lse_val = sink;
-          }
-        }
-        inv_l *= p.o_scale;
-        const size_t orow_idx = p.varlen ? static_cast<size_t>(u.q_tok + row) * p.Hq + u.h
-                                         : (static_cast<size_t>(u.b) * p.Hq + u.h) * p.Nq + row;
-        uint16_t* orow = static_cast<uint16_t*>(p.o) + orow_idx * HD;
-        // the row's HD outputs, normalised and packed: word k holds outputs 2k, 2k + 1
-        uint32_t w[HD / 2];
-#pragma unroll
-        for (int k = 0; k < HD / 2; ++k)
-          w[k] = pack2<F16>(__uint_as_float(o[2 * k]) * inv_l, __uint_as_float(o[2 * k + 1]) * inv_l);
-        if (p.o_align32) {
-          // 32-byte stores: each thread writes its own row, so a warp's store touches 32
-          // rows; whole 32-byte sectors halve the write requests of 16-byte stores
-#pragma unroll
-          for (int i = 0; i < HD / 16; ++i) st_global_v8_hint(orow + 16 * i, &w[8 * i], out_policy);
+      // ---- the row's normaliser 1 / l, handed to the epilogue warps, and LSE; a
+      // sink adds 2^(sink - m) to the row sum (in the common maximum M = max(m,
+      // sink)); a row with no visible key has O = 0 and LSE = sink
+      float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+      float lse_val = (l > 0.f) ? (m + log2f(l)) * 0.69314718055994531f : -CUDART_INF_F;
+      if (p.sinks != nullptr) {
+        const float sink = __ldg(p.sinks + u.h);
+        if (l > 0.f) {
+          const float M = fmaxf(m, sink * 1.4426950408889634f);
+          const float w = ex2_approx(m - M);
+          const float lt = fmaf(l, w, ex2_approx(sink * 1.4426950408889634f - M));
+          inv_l = w / lt;
+          lse_val = (M + log2f(lt)) * 0.69314718055994531f;
         } else {
-#pragma unroll
-          for (int i = 0; i < HD / 8; ++i)
-            reinterpret_cast<uint4*>(orow)[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+          inv_l = 0.f;
+          lse_val = sink;
         }
-        if (p.lse != nullptr) {
-          const float lse = lse_val;
-          const size_t li = p.varlen ? static_cast<size_t>(u.h) * p.total_q + u.q_tok + row
-                                     : (static_cast<size_t>(u.b) * p.Hq + u.h) * p.Nq + row;
-          p.lse[li] = lse;
-        }
+      }
+      inv_l *= p.o_scale;
+      // the epilogue warps must have taken the previous unit's normalisers
+      if (n_unit > 0) {
+        ok = __all_sync(0xffffffffu, mbar_wait(bar_stats_empty(t), (n_unit - 1) & 1, abort_flag, p.err));
+        if (!ok) break;
+      }
+      stats[t * BM + quad * 32 + lane] = inv_l;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_stats_full(t));
+      ++n_unit;
+      if (row < u.Nq && p.lse != nullptr) {
+        const size_t li = p.varlen ? static_cast<size_t>(u.h) * p.total_q + u.q_tok + row
+                                   : (static_cast<size_t>(u.b) * p.Hq + u.h) * p.Nq + row;
+        p.lse[li] = lse_val;
       }
     }
   }
@@ -874,6 +938,15 @@ int launch_impl(const void* q, const void* k, const void* v, void* o, float* lse
   static KernelSetup setup;
   if (const int rc = prepare_kernel(setup, attn_fwd_bf16_kernel<HD, F16, CAP, QK8>, C::SMEM_ALLOC); rc != ATTN_OK)
     return rc;
+  // The warpgroups' setmaxnreg shares add up to 65536 registers, which the block's pool
+  // (its registers per thread at launch x NTHREADS) must hold, or an `inc` never returns.
+  static std::atomic<int> regs_ok{-1};
+  if (regs_ok.load() < 0) {
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, attn_fwd_bf16_kernel<HD, F16, CAP, QK8>) != cudaSuccess) return ATTN_ERR_CUDA;
+    regs_ok.store(fa.numRegs * NTHREADS >= 65536 ? 1 : 0);
+  }
+  if (regs_ok.load() != 1) return ATTN_ERR_CUDA;
   FwdParams prm;
   prm.o = o;
   prm.lse = lse;
